@@ -1,0 +1,369 @@
+/*
+ * moe_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded CPU statement of what the routed-expert FP4 MoE layer
+ * computes.  It exists to check the CUDA library against; only the tests, the smoke check
+ * and the CPU-baseline leg of the benchmark may load it.  It shares no code, header, table
+ * or helper with the CUDA library.  Build: gcc -O2 -std=c11 -ffp-contract=off.
+ *
+ * Sources (web pages on the DeepSeek-V4.1-Flash single-box runtimes):
+ *  - "DeepSeek-V4.1-Flash on a single NVIDIA DGX Spark" (shadowgraph.io), section "Why it is
+ *    built this way": routed experts are 15,360 x 3 x 2304 x 5120 FP4 weights with one UE8M0
+ *    scale per 32 elements (e2m1 codes, the checkpoint's own format, never requantised).
+ *  - "Start the expert reads before the GPU is done" (argonautlabs.ai), 30 September
+ *    follow-up: every (token, slot) row is written once and the slot sum is a separate
+ *    fixed-order step.
+ *  - "Fast single-box DeepSeek v4.1 Flash runtime" (wpnews.pro mirror of ds4-recipe),
+ *    section "Conventions": a correct slow baseline is the oracle; evaluation orders are
+ *    pinned once ("reference-defining") and reproduced by every fast path.
+ *  The pages name the router, top-k, FP4 experts and weighted combine but print no formula
+ *  for them.  Readings taken where they are silent (each also listed in the design notes):
+ *  - router score s = sigmoid(x . W_r[e]); selection key = s + bias[e] (bias selects only),
+ *    -inf for experts without a slot; top-k by key, ties to the lower expert id; weights
+ *    w_j = s_j / sum of the selected s, summed in ascending expert id; ids are emitted in
+ *    ascending expert id.
+ *  - the router logit is the exact dot product rounded once to fp32 (order independent);
+ *    s = fp32(1 / (1 + exp(-logit))) evaluated in double.
+ *  - expert FFN = SwiGLU: h = silu(W_gate x) * (W_up x), z = W_down h; y = sum_j w_j z_j.
+ *    All FFN arithmetic here is fp64 (every product is exact in fp64).
+ *  - code 2i of a row is the low nibble of byte i; scale byte b means 2^(b-127);
+ *    b = 255 is not a number.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_STATUS_FEW_RESIDENT 1
+#define ORACLE_STATUS_NONFINITE 8
+
+/* ---- formats ------------------------------------------------------------------------ */
+
+/* e2m1: 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit; exponent 0 is subnormal. */
+static const double E2M1_TABLE[16] = {
+    0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+    -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0};
+
+double oracle_e2m1_value(int code) { return E2M1_TABLE[code & 15]; }
+
+/* UE8M0: an unsigned 8-bit power-of-two exponent with bias 127; 255 encodes NaN. */
+double oracle_ue8m0_value(int byte) {
+    if (byte == 255) return NAN;
+    return ldexp(1.0, byte - 127);
+}
+
+/* Code k of a packed row: byte k/2, low nibble for even k. */
+int oracle_code_at(const uint8_t* row, int k) {
+    uint8_t b = row[k / 2];
+    return (k % 2 == 0) ? (b & 15) : (b >> 4);
+}
+
+double oracle_weight_at(const uint8_t* qrow, const uint8_t* srow, int k) {
+    return oracle_e2m1_value(oracle_code_at(qrow, k)) * oracle_ue8m0_value(srow[k / 32]);
+}
+
+/* bfloat16 bit pattern -> double (exact). */
+double oracle_bf16_value(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* double -> bfloat16 bit pattern, round to nearest, ties to even (one rounding). */
+uint16_t oracle_bf16_from_double(double v) {
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                       /* a in [2^(e-1), 2^e) */
+    int q = e - 8;                      /* 8 significant bits: quantum 2^(e-8) */
+    if (q < -133) q = -133;             /* bf16 subnormal quantum 2^-133 */
+    double r = ldexp(a, -q);            /* exact: a scaled so the quantum is 1 */
+    double fl = floor(r), rem = r - fl;
+    if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) fl += 1.0;
+    double res = ldexp(fl, q);
+    if (res >= ldexp(1.0, 128)) return sign | 0x7F80;  /* overflow to infinity */
+    float f = (float)res;               /* exact: at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | ((u >> 16) & 0x7FFF));
+}
+
+/* ---- router logit: exact dot product of bf16 vectors, rounded once to fp32 ---------- */
+
+/* A bf16 value is (-1)^sign * mant * 2^exp2 with an integer mant < 256 and
+ * exp2 >= -133, so a product of two is an integer < 2^16 times 2^(e), e >= -266.  The
+ * exact sum is held as a signed big integer in units of 2^-266 (a Kulisch accumulator):
+ * 18 limbs of 32 bits cover 576 bits, above the 522 bits of the largest product plus the
+ * carries of up to 2^30 terms. */
+#define KL_LIMBS 18
+#define KL_UNIT 266
+
+static int bf16_split(uint16_t b, int* sign, int* mant, int* exp2) {
+    int e = (b >> 7) & 0xFF, m = b & 0x7F;
+    *sign = b >> 15;
+    if (e == 0xFF) return -1;            /* inf or NaN */
+    if (e == 0) { *mant = m; *exp2 = 1 - 127 - 7; }
+    else { *mant = m | 0x80; *exp2 = e - 127 - 7; }
+    return 0;
+}
+
+static int big_bit(const uint32_t* dig, int i) { return (int)((dig[i / 32] >> (i % 32)) & 1u); }
+
+/* Returns RN_fp32(sum_k x[k] w[k]); sets *bad if an input is inf or NaN. */
+float oracle_dot_bf16_rn32(const uint16_t* x, const uint16_t* w, int n, int* bad) {
+    int64_t acc[KL_LIMBS];
+    memset(acc, 0, sizeof acc);
+    if (bad) *bad = 0;
+    for (int k = 0; k < n; ++k) {
+        int sx, mx, ex, sw, mw, ew;
+        if (bf16_split(x[k], &sx, &mx, &ex) || bf16_split(w[k], &sw, &mw, &ew)) {
+            if (bad) *bad = 1;
+            return NAN;
+        }
+        uint64_t p = (uint64_t)mx * (uint64_t)mw;
+        if (p == 0) continue;
+        int pos = ex + ew + KL_UNIT;     /* >= 0 */
+        uint64_t v = p << (pos % 32);    /* < 2^47 */
+        int64_t lo = (int64_t)(v & 0xFFFFFFFFu), hi = (int64_t)(v >> 32);
+        if (sx ^ sw) { lo = -lo; hi = -hi; }
+        acc[pos / 32] += lo;
+        acc[pos / 32 + 1] += hi;
+    }
+    /* carry-normalise into 32-bit digits; a final carry of -1 means a negative total */
+    uint32_t dig[KL_LIMBS];
+    int64_t carry = 0;
+    for (int i = 0; i < KL_LIMBS; ++i) {
+        int64_t v = acc[i] + carry;
+        int64_t d = v & 0xFFFFFFFFLL;
+        dig[i] = (uint32_t)d;
+        carry = (v - d) / 4294967296LL;
+    }
+    int negative = carry < 0;
+    if (negative) {                      /* magnitude = 2^576 - digits */
+        uint64_t c = 1;
+        for (int i = 0; i < KL_LIMBS; ++i) {
+            uint64_t v = (uint64_t)(uint32_t)~dig[i] + c;
+            dig[i] = (uint32_t)v;
+            c = v >> 32;
+        }
+    }
+    int msb = -1;
+    for (int i = KL_LIMBS * 32 - 1; i >= 0; --i)
+        if (big_bit(dig, i)) { msb = i; break; }
+    if (msb < 0) return 0.0f;
+    /* keep 24 significant bits, but no quantum below fp32's 2^-149 */
+    int q = msb - 23;
+    if (q < KL_UNIT - 149) q = KL_UNIT - 149;
+    uint64_t r = 0;
+    for (int i = msb; i >= q; --i) r = (r << 1) | (uint64_t)big_bit(dig, i);
+    int half = (q >= 1) ? big_bit(dig, q - 1) : 0;
+    int sticky = 0;
+    for (int i = q - 2; i >= 0; --i)
+        if (big_bit(dig, i)) { sticky = 1; break; }
+    if (half && (sticky || (r & 1))) r += 1;
+    double mag = ldexp((double)r, q - KL_UNIT);
+    float f = (float)mag;                /* exact, or +inf beyond the fp32 range */
+    return negative ? -f : f;
+}
+
+float oracle_router_logit(const uint16_t* x, const uint16_t* w, int d) {
+    return oracle_dot_bf16_rn32(x, w, d, NULL);
+}
+
+/* Router score: sigmoid of the fp32 logit, evaluated in double, rounded once to fp32. */
+float oracle_router_score(float logit) {
+    return (float)(1.0 / (1.0 + exp(-(double)logit)));
+}
+
+/* ---- router: score, mask, top-k, renormalise, slot lookup -------------------------- */
+
+/* For each token t: key[e] = s[e] + bias[e] in fp32 (bias NULL means 0) for experts with
+ * expert_to_slot[e] >= 0; the k largest keys are chosen, ties to the lower expert id.
+ * Outputs per token, in ascending expert id: ids, weights w = s / sum(s) (fp32, summed in
+ * ascending id), slots.  If fewer than k experts are resident the missing entries are
+ * id -1, weight 0, slot -1 and status bit 1 is set.  If the chosen scores sum to zero the
+ * weights are zero.  logits/scores (optional, [T,E]) receive the fp32 values. */
+int oracle_route_topk(int T, int d, int E, int k, const uint16_t* x, const uint16_t* w_router,
+                      const float* bias, const int32_t* expert_to_slot, int32_t* ids,
+                      float* weights, int32_t* slots, float* logits, float* scores) {
+    int status = 0;
+    float* s = (float*)malloc(sizeof(float) * (size_t)E);
+    float* key = (float*)malloc(sizeof(float) * (size_t)E);
+    char* taken = (char*)malloc((size_t)E);
+    int32_t* pick = (int32_t*)malloc(sizeof(int32_t) * (size_t)(k > 0 ? k : 1));
+    for (int t = 0; t < T; ++t) {
+        const uint16_t* xt = x + (size_t)t * d;
+        for (int e = 0; e < E; ++e) {
+            int bad = 0;
+            float l = oracle_dot_bf16_rn32(xt, w_router + (size_t)e * d, d, &bad);
+            if (bad) status |= ORACLE_STATUS_NONFINITE;
+            s[e] = oracle_router_score(l);
+            key[e] = s[e] + (bias ? bias[e] : 0.0f);   /* one fp32 rounding */
+            taken[e] = 0;
+            if (logits) logits[(size_t)t * E + e] = l;
+            if (scores) scores[(size_t)t * E + e] = s[e];
+        }
+        int n = 0;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e] || expert_to_slot[e] < 0) continue;
+                if (best < 0 || key[e] > key[best]) best = e;   /* strict: lower id wins ties */
+            }
+            if (best < 0) break;
+            taken[best] = 1;
+            pick[n++] = best;
+        }
+        if (n < k) status |= ORACLE_STATUS_FEW_RESIDENT;
+        /* ascending expert id */
+        for (int a = 1; a < n; ++a)
+            for (int b = a; b > 0 && pick[b - 1] > pick[b]; --b) {
+                int32_t tmp = pick[b]; pick[b] = pick[b - 1]; pick[b - 1] = tmp;
+            }
+        float sum = 0.0f;
+        for (int j = 0; j < n; ++j) sum += s[pick[j]];
+        for (int j = 0; j < k; ++j) {
+            size_t o = (size_t)t * k + j;
+            if (j < n) {
+                ids[o] = pick[j];
+                weights[o] = (sum > 0.0f) ? s[pick[j]] / sum : 0.0f;
+                slots[o] = expert_to_slot[pick[j]];
+            } else {
+                ids[o] = -1; weights[o] = 0.0f; slots[o] = -1;
+            }
+        }
+    }
+    free(s); free(key); free(taken); free(pick);
+    return status;
+}
+
+/* ---- permutation: group the (token, j) rows by expert, stable -------------------- */
+
+/* Rows are ordered by (expert id, token, j).  offsets[e] is the first row of expert e and
+ * offsets[E] the number of rows; row_src[r] = t*k + j; row_dst[t*k + j] = r, or -1 for
+ * an entry with id -1.  Returns the number of rows. */
+int oracle_permute(int T, int k, int E, const int32_t* ids, int32_t* offsets,
+                   int32_t* row_src, int32_t* row_dst) {
+    int r = 0;
+    for (int i = 0; i < T * k; ++i) row_dst[i] = -1;
+    for (int e = 0; e < E; ++e) {
+        offsets[e] = r;
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < k; ++j)
+                if (ids[t * k + j] == e) {
+                    row_src[r] = t * k + j;
+                    row_dst[t * k + j] = r;
+                    ++r;
+                }
+    }
+    offsets[E] = r;
+    return r;
+}
+
+/* ---- one expert on one token: SwiGLU FFN in fp64 ------------------------------------ */
+
+/* g_i = sum_k x_k Wg[i,k], u_i = sum_k x_k Wu[i,k] (i < f, k < d);
+ * h_i = g_i / (1 + exp(-g_i)) * u_i;  z_r = sum_i Wd[r,i] h_i (r < d). */
+void oracle_expert_ffn(int d, int f, const uint16_t* x, const uint8_t* gate_q,
+                       const uint8_t* gate_s, const uint8_t* up_q, const uint8_t* up_s,
+                       const uint8_t* down_q, const uint8_t* down_s, double* h_out,
+                       double* z_out) {
+    double* h = h_out ? h_out : (double*)malloc(sizeof(double) * (size_t)f);
+    double* xd = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int k = 0; k < d; ++k) xd[k] = oracle_bf16_value(x[k]);
+    for (int i = 0; i < f; ++i) {
+        const uint8_t* gq = gate_q + (size_t)i * (d / 2);
+        const uint8_t* gs = gate_s + (size_t)i * (d / 32);
+        const uint8_t* uq = up_q + (size_t)i * (d / 2);
+        const uint8_t* us = up_s + (size_t)i * (d / 32);
+        double g = 0.0, u = 0.0;
+        for (int k = 0; k < d; ++k) {
+            g += xd[k] * oracle_weight_at(gq, gs, k);
+            u += xd[k] * oracle_weight_at(uq, us, k);
+        }
+        h[i] = g / (1.0 + exp(-g)) * u;
+    }
+    for (int r = 0; r < d; ++r) {
+        const uint8_t* dq = down_q + (size_t)r * (f / 2);
+        const uint8_t* ds = down_s + (size_t)r * (f / 32);
+        double z = 0.0;
+        for (int i = 0; i < f; ++i) z += oracle_weight_at(dq, ds, i) * h[i];
+        z_out[r] = z;
+    }
+    free(xd);
+    if (!h_out) free(h);
+}
+
+/* ---- combine: y = sum_j w_j z_j in ascending j (= ascending expert id) ------------- */
+
+void oracle_combine(int d, int k, const double* z, const float* w, double* y) {
+    for (int r = 0; r < d; ++r) {
+        double acc = 0.0;
+        for (int j = 0; j < k; ++j) acc += (double)w[j] * z[(size_t)j * d + r];
+        y[r] = acc;
+    }
+}
+
+/* ---- the whole layer on small shapes ------------------------------------------------ */
+
+/* Experts live in slots: the six canonical tensors of slot s start at
+ * gate_q + s*f*d/2, gate_s + s*f*d/32, ... down_s + s*d*f/32.  y [T,d] in fp64;
+ * y_bf16 (optional) is y rounded once to bf16.  Returns the router status; a slot outside
+ * [0, num_slots) sets bit 2 and that term is skipped. */
+int oracle_moe_layer(int T, int d, int f, int E, int k, int num_slots, const uint16_t* x,
+                     const uint16_t* w_router, const float* bias, const int32_t* expert_to_slot,
+                     const uint8_t* gate_q, const uint8_t* gate_s, const uint8_t* up_q,
+                     const uint8_t* up_s, const uint8_t* down_q, const uint8_t* down_s,
+                     int32_t* ids, float* weights, int32_t* slots, double* y, uint16_t* y_bf16) {
+    int status = oracle_route_topk(T, d, E, k, x, w_router, bias, expert_to_slot, ids, weights,
+                                   slots, NULL, NULL);
+    size_t wq = (size_t)f * d / 2, ws = (size_t)f * d / 32;
+    double* z = (double*)calloc((size_t)k * d, sizeof(double));
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int s = slots[t * k + j];
+            double* zj = z + (size_t)j * d;
+            if (s < 0 || s >= num_slots) {
+                if (s >= num_slots) status |= 2;
+                for (int r = 0; r < d; ++r) zj[r] = 0.0;
+                continue;
+            }
+            oracle_expert_ffn(d, f, x + (size_t)t * d, gate_q + s * wq, gate_s + s * ws,
+                              up_q + s * wq, up_s + s * ws, down_q + s * wq, down_s + s * ws,
+                              NULL, zj);
+        }
+        oracle_combine(d, k, z, weights + (size_t)t * k, y + (size_t)t * d);
+        if (y_bf16)
+            for (int r = 0; r < d; ++r) y_bf16[(size_t)t * d + r] = oracle_bf16_from_double(y[(size_t)t * d + r]);
+    }
+    free(z);
+    return status;
+}
+
+/* ---- layer chaining used by the multi-layer workloads -------------------------------- */
+
+/* x_next = bf16( RMSNorm(x + y) ), RMSNorm(v) = v / sqrt(mean(v^2) + eps), unit weight,
+ * evaluated in fp64 with one final rounding to bf16. */
+void oracle_residual_rmsnorm(int T, int d, const uint16_t* x, const double* y, double eps,
+                             uint16_t* x_next) {
+    double* v = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int t = 0; t < T; ++t) {
+        double ss = 0.0;
+        for (int i = 0; i < d; ++i) {
+            v[i] = oracle_bf16_value(x[(size_t)t * d + i]) + y[(size_t)t * d + i];
+            ss += v[i] * v[i];
+        }
+        double inv = 1.0 / sqrt(ss / d + eps);
+        for (int i = 0; i < d; ++i) x_next[(size_t)t * d + i] = oracle_bf16_from_double(v[i] * inv);
+    }
+    free(v);
+}
+
+/* Bytes of one expert in the canonical format: three f x d matrices, half a byte per code
+ * and one scale byte per 32 codes. */
+long long oracle_expert_bytes(int d, int f) {
+    return 3LL * f * d / 2 + 3LL * f * d / 32;
+}

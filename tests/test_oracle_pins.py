@@ -1,0 +1,476 @@
+"""Pins for the CPU oracle: each test checks an oracle function against something other
+than the oracle itself -- a bit-field definition, a library conversion, exact rational
+arithmetic, multi-precision evaluation, brute force, a closed form, a hand-worked fixture,
+or an independent fp64 re-derivation written here.  No GPU is involved."""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from synth import tensors as syn
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def e2m1_from_bits(code):
+    """e2m1 from its fields: sign, 2-bit exponent with bias 1, 1 mantissa bit."""
+    s, e, m = code >> 3, (code >> 1) & 3, code & 1
+    mag = m * 0.5 if e == 0 else 2.0 ** (e - 1) * (1 + m / 2)
+    return -mag if s else mag
+
+
+def bf16_exact(bits):
+    """Exact rational value of a finite bf16 bit pattern, from its fields."""
+    s, e, m = bits >> 15, (bits >> 7) & 0xFF, bits & 0x7F
+    v = Fraction(m, 128) * Fraction(2) ** -126 if e == 0 else (1 + Fraction(m, 128)) * Fraction(2) ** (e - 127)
+    return -v if s else v
+
+
+def round_fraction_to_f32(v: Fraction) -> np.float32:
+    """Round an exact rational to the nearest fp32 (ties to even), by integer arithmetic."""
+    if v == 0:
+        return np.float32(0.0)
+    neg = v < 0
+    a = -v if neg else v
+    # find e with 2^e <= a < 2^(e+1)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    elif Fraction(2) ** (e + 1) <= a:
+        e += 1
+    q = max(e - 23, -149)                 # quantum exponent
+    scaled = a / Fraction(2) ** q
+    n = scaled.numerator // scaled.denominator
+    rem = scaled - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    val = n * (2.0 ** q) if q >= -1074 else 0.0
+    r = np.float32(val) if val < 2.0 ** 128 else np.float32(np.inf)
+    return -r if neg else r
+
+
+def random_bf16(rng, n, lo_exp=-30, hi_exp=10):
+    """bf16 bit patterns with exponents spread over [lo_exp, hi_exp] and random signs."""
+    e = rng.integers(lo_exp, hi_exp + 1, n) + 127
+    e = np.clip(e, 0, 254)
+    m = rng.integers(0, 128, n)
+    s = rng.integers(0, 2, n)
+    return ((s << 15) | (e << 7) | m).astype(np.uint16)
+
+
+def decode_matrix(q, s):
+    """Independent numpy decode of a canonical [rows, K/2] code matrix and [rows, K/32]
+    scale matrix into fp64, from the e2m1 and UE8M0 bit-field definitions."""
+    q = np.asarray(q, np.uint8)
+    rows, half = q.shape
+    codes = np.empty((rows, half * 2), np.int64)
+    codes[:, 0::2] = q & 15
+    codes[:, 1::2] = q >> 4
+    table = np.array([e2m1_from_bits(c) for c in range(16)])
+    scale = np.ldexp(1.0, np.asarray(s, np.int64) - 127)
+    return table[codes] * np.repeat(scale, 32, axis=1)
+
+
+def bf16_to_f64(b):
+    return syn.bf16_bits_to_f32(b).astype(np.float64)
+
+
+# ----------------------------------------------------------------------------- formats
+
+def test_e2m1_table_matches_field_definition():
+    for c in range(16):
+        want = e2m1_from_bits(c)
+        got = oracle.e2m1_value(c)
+        assert got == want
+        assert math.copysign(1.0, got) == math.copysign(1.0, want if c != 8 else -0.0)
+    assert math.copysign(1.0, oracle.e2m1_value(8)) < 0  # code 8 is -0
+
+
+def test_ue8m0_is_an_fp32_exponent_field():
+    for b in range(1, 255):
+        want = np.array([b << 23], np.uint32).view(np.float32)[0]
+        assert oracle.ue8m0_value(b) == float(want)
+    # byte 0 is 2^-127, the fp32 subnormal with only mantissa bit 22 set -- not zero
+    assert oracle.ue8m0_value(0) == float(np.array([1 << 22], np.uint32).view(np.float32)[0])
+    assert math.isnan(oracle.ue8m0_value(255))
+
+
+def test_code_times_scale_brute_force():
+    """All 16 codes x 255 finite scale bytes through the packed-row accessor."""
+    import ctypes
+    L = oracle.lib()
+    for code in range(16):
+        row = np.full(16, code | (code << 4), np.uint8)   # 32 codes
+        for b in range(255):
+            srow = np.array([b], np.uint8)
+            got = L.oracle_weight_at(row.ctypes.data_as(ctypes.c_void_p),
+                                     srow.ctypes.data_as(ctypes.c_void_p), 5)
+            scale = float(np.array([b << 23 if b else 1 << 22], np.uint32).view(np.float32)[0])
+            want = e2m1_from_bits(code) * scale
+            assert got == want, (code, b)
+
+
+def test_nibble_order_hand_packed():
+    """Byte 0x21 holds codes (1, 2) = (0.5, 1.0); byte 0xF8 holds (8, 15) = (-0, -6)."""
+    import ctypes
+    L = oracle.lib()
+    row = np.array([0x21, 0xF8], np.uint8)
+    p = row.ctypes.data_as(ctypes.c_void_p)
+    assert [L.oracle_code_at(p, k) for k in range(4)] == [1, 2, 8, 15]
+    s = np.array([127], np.uint8)
+    ps = s.ctypes.data_as(ctypes.c_void_p)
+    assert [L.oracle_weight_at(p, ps, k) for k in range(4)] == [0.5, 1.0, -0.0, -6.0]
+
+
+def test_bf16_decode_matches_torch_for_every_pattern():
+    torch = pytest.importorskip("torch")
+    bits = np.arange(65536, dtype=np.int64)
+    finite = ((bits >> 7) & 0xFF) != 0xFF
+    t = torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    for b in bits[finite][::7]:
+        assert oracle.bf16_value(int(b)) == t[b]
+
+
+def test_bf16_rounding_from_double():
+    rng = np.random.default_rng(1)
+    vals = list(rng.normal(size=2000) * np.exp(rng.uniform(-60, 60, size=2000)))
+    # exact ties: 1 + 2^-8 (tie, even -> 1), 1 + 3*2^-8 (tie, even -> 1 + 2^-6)
+    vals += [1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 2.0 ** -134, 3 * 2.0 ** -135,
+             2.0 ** -140, 3.4e38, 3.4e39, 0.0, -0.0]
+    for v in vals:
+        got = oracle.bf16_from_double(float(v))
+        # independent: exact rational rounding with 8 significant bits, subnormal quantum 2^-133
+        a = Fraction(abs(v))
+        if a == 0:
+            want = 0x8000 if math.copysign(1, v) < 0 else 0
+        else:
+            e = math.frexp(abs(v))[1] - 1
+            q = max(e - 7, -133)
+            n = a / Fraction(2) ** q
+            fl = n.numerator // n.denominator
+            rem = n - fl
+            if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2):
+                fl += 1
+            r = Fraction(fl) * Fraction(2) ** q
+            if r >= Fraction(2) ** 128:
+                want = 0x7F80
+            else:
+                f32 = np.array([float(r)], np.float32).view(np.uint32)[0]
+                want = int(f32 >> 16) & 0x7FFF
+            if v < 0:
+                want |= 0x8000
+        assert got == want, v
+
+
+# ----------------------------------------------------------------------------- exact logit
+
+def test_dot_rn32_matches_exact_rational_sum():
+    rng = np.random.default_rng(2)
+    for trial in range(120):
+        n = int(rng.integers(1, 200))
+        lo = int(rng.integers(-140, 0))
+        x = random_bf16(rng, n, lo, lo + int(rng.integers(0, 60)))
+        w = random_bf16(rng, n, -40, 5)
+        if trial % 5 == 4:          # bf16 subnormals against large partners
+            x = random_bf16(rng, n, -160, -127)
+            w = random_bf16(rng, n, 90, 126)
+        if trial % 3 == 0:          # heavy cancellation
+            w[: n // 2] = w[n // 2: 2 * (n // 2)] ^ 0x8000
+            x[: n // 2] = x[n // 2: 2 * (n // 2)]
+        exact = sum((bf16_exact(int(a)) * bf16_exact(int(b)) for a, b in zip(x, w)), Fraction(0))
+        got, bad = oracle.dot_bf16_rn32(x, w)
+        assert not bad
+        want = round_fraction_to_f32(exact)
+        assert got == want or (got == 0 and want == 0), (trial, got, want)
+
+
+def bf16_of(v):
+    return int(syn.f32_to_bf16_bits(np.array([v], np.float32))[0])
+
+
+def test_dot_rn32_hand_midpoints():
+    """Sums built to sit on or just beside an fp32 rounding midpoint."""
+    one, t24, t60 = bf16_of(1.0), bf16_of(2.0 ** -24), bf16_of(2.0 ** -60)
+    ones = [one] * 3
+    # 1 + 2^-24 is exactly halfway between 1 and 1 + 2^-23: ties to even -> 1
+    assert oracle.dot_bf16_rn32(np.array([one, t24], np.uint16), np.array(ones[:2], np.uint16))[0] == np.float32(1.0)
+    # a 2^-60 term past the midpoint must round up -- an fp64 running sum would lose it
+    v, _ = oracle.dot_bf16_rn32(np.array([one, t24, t60], np.uint16), np.array(ones, np.uint16))
+    assert v == np.float32(1.0 + 2.0 ** -23)
+    # the same term below the midpoint rounds down
+    v, _ = oracle.dot_bf16_rn32(np.array([one, t24, t60 | 0x8000], np.uint16), np.array(ones, np.uint16))
+    assert v == np.float32(1.0)
+    # complete cancellation of huge terms leaves the small one exactly
+    big = bf16_of(2.0 ** 100)
+    v, _ = oracle.dot_bf16_rn32(np.array([big, bf16_of(3.0), big ^ 0x8000], np.uint16), np.array(ones, np.uint16))
+    assert v == np.float32(3.0)
+    # a bf16 subnormal (0x0003 = 3 * 2^-133) times 2^120 is exactly 3 * 2^-13
+    v, _ = oracle.dot_bf16_rn32(np.array([3], np.uint16), np.array([bf16_of(2.0 ** 120)], np.uint16))
+    assert v == np.float32(3 * 2.0 ** -13)
+    # subnormal products: 2^-133 * 2^-133 = 2^-266 is far below fp32's 2^-149 -> 0
+    tiny = 1  # bf16 subnormal 2^-133
+    assert oracle.dot_bf16_rn32(np.array([tiny], np.uint16), np.array([tiny], np.uint16))[0] == 0
+    # overflow beyond fp32 gives infinity
+    huge = bf16_of(2.0 ** 127)
+    v, _ = oracle.dot_bf16_rn32(np.array([huge, huge], np.uint16), np.array([bf16_of(4.0)] * 2, np.uint16))
+    assert np.isinf(v) and v > 0
+    # non-finite inputs are flagged
+    _, bad = oracle.dot_bf16_rn32(np.array([0x7F80], np.uint16), np.array([one], np.uint16))
+    assert bad
+
+
+def test_router_score_is_correctly_rounded_sigmoid():
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.prec = 200
+    rng = np.random.default_rng(3)
+    ls = np.concatenate([rng.normal(size=4000) * 3, rng.uniform(-110, 30, size=1000),
+                         [0.0, -0.0, 1e-30, -1e-30, 20.0, 40.0, -80.0, -103.0, -104.0, -200.0]]).astype(np.float32)
+    mism = 0
+    for l in ls:
+        got = oracle.router_score(l)
+        exact = 1 / (1 + mpmath.exp(-mpmath.mpf(float(l))))
+        want = round_fraction_to_f32(Fraction(int(exact.man)) * Fraction(2) ** int(exact.exp))
+        if got != want:
+            mism += 1
+            assert abs(float(got) - float(want)) <= np.spacing(np.float32(want)), l
+    assert mism == 0
+    assert oracle.router_score(0.0) == np.float32(0.5)
+    assert oracle.router_score(40.0) == np.float32(1.0)
+
+
+# ----------------------------------------------------------------------------- router
+
+def _golden_router_case(g, case):
+    d, E = g["d"], g["E"]
+    wr = np.stack([syn.f32_to_bf16_bits(np.full(d, c, np.float32)) for c in g["row_constants"]])
+    x = syn.f32_to_bf16_bits(np.full((1, d), case["x"], np.float32))
+    bias = None if case["bias"] is None else np.array(case["bias"], np.float32)
+    return x, wr, bias, np.array(case["slots"], np.int32)
+
+
+def test_router_hand_worked_cases():
+    g = json.load(open(os.path.join(GOLDEN, "router_hand.json")))
+    for case in g["cases"]:
+        x, wr, bias, tab = _golden_router_case(g, case)
+        r = oracle.route_topk(x, wr, bias, tab, g["k"])
+        assert r["ids"][0].tolist() == case["ids"], case["name"]
+        assert r["slots"][0].tolist() == case["out_slots"], case["name"]
+        assert r["status"] == case["status"], case["name"]
+        np.testing.assert_allclose(r["weights"][0], case["weights"], rtol=2e-7, atol=0, err_msg=case["name"])
+
+
+def test_router_brute_force_tiny():
+    """Independent restatement on random tiny inputs: exact rational logits, double sigmoid,
+    python sort by (-key, id)."""
+    rng = np.random.default_rng(4)
+    for trial in range(25):
+        T, d, E, k = 3, 64, 12, 3
+        x = syn.f32_to_bf16_bits(rng.normal(size=(T, d)).astype(np.float32))
+        wr = syn.f32_to_bf16_bits((rng.normal(size=(E, d)) * 0.05).astype(np.float32))
+        if trial % 4 == 1:                      # forced exact ties between experts
+            wr[5] = wr[2]
+            wr[9] = wr[2]
+        tab = np.arange(E, dtype=np.int32)
+        if trial % 4 == 2:
+            tab[rng.choice(E, 4, replace=False)] = -1
+        bias = (rng.normal(size=E) * 0.05).astype(np.float32) if trial % 2 else None
+        r = oracle.route_topk(x, wr, bias, tab, k)
+        for t in range(T):
+            keys = []
+            s32 = {}
+            for e in range(E):
+                ex = sum((bf16_exact(int(a)) * bf16_exact(int(b)) for a, b in zip(x[t], wr[e])), Fraction(0))
+                l32 = round_fraction_to_f32(ex)
+                s = np.float32(1.0 / (1.0 + math.exp(-float(l32))))
+                s32[e] = s
+                key = np.float32(s + (bias[e] if bias is not None else np.float32(0)))
+                if tab[e] >= 0:
+                    keys.append((-float(key), e))
+            chosen = sorted(e for _, e in sorted(keys)[:k])
+            assert r["ids"][t].tolist() == chosen
+            tot = np.float32(0)
+            for e in chosen:
+                tot = np.float32(tot + s32[e])
+            np.testing.assert_array_equal(r["weights"][t], np.array([np.float32(s32[e] / tot) for e in chosen], np.float32))
+
+
+# ----------------------------------------------------------------------------- permute
+
+def test_permute_matches_stable_sort_and_invariants():
+    rng = np.random.default_rng(5)
+    for trial in range(30):
+        T, k, E = int(rng.integers(1, 40)), int(rng.integers(1, 7)), int(rng.integers(1, 20))
+        ids = rng.integers(-1, E, size=(T, k)).astype(np.int32)
+        p = oracle.permute(ids, E)
+        flat = [(int(ids[t, j]), t, j) for t in range(T) for j in range(k) if ids[t, j] >= 0]
+        want = [t * k + j for (_, t, j) in sorted(flat)]
+        assert p["row_src"].tolist() == want
+        off = p["offsets"]
+        assert off[0] == 0 and off[E] == len(want) and np.all(np.diff(off) >= 0)
+        for e in range(E):
+            assert off[e + 1] - off[e] == int((ids == e).sum())
+        for r, src in enumerate(p["row_src"]):
+            assert p["row_dst"][src] == r
+        assert np.all(p["row_dst"][ids.reshape(-1) < 0] == -1)
+
+
+# ----------------------------------------------------------------------------- FFN
+
+def _expert(rng, d, f, lo=-8, hi=-4):
+    return {
+        "gate_q": rng.integers(0, 256, (f, d // 2), dtype=np.uint8),
+        "gate_s": (127 + rng.integers(lo, hi + 1, (f, d // 32))).astype(np.uint8),
+        "up_q": rng.integers(0, 256, (f, d // 2), dtype=np.uint8),
+        "up_s": (127 + rng.integers(lo, hi + 1, (f, d // 32))).astype(np.uint8),
+        "down_q": rng.integers(0, 256, (d, f // 2), dtype=np.uint8),
+        "down_s": (127 + rng.integers(lo, hi + 1, (d, f // 32))).astype(np.uint8),
+    }
+
+
+def test_ffn_closed_form_all_ones():
+    """Every weight 1.0 (code 2, scale byte 127): g = u = S = sum(x), h = silu(S) S,
+    z_r = f h."""
+    d, f = 64, 32
+    ex = {n: np.full(s, 0x22 if n.endswith("_q") else 127, np.uint8)
+          for n, s in syn.expert_tensor_shapes(d, f).items()}
+    rng = np.random.default_rng(6)
+    x = syn.f32_to_bf16_bits(rng.normal(size=d).astype(np.float32) * 0.1)
+    S = float(np.sum(bf16_to_f64(x)))
+    h, z = oracle.expert_ffn(x, ex)
+    hs = S / (1 + math.exp(-S)) * S
+    np.testing.assert_allclose(h, hs, rtol=1e-14)
+    np.testing.assert_allclose(z, f * hs, rtol=1e-14)
+
+
+def test_ffn_closed_form_diagonal():
+    """W_gate = I (code 2), W_up = 2I (code 4), W_down = I: z = h = silu(x) * 2x."""
+    d = f = 32
+    eye = np.zeros((32, 32), np.int64)
+    def pack(codes):
+        return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    ex = {"gate_q": pack(np.eye(32, dtype=np.int64) * 2), "up_q": pack(np.eye(32, dtype=np.int64) * 4),
+          "down_q": pack(np.eye(32, dtype=np.int64) * 2)}
+    for n in ("gate_s", "up_s", "down_s"):
+        ex[n] = np.full((32, 1), 127, np.uint8)
+    x = syn.f32_to_bf16_bits(np.linspace(-3, 3, 32).astype(np.float32))
+    xv = bf16_to_f64(x)
+    h, z = oracle.expert_ffn(x, ex)
+    want = xv / (1 + np.exp(-xv)) * 2 * xv
+    np.testing.assert_allclose(h, want, rtol=1e-15, atol=1e-300)
+    np.testing.assert_allclose(z, want, rtol=1e-15, atol=1e-300)
+    del eye
+
+
+def test_ffn_against_independent_numpy():
+    rng = np.random.default_rng(7)
+    d, f = 128, 64
+    ex = _expert(rng, d, f)
+    x = syn.f32_to_bf16_bits(rng.normal(size=d).astype(np.float32))
+    h, z = oracle.expert_ffn(x, ex)
+    xv = bf16_to_f64(x)
+    g = decode_matrix(ex["gate_q"], ex["gate_s"]) @ xv
+    u = decode_matrix(ex["up_q"], ex["up_s"]) @ xv
+    hh = g * u / (1 + np.exp(-g))
+    zz = decode_matrix(ex["down_q"], ex["down_s"]) @ hh
+    np.testing.assert_allclose(h, hh, rtol=1e-12, atol=1e-12 * np.abs(hh).max())
+    np.testing.assert_allclose(z, zz, rtol=1e-12, atol=1e-12 * np.abs(zz).max())
+
+
+def test_combine_fixed_order_and_one_hot():
+    rng = np.random.default_rng(8)
+    z = rng.normal(size=(3, 16))
+    y = oracle.combine(z, np.array([1.0, 0.0, 0.0], np.float32))
+    np.testing.assert_array_equal(y, z[0])
+    w = np.array([0.25, 0.5, 0.25], np.float32)
+    y = oracle.combine(z, w)
+    want = (0.25 * z[0] + 0.5 * z[1]) + 0.25 * z[2]
+    np.testing.assert_array_equal(y, want)
+
+
+# ----------------------------------------------------------------------------- layer
+
+def _tiny_layer_inputs(seed=0):
+    """The tiny configuration: d=512, f=256, E=16, k=2, T=4, identity slots, seed 0."""
+    d, f, E, k, T = 512, 256, 16, 2, 4
+    x = syn.activations(seed, 0, T, d)
+    wr = syn.router_weight(seed, 0, E, d)
+    tab = syn.identity_slot_table(E)
+    experts = [syn.expert_tensors(seed, 0, e, d, f, -8, -4) for e in range(E)]
+    stacked = {n: np.stack([ex[n] for ex in experts]) for n in syn.EXPERT_TENSORS}
+    return d, f, E, k, T, x, wr, tab, experts, stacked
+
+
+def test_tiny_layer_against_independent_rederivation():
+    d, f, E, k, T, x, wr, tab, experts, stacked = _tiny_layer_inputs()
+    r = oracle.moe_layer(x, wr, None, tab, k, stacked)
+    assert r["status"] == 0
+    for t in range(T):
+        keys, s32 = [], {}
+        for e in range(E):
+            ex = sum((bf16_exact(int(a)) * bf16_exact(int(b)) for a, b in zip(x[t], wr[e])), Fraction(0))
+            l32 = round_fraction_to_f32(ex)
+            s32[e] = np.float32(1.0 / (1.0 + math.exp(-float(l32))))
+            keys.append((-float(s32[e]), e))
+        chosen = sorted(e for _, e in sorted(keys)[:k])
+        assert r["ids"][t].tolist() == chosen
+        tot = np.float32(0)
+        for e in chosen:
+            tot = np.float32(tot + s32[e])
+        xv = bf16_to_f64(x[t])
+        y = np.zeros(d)
+        for e in chosen:
+            ex = experts[tab[e]]
+            g = decode_matrix(ex["gate_q"], ex["gate_s"]) @ xv
+            u = decode_matrix(ex["up_q"], ex["up_s"]) @ xv
+            hh = g * u / (1 + np.exp(-g))
+            y += float(np.float32(s32[e] / tot)) * (decode_matrix(ex["down_q"], ex["down_s"]) @ hh)
+        np.testing.assert_allclose(r["y"][t], y, rtol=1e-9, atol=1e-9 * np.abs(y).max())
+        # bf16 output is the one-step rounding of y
+        yb = syn.bf16_bits_to_f32(r["y_bf16"][t]).astype(np.float64)
+        assert np.all(np.abs(yb - r["y"][t]) <= np.abs(r["y"][t]) * 2.0 ** -8 + 1e-300)
+
+
+def test_layer_invariant_under_slot_relabelling_and_token_order():
+    d, f, E, k, T, x, wr, tab, experts, stacked = _tiny_layer_inputs(seed=3)
+    base = oracle.moe_layer(x, wr, None, tab, k, stacked)
+    perm = np.random.default_rng(9).permutation(E)          # expert e now lives in slot perm[e]
+    tab2 = perm.astype(np.int32)
+    stacked2 = {n: np.empty_like(a) for n, a in stacked.items()}
+    for e in range(E):
+        for n in stacked:
+            stacked2[n][perm[e]] = stacked[n][e]
+    r2 = oracle.moe_layer(x, wr, None, tab2, k, stacked2)
+    np.testing.assert_array_equal(r2["y"], base["y"])
+    np.testing.assert_array_equal(r2["ids"], base["ids"])
+    order = np.array([2, 0, 3, 1])
+    r3 = oracle.moe_layer(x[order], wr, None, tab, k, stacked)
+    np.testing.assert_array_equal(r3["y"], base["y"][order])
+
+
+def test_residual_rmsnorm_against_numpy():
+    rng = np.random.default_rng(10)
+    T, d = 3, 256
+    x = syn.f32_to_bf16_bits(rng.normal(size=(T, d)).astype(np.float32))
+    y = rng.normal(size=(T, d)) * 0.3
+    out = oracle.residual_rmsnorm(x, y, 1e-6)
+    v = bf16_to_f64(x) + y
+    ref = v / np.sqrt(np.mean(v * v, axis=1, keepdims=True) + 1e-6)
+    got = syn.bf16_bits_to_f32(out).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
+
+
+def test_expert_size_matches_the_pages():
+    g = dict(l.split() for l in open(os.path.join(GOLDEN, "expert_bytes.txt")) if l.strip() and not l.startswith("#"))
+    d, f = int(g["d"]), int(g["f"])
+    b = oracle.expert_bytes(d, f)
+    assert b == 18_800_640
+    assert round(b / 1e6, 1) == float(g["bytes_per_expert_mb"])
+    n = int(g["experts_total"])
+    assert round(n * b / 1e9, 1) == float(g["bytes_total_gb"])
+    assert round(n * 3 * d * f / 1e9, 1) == float(g["weights_total_billion"])
