@@ -1,0 +1,382 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed-expert FP4 MoE layer on GB300.
+
+Default workload: one MoE layer at the pages' shape (d=5120, f=2304, E=384 experts, top-k 6,
+every expert resident in a 7.22 GB arena behind a permuted expert->slot table), decode with
+T=1 token per call.  A step is 1000 fresh synthetic tokens processed one call at a time
+(each call = router + top-k + slot lookup + gate/up SwiGLU + down + fixed-order combine),
+replayed from a CUDA graph.  Metric: MoE-layer tokens/s.  The arena (7.2 GB) is far larger
+than L2, so no L2 flush is inserted between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 (torchrun, one process per GPU) every rank runs an independent replica of the
+layer (the path has no exchange step); value = all ranks' tokens / the slowest rank's time.
+--impl reference times the CPU oracle (plain C, one host core) on a bounded sample of the
+same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+D, F, E, K = 5120, 2304, 384, 6
+TOKENS = 1000
+SCALE = (-10, -6)
+EXPERT_BYTES = 18_800_640
+ROUTER_BYTES = E * D * 2
+# per token: 6 experts' full FP4 weights + scales, the router matrix, x in and y out
+ALG_BYTES_PER_TOKEN = K * EXPERT_BYTES + ROUTER_BYTES + 2 * D * 2
+# dominant kernel (gate/up + SwiGLU): 6 slots x (2f rows x (d/2 + d/32) bytes) + x in + h out
+GATEUP_BYTES = K * 2 * F * (D // 2 + D // 32) + D * 2 + K * F * 4
+METRIC = "MoE-layer tokens/s (T=1 decode, d=5120 f=2304 E=384 k=6)"
+CONFIG = {"workload": "decode T=1, one MoE layer, d=5120 f=2304 E=384 top-k=6, 384 resident experts (7.22 GB arena, "
+                      "permuted slot table), 1000 fresh tokens per step",
+          "tokens_per_step": TOKENS, "l2": "inputs larger than L2 (7.22 GB arena), no flush"}
+
+
+def env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            return json.load(open(p)), "measured"
+        except Exception:
+            pass
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % gpu_index)
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [s.strip() for s in line.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                sm.append(float(p[0]))
+                mx.append(float(p[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- workload
+
+def build_workload(device):
+    import torch
+    import fp4_routed_expert_gb300 as moe
+    from fp4_routed_expert_gb300.layer import Arena, MoeLayer
+    from synth import gpu as sgpu
+    from synth import tensors as syn
+    dims = moe.moe_dims(D, F, E, K)
+    table = syn.permuted_slot_table(0, 0, E)
+    arena = Arena(dims, E, device)
+    stage = sgpu.ExpertStaging(D, F, device)
+    for e in range(E):
+        arena.pack(int(table[e]), stage.fill(0, 0, e, *SCALE))
+    torch.cuda.synchronize()
+    del stage
+    x_bits = syn.activations(0, 0, TOKENS, D, stream=7)
+    wr_bits = syn.router_weight(0, 0, E, D)
+    def to_dev(b):
+        return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).to(device).view(torch.bfloat16)
+    x = to_dev(x_bits)
+    wr = to_dev(wr_bits)
+    tab = torch.from_numpy(table).to(device)
+    layer = MoeLayer(D, F, E, K, 1, arena, device)
+    y = torch.empty((TOKENS, D), dtype=torch.bfloat16, device=device)
+    return dict(layer=layer, arena=arena, x=x, wr=wr, tab=tab, y=y, x_bits=x_bits, wr_bits=wr_bits, table=table)
+
+
+def token_calls(w, i, stream=None):
+    layer = w["layer"]
+    layer.route(w["x"][i:i + 1], w["wr"], w["tab"], None, T=1, stream=stream)
+    layer.experts(w["x"][i:i + 1], T=1, stream=stream, y=w["y"][i:i + 1])
+
+
+class CudaRt:
+    """Event record nodes inside a captured graph (external events) for per-kernel timing."""
+
+    def __init__(self):
+        self.rt = None
+        for name in ("libcudart.so.13", "libcudart.so"):
+            try:
+                self.rt = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+
+    def ok(self):
+        return self.rt is not None
+
+    def event(self):
+        ev = ctypes.c_void_p()
+        if self.rt.cudaEventCreate(ctypes.byref(ev)) != 0:
+            raise RuntimeError("cudaEventCreate failed")
+        return ev
+
+    def record_external(self, ev, stream_handle):
+        # cudaEventRecordExternal = 1: an event record node when the stream is capturing
+        return self.rt.cudaEventRecordWithFlags(ev, ctypes.c_void_p(stream_handle), 1)
+
+    def elapsed_ms(self, a, b):
+        ms = ctypes.c_float()
+        if self.rt.cudaEventElapsedTime(ctypes.byref(ms), a, b) != 0:
+            return None
+        return ms.value
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    w = build_workload(device)
+    stream = torch.cuda.Stream(device)
+    torch.cuda.synchronize()
+    # eager warm-up (sets kernel attributes before capture)
+    with torch.cuda.stream(stream):
+        for i in range(4):
+            token_calls(w, i)
+    torch.cuda.synchronize()
+    # graph of one step; every 10th token's gate/up kernel bracketed by external event nodes
+    rt = CudaRt()
+    probes = []
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        h = torch.cuda.current_stream().cuda_stream
+        for i in range(TOKENS):
+            layer = w["layer"]
+            layer.route(w["x"][i:i + 1], w["wr"], w["tab"], None, T=1)
+            probe = rt.ok() and i % 10 == 5
+            if probe:
+                a, b = rt.event(), rt.event()
+                rt.record_external(a, h)
+            layer.experts(w["x"][i:i + 1], T=1, y=w["y"][i:i + 1])
+            if probe:
+                rt.record_external(b, h)
+                probes.append((a, b))
+    launches_per_step = 3 * TOKENS   # route, gate/up, down per token
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kernel_ms = []
+    with torch.cuda.stream(stream):
+        ev0.record()
+        for _ in range(args.steps):
+            g.replay()
+        ev1.record()
+    torch.cuda.synchronize()
+    if probes:
+        # the probe events hold the last replay's times
+        kernel_ms = [rt.elapsed_ms(a, b) for a, b in probes]
+        kernel_ms = [v for v in kernel_ms if v is not None]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * TOKENS / (ms_per_step / 1e3)
+    # end-to-end through the public API with host buffers: pinned x in, y out, every step
+    x_host = torch.empty((TOKENS, D), dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(w["x"].cpu())
+    y_host = torch.empty((TOKENS, D), dtype=torch.bfloat16, pin_memory=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(args.steps):
+            w["x"].copy_(x_host, non_blocking=True)
+            g.replay()
+            y_host.copy_(w["y"], non_blocking=True)
+        e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    status = int(w["layer"].status.item())
+    peaks, peak_kind = measured_peaks()
+    out = None
+    if rank == 0:
+        k_ms = statistics.mean(kernel_ms) if kernel_ms else None
+        achieved = (GATEUP_BYTES / (k_ms * 1e-3) / 1e9) if k_ms else None
+        peak = float(peaks["hbm_gbs"])
+        out = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp32 (e2m1 x bf16 exact products, fp32 accumulate)",
+            "data": "synthetic (seeded Philox FP4 experts, N(0,1) bf16 tokens, N(0,0.02) bf16 router)",
+            "config": dict(CONFIG, parallelism="replicas" if world > 1 else "single GPU"),
+            "roofline": {"bound": "hbm", "kernel": "decode_gateup_kernel (gate/up + SwiGLU, T=1)",
+                         "achieved": round(achieved, 1) if achieved else None, "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4) if achieved else None, "traffic": None,
+                         "bytes_per_launch": GATEUP_BYTES, "launch_ms": round(k_ms, 5) if k_ms else None,
+                         "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured" else "fallback 6.8 TB/s"},
+            "layer_roofline": {"bytes_per_token": ALG_BYTES_PER_TOKEN,
+                               "achieved_gbs": round(ALG_BYTES_PER_TOKEN * value / world / 1e9, 1),
+                               "frac": round(ALG_BYTES_PER_TOKEN * value / world / 1e9 / peak, 4)},
+            "e2e": {"value": round(world * TOKENS / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": TOKENS * D * 2, "d2h_bytes_per_step": TOKENS * D * 2},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "device_status": status,
+        }
+    return out, w
+
+
+# ---------------------------------------------------------------------------- oracle timing
+
+def oracle_sample(n_tokens, time_budget_s=None, x_bits=None, wr_bits=None, table=None):
+    """Time the oracle on the first tokens of the same workload; expert tensors are generated
+    beforehand (outside the timing)."""
+    import oracle
+    from synth import tensors as syn
+    if x_bits is None:
+        x_bits = syn.activations(0, 0, n_tokens, D, stream=7)
+        wr_bits = syn.router_weight(0, 0, E, D)
+        table = syn.permuted_slot_table(0, 0, E)
+    r = oracle.route_topk(x_bits[:n_tokens], wr_bits, None, table, K)
+    inv = {int(s): e for e, s in enumerate(table)}
+    cache = {}
+    for t in range(n_tokens):
+        for s in r["slots"][t]:
+            if int(s) not in cache:
+                cache[int(s)] = syn.expert_tensors(0, 0, inv[int(s)], D, F, *SCALE)
+    t0 = time.perf_counter()
+    done = 0
+    for t in range(n_tokens):
+        rr = oracle.route_topk(x_bits[t:t + 1], wr_bits, None, table, K)
+        z = np.zeros((K, D))
+        for j in range(K):
+            _, z[j] = oracle.expert_ffn(x_bits[t], cache[int(rr["slots"][0, j])])
+        oracle.combine(z, rr["weights"][0])
+        done += 1
+        if time_budget_s and time.perf_counter() - t0 > time_budget_s:
+            break
+    el = time.perf_counter() - t0
+    return done, el
+
+
+def cpu_baseline_block():
+    n, el = oracle_sample(24, time_budget_s=15.0)
+    return {"value": round(n / el, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "%d tokens of the same workload (full layer per token: exact router over 384 experts, "
+                      "6 experts' SwiGLU FFN in fp64, combine), single-threaded C, %.1f s" % (n, el)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    per_step = 2
+    for _ in range(args.warmup):
+        oracle_sample(per_step)
+    times = []
+    for _ in range(args.steps):
+        n, el = oracle_sample(per_step)
+        times.append(el / n)
+    tps = 1.0 / statistics.mean(times)
+    return {"metric": METRIC, "value": round(tps, 4), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * per_step / tps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle FFN), exact-then-fp32 router",
+            "data": "synthetic", "config": dict(CONFIG, parallelism="single host core"), "impl": "reference",
+            "cpu_baseline": {"value": round(tps, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": "%d tokens per step of the same workload" % per_step},
+            "e2e": {"value": round(tps, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local_rank = env_rank()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+    import fp4_routed_expert_gb300 as moe
+    moe.lib()
+    out, w = run_ours(args, rank, world, local_rank)
+    if rank == 0 and out is not None:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline_block()
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

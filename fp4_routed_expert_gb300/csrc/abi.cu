@@ -1,0 +1,202 @@
+// abi.cu -- the extern "C" entry points declared in include/fp4moe.h: argument checks on the
+// host, then kernel launches on the caller's stream.  Nothing here allocates, synchronises
+// or reads device memory back.
+#include <cstdio>
+
+#include "moe_internal.cuh"
+
+namespace fp4moe {
+
+int launch_route(const moe_dims* m, int T, const uint16_t* x, const uint16_t* wr, const float* bias,
+                 const int32_t* table, int32_t* ids, float* w, int32_t* slots, int32_t* status,
+                 char* ws, const WsLayout& L, cudaStream_t st, int num_sms);
+int launch_permute(const moe_dims* m, int T, const int32_t* ids, int32_t* offsets, int32_t* row_src,
+                   int32_t* row_dst, cudaStream_t st);
+int launch_decode_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x,
+                      const int32_t* slot, const float* w, uint16_t* y, int32_t* status, char* ws,
+                      const WsLayout& L, cudaStream_t st, int num_sms);
+int launch_prefill_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
+                       const int32_t* offsets, const int32_t* row_src, float* rows_out, int32_t* status, char* ws,
+                       const WsLayout& L, cudaStream_t st, int num_sms);
+int launch_combine(const moe_dims* m, int T, const float* rows, const int32_t* row_dst, const float* w,
+                   uint16_t* y, cudaStream_t st, int num_sms);
+
+// Gate/up interleave: destination row 2i <- gate row i, row 2i+1 <- up row i (32-bit words).
+__global__ void pack_interleave_kernel(const uint32_t* __restrict__ gate, const uint32_t* __restrict__ up,
+                                       uint32_t* __restrict__ dst, int rows, int words_per_row) {
+    long total = (long)rows * 2 * words_per_row;
+    for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+        long drow = idx / words_per_row;
+        int wi = (int)(idx % words_per_row);
+        long srow = drow >> 1;
+        const uint32_t* src = (drow & 1) ? up : gate;
+        dst[idx] = src[srow * words_per_row + wi];
+    }
+}
+
+static int num_sms_of_current_device() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+    if (dev < 64 && cache[dev]) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+static int check_ws(const moe_dims* m, int T, void* ws, size_t ws_bytes, WsLayout* out) {
+    if (!ws) return MOE_ERR_NULL;
+    if (!aligned16(ws)) return MOE_ERR_ALIGN;
+    WsLayout L = ws_layout(m, T);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    *out = L;
+    return MOE_OK;
+}
+
+static int check_arena(const moe_dims* m, const moe_arena* ar) {
+    if (!ar || !ar->base) return MOE_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(ar->base) & 1023u) != 0) return MOE_ERR_ARENA;
+    if (ar->slot_bytes != slot_layout(m->d, m->f).bytes || ar->num_slots <= 0) return MOE_ERR_ARENA;
+    return MOE_OK;
+}
+
+}  // namespace fp4moe
+
+using namespace fp4moe;
+
+extern "C" {
+
+int64_t moe_slot_bytes(const moe_dims* dims) {
+    if (!dims_ok(dims)) return -1;
+    return slot_layout(dims->d, dims->f).bytes;
+}
+
+size_t moe_workspace_bytes(const moe_dims* dims, int32_t T_max) {
+    if (!dims_ok(dims) || T_max < 0) return 0;
+    return ws_layout(dims, T_max).total;
+}
+
+int moe_workspace_init(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    WsLayout L;
+    int rc = check_ws(dims, 0, ws, ws_bytes, &L);
+    if (rc) return rc;
+    cudaError_t e = cudaMemsetAsync(static_cast<char*>(ws) + L.counter, 0, 4 * 64, (cudaStream_t)stream);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
+int moe_pack_expert(const moe_dims* dims, const uint8_t* gate_q, const uint8_t* gate_s, const uint8_t* up_q,
+                    const uint8_t* up_s, const uint8_t* down_q, const uint8_t* down_s, const moe_arena* arena,
+                    int32_t slot, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (!gate_q || !gate_s || !up_q || !up_s || !down_q || !down_s) return MOE_ERR_NULL;
+    int rc = check_arena(dims, arena);
+    if (rc) return rc;
+    if (slot < 0 || slot >= arena->num_slots) return MOE_ERR_ARENA;
+    if (!aligned4(gate_q) || !aligned4(gate_s) || !aligned4(up_q) || !aligned4(up_s)) return MOE_ERR_ALIGN;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int d = dims->d, f = dims->f;
+    SlotLayout L = slot_layout(d, f);
+    uint8_t* base = static_cast<uint8_t*>(arena->base) + (int64_t)slot * arena->slot_bytes;
+    int sms = num_sms_of_current_device();
+    pack_interleave_kernel<<<2 * sms, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(gate_q),
+                                                    reinterpret_cast<const uint32_t*>(up_q),
+                                                    reinterpret_cast<uint32_t*>(base + L.gu_q), f, d / 8);
+    pack_interleave_kernel<<<sms, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(gate_s),
+                                                reinterpret_cast<const uint32_t*>(up_s),
+                                                reinterpret_cast<uint32_t*>(base + L.gu_s), f, d / 128);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_LAUNCH;
+    if (cudaMemcpyAsync(base + L.dn_q, down_q, (size_t)d * f / 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
+    if (cudaMemcpyAsync(base + L.dn_s, down_s, (size_t)d * f / 32, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
+    return MOE_OK;
+}
+
+int moe_route_topk(const moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* w_router,
+                   const float* score_bias, const int32_t* expert_to_slot, int32_t* topk_ids, float* topk_w,
+                   int32_t* topk_slot, int32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (T < 0) return MOE_ERR_TOKENS;
+    if (!x || !w_router || !expert_to_slot || !topk_ids || !topk_w || !topk_slot || !dev_status) return MOE_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_ALIGN;
+    WsLayout L;
+    int rc = check_ws(dims, T, ws, ws_bytes, &L);
+    if (rc) return rc;
+    return launch_route(dims, T, x, w_router, score_bias, expert_to_slot, topk_ids, topk_w, topk_slot, dev_status,
+                        static_cast<char*>(ws), L, (cudaStream_t)stream, num_sms_of_current_device());
+}
+
+int moe_permute(const moe_dims* dims, int32_t T, const int32_t* topk_ids, int32_t* group_offsets, int32_t* row_src,
+                int32_t* row_dst, void* ws, size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (T < 0) return MOE_ERR_TOKENS;
+    if (!group_offsets || (T > 0 && (!topk_ids || !row_src || !row_dst))) return MOE_ERR_NULL;
+    WsLayout L;
+    int rc = check_ws(dims, T, ws, ws_bytes, &L);
+    if (rc) return rc;
+    return launch_permute(dims, T, topk_ids, group_offsets, row_src, row_dst, (cudaStream_t)stream);
+}
+
+int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, const uint16_t* x,
+                       const int32_t* topk_ids, const int32_t* topk_slot, const float* topk_w,
+                       const int32_t* group_offsets, const int32_t* row_src, const int32_t* row_dst, int32_t flags,
+                       float* rows_out, uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (T < 0) return MOE_ERR_TOKENS;
+    if (flags & ~MOE_FUSE_COMBINE) return MOE_ERR_FLAGS;
+    int rc = check_arena(dims, arena);
+    if (rc) return rc;
+    if (!x || !topk_ids || !topk_slot || !topk_w || !dev_status) return MOE_ERR_NULL;
+    if (!aligned16(x)) return MOE_ERR_ALIGN;
+    const bool fused = (flags & MOE_FUSE_COMBINE) != 0;
+    if (fused && !y) return MOE_ERR_NULL;
+    if (!fused && !rows_out) return MOE_ERR_NULL;
+    WsLayout L;
+    rc = check_ws(dims, T, ws, ws_bytes, &L);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    char* w = static_cast<char*>(ws);
+    int sms = num_sms_of_current_device();
+    if (T <= kDecodeMaxT && fused) {
+        return launch_decode_ffn(dims, arena, T, x, topk_slot, topk_w, y, dev_status, w, L, st, sms);
+    }
+    if (!group_offsets || !row_src || (fused && !row_dst)) return MOE_ERR_NULL;
+    if (rows_out && !aligned16(rows_out)) return MOE_ERR_ALIGN;
+    float* rows = fused ? reinterpret_cast<float*>(w + L.rows) : rows_out;
+    if (fused && T > kDecodeMaxT && L.rows + (size_t)T * dims->top_k * dims->d * 4 > ws_bytes) return MOE_ERR_WORKSPACE;
+    if (fused && T <= kDecodeMaxT) return MOE_ERR_FLAGS;   // unreachable: decode handles it
+    rc = launch_prefill_ffn(dims, arena, T, x, topk_slot, group_offsets, row_src, rows, dev_status, w, L, st, sms);
+    if (rc || !fused) return rc;
+    return launch_combine(dims, T, rows, row_dst, topk_w, y, st, sms);
+}
+
+int moe_combine(const moe_dims* dims, int32_t T, const float* rows, const int32_t* row_dst, const float* topk_w,
+                uint16_t* y, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (T < 0) return MOE_ERR_TOKENS;
+    if (T > 0 && (!rows || !row_dst || !topk_w || !y)) return MOE_ERR_NULL;
+    if (T > 0 && (!aligned16(rows) || !aligned16(y))) return MOE_ERR_ALIGN;
+    return launch_combine(dims, T, rows, row_dst, topk_w, y, (cudaStream_t)stream, num_sms_of_current_device());
+}
+
+const char* moe_status_str(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_NULL: return "a required pointer is NULL";
+        case MOE_ERR_DIMS: return "unsupported dims (d, f multiples of 128; 1 <= k <= E <= 1024; k <= 32)";
+        case MOE_ERR_TOKENS: return "token count out of range";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_ARENA: return "arena misaligned, wrong slot_bytes or slot out of range";
+        case MOE_ERR_FLAGS: return "unknown flags or missing output for the chosen flags";
+        case MOE_ERR_LAUNCH: return "kernel launch failed";
+        case MOE_ERR_ALIGN: return "pointer not sufficiently aligned";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

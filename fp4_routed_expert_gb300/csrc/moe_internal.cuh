@@ -1,0 +1,131 @@
+// moe_internal.cuh -- shared definitions of the routed-expert FP4 MoE library (sm_103a).
+//
+// Arena slot layout (private to this library; moe_pack_expert is its only writer):
+//   [0, f*d)                       gate/up codes, 2f rows of d/2 bytes; row 2i = gate row i,
+//                                  row 2i+1 = up row i (a gate row and its up row are adjacent)
+//   [f*d, f*d + f*d/16)            gate/up scales, 2f rows of d/32 bytes, same interleave
+//   [.., + d*f/2)                  down codes, d rows of f/2 bytes
+//   [.., + d*f/32)                 down scales, d rows of f/32 bytes
+// Codes keep the checkpoint's e2m1 nibble order (element 2i in the low nibble) and scales
+// are UE8M0 bytes, one per 32 consecutive K elements.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/fp4moe.h"
+
+namespace fp4moe {
+
+constexpr int kDecodeMaxT = 16;     // tokens handled by the decode regime
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kChunk = 32;          // K elements per UE8M0 scale = 16 code bytes
+
+struct SlotLayout {
+    int64_t gu_q, gu_s, dn_q, dn_s, bytes;
+};
+
+__host__ __device__ inline SlotLayout slot_layout(int d, int f) {
+    SlotLayout L;
+    int64_t fd = (int64_t)f * d;
+    L.gu_q = 0;
+    L.gu_s = fd;
+    L.dn_q = fd + fd / 16;
+    L.dn_s = L.dn_q + fd / 2;
+    int64_t end = L.dn_s + fd / 32;
+    L.bytes = (end + 1023) / 1024 * 1024;
+    return L;
+}
+
+inline bool dims_ok(const moe_dims* m) {
+    return m && m->d >= 128 && m->f >= 128 && m->d % 128 == 0 && m->f % 128 == 0 &&
+           m->num_experts >= 1 && m->num_experts <= kMaxExperts && m->top_k >= 1 &&
+           m->top_k <= kMaxTopK && m->top_k <= m->num_experts && m->d <= 65536 && m->f <= 65536;
+}
+
+// Workspace sections, each 256-byte aligned.  The persistent counters come first so that
+// their offset is the same for every token count; the other sections are per call.
+struct WsLayout {
+    size_t logit;       // fp32 [T_max, E]   fast router logits
+    size_t xnorm;       // fp32 [T_max]      ||x_t||_2
+    size_t wnorm;       // fp32 [E]          ||W_r[e]||_2
+    size_t counter;     // uint32 [64]       completion tickets (zeroed once, self-resetting)
+    size_t active;      // int32 [2 + 2E]    group plan: n_active, tiles, expert ids, tile prefix
+    size_t h;           // fp32 [T_max*k, f] SwiGLU output per (token, j) pair or permuted row
+    size_t rows;        // fp32 [T_max*k, d] per-row expert outputs (prefill with fused combine)
+    size_t total;
+};
+
+inline size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+inline WsLayout ws_layout(const moe_dims* m, int T_max) {
+    WsLayout w;
+    size_t o = 0;
+    size_t T = (size_t)(T_max > 0 ? T_max : 1), E = (size_t)m->num_experts, k = (size_t)m->top_k;
+    w.counter = o; o = align256(o + 4 * 64);     // first: its offset must not depend on T
+    w.logit = o;   o = align256(o + 4 * T * E);
+    w.xnorm = o;   o = align256(o + 4 * T);
+    w.wnorm = o;   o = align256(o + 4 * E);
+    w.active = o;  o = align256(o + 4 * (2 + 2 * E));
+    w.h = o;       o = align256(o + 4 * T * k * (size_t)m->f);
+    w.rows = o;
+    if (T_max > kDecodeMaxT) o = align256(o + 4 * T * k * (size_t)m->d);
+    w.total = o;
+    return w;
+}
+
+// Counters inside the counter section.
+enum { kCtrRoute = 0, kCtrDecodeUp = 1 };
+
+// ---------------------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// bf16 from fp32, round to nearest even (NaN kept quiet).
+__device__ __forceinline__ uint16_t f32_to_bf16(float v) {
+    uint32_t u = __float_as_uint(v);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+// 2^(b-127) for a UE8M0 byte b < 255 (b = 0 gives the fp32 subnormal 2^-127).
+__device__ __forceinline__ float ue8m0_to_f32(uint32_t b) {
+    return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
+}
+
+// e2m1 code in nibble position i of w, as an fp32 bit pattern equal to code * 2^-126:
+// the 3 magnitude bits (2 exponent, 1 mantissa) land in fp32 exponent bits 23-24 and
+// mantissa bit 22, so exponent 0 codes become fp32 subnormals of the same relative value.
+template <int I>
+__device__ __forceinline__ float e2m1_scaled(uint32_t w) {
+    uint32_t mag = (I <= 5) ? (w << (22 - 4 * I)) : (w >> (4 * I - 22));
+    uint32_t sgn = (I <= 7) ? (w << (28 - 4 * I)) : 0u;
+    return __uint_as_float((mag & 0x01C00000u) | (sgn & 0x80000000u));
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Power-of-two exponent p (as an integer) such that x * 2^p keeps every |x| below 2^64 and
+// every code*x product within the fp32 normal range for |x| >= 2^-60 * max|x|.
+__device__ __forceinline__ int prescale_exponent(float amax) {
+    int e = 0;
+    if (amax > 0.f) e = ((__float_as_uint(amax) >> 23) & 0xFF) - 127;   // floor(log2 amax)
+    int p = 100 - (e > 0 ? e : 0);                                        // amax * 2^p < 2^101
+    if (p > 100) p = 100;
+    return p;
+}
+
+// 2^p as float for -126 <= p <= 127.
+__device__ __forceinline__ float exp2i(int p) { return __uint_as_float((uint32_t)(p + 127) << 23); }
+
+}  // namespace fp4moe

@@ -1,0 +1,522 @@
+// route.cu -- router logits, certified top-k selection and slot lookup (sm_103a).
+//
+// What is computed (per token t, expert e):
+//   logit l32 = the exact dot product x[t] . W_r[e] rounded once to fp32
+//   score s32 = fp32(1 / (1 + exp(-(double)l32)))
+//   key       = fp32(s32 + bias[e])            (-inf when expert_to_slot[e] < 0)
+//   top-k keys, ties to the lower expert id; weights w_j = s_j / sum s (fp32, ascending id)
+// The pages ("Start the expert reads before the GPU is done", 28 September follow-up) name
+// the router and its top-k but no formula; the exact-then-round logit makes the chosen set
+// independent of summation order.
+//
+// How the device reaches the exact set without computing every exact logit:
+//  1. fast logit lf: fp32 FMA chains with at most L roundings on any path, so
+//       |lf - exact| <= gamma_L * sum|x_k w_k| <= gamma_L * ||x|| ||w||   (Cauchy-Schwarz),
+//     gamma_L = L u / (1 - L u), u = 2^-24, inflated by 2^-10 for the norms' own rounding;
+//  2. the logit interval maps through the monotone sigmoid (fp32 sigmoid with a 2^-20
+//     absolute margin that covers its error and the final fp32 rounding) and the bias add
+//     (directed rounding) into a key interval [klo, khi] that contains the exact key;
+//  3. S = top-k by the point estimate; an expert of S whose klo exceeds every outside khi is
+//     certainly chosen, an outside expert whose khi is below every klo of S certainly not;
+//  4. the rest are recomputed exactly (integer Kulisch accumulation of the bf16 products,
+//     one rounding to fp32, double sigmoid) and ranked by exact key.
+#include "moe_internal.cuh"
+
+namespace fp4moe {
+
+struct RouteArgs {
+    int T, d, E, k;
+    const uint16_t* x;
+    const uint16_t* wr;
+    const float* bias;
+    const int32_t* table;
+    int32_t* ids;
+    float* w;
+    int32_t* slots;
+    int32_t* status;
+    float* logit;      // [T, E]
+    float* xnorm;      // [T]
+    float* wnorm;      // [E]
+    unsigned* counter;
+    float bound_coef;  // gamma_L * (1 + 2^-10)
+};
+
+// ------------------------------------------------------------------ exact logit (Kulisch)
+
+constexpr int kLimbs = 18;   // 18 x 32 bits hold any sum of up to 2^30 bf16*bf16 products
+constexpr int kUnit = 266;   // fixed point unit 2^-266 (smallest product quantum)
+
+__device__ __forceinline__ uint32_t limb_window(const uint32_t* dig, int bit) {
+    // 32 bits of the big number starting at bit index `bit` (bit >= 0)
+    int li = bit >> 5, sh = bit & 31;
+    uint64_t lo = dig[li];
+    uint64_t hi = (li + 1 < kLimbs) ? dig[li + 1] : 0u;
+    return (uint32_t)(((hi << 32) | lo) >> sh);
+}
+
+// Exact x.w rounded once to fp32, computed by the whole warp (every lane returns it).
+__device__ float exact_dot_bf16_warp(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w,
+                                     int d, int lane) {
+    long long acc[kLimbs];
+#pragma unroll
+    for (int i = 0; i < kLimbs; ++i) acc[i] = 0;
+    for (int kk = lane; kk < d; kk += 32) {
+        uint32_t bx = x[kk], bw = w[kk];
+        uint32_t ex = (bx >> 7) & 0xFFu, ew = (bw >> 7) & 0xFFu;
+        uint32_t mx = (bx & 0x7Fu) | (ex ? 0x80u : 0u);
+        uint32_t mw = (bw & 0x7Fu) | (ew ? 0x80u : 0u);
+        uint32_t P = mx * mw;
+        if (P == 0) continue;
+        int pos = (int)(ex ? ex : 1u) + (int)(ew ? ew : 1u) - 268 + kUnit;   // (e-134) twice
+        uint64_t v = (uint64_t)P << (pos & 31);
+        long long lo = (long long)(v & 0xFFFFFFFFull), hi = (long long)(v >> 32);
+        if ((bx ^ bw) & 0x8000u) { lo = -lo; hi = -hi; }
+        acc[pos >> 5] += lo;
+        acc[(pos >> 5) + 1] += hi;
+    }
+#pragma unroll
+    for (int i = 0; i < kLimbs; ++i) acc[i] = warp_sum(acc[i]);
+    // carry-normalise; a final carry of -1 means a negative total (two's complement digits)
+    uint32_t dig[kLimbs];
+    long long carry = 0;
+#pragma unroll
+    for (int i = 0; i < kLimbs; ++i) {
+        long long v = acc[i] + carry;
+        long long dgt = v & 0xFFFFFFFFll;
+        dig[i] = (uint32_t)dgt;
+        carry = (v - dgt) >> 32;   // exact: v - dgt is a multiple of 2^32
+    }
+    bool neg = carry < 0;
+    if (neg) {
+        unsigned long long c = 1;
+#pragma unroll
+        for (int i = 0; i < kLimbs; ++i) {
+            unsigned long long v = (unsigned long long)(uint32_t)(~dig[i]) + c;
+            dig[i] = (uint32_t)v;
+            c = v >> 32;
+        }
+    }
+    int msb = -1;
+    for (int i = kLimbs - 1; i >= 0 && msb < 0; --i)
+        if (dig[i]) msb = i * 32 + 31 - __clz(dig[i]);
+    if (msb < 0) return 0.0f;
+    int q = msb - 23;                       // 24 significant bits ...
+    if (q < kUnit - 149) q = kUnit - 149;   // ... but no quantum below 2^-149
+    uint32_t r = (msb >= q) ? (limb_window(dig, q) & ((msb - q + 1 >= 32) ? 0xFFFFFFFFu : ((1u << (msb - q + 1)) - 1u))) : 0u;
+    bool half = (limb_window(dig, q - 1) & 1u) != 0;
+    bool sticky = false;
+    {
+        int below = q - 1;                  // bits [0, below) are the sticky bits
+        int full = below >> 5;
+        for (int i = 0; i < full && !sticky; ++i) sticky = dig[i] != 0;
+        int rem = below & 31;
+        if (!sticky && rem) sticky = (dig[full] & ((1u << rem) - 1u)) != 0;
+    }
+    if (half && (sticky || (r & 1u))) r += 1;
+    float mag = scalbnf((float)r, q - kUnit);   // exact, or +inf beyond the fp32 range
+    return neg ? -mag : mag;
+}
+
+__device__ __forceinline__ float sigmoid_fast(float v) { return 1.0f / (1.0f + expf(-v)); }
+
+__device__ __forceinline__ float sigmoid_exact32(float l32) {
+    return __double2float_rn(1.0 / (1.0 + exp(-(double)l32)));
+}
+
+// ------------------------------------------------------------------ certified selection
+
+struct Cand {
+    float key;
+    int e;
+};
+
+// (key desc, id asc): is a better than b?
+__device__ __forceinline__ bool better(float ka, int ea, float kb, int eb) {
+    if (eb < 0) return ea >= 0;
+    if (ea < 0) return false;
+    return ka > kb || (ka == kb && ea < eb);
+}
+
+__device__ __forceinline__ void warp_best(float& k, int& e) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        float ko = __shfl_xor_sync(0xffffffffu, k, o);
+        int eo = __shfl_xor_sync(0xffffffffu, e, o);
+        if (better(ko, eo, k, e)) { k = ko; e = eo; }
+    }
+}
+
+// One warp selects the experts of token t.  EPL = experts per lane (E <= 32 * EPL).
+template <int EPL>
+__device__ void select_token(const RouteArgs& a, int t, int lane) {
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const float* lrow = a.logit + (size_t)t * a.E;
+    const float xn = __ldcg(a.xnorm + t);
+    float kf[EPL], klo[EPL], khi[EPL], sv[EPL], exk[EPL];
+    uint32_t valid = 0, picked = 0, exact_done = 0;
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+        int e = lane + 32 * m;
+        kf[m] = klo[m] = khi[m] = NEG_INF;
+        sv[m] = 0.f;
+        exk[m] = NEG_INF;
+        if (e < a.E && a.table[e] >= 0) {
+            valid |= 1u << m;
+            float l = __ldcg(lrow + e);
+            float delta = fmaf(a.bound_coef * xn, __ldcg(a.wnorm + e), 7.5e-37f);
+            delta = __fmul_ru(delta, 1.0f + 1.0f / 1048576.0f);
+            float lo = __fsub_rd(l, delta), hi = __fadd_ru(l, delta);
+            float b = a.bias ? a.bias[e] : 0.0f;
+            sv[m] = sigmoid_fast(l);
+            kf[m] = sv[m] + b;
+            const float margin = 1.0f / 1048576.0f;   // 2^-20
+            klo[m] = __fadd_rd(__fsub_rd(sigmoid_fast(lo), margin), b);
+            khi[m] = __fadd_ru(__fadd_ru(sigmoid_fast(hi), margin), b);
+        }
+    }
+    // S = top-k by point estimate
+    int nsel = 0;
+    for (int j = 0; j < a.k; ++j) {
+        float bk = NEG_INF;
+        int be = -1;
+#pragma unroll
+        for (int m = 0; m < EPL; ++m)
+            if (((valid & ~picked) >> m) & 1u)
+                if (better(kf[m], lane + 32 * m, bk, be)) { bk = kf[m]; be = lane + 32 * m; }
+        warp_best(bk, be);
+        if (be < 0) break;
+        if ((be & 31) == lane) picked |= 1u << (be >> 5);
+        ++nsel;
+    }
+    if (nsel < a.k && lane == 0) atomicOr(a.status, MOE_STATUS_FEW_RESIDENT);
+    // interval thresholds
+    float min_lo_in = __int_as_float(0x7f800000), max_hi_out = NEG_INF;
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+        if ((picked >> m) & 1u) min_lo_in = fminf(min_lo_in, klo[m]);
+        else if ((valid >> m) & 1u) max_hi_out = fmaxf(max_hi_out, khi[m]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        min_lo_in = fminf(min_lo_in, __shfl_xor_sync(0xffffffffu, min_lo_in, o));
+        max_hi_out = fmaxf(max_hi_out, __shfl_xor_sync(0xffffffffu, max_hi_out, o));
+    }
+    uint32_t certain = 0, uncertain = 0;
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+        bool p = (picked >> m) & 1u, v = (valid >> m) & 1u;
+        if (p && klo[m] > max_hi_out) certain |= 1u << m;
+        else if (p || (v && khi[m] >= min_lo_in)) uncertain |= 1u << m;
+    }
+    uint32_t final_mask = certain;
+    int n_unc = __popc(uncertain);
+    n_unc = warp_sum(n_unc);
+    if (n_unc > 0) {
+        int n_cert = warp_sum(__popc(certain));
+        int need = nsel - n_cert;
+        // exact keys of every uncertain expert, one expert at a time by the whole warp
+        const uint16_t* xt = a.x + (size_t)t * a.d;
+#pragma unroll 1
+        for (int m = 0; m < EPL; ++m) {
+            uint32_t bal = __ballot_sync(0xffffffffu, (uncertain >> m) & 1u);
+            while (bal) {
+                int src = __ffs(bal) - 1;
+                bal &= bal - 1;
+                int e = src + 32 * m;
+                float l32 = exact_dot_bf16_warp(xt, a.wr + (size_t)e * a.d, a.d, lane);
+                float s32 = sigmoid_exact32(l32);
+                if (lane == src) {
+                    float b = a.bias ? a.bias[e] : 0.0f;
+                    exk[m] = __fadd_rn(s32, b);
+                    sv[m] = s32;
+                    exact_done |= 1u << m;
+                }
+            }
+        }
+        uint32_t chosen = 0;
+        for (int j = 0; j < need; ++j) {
+            float bk = NEG_INF;
+            int be = -1;
+#pragma unroll
+            for (int m = 0; m < EPL; ++m)
+                if (((uncertain & ~chosen) >> m) & 1u)
+                    if (better(exk[m], lane + 32 * m, bk, be)) { bk = exk[m]; be = lane + 32 * m; }
+            warp_best(bk, be);
+            if (be < 0) break;
+            if ((be & 31) == lane) chosen |= 1u << (be >> 5);
+        }
+        final_mask |= chosen;
+    }
+    (void)exact_done;
+    // outputs in ascending expert id: e = lane + 32 m, so m outer, lane inner
+    float sum = 0.0f;
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+        uint32_t bal = __ballot_sync(0xffffffffu, (final_mask >> m) & 1u);
+        while (bal) {
+            int src = __ffs(bal) - 1;
+            bal &= bal - 1;
+            sum += __shfl_sync(0xffffffffu, sv[m], src);
+        }
+    }
+    int pos = 0;
+    int32_t* ids = a.ids + (size_t)t * a.k;
+    float* wo = a.w + (size_t)t * a.k;
+    int32_t* so = a.slots + (size_t)t * a.k;
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+        uint32_t bal = __ballot_sync(0xffffffffu, (final_mask >> m) & 1u);
+        if ((final_mask >> m) & 1u) {
+            int idx = pos + __popc(bal & ((1u << lane) - 1u));
+            int e = lane + 32 * m;
+            ids[idx] = e;
+            wo[idx] = (sum > 0.0f) ? __fdiv_rn(sv[m], sum) : 0.0f;
+            so[idx] = a.table[e];
+        }
+        pos += __popc(bal);
+    }
+    for (int j = pos + lane; j < a.k; j += 32) {
+        ids[j] = -1;
+        wo[j] = 0.0f;
+        so[j] = -1;
+    }
+}
+
+template <int EPL>
+__device__ void select_tokens_block(const RouteArgs& a, int t0, int tstep) {
+    int lane = threadIdx.x & 31;
+    for (int t = t0; t < a.T; t += tstep) select_token<EPL>(a, t, lane);
+}
+
+#define FP4MOE_EPL_DISPATCH(E, ...)                                   \
+    do {                                                              \
+        int epl_ = ((E) + 31) / 32;                                   \
+        if (epl_ <= 2) { constexpr int EPL = 2; __VA_ARGS__; }        \
+        else if (epl_ <= 4) { constexpr int EPL = 4; __VA_ARGS__; }   \
+        else if (epl_ <= 8) { constexpr int EPL = 8; __VA_ARGS__; }   \
+        else if (epl_ <= 12) { constexpr int EPL = 12; __VA_ARGS__; } \
+        else if (epl_ <= 16) { constexpr int EPL = 16; __VA_ARGS__; } \
+        else if (epl_ <= 24) { constexpr int EPL = 24; __VA_ARGS__; } \
+        else { constexpr int EPL = 32; __VA_ARGS__; }                 \
+    } while (0)
+
+// ------------------------------------------------------------------ small T: one warp per expert
+
+// Fast logits for T <= kDecodeMaxT; the last block to finish selects every token.
+// Per lane: ceil(d/256) chunks of 8 bf16, an FMA chain of 8 per chunk, then 5 shuffle adds.
+template <int MAXT>
+__global__ void __launch_bounds__(128) route_small_kernel(RouteArgs a) {
+    extern __shared__ uint4 smem_u4[];
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_u4);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const int T = a.T, d = a.d, E = a.E;
+    const int nvec = d / 8;   // 16-byte vectors per row
+    for (int i = tid; i < T * nvec; i += blockDim.x)
+        smem_u4[i] = reinterpret_cast<const uint4*>(a.x)[i];
+    __syncthreads();
+    const int gw = blockIdx.x * nwarps + warp, nw = gridDim.x * nwarps;
+    for (int e = gw; e < E; e += nw) {
+        const uint4* wrow = reinterpret_cast<const uint4*>(a.wr + (size_t)e * d);
+        float acc[MAXT];
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t) acc[t] = 0.f;
+        float wsq = 0.f;
+        constexpr int B = 8;   // vectors in flight per lane
+        for (int c0 = lane; c0 < nvec; c0 += 32 * B) {
+            uint4 wv[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                int c = c0 + 32 * b;
+                wv[b] = (c < nvec) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                int c = c0 + 32 * b;
+                if (c >= nvec) break;
+                float w8[8] = {bf16_lo(wv[b].x), bf16_hi(wv[b].x), bf16_lo(wv[b].y), bf16_hi(wv[b].y),
+                               bf16_lo(wv[b].z), bf16_hi(wv[b].z), bf16_lo(wv[b].w), bf16_hi(wv[b].w)};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) wsq = fmaf(w8[i], w8[i], wsq);
+#pragma unroll
+                for (int t = 0; t < MAXT; ++t) {
+                    if (t >= T) break;
+                    uint4 xv = reinterpret_cast<const uint4*>(xs + (size_t)t * d)[c];
+                    float x8[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
+                                   bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[t] = fmaf(x8[i], w8[i], acc[t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < MAXT; ++t) {
+            if (t >= T) break;
+            float v = warp_sum(acc[t]);
+            if (lane == 0) a.logit[(size_t)t * E + e] = v;
+        }
+        wsq = warp_sum(wsq);
+        if (lane == 0) a.wnorm[e] = sqrtf(wsq);
+    }
+    if (blockIdx.x == 0) {
+        for (int t = warp; t < T; t += nwarps) {
+            float s = 0.f;
+            for (int i = lane; i < d; i += 32) {
+                float v = bf16_to_f32(xs[(size_t)t * d + i]);
+                s = fmaf(v, v, s);
+            }
+            s = warp_sum(s);
+            if (lane == 0) a.xnorm[t] = sqrtf(s);
+        }
+    }
+    // completion ticket: the last block to arrive selects for every token
+    __shared__ int is_last;
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        unsigned tk = atomicAdd(a.counter, 1u);
+        is_last = (tk == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    FP4MOE_EPL_DISPATCH(E, select_tokens_block<EPL>(a, warp, nwarps));
+    __syncthreads();
+    if (tid == 0) atomicExch(a.counter, 0u);
+}
+
+// ------------------------------------------------------------------ large T: tiled logits
+
+// 64 tokens x 64 experts per block, 4x4 per thread, K staged 32 at a time.  Each output is
+// accumulated in chunks of 256 products (fresh partial sums) added into a running total, so
+// every rounding path has at most 256 + ceil(d/256) roundings.
+constexpr int kTileT = 64, kTileE = 64, kTileK = 32, kChunkK = 256;
+
+__global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
+    __shared__ float xs[kTileK][kTileT + 4];
+    __shared__ float ws[kTileK][kTileE + 4];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int t0 = blockIdx.y * kTileT, e0 = blockIdx.x * kTileE;
+    float tot[4][4], part[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tot[i][j] = part[i][j] = 0.f;
+    for (int k0 = 0; k0 < a.d; k0 += kTileK) {
+        // 64 rows x 32 bf16 = 256 vectors of 8 per operand
+        {
+            int r = tid >> 2, c = (tid & 3) * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (t0 + r < a.T) v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + r) * a.d + k0 + c));
+            float f8[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                           bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xs[c + i][r] = f8[i];
+            uint4 u = make_uint4(0, 0, 0, 0);
+            if (e0 + r < a.E) u = __ldg(reinterpret_cast<const uint4*>(a.wr + (size_t)(e0 + r) * a.d + k0 + c));
+            float g8[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                           bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ws[c + i][r] = g8[i];
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < kTileK; ++kk) {
+            float4 xa = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
+            float4 wb = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+            float xv[4] = {xa.x, xa.y, xa.z, xa.w}, wv[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) part[i][j] = fmaf(xv[i], wv[j], part[i][j]);
+        }
+        __syncthreads();
+        if (((k0 + kTileK) % kChunkK) == 0 || k0 + kTileK >= a.d) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) { tot[i][j] += part[i][j]; part[i][j] = 0.f; }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int t = t0 + ty * 4 + i;
+        if (t >= a.T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            int e = e0 + tx * 4 + j;
+            if (e < a.E) a.logit[(size_t)t * a.E + e] = tot[i][j];
+        }
+    }
+}
+
+// ||x_t|| and ||W_r[e]|| (one warp per row).
+__global__ void route_norms_kernel(RouteArgs a) {
+    int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    int rows = a.T + a.E;
+    for (int r = gw; r < rows; r += (gridDim.x * blockDim.x) >> 5) {
+        const uint16_t* p = (r < a.T) ? a.x + (size_t)r * a.d : a.wr + (size_t)(r - a.T) * a.d;
+        float s = 0.f;
+        for (int i = lane; i < a.d; i += 32) {
+            float v = bf16_to_f32(p[i]);
+            s = fmaf(v, v, s);
+        }
+        s = warp_sum(s);
+        if (lane == 0) {
+            if (r < a.T) a.xnorm[r] = sqrtf(s);
+            else a.wnorm[r - a.T] = sqrtf(s);
+        }
+    }
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(128) route_select_kernel(RouteArgs a) {
+    int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
+    select_tokens_block<EPL>(a, gw, nw);
+}
+
+// ------------------------------------------------------------------ host side
+
+static float gamma_coef(int L) {
+    double u = 1.0 / 16777216.0;
+    double g = L * u / (1.0 - L * u);
+    return (float)(g * (1.0 + 1.0 / 1024.0));
+}
+
+int launch_route(const moe_dims* m, int T, const uint16_t* x, const uint16_t* wr, const float* bias,
+                 const int32_t* table, int32_t* ids, float* w, int32_t* slots, int32_t* status,
+                 char* ws, const WsLayout& L, cudaStream_t st, int num_sms) {
+    RouteArgs a;
+    a.T = T; a.d = m->d; a.E = m->num_experts; a.k = m->top_k;
+    a.x = x; a.wr = wr; a.bias = bias; a.table = table;
+    a.ids = ids; a.w = w; a.slots = slots; a.status = status;
+    a.logit = reinterpret_cast<float*>(ws + L.logit);
+    a.xnorm = reinterpret_cast<float*>(ws + L.xnorm);
+    a.wnorm = reinterpret_cast<float*>(ws + L.wnorm);
+    a.counter = reinterpret_cast<unsigned*>(ws + L.counter) + kCtrRoute;
+    if (T == 0) return MOE_OK;
+    if (T <= kDecodeMaxT) {
+        int per_lane = (m->d / 8 + 31) / 32;
+        a.bound_coef = gamma_coef(per_lane * 8 + 5);
+        int warps = 4;
+        int blocks = (a.E + warps - 1) / warps;
+        size_t smem = (size_t)T * m->d * 2;
+        if (smem > 48 * 1024) {
+            if (cudaFuncSetAttribute(route_small_kernel<kDecodeMaxT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem) != cudaSuccess)
+                return MOE_ERR_LAUNCH;
+        }
+        route_small_kernel<kDecodeMaxT><<<blocks, warps * 32, smem, st>>>(a);
+    } else {
+        a.bound_coef = gamma_coef(kChunkK + (m->d + kChunkK - 1) / kChunkK + 1);
+        dim3 grid((a.E + kTileE - 1) / kTileE, (T + kTileT - 1) / kTileT);
+        route_tiled_kernel<<<grid, 256, 0, st>>>(a);
+        int rows = T + a.E;
+        route_norms_kernel<<<(rows + 7) / 8, 256, 0, st>>>(a);
+        int sel_blocks = (T + 3) / 4;
+        FP4MOE_EPL_DISPATCH(a.E, route_select_kernel<EPL><<<sel_blocks, 128, 0, st>>>(a));
+    }
+    (void)num_sms;
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
+}  // namespace fp4moe

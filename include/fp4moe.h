@@ -1,0 +1,150 @@
+/*
+ * fp4moe.h -- C ABI of the GB300 (sm_103a) routed-expert FP4 MoE layer.
+ *
+ * The layer (DeepSeek-V4.1-Flash routed experts) per token t:
+ *   a1  l[t,e]   = x[t] . W_r[e]                                  router logits
+ *   a2  s = sigmoid(l); key = s + bias[e] (-inf when expert e has no slot);
+ *       top-k keys (ties to the lower expert id); w_j = s_j / sum(s)   selection
+ *   a3  slot_j   = expert_to_slot[id_j]                           slot lookup
+ *   a4  rows grouped by expert (prefill)                           permutation
+ *   a5  h        = silu(W_gate x) * (W_up x)                       gate/up + SwiGLU
+ *   a6  y[t]     = sum_j w_j * (W_down h_j), fixed ascending-id order, bf16 out
+ * Experts are FP4: e2m1 codes, one UE8M0 scale per 32 consecutive K elements, three
+ * f x d matrices per expert ("DeepSeek-V4.1-Flash on a single NVIDIA DGX Spark", section
+ * "Why it is built this way": 15,360 x 3 x 2304 x 5120, 288.8 GB at FP4 + UE8M0/32).
+ * Experts sit in a resident slot arena reached through an expert->slot table (same page,
+ * headline list: a 73.8 GB arena of slots).  Rows are written once and summed by a
+ * separate fixed-order step ("Start the expert reads before the GPU is done",
+ * 30 September follow-up).
+ *
+ * Conventions for every call:
+ *  - Pointers are DEVICE pointers unless stated.  The caller owns every buffer; no call
+ *    allocates device memory, synchronises the device or reads results back.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*; NULL is the
+ *    legacy default stream).
+ *  - bf16 tensors are raw 16-bit bfloat16 bit patterns (uint16_t).  All tensors are dense
+ *    row-major with the shapes given.
+ *  - Return value: MOE_OK (0), or a negative MOE_ERR_* for an argument error detected on
+ *    the host before anything is launched (nothing was enqueued).
+ *  - Device-side conditions are OR-ed into *dev_status (an int32 the caller zeroes and reads
+ *    after its own synchronisation): MOE_STATUS_* bits below.
+ *  - Calls on different streams are independent when given different workspaces.
+ */
+#ifndef FP4MOE_H
+#define FP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Per-layer shape.  d (hidden) and f (expert intermediate) must be multiples of 128;
+ * 1 <= top_k <= num_experts <= 1024. */
+typedef struct {
+    int32_t d;
+    int32_t f;
+    int32_t num_experts;
+    int32_t top_k;
+} moe_dims;
+
+/* Resident expert arena: num_slots slots of slot_bytes each, starting at base (device
+ * memory, 1024-byte aligned).  slot_bytes must equal moe_slot_bytes(dims).  The layout
+ * inside a slot is private to this library; moe_pack_expert is its only writer. */
+typedef struct {
+    void* base;
+    int64_t slot_bytes;
+    int32_t num_slots;
+} moe_arena;
+
+enum {
+    MOE_OK = 0,
+    MOE_ERR_NULL = -1,       /* a required pointer is NULL */
+    MOE_ERR_DIMS = -2,       /* unsupported d, f, num_experts or top_k */
+    MOE_ERR_TOKENS = -3,     /* T < 0 or T beyond what the workspace was sized for */
+    MOE_ERR_WORKSPACE = -4,  /* ws_bytes smaller than moe_workspace_bytes(dims, T) */
+    MOE_ERR_ARENA = -5,      /* arena base misaligned, slot_bytes mismatch or slot index out of range */
+    MOE_ERR_FLAGS = -6,      /* unknown flag or inconsistent optional outputs */
+    MOE_ERR_LAUNCH = -7,     /* a kernel launch was rejected by the CUDA runtime */
+    MOE_ERR_ALIGN = -8       /* a pointer is not 16-byte aligned */
+};
+
+#define MOE_STATUS_FEW_RESIDENT 1  /* a token had fewer than top_k resident experts */
+#define MOE_STATUS_BAD_SLOT 2      /* a slot id outside [0, num_slots): that term was skipped */
+#define MOE_STATUS_TIMEOUT 4       /* a bounded device wait gave up */
+
+/* Flags of moe_expert_ffn_fp4. */
+#define MOE_FUSE_COMBINE 1         /* write y directly (fixed-order combine fused in) */
+
+/* Bytes of one arena slot: 3*f*d/2 code bytes + 3*f*d/32 scale bytes, rounded up to
+ * 1024 (18,800,640 at d=5120, f=2304).  Returns -1 for unsupported dims. */
+int64_t moe_slot_bytes(const moe_dims* dims);
+
+/* Workspace bytes needed by every call of this API for up to T_max tokens.  One workspace
+ * may be shared by the calls of one layer issued in order on one stream.  Its contents
+ * between calls are private; the first call on a new workspace needs no initialisation
+ * beyond what moe_workspace_init performs.  Returns 0 for unsupported dims. */
+size_t moe_workspace_bytes(const moe_dims* dims, int32_t T_max);
+
+/* Zero the workspace's persistent counters (once, after allocating it). */
+int moe_workspace_init(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream);
+
+/* Pack one expert from the canonical (checkpoint) layout into arena slot `slot`.
+ * Canonical layout, device pointers, two e2m1 codes per byte (element 2i in the low
+ * nibble), one UE8M0 byte per 32 consecutive K elements, row-major:
+ *   gate_q, up_q : uint8 [f, d/2]     gate_s, up_s : uint8 [f, d/32]
+ *   down_q       : uint8 [d, f/2]     down_s       : uint8 [d, f/32]
+ * The source buffers may be reused once the stream has passed this call. */
+int moe_pack_expert(const moe_dims* dims, const uint8_t* gate_q, const uint8_t* gate_s,
+                    const uint8_t* up_q, const uint8_t* up_s, const uint8_t* down_q,
+                    const uint8_t* down_s, const moe_arena* arena, int32_t slot, void* stream);
+
+/* a1-a3: router scoring, top-k selection and slot lookup for T tokens.
+ *   x              bf16 [T, d]
+ *   w_router       bf16 [E, d]
+ *   score_bias     fp32 [E] added to the score for selection only, or NULL
+ *   expert_to_slot int32 [E]; -1 marks an expert without a slot (never selected)
+ * Outputs, per token in ascending expert id:
+ *   topk_ids int32 [T, k], topk_w fp32 [T, k] (sum to 1), topk_slot int32 [T, k];
+ *   missing entries (fewer than k resident) are -1 / 0 / -1 with MOE_STATUS_FEW_RESIDENT.
+ * The logit is the exact dot product rounded once to fp32 and the score is
+ * fp32(1/(1+exp(-logit))) from a double evaluation; the chosen set is certified against
+ * these exact values (fast fp32 logits with a rigorous error bound, exact recomputation of
+ * any expert whose key interval straddles the k-th place). */
+int moe_route_topk(const moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* w_router,
+                   const float* score_bias, const int32_t* expert_to_slot, int32_t* topk_ids,
+                   float* topk_w, int32_t* topk_slot, int32_t* dev_status, void* ws,
+                   size_t ws_bytes, void* stream);
+
+/* a4: stable grouping of the T*k (token, j) rows by expert id (tokens ascending inside a
+ * group).  group_offsets int32 [E+1] (group e = rows [off[e], off[e+1]), off[E] = rows
+ * with a valid id), row_src int32 [T*k] (row r came from t*k + j; entries >= off[E] are
+ * -1), row_dst int32 [T*k] (the inverse; -1 for id -1). */
+int moe_permute(const moe_dims* dims, int32_t T, const int32_t* topk_ids, int32_t* group_offsets,
+                int32_t* row_src, int32_t* row_dst, void* ws, size_t ws_bytes, void* stream);
+
+/* a5-a6: the experts.  Reads x bf16 [T, d], the routing outputs and the permutation
+ * (group_offsets/row_src/row_dst from moe_permute of the same topk_ids).
+ * flags = MOE_FUSE_COMBINE: writes y bf16 [T, d] (rows_out may be NULL).
+ * flags = 0: writes rows_out fp32 [T*k, d] (row r = z for row_src[r], unweighted); y unused.
+ * Slots outside [0, num_slots) set MOE_STATUS_BAD_SLOT and contribute zero. */
+int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, const uint16_t* x,
+                       const int32_t* topk_ids, const int32_t* topk_slot, const float* topk_w,
+                       const int32_t* group_offsets, const int32_t* row_src, const int32_t* row_dst,
+                       int32_t flags, float* rows_out, uint16_t* y, int32_t* dev_status, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/* a6 (unfused): y[t] = bf16( sum_j topk_w[t,j] * rows[row_dst[t*k+j]] ) in ascending j,
+ * skipping row_dst = -1.  rows fp32 [T*k, d]. */
+int moe_combine(const moe_dims* dims, int32_t T, const float* rows, const int32_t* row_dst,
+                const float* topk_w, uint16_t* y, void* stream);
+
+/* Human-readable text of a return code. */
+const char* moe_status_str(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4MOE_H */

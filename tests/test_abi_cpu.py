@@ -1,0 +1,55 @@
+"""The C-ABI library loads and exports every entry point its header declares; host-side
+argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp4_routed_expert_gb300 as moe
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "fp4moe.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = moe.lib()
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_slot_bytes_and_workspace():
+    assert moe.moe_slot_bytes((5120, 2304, 384, 6)) == 18_800_640
+    assert moe.moe_slot_bytes((512, 256, 16, 2)) == 208_896
+    assert moe.moe_slot_bytes((500, 256, 16, 2)) == -1
+    assert moe.moe_workspace_bytes((5120, 2304, 384, 6), 1) > 0
+    assert moe.moe_workspace_bytes((5120, 2304, 384, 6), 4096) > moe.moe_workspace_bytes((5120, 2304, 384, 6), 16)
+    assert moe.moe_workspace_bytes((5120, 2304, 2000, 6), 1) == 0
+
+
+def test_host_argument_errors_return_before_any_launch():
+    L = moe.lib()
+    good = moe.moe_dims(512, 256, 16, 2)
+    bad = moe.moe_dims(512, 256, 16, 40)
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: every call below fails its host checks first
+    assert L.moe_route_topk(ctypes.byref(bad), 1, fake, fake, None, fake, fake, fake, fake, fake, fake, 1 << 30, None) == -2
+    assert L.moe_route_topk(ctypes.byref(good), -1, fake, fake, None, fake, fake, fake, fake, fake, fake, 1 << 30, None) == -3
+    assert L.moe_route_topk(ctypes.byref(good), 1, None, fake, None, fake, fake, fake, fake, fake, fake, 1 << 30, None) == -1
+    assert L.moe_route_topk(ctypes.byref(good), 1, fake, fake, None, fake, fake, fake, fake, fake, fake, 16, None) == -4
+    assert L.moe_route_topk(ctypes.byref(good), 1, P((1 << 20) + 2), fake, None, fake, fake, fake, fake, fake, fake, 1 << 30, None) == -8
+    ar = moe.moe_arena(1 << 20, 12345, 4)
+    assert L.moe_expert_ffn_fp4(ctypes.byref(good), ctypes.byref(ar), 1, fake, fake, fake, fake, None, None, None, 1,
+                                None, fake, fake, fake, 1 << 30, None) == -5
+    ar = moe.moe_arena(1 << 20, moe.moe_slot_bytes(good), 4)
+    assert L.moe_expert_ffn_fp4(ctypes.byref(good), ctypes.byref(ar), 1, fake, fake, fake, fake, None, None, None, 7,
+                                None, fake, fake, fake, 1 << 30, None) == -6
+    assert L.moe_pack_expert(ctypes.byref(good), fake, fake, fake, fake, fake, fake, ctypes.byref(ar), 9, None) == -5
+    assert moe.moe_status_str(-4) == "workspace too small"

@@ -1,0 +1,218 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the CPU oracle on the same
+seeded inputs.  Routing ids, slots and the permutation must match bit for bit; layer outputs
+must satisfy the per-row bound max|y_gpu - y_ref| / max|y_ref| <= 1e-2."""
+import numpy as np
+import pytest
+import torch
+
+import fp4_routed_expert_gb300 as moe
+from fp4_routed_expert_gb300.layer import MoeLayer
+import oracle
+from synth import gpu as sgpu
+from synth import tensors as syn
+
+from workloads import bits_to_torch, make_workload, row_rel_err
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+DEV = "cuda"
+
+
+def run_layer(wl, x_bits, bias=None, fused_prefill=False):
+    T = x_bits.shape[0]
+    layer = MoeLayer(wl.d, wl.f, wl.E, wl.k, max(T, 1), wl.arena)
+    x = bits_to_torch(x_bits, DEV)
+    wr = bits_to_torch(wl.wr, DEV)
+    tab = torch.from_numpy(wl.table).to(DEV)
+    b = None if bias is None else torch.from_numpy(bias).to(DEV)
+    y = layer.forward(x, wr, tab, b) if not fused_prefill else None
+    if fused_prefill:
+        layer.route(x, wr, tab, b)
+        y = layer.experts(x, fused_prefill=True)
+    torch.cuda.synchronize()
+    out = dict(ids=layer.ids[:T].cpu().numpy(), w=layer.w[:T].cpu().numpy(), slots=layer.slots[:T].cpu().numpy(),
+               status=int(layer.status.item()), y=y[:T].float().cpu().numpy())
+    if T > moe.DECODE_MAX_T:
+        n = T * wl.k
+        out["offsets"] = layer.offsets.cpu().numpy()
+        out["row_src"] = layer.row_src[:n].cpu().numpy()
+        out["row_dst"] = layer.row_dst[:n].cpu().numpy()
+    return out
+
+
+def oracle_tokens(wl, x_bits, tokens, bias=None):
+    """Oracle routing and output for the given token indices (one by one)."""
+    r = oracle.route_topk(x_bits[tokens], wl.wr, bias, wl.table, wl.k)
+    ys = []
+    cache = {}
+    for n, t in enumerate(tokens):
+        z = np.zeros((wl.k, wl.d))
+        for j in range(wl.k):
+            s = int(r["slots"][n, j])
+            if s < 0:
+                continue
+            if s not in cache:
+                cache[s] = wl.expert_tensors(s)
+            _, z[j] = oracle.expert_ffn(x_bits[t], cache[s])
+        ys.append(oracle.combine(z, r["weights"][n]))
+    return r, np.stack(ys)
+
+
+def check_tokens(wl, x_bits, got, tokens, bias=None):
+    r, y = oracle_tokens(wl, x_bits, tokens, bias)
+    np.testing.assert_array_equal(got["ids"][tokens], r["ids"])
+    np.testing.assert_array_equal(got["slots"][tokens], r["slots"])
+    np.testing.assert_allclose(got["w"][tokens], r["weights"], rtol=2e-6, atol=1e-7)
+    err = row_rel_err(got["y"][tokens], y)
+    assert err.max() <= TOL, err
+    return r
+
+
+# ---------------------------------------------------------------------------- generator
+
+def test_device_generator_matches_host():
+    st = sgpu.ExpertStaging(512, 256, DEV)
+    t = st.fill(0, 3, 11, -10, -6)
+    torch.cuda.synchronize()
+    ref = syn.expert_tensors(0, 3, 11, 512, 256, -10, -6)
+    for n in syn.EXPERT_TENSORS:
+        np.testing.assert_array_equal(t[n].cpu().numpy(), ref[n])
+
+
+# ---------------------------------------------------------------------------- tiny workload
+
+@pytest.fixture(scope="module")
+def tiny():
+    return make_workload(512, 256, 16, 2, seed=0, scale=(-8, -4))
+
+
+def test_tiny_layer_matches_oracle(tiny):
+    x = syn.activations(0, 0, 4, 512)
+    got = run_layer(tiny, x)
+    assert got["status"] == 0
+    slots = {n: np.stack([tiny.expert_tensors(s)[n] for s in range(16)]) for n in syn.EXPERT_TENSORS}
+    ref = oracle.moe_layer(x, tiny.wr, None, tiny.table, 2, slots)
+    np.testing.assert_array_equal(got["ids"], ref["ids"])
+    np.testing.assert_array_equal(got["slots"], ref["slots"])
+    np.testing.assert_allclose(got["w"], ref["weights"], rtol=2e-6)
+    assert row_rel_err(got["y"], ref["y"]).max() <= TOL
+
+
+@pytest.mark.parametrize("T", [1, 3, 16, 17, 100])
+def test_tiny_shapes_decode_and_prefill(tiny, T):
+    x = syn.activations(0, 0, T, 512, stream=1)
+    got = run_layer(tiny, x)
+    r = check_tokens(tiny, x, got, list(range(T)))
+    if T > moe.DECODE_MAX_T:
+        p = oracle.permute(r["ids"], 16)
+        np.testing.assert_array_equal(got["offsets"], p["offsets"])
+        np.testing.assert_array_equal(got["row_src"][:p["rows"]], p["row_src"])
+        np.testing.assert_array_equal(got["row_dst"], p["row_dst"])
+
+
+def test_prefill_fused_combine_matches_unfused(tiny):
+    x = syn.activations(0, 0, 40, 512, stream=2)
+    a = run_layer(tiny, x)
+    b = run_layer(tiny, x, fused_prefill=True)
+    np.testing.assert_array_equal(a["y"], b["y"])
+
+
+# ---------------------------------------------------------------------------- routing edge cases
+
+def test_router_ties_mask_bias_and_few_resident():
+    d, E, k = 256, 40, 4
+    wl = make_workload(d, 128, E, k, seed=5, scale=(-8, -4))
+    wr = wl.wr.copy()
+    wr[7] = wr[3]          # exact ties between experts 3, 7 and 21
+    wr[21] = wr[3]
+    wl.wr = wr
+    x = syn.activations(5, 0, 24, d)
+    got = run_layer(wl, x)
+    check_tokens(wl, x, got, list(range(24)))
+    bias = syn.zipf_score_bias(5, 0, E, 1.2, 0.5)
+    got = run_layer(wl, x, bias=bias)
+    check_tokens(wl, x, got, list(range(24)), bias=bias)
+    # keep-set mask: half the experts have no slot
+    tab = wl.table.copy()
+    tab[::2] = -1
+    wl.table = tab
+    got = run_layer(wl, x)
+    assert np.all(got["ids"] % 2 == 1)
+    check_tokens(wl, x, got, list(range(24)))
+    # fewer than k resident
+    tab = np.full(E, -1, np.int32)
+    tab[[5, 9]] = [5, 9]
+    wl.table = tab
+    got = run_layer(wl, x[:2])
+    assert got["status"] & moe.MOE_STATUS_FEW_RESIDENT
+    assert got["ids"].tolist() == [[5, 9, -1, -1]] * 2
+    r = oracle.route_topk(x[:2], wl.wr, None, tab, k)
+    np.testing.assert_array_equal(got["ids"], r["ids"])
+    np.testing.assert_allclose(got["w"], r["weights"], rtol=2e-6)
+
+
+def test_router_large_batch_bit_exact_ids():
+    """Tiled router path (T > 16) with a skewing bias: every token's ids and slots."""
+    d, E, k, T = 1024, 96, 6, 300
+    wl = make_workload(d, 128, E, k, seed=2, table="permuted", scale=(-10, -6))
+    bias = syn.zipf_score_bias(2, 0, E, 1.2, 0.04)
+    x = syn.activations(2, 0, T, d)
+    got = run_layer(wl, x, bias=bias)
+    r = oracle.route_topk(x, wl.wr, bias, wl.table, k)
+    np.testing.assert_array_equal(got["ids"], r["ids"])
+    np.testing.assert_array_equal(got["slots"], r["slots"])
+    np.testing.assert_allclose(got["w"], r["weights"], rtol=2e-6, atol=1e-7)
+
+
+def test_bad_slot_is_reported_and_skipped():
+    d, E, k = 256, 8, 2
+    wl = make_workload(d, 128, E, k, seed=6, num_slots=8)
+    tab = wl.table.copy()
+    tab[:] = 100                # every slot outside the arena
+    wl.table = tab
+    x = syn.activations(6, 0, 2, d)
+    got = run_layer(wl, x)
+    assert got["status"] & moe.MOE_STATUS_BAD_SLOT
+    assert np.all(got["y"] == 0)
+
+
+def test_zero_tokens_is_a_no_op(tiny):
+    layer = MoeLayer(512, 256, 16, 2, 4, tiny.arena)
+    x = torch.zeros((0, 512), dtype=torch.bfloat16, device=DEV)
+    moe.moe_route_topk(layer.dims, 0, layer.y, bits_to_torch(tiny.wr, DEV), None,
+                       torch.from_numpy(tiny.table).to(DEV), layer.ids, layer.w, layer.slots, layer.status, layer.ws)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    del x
+
+
+# ---------------------------------------------------------------------------- pages' shape
+
+@pytest.fixture(scope="module")
+def full_decode():
+    """d=5120, f=2304, E=384, k=6, all experts resident behind a permuted slot table."""
+    return make_workload(5120, 2304, 384, 6, seed=0, table="permuted", scale=(-10, -6))
+
+
+def test_full_shape_decode_T1_sampled_tokens(full_decode):
+    wl = full_decode
+    x = syn.activations(0, 0, 6, 5120, stream=3)
+    for t in range(3):
+        got = run_layer(wl, x[t:t + 1])
+        check_tokens(wl, x[t:t + 1], got, [0])
+
+
+def test_full_shape_verify_T16(full_decode):
+    wl = full_decode
+    x = syn.activations(0, 0, 16, 5120, stream=4)
+    got = run_layer(wl, x)
+    check_tokens(wl, x, got, [0, 7, 15])
+
+
+def test_full_shape_prefill_sampled_tokens(full_decode):
+    wl = full_decode
+    T = 512
+    bias = syn.zipf_score_bias(0, 0, 384, 1.2, 0.04)
+    x = syn.activations(0, 0, T, 5120, stream=5)
+    got = run_layer(wl, x, bias=bias)
+    check_tokens(wl, x, got, [0, 1, 255, 511], bias=bias)
