@@ -17,7 +17,7 @@ from . import build as _build
 
 __all__ = [
     "MoeError", "moe_dims", "moe_arena", "lib", "moe_slot_bytes", "moe_workspace_bytes",
-    "moe_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_permute",
+    "moe_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_route_topk_noalloc", "moe_permute",
     "moe_expert_ffn_fp4", "moe_combine", "moe_status_str", "MOE_FUSE_COMBINE",
     "MOE_STATUS_FEW_RESIDENT", "MOE_STATUS_BAD_SLOT", "MOE_STATUS_TIMEOUT", "DECODE_MAX_T",
 ]
@@ -56,6 +56,7 @@ _SIG = {
     "moe_permute": (ctypes.c_int, [_P, _I] + [_P] * 5 + [ctypes.c_size_t, _P]),
     "moe_expert_ffn_fp4": (ctypes.c_int, [_P, _P, _I] + [_P] * 7 + [_I] + [_P] * 4 + [ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [_P, _I] + [_P] * 5),
+    "moe_route_topk_noalloc": (ctypes.c_int, [_P, _I] + [_P] * 9),
     "moe_status_str": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -130,6 +131,14 @@ def moe_route_topk(dims, T, x, w_router, score_bias, expert_to_slot, topk_ids, t
         ctypes.byref(_dims(dims)), int(T), _ptr(x), _ptr(w_router), _ptr(score_bias), _ptr(expert_to_slot),
         _ptr(topk_ids), _ptr(topk_w), _ptr(topk_slot), _ptr(dev_status), _ptr(ws), ws.numel() * ws.element_size(),
         _stream(stream)))
+
+
+def moe_route_topk_noalloc(dims, T, x, w_router, score_bias, expert_to_slot, topk_ids, topk_w, topk_slot,
+                           dev_status, stream=None):
+    """moe_route_topk with the library's own static scratch (no workspace; T <= 16)."""
+    _check("moe_route_topk_noalloc", lib().moe_route_topk_noalloc(
+        ctypes.byref(_dims(dims)), int(T), _ptr(x), _ptr(w_router), _ptr(score_bias), _ptr(expert_to_slot),
+        _ptr(topk_ids), _ptr(topk_w), _ptr(topk_slot), _ptr(dev_status), _stream(stream)))
 
 
 def moe_permute(dims, T, topk_ids, group_offsets, row_src, row_dst, ws, stream=None):

@@ -520,3 +520,78 @@ int launch_route(const moe_dims* m, int T, const uint16_t* x, const uint16_t* wr
 }
 
 }  // namespace fp4moe
+
+// ------------------------------------------------------------------ router with static scratch
+//
+// A variant of the decode-regime router for callers that cannot allocate device memory: an
+// op hosted by an engine that owns the whole device pool and hands its ops no workspace, or
+// a serving loop that must not allocate between steps.  Its scratch (fast logits, norms and
+// the completion ticket) lives in the file-scope array below instead of a caller workspace.
+// Every GPU that loads this library holds the array until the process exits.
+
+namespace fp4moe {
+
+constexpr int kStaticMaxT = kDecodeMaxT;   // tokens per call
+constexpr size_t kStaticCounterBytes = 256;
+constexpr size_t kStaticLogitBytes = sizeof(float) * kStaticMaxT * kMaxExperts;
+constexpr size_t kStaticXnormBytes = 256;
+constexpr size_t kStaticWnormBytes = sizeof(float) * kMaxExperts;
+constexpr size_t kStaticScratchBytes = kStaticCounterBytes + kStaticLogitBytes + kStaticXnormBytes + kStaticWnormBytes;
+
+static __device__ __align__(256) unsigned char g_route_scratch[kStaticScratchBytes];
+
+}  // namespace fp4moe
+
+#include <mutex>
+
+namespace {
+std::mutex g_route_scratch_mu;
+void* g_route_scratch_addr[64] = {nullptr};
+}  // namespace
+
+extern "C" int moe_route_topk_noalloc(const moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* w_router,
+                                      const float* score_bias, const int32_t* expert_to_slot, int32_t* topk_ids,
+                                      float* topk_w, int32_t* topk_slot, int32_t* dev_status, void* stream) {
+    using namespace fp4moe;
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (T < 0 || T > kStaticMaxT) return MOE_ERR_TOKENS;
+    if (!x || !w_router || !expert_to_slot || !topk_ids || !topk_w || !topk_slot || !dev_status) return MOE_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(w_router) & 15u)) return MOE_ERR_ALIGN;
+    if (T == 0) return MOE_OK;
+    // Host code may not use g_route_scratch as an address: look up its device address once
+    // per device, with that device current.
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_LAUNCH;
+    unsigned char* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_route_scratch_mu);
+        if (!g_route_scratch_addr[dev]) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return MOE_ERR_LAUNCH;
+            g_route_scratch_addr[dev] = p;
+        }
+        base = static_cast<unsigned char*>(g_route_scratch_addr[dev]);
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    // the completion ticket must start at zero
+    if (cudaMemsetAsync(base, 0, kStaticCounterBytes, st) != cudaSuccess) return MOE_ERR_LAUNCH;
+    RouteArgs a;
+    a.T = T; a.d = dims->d; a.E = dims->num_experts; a.k = dims->top_k;
+    a.x = x; a.wr = w_router; a.bias = score_bias; a.table = expert_to_slot;
+    a.ids = topk_ids; a.w = topk_w; a.slots = topk_slot; a.status = dev_status;
+    a.counter = reinterpret_cast<unsigned*>(base);
+    a.logit = reinterpret_cast<float*>(base + kStaticCounterBytes);
+    a.xnorm = reinterpret_cast<float*>(base + kStaticCounterBytes + kStaticLogitBytes);
+    a.wnorm = reinterpret_cast<float*>(base + kStaticCounterBytes + kStaticLogitBytes + kStaticXnormBytes);
+    int per_lane = (a.d / 8 + 31) / 32;
+    a.bound_coef = gamma_coef(per_lane * 8 + 5);
+    const int warps = 4;
+    int blocks = (a.E + warps - 1) / warps;
+    size_t smem = (size_t)T * a.d * 2;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(route_small_kernel<kDecodeMaxT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+        return MOE_ERR_LAUNCH;
+    route_small_kernel<kDecodeMaxT><<<blocks, warps * 32, smem, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}

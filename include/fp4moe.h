@@ -117,6 +117,23 @@ int moe_route_topk(const moe_dims* dims, int32_t T, const uint16_t* x, const uin
                    float* topk_w, int32_t* topk_slot, int32_t* dev_status, void* ws,
                    size_t ws_bytes, void* stream);
 
+/* moe_route_topk without a workspace, for callers that cannot allocate device memory: an
+ * op hosted by an engine that owns the whole device pool and gives its ops no workspace, or
+ * a serving loop that must not allocate between steps.  The pages have no counterpart to
+ * this entry point; it computes exactly what moe_route_topk computes.
+ * Limits: 0 <= T <= 16 (larger T returns MOE_ERR_TOKENS before anything is enqueued) and the
+ * dims limits above.  Its scratch (fast logits, norms and a completion ticket, about 69 KB)
+ * is a static device array inside this library, held by every GPU that loads the library
+ * until the process exits.  It allocates nothing and calls no allocating routine.
+ * The first call on each device looks up the array's device address with that device
+ * current; make that first call before any stream capture.  Every call clears the ticket
+ * (an asynchronous memset on `stream`) and overwrites the rest of the array: calls whose
+ * execution overlaps on the GPU -- on different streams, or from different threads --
+ * race on the shared array and must be serialised by the caller. */
+int moe_route_topk_noalloc(const moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* w_router,
+                           const float* score_bias, const int32_t* expert_to_slot, int32_t* topk_ids,
+                           float* topk_w, int32_t* topk_slot, int32_t* dev_status, void* stream);
+
 /* a4: stable grouping of the T*k (token, j) rows by expert id (tokens ascending inside a
  * group).  group_offsets int32 [E+1] (group e = rows [off[e], off[e+1]), off[E] = rows
  * with a valid id), row_src int32 [T*k] (row r came from t*k + j; entries >= off[E] are
