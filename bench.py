@@ -358,7 +358,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=384,
+                    help="experts resident in the arena (profiling runs use fewer; the metric is defined at 384)")
+    ap.add_argument("--tokens", type=int, default=1000, help="tokens per step")
     args = ap.parse_args()
+    global E, TOKENS, ROUTER_BYTES, ALG_BYTES_PER_TOKEN
+    E, TOKENS = args.experts, args.tokens
+    ROUTER_BYTES = E * D * 2
+    ALG_BYTES_PER_TOKEN = K * EXPERT_BYTES + ROUTER_BYTES + 2 * D * 2
+    if E != 384 or TOKENS != 1000:
+        CONFIG["workload"] = "PROFILING VARIANT (not the metric's workload): E=%d experts, %d tokens per step" % (E, TOKENS)
+        CONFIG["tokens_per_step"] = TOKENS
     rank, world, local_rank = env_rank()
     if args.impl == "reference":
         out = run_reference(args, rank, world)

@@ -20,6 +20,12 @@ namespace fp4moe {
 
 constexpr int kXT = 8;   // tokens staged per pass of kernel 1
 
+// Shared-memory rows are padded by 4 floats after every 32 (one 16-byte code chunk's worth
+// of activations): a lane's 32-float chunk starts at 36c, so the 16-byte reads of 8
+// consecutive chunks fall in 8 distinct groups of 4 banks.
+__host__ __device__ constexpr int padded(int n) { return n + n / 8; }
+__device__ __forceinline__ int pad_idx(int i) { return i + 4 * (i >> 5); }
+
 struct DecodeArgs {
     int T, d, f, k, num_slots;
     int t0, tn;                 // token pass [t0, t0 + tn) of kernel 1
@@ -93,8 +99,9 @@ __device__ float block_absmax(float v, float* red) {
 // Items are (unique slot u, output i).  A warp loads gate row i and up row i of slot u
 // (lane owns chunks lane, lane+32, ...), then reduces for every token of this pass routed
 // to u.  Shared memory: staged activations [tn][d] fp32 and the slot/member lists.
+template <int XT>
 __global__ void __launch_bounds__(256) decode_gateup_kernel(DecodeArgs a) {
-    extern __shared__ float xs[];                         // [tn][d]
+    extern __shared__ float xs[];                         // [tn][padded(d)]
     __shared__ int uniq_slot[kXT * kMaxTopK];
     __shared__ int mem_cnt[kXT * kMaxTopK];
     __shared__ int mem_pair[kXT * kMaxTopK][kXT];
@@ -114,7 +121,7 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(DecodeArgs a) {
             if (s < 0) continue;
             if (s >= a.num_slots) { if (blockIdx.x == 0) atomicOr(a.status, MOE_STATUS_BAD_SLOT); continue; }
             int u = 0;
-            while (u < nu && !(uniq_slot[u] == s && mem_cnt[u] < kXT)) ++u;
+            while (u < nu && !(uniq_slot[u] == s && mem_cnt[u] < XT)) ++u;
             if (u == nu) { uniq_slot[nu] = s; mem_cnt[nu] = 0; ++nu; }
             mem_pair[u][mem_cnt[u]++] = p;
         }
@@ -129,7 +136,7 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(DecodeArgs a) {
         int p = prescale_exponent(m);
         if (tid == 0) pexp[t] = p;
         float sc = exp2i(p > 127 ? 127 : p);
-        for (int i = tid; i < d; i += blockDim.x) xs[(size_t)t * d + i] = bf16_to_f32(xt[i]) * sc;
+        for (int i = tid; i < d; i += blockDim.x) xs[(size_t)t * padded(d) + pad_idx(i)] = bf16_to_f32(xt[i]) * sc;
     }
     __syncthreads();
     const int nu = n_uniq;
@@ -144,9 +151,9 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(DecodeArgs a) {
         const uint8_t* uq = gq + rowq;
         const uint8_t* gs = base + a.L.gu_s + (int64_t)(2 * i) * rows_s;
         const uint8_t* us = gs + rows_s;
-        float accg[kXT], accu[kXT];
+        float accg[XT], accu[XT];
 #pragma unroll
-        for (int q = 0; q < kXT; ++q) accg[q] = accu[q] = 0.f;
+        for (int q = 0; q < XT; ++q) accg[q] = accu[q] = 0.f;
         const int nmem = mem_cnt[u];
         for (int c0 = lane; c0 < nchunk; c0 += 32 * 5) {
             uint4 qg[5], qu[5];
@@ -166,17 +173,19 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(DecodeArgs a) {
                 int c = c0 + 32 * b;
                 if (c >= nchunk) break;
 #pragma unroll
-                for (int q = 0; q < kXT; ++q) {
+                for (int q = 0; q < XT; ++q) {
                     if (q >= nmem) break;
                     int t = mem_pair[u][q] / k - a.t0;
-                    const float* xa = xs + (size_t)t * d + kChunk * c;
+                    const float* xa = xs + (size_t)t * padded(d) + 36 * c;
                     int p = pexp[t];
                     accg[q] = fmaf(chunk_dot(qg[b], xa), pow2f((int)sg[b] - 1 - p), accg[q]);
                     accu[q] = fmaf(chunk_dot(qu[b], xa), pow2f((int)su[b] - 1 - p), accu[q]);
                 }
             }
         }
-        for (int q = 0; q < nmem; ++q) {
+#pragma unroll
+        for (int q = 0; q < XT; ++q) {
+            if (q >= nmem) break;
             float g = warp_sum(accg[q]), uu = warp_sum(accu[q]);
             if (lane == 0) a.h[(size_t)mem_pair[u][q] * f + i] = silu_mul(g, uu);
         }
@@ -189,7 +198,7 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(DecodeArgs a) {
 // token, the k pairs are visited in ascending j and combined in that order.  Shared memory:
 // the token's k vectors h * 2^p (exact) [k][f].
 __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
-    extern __shared__ float hs[];                         // [k][f]
+    extern __shared__ float hs[];                         // [k][padded(f)]
     __shared__ int pexp[kMaxTopK];
     __shared__ float red[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -213,7 +222,7 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
             int p = prescale_exponent(m);
             if (tid == 0) pexp[j] = p;
             float sc = exp2i(p > 127 ? 127 : p);
-            for (int i = tid; i < f; i += blockDim.x) hs[(size_t)j * f + i] = ok ? __ldcg(hp + i) * sc : 0.f;
+            for (int i = tid; i < f; i += blockDim.x) hs[(size_t)j * padded(f) + pad_idx(i)] = ok ? __ldcg(hp + i) * sc : 0.f;
         }
         __syncthreads();
         if (r < d) {
@@ -239,7 +248,7 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
                     for (int b = 0; b < 9; ++b) {
                         int c = c0 + 8 * b;
                         if (c >= nchunk) break;
-                        acc = fmaf(chunk_dot(qv[b], hs + (size_t)j * f + kChunk * c), pow2f((int)sb[b] - 1 - p), acc);
+                        acc = fmaf(chunk_dot(qv[b], hs + (size_t)j * padded(f) + 36 * c), pow2f((int)sb[b] - 1 - p), acc);
                     }
                 }
                 acc += __shfl_xor_sync(0xffffffffu, acc, 4);
@@ -253,6 +262,15 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
 }
 
 // ---------------------------------------------------------------------------- host side
+
+template <int XT>
+static int launch_gateup(const DecodeArgs& a, size_t smem, int blocks, cudaStream_t st) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(decode_gateup_kernel<XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
+    decode_gateup_kernel<XT><<<blocks, 256, smem, st>>>(a);
+    return MOE_OK;
+}
 
 int launch_decode_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x,
                       const int32_t* slot, const float* w, uint16_t* y, int32_t* status, char* ws,
@@ -269,14 +287,16 @@ int launch_decode_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint1
     for (int t0 = 0; t0 < T; t0 += kXT) {
         a.t0 = t0;
         a.tn = (T - t0 < kXT) ? T - t0 : kXT;
-        size_t smem = (size_t)a.tn * m->d * 4;
-        if (smem > 48 * 1024 &&
-            cudaFuncSetAttribute(decode_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-            return MOE_ERR_LAUNCH;
+        size_t smem = (size_t)a.tn * padded(m->d) * 4;
         int blocks = 2 * num_sms;
-        decode_gateup_kernel<<<blocks, 256, smem, st>>>(a);
+        int rc = MOE_OK;
+        if (a.tn == 1) rc = launch_gateup<1>(a, smem, blocks, st);
+        else if (a.tn == 2) rc = launch_gateup<2>(a, smem, blocks, st);
+        else if (a.tn <= 4) rc = launch_gateup<4>(a, smem, blocks, st);
+        else rc = launch_gateup<8>(a, smem, blocks, st);
+        if (rc) return rc;
     }
-    size_t smem2 = (size_t)m->top_k * m->f * 4;
+    size_t smem2 = (size_t)m->top_k * padded(m->f) * 4;
     if (smem2 > 48 * 1024 &&
         cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) != cudaSuccess)
         return MOE_ERR_LAUNCH;

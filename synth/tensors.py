@@ -83,8 +83,11 @@ def activations(seed: int, layer: int, T: int, d: int, start_token: int = 0,
     """x [T, d] as bf16 bits: N(0,1) drawn in double, rounded to fp32, then to bf16.
 
     Token t of the stream uses words from row (start_token + t), so any subset of tokens
-    can be regenerated alone.  ``stream`` selects independent token streams.
+    can be regenerated alone.  ``stream`` (0..15) selects independent token streams of up
+    to 65,536 tokens each.
     """
+    if not (0 <= stream < 16 and 0 <= start_token and start_token + T <= 65536):
+        raise ValueError("activation stream must be 0..15 with at most 65,536 tokens")
     rows = []
     for t in range(start_token, start_token + T):
         z = philox.normal(seed, tag(KIND_X, layer, (stream << 16) + t) , d)
