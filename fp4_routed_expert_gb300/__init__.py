@@ -18,11 +18,12 @@ from . import build as _build
 __all__ = [
     "MoeError", "moe_dims", "moe_arena", "lib", "moe_slot_bytes", "moe_workspace_bytes",
     "moe_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_route_topk_noalloc", "moe_permute",
-    "moe_expert_ffn_fp4", "moe_combine", "moe_status_str", "MOE_FUSE_COMBINE",
+    "moe_expert_ffn_fp4", "moe_combine", "moe_status_str", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
     "MOE_STATUS_FEW_RESIDENT", "MOE_STATUS_BAD_SLOT", "MOE_STATUS_TIMEOUT", "DECODE_MAX_T",
 ]
 
 MOE_FUSE_COMBINE = 1
+MOE_FFN_CUDA_CORES = 2
 MOE_STATUS_FEW_RESIDENT = 1
 MOE_STATUS_BAD_SLOT = 2
 MOE_STATUS_TIMEOUT = 4

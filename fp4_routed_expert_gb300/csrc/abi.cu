@@ -20,6 +20,14 @@ int launch_prefill_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint
                        const WsLayout& L, cudaStream_t st, int num_sms);
 int launch_combine(const moe_dims* m, int T, const float* rows, const int32_t* row_dst, const float* w,
                    uint16_t* y, cudaStream_t st, int num_sms);
+bool tc_supported(const moe_dims* m);
+bool tc_decode_supported(const moe_dims* m, int T);
+int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
+                     const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
+                     int num_sms);
+int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
+                      const int32_t* offsets, const int32_t* row_src, float* rows_out, int32_t* status, char* ws,
+                      const WsLayout& L, cudaStream_t st, int num_sms);
 
 // Gate/up interleave: destination row 2i <- gate row i, row 2i+1 <- up row i (32-bit words).
 __global__ void pack_interleave_kernel(const uint32_t* __restrict__ gate, const uint32_t* __restrict__ up,
@@ -148,12 +156,13 @@ int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, 
                        float* rows_out, uint16_t* y, int32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
     if (!dims_ok(dims)) return MOE_ERR_DIMS;
     if (T < 0) return MOE_ERR_TOKENS;
-    if (flags & ~MOE_FUSE_COMBINE) return MOE_ERR_FLAGS;
+    if (flags & ~(MOE_FUSE_COMBINE | MOE_FFN_CUDA_CORES)) return MOE_ERR_FLAGS;
     int rc = check_arena(dims, arena);
     if (rc) return rc;
     if (!x || !topk_ids || !topk_slot || !topk_w || !dev_status) return MOE_ERR_NULL;
     if (!aligned16(x)) return MOE_ERR_ALIGN;
     const bool fused = (flags & MOE_FUSE_COMBINE) != 0;
+    const bool cuda_cores = (flags & MOE_FFN_CUDA_CORES) != 0;
     if (fused && !y) return MOE_ERR_NULL;
     if (!fused && !rows_out) return MOE_ERR_NULL;
     WsLayout L;
@@ -163,14 +172,18 @@ int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, 
     char* w = static_cast<char*>(ws);
     int sms = num_sms_of_current_device();
     if (T <= kDecodeMaxT && fused) {
+        if (!cuda_cores && tc_decode_supported(dims, T))
+            return launch_tc_decode(dims, arena, T, x, topk_slot, topk_w, y, dev_status, w, L, st, sms);
         return launch_decode_ffn(dims, arena, T, x, topk_slot, topk_w, y, dev_status, w, L, st, sms);
     }
     if (!group_offsets || !row_src || (fused && !row_dst)) return MOE_ERR_NULL;
     if (rows_out && !aligned16(rows_out)) return MOE_ERR_ALIGN;
+    // fused requests reach this point only for T > kDecodeMaxT, where the workspace holds rows
     float* rows = fused ? reinterpret_cast<float*>(w + L.rows) : rows_out;
-    if (fused && T > kDecodeMaxT && L.rows + (size_t)T * dims->top_k * dims->d * 4 > ws_bytes) return MOE_ERR_WORKSPACE;
-    if (fused && T <= kDecodeMaxT) return MOE_ERR_FLAGS;   // unreachable: decode handles it
-    rc = launch_prefill_ffn(dims, arena, T, x, topk_slot, group_offsets, row_src, rows, dev_status, w, L, st, sms);
+    if (!cuda_cores && tc_supported(dims))
+        rc = launch_tc_prefill(dims, arena, T, x, topk_slot, group_offsets, row_src, rows, dev_status, w, L, st, sms);
+    else
+        rc = launch_prefill_ffn(dims, arena, T, x, topk_slot, group_offsets, row_src, rows, dev_status, w, L, st, sms);
     if (rc || !fused) return rc;
     return launch_combine(dims, T, rows, row_dst, topk_w, y, st, sms);
 }

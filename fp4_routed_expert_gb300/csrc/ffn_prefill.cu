@@ -88,8 +88,8 @@ __global__ void permute_tail_kernel(int n, int E, const int32_t* offsets, int32_
 // ---------------------------------------------------------------------------- plan
 
 // Validates group_offsets (monotone in [0, n]) and lists the non-empty groups with the
-// prefix of their 64-row tile counts.  plan = [n_active, total_tiles, e_0.., tile_start_0..]
-__global__ void plan_kernel(int E, int n, const int32_t* offsets, int32_t* plan, int32_t* status) {
+// prefix of their tile counts (tile_rows rows per tile).  plan = [n_active, total_tiles, e_0.., tile_start_0..]
+__global__ void plan_kernel(int E, int n, const int32_t* offsets, int32_t* plan, int32_t* status, int tile_rows) {
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
     int na = 0, tiles = 0, prev = 0;
     bool bad = offsets[0] != 0;
@@ -100,7 +100,7 @@ __global__ void plan_kernel(int E, int n, const int32_t* offsets, int32_t* plan,
         if (o1 > o0) {
             plan[2 + na] = e;
             plan[2 + E + na] = tiles;
-            tiles += (o1 - o0 + 63) / 64;
+            tiles += (o1 - o0 + tile_rows - 1) / tile_rows;
             ++na;
         }
     }
@@ -332,7 +332,7 @@ int launch_prefill_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint
     a.rows = rows_out;
     a.status = status;
     if (T == 0) return MOE_OK;
-    plan_kernel<<<1, 32, 0, st>>>(a.E, a.n, offsets, reinterpret_cast<int32_t*>(ws + L.active), status);
+    plan_kernel<<<1, 32, 0, st>>>(a.E, a.n, offsets, reinterpret_cast<int32_t*>(ws + L.active), status, kBT);
     int blocks = 4 * num_sms;
     grouped_gemm_kernel<false><<<blocks, 256, 0, st>>>(a);
     grouped_gemm_kernel<true><<<blocks, 256, 0, st>>>(a);

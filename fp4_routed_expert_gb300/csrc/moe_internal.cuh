@@ -55,10 +55,13 @@ struct WsLayout {
     size_t active;      // int32 [2 + 2E]    group plan: n_active, tiles, expert ids, tile prefix
     size_t h;           // fp32 [T_max*k, f] SwiGLU output per (token, j) pair or permuted row
     size_t rows;        // fp32 [T_max*k, d] per-row expert outputs (prefill with fused combine)
+    size_t tc;          // tensor-core path: quantised activations, quantised h, per-row outputs
     size_t total;
 };
 
 inline size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+size_t tc_workspace_bytes(const moe_dims* m, int T);   // mxf4_gemm.cu
 
 inline WsLayout ws_layout(const moe_dims* m, int T_max) {
     WsLayout w;
@@ -72,6 +75,7 @@ inline WsLayout ws_layout(const moe_dims* m, int T_max) {
     w.h = o;       o = align256(o + 4 * T * k * (size_t)m->f);
     w.rows = o;
     if (T_max > kDecodeMaxT) o = align256(o + 4 * T * k * (size_t)m->d);
+    w.tc = o;      o = align256(o + tc_workspace_bytes(m, (int)T));
     w.total = o;
     return w;
 }

@@ -4,7 +4,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (DECODE_MAX_T, MOE_FUSE_COMBINE, moe_arena, moe_dims, moe_expert_ffn_fp4, moe_pack_expert,
+from . import (DECODE_MAX_T, MOE_FFN_CUDA_CORES, MOE_FUSE_COMBINE, moe_arena, moe_dims, moe_expert_ffn_fp4, moe_pack_expert,
                moe_permute, moe_route_topk, moe_slot_bytes, moe_workspace_bytes, moe_workspace_init)
 
 
@@ -62,24 +62,28 @@ class MoeLayer:
         moe_route_topk(self.dims, T, x, w_router, bias, table, self.ids, self.w, self.slots, self.status, self.ws,
                        stream)
 
-    def experts(self, x, T=None, fused_prefill=False, stream=None, y=None):
+    def experts(self, x, T=None, fused_prefill=False, stream=None, y=None, cuda_cores=False):
+        """Expert FFN + combine.  cuda_cores=True selects the CUDA-core kernels (exact fp4 x bf16
+        products); the default uses the tensor-core kernels where the shape allows."""
         T = x.shape[0] if T is None else T
         y = self.y if y is None else y
+        extra = MOE_FFN_CUDA_CORES if cuda_cores else 0
         if T <= DECODE_MAX_T:
             moe_expert_ffn_fp4(self.dims, self.arena.c, T, x, self.ids, self.slots, self.w, None, None, None,
-                               MOE_FUSE_COMBINE, None, y, self.status, self.ws, stream)
+                               MOE_FUSE_COMBINE | extra, None, y, self.status, self.ws, stream)
             return y
         moe_permute(self.dims, T, self.ids, self.offsets, self.row_src, self.row_dst, self.ws, stream)
         if fused_prefill:
             moe_expert_ffn_fp4(self.dims, self.arena.c, T, x, self.ids, self.slots, self.w, self.offsets,
-                               self.row_src, self.row_dst, MOE_FUSE_COMBINE, None, y, self.status, self.ws, stream)
+                               self.row_src, self.row_dst, MOE_FUSE_COMBINE | extra, None, y, self.status, self.ws,
+                               stream)
         else:
             from . import moe_combine
             moe_expert_ffn_fp4(self.dims, self.arena.c, T, x, self.ids, self.slots, self.w, self.offsets,
-                               self.row_src, self.row_dst, 0, self.rows, None, self.status, self.ws, stream)
+                               self.row_src, self.row_dst, extra, self.rows, None, self.status, self.ws, stream)
             moe_combine(self.dims, T, self.rows, self.row_dst, self.w, y, stream)
         return y
 
-    def forward(self, x, w_router, table, bias=None, stream=None, y=None):
+    def forward(self, x, w_router, table, bias=None, stream=None, y=None, cuda_cores=False):
         self.route(x, w_router, table, bias, stream=stream)
-        return self.experts(x, stream=stream, y=y)
+        return self.experts(x, stream=stream, y=y, cuda_cores=cuda_cores)

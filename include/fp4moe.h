@@ -76,6 +76,8 @@ enum {
 
 /* Flags of moe_expert_ffn_fp4. */
 #define MOE_FUSE_COMBINE 1         /* write y directly (fixed-order combine fused in) */
+#define MOE_FFN_CUDA_CORES 2       /* use the CUDA-core kernels (exact fp4 x bf16 products,
+                                      fp32 accumulation) instead of the tensor-core kernels */
 
 /* Bytes of one arena slot: 3*f*d/2 code bytes + 3*f*d/32 scale bytes, rounded up to
  * 1024 (18,800,640 at d=5120, f=2304).  Returns -1 for unsupported dims. */

@@ -18,17 +18,15 @@ TOL = 1e-2
 DEV = "cuda"
 
 
-def run_layer(wl, x_bits, bias=None, fused_prefill=False):
+def run_layer(wl, x_bits, bias=None, fused_prefill=False, cuda_cores=False):
     T = x_bits.shape[0]
     layer = MoeLayer(wl.d, wl.f, wl.E, wl.k, max(T, 1), wl.arena)
     x = bits_to_torch(x_bits, DEV)
     wr = bits_to_torch(wl.wr, DEV)
     tab = torch.from_numpy(wl.table).to(DEV)
     b = None if bias is None else torch.from_numpy(bias).to(DEV)
-    y = layer.forward(x, wr, tab, b) if not fused_prefill else None
-    if fused_prefill:
-        layer.route(x, wr, tab, b)
-        y = layer.experts(x, fused_prefill=True)
+    layer.route(x, wr, tab, b)
+    y = layer.experts(x, fused_prefill=fused_prefill, cuda_cores=cuda_cores)
     torch.cuda.synchronize()
     out = dict(ids=layer.ids[:T].cpu().numpy(), w=layer.w[:T].cpu().numpy(), slots=layer.slots[:T].cpu().numpy(),
                status=int(layer.status.item()), y=y[:T].float().cpu().numpy())
@@ -64,6 +62,7 @@ def check_tokens(wl, x_bits, got, tokens, bias=None):
     np.testing.assert_array_equal(got["slots"][tokens], r["slots"])
     np.testing.assert_allclose(got["w"][tokens], r["weights"], rtol=2e-6, atol=1e-7)
     err = row_rel_err(got["y"][tokens], y)
+    print("max row error %.3e over %d tokens" % (err.max(), len(tokens)))
     assert err.max() <= TOL, err
     return r
 
@@ -98,10 +97,11 @@ def test_tiny_layer_matches_oracle(tiny):
     assert row_rel_err(got["y"], ref["y"]).max() <= TOL
 
 
+@pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor_cores", "cuda_cores"])
 @pytest.mark.parametrize("T", [1, 3, 16, 17, 100])
-def test_tiny_shapes_decode_and_prefill(tiny, T):
+def test_tiny_shapes_decode_and_prefill(tiny, T, cuda_cores):
     x = syn.activations(0, 0, T, 512, stream=1)
-    got = run_layer(tiny, x)
+    got = run_layer(tiny, x, cuda_cores=cuda_cores)
     r = check_tokens(tiny, x, got, list(range(T)))
     if T > moe.DECODE_MAX_T:
         p = oracle.permute(r["ids"], 16)
@@ -110,10 +110,11 @@ def test_tiny_shapes_decode_and_prefill(tiny, T):
         np.testing.assert_array_equal(got["row_dst"], p["row_dst"])
 
 
-def test_prefill_fused_combine_matches_unfused(tiny):
+@pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor_cores", "cuda_cores"])
+def test_prefill_fused_combine_matches_unfused(tiny, cuda_cores):
     x = syn.activations(0, 0, 40, 512, stream=2)
-    a = run_layer(tiny, x)
-    b = run_layer(tiny, x, fused_prefill=True)
+    a = run_layer(tiny, x, cuda_cores=cuda_cores)
+    b = run_layer(tiny, x, fused_prefill=True, cuda_cores=cuda_cores)
     np.testing.assert_array_equal(a["y"], b["y"])
 
 
@@ -194,25 +195,28 @@ def full_decode():
     return make_workload(5120, 2304, 384, 6, seed=0, table="permuted", scale=(-10, -6))
 
 
-def test_full_shape_decode_T1_sampled_tokens(full_decode):
+@pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor_cores", "cuda_cores"])
+def test_full_shape_decode_T1_sampled_tokens(full_decode, cuda_cores):
     wl = full_decode
     x = syn.activations(0, 0, 6, 5120, stream=3)
     for t in range(3):
-        got = run_layer(wl, x[t:t + 1])
+        got = run_layer(wl, x[t:t + 1], cuda_cores=cuda_cores)
         check_tokens(wl, x[t:t + 1], got, [0])
 
 
-def test_full_shape_verify_T16(full_decode):
+@pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor_cores", "cuda_cores"])
+def test_full_shape_verify_T16(full_decode, cuda_cores):
     wl = full_decode
     x = syn.activations(0, 0, 16, 5120, stream=4)
-    got = run_layer(wl, x)
+    got = run_layer(wl, x, cuda_cores=cuda_cores)
     check_tokens(wl, x, got, [0, 7, 15])
 
 
-def test_full_shape_prefill_sampled_tokens(full_decode):
+@pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor_cores", "cuda_cores"])
+def test_full_shape_prefill_sampled_tokens(full_decode, cuda_cores):
     wl = full_decode
     T = 512
     bias = syn.zipf_score_bias(0, 0, 384, 1.2, 0.04)
     x = syn.activations(0, 0, T, 5120, stream=5)
-    got = run_layer(wl, x, bias=bias)
+    got = run_layer(wl, x, bias=bias, cuda_cores=cuda_cores)
     check_tokens(wl, x, got, [0, 1, 255, 511], bias=bias)
