@@ -29,16 +29,29 @@ int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint1
                       const int32_t* offsets, const int32_t* row_src, float* rows_out, int32_t* status, char* ws,
                       const WsLayout& L, cudaStream_t st, int num_sms);
 
-// Gate/up interleave: destination row 2i <- gate row i, row 2i+1 <- up row i (32-bit words).
-__global__ void pack_interleave_kernel(const uint32_t* __restrict__ gate, const uint32_t* __restrict__ up,
-                                       uint32_t* __restrict__ dst, int rows, int words_per_row) {
-    long total = (long)rows * 2 * words_per_row;
+// Canonical rows -> arena tiles.  With `up` set, matrix row 2i takes row i of `gate` and
+// row 2i+1 takes row i of `up` (the gate/up interleave); otherwise matrix row R is row R of
+// `gate`.  One thread per 16-byte code chunk.
+__global__ void pack_codes_kernel(const uint8_t* __restrict__ gate, const uint8_t* __restrict__ up,
+                                  uint8_t* __restrict__ dst, int rows, int K) {
+    const int chunks = K / 32;
+    const long total = (long)rows * chunks;
     for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
-        long drow = idx / words_per_row;
-        int wi = (int)(idx % words_per_row);
-        long srow = drow >> 1;
-        const uint32_t* src = (drow & 1) ? up : gate;
-        dst[idx] = src[srow * words_per_row + wi];
+        const int R = (int)(idx / chunks), c = (int)(idx % chunks);
+        const uint8_t* src = up ? ((R & 1) ? up : gate) + (size_t)(R >> 1) * (K / 2) : gate + (size_t)R * (K / 2);
+        *reinterpret_cast<uint4*>(dst + code_chunk_off(R, c, K)) = *reinterpret_cast<const uint4*>(src + 16 * c);
+    }
+}
+
+// Canonical scale rows [rows][K/32] -> arena scale atoms (same row mapping as the codes).
+__global__ void pack_scales_kernel(const uint8_t* __restrict__ gate, const uint8_t* __restrict__ up,
+                                   uint8_t* __restrict__ dst, int rows, int K) {
+    const int nb = K / 32;
+    const long total = (long)rows * nb;
+    for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+        const int R = (int)(idx / nb), kb = (int)(idx % nb);
+        const uint8_t* src = up ? ((R & 1) ? up : gate) + (size_t)(R >> 1) * nb : gate + (size_t)R * nb;
+        dst[scale_off(R, kb, K)] = src[kb];
     }
 }
 
@@ -54,7 +67,6 @@ static int num_sms_of_current_device() {
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 static int check_ws(const moe_dims* m, int T, void* ws, size_t ws_bytes, WsLayout* out) {
     if (!ws) return MOE_ERR_NULL;
@@ -105,23 +117,17 @@ int moe_pack_expert(const moe_dims* dims, const uint8_t* gate_q, const uint8_t* 
     int rc = check_arena(dims, arena);
     if (rc) return rc;
     if (slot < 0 || slot >= arena->num_slots) return MOE_ERR_ARENA;
-    if (!aligned4(gate_q) || !aligned4(gate_s) || !aligned4(up_q) || !aligned4(up_s)) return MOE_ERR_ALIGN;
+    if (!aligned16(gate_q) || !aligned16(up_q) || !aligned16(down_q)) return MOE_ERR_ALIGN;
     cudaStream_t st = (cudaStream_t)stream;
     const int d = dims->d, f = dims->f;
     SlotLayout L = slot_layout(d, f);
     uint8_t* base = static_cast<uint8_t*>(arena->base) + (int64_t)slot * arena->slot_bytes;
     int sms = num_sms_of_current_device();
-    pack_interleave_kernel<<<2 * sms, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(gate_q),
-                                                    reinterpret_cast<const uint32_t*>(up_q),
-                                                    reinterpret_cast<uint32_t*>(base + L.gu_q), f, d / 8);
-    pack_interleave_kernel<<<sms, 256, 0, st>>>(reinterpret_cast<const uint32_t*>(gate_s),
-                                                reinterpret_cast<const uint32_t*>(up_s),
-                                                reinterpret_cast<uint32_t*>(base + L.gu_s), f, d / 128);
+    pack_codes_kernel<<<2 * sms, 256, 0, st>>>(gate_q, up_q, base + L.gu_q, 2 * f, d);
+    pack_scales_kernel<<<sms, 256, 0, st>>>(gate_s, up_s, base + L.gu_s, 2 * f, d);
+    pack_codes_kernel<<<2 * sms, 256, 0, st>>>(down_q, nullptr, base + L.dn_q, d, f);
+    pack_scales_kernel<<<sms, 256, 0, st>>>(down_s, nullptr, base + L.dn_s, d, f);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_LAUNCH;
-    if (cudaMemcpyAsync(base + L.dn_q, down_q, (size_t)d * f / 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-        return MOE_ERR_LAUNCH;
-    if (cudaMemcpyAsync(base + L.dn_s, down_s, (size_t)d * f / 32, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-        return MOE_ERR_LAUNCH;
     return MOE_OK;
 }
 

@@ -141,16 +141,13 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(DecodeArgs a) {
     __syncthreads();
     const int nu = n_uniq;
     const int nchunk = d / kChunk;
-    const int64_t rowq = d / 2, rows_s = d / 32;
     const int gw = blockIdx.x * (blockDim.x >> 5) + warp, nw = gridDim.x * (blockDim.x >> 5);
     const int items = nu * f;
     for (int it = gw; it < items; it += nw) {
         const int u = it / f, i = it % f;
         const uint8_t* base = a.arena + (int64_t)uniq_slot[u] * a.slot_bytes;
-        const uint8_t* gq = base + a.L.gu_q + (int64_t)(2 * i) * rowq;
-        const uint8_t* uq = gq + rowq;
-        const uint8_t* gs = base + a.L.gu_s + (int64_t)(2 * i) * rows_s;
-        const uint8_t* us = gs + rows_s;
+        const uint8_t* cq = base + a.L.gu_q;   // gate row 2i, up row 2i+1 of the tiled matrix
+        const uint8_t* cs = base + a.L.gu_s;
         float accg[XT], accu[XT];
 #pragma unroll
         for (int q = 0; q < XT; ++q) accg[q] = accu[q] = 0.f;
@@ -162,10 +159,10 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(DecodeArgs a) {
             for (int b = 0; b < 5; ++b) {
                 int c = c0 + 32 * b;
                 if (c < nchunk) {
-                    qg[b] = ldg_stream(gq + 16 * c);
-                    qu[b] = ldg_stream(uq + 16 * c);
-                    sg[b] = __ldg(gs + c);
-                    su[b] = __ldg(us + c);
+                    qg[b] = ldg_stream(cq + code_chunk_off(2 * i, c, d));
+                    qu[b] = ldg_stream(cq + code_chunk_off(2 * i + 1, c, d));
+                    sg[b] = __ldg(cs + scale_off(2 * i, c, d));
+                    su[b] = __ldg(cs + scale_off(2 * i + 1, c, d));
                 }
             }
 #pragma unroll
@@ -205,7 +202,6 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
     const int d = a.d, f = a.f, k = a.k;
     const int l8 = lane & 7, grp = lane >> 3;
     const int nchunk = f / kChunk;
-    const int64_t rowq = f / 2, rows_s = f / 32;
     const int rows_per_block = (blockDim.x >> 5) * 4;
     const int r = blockIdx.x * rows_per_block + warp * 4 + grp;
     for (int t = 0; t < a.T; ++t) {
@@ -232,8 +228,8 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
                 int s = a.slot[pair];
                 if (s < 0 || s >= a.num_slots) continue;   // group-uniform: same pair for the warp
                 const uint8_t* base = a.arena + (int64_t)s * a.slot_bytes;
-                const uint8_t* dq = base + a.L.dn_q + (int64_t)r * rowq;
-                const uint8_t* ds = base + a.L.dn_s + (int64_t)r * rows_s;
+                const uint8_t* dq = base + a.L.dn_q;
+                const uint8_t* ds = base + a.L.dn_s;
                 const int p = pexp[j];
                 float acc = 0.f;
                 for (int c0 = l8; c0 < nchunk; c0 += 8 * 9) {
@@ -242,7 +238,7 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
 #pragma unroll
                     for (int b = 0; b < 9; ++b) {
                         int c = c0 + 8 * b;
-                        if (c < nchunk) { qv[b] = ldg_stream(dq + 16 * c); sb[b] = __ldg(ds + c); }
+                        if (c < nchunk) { qv[b] = ldg_stream(dq + code_chunk_off(r, c, f)); sb[b] = __ldg(ds + scale_off(r, c, f)); }
                     }
 #pragma unroll
                     for (int b = 0; b < 9; ++b) {

@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(256) grouped_gemm_kernel(GroupedArgs a) {
         const uint8_t* base = a.arena + (slot_ok ? (int64_t)s * a.slot_bytes : 0);
         const uint8_t* wq = base + (DOWN ? a.L.dn_q : a.L.gu_q);
         const uint8_t* wsb = base + (DOWN ? a.L.dn_s : a.L.gu_s);
-        const int64_t rowq = K / 2, rows_s = K / 32;
         float acc[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -217,8 +216,8 @@ __global__ void __launch_bounds__(256) grouped_gemm_kernel(GroupedArgs a) {
                 uint4 q = make_uint4(0, 0, 0, 0);
                 uint32_t sb = 127;
                 if (slot_ok) {
-                    q = __ldg(reinterpret_cast<const uint4*>(wq + (int64_t)wr * rowq + k0 / 2));
-                    sb = __ldg(wsb + (int64_t)wr * rows_s + k0 / 32);
+                    q = __ldg(reinterpret_cast<const uint4*>(wq + code_chunk_off(wr, k0 / 32, K)));
+                    sb = __ldg(wsb + scale_off(wr, k0 / 32, K));
                 }
                 decode_chunk(q, sb, &Ws[0][tid], kBR + 4);
             }

@@ -1,13 +1,20 @@
 // moe_internal.cuh -- shared definitions of the routed-expert FP4 MoE library (sm_103a).
 //
-// Arena slot layout (private to this library; moe_pack_expert is its only writer):
-//   [0, f*d)                       gate/up codes, 2f rows of d/2 bytes; row 2i = gate row i,
-//                                  row 2i+1 = up row i (a gate row and its up row are adjacent)
-//   [f*d, f*d + f*d/16)            gate/up scales, 2f rows of d/32 bytes, same interleave
-//   [.., + d*f/2)                  down codes, d rows of f/2 bytes
-//   [.., + d*f/32)                 down scales, d rows of f/32 bytes
+// Arena slot layout (private to this library; moe_pack_expert is its only writer).  A slot
+// holds two matrices:
+//   gate/up: 2f rows, K = d; row 2i is gate row i and row 2i+1 is up row i
+//   down:    d rows, K = f
+// Each matrix is stored as tiles of 128 rows x 256 K elements, tile (rt, kb) at index
+// rt * (K/256) + kb, codes and scales in separate regions:
+//   codes  16,384 bytes per tile.  Byte c (0..127) of tile row r sits at
+//          r*128 + ((c/16) ^ (r%8))*16 + c%16 -- the SWIZZLE_128B arrangement, so one
+//          contiguous copy lands a tile in shared memory ready for the tensor cores.
+//   scales 1,024 bytes per tile: two 512-byte tensor-memory scale atoms.  Scale block j
+//          (0..7) of tile row r sits at (j/4)*512 + (r%32)*16 + (r/32)*4 + j%4.
 // Codes keep the checkpoint's e2m1 nibble order (element 2i in the low nibble) and scales
-// are UE8M0 bytes, one per 32 consecutive K elements.
+// are UE8M0 bytes, one per 32 consecutive K elements; only their placement changes.
+// Region order: gate/up codes [0, f*d), gate/up scales (f*d/16 bytes), down codes (d*f/2),
+// down scales (d*f/32); 18,800,640 bytes in all at d=5120, f=2304.
 #pragma once
 
 #include <cstddef>
@@ -22,6 +29,10 @@ constexpr int kDecodeMaxT = 16;     // tokens handled by the decode regime
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kChunk = 32;          // K elements per UE8M0 scale = 16 code bytes
+constexpr int kTileRows = 128;      // rows per arena tile
+constexpr int kTileK = 256;         // K elements per arena tile
+constexpr int kTileCodeBytes = 16384;
+constexpr int kTileScaleBytes = 1024;
 
 struct SlotLayout {
     int64_t gu_q, gu_s, dn_q, dn_s, bytes;
@@ -39,8 +50,24 @@ __host__ __device__ inline SlotLayout slot_layout(int d, int f) {
     return L;
 }
 
+// Offset, inside a matrix's code region, of 16-byte chunk `chunk` (K elements 32*chunk..+31)
+// of matrix row `row`, for a matrix with reduction length K.
+__host__ __device__ inline int64_t code_chunk_off(int row, int chunk, int K) {
+    const int64_t tile = (int64_t)(row / kTileRows) * (K / kTileK) + chunk / 8;
+    const int r = row % kTileRows;
+    return tile * kTileCodeBytes + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
+}
+
+// Offset, inside a matrix's scale region, of the scale byte of K block `kb` (32 elements)
+// of matrix row `row`.
+__host__ __device__ inline int64_t scale_off(int row, int kb, int K) {
+    const int64_t tile = (int64_t)(row / kTileRows) * (K / kTileK) + kb / 8;
+    const int r = row % kTileRows, j = kb & 7;
+    return tile * kTileScaleBytes + (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
+}
+
 inline bool dims_ok(const moe_dims* m) {
-    return m && m->d >= 128 && m->f >= 128 && m->d % 128 == 0 && m->f % 128 == 0 &&
+    return m && m->d >= 256 && m->f >= 256 && m->d % 256 == 0 && m->f % 256 == 0 &&
            m->num_experts >= 1 && m->num_experts <= kMaxExperts && m->top_k >= 1 &&
            m->top_k <= kMaxTopK && m->top_k <= m->num_experts && m->d <= 65536 && m->f <= 65536;
 }

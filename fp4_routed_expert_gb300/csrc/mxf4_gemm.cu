@@ -10,15 +10,17 @@
 // quantising the residual left by q_1..q_(i-1)); the MMA accumulates every term into the same
 // fp32 accumulator, so D = W . x up to the residual after kTerms terms.
 //
-// One persistent kernel, one CTA per SM, 7 warps:
-//   warp 0  TMA producer: weight tile (128 rows x 128 bytes) and kTerms activation tiles
-//           (NT rows x 128 bytes) per 256-element K block, SWIZZLE_128B
-//   warp 1  scale stager: gathers the 8 scale bytes per row of both operands and writes
-//           them in the 512-byte tensor-memory scale atom layout
-//   warp 2  MMA issuer (one lane): tcgen05.cp of the scale atoms, 4 x kTerms MMAs per
+// Every operand sits in global memory in 16 KB code tiles (128 rows x 256 K elements,
+// pre-swizzled for SWIZZLE_128B) and 1 KB scale-atom tiles, so each pipeline stage is four
+// contiguous bulk copies (cp.async.bulk) into shared memory.
+//
+// One persistent kernel, one CTA per SM, 6 warps:
+//   warp 0  producer: bulk copies of the weight tile, its scale atoms, the kTerms activation
+//           tiles (NT rows) and their scale atoms per 256-element K block
+//   warp 1  MMA issuer (one lane): tcgen05.cp of the scale atoms, 4 x kTerms MMAs per
 //           K block, tcgen05.commit to release smem stages and publish accumulators
-//   warps 3-6  epilogue: tcgen05.ld of the accumulator (double-buffered in TMEM), then
-//           gate/up: SwiGLU + requantisation of h into kTerms MXFP4 terms for the down GEMM
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (double-buffered in TMEM), then
+//           gate/up: SwiGLU + requantisation of h into kTerms MXFP4 tiles for the down GEMM
 //           down:    fp32 rows for the fixed-order combine
 // Every wait is bounded; a timeout sets MOE_STATUS_TIMEOUT and the CTA drains and exits.
 #include <cuda.h>
@@ -31,11 +33,10 @@ constexpr int kTerms = 4;
 constexpr int kBM = 128;              // weight rows per tile
 constexpr int kKB = 256;              // K elements per stage
 constexpr int kKBytes = 128;          // code bytes per row per stage
-constexpr int kThreadsGemm = 7 * 32;
+constexpr int kThreadsGemm = 6 * 32;
 constexpr unsigned kSpinLimit = 1u << 25;
 constexpr int kTmemCols = 512;
-constexpr int kSfCols = 8 + 8 * kTerms;   // scale columns per stage in TMEM (A: 2 atoms, B: 2 per term)
-constexpr int kSfRing = 2;
+constexpr int kSfRing = 2;               // scale buffers in TMEM (tcgen05.cp and MMAs run in issue order)
 
 enum { kModeGateUp = 0, kModeDown = 1 };
 enum { kRegimeDecode = 0, kRegimePrefill = 1 };
@@ -69,14 +70,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
     return false;
 }
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
-            dst),
-        "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
+// Contiguous global->shared bulk copy completing on an mbarrier (16-byte aligned, size a
+// multiple of 16).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -130,78 +130,113 @@ __device__ __forceinline__ float e2m1_mag_value(uint32_t c) {
     return c < 4 ? 0.5f * (float)c : (float)(1u << ((c >> 1) - 1)) * (1.0f + 0.5f * (float)(c & 1u));
 }
 
-// Quantise 32 values into kTerms MXFP4 terms (codes: 16 bytes per term, scale byte per term).
-// Term i takes the residual r left by terms 0..i-1: scale 2^e with e the smallest integer
-// such that max|r| <= 6 * 2^e (clamped to the UE8M0 range), codes = nearest e2m1 of r/2^e.
-__device__ void quantize_block32(float* v /*[32], destroyed*/, uint4* codes /*[kTerms]*/, uint8_t* scales /*[kTerms]*/) {
-#pragma unroll 1
-    for (int t = 0; t < kTerms; ++t) {
-        float amax = 0.f;
+// One warp quantises one 32-element block (lane i holds element i) into kTerms MXFP4
+// terms.  Term t takes the residual r left by terms 0..t-1: scale 2^e with e the smallest
+// integer such that max|r| <= 6 * 2^e (clamped to the UE8M0 range), codes = nearest e2m1
+// of r/2^e.  Lane 0 receives the 16 code bytes of every term in codes[t]; every lane
+// receives the scale bytes.
+__device__ __forceinline__ void warp_quantize32(float v, int lane, uint4* codes /*[kTerms], lane 0*/,
+                                                uint32_t* scales /*[kTerms]*/) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    for (int t = 0; t < kTerms; ++t) {
+        float amax = fabsf(v);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         int e = -127;
         const uint32_t u = __float_as_uint(amax);
-        if (amax > 0.f && (u >> 23) != 0u) {                    // normal amax; subnormal residuals are dropped
-            const int e0 = (int)((u >> 23) & 0xFF) - 127;       // floor(log2 amax)
+        if ((u >> 23) != 0u) {                                   // normal amax; subnormal residuals are dropped
+            const int e0 = (int)((u >> 23) & 0xFF) - 127;        // floor(log2 amax)
             const float m = __uint_as_float((u & 0x007FFFFFu) | 0x3F800000u);   // amax / 2^e0 in [1, 2)
-            e = (m <= 1.5f) ? e0 - 2 : e0 - 1;                  // amax <= 6 * 2^e, minimal e
+            e = (m <= 1.5f) ? e0 - 2 : e0 - 1;                   // amax <= 6 * 2^e, minimal e
         }
-        if (e < -127) e = -127;
-        if (e > 127) e = 127;
-        scales[t] = (uint8_t)(e + 127);
+        e = max(-127, min(127, e));
+        scales[t] = (uint32_t)(e + 127);
         const float inv = (e >= -126 && e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : 0.f;   // 2^-e
         const float sc = (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
-        uint32_t w[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float q = v[i] * inv;
-            const uint32_t c = e2m1_mag_code(fminf(fabsf(q), 6.0f));
-            float val = e2m1_mag_value(c) * sc;
-            const uint32_t sgn = (q < 0.f && c) ? 8u : 0u;
-            if (sgn) val = -val;
-            v[i] -= val;
-            w[i >> 3] |= (c | sgn) << (4 * (i & 7));
-        }
-        codes[t] = make_uint4(w[0], w[1], w[2], w[3]);
+        const float q = v * inv;
+        const uint32_t c = e2m1_mag_code(fminf(fabsf(q), 6.0f));
+        const float val = e2m1_mag_value(c) * sc;
+        const bool neg = q < 0.f && c;
+        v -= neg ? -val : val;
+        uint32_t nib = (c | (neg ? 8u : 0u)) << (4 * (lane & 7));
+        nib |= __shfl_xor_sync(0xffffffffu, nib, 1);
+        nib |= __shfl_xor_sync(0xffffffffu, nib, 2);
+        nib |= __shfl_xor_sync(0xffffffffu, nib, 4);              // lanes 8w.. hold word w
+        const uint32_t w1 = __shfl_sync(0xffffffffu, nib, 8), w2 = __shfl_sync(0xffffffffu, nib, 16),
+                       w3 = __shfl_sync(0xffffffffu, nib, 24);
+        codes[t] = make_uint4(nib, w1, w2, w3);
     }
 }
 
-// Activation rows -> kTerms MXFP4 terms.  Output row r (r < nrows) takes token row_src[r]/k,
-// or token r when row_src is NULL (rows r >= T are zero).  Codes [kTerms][nrows][d/2],
-// scales [kTerms][nrows][d/32].  One thread per 32-element block.
-__global__ void quantize_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row_src, int k, int T,
-                                     int nrows, int d, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
-    const int nblk = d / 32;
-    const long total = (long)nrows * nblk;
-    for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
-        const int r = (int)(idx / nblk), b = (int)(idx % nblk);
-        int tok = (r < T) ? r : -1;
-        if (row_src) {
-            const int s = row_src[r];
-            tok = (s >= 0 && s < T * k) ? s / k : -1;
-        }
-        float v[32];
-        if (tok >= 0) {
-            const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * d + 32 * b);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 u = src[i];
-                v[8 * i + 0] = bf16_lo(u.x); v[8 * i + 1] = bf16_hi(u.x);
-                v[8 * i + 2] = bf16_lo(u.y); v[8 * i + 3] = bf16_hi(u.y);
-                v[8 * i + 4] = bf16_lo(u.z); v[8 * i + 5] = bf16_hi(u.z);
-                v[8 * i + 6] = bf16_lo(u.w); v[8 * i + 7] = bf16_hi(u.w);
-            }
+// Activation operands are kept in tiles: tile (t, kb) holds the kTerms x NT rows of B
+// (row r' = term*NT + row, codes pre-swizzled, 128 bytes per row) and their scale atoms,
+// 1 KB per 128 rows of r'.
+__device__ __forceinline__ int64_t act_code_off(int tile, int kb, int term, int row, int chunk, int NT, int KB) {
+    return (((int64_t)tile * KB + kb) * kTerms + term) * NT * 128 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+__device__ __forceinline__ int64_t act_scale_off(int tile, int kb, int term, int row, int j /*0..7*/, int NT, int KB) {
+    const int rr = term * NT + row, blocks = (kTerms * NT + 127) / 128;
+    const int r = rr & 127;
+    return (((int64_t)tile * KB + kb) * blocks + (rr >> 7)) * 1024 + (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
+}
+
+// Group g of the plan holding tile `tile` (plan = [n_active, tiles, e_0.., tile_start_0..]).
+__device__ __forceinline__ int plan_group_of_tile(const int32_t* plan, int E, int tile) {
+    int lo = 0, hi = plan[0] - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (plan[2 + E + mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Activations -> kTerms MXFP4 terms in tile layout, one warp per (tile, row, 32-element
+// block).  Decode (plan == NULL): one tile, row r holds token r (rows >= T are zero).
+// Prefill: the plan's tiles; row r of tile t of group g holds permuted row
+// offsets[e_g] + NT*(t - tile_start_g) + r, i.e. token row_src[n]/k (rows past the group's
+// end are zero).
+__global__ void quantize_tiles_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row_src,
+                                      const int32_t* __restrict__ plan, const int32_t* __restrict__ offsets, int E, int k,
+                                      int T, int d, int NT, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+    const int lane = threadIdx.x & 31;
+    const int nblk = d / 32, KB = d / kKB;
+    const int ntiles = plan ? plan[1] : 1;
+    const long total = (long)ntiles * NT * nblk;
+    const long gw = (blockIdx.x * (long)blockDim.x + threadIdx.x) >> 5, nw = ((long)gridDim.x * blockDim.x) >> 5;
+    for (long idx = gw; idx < total; idx += nw) {
+        const int b = (int)(idx % nblk);
+        const int r = (int)((idx / nblk) % NT);
+        const int tile = (int)(idx / ((long)nblk * NT));
+        int tok = -1;
+        if (!plan) {
+            tok = (r < T) ? r : -1;
         } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            const int g = plan_group_of_tile(plan, E, tile);
+            const int e = plan[2 + g];
+            const int n = offsets[e] + NT * (tile - plan[2 + E + g]) + r;
+            if (n < offsets[e + 1]) {
+                const int s = row_src[n];
+                tok = (s >= 0 && s < T * k) ? s / k : -1;
+            }
         }
+        const int kb = b / 8, j = b % 8;
+        if (tok < 0) {                                       // padding row: zero codes, zero scale
+            if (lane < kTerms) {
+                *reinterpret_cast<uint4*>(q + act_code_off(tile, kb, lane, r, j, NT, KB)) = make_uint4(0, 0, 0, 0);
+                sf[act_scale_off(tile, kb, lane, r, j, NT, KB)] = 0;
+            }
+            continue;
+        }
+        const float v = bf16_to_f32(x[(size_t)tok * d + 32 * b + lane]);
         uint4 codes[kTerms];
-        uint8_t scales[kTerms];
-        quantize_block32(v, codes, scales);
+        uint32_t scales[kTerms];
+        warp_quantize32(v, lane, codes, scales);
+        if (lane == 0) {
 #pragma unroll
-        for (int t = 0; t < kTerms; ++t) {
-            reinterpret_cast<uint4*>(q + ((size_t)t * nrows + r) * (d / 2))[b] = codes[t];
-            sf[((size_t)t * nrows + r) * nblk + b] = scales[t];
+            for (int t = 0; t < kTerms; ++t) {
+                *reinterpret_cast<uint4*>(q + act_code_off(tile, kb, t, r, j, NT, KB)) = codes[t];
+                sf[act_scale_off(tile, kb, t, r, j, NT, KB)] = (uint8_t)scales[t];
+            }
         }
     }
 }
@@ -213,32 +248,43 @@ struct GemmParams {
     int K, kblocks, mtiles;          // reduction length, K / 256, weight rows / 128
     int T, k, E, num_slots;
     const int32_t* slot;             // [T*k]
-    int brows;                       // rows of the B operand buffers
-    int decode_cols;                 // decode: B rows [0, decode_cols) in every unit
+    int decode_cols;                 // decode: valid columns (B rows) in every unit
     const int32_t* plan;             // prefill: [n_active, tiles, e_0.., tile_start_0..] (NT-row tiles)
     const int32_t* offsets;
     const int32_t* row_src;
     const uint8_t* arena;
-    int64_t slot_bytes, a_sf_off;    // scales of the A matrix inside a slot (row-major [rows][K/32])
-    const uint8_t* b_sf;             // activations' scales, row-major [kTerms][brows][K/32]
-    uint8_t* hq;                     // gate/up: h codes [kTerms][hrows][f/2]
-    uint8_t* hsf;                    // gate/up: h scales [kTerms][hrows][f/32]
-    int hrows;
+    int64_t slot_bytes, a_code_off, a_sf_off;   // weight matrix regions inside a slot
+    const uint8_t* b_q;              // activation tiles (codes)
+    const uint8_t* b_sf;             // activation tiles (scale atoms)
+    uint8_t* hq;                     // gate/up: h tiles for the down GEMM (codes)
+    uint8_t* hsf;                    // gate/up: h tiles (scale atoms)
+    int h_nt;                        // rows per h tile
     int f;
     float* rows_out;                 // down: [rows][d]
     int d;
     int32_t* status;
 };
 
+// Per-NT shape of the pipeline.  B rows per tile = kTerms*NT, split into MMA groups of at
+// most 128 rows (N of one MMA).  ACC independent accumulators (K slices alternate between
+// them so the tensor core can overlap their dependency chains) and DBUF accumulator sets
+// (epilogue of one unit overlapping the next unit's MMAs) fit in TMEM columns [0, 256).
 template <int NT>
-struct GemmSmem {
+struct GemmCfg {
+    static constexpr int kRows = kTerms * NT;
+    static constexpr int kGroups = kRows > 128 ? kRows / 128 : 1;
+    static constexpr int kN = kRows > 128 ? 128 : kRows;
+    static constexpr int kAcc = kRows <= 128 ? 2 : 1;
+    static constexpr int kDbuf = kRows <= 64 ? 2 : 1;
+    static_assert(kDbuf * kAcc * kRows <= 256, "accumulators exceed their TMEM columns");
+    static constexpr int kSfCols = 8 + 8 * kGroups;          // scale columns per stage (A + B)
     static constexpr int kA = kBM * kKBytes;                 // 16 KB
-    static constexpr int kB = kTerms * NT * kKBytes;
+    static constexpr int kB = kRows * kKBytes;
     static constexpr int kSFA = 1024;
-    static constexpr int kSFB = kTerms * 1024;
+    static constexpr int kSFB = kGroups * 1024;
     static constexpr int kStage = kA + kB + kSFA + kSFB;     // a multiple of 1024
     static constexpr int kH = NT * 64 * 4;                   // gate/up epilogue h tile
-    static constexpr int kBudget = 224 * 1024;               // dynamic smem (static use stays below 3 KB)
+    static constexpr int kBudget = 224 * 1024;               // dynamic smem (static use stays below 1 KB)
     static constexpr int kFit = (kBudget - kH - 2048) / kStage;
     static constexpr int kStages = kFit > 8 ? 8 : kFit;
     static constexpr int kBytes = kStages * kStage + kH + 1024 /*barriers*/ + 1024 /*alignment*/;
@@ -248,8 +294,9 @@ struct GemmSmem {
 struct UnitInfo {
     int slot;       // arena slot of the weights
     int m;          // weight row tile
-    int brow0;      // first B row
-    int ncols;      // valid B rows (columns of D)
+    int btile;      // activation tile
+    int brow0;      // first B row (row index of the activation rows / outputs)
+    int ncols;      // valid columns of D
 };
 
 template <int NT>
@@ -257,6 +304,7 @@ __device__ __forceinline__ bool unit_info(const GemmParams& p, int unit, const i
     if (p.regime == kRegimeDecode) {
         u.m = unit % p.mtiles;
         u.slot = uslots[unit / p.mtiles];
+        u.btile = 0;
         u.brow0 = 0;
         u.ncols = p.decode_cols;
         return true;
@@ -273,7 +321,9 @@ __device__ __forceinline__ bool unit_info(const GemmParams& p, int unit, const i
     const int ntiles = (o1 - o0 + NT - 1) / NT;
     const int local = unit - p.plan[2 + E + g] * p.mtiles;
     u.m = local / ntiles;
-    u.brow0 = o0 + (local % ntiles) * NT;
+    const int nt = local % ntiles;
+    u.btile = p.plan[2 + E + g] + nt;
+    u.brow0 = o0 + nt * NT;
     u.ncols = min(NT, o1 - u.brow0);
     const int src = p.row_src[o0];
     u.slot = (src >= 0 && src < p.T * p.k) ? p.slot[src] : -1;
@@ -281,19 +331,17 @@ __device__ __forceinline__ bool unit_info(const GemmParams& p, int unit, const i
 }
 
 template <int NT, int MODE>
-__global__ void __launch_bounds__(kThreadsGemm, 1)
-    mxf4_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, GemmParams p) {
-    using S = GemmSmem<NT>;
+__global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p) {
+    using C = GemmCfg<NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stage_base = smem;
-    float* hbuf = reinterpret_cast<float*>(smem + S::kStages * S::kStage);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStage + S::kH);
-    uint64_t* full = bars;                       // TMA bytes of a stage landed
-    uint64_t* sf_full = bars + S::kStages;       // scales of a stage staged
-    uint64_t* empty = bars + 2 * S::kStages;     // MMAs of a stage finished
-    uint64_t* tfull = bars + 3 * S::kStages;     // [2] accumulator ready
-    uint64_t* tempty = tfull + 2;                // [2] accumulator drained
+    float* hbuf = reinterpret_cast<float*>(smem + C::kStages * C::kStage);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage + C::kH);
+    uint64_t* full = bars;                       // bytes of a stage landed
+    uint64_t* empty = bars + C::kStages;         // MMAs of a stage finished
+    uint64_t* tfull = bars + 2 * C::kStages;     // [2] accumulator set ready
+    uint64_t* tempty = tfull + 2;                // [2] accumulator set drained
     uint64_t* epibar = tempty + 2;               // [2] epilogue warps' h-tile hand-offs
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
@@ -304,9 +352,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         abort_flag = 0;
-        for (int s = 0; s < S::kStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&sf_full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -316,7 +363,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 2) {
+    if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_sh)),
                      "r"(kTmemCols)
                      : "memory");
@@ -357,34 +404,36 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     volatile int* abortp = &abort_flag;
 
     if (warp == 0) {
-        // ---------------- TMA producer
+        // ---------------- producer: four contiguous bulk copies per stage
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_parity = 0;   // per-stage bit masks
             for (int unit = blockIdx.x; unit < n_units && !*abortp; unit += gridDim.x) {
                 UnitInfo u;
                 const bool ok = unit_info<NT>(p, unit, uslots, u);
-                const int slot = ok ? u.slot : 0;
+                const uint8_t* sbase = p.arena + (int64_t)(ok ? u.slot : 0) * p.slot_bytes;
                 for (int kb = 0; kb < p.kblocks; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abortp)) {
                         atomicOr(p.status, MOE_STATUS_TIMEOUT);
                         *abortp = 1;
                         break;
                     }
-                    uint8_t* st = stage_base + stage * S::kStage;
+                    const uint32_t st = smem_u32(stage_base + stage * C::kStage);
                     const uint32_t bar = smem_u32(&full[stage]);
-                    mbar_expect_tx(bar, S::kA + S::kB);
-                    tma_load_3d(smem_u32(st), &mapA, kb * kKBytes, u.m * kBM, slot, bar);
-#pragma unroll
-                    for (int t = 0; t < kTerms; ++t)
-                        tma_load_3d(smem_u32(st + S::kA + t * NT * kKBytes), &mapB, kb * kKBytes, u.brow0, t, bar);
+                    const int64_t atile = (int64_t)u.m * p.kblocks + kb;
+                    const int64_t btile = (int64_t)u.btile * p.kblocks + kb;
+                    mbar_expect_tx(bar, C::kStage);
+                    bulk_g2s(st, sbase + p.a_code_off + atile * kTileCodeBytes, C::kA, bar);
+                    bulk_g2s(st + C::kA, p.b_q + btile * C::kB, C::kB, bar);
+                    bulk_g2s(st + C::kA + C::kB, sbase + p.a_sf_off + atile * kTileScaleBytes, C::kSFA, bar);
+                    bulk_g2s(st + C::kA + C::kB + C::kSFA, p.b_sf + btile * C::kSFB, C::kSFB, bar);
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
-            // every issued load lands before the CTA may exit (bounded)
-            for (int s2 = 0; s2 < S::kStages; ++s2) {
+            // every issued copy lands before the CTA may exit (bounded)
+            for (int s2 = 0; s2 < C::kStages; ++s2) {
                 if (!((issued >> s2) & 1u)) continue;
                 const uint32_t ph = (issued_parity >> s2) & 1u;
                 for (unsigned i = 0; i < kSpinLimit; ++i)
@@ -392,56 +441,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             }
         }
     } else if (warp == 1) {
-        // ---------------- scale stager: 8 bytes per row and 256-element K block
-        int stage = 0;
-        uint32_t phase = 0;
-        const int rowbytes = p.K / 32;
-        for (int unit = blockIdx.x; unit < n_units && !*abortp; unit += gridDim.x) {
-            UnitInfo u;
-            const bool ok = unit_info<NT>(p, unit, uslots, u);
-            const uint8_t* asf = p.arena + (int64_t)(ok ? u.slot : 0) * p.slot_bytes + p.a_sf_off;
-            bool failed = false;
-            for (int kb = 0; kb < p.kblocks; ++kb) {
-                if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abortp)) {
-                    if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
-                    failed = true;
-                    break;
-                }
-                uint8_t* st = stage_base + stage * S::kStage;
-                uint8_t* sfa = st + S::kA + S::kB;
-                uint8_t* sfb = sfa + S::kSFA;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = lane + 32 * i;
-                    const uint2 v = *reinterpret_cast<const uint2*>(asf + (int64_t)(u.m * kBM + r) * rowbytes + kb * 8);
-                    const int o = (r & 31) * 16 + (r >> 5) * 4;
-                    *reinterpret_cast<uint32_t*>(sfa + o) = v.x;
-                    *reinterpret_cast<uint32_t*>(sfa + 512 + o) = v.y;
-                }
-#pragma unroll
-                for (int t = 0; t < kTerms; ++t) {
-                    for (int r = lane; r < NT; r += 32) {
-                        const int row = u.brow0 + r;
-                        uint2 v = make_uint2(0, 0);
-                        if (row < p.brows)
-                            v = *reinterpret_cast<const uint2*>(p.b_sf + ((int64_t)t * p.brows + row) * rowbytes + kb * 8);
-                        const int o = (r & 31) * 16 + (r >> 5) * 4;
-                        *reinterpret_cast<uint32_t*>(sfb + t * 1024 + o) = v.x;
-                        *reinterpret_cast<uint32_t*>(sfb + t * 1024 + 512 + o) = v.y;
-                    }
-                }
-                fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sf_full[stage]));
-                if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
-            }
-            if (failed) break;
-        }
-    } else if (warp == 2) {
         // ---------------- MMA issuer
         if (lane == 0) {
             int stage = 0, sfring = 0, acc = 0;
             uint32_t phase = 0, aphase = 0;
+            const uint32_t idesc_lo = idesc_mxf4(C::kN, 0), idesc_hi = idesc_mxf4(C::kN, 2);
             for (int unit = blockIdx.x; unit < n_units && !*abortp; unit += gridDim.x) {
                 if (!mbar_wait(smem_u32(&tempty[acc]), aphase ^ 1u, abortp)) {
                     atomicOr(p.status, MOE_STATUS_TIMEOUT);
@@ -449,54 +453,55 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dcol = tmem + acc * NT;
+                const uint32_t dset = tmem + acc * C::kAcc * C::kRows;
                 bool failed = false;
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!mbar_wait(smem_u32(&full[stage]), phase, abortp) ||
-                        !mbar_wait(smem_u32(&sf_full[stage]), phase, abortp)) {
+                    if (!mbar_wait(smem_u32(&full[stage]), phase, abortp)) {
                         atomicOr(p.status, MOE_STATUS_TIMEOUT);
                         *abortp = 1;
                         failed = true;
                         break;
                     }
                     tc_fence_after();
-                    uint8_t* st = stage_base + stage * S::kStage;
-                    const uint32_t sa = smem_u32(st), sb = smem_u32(st + S::kA);
-                    const uint32_t ssfa = smem_u32(st + S::kA + S::kB), ssfb = ssfa + S::kSFA;
-                    const uint32_t sfcol = tmem + 256 + sfring * kSfCols;
+                    uint8_t* st = stage_base + stage * C::kStage;
+                    const uint32_t sa = smem_u32(st), sb = smem_u32(st + C::kA);
+                    const uint32_t ssfa = smem_u32(st + C::kA + C::kB), ssfb = ssfa + C::kSFA;
+                    const uint32_t sfcol = tmem + 256 + sfring * C::kSfCols;
                     tc_cp_sf(sfcol + 0, desc_sf(ssfa));
                     tc_cp_sf(sfcol + 4, desc_sf(ssfa + 512));
 #pragma unroll
-                    for (int t = 0; t < kTerms; ++t) {
-                        tc_cp_sf(sfcol + 8 + 8 * t, desc_sf(ssfb + t * 1024));
-                        tc_cp_sf(sfcol + 8 + 8 * t + 4, desc_sf(ssfb + t * 1024 + 512));
+                    for (int g = 0; g < C::kGroups; ++g) {
+                        tc_cp_sf(sfcol + 8 + 8 * g, desc_sf(ssfb + g * 1024));
+                        tc_cp_sf(sfcol + 8 + 8 * g + 4, desc_sf(ssfb + g * 1024 + 512));
                     }
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const uint32_t id = idesc_mxf4(NT, 2 * (j & 1));
+                        const int a = j % C::kAcc;
                         const uint64_t ad = desc_sw128(sa + 32 * j);
+                        const uint32_t accumulate = (kb > 0 || j >= C::kAcc) ? 1u : 0u;
 #pragma unroll
-                        for (int t = 0; t < kTerms; ++t) {
-                            const uint64_t bd = desc_sw128(sb + t * NT * kKBytes + 32 * j);
-                            mma_mxf4(dcol, ad, bd, id, sfcol + 4 * (j >> 1), sfcol + 8 + 8 * t + 4 * (j >> 1),
-                                     (kb | j | t) ? 1u : 0u);
+                        for (int g = 0; g < C::kGroups; ++g) {
+                            const uint64_t bd = desc_sw128(sb + g * 128 * kKBytes + 32 * j);
+                            mma_mxf4(dset + a * C::kRows + g * 128, ad, bd, (j & 1) ? idesc_hi : idesc_lo,
+                                     sfcol + 4 * (j >> 1), sfcol + 8 + 8 * g + 4 * (j >> 1), accumulate);
                         }
                     }
                     tc_commit(smem_u32(&empty[stage]));
-                    if (++stage == S::kStages) { stage = 0; phase ^= 1u; }
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                     sfring = (sfring + 1) % kSfRing;
                 }
                 if (failed) break;
                 tc_commit(smem_u32(&tfull[acc]));
-                if (++acc == 2) { acc = 0; aphase ^= 1u; }
+                if (++acc == C::kDbuf) { acc = 0; aphase ^= 1u; }
             }
         }
     } else {
-        // ---------------- epilogue (warps 3..6 -> TMEM lane quarters 3, 0, 1, 2)
+        // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
         const int q = warp & 3;
-        const int ew = warp - 3;
+        const int ew = warp - 2;
         int acc = 0;
         uint32_t aphase = 0, ephase = 0;
+        const int KBf = p.f / kKB;
         for (int unit = blockIdx.x; unit < n_units && !*abortp; unit += gridDim.x) {
             UnitInfo u;
             const bool ok = unit_info<NT>(p, unit, uslots, u);
@@ -506,13 +511,26 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
             }
             tc_fence_after();
             const int row = q * 32 + lane;       // accumulator row = weight row within the tile
+            // D[row][n] = sum over accumulators and terms of column (a*kRows + t*NT + n)
             float vals[NT];
 #pragma unroll
-            for (int c0 = 0; c0 < NT; c0 += 16) tc_ld16(tmem + ((uint32_t)(q * 32) << 16) + acc * NT + c0, vals + c0);
+            for (int c = 0; c < NT; ++c) vals[c] = 0.f;
+            const uint32_t lanebase = tmem + ((uint32_t)(q * 32) << 16) + acc * C::kAcc * C::kRows;
+#pragma unroll
+            for (int a = 0; a < C::kAcc; ++a)
+#pragma unroll
+                for (int t = 0; t < kTerms; ++t)
+#pragma unroll
+                    for (int c0 = 0; c0 < NT; c0 += 16) {
+                        float tmp[16];
+                        tc_ld16(lanebase + a * C::kRows + t * NT + c0, tmp);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) vals[c0 + i] += tmp[i];
+                    }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
-            if (++acc == 2) { acc = 0; aphase ^= 1u; }
+            if (++acc == C::kDbuf) { acc = 0; aphase ^= 1u; }
             if (!ok) continue;
             if (MODE == kModeDown) {
                 const int r = u.m * kBM + row;    // output feature
@@ -538,30 +556,29 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
                     if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
                     break;
                 }
-                // quantise: job = (column c, block b of 32 outputs)
-                const int fblk = p.f / 32;
-                for (int job = ew * 32 + lane; job < NT * 2; job += 128) {
+                // quantise, one warp per job = (column c, block b of 32 outputs i0 = 64m + 32b)
+                for (int job = ew; job < NT * 2; job += 4) {
                     const int c = job >> 1, b = job & 1;
-                    float v[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = hbuf[c * 64 + 32 * b + i];
                     uint4 codes[kTerms];
-                    uint8_t scales[kTerms];
-                    quantize_block32(v, codes, scales);
-                    auto write_row = [&](int hrow) {
+                    uint32_t scales[kTerms];
+                    warp_quantize32(hbuf[c * 64 + 32 * b + lane], lane, codes, scales);
+                    const int i0 = u.m * 64 + 32 * b, kb = i0 / kKB, j = (i0 % kKB) / 32;
+                    if (lane == 0) {
+                        auto write_row = [&](int htile, int hrow) {
 #pragma unroll
-                        for (int t = 0; t < kTerms; ++t) {
-                            reinterpret_cast<uint4*>(p.hq + ((size_t)t * p.hrows + hrow) * (p.f / 2))[u.m * 2 + b] = codes[t];
-                            p.hsf[((size_t)t * p.hrows + hrow) * fblk + u.m * 2 + b] = scales[t];
+                            for (int t = 0; t < kTerms; ++t) {
+                                *reinterpret_cast<uint4*>(p.hq + act_code_off(htile, kb, t, hrow, j, p.h_nt, KBf)) = codes[t];
+                                p.hsf[act_scale_off(htile, kb, t, hrow, j, p.h_nt, KBf)] = (uint8_t)scales[t];
+                            }
+                        };
+                        if (p.regime == kRegimeDecode) {
+                            // column c = token; h for every pair (c, jj) routed to this slot
+                            if (c < p.T)
+                                for (int jj = 0; jj < p.k; ++jj)
+                                    if (p.slot[c * p.k + jj] == u.slot) write_row(0, c * p.k + jj);
+                        } else if (c < u.ncols) {
+                            write_row(u.btile, c);
                         }
-                    };
-                    if (p.regime == kRegimeDecode) {
-                        // column c = token; h for every pair (c, j) routed to this slot
-                        if (c < p.T)
-                            for (int j = 0; j < p.k; ++j)
-                                if (p.slot[c * p.k + j] == u.slot) write_row(c * p.k + j);
-                    } else if (c < u.ncols) {
-                        write_row(u.brow0 + c);
                     }
                 }
                 // hand-off 2: hbuf may be overwritten by the next unit
@@ -578,7 +595,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
 // y[t] = bf16( sum_j w[t,j] rows[t*k + j] ) in ascending j, skipping pairs without a valid slot.
@@ -606,61 +623,46 @@ __global__ void decode_combine_kernel(int T, int d, int k, int num_slots, const 
 
 // ------------------------------------------------------------------ host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (EncodeTiledFn)ptr;
-    }
-    return fn;
-}
-
-// 3-D uint8 tensor [planes][rows][xbytes] with the given row and plane strides;
-// box {128 bytes, box_rows, 1}, SWIZZLE_128B; out-of-range rows read as zero.
-static bool make_map(CUtensorMap* m, const void* base, uint64_t xbytes, uint64_t rows, uint64_t planes,
-                     uint64_t row_stride, uint64_t plane_stride, uint32_t box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {xbytes, rows, planes};
-    cuuint64_t strides[2] = {row_stride, plane_stride};
-    cuuint32_t box[3] = {128, box_rows, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int NT, int MODE>
-static int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int grid, cudaStream_t st) {
-    using S = GemmSmem<NT>;
-    if (cudaFuncSetAttribute(mxf4_gemm_kernel<NT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kBytes) !=
+static int launch_gemm(const GemmParams& p, int grid, cudaStream_t st) {
+    using C = GemmCfg<NT>;
+    if (cudaFuncSetAttribute(mxf4_gemm_kernel<NT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes) !=
         cudaSuccess)
         return MOE_ERR_LAUNCH;
-    mxf4_gemm_kernel<NT, MODE><<<grid, kThreadsGemm, S::kBytes, st>>>(ma, mb, p);
+    mxf4_gemm_kernel<NT, MODE><<<grid, kThreadsGemm, C::kBytes, st>>>(p);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
 template <int MODE>
-static int launch_gemm_nt(int NT, const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int grid,
-                          cudaStream_t st) {
+static int launch_gemm_nt(int NT, const GemmParams& p, int grid, cudaStream_t st) {
     switch (NT) {
-        case 16: return launch_gemm<16, MODE>(ma, mb, p, grid, st);
-        case 32: return launch_gemm<32, MODE>(ma, mb, p, grid, st);
-        case 64: return launch_gemm<64, MODE>(ma, mb, p, grid, st);
-        case 128: return launch_gemm<128, MODE>(ma, mb, p, grid, st);
+        case 16: return launch_gemm<16, MODE>(p, grid, st);
+        case 32: return launch_gemm<32, MODE>(p, grid, st);
+        case 64: return launch_gemm<64, MODE>(p, grid, st);
         default: return MOE_ERR_LAUNCH;
     }
 }
 
-// Tensor-core buffers inside the workspace (WsLayout.tc), sized for R = T*k rows.
+constexpr int kPrefillNT = 32;
+constexpr int kMaxNT = 64;
+
+// Capacity of the activation tile buffers for T tokens: decode uses one tile of up to kMaxNT
+// rows; the prefill plan needs at most ceil(T*k/NT) + min(E, T*k) tiles of kPrefillNT rows.
+static size_t act_tiles(const moe_dims* m, int T) {
+    const size_t n = (size_t)(T > 0 ? T : 1) * m->top_k;
+    const size_t t = (n + kPrefillNT - 1) / kPrefillNT + (n < (size_t)m->num_experts ? n : (size_t)m->num_experts);
+    return t > 1 ? t : 1;
+}
+static size_t act_rows(const moe_dims* m, int T) {
+    const size_t r = act_tiles(m, T) * kPrefillNT;
+    return r > (size_t)kMaxNT ? r : (size_t)kMaxNT;
+}
+static size_t act_sf_blocks(const moe_dims* m, int T) {      // 1 KB scale blocks per K block
+    const size_t b = act_tiles(m, T) * ((kTerms * kPrefillNT + 127) / 128);
+    const size_t dec = (kTerms * kMaxNT + 127) / 128;
+    return b > dec ? b : dec;
+}
+
 struct TcBuffers {
     uint8_t *xq, *xsf, *hq, *hsf;
     float* rows;
@@ -669,12 +671,12 @@ struct TcBuffers {
 
 static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& L) {
     TcBuffers b;
-    const size_t R = (size_t)(T > 0 ? T : 1) * m->top_k;
+    const size_t rows = act_rows(m, T), sfb = act_sf_blocks(m, T);
     char* o = ws + L.tc;
-    b.xq = reinterpret_cast<uint8_t*>(o);  o += align256((size_t)kTerms * R * m->d / 2);
-    b.xsf = reinterpret_cast<uint8_t*>(o); o += align256((size_t)kTerms * R * m->d / 32);
-    b.hq = reinterpret_cast<uint8_t*>(o);  o += align256((size_t)kTerms * R * m->f / 2);
-    b.hsf = reinterpret_cast<uint8_t*>(o); o += align256((size_t)kTerms * R * m->f / 32);
+    b.xq = reinterpret_cast<uint8_t*>(o);  o += align256(rows * kTerms * m->d / 2);
+    b.xsf = reinterpret_cast<uint8_t*>(o); o += align256(sfb * (m->d / kKB) * 1024);
+    b.hq = reinterpret_cast<uint8_t*>(o);  o += align256(rows * kTerms * m->f / 2);
+    b.hsf = reinterpret_cast<uint8_t*>(o); o += align256(sfb * (m->f / kKB) * 1024);
     b.rows = reinterpret_cast<float*>(o);
     b.plan = reinterpret_cast<int32_t*>(ws + L.active);
     return b;
@@ -682,47 +684,52 @@ static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& 
 
 size_t tc_workspace_bytes(const moe_dims* m, int T) {
     const size_t R = (size_t)(T > 0 ? T : 1) * m->top_k;
-    return align256((size_t)kTerms * R * m->d / 2) + align256((size_t)kTerms * R * m->d / 32) +
-           align256((size_t)kTerms * R * m->f / 2) + align256((size_t)kTerms * R * m->f / 32) + align256(R * m->d * 4);
+    const size_t rows = act_rows(m, T), sfb = act_sf_blocks(m, T);
+    return align256(rows * kTerms * m->d / 2) + align256(sfb * (m->d / kKB) * 1024) + align256(rows * kTerms * m->f / 2) +
+           align256(sfb * (m->f / kKB) * 1024) + align256(R * m->d * 4);
 }
 
-static int nt_for(int cols) { return cols <= 16 ? 16 : cols <= 32 ? 32 : cols <= 64 ? 64 : 128; }
+static int nt_for(int cols) { return cols <= 16 ? 16 : cols <= 32 ? 32 : 64; }
 
 bool tc_supported(const moe_dims* m) { return m->d % kKB == 0 && m->f % kKB == 0; }
-bool tc_decode_supported(const moe_dims* m, int T) { return tc_supported(m) && T >= 1 && T * m->top_k <= 128; }
+bool tc_decode_supported(const moe_dims* m, int T) { return tc_supported(m) && T >= 1 && T * m->top_k <= kMaxNT; }
 
-// Decode regime: quantise x, gate/up GEMM (SwiGLU, h quantised per (token, j) pair), down
-// GEMM (one fp32 row per pair), fixed-order combine into y.
+static GemmParams base_params(const moe_dims* m, const moe_arena* ar, int T, const int32_t* slot, int32_t* status) {
+    GemmParams p{};
+    p.T = T; p.k = m->top_k; p.E = m->num_experts; p.num_slots = ar->num_slots;
+    p.slot = slot; p.arena = reinterpret_cast<const uint8_t*>(ar->base); p.slot_bytes = ar->slot_bytes;
+    p.f = m->f; p.d = m->d; p.status = status;
+    return p;
+}
+
+// Decode regime: quantise x into one tile, gate/up GEMM (SwiGLU, h quantised per (token, j)
+// pair into one tile), down GEMM (one fp32 row per pair), fixed-order combine into y.
 int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                      const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
                      int num_sms) {
     if (T == 0) return MOE_OK;
     TcBuffers b = tc_buffers(m, T, ws, L);
-    const int d = m->d, f = m->f, k = m->top_k;
-    const int R = T * k;
+    const int d = m->d, f = m->f, k = m->top_k, R = T * k;
     const SlotLayout SL = slot_layout(d, f);
-    quantize_rows_kernel<<<(T * (d / 32) + 255) / 256, 256, 0, st>>>(x, nullptr, k, T, T, d, b.xq, b.xsf);
-    const uint8_t* base = reinterpret_cast<const uint8_t*>(ar->base);
-    CUtensorMap mA, mB, mA2, mB2;
-    const int nt1 = nt_for(T);
-    if (!make_map(&mA, base + SL.gu_q, d / 2, 2 * f, ar->num_slots, d / 2, ar->slot_bytes, kBM)) return MOE_ERR_LAUNCH;
-    if (!make_map(&mB, b.xq, d / 2, T, kTerms, d / 2, (uint64_t)T * d / 2, nt1)) return MOE_ERR_LAUNCH;
-    GemmParams p{};
+    const int nt1 = nt_for(T), nt2 = nt_for(R);
+    const int qwarps = nt1 * (d / 32);
+    quantize_tiles_kernel<<<(qwarps + 7) / 8, 256, 0, st>>>(x, nullptr, nullptr, nullptr, m->num_experts, k, T, d, nt1,
+                                                          b.xq, b.xsf);
+    GemmParams p = base_params(m, ar, T, slot, status);
     p.mode = kModeGateUp; p.regime = kRegimeDecode;
     p.K = d; p.kblocks = d / kKB; p.mtiles = 2 * f / kBM;
-    p.T = T; p.k = k; p.E = m->num_experts; p.num_slots = ar->num_slots;
-    p.slot = slot; p.brows = T; p.hrows = R; p.decode_cols = T;
-    p.arena = base; p.slot_bytes = ar->slot_bytes; p.a_sf_off = SL.gu_s;
-    p.b_sf = b.xsf; p.hq = b.hq; p.hsf = b.hsf; p.f = f; p.rows_out = b.rows; p.d = d; p.status = status;
-    int rc = launch_gemm_nt<kModeGateUp>(nt1, mA, mB, p, num_sms, st);
+    p.decode_cols = T;
+    p.a_code_off = SL.gu_q; p.a_sf_off = SL.gu_s;
+    p.b_q = b.xq; p.b_sf = b.xsf;
+    p.hq = b.hq; p.hsf = b.hsf; p.h_nt = nt2;
+    int rc = launch_gemm_nt<kModeGateUp>(nt1, p, num_sms, st);
     if (rc) return rc;
-    const int nt2 = nt_for(R);
-    if (!make_map(&mA2, base + SL.dn_q, f / 2, d, ar->num_slots, f / 2, ar->slot_bytes, kBM)) return MOE_ERR_LAUNCH;
-    if (!make_map(&mB2, b.hq, f / 2, R, kTerms, f / 2, (uint64_t)R * f / 2, nt2)) return MOE_ERR_LAUNCH;
     GemmParams q = p;
     q.mode = kModeDown; q.K = f; q.kblocks = f / kKB; q.mtiles = d / kBM;
-    q.brows = R; q.decode_cols = R; q.a_sf_off = SL.dn_s; q.b_sf = b.hsf;
-    rc = launch_gemm_nt<kModeDown>(nt2, mA2, mB2, q, num_sms, st);
+    q.decode_cols = R;
+    q.a_code_off = SL.dn_q; q.a_sf_off = SL.dn_s;
+    q.b_q = b.hq; q.b_sf = b.hsf; q.rows_out = b.rows;
+    rc = launch_gemm_nt<kModeDown>(nt2, q, num_sms, st);
     if (rc) return rc;
     decode_combine_kernel<<<(T * (d / 4) + 255) / 256, 256, 0, st>>>(T, d, k, ar->num_slots, b.rows, slot, w, y);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
@@ -730,11 +737,9 @@ int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16
 
 __global__ void plan_kernel(int E, int n, const int32_t* offsets, int32_t* plan, int32_t* status, int tile_rows);
 
-constexpr int kPrefillNT = 64;
-
-// Prefill regime: x rows quantised in permuted (grouped) order, gate/up GEMM per (group,
-// weight tile, 64-row tile) with SwiGLU + h quantisation, down GEMM to per-row fp32 outputs;
-// the caller's combine sums them in fixed order.
+// Prefill regime: x rows quantised into the plan's tiles (grouped by expert), gate/up GEMM
+// per (group, weight tile, row tile) with SwiGLU + h quantisation into the same tiles, down
+// GEMM to per-row fp32 outputs; the caller's combine sums them in fixed order.
 int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                       const int32_t* offsets, const int32_t* row_src, float* rows_out, int32_t* status, char* ws,
                       const WsLayout& L, cudaStream_t st, int num_sms) {
@@ -743,28 +748,25 @@ int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint1
     const int d = m->d, f = m->f, k = m->top_k, n = T * k;
     const SlotLayout SL = slot_layout(d, f);
     plan_kernel<<<1, 32, 0, st>>>(m->num_experts, n, offsets, b.plan, status, kPrefillNT);
-    const long qblocks = ((long)n * (d / 32) + 255) / 256;
-    quantize_rows_kernel<<<(int)(qblocks > 8L * num_sms ? 8L * num_sms : qblocks), 256, 0, st>>>(x, row_src, k, T, n, d,
-                                                                                                 b.xq, b.xsf);
-    const uint8_t* base = reinterpret_cast<const uint8_t*>(ar->base);
-    CUtensorMap mA, mB, mA2, mB2;
-    if (!make_map(&mA, base + SL.gu_q, d / 2, 2 * f, ar->num_slots, d / 2, ar->slot_bytes, kBM)) return MOE_ERR_LAUNCH;
-    if (!make_map(&mB, b.xq, d / 2, n, kTerms, d / 2, (uint64_t)n * d / 2, kPrefillNT)) return MOE_ERR_LAUNCH;
-    GemmParams p{};
+    const long qwarps = (long)act_tiles(m, T) * kPrefillNT * (d / 32);
+    const long qblocks = (qwarps + 7) / 8;
+    quantize_tiles_kernel<<<(int)(qblocks > 16L * num_sms ? 16L * num_sms : qblocks), 256, 0, st>>>(
+        x, row_src, b.plan, offsets, m->num_experts, k, T, d, kPrefillNT, b.xq, b.xsf);
+    GemmParams p = base_params(m, ar, T, slot, status);
     p.mode = kModeGateUp; p.regime = kRegimePrefill;
     p.K = d; p.kblocks = d / kKB; p.mtiles = 2 * f / kBM;
-    p.T = T; p.k = k; p.E = m->num_experts; p.num_slots = ar->num_slots;
-    p.slot = slot; p.brows = n; p.hrows = n; p.decode_cols = 0;
     p.plan = b.plan; p.offsets = offsets; p.row_src = row_src;
-    p.arena = base; p.slot_bytes = ar->slot_bytes; p.a_sf_off = SL.gu_s;
-    p.b_sf = b.xsf; p.hq = b.hq; p.hsf = b.hsf; p.f = f; p.rows_out = rows_out; p.d = d; p.status = status;
-    int rc = launch_gemm_nt<kModeGateUp>(kPrefillNT, mA, mB, p, num_sms, st);
+    p.a_code_off = SL.gu_q; p.a_sf_off = SL.gu_s;
+    p.b_q = b.xq; p.b_sf = b.xsf;
+    p.hq = b.hq; p.hsf = b.hsf; p.h_nt = kPrefillNT;
+    p.rows_out = rows_out;
+    int rc = launch_gemm_nt<kModeGateUp>(kPrefillNT, p, num_sms, st);
     if (rc) return rc;
-    if (!make_map(&mA2, base + SL.dn_q, f / 2, d, ar->num_slots, f / 2, ar->slot_bytes, kBM)) return MOE_ERR_LAUNCH;
-    if (!make_map(&mB2, b.hq, f / 2, n, kTerms, f / 2, (uint64_t)n * f / 2, kPrefillNT)) return MOE_ERR_LAUNCH;
     GemmParams q = p;
-    q.mode = kModeDown; q.K = f; q.kblocks = f / kKB; q.mtiles = d / kBM; q.a_sf_off = SL.dn_s; q.b_sf = b.hsf;
-    return launch_gemm_nt<kModeDown>(kPrefillNT, mA2, mB2, q, num_sms, st);
+    q.mode = kModeDown; q.K = f; q.kblocks = f / kKB; q.mtiles = d / kBM;
+    q.a_code_off = SL.dn_q; q.a_sf_off = SL.dn_s;
+    q.b_q = b.hq; q.b_sf = b.hsf;
+    return launch_gemm_nt<kModeDown>(kPrefillNT, q, num_sms, st);
 }
 
 }  // namespace fp4moe

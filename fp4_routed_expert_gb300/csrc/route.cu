@@ -60,19 +60,27 @@ __device__ float exact_dot_bf16_warp(const uint16_t* __restrict__ x, const uint1
     long long acc[kLimbs];
 #pragma unroll
     for (int i = 0; i < kLimbs; ++i) acc[i] = 0;
-    for (int kk = lane; kk < d; kk += 32) {
-        uint32_t bx = x[kk], bw = w[kk];
-        uint32_t ex = (bx >> 7) & 0xFFu, ew = (bw >> 7) & 0xFFu;
-        uint32_t mx = (bx & 0x7Fu) | (ex ? 0x80u : 0u);
-        uint32_t mw = (bw & 0x7Fu) | (ew ? 0x80u : 0u);
-        uint32_t P = mx * mw;
-        if (P == 0) continue;
-        int pos = (int)(ex ? ex : 1u) + (int)(ew ? ew : 1u) - 268 + kUnit;   // (e-134) twice
-        uint64_t v = (uint64_t)P << (pos & 31);
-        long long lo = (long long)(v & 0xFFFFFFFFull), hi = (long long)(v >> 32);
-        if ((bx ^ bw) & 0x8000u) { lo = -lo; hi = -hi; }
-        acc[pos >> 5] += lo;
-        acc[(pos >> 5) + 1] += hi;
+    // lane reads 8 consecutive bf16 of each vector per step (d is a multiple of 256)
+    for (int base = lane * 8; base < d; base += 256) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(x + base);
+        const uint4 wv = *reinterpret_cast<const uint4*>(w + base);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+            const uint32_t bx = (xw[h >> 1] >> (16 * (h & 1))) & 0xFFFFu;
+            const uint32_t bw = (ww[h >> 1] >> (16 * (h & 1))) & 0xFFFFu;
+            const uint32_t ex = (bx >> 7) & 0xFFu, ew = (bw >> 7) & 0xFFu;
+            const uint32_t mx = (bx & 0x7Fu) | (ex ? 0x80u : 0u);
+            const uint32_t mw = (bw & 0x7Fu) | (ew ? 0x80u : 0u);
+            const uint32_t P = mx * mw;
+            if (P == 0) continue;
+            const int pos = (int)(ex ? ex : 1u) + (int)(ew ? ew : 1u) - 268 + kUnit;   // (e-134) twice
+            const uint64_t v = (uint64_t)P << (pos & 31);
+            long long lo = (long long)(v & 0xFFFFFFFFull), hi = (long long)(v >> 32);
+            if ((bx ^ bw) & 0x8000u) { lo = -lo; hi = -hi; }
+            acc[pos >> 5] += lo;
+            acc[(pos >> 5) + 1] += hi;
+        }
     }
 #pragma unroll
     for (int i = 0; i < kLimbs; ++i) acc[i] = warp_sum(acc[i]);
@@ -389,11 +397,11 @@ __global__ void __launch_bounds__(128) route_small_kernel(RouteArgs a) {
 // 64 tokens x 64 experts per block, 4x4 per thread, K staged 32 at a time.  Each output is
 // accumulated in chunks of 256 products (fresh partial sums) added into a running total, so
 // every rounding path has at most 256 + ceil(d/256) roundings.
-constexpr int kTileT = 64, kTileE = 64, kTileK = 32, kChunkK = 256;
+constexpr int kTileT = 64, kTileE = 64, kRouteTileK = 32, kChunkK = 256;
 
 __global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
-    __shared__ float xs[kTileK][kTileT + 4];
-    __shared__ float ws[kTileK][kTileE + 4];
+    __shared__ float xs[kRouteTileK][kTileT + 4];
+    __shared__ float ws[kRouteTileK][kTileE + 4];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int t0 = blockIdx.y * kTileT, e0 = blockIdx.x * kTileE;
     float tot[4][4], part[4][4];
@@ -401,7 +409,7 @@ __global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) tot[i][j] = part[i][j] = 0.f;
-    for (int k0 = 0; k0 < a.d; k0 += kTileK) {
+    for (int k0 = 0; k0 < a.d; k0 += kRouteTileK) {
         // 64 rows x 32 bf16 = 256 vectors of 8 per operand
         {
             int r = tid >> 2, c = (tid & 3) * 8;
@@ -420,7 +428,7 @@ __global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
         }
         __syncthreads();
 #pragma unroll 8
-        for (int kk = 0; kk < kTileK; ++kk) {
+        for (int kk = 0; kk < kRouteTileK; ++kk) {
             float4 xa = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
             float4 wb = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
             float xv[4] = {xa.x, xa.y, xa.z, xa.w}, wv[4] = {wb.x, wb.y, wb.z, wb.w};
@@ -430,7 +438,7 @@ __global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
                 for (int j = 0; j < 4; ++j) part[i][j] = fmaf(xv[i], wv[j], part[i][j]);
         }
         __syncthreads();
-        if (((k0 + kTileK) % kChunkK) == 0 || k0 + kTileK >= a.d) {
+        if (((k0 + kRouteTileK) % kChunkK) == 0 || k0 + kRouteTileK >= a.d) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll

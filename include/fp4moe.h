@@ -40,8 +40,8 @@
 extern "C" {
 #endif
 
-/* Per-layer shape.  d (hidden) and f (expert intermediate) must be multiples of 128;
- * 1 <= top_k <= num_experts <= 1024. */
+/* Per-layer shape.  d (hidden) and f (expert intermediate) must be multiples of 256;
+ * 1 <= top_k <= num_experts <= 1024; top_k <= 32. */
 typedef struct {
     int32_t d;
     int32_t f;
@@ -61,7 +61,7 @@ typedef struct {
 enum {
     MOE_OK = 0,
     MOE_ERR_NULL = -1,       /* a required pointer is NULL */
-    MOE_ERR_DIMS = -2,       /* unsupported d, f, num_experts or top_k */
+    MOE_ERR_DIMS = -2,       /* unsupported d, f, num_experts or top_k (see moe_dims) */
     MOE_ERR_TOKENS = -3,     /* T < 0 or T beyond what the workspace was sized for */
     MOE_ERR_WORKSPACE = -4,  /* ws_bytes smaller than moe_workspace_bytes(dims, T) */
     MOE_ERR_ARENA = -5,      /* arena base misaligned, slot_bytes mismatch or slot index out of range */

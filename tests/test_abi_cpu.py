@@ -29,6 +29,7 @@ def test_slot_bytes_and_workspace():
     assert moe.moe_slot_bytes((5120, 2304, 384, 6)) == 18_800_640
     assert moe.moe_slot_bytes((512, 256, 16, 2)) == 208_896
     assert moe.moe_slot_bytes((500, 256, 16, 2)) == -1
+    assert moe.moe_slot_bytes((384, 256, 16, 2)) == -1      # d, f must be multiples of 256
     assert moe.moe_workspace_bytes((5120, 2304, 384, 6), 1) > 0
     assert moe.moe_workspace_bytes((5120, 2304, 384, 6), 4096) > moe.moe_workspace_bytes((5120, 2304, 384, 6), 16)
     assert moe.moe_workspace_bytes((5120, 2304, 2000, 6), 1) == 0

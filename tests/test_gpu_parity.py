@@ -122,7 +122,7 @@ def test_prefill_fused_combine_matches_unfused(tiny, cuda_cores):
 
 def test_router_ties_mask_bias_and_few_resident():
     d, E, k = 256, 40, 4
-    wl = make_workload(d, 128, E, k, seed=5, scale=(-8, -4))
+    wl = make_workload(d, 256, E, k, seed=5, scale=(-8, -4))
     wr = wl.wr.copy()
     wr[7] = wr[3]          # exact ties between experts 3, 7 and 21
     wr[21] = wr[3]
@@ -155,7 +155,7 @@ def test_router_ties_mask_bias_and_few_resident():
 def test_router_large_batch_bit_exact_ids():
     """Tiled router path (T > 16) with a skewing bias: every token's ids and slots."""
     d, E, k, T = 1024, 96, 6, 300
-    wl = make_workload(d, 128, E, k, seed=2, table="permuted", scale=(-10, -6))
+    wl = make_workload(d, 256, E, k, seed=2, table="permuted", scale=(-10, -6))
     bias = syn.zipf_score_bias(2, 0, E, 1.2, 0.04)
     x = syn.activations(2, 0, T, d)
     got = run_layer(wl, x, bias=bias)
@@ -167,7 +167,7 @@ def test_router_large_batch_bit_exact_ids():
 
 def test_bad_slot_is_reported_and_skipped():
     d, E, k = 256, 8, 2
-    wl = make_workload(d, 128, E, k, seed=6, num_slots=8)
+    wl = make_workload(d, 256, E, k, seed=6, num_slots=8)
     tab = wl.table.copy()
     tab[:] = 100                # every slot outside the arena
     wl.table = tab
