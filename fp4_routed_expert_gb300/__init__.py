@@ -18,7 +18,7 @@ from . import build as _build
 __all__ = [
     "MoeError", "moe_dims", "moe_arena", "lib", "moe_slot_bytes", "moe_workspace_bytes",
     "moe_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_route_topk_noalloc", "moe_permute",
-    "moe_expert_ffn_fp4", "moe_combine", "moe_status_str", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
+    "moe_expert_ffn_fp4", "moe_combine", "moe_status_str", "moe_kernel_launches", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
     "MOE_STATUS_FEW_RESIDENT", "MOE_STATUS_BAD_SLOT", "MOE_STATUS_TIMEOUT", "DECODE_MAX_T",
 ]
 
@@ -59,6 +59,7 @@ _SIG = {
     "moe_combine": (ctypes.c_int, [_P, _I] + [_P] * 5),
     "moe_route_topk_noalloc": (ctypes.c_int, [_P, _I] + [_P] * 9),
     "moe_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+    "moe_kernel_launches": (ctypes.c_uint64, []),
 }
 
 
@@ -106,6 +107,11 @@ def _dims(d):
 
 def moe_status_str(code: int) -> str:
     return lib().moe_status_str(int(code)).decode()
+
+
+def moe_kernel_launches() -> int:
+    """Kernels the library has enqueued in this process (a graph capture counts once)."""
+    return int(lib().moe_kernel_launches())
 
 
 def moe_slot_bytes(dims) -> int:

@@ -1,11 +1,15 @@
 // abi.cu -- the extern "C" entry points declared in include/fp4moe.h: argument checks on the
 // host, then kernel launches on the caller's stream.  Nothing here allocates, synchronises
 // or reads device memory back.
+#include <atomic>
 #include <cstdio>
 
 #include "moe_internal.cuh"
 
 namespace fp4moe {
+
+static std::atomic<unsigned long long> g_kernel_launches{0};
+void note_launch(int n) { g_kernel_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
 int launch_route(const moe_dims* m, int T, const uint16_t* x, const uint16_t* wr, const float* bias,
                  const int32_t* table, int32_t* ids, float* w, int32_t* slots, int32_t* status,
@@ -127,6 +131,7 @@ int moe_pack_expert(const moe_dims* dims, const uint8_t* gate_q, const uint8_t* 
     pack_scales_kernel<<<sms, 256, 0, st>>>(gate_s, up_s, base + L.gu_s, 2 * f, d);
     pack_codes_kernel<<<2 * sms, 256, 0, st>>>(down_q, nullptr, base + L.dn_q, d, f);
     pack_scales_kernel<<<sms, 256, 0, st>>>(down_s, nullptr, base + L.dn_s, d, f);
+    note_launch(4);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_LAUNCH;
     return MOE_OK;
 }
@@ -203,11 +208,13 @@ int moe_combine(const moe_dims* dims, int32_t T, const float* rows, const int32_
     return launch_combine(dims, T, rows, row_dst, topk_w, y, (cudaStream_t)stream, num_sms_of_current_device());
 }
 
+uint64_t moe_kernel_launches(void) { return fp4moe::g_kernel_launches.load(std::memory_order_relaxed); }
+
 const char* moe_status_str(int code) {
     switch (code) {
         case MOE_OK: return "ok";
         case MOE_ERR_NULL: return "a required pointer is NULL";
-        case MOE_ERR_DIMS: return "unsupported dims (d, f multiples of 128; 1 <= k <= E <= 1024; k <= 32)";
+        case MOE_ERR_DIMS: return "unsupported dims (d, f multiples of 256 up to 65536; 1 <= k <= E <= 1024; k <= 32)";
         case MOE_ERR_TOKENS: return "token count out of range";
         case MOE_ERR_WORKSPACE: return "workspace too small";
         case MOE_ERR_ARENA: return "arena misaligned, wrong slot_bytes or slot out of range";

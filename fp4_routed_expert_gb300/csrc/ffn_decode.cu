@@ -265,6 +265,7 @@ static int launch_gateup(const DecodeArgs& a, size_t smem, int blocks, cudaStrea
         cudaFuncSetAttribute(decode_gateup_kernel<XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MOE_ERR_LAUNCH;
     decode_gateup_kernel<XT><<<blocks, 256, smem, st>>>(a);
+    note_launch(1);
     return MOE_OK;
 }
 
@@ -298,6 +299,7 @@ int launch_decode_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint1
         return MOE_ERR_LAUNCH;
     int rows_per_block = 8 * 4;
     decode_down_kernel<<<(m->d + rows_per_block - 1) / rows_per_block, 256, smem2, st>>>(a);
+    note_launch(1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 

@@ -313,6 +313,7 @@ int launch_permute(const moe_dims* m, int T, const int32_t* ids, int32_t* offset
     }
     permute_kernel<<<1, 1024, 0, st>>>(n, m->num_experts, ids, offsets, row_src, row_dst);
     permute_tail_kernel<<<(n + 255) / 256, 256, 0, st>>>(n, m->num_experts, offsets, row_src);
+    note_launch(2);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
@@ -335,6 +336,7 @@ int launch_prefill_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint
     int blocks = 4 * num_sms;
     grouped_gemm_kernel<false><<<blocks, 256, 0, st>>>(a);
     grouped_gemm_kernel<true><<<blocks, 256, 0, st>>>(a);
+    note_launch(3);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
@@ -345,6 +347,7 @@ int launch_combine(const moe_dims* m, int T, const float* rows, const int32_t* r
     int blocks = (int)((work + 255) / 256);
     if (blocks > 8 * num_sms) blocks = 8 * num_sms;
     combine_kernel<<<blocks, 256, 0, st>>>(T, m->d, m->top_k, rows, row_dst, w, T * m->top_k, y);
+    note_launch(1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 

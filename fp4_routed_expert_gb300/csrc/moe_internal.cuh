@@ -75,7 +75,7 @@ inline bool dims_ok(const moe_dims* m) {
 // Workspace sections, each 256-byte aligned.  The persistent counters come first so that
 // their offset is the same for every token count; the other sections are per call.
 struct WsLayout {
-    size_t logit;       // fp32 [T_max, E]   fast router logits
+    size_t keys;        // float4 [T_max, E] router key records {key, key lo, key hi, score}
     size_t xnorm;       // fp32 [T_max]      ||x_t||_2
     size_t wnorm;       // fp32 [E]          ||W_r[e]||_2
     size_t counter;     // uint32 [64]       completion tickets (zeroed once, self-resetting)
@@ -90,12 +90,15 @@ inline size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 size_t tc_workspace_bytes(const moe_dims* m, int T);   // mxf4_gemm.cu
 
+// Adds n to the count of kernels this library has enqueued (abi.cu).
+void note_launch(int n);
+
 inline WsLayout ws_layout(const moe_dims* m, int T_max) {
     WsLayout w;
     size_t o = 0;
     size_t T = (size_t)(T_max > 0 ? T_max : 1), E = (size_t)m->num_experts, k = (size_t)m->top_k;
     w.counter = o; o = align256(o + 4 * 64);     // first: its offset must not depend on T
-    w.logit = o;   o = align256(o + 4 * T * E);
+    w.keys = o;    o = align256(o + 16 * T * E);
     w.xnorm = o;   o = align256(o + 4 * T);
     w.wnorm = o;   o = align256(o + 4 * E);
     w.active = o;  o = align256(o + 4 * (2 + 2 * E));

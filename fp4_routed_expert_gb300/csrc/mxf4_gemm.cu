@@ -191,14 +191,17 @@ __device__ __forceinline__ int plan_group_of_tile(const int32_t* plan, int E, in
 }
 
 // Activations -> kTerms MXFP4 terms in tile layout, one warp per (tile, row, 32-element
-// block).  Decode (plan == NULL): one tile, row r holds token r (rows >= T are zero).
+// block); also clears `nzero` counters for the GEMMs that follow.  Decode (plan == NULL): one tile, row r holds token r (rows >= T are zero).
 // Prefill: the plan's tiles; row r of tile t of group g holds permuted row
 // offsets[e_g] + NT*(t - tile_start_g) + r, i.e. token row_src[n]/k (rows past the group's
 // end are zero).
 __global__ void quantize_tiles_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row_src,
                                       const int32_t* __restrict__ plan, const int32_t* __restrict__ offsets, int E, int k,
-                                      int T, int d, int NT, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+                                      int T, int d, int NT, uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                      int32_t* __restrict__ zero, int nzero) {
     const int lane = threadIdx.x & 31;
+    // the GEMMs' per-unit arrival counters start at zero
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += gridDim.x * blockDim.x) zero[i] = 0;
     const int nblk = d / 32, KB = d / kKB;
     const int ntiles = plan ? plan[1] : 1;
     const long total = (long)ntiles * NT * nblk;
@@ -263,7 +266,27 @@ struct GemmParams {
     float* rows_out;                 // down: [rows][d]
     int d;
     int32_t* status;
+    float* part;                     // split units: [CTA][2][128][NT] fp32 partial accumulators
+    int32_t* ctr;                    // split units: arrivals per unit (zero at launch)
 };
+
+// Stream-K schedule.  The n_units * kblocks (unit, K block) iterations are cut into gridDim.x
+// contiguous ranges, CTA c taking [it0(c), it0(c+1)) with it0(c) = floor(total c / G); a CTA
+// walks its range as segments (unit, kb0, kb1).  A unit cut between CTAs is finished by the
+// last of its pieces to arrive, which adds the pieces' partial accumulators in CTA order.
+struct Seg {
+    int unit, kb0, kb1;
+};
+__device__ __forceinline__ Seg seg_at(long long it, long long it1, int KB) {
+    Seg s;
+    s.unit = (int)(it / KB);
+    s.kb0 = (int)(it % KB);
+    s.kb1 = (int)min((long long)KB, (long long)s.kb0 + (it1 - it));
+    return s;
+}
+__device__ __forceinline__ long long sk_it0(long long total, int c, int G) { return total * c / G; }
+// CTA whose range holds iteration i
+__device__ __forceinline__ int sk_cta_of(long long total, long long i, int G) { return (int)(((i + 1) * G - 1) / total); }
 
 // Per-NT shape of the pipeline.  B rows per tile = kTerms*NT, split into MMA groups of at
 // most 128 rows (N of one MMA).  ACC independent accumulators (K slices alternate between
@@ -343,9 +366,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
     uint64_t* tfull = bars + 2 * C::kStages;     // [2] accumulator set ready
     uint64_t* tempty = tfull + 2;                // [2] accumulator set drained
     uint64_t* epibar = tempty + 2;               // [2] epilogue warps' h-tile hand-offs
+    uint64_t* fixbar = epibar + 2;               // [2] split-unit arrival hand-offs
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     __shared__ int n_units_sh;
+    __shared__ int fix_last;
     __shared__ int wcount[8];
     __shared__ int uslots[128];
 
@@ -361,6 +386,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
             mbar_init(smem_u32(&tempty[a]), 4);
             mbar_init(smem_u32(&epibar[a]), 4);
         }
+        mbar_init(smem_u32(&fixbar[0]), 4);
+        mbar_init(smem_u32(&fixbar[1]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -402,17 +429,24 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
     const uint32_t tmem = tmem_base_sh;
     const int n_units = n_units_sh;
     volatile int* abortp = &abort_flag;
+    const int KB = p.kblocks;
+    const long long total = (long long)n_units * KB;
+    const int G = (int)min((long long)gridDim.x, total);   // ranges; none is empty
+    const long long it0 = (int)blockIdx.x < G ? sk_it0(total, blockIdx.x, G) : 0;
+    const long long it1 = (int)blockIdx.x < G ? sk_it0(total, blockIdx.x + 1, G) : 0;
 
     if (warp == 0) {
         // ---------------- producer: four contiguous bulk copies per stage
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_parity = 0;   // per-stage bit masks
-            for (int unit = blockIdx.x; unit < n_units && !*abortp; unit += gridDim.x) {
+            for (long long it = it0; it < it1 && !*abortp;) {
+                const Seg sg = seg_at(it, it1, KB);
+                it += sg.kb1 - sg.kb0;
                 UnitInfo u;
-                const bool ok = unit_info<NT>(p, unit, uslots, u);
+                const bool ok = unit_info<NT>(p, sg.unit, uslots, u);
                 const uint8_t* sbase = p.arena + (int64_t)(ok ? u.slot : 0) * p.slot_bytes;
-                for (int kb = 0; kb < p.kblocks; ++kb) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abortp)) {
                         atomicOr(p.status, MOE_STATUS_TIMEOUT);
                         *abortp = 1;
@@ -446,7 +480,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
             int stage = 0, sfring = 0, acc = 0;
             uint32_t phase = 0, aphase = 0;
             const uint32_t idesc_lo = idesc_mxf4(C::kN, 0), idesc_hi = idesc_mxf4(C::kN, 2);
-            for (int unit = blockIdx.x; unit < n_units && !*abortp; unit += gridDim.x) {
+            for (long long it = it0; it < it1 && !*abortp;) {
+                const Seg sg = seg_at(it, it1, KB);
+                it += sg.kb1 - sg.kb0;
                 if (!mbar_wait(smem_u32(&tempty[acc]), aphase ^ 1u, abortp)) {
                     atomicOr(p.status, MOE_STATUS_TIMEOUT);
                     *abortp = 1;
@@ -455,7 +491,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
                 tc_fence_after();
                 const uint32_t dset = tmem + acc * C::kAcc * C::kRows;
                 bool failed = false;
-                for (int kb = 0; kb < p.kblocks; ++kb) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abortp)) {
                         atomicOr(p.status, MOE_STATUS_TIMEOUT);
                         *abortp = 1;
@@ -478,7 +514,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
                     for (int j = 0; j < 4; ++j) {
                         const int a = j % C::kAcc;
                         const uint64_t ad = desc_sw128(sa + 32 * j);
-                        const uint32_t accumulate = (kb > 0 || j >= C::kAcc) ? 1u : 0u;
+                        const uint32_t accumulate = (kb > sg.kb0 || j >= C::kAcc) ? 1u : 0u;
 #pragma unroll
                         for (int g = 0; g < C::kGroups; ++g) {
                             const uint64_t bd = desc_sw128(sb + g * 128 * kKBytes + 32 * j);
@@ -500,11 +536,14 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
         const int q = warp & 3;
         const int ew = warp - 2;
         int acc = 0;
-        uint32_t aphase = 0, ephase = 0;
+        uint32_t aphase = 0, ephase = 0, fphase = 0;
         const int KBf = p.f / kKB;
-        for (int unit = blockIdx.x; unit < n_units && !*abortp; unit += gridDim.x) {
+        for (long long it = it0; it < it1 && !*abortp;) {
+            const long long seg_first = it;
+            const Seg sg = seg_at(it, it1, KB);
+            it += sg.kb1 - sg.kb0;
             UnitInfo u;
-            const bool ok = unit_info<NT>(p, unit, uslots, u);
+            const bool ok = unit_info<NT>(p, sg.unit, uslots, u);
             if (!mbar_wait(smem_u32(&tfull[acc]), aphase, abortp)) {
                 if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
                 break;
@@ -522,6 +561,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
                 for (int t = 0; t < kTerms; ++t)
 #pragma unroll
                     for (int c0 = 0; c0 < NT; c0 += 16) {
+                        if (c0 >= u.ncols) break;        // warp-uniform: columns past ncols are padding
                         float tmp[16];
                         tc_ld16(lanebase + a * C::kRows + t * NT + c0, tmp);
 #pragma unroll
@@ -532,6 +572,52 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
             if (++acc == C::kDbuf) { acc = 0; aphase ^= 1u; }
             if (!ok) continue;
+            if (sg.kb0 != 0 || sg.kb1 != KB) {
+                // a piece of a split unit: publish the partial accumulator, count the arrival;
+                // the last piece to arrive sums every piece's partial in CTA order
+                const int slot = (seg_first == it0) ? 0 : 1;
+                float* mine = p.part + ((size_t)blockIdx.x * 2 + slot) * (kBM * NT);
+#pragma unroll
+                for (int c = 0; c < NT; ++c)
+                    if (c < u.ncols) mine[c * kBM + row] = vals[c];
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&fixbar[0]));
+                const long long u_first = (long long)sg.unit * KB;
+                const int c_first = sk_cta_of(total, u_first, G), c_last = sk_cta_of(total, u_first + KB - 1, G);
+                if (ew == 0) {
+                    const bool okw = mbar_wait(smem_u32(&fixbar[0]), fphase, abortp);
+                    if (lane == 0) {
+                        int last = 0;
+                        if (okw) {
+                            __threadfence();
+                            last = (atomicAdd(p.ctr + sg.unit, 1) == c_last - c_first);
+                            __threadfence();
+                        } else {
+                            atomicOr(p.status, MOE_STATUS_TIMEOUT);
+                            *abortp = 1;
+                        }
+                        fix_last = last;
+                        mbar_arrive(smem_u32(&fixbar[1]));
+                    }
+                    __syncwarp();
+                }
+                if (!mbar_wait(smem_u32(&fixbar[1]), fphase, abortp)) {
+                    if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
+                    break;
+                }
+                fphase ^= 1u;
+                if (!fix_last) continue;
+#pragma unroll
+                for (int c = 0; c < NT; ++c) vals[c] = 0.f;
+                for (int pc = c_first; pc <= c_last; ++pc) {
+                    const int ps = (sk_it0(total, pc, G) >= u_first) ? 0 : 1;   // the unit is pc's first segment
+                    const float* pp = p.part + ((size_t)pc * 2 + ps) * (kBM * NT);
+#pragma unroll
+                    for (int c = 0; c < NT; ++c)
+                        if (c < u.ncols) vals[c] += __ldcg(pp + c * kBM + row);
+                }
+            }
             if (MODE == kModeDown) {
                 const int r = u.m * kBM + row;    // output feature
 #pragma unroll
@@ -543,6 +629,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
                 // rows 2i' = gate, 2i'+1 = up of output i' = row/2 within the tile (i = 64m + i')
 #pragma unroll
                 for (int c = 0; c < NT; ++c) {
+                    if (c >= u.ncols) break;
                     const float partner = __shfl_xor_sync(0xffffffffu, vals[c], 1);
                     if ((lane & 1) == 0) {
                         const float g = vals[c];
@@ -557,7 +644,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
                     break;
                 }
                 // quantise, one warp per job = (column c, block b of 32 outputs i0 = 64m + 32b)
-                for (int job = ew; job < NT * 2; job += 4) {
+                for (int job = ew; job < u.ncols * 2; job += 4) {
                     const int c = job >> 1, b = job & 1;
                     uint4 codes[kTerms];
                     uint32_t scales[kTerms];
@@ -630,6 +717,7 @@ static int launch_gemm(const GemmParams& p, int grid, cudaStream_t st) {
         cudaSuccess)
         return MOE_ERR_LAUNCH;
     mxf4_gemm_kernel<NT, MODE><<<grid, kThreadsGemm, C::kBytes, st>>>(p);
+    note_launch(1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
@@ -663,8 +751,19 @@ static size_t act_sf_blocks(const moe_dims* m, int T) {      // 1 KB scale block
     return b > dec ? b : dec;
 }
 
+constexpr int kMaxGemmCtas = 256;
+
+// Units of either GEMM for T tokens: weight tiles (2f/128 or d/128) x activation tiles.
+static size_t max_units(const moe_dims* m, int T) {
+    const size_t mt = (size_t)(2 * m->f > m->d ? 2 * m->f : m->d) / kBM;
+    return (act_tiles(m, T) > (size_t)kMaxNT ? act_tiles(m, T) : (size_t)kMaxNT) * mt;
+}
+
 struct TcBuffers {
     uint8_t *xq, *xsf, *hq, *hsf;
+    float* part;           // [kMaxGemmCtas][2][128][kMaxNT]
+    int32_t* ctr;          // [2][max_units]: gate/up, down
+    size_t nctr;           // max_units
     float* rows;
     int32_t* plan;
 };
@@ -677,6 +776,9 @@ static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& 
     b.xsf = reinterpret_cast<uint8_t*>(o); o += align256(sfb * (m->d / kKB) * 1024);
     b.hq = reinterpret_cast<uint8_t*>(o);  o += align256(rows * kTerms * m->f / 2);
     b.hsf = reinterpret_cast<uint8_t*>(o); o += align256(sfb * (m->f / kKB) * 1024);
+    b.part = reinterpret_cast<float*>(o);  o += align256((size_t)kMaxGemmCtas * 2 * kBM * kMaxNT * 4);
+    b.nctr = max_units(m, T);
+    b.ctr = reinterpret_cast<int32_t*>(o); o += align256(2 * b.nctr * 4);
     b.rows = reinterpret_cast<float*>(o);
     b.plan = reinterpret_cast<int32_t*>(ws + L.active);
     return b;
@@ -686,7 +788,8 @@ size_t tc_workspace_bytes(const moe_dims* m, int T) {
     const size_t R = (size_t)(T > 0 ? T : 1) * m->top_k;
     const size_t rows = act_rows(m, T), sfb = act_sf_blocks(m, T);
     return align256(rows * kTerms * m->d / 2) + align256(sfb * (m->d / kKB) * 1024) + align256(rows * kTerms * m->f / 2) +
-           align256(sfb * (m->f / kKB) * 1024) + align256(R * m->d * 4);
+           align256(sfb * (m->f / kKB) * 1024) + align256((size_t)kMaxGemmCtas * 2 * kBM * kMaxNT * 4) +
+           align256(2 * max_units(m, T) * 4) + align256(R * m->d * 4);
 }
 
 static int nt_for(int cols) { return cols <= 16 ? 16 : cols <= 32 ? 32 : 64; }
@@ -702,6 +805,12 @@ static GemmParams base_params(const moe_dims* m, const moe_arena* ar, int T, con
     return p;
 }
 
+static GemmParams with_split(GemmParams p, const TcBuffers& b, int which) {
+    p.part = b.part;
+    p.ctr = b.ctr + (size_t)which * b.nctr;
+    return p;
+}
+
 // Decode regime: quantise x into one tile, gate/up GEMM (SwiGLU, h quantised per (token, j)
 // pair into one tile), down GEMM (one fp32 row per pair), fixed-order combine into y.
 int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
@@ -714,7 +823,8 @@ int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16
     const int nt1 = nt_for(T), nt2 = nt_for(R);
     const int qwarps = nt1 * (d / 32);
     quantize_tiles_kernel<<<(qwarps + 7) / 8, 256, 0, st>>>(x, nullptr, nullptr, nullptr, m->num_experts, k, T, d, nt1,
-                                                          b.xq, b.xsf);
+                                                          b.xq, b.xsf, b.ctr, (int)(2 * b.nctr));
+    note_launch(1);
     GemmParams p = base_params(m, ar, T, slot, status);
     p.mode = kModeGateUp; p.regime = kRegimeDecode;
     p.K = d; p.kblocks = d / kKB; p.mtiles = 2 * f / kBM;
@@ -722,16 +832,18 @@ int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16
     p.a_code_off = SL.gu_q; p.a_sf_off = SL.gu_s;
     p.b_q = b.xq; p.b_sf = b.xsf;
     p.hq = b.hq; p.hsf = b.hsf; p.h_nt = nt2;
-    int rc = launch_gemm_nt<kModeGateUp>(nt1, p, num_sms, st);
+    const int grid = num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas;
+    int rc = launch_gemm_nt<kModeGateUp>(nt1, with_split(p, b, 0), grid, st);
     if (rc) return rc;
     GemmParams q = p;
     q.mode = kModeDown; q.K = f; q.kblocks = f / kKB; q.mtiles = d / kBM;
     q.decode_cols = R;
     q.a_code_off = SL.dn_q; q.a_sf_off = SL.dn_s;
     q.b_q = b.hq; q.b_sf = b.hsf; q.rows_out = b.rows;
-    rc = launch_gemm_nt<kModeDown>(nt2, q, num_sms, st);
+    rc = launch_gemm_nt<kModeDown>(nt2, with_split(q, b, 1), grid, st);
     if (rc) return rc;
     decode_combine_kernel<<<(T * (d / 4) + 255) / 256, 256, 0, st>>>(T, d, k, ar->num_slots, b.rows, slot, w, y);
+    note_launch(1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
@@ -751,7 +863,8 @@ int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint1
     const long qwarps = (long)act_tiles(m, T) * kPrefillNT * (d / 32);
     const long qblocks = (qwarps + 7) / 8;
     quantize_tiles_kernel<<<(int)(qblocks > 16L * num_sms ? 16L * num_sms : qblocks), 256, 0, st>>>(
-        x, row_src, b.plan, offsets, m->num_experts, k, T, d, kPrefillNT, b.xq, b.xsf);
+        x, row_src, b.plan, offsets, m->num_experts, k, T, d, kPrefillNT, b.xq, b.xsf, b.ctr, (int)(2 * b.nctr));
+    note_launch(2);
     GemmParams p = base_params(m, ar, T, slot, status);
     p.mode = kModeGateUp; p.regime = kRegimePrefill;
     p.K = d; p.kblocks = d / kKB; p.mtiles = 2 * f / kBM;
@@ -760,13 +873,14 @@ int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint1
     p.b_q = b.xq; p.b_sf = b.xsf;
     p.hq = b.hq; p.hsf = b.hsf; p.h_nt = kPrefillNT;
     p.rows_out = rows_out;
-    int rc = launch_gemm_nt<kModeGateUp>(kPrefillNT, p, num_sms, st);
+    const int grid = num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas;
+    int rc = launch_gemm_nt<kModeGateUp>(kPrefillNT, with_split(p, b, 0), grid, st);
     if (rc) return rc;
     GemmParams q = p;
     q.mode = kModeDown; q.K = f; q.kblocks = f / kKB; q.mtiles = d / kBM;
     q.a_code_off = SL.dn_q; q.a_sf_off = SL.dn_s;
     q.b_q = b.hq; q.b_sf = b.hsf;
-    return launch_gemm_nt<kModeDown>(kPrefillNT, q, num_sms, st);
+    return launch_gemm_nt<kModeDown>(kPrefillNT, with_split(q, b, 1), grid, st);
 }
 
 }  // namespace fp4moe

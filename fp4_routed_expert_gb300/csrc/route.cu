@@ -10,16 +10,25 @@
 // independent of summation order.
 //
 // How the device reaches the exact set without computing every exact logit:
-//  1. fast logit lf: fp32 FMA chains with at most L roundings on any path, so
-//       |lf - exact| <= gamma_L * sum|x_k w_k| <= gamma_L * ||x|| ||w||   (Cauchy-Schwarz),
-//     gamma_L = L u / (1 - L u), u = 2^-24, inflated by 2^-10 for the norms' own rounding;
-//  2. the logit interval maps through the monotone sigmoid (fp32 sigmoid with a 2^-20
-//     absolute margin that covers its error and the final fp32 rounding) and the bias add
-//     (directed rounding) into a key interval [klo, khi] that contains the exact key;
+//  1. a fast logit D with an error bound delta, |D - exact| <= delta:
+//     decode (T <= 16): each lane sums its bf16 products (exact in fp32) with TwoSum
+//       compensation (Ogita, Rump, Oishi, "Accurate sum and dot product", SIAM J. Sci.
+//       Comput. 26(6), 2005, Sum2), the lanes' (sum, compensation) pairs are added in fp64:
+//       delta = (gamma_(c-1) + gamma_m^2 + 2^-49) * sum|x_k w_k| + d 2^-147, with c products
+//       per plain FMA chunk and m chunks per lane (a few 1e-9 at d = 5120);
+//     prefill: fp32 FMA chains with at most L roundings on any path,
+//       delta = gamma_L * ||x|| ||w|| (Cauchy-Schwarz), inflated by 2^-10 for the norms;
+//  2. [D - delta, D + delta] rounded outward to fp32 holds l32; through the monotone
+//     sigmoid (fp32 with a 2^-21 absolute margin that covers its error, at most 3 ulp, and
+//     the final fp32 rounding) and the bias add (directed rounding) it gives a key interval [klo, khi];
 //  3. S = top-k by the point estimate; an expert of S whose klo exceeds every outside khi is
 //     certainly chosen, an outside expert whose khi is below every klo of S certainly not;
 //  4. the rest are recomputed exactly (integer Kulisch accumulation of the bf16 products,
-//     one rounding to fp32, double sigmoid) and ranked by exact key.
+//     one rounding to fp32, double sigmoid) and ranked by exact key;
+//  5. a chosen expert whose key interval is wider than 1e-5 of its score also gets its
+//     exact score, so every weight is within 2e-5 (relative) of the exact one.
+// Each (token, expert) gets one 16-byte key record {point key, klo, khi, score}; score < 0
+// marks an expert that is not resident.
 #include "moe_internal.cuh"
 
 namespace fp4moe {
@@ -34,11 +43,12 @@ struct RouteArgs {
     float* w;
     int32_t* slots;
     int32_t* status;
-    float* logit;      // [T, E]
-    float* xnorm;      // [T]
-    float* wnorm;      // [E]
+    float4* keys;      // [T, E] key records
+    float* xnorm;      // [T]   (prefill bound)
+    float* wnorm;      // [E]   (prefill bound)
     unsigned* counter;
-    float bound_coef;  // gamma_L * (1 + 2^-10)
+    float bound_coef;  // prefill: gamma_L * (1 + 2^-10)
+    double g1, g2;     // decode: gamma_(c-1) and gamma_m^2 (fp32 unit roundoff)
 };
 
 // ------------------------------------------------------------------ exact logit (Kulisch)
@@ -55,7 +65,7 @@ __device__ __forceinline__ uint32_t limb_window(const uint32_t* dig, int bit) {
 }
 
 // Exact x.w rounded once to fp32, computed by the whole warp (every lane returns it).
-__device__ float exact_dot_bf16_warp(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w,
+__device__ __noinline__ float exact_dot_bf16_warp(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w,
                                      int d, int lane) {
     long long acc[kLimbs];
 #pragma unroll
@@ -131,12 +141,18 @@ __device__ __forceinline__ float sigmoid_exact32(float l32) {
     return __double2float_rn(1.0 / (1.0 + exp(-(double)l32)));
 }
 
-// ------------------------------------------------------------------ certified selection
+// Key record of expert e from a point logit and an fp32 interval [lo, hi] holding l32.
+__device__ __forceinline__ float4 make_key(const RouteArgs& a, int e, float lf, float lo, float hi) {
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    if (a.table[e] < 0) return make_float4(NEG_INF, NEG_INF, NEG_INF, -1.0f);
+    const float b = a.bias ? a.bias[e] : 0.0f;
+    const float margin = 1.0f / 2097152.0f;   // 2^-21
+    const float sv = sigmoid_fast(lf);
+    return make_float4(sv + b, __fadd_rd(__fsub_rd(sigmoid_fast(lo), margin), b),
+                       __fadd_ru(__fadd_ru(sigmoid_fast(hi), margin), b), sv);
+}
 
-struct Cand {
-    float key;
-    int e;
-};
+// ------------------------------------------------------------------ certified selection
 
 // (key desc, id asc): is a better than b?
 __device__ __forceinline__ bool better(float ka, int ea, float kb, int eb) {
@@ -154,33 +170,25 @@ __device__ __forceinline__ void warp_best(float& k, int& e) {
     }
 }
 
-// One warp selects the experts of token t.  EPL = experts per lane (E <= 32 * EPL).
+// One warp selects the experts of token t from its key records.  EPL = experts per lane
+// (E <= 32 * EPL); expert e = lane + 32 m.
 template <int EPL>
 __device__ void select_token(const RouteArgs& a, int t, int lane) {
     const float NEG_INF = -__int_as_float(0x7f800000);
-    const float* lrow = a.logit + (size_t)t * a.E;
-    const float xn = __ldcg(a.xnorm + t);
-    float kf[EPL], klo[EPL], khi[EPL], sv[EPL], exk[EPL];
-    uint32_t valid = 0, picked = 0, exact_done = 0;
+    const float4* krow = a.keys + (size_t)t * a.E;
+    float4 kr[EPL];
 #pragma unroll
     for (int m = 0; m < EPL; ++m) {
-        int e = lane + 32 * m;
-        kf[m] = klo[m] = khi[m] = NEG_INF;
-        sv[m] = 0.f;
+        const int e = lane + 32 * m;
+        kr[m] = (e < a.E) ? __ldcg(krow + e) : make_float4(NEG_INF, NEG_INF, NEG_INF, -1.0f);
+    }
+    float sv[EPL], exk[EPL];
+    uint32_t valid = 0, picked = 0;
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+        sv[m] = kr[m].w;
         exk[m] = NEG_INF;
-        if (e < a.E && a.table[e] >= 0) {
-            valid |= 1u << m;
-            float l = __ldcg(lrow + e);
-            float delta = fmaf(a.bound_coef * xn, __ldcg(a.wnorm + e), 7.5e-37f);
-            delta = __fmul_ru(delta, 1.0f + 1.0f / 1048576.0f);
-            float lo = __fsub_rd(l, delta), hi = __fadd_ru(l, delta);
-            float b = a.bias ? a.bias[e] : 0.0f;
-            sv[m] = sigmoid_fast(l);
-            kf[m] = sv[m] + b;
-            const float margin = 1.0f / 1048576.0f;   // 2^-20
-            klo[m] = __fadd_rd(__fsub_rd(sigmoid_fast(lo), margin), b);
-            khi[m] = __fadd_ru(__fadd_ru(sigmoid_fast(hi), margin), b);
-        }
+        if (kr[m].w >= 0.0f) valid |= 1u << m;
     }
     // S = top-k by point estimate
     int nsel = 0;
@@ -190,7 +198,7 @@ __device__ void select_token(const RouteArgs& a, int t, int lane) {
 #pragma unroll
         for (int m = 0; m < EPL; ++m)
             if (((valid & ~picked) >> m) & 1u)
-                if (better(kf[m], lane + 32 * m, bk, be)) { bk = kf[m]; be = lane + 32 * m; }
+                if (better(kr[m].x, lane + 32 * m, bk, be)) { bk = kr[m].x; be = lane + 32 * m; }
         warp_best(bk, be);
         if (be < 0) break;
         if ((be & 31) == lane) picked |= 1u << (be >> 5);
@@ -201,8 +209,8 @@ __device__ void select_token(const RouteArgs& a, int t, int lane) {
     float min_lo_in = __int_as_float(0x7f800000), max_hi_out = NEG_INF;
 #pragma unroll
     for (int m = 0; m < EPL; ++m) {
-        if ((picked >> m) & 1u) min_lo_in = fminf(min_lo_in, klo[m]);
-        else if ((valid >> m) & 1u) max_hi_out = fmaxf(max_hi_out, khi[m]);
+        if ((picked >> m) & 1u) min_lo_in = fminf(min_lo_in, kr[m].y);
+        else if ((valid >> m) & 1u) max_hi_out = fmaxf(max_hi_out, kr[m].z);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -213,34 +221,32 @@ __device__ void select_token(const RouteArgs& a, int t, int lane) {
 #pragma unroll
     for (int m = 0; m < EPL; ++m) {
         bool p = (picked >> m) & 1u, v = (valid >> m) & 1u;
-        if (p && klo[m] > max_hi_out) certain |= 1u << m;
-        else if (p || (v && khi[m] >= min_lo_in)) uncertain |= 1u << m;
+        if (p && kr[m].y > max_hi_out) certain |= 1u << m;
+        else if (p || (v && kr[m].z >= min_lo_in)) uncertain |= 1u << m;
     }
-    uint32_t final_mask = certain;
-    int n_unc = __popc(uncertain);
-    n_unc = warp_sum(n_unc);
-    if (n_unc > 0) {
-        int n_cert = warp_sum(__popc(certain));
-        int need = nsel - n_cert;
-        // exact keys of every uncertain expert, one expert at a time by the whole warp
-        const uint16_t* xt = a.x + (size_t)t * a.d;
-#pragma unroll 1
+    uint32_t final_mask = certain, exact_done = 0;
+    const uint16_t* xt = a.x + (size_t)t * a.d;
+    // exact scores (and keys) of the experts in `mask`, one expert at a time by the whole warp
+    auto exact_scores = [&](uint32_t mask) {
+#pragma unroll
         for (int m = 0; m < EPL; ++m) {
-            uint32_t bal = __ballot_sync(0xffffffffu, (uncertain >> m) & 1u);
+            uint32_t bal = __ballot_sync(0xffffffffu, (mask >> m) & 1u);
             while (bal) {
-                int src = __ffs(bal) - 1;
+                const int src = __ffs(bal) - 1;
                 bal &= bal - 1;
-                int e = src + 32 * m;
-                float l32 = exact_dot_bf16_warp(xt, a.wr + (size_t)e * a.d, a.d, lane);
-                float s32 = sigmoid_exact32(l32);
+                const int e = src + 32 * m;
+                const float s32 = sigmoid_exact32(exact_dot_bf16_warp(xt, a.wr + (size_t)e * a.d, a.d, lane));
                 if (lane == src) {
-                    float b = a.bias ? a.bias[e] : 0.0f;
-                    exk[m] = __fadd_rn(s32, b);
+                    exk[m] = __fadd_rn(s32, a.bias ? a.bias[e] : 0.0f);
                     sv[m] = s32;
-                    exact_done |= 1u << m;
                 }
             }
         }
+        exact_done |= mask;
+    };
+    if (warp_sum(__popc(uncertain)) > 0) {
+        const int need = nsel - warp_sum(__popc(certain));
+        exact_scores(uncertain);
         uint32_t chosen = 0;
         for (int j = 0; j < need; ++j) {
             float bk = NEG_INF;
@@ -255,14 +261,24 @@ __device__ void select_token(const RouteArgs& a, int t, int lane) {
         }
         final_mask |= chosen;
     }
-    (void)exact_done;
+    // weights: a chosen expert whose key interval is wider than 1e-5 of its score gets its
+    // score from the exact logit, so every score has relative error below 1e-5
+    uint32_t wide = 0;
+#pragma unroll
+    for (int m = 0; m < EPL; ++m)
+        if (((final_mask & ~exact_done) >> m) & 1u)
+            if (kr[m].z - kr[m].y > 1e-5f * sv[m]) wide |= 1u << m;
+    if (__any_sync(0xffffffffu, wide != 0)) exact_scores(wide);
     // outputs in ascending expert id: e = lane + 32 m, so m outer, lane inner
+    int32_t slot[EPL];
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) slot[m] = ((final_mask >> m) & 1u) ? a.table[lane + 32 * m] : -1;
     float sum = 0.0f;
 #pragma unroll
     for (int m = 0; m < EPL; ++m) {
         uint32_t bal = __ballot_sync(0xffffffffu, (final_mask >> m) & 1u);
         while (bal) {
-            int src = __ffs(bal) - 1;
+            const int src = __ffs(bal) - 1;
             bal &= bal - 1;
             sum += __shfl_sync(0xffffffffu, sv[m], src);
         }
@@ -273,13 +289,12 @@ __device__ void select_token(const RouteArgs& a, int t, int lane) {
     int32_t* so = a.slots + (size_t)t * a.k;
 #pragma unroll
     for (int m = 0; m < EPL; ++m) {
-        uint32_t bal = __ballot_sync(0xffffffffu, (final_mask >> m) & 1u);
+        const uint32_t bal = __ballot_sync(0xffffffffu, (final_mask >> m) & 1u);
         if ((final_mask >> m) & 1u) {
-            int idx = pos + __popc(bal & ((1u << lane) - 1u));
-            int e = lane + 32 * m;
-            ids[idx] = e;
+            const int idx = pos + __popc(bal & ((1u << lane) - 1u));
+            ids[idx] = lane + 32 * m;
             wo[idx] = (sum > 0.0f) ? __fdiv_rn(sv[m], sum) : 0.0f;
-            so[idx] = a.table[e];
+            so[idx] = slot[m];
         }
         pos += __popc(bal);
     }
@@ -292,7 +307,7 @@ __device__ void select_token(const RouteArgs& a, int t, int lane) {
 
 template <int EPL>
 __device__ void select_tokens_block(const RouteArgs& a, int t0, int tstep) {
-    int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31;
     for (int t = t0; t < a.T; t += tstep) select_token<EPL>(a, t, lane);
 }
 
@@ -308,72 +323,97 @@ __device__ void select_tokens_block(const RouteArgs& a, int t0, int tstep) {
         else { constexpr int EPL = 32; __VA_ARGS__; }                 \
     } while (0)
 
-// ------------------------------------------------------------------ small T: one warp per expert
+// ------------------------------------------------------------------ decode: one warp per expert
 
-// Fast logits for T <= kDecodeMaxT; the last block to finish selects every token.
-// Per lane: ceil(d/256) chunks of 8 bf16, an FMA chain of 8 per chunk, then 5 shuffle adds.
-template <int MAXT>
-__global__ void __launch_bounds__(128) route_small_kernel(RouteArgs a) {
+// TwoSum (Knuth): s + err == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& err) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeVec = 20;              // weight vectors (8 bf16) per lane in flight
+constexpr size_t kDecodeSmemMax = 200 * 1024;
+
+// Key records for T <= TB tokens; x rows staged in shared memory.  Lane l of the warp of
+// expert e owns vectors l, l+32, ...; per token it keeps (s, c) of a compensated sum of
+// plain FMA chunks of CH products, and sum|x w|.  The last block to finish selects.
+template <int TB, int CH>
+__global__ void __launch_bounds__(kDecodeWarps * 32) route_decode_kernel(RouteArgs a) {
     extern __shared__ uint4 smem_u4[];
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem_u4);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-    const int T = a.T, d = a.d, E = a.E;
-    const int nvec = d / 8;   // 16-byte vectors per row
-    for (int i = tid; i < T * nvec; i += blockDim.x)
-        smem_u4[i] = reinterpret_cast<const uint4*>(a.x)[i];
-    __syncthreads();
-    const int gw = blockIdx.x * nwarps + warp, nw = gridDim.x * nwarps;
-    for (int e = gw; e < E; e += nw) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = a.T, d = a.d, E = a.E, nvec = d / 8;
+    const int gw = blockIdx.x * kDecodeWarps + warp, nw = gridDim.x * kDecodeWarps;
+    // the first batch of this warp's weights is in flight while x is staged
+    uint4 wv[kDecodeVec];
+    int e = gw;
+    if (e < E) {
         const uint4* wrow = reinterpret_cast<const uint4*>(a.wr + (size_t)e * d);
-        float acc[MAXT];
 #pragma unroll
-        for (int t = 0; t < MAXT; ++t) acc[t] = 0.f;
-        float wsq = 0.f;
-        constexpr int B = 8;   // vectors in flight per lane
-        for (int c0 = lane; c0 < nvec; c0 += 32 * B) {
-            uint4 wv[B];
+        for (int b = 0; b < kDecodeVec; ++b) {
+            const int c = lane + 32 * b;
+            wv[b] = (c < nvec) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+        }
+    }
+    for (int i = tid; i < T * nvec; i += blockDim.x) smem_u4[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+    __syncthreads();
+    for (; e < E; e += nw) {
+        const uint4* wrow = reinterpret_cast<const uint4*>(a.wr + (size_t)e * d);
+        float s[TB], c[TB], A[TB];
 #pragma unroll
-            for (int b = 0; b < B; ++b) {
-                int c = c0 + 32 * b;
-                wv[b] = (c < nvec) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+        for (int t = 0; t < TB; ++t) s[t] = c[t] = A[t] = 0.f;
+        for (int c0 = 0; c0 < nvec; c0 += 32 * kDecodeVec) {
+            if (c0 > 0) {
+#pragma unroll
+                for (int b = 0; b < kDecodeVec; ++b) {
+                    const int cv = c0 + lane + 32 * b;
+                    wv[b] = (cv < nvec) ? __ldg(wrow + cv) : make_uint4(0, 0, 0, 0);
+                }
             }
 #pragma unroll
-            for (int b = 0; b < B; ++b) {
-                int c = c0 + 32 * b;
-                if (c >= nvec) break;
-                float w8[8] = {bf16_lo(wv[b].x), bf16_hi(wv[b].x), bf16_lo(wv[b].y), bf16_hi(wv[b].y),
-                               bf16_lo(wv[b].z), bf16_hi(wv[b].z), bf16_lo(wv[b].w), bf16_hi(wv[b].w)};
+            for (int b = 0; b < kDecodeVec; ++b) {
+                const int cv = c0 + lane + 32 * b;
+                if (cv >= nvec) break;
+                const float w8[8] = {bf16_lo(wv[b].x), bf16_hi(wv[b].x), bf16_lo(wv[b].y), bf16_hi(wv[b].y),
+                                     bf16_lo(wv[b].z), bf16_hi(wv[b].z), bf16_lo(wv[b].w), bf16_hi(wv[b].w)};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) wsq = fmaf(w8[i], w8[i], wsq);
-#pragma unroll
-                for (int t = 0; t < MAXT; ++t) {
+                for (int t = 0; t < TB; ++t) {
                     if (t >= T) break;
-                    uint4 xv = reinterpret_cast<const uint4*>(xs + (size_t)t * d)[c];
-                    float x8[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
-                                   bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
+                    const uint4 xv = smem_u4[(size_t)t * nvec + cv];
+                    const float x8[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
+                                         bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[t] = fmaf(x8[i], w8[i], acc[t]);
+                    for (int i0 = 0; i0 < 8; i0 += CH) {
+                        float q = __fmul_rn(x8[i0], w8[i0]);
+#pragma unroll
+                        for (int i = i0 + 1; i < i0 + CH; ++i) q = __fmaf_rn(x8[i], w8[i], q);
+                        float err;
+                        two_sum(s[t], q, s[t], err);
+                        c[t] = __fadd_rn(c[t], err);
+#pragma unroll
+                        for (int i = i0; i < i0 + CH; ++i) A[t] = __fmaf_rn(fabsf(x8[i]), fabsf(w8[i]), A[t]);
+                    }
                 }
             }
         }
+        // per token: D = sum over lanes of (s + c) in fp64, Asum = sum|x w|; lane t keeps token t
+        double myD = 0.0, myA = 0.0;
 #pragma unroll
-        for (int t = 0; t < MAXT; ++t) {
+        for (int t = 0; t < TB; ++t) {
             if (t >= T) break;
-            float v = warp_sum(acc[t]);
-            if (lane == 0) a.logit[(size_t)t * E + e] = v;
+            const double D = warp_sum((double)s[t] + (double)c[t]);
+            const double As = warp_sum((double)A[t]);
+            if (lane == t) { myD = D; myA = As; }
         }
-        wsq = warp_sum(wsq);
-        if (lane == 0) a.wnorm[e] = sqrtf(wsq);
-    }
-    if (blockIdx.x == 0) {
-        for (int t = warp; t < T; t += nwarps) {
-            float s = 0.f;
-            for (int i = lane; i < d; i += 32) {
-                float v = bf16_to_f32(xs[(size_t)t * d + i]);
-                s = fmaf(v, v, s);
-            }
-            s = warp_sum(s);
-            if (lane == 0) a.xnorm[t] = sqrtf(s);
+        if (lane < T) {
+            // |D - exact| <= (g1 + g2 + 2^-49) * sum|x w| * (1 + 2^-9) + d * 2^-147
+            const double coef = __dadd_ru(__dadd_ru(a.g1, a.g2), 1.7763568394002505e-15);
+            double delta = __dmul_ru(__dmul_ru(coef, myA), 1.001953125);
+            delta = __dadd_ru(delta, (double)d * 5.605193857299268e-45);
+            const float lo = __double2float_rd(__dsub_rd(myD, delta));
+            const float hi = __double2float_ru(__dadd_ru(myD, delta));
+            a.keys[(size_t)lane * E + e] = make_key(a, e, __double2float_rn(myD), lo, hi);
         }
     }
     // completion ticket: the last block to arrive selects for every token
@@ -381,22 +421,42 @@ __global__ void __launch_bounds__(128) route_small_kernel(RouteArgs a) {
     __syncthreads();
     if (tid == 0) {
         __threadfence();
-        unsigned tk = atomicAdd(a.counter, 1u);
+        const unsigned tk = atomicAdd(a.counter, 1u);
         is_last = (tk == gridDim.x - 1);
     }
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    FP4MOE_EPL_DISPATCH(E, select_tokens_block<EPL>(a, warp, nwarps));
+    FP4MOE_EPL_DISPATCH(E, select_tokens_block<EPL>(a, warp, kDecodeWarps));
     __syncthreads();
     if (tid == 0) atomicExch(a.counter, 0u);
 }
 
 // ------------------------------------------------------------------ large T: tiled logits
 
+// ||x_t|| and ||W_r[e]|| (one warp per row).
+__global__ void route_norms_kernel(RouteArgs a) {
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    const int rows = a.T + a.E;
+    for (int r = gw; r < rows; r += (gridDim.x * blockDim.x) >> 5) {
+        const uint16_t* p = (r < a.T) ? a.x + (size_t)r * a.d : a.wr + (size_t)(r - a.T) * a.d;
+        float s = 0.f;
+        for (int i = lane; i < a.d; i += 32) {
+            const float v = bf16_to_f32(p[i]);
+            s = fmaf(v, v, s);
+        }
+        s = warp_sum(s);
+        if (lane == 0) {
+            if (r < a.T) a.xnorm[r] = sqrtf(s);
+            else a.wnorm[r - a.T] = sqrtf(s);
+        }
+    }
+}
+
 // 64 tokens x 64 experts per block, 4x4 per thread, K staged 32 at a time.  Each output is
 // accumulated in chunks of 256 products (fresh partial sums) added into a running total, so
-// every rounding path has at most 256 + ceil(d/256) roundings.
+// every rounding path has at most 256 + ceil(d/256) roundings.  The epilogue turns each
+// logit into its key record with the Cauchy-Schwarz bound (norms computed beforehand).
 constexpr int kTileT = 64, kTileE = 64, kRouteTileK = 32, kChunkK = 256;
 
 __global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
@@ -412,26 +472,26 @@ __global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
     for (int k0 = 0; k0 < a.d; k0 += kRouteTileK) {
         // 64 rows x 32 bf16 = 256 vectors of 8 per operand
         {
-            int r = tid >> 2, c = (tid & 3) * 8;
+            const int r = tid >> 2, c = (tid & 3) * 8;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (t0 + r < a.T) v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + r) * a.d + k0 + c));
-            float f8[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                           bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+            const float f8[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                                 bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
 #pragma unroll
             for (int i = 0; i < 8; ++i) xs[c + i][r] = f8[i];
             uint4 u = make_uint4(0, 0, 0, 0);
             if (e0 + r < a.E) u = __ldg(reinterpret_cast<const uint4*>(a.wr + (size_t)(e0 + r) * a.d + k0 + c));
-            float g8[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                           bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+            const float g8[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                                 bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
 #pragma unroll
             for (int i = 0; i < 8; ++i) ws[c + i][r] = g8[i];
         }
         __syncthreads();
 #pragma unroll 8
         for (int kk = 0; kk < kRouteTileK; ++kk) {
-            float4 xa = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
-            float4 wb = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
-            float xv[4] = {xa.x, xa.y, xa.z, xa.w}, wv[4] = {wb.x, wb.y, wb.z, wb.w};
+            const float4 xa = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
+            const float4 wb = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+            const float xv[4] = {xa.x, xa.y, xa.z, xa.w}, wv[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -447,84 +507,88 @@ __global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        int t = t0 + ty * 4 + i;
+        const int t = t0 + ty * 4 + i;
         if (t >= a.T) continue;
+        const float xn = __ldg(a.xnorm + t);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            int e = e0 + tx * 4 + j;
-            if (e < a.E) a.logit[(size_t)t * a.E + e] = tot[i][j];
-        }
-    }
-}
-
-// ||x_t|| and ||W_r[e]|| (one warp per row).
-__global__ void route_norms_kernel(RouteArgs a) {
-    int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    int rows = a.T + a.E;
-    for (int r = gw; r < rows; r += (gridDim.x * blockDim.x) >> 5) {
-        const uint16_t* p = (r < a.T) ? a.x + (size_t)r * a.d : a.wr + (size_t)(r - a.T) * a.d;
-        float s = 0.f;
-        for (int i = lane; i < a.d; i += 32) {
-            float v = bf16_to_f32(p[i]);
-            s = fmaf(v, v, s);
-        }
-        s = warp_sum(s);
-        if (lane == 0) {
-            if (r < a.T) a.xnorm[r] = sqrtf(s);
-            else a.wnorm[r - a.T] = sqrtf(s);
+            const int e = e0 + tx * 4 + j;
+            if (e >= a.E) continue;
+            const float l = tot[i][j];
+            float delta = fmaf(a.bound_coef * xn, __ldg(a.wnorm + e), 7.5e-37f);
+            delta = __fmul_ru(delta, 1.0f + 1.0f / 1048576.0f);
+            a.keys[(size_t)t * a.E + e] = make_key(a, e, l, __fsub_rd(l, delta), __fadd_ru(l, delta));
         }
     }
 }
 
 template <int EPL>
 __global__ void __launch_bounds__(128) route_select_kernel(RouteArgs a) {
-    int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
+    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
     select_tokens_block<EPL>(a, gw, nw);
 }
 
 // ------------------------------------------------------------------ host side
 
-static float gamma_coef(int L) {
-    double u = 1.0 / 16777216.0;
-    double g = L * u / (1.0 - L * u);
-    return (float)(g * (1.0 + 1.0 / 1024.0));
+// gamma_n = n u / (1 - n u), u = 2^-24
+static double gamma32(int n) {
+    const double u = 1.0 / 16777216.0;
+    return n * u / (1.0 - n * u);
+}
+
+static float gamma_coef(int L) { return (float)(gamma32(L) * (1.0 + 1.0 / 1024.0)); }
+
+template <int TB, int CH>
+static int launch_decode_tb(RouteArgs a, cudaStream_t st) {
+    const size_t smem = (size_t)a.T * a.d * 2;
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(route_decode_kernel<TB, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+        return MOE_ERR_LAUNCH;
+    const int m = a.d / 32 / CH;   // compensated steps per lane
+    a.g1 = gamma32(CH - 1);
+    a.g2 = gamma32(m) * gamma32(m);
+    const int blocks = (a.E + kDecodeWarps - 1) / kDecodeWarps;
+    route_decode_kernel<TB, CH><<<blocks, kDecodeWarps * 32, smem, st>>>(a);
+    note_launch(1);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
+// Router launches for RouteArgs with every pointer set: the decode kernel when the tokens'
+// rows fit in shared memory, else norms -> tiled logits -> selection.
+static int launch_route_args(RouteArgs& a, cudaStream_t st) {
+    if (a.T == 0) return MOE_OK;
+    if (a.T <= kDecodeMaxT && (size_t)a.T * a.d * 2 <= kDecodeSmemMax) {
+        if (a.T == 1) return launch_decode_tb<1, 1>(a, st);
+        if (a.T == 2) return launch_decode_tb<2, 1>(a, st);
+        if (a.T <= 4) return launch_decode_tb<4, 2>(a, st);
+        if (a.T <= 8) return launch_decode_tb<8, 4>(a, st);
+        return launch_decode_tb<16, 4>(a, st);
+    }
+    a.bound_coef = gamma_coef(kChunkK + (a.d + kChunkK - 1) / kChunkK + 1);
+    const int rows = a.T + a.E;
+    route_norms_kernel<<<(rows + 7) / 8, 256, 0, st>>>(a);
+    dim3 grid((a.E + kTileE - 1) / kTileE, (a.T + kTileT - 1) / kTileT);
+    route_tiled_kernel<<<grid, 256, 0, st>>>(a);
+    const int sel_blocks = (a.T + 3) / 4;
+    FP4MOE_EPL_DISPATCH(a.E, route_select_kernel<EPL><<<sel_blocks, 128, 0, st>>>(a));
+    note_launch(3);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
 int launch_route(const moe_dims* m, int T, const uint16_t* x, const uint16_t* wr, const float* bias,
                  const int32_t* table, int32_t* ids, float* w, int32_t* slots, int32_t* status,
                  char* ws, const WsLayout& L, cudaStream_t st, int num_sms) {
-    RouteArgs a;
+    RouteArgs a{};
     a.T = T; a.d = m->d; a.E = m->num_experts; a.k = m->top_k;
     a.x = x; a.wr = wr; a.bias = bias; a.table = table;
     a.ids = ids; a.w = w; a.slots = slots; a.status = status;
-    a.logit = reinterpret_cast<float*>(ws + L.logit);
+    a.keys = reinterpret_cast<float4*>(ws + L.keys);
     a.xnorm = reinterpret_cast<float*>(ws + L.xnorm);
     a.wnorm = reinterpret_cast<float*>(ws + L.wnorm);
     a.counter = reinterpret_cast<unsigned*>(ws + L.counter) + kCtrRoute;
-    if (T == 0) return MOE_OK;
-    if (T <= kDecodeMaxT) {
-        int per_lane = (m->d / 8 + 31) / 32;
-        a.bound_coef = gamma_coef(per_lane * 8 + 5);
-        int warps = 4;
-        int blocks = (a.E + warps - 1) / warps;
-        size_t smem = (size_t)T * m->d * 2;
-        if (smem > 48 * 1024) {
-            if (cudaFuncSetAttribute(route_small_kernel<kDecodeMaxT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem) != cudaSuccess)
-                return MOE_ERR_LAUNCH;
-        }
-        route_small_kernel<kDecodeMaxT><<<blocks, warps * 32, smem, st>>>(a);
-    } else {
-        a.bound_coef = gamma_coef(kChunkK + (m->d + kChunkK - 1) / kChunkK + 1);
-        dim3 grid((a.E + kTileE - 1) / kTileE, (T + kTileT - 1) / kTileT);
-        route_tiled_kernel<<<grid, 256, 0, st>>>(a);
-        int rows = T + a.E;
-        route_norms_kernel<<<(rows + 7) / 8, 256, 0, st>>>(a);
-        int sel_blocks = (T + 3) / 4;
-        FP4MOE_EPL_DISPATCH(a.E, route_select_kernel<EPL><<<sel_blocks, 128, 0, st>>>(a));
-    }
     (void)num_sms;
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+    return launch_route_args(a, st);
 }
 
 }  // namespace fp4moe
@@ -541,10 +605,10 @@ namespace fp4moe {
 
 constexpr int kStaticMaxT = kDecodeMaxT;   // tokens per call
 constexpr size_t kStaticCounterBytes = 256;
-constexpr size_t kStaticLogitBytes = sizeof(float) * kStaticMaxT * kMaxExperts;
+constexpr size_t kStaticKeyBytes = sizeof(float4) * kStaticMaxT * kMaxExperts;
 constexpr size_t kStaticXnormBytes = 256;
 constexpr size_t kStaticWnormBytes = sizeof(float) * kMaxExperts;
-constexpr size_t kStaticScratchBytes = kStaticCounterBytes + kStaticLogitBytes + kStaticXnormBytes + kStaticWnormBytes;
+constexpr size_t kStaticScratchBytes = kStaticCounterBytes + kStaticKeyBytes + kStaticXnormBytes + kStaticWnormBytes;
 
 static __device__ __align__(256) unsigned char g_route_scratch[kStaticScratchBytes];
 
@@ -583,23 +647,13 @@ extern "C" int moe_route_topk_noalloc(const moe_dims* dims, int32_t T, const uin
     cudaStream_t st = (cudaStream_t)stream;
     // the completion ticket must start at zero
     if (cudaMemsetAsync(base, 0, kStaticCounterBytes, st) != cudaSuccess) return MOE_ERR_LAUNCH;
-    RouteArgs a;
+    RouteArgs a{};
     a.T = T; a.d = dims->d; a.E = dims->num_experts; a.k = dims->top_k;
     a.x = x; a.wr = w_router; a.bias = score_bias; a.table = expert_to_slot;
     a.ids = topk_ids; a.w = topk_w; a.slots = topk_slot; a.status = dev_status;
     a.counter = reinterpret_cast<unsigned*>(base);
-    a.logit = reinterpret_cast<float*>(base + kStaticCounterBytes);
-    a.xnorm = reinterpret_cast<float*>(base + kStaticCounterBytes + kStaticLogitBytes);
-    a.wnorm = reinterpret_cast<float*>(base + kStaticCounterBytes + kStaticLogitBytes + kStaticXnormBytes);
-    int per_lane = (a.d / 8 + 31) / 32;
-    a.bound_coef = gamma_coef(per_lane * 8 + 5);
-    const int warps = 4;
-    int blocks = (a.E + warps - 1) / warps;
-    size_t smem = (size_t)T * a.d * 2;
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(route_small_kernel<kDecodeMaxT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-        return MOE_ERR_LAUNCH;
-    route_small_kernel<kDecodeMaxT><<<blocks, warps * 32, smem, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+    a.keys = reinterpret_cast<float4*>(base + kStaticCounterBytes);
+    a.xnorm = reinterpret_cast<float*>(base + kStaticCounterBytes + kStaticKeyBytes);
+    a.wnorm = reinterpret_cast<float*>(base + kStaticCounterBytes + kStaticKeyBytes + kStaticXnormBytes);
+    return launch_route_args(a, st);
 }

@@ -159,6 +159,12 @@ int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, 
 int moe_combine(const moe_dims* dims, int32_t T, const float* rows, const int32_t* row_dst,
                 const float* topk_w, uint16_t* y, void* stream);
 
+/* Number of kernels this library has enqueued in this process so far (every entry point
+ * above counts the kernels it launches).  A call captured into a CUDA graph counts once, at
+ * capture, so the difference across a capture is the kernel count of one graph replay.
+ * Thread-safe; never fails. */
+uint64_t moe_kernel_launches(void);
+
 /* Human-readable text of a return code. */
 const char* moe_status_str(int code);
 

@@ -37,6 +37,7 @@ def test_slot_bytes_and_workspace():
 
 def test_host_argument_errors_return_before_any_launch():
     L = moe.lib()
+    launched = moe.moe_kernel_launches()
     good = moe.moe_dims(512, 256, 16, 2)
     bad = moe.moe_dims(512, 256, 16, 40)
     P = ctypes.c_void_p
@@ -54,3 +55,4 @@ def test_host_argument_errors_return_before_any_launch():
                                 None, fake, fake, fake, 1 << 30, None) == -6
     assert L.moe_pack_expert(ctypes.byref(good), fake, fake, fake, fake, fake, fake, ctypes.byref(ar), 9, None) == -5
     assert moe.moe_status_str(-4) == "workspace too small"
+    assert moe.moe_kernel_launches() == launched      # every rejected call launched nothing

@@ -60,7 +60,7 @@ def check_tokens(wl, x_bits, got, tokens, bias=None):
     r, y = oracle_tokens(wl, x_bits, tokens, bias)
     np.testing.assert_array_equal(got["ids"][tokens], r["ids"])
     np.testing.assert_array_equal(got["slots"][tokens], r["slots"])
-    np.testing.assert_allclose(got["w"][tokens], r["weights"], rtol=2e-6, atol=1e-7)
+    np.testing.assert_allclose(got["w"][tokens], r["weights"], rtol=2e-5, atol=1e-7)
     err = row_rel_err(got["y"][tokens], y)
     print("max row error %.3e over %d tokens" % (err.max(), len(tokens)))
     assert err.max() <= TOL, err
@@ -93,7 +93,7 @@ def test_tiny_layer_matches_oracle(tiny):
     ref = oracle.moe_layer(x, tiny.wr, None, tiny.table, 2, slots)
     np.testing.assert_array_equal(got["ids"], ref["ids"])
     np.testing.assert_array_equal(got["slots"], ref["slots"])
-    np.testing.assert_allclose(got["w"], ref["weights"], rtol=2e-6)
+    np.testing.assert_allclose(got["w"], ref["weights"], rtol=2e-5)
     assert row_rel_err(got["y"], ref["y"]).max() <= TOL
 
 
@@ -120,36 +120,94 @@ def test_prefill_fused_combine_matches_unfused(tiny, cuda_cores):
 
 # ---------------------------------------------------------------------------- routing edge cases
 
-def test_router_ties_mask_bias_and_few_resident():
+def route_only(wl, x_bits, bias=None):
+    T = x_bits.shape[0]
+    layer = MoeLayer(wl.d, wl.f, wl.E, wl.k, max(T, 1), wl.arena)
+    b = None if bias is None else torch.from_numpy(bias).to(DEV)
+    layer.route(bits_to_torch(x_bits, DEV), bits_to_torch(wl.wr, DEV), torch.from_numpy(wl.table).to(DEV), b)
+    torch.cuda.synchronize()
+    return dict(ids=layer.ids[:T].cpu().numpy(), w=layer.w[:T].cpu().numpy(), slots=layer.slots[:T].cpu().numpy(),
+                status=int(layer.status.item()))
+
+
+def check_route(wl, x_bits, got, bias=None):
+    r = oracle.route_topk(x_bits, wl.wr, bias, wl.table, wl.k)
+    np.testing.assert_array_equal(got["ids"], r["ids"])
+    np.testing.assert_array_equal(got["slots"], r["slots"])
+    np.testing.assert_allclose(got["w"], r["weights"], rtol=2e-5, atol=1e-7)
+
+
+# T = 1, 5 and 16 take the decode router (one warp per expert, compensated logits, the
+# last block selects); T = 24 the tiled router.
+@pytest.mark.parametrize("T", [1, 5, 16, 24])
+def test_router_ties_mask_bias_and_few_resident(T):
     d, E, k = 256, 40, 4
     wl = make_workload(d, 256, E, k, seed=5, scale=(-8, -4))
     wr = wl.wr.copy()
     wr[7] = wr[3]          # exact ties between experts 3, 7 and 21
     wr[21] = wr[3]
     wl.wr = wr
-    x = syn.activations(5, 0, 24, d)
+    x = syn.activations(5, 0, T, d)
     got = run_layer(wl, x)
-    check_tokens(wl, x, got, list(range(24)))
+    check_tokens(wl, x, got, list(range(T)))
     bias = syn.zipf_score_bias(5, 0, E, 1.2, 0.5)
     got = run_layer(wl, x, bias=bias)
-    check_tokens(wl, x, got, list(range(24)), bias=bias)
+    check_tokens(wl, x, got, list(range(T)), bias=bias)
     # keep-set mask: half the experts have no slot
     tab = wl.table.copy()
     tab[::2] = -1
     wl.table = tab
     got = run_layer(wl, x)
     assert np.all(got["ids"] % 2 == 1)
-    check_tokens(wl, x, got, list(range(24)))
+    check_tokens(wl, x, got, list(range(T)))
     # fewer than k resident
     tab = np.full(E, -1, np.int32)
     tab[[5, 9]] = [5, 9]
     wl.table = tab
     got = run_layer(wl, x[:2])
     assert got["status"] & moe.MOE_STATUS_FEW_RESIDENT
-    assert got["ids"].tolist() == [[5, 9, -1, -1]] * 2
+    assert got["ids"].tolist() == [[5, 9, -1, -1]] * min(T, 2)
     r = oracle.route_topk(x[:2], wl.wr, None, tab, k)
     np.testing.assert_array_equal(got["ids"], r["ids"])
-    np.testing.assert_allclose(got["w"], r["weights"], rtol=2e-6)
+    np.testing.assert_allclose(got["w"], r["weights"], rtol=2e-5)
+
+
+@pytest.mark.parametrize("T", [1, 3, 8, 16, 40])
+def test_router_wide_dynamic_range_and_saturation(T):
+    """Activations scaled by 2^u, u uniform in [-24, 24] per element: logits span many
+    orders of magnitude, most scores saturate to exactly 0 or 1 (ties broken by id), and
+    the fast logit's error bound is exercised far from the N(0, 1) regime."""
+    d, E, k = 1024, 200, 6
+    wl = make_workload(d, 256, E, k, seed=11, table="permuted", scale=(-8, -4))
+    x = syn.bf16_bits_to_f32(syn.activations(11, 0, T, d)).astype(np.float64)
+    u = np.random.default_rng(11).integers(-24, 25, size=x.shape)
+    xb = syn.f32_to_bf16_bits(np.ldexp(x, u).astype(np.float32))
+    got = route_only(wl, xb)
+    check_route(wl, xb, got)
+    # moderate scale: scores spread over (0, 1) with close neighbours
+    xb2 = syn.f32_to_bf16_bits((x * 3.0).astype(np.float32))
+    bias = syn.zipf_score_bias(11, 0, E, 1.0, 1e-3)
+    got = route_only(wl, xb2, bias=bias)
+    check_route(wl, xb2, got, bias=bias)
+
+
+def test_router_cancellation_of_large_products():
+    """Each token carries +-2^20 at elements 0/1 (one lane's chunk) and 16/24 (two lanes),
+    against equal router weights, so those products cancel exactly in the true logit while
+    an uncompensated fp32 chain holding them loses the bits of every small product."""
+    d, E, k, T = 512, 64, 4, 6
+    wl = make_workload(d, 256, E, k, seed=12, scale=(-8, -4))
+    x = syn.bf16_bits_to_f32(syn.activations(12, 0, T, d)).copy()
+    big = np.float32(2.0 ** 20)
+    x[:, 0], x[:, 1], x[:, 16], x[:, 24] = big, -big, big, -big
+    w = syn.bf16_bits_to_f32(wl.wr).copy()
+    w[:, 1] = w[:, 0]
+    w[:, 24] = w[:, 16]
+    wl.wr = syn.f32_to_bf16_bits(w)
+    xb = syn.f32_to_bf16_bits(x)
+    for n in (1, T):
+        got = route_only(wl, xb[:n])
+        check_route(wl, xb[:n], got)
 
 
 def test_router_large_batch_bit_exact_ids():
@@ -162,7 +220,7 @@ def test_router_large_batch_bit_exact_ids():
     r = oracle.route_topk(x, wl.wr, bias, wl.table, k)
     np.testing.assert_array_equal(got["ids"], r["ids"])
     np.testing.assert_array_equal(got["slots"], r["slots"])
-    np.testing.assert_allclose(got["w"], r["weights"], rtol=2e-6, atol=1e-7)
+    np.testing.assert_allclose(got["w"], r["weights"], rtol=2e-5, atol=1e-7)
 
 
 def test_bad_slot_is_reported_and_skipped():
