@@ -36,7 +36,9 @@ constexpr int kKBytes = 128;          // code bytes per row per stage
 constexpr int kThreadsGemm = 6 * 32;
 constexpr unsigned kSpinLimit = 1u << 25;
 constexpr int kTmemCols = 512;
-constexpr int kSfRing = 2;               // scale buffers in TMEM (tcgen05.cp and MMAs run in issue order)
+constexpr int kSfRing = 2;
+constexpr int kPrefillNT = 32;           // activation rows per tile (prefill)
+constexpr int kMaxNT = 64;               // activation rows per tile (decode: T*k pairs)               // scale buffers in TMEM (tcgen05.cp and MMAs run in issue order)
 
 enum { kModeGateUp = 0, kModeDown = 1 };
 enum { kRegimeDecode = 0, kRegimePrefill = 1 };
@@ -108,16 +110,21 @@ __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float* v) {
-    uint32_t r[16];
+// Asynchronous 32x32b.x16 load: the registers are valid only after tc_wait_ld16 on them (the
+// wait takes them as operands, so no use can be scheduled before it).
+__device__ __forceinline__ void tc_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
           "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_wait_ld16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
 }
 
 // ------------------------------------------------------------------ MXFP4 multi-term quantiser
@@ -244,49 +251,45 @@ __global__ void quantize_tiles_kernel(const uint16_t* __restrict__ x, const int3
     }
 }
 
-// ------------------------------------------------------------------ the GEMM kernel
+// ------------------------------------------------------------------ the expert FFN kernel
 
-struct GemmParams {
-    int mode, regime;
-    int K, kblocks, mtiles;          // reduction length, K / 256, weight rows / 128
+// One GEMM of the FFN: gate/up (phase 0, K = d, weight rows 2f interleaved gate/up) or down
+// (phase 1, K = f, weight rows d).
+struct PhaseParams {
+    int kblocks, mtiles;             // K / 256, weight rows / 128
+    int64_t a_code_off, a_sf_off;    // weight matrix regions inside a slot
+    const uint8_t* b_q;              // activation tiles (codes)
+    const uint8_t* b_sf;             // activation tiles (scale atoms)
+    int decode_cols;                 // decode: valid columns (B rows) of every unit
+};
+
+struct FfnParams {
+    int regime;
     int T, k, E, num_slots;
     const int32_t* slot;             // [T*k]
-    int decode_cols;                 // decode: valid columns (B rows) in every unit
+    const float* w;                  // [T*k] routing weights (decode combine)
     const int32_t* plan;             // prefill: [n_active, tiles, e_0.., tile_start_0..] (NT-row tiles)
     const int32_t* offsets;
     const int32_t* row_src;
     const uint8_t* arena;
-    int64_t slot_bytes, a_code_off, a_sf_off;   // weight matrix regions inside a slot
-    const uint8_t* b_q;              // activation tiles (codes)
-    const uint8_t* b_sf;             // activation tiles (scale atoms)
-    uint8_t* hq;                     // gate/up: h tiles for the down GEMM (codes)
-    uint8_t* hsf;                    // gate/up: h tiles (scale atoms)
-    int h_nt;                        // rows per h tile
-    int f;
-    float* rows_out;                 // down: [rows][d]
-    int d;
+    int64_t slot_bytes;
+    PhaseParams ph[2];
+    uint8_t* hq;                     // h tiles written by phase 0, read by phase 1 (codes)
+    uint8_t* hsf;                    // h tiles (scale atoms)
+    int f, d;
+    float* rows_out;                 // phase 1 output rows [rows][d] (fp32)
+    uint16_t* y;                     // decode: combined output [T][d] (bf16)
     int32_t* status;
-    float* part;                     // split units: [CTA][2][128][NT] fp32 partial accumulators
-    int32_t* ctr;                    // split units: arrivals per unit (zero at launch)
+    int32_t* work;                   // next unit to hand out (zero at launch)
+    int32_t* ready;                  // phase 0 units finished, per key (decode: slot ordinal; prefill: tile)
+    int32_t* ycnt;                   // decode: pair rows finished per 128-feature block of y
 };
 
-// Stream-K schedule.  The n_units * kblocks (unit, K block) iterations are cut into gridDim.x
-// contiguous ranges, CTA c taking [it0(c), it0(c+1)) with it0(c) = floor(total c / G); a CTA
-// walks its range as segments (unit, kb0, kb1).  A unit cut between CTAs is finished by the
-// last of its pieces to arrive, which adds the pieces' partial accumulators in CTA order.
-struct Seg {
-    int unit, kb0, kb1;
-};
-__device__ __forceinline__ Seg seg_at(long long it, long long it1, int KB) {
-    Seg s;
-    s.unit = (int)(it / KB);
-    s.kb0 = (int)(it % KB);
-    s.kb1 = (int)min((long long)KB, (long long)s.kb0 + (it1 - it));
-    return s;
-}
-__device__ __forceinline__ long long sk_it0(long long total, int c, int G) { return total * c / G; }
-// CTA whose range holds iteration i
-__device__ __forceinline__ int sk_cta_of(long long total, long long i, int G) { return (int)(((i + 1) * G - 1) / total); }
+// Work list: units [0, n0) are gate/up units, [n0, n0 + n1) down units, n_i = n_keys x
+// weight tiles of phase i; a unit is one (key, weight tile) pair over the whole K.  CTAs take
+// units in that order from a global counter, so every gate/up unit is handed out before any
+// down unit, and the keys' gate/up units (key-major order) finish in key order.
+constexpr int kUQ = 8;   // unit ids in flight from the producer to the MMA and epilogue warps
 
 // Per-NT shape of the pipeline.  B rows per tile = kTerms*NT, split into MMA groups of at
 // most 128 rows (N of one MMA).  ACC independent accumulators (K slices alternate between
@@ -317,19 +320,22 @@ struct GemmCfg {
 struct UnitInfo {
     int slot;       // arena slot of the weights
     int m;          // weight row tile
+    int key;        // decode: slot ordinal; prefill: activation tile
     int btile;      // activation tile
     int brow0;      // first B row (row index of the activation rows / outputs)
     int ncols;      // valid columns of D
 };
 
 template <int NT>
-__device__ __forceinline__ bool unit_info(const GemmParams& p, int unit, const int* uslots, UnitInfo& u) {
+__device__ __forceinline__ bool unit_info(const FfnParams& p, const PhaseParams& P, int unit, const int* uslots,
+                                          UnitInfo& u) {
     if (p.regime == kRegimeDecode) {
-        u.m = unit % p.mtiles;
-        u.slot = uslots[unit / p.mtiles];
+        u.m = unit % P.mtiles;
+        u.key = unit / P.mtiles;
+        u.slot = uslots[u.key];
         u.btile = 0;
         u.brow0 = 0;
-        u.ncols = p.decode_cols;
+        u.ncols = P.decode_cols;
         return true;
     }
     // prefill: unit = tile_start[g]*mtiles + m*ntiles_g + ntile (tiles sharing weights adjacent)
@@ -337,15 +343,16 @@ __device__ __forceinline__ bool unit_info(const GemmParams& p, int unit, const i
     int lo = 0, hi = na - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (p.plan[2 + E + mid] * p.mtiles <= unit) lo = mid; else hi = mid - 1;
+        if (p.plan[2 + E + mid] * P.mtiles <= unit) lo = mid; else hi = mid - 1;
     }
     const int g = lo, e = p.plan[2 + g];
     const int o0 = p.offsets[e], o1 = p.offsets[e + 1];
     const int ntiles = (o1 - o0 + NT - 1) / NT;
-    const int local = unit - p.plan[2 + E + g] * p.mtiles;
+    const int local = unit - p.plan[2 + E + g] * P.mtiles;
     u.m = local / ntiles;
     const int nt = local % ntiles;
     u.btile = p.plan[2 + E + g] + nt;
+    u.key = u.btile;
     u.brow0 = o0 + nt * NT;
     u.ncols = min(NT, o1 - u.brow0);
     const int src = p.row_src[o0];
@@ -353,8 +360,21 @@ __device__ __forceinline__ bool unit_info(const GemmParams& p, int unit, const i
     return u.slot >= 0 && u.slot < p.num_slots;
 }
 
-template <int NT, int MODE>
-__global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p) {
+__device__ __forceinline__ int ld_acquire(const int32_t* a) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// The whole expert FFN in one persistent launch (one CTA per SM, every CTA resident).  The
+// producer takes units from the work list; a down unit needs the h rows of its key (decode:
+// its slot; prefill: its tile) from every gate/up unit of that key, so the producer issues the
+// unit's first weight copy, then waits (bounded) for the key's count of finished gate/up units
+// before issuing the h copy.  Decode also combines: the last down unit to finish a
+// 128-feature block of y sums the token's pair rows in ascending j.
+template <int NT>
+__global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) {
     using C = GemmCfg<NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -366,13 +386,17 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
     uint64_t* tfull = bars + 2 * C::kStages;     // [2] accumulator set ready
     uint64_t* tempty = tfull + 2;                // [2] accumulator set drained
     uint64_t* epibar = tempty + 2;               // [2] epilogue warps' h-tile hand-offs
-    uint64_t* fixbar = epibar + 2;               // [2] split-unit arrival hand-offs
+    uint64_t* fixbar = epibar + 2;               // [2] arrival-count hand-offs
+    uint64_t* uqfull = fixbar + 2;               // [kUQ] unit id written
+    uint64_t* uqempty = uqfull + kUQ;            // [kUQ] unit id read by the MMA and epilogue warps
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
-    __shared__ int n_units_sh;
+    __shared__ int n_keys_sh, pairs_total_sh;
     __shared__ int fix_last;
     __shared__ int wcount[8];
-    __shared__ int uslots[128];
+    __shared__ int uslots[kMaxNT];
+    __shared__ int upairs[kMaxNT];
+    __shared__ int uq[kUQ];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
@@ -388,6 +412,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
         }
         mbar_init(smem_u32(&fixbar[0]), 4);
         mbar_init(smem_u32(&fixbar[1]), 1);
+        for (int i = 0; i < kUQ; ++i) {
+            mbar_init(smem_u32(&uqfull[i]), 1);
+            mbar_init(smem_u32(&uqempty[i]), 5);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -396,9 +424,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // decode: the unique valid slots, in order of first appearance, give the units
+    // decode: the unique valid slots, in order of first appearance, are the keys
     if (p.regime == kRegimeDecode) {
-        const int n = p.T * p.k;   // <= 128, checked on the host
+        const int n = p.T * p.k;   // <= kMaxNT, checked on the host
         int s = -1;
         bool first = false;
         if (tid < n) {
@@ -414,39 +442,60 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
         __syncthreads();
         int off = 0;
         for (int w = 0; w < warp; ++w) off += wcount[w];
-        if (first) uslots[off + __popc(bal & ((1u << lane) - 1u))] = s;
+        if (first) {
+            int np = 0;
+            for (int j = 0; j < n; ++j) np += (p.slot[j] == s);
+            uslots[off + __popc(bal & ((1u << lane) - 1u))] = s;
+            upairs[off + __popc(bal & ((1u << lane) - 1u))] = np;
+        }
         if (tid == 0) {
-            int tot = 0;
+            int tot = 0, pairs = 0;
             for (int w = 0; w < kThreadsGemm / 32; ++w) tot += wcount[w];
-            n_units_sh = tot * p.mtiles;
+            for (int j = 0; j < n; ++j) pairs += (p.slot[j] >= 0 && p.slot[j] < p.num_slots);
+            n_keys_sh = tot;
+            pairs_total_sh = pairs;
         }
     } else if (tid == 0) {
-        n_units_sh = p.plan[1] * p.mtiles;
+        n_keys_sh = p.plan[1];
+        pairs_total_sh = 0;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
-    const int n_units = n_units_sh;
+    const int n_keys = n_keys_sh;
+    const int n0 = n_keys * p.ph[0].mtiles, n_all = n0 + n_keys * p.ph[1].mtiles;
     volatile int* abortp = &abort_flag;
-    const int KB = p.kblocks;
-    const long long total = (long long)n_units * KB;
-    const int G = (int)min((long long)gridDim.x, total);   // ranges; none is empty
-    const long long it0 = (int)blockIdx.x < G ? sk_it0(total, blockIdx.x, G) : 0;
-    const long long it1 = (int)blockIdx.x < G ? sk_it0(total, blockIdx.x + 1, G) : 0;
+    // decode with no valid pair: y is zero
+    if (p.regime == kRegimeDecode && p.y && n_keys == 0 && blockIdx.x == 0)
+        for (int i = tid; i < p.T * p.d; i += blockDim.x) p.y[i] = 0;
+    // position in the unit-id ring (same sequence for every role)
+    int qi = 0;
+    uint32_t qphase = 0;
 
     if (warp == 0) {
-        // ---------------- producer: four contiguous bulk copies per stage
+        // ---------------- producer: takes units, four contiguous bulk copies per stage
         if (lane == 0) {
-            int stage = 0;
+            int stage = 0, ready_key = -1;
             uint32_t phase = 0, issued = 0, issued_parity = 0;   // per-stage bit masks
-            for (long long it = it0; it < it1 && !*abortp;) {
-                const Seg sg = seg_at(it, it1, KB);
-                it += sg.kb1 - sg.kb0;
+            while (true) {
+                int unit = *abortp ? -1 : atomicAdd(p.work, 1);
+                if (unit >= n_all) unit = -1;
+                if (!mbar_wait(smem_u32(&uqempty[qi]), qphase ^ 1u, abortp)) {
+                    atomicOr(p.status, MOE_STATUS_TIMEOUT);
+                    *abortp = 1;
+                    unit = -1;
+                }
+                uq[qi] = unit;
+                mbar_arrive(smem_u32(&uqfull[qi]));
+                if (++qi == kUQ) { qi = 0; qphase ^= 1u; }
+                if (unit < 0) break;
+                const int ph = unit < n0 ? 0 : 1;
+                const PhaseParams& P = p.ph[ph];
                 UnitInfo u;
-                const bool ok = unit_info<NT>(p, sg.unit, uslots, u);
+                const bool ok = unit_info<NT>(p, P, ph ? unit - n0 : unit, uslots, u);
                 const uint8_t* sbase = p.arena + (int64_t)(ok ? u.slot : 0) * p.slot_bytes;
-                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                for (int kb = 0; kb < P.kblocks; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abortp)) {
                         atomicOr(p.status, MOE_STATUS_TIMEOUT);
                         *abortp = 1;
@@ -454,13 +503,28 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
                     }
                     const uint32_t st = smem_u32(stage_base + stage * C::kStage);
                     const uint32_t bar = smem_u32(&full[stage]);
-                    const int64_t atile = (int64_t)u.m * p.kblocks + kb;
-                    const int64_t btile = (int64_t)u.btile * p.kblocks + kb;
+                    const int64_t atile = (int64_t)u.m * P.kblocks + kb;
+                    const int64_t btile = (int64_t)u.btile * P.kblocks + kb;
                     mbar_expect_tx(bar, C::kStage);
-                    bulk_g2s(st, sbase + p.a_code_off + atile * kTileCodeBytes, C::kA, bar);
-                    bulk_g2s(st + C::kA, p.b_q + btile * C::kB, C::kB, bar);
-                    bulk_g2s(st + C::kA + C::kB, sbase + p.a_sf_off + atile * kTileScaleBytes, C::kSFA, bar);
-                    bulk_g2s(st + C::kA + C::kB + C::kSFA, p.b_sf + btile * C::kSFB, C::kSFB, bar);
+                    bulk_g2s(st, sbase + P.a_code_off + atile * kTileCodeBytes, C::kA, bar);
+                    bulk_g2s(st + C::kA + C::kB, sbase + P.a_sf_off + atile * kTileScaleBytes, C::kSFA, bar);
+                    if (ph == 1 && ok && u.key != ready_key) {
+                        // h rows of this key: every gate/up unit of the key has written them
+                        unsigned spins = 0;
+                        while (ld_acquire(p.ready + u.key) < p.ph[0].mtiles) {
+                            if (++spins > kSpinLimit || *abortp) {
+                                atomicOr(p.status, MOE_STATUS_TIMEOUT);
+                                *abortp = 1;
+                                break;
+                            }
+                            __nanosleep(32);
+                        }
+                        fence_proxy_async();
+                        ready_key = u.key;
+                    }
+                    // (issued even after a timeout so that the stage's barrier completes)
+                    bulk_g2s(st + C::kA, P.b_q + btile * C::kB, C::kB, bar);
+                    bulk_g2s(st + C::kA + C::kB + C::kSFA, P.b_sf + btile * C::kSFB, C::kSFB, bar);
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -480,9 +544,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
             int stage = 0, sfring = 0, acc = 0;
             uint32_t phase = 0, aphase = 0;
             const uint32_t idesc_lo = idesc_mxf4(C::kN, 0), idesc_hi = idesc_mxf4(C::kN, 2);
-            for (long long it = it0; it < it1 && !*abortp;) {
-                const Seg sg = seg_at(it, it1, KB);
-                it += sg.kb1 - sg.kb0;
+            while (true) {
+                int unit = -1;
+                if (mbar_wait(smem_u32(&uqfull[qi]), qphase, abortp)) unit = uq[qi];
+                mbar_arrive(smem_u32(&uqempty[qi]));
+                if (++qi == kUQ) { qi = 0; qphase ^= 1u; }
+                if (unit < 0) break;
+                const int KB = p.ph[unit < n0 ? 0 : 1].kblocks;
                 if (!mbar_wait(smem_u32(&tempty[acc]), aphase ^ 1u, abortp)) {
                     atomicOr(p.status, MOE_STATUS_TIMEOUT);
                     *abortp = 1;
@@ -491,7 +559,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
                 tc_fence_after();
                 const uint32_t dset = tmem + acc * C::kAcc * C::kRows;
                 bool failed = false;
-                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abortp)) {
                         atomicOr(p.status, MOE_STATUS_TIMEOUT);
                         *abortp = 1;
@@ -514,7 +582,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
                     for (int j = 0; j < 4; ++j) {
                         const int a = j % C::kAcc;
                         const uint64_t ad = desc_sw128(sa + 32 * j);
-                        const uint32_t accumulate = (kb > sg.kb0 || j >= C::kAcc) ? 1u : 0u;
+                        const uint32_t accumulate = (kb > 0 || j >= C::kAcc) ? 1u : 0u;
 #pragma unroll
                         for (int g = 0; g < C::kGroups; ++g) {
                             const uint64_t bd = desc_sw128(sb + g * 128 * kKBytes + 32 * j);
@@ -535,21 +603,55 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
         // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
         const int q = warp & 3;
         const int ew = warp - 2;
+        const int row = q * 32 + lane;       // accumulator row = weight row within the tile
         int acc = 0;
         uint32_t aphase = 0, ephase = 0, fphase = 0;
         const int KBf = p.f / kKB;
-        for (long long it = it0; it < it1 && !*abortp;) {
-            const long long seg_first = it;
-            const Seg sg = seg_at(it, it1, KB);
-            it += sg.kb1 - sg.kb0;
+        // All four warps together: add `add` to *counter after this CTA's global writes (one
+        // gpu-scope fence after the CTA hand-off); every warp learns whether that addition
+        // reached `target`.  False on a timeout.
+        auto count_arrival = [&](int32_t* counter, int add, int target, bool& last) -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&fixbar[0]));
+            if (ew == 0) {
+                const bool okw = mbar_wait(smem_u32(&fixbar[0]), fphase, abortp);
+                if (lane == 0) {
+                    int l = 0;
+                    if (okw) {
+                        __threadfence();
+                        l = (atomicAdd(counter, add) + add == target);
+                        __threadfence();
+                    } else {
+                        atomicOr(p.status, MOE_STATUS_TIMEOUT);
+                        *abortp = 1;
+                    }
+                    fix_last = l;
+                    mbar_arrive(smem_u32(&fixbar[1]));
+                }
+                __syncwarp();
+            }
+            const bool ok1 = mbar_wait(smem_u32(&fixbar[1]), fphase, abortp);
+            if (!ok1 && lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
+            fphase ^= 1u;
+            last = ok1 && fix_last;
+            return ok1;
+        };
+        while (true) {
+            int unit = -1;
+            if (mbar_wait(smem_u32(&uqfull[qi]), qphase, abortp)) unit = uq[qi];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&uqempty[qi]));
+            if (++qi == kUQ) { qi = 0; qphase ^= 1u; }
+            if (unit < 0) break;
+            const int ph = unit < n0 ? 0 : 1;
+            const PhaseParams& P = p.ph[ph];
             UnitInfo u;
-            const bool ok = unit_info<NT>(p, sg.unit, uslots, u);
+            const bool ok = unit_info<NT>(p, P, ph ? unit - n0 : unit, uslots, u);
             if (!mbar_wait(smem_u32(&tfull[acc]), aphase, abortp)) {
                 if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
                 break;
             }
             tc_fence_after();
-            const int row = q * 32 + lane;       // accumulator row = weight row within the tile
             // D[row][n] = sum over accumulators and terms of column (a*kRows + t*NT + n)
             float vals[NT];
 #pragma unroll
@@ -558,72 +660,45 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
 #pragma unroll
             for (int a = 0; a < C::kAcc; ++a)
 #pragma unroll
-                for (int t = 0; t < kTerms; ++t)
+                for (int c0 = 0; c0 < NT; c0 += 16) {
+                    if (c0 >= u.ncols) break;        // warp-uniform: columns past ncols are padding
+                    uint32_t tmp[kTerms][16];
 #pragma unroll
-                    for (int c0 = 0; c0 < NT; c0 += 16) {
-                        if (c0 >= u.ncols) break;        // warp-uniform: columns past ncols are padding
-                        float tmp[16];
-                        tc_ld16(lanebase + a * C::kRows + t * NT + c0, tmp);
+                    for (int t = 0; t < kTerms; ++t) tc_ld16_issue(lanebase + a * C::kRows + t * NT + c0, tmp[t]);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) vals[c0 + i] += tmp[i];
+                    for (int t = 0; t < kTerms; ++t) {
+                        tc_wait_ld16(tmp[t]);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) vals[c0 + i] += __uint_as_float(tmp[t][i]);
                     }
+                }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
             if (++acc == C::kDbuf) { acc = 0; aphase ^= 1u; }
             if (!ok) continue;
-            if (sg.kb0 != 0 || sg.kb1 != KB) {
-                // a piece of a split unit: publish the partial accumulator, count the arrival;
-                // the last piece to arrive sums every piece's partial in CTA order
-                const int slot = (seg_first == it0) ? 0 : 1;
-                float* mine = p.part + ((size_t)blockIdx.x * 2 + slot) * (kBM * NT);
-#pragma unroll
-                for (int c = 0; c < NT; ++c)
-                    if (c < u.ncols) mine[c * kBM + row] = vals[c];
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&fixbar[0]));
-                const long long u_first = (long long)sg.unit * KB;
-                const int c_first = sk_cta_of(total, u_first, G), c_last = sk_cta_of(total, u_first + KB - 1, G);
-                if (ew == 0) {
-                    const bool okw = mbar_wait(smem_u32(&fixbar[0]), fphase, abortp);
-                    if (lane == 0) {
-                        int last = 0;
-                        if (okw) {
-                            __threadfence();
-                            last = (atomicAdd(p.ctr + sg.unit, 1) == c_last - c_first);
-                            __threadfence();
-                        } else {
-                            atomicOr(p.status, MOE_STATUS_TIMEOUT);
-                            *abortp = 1;
-                        }
-                        fix_last = last;
-                        mbar_arrive(smem_u32(&fixbar[1]));
-                    }
-                    __syncwarp();
-                }
-                if (!mbar_wait(smem_u32(&fixbar[1]), fphase, abortp)) {
-                    if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
-                    break;
-                }
-                fphase ^= 1u;
-                if (!fix_last) continue;
-#pragma unroll
-                for (int c = 0; c < NT; ++c) vals[c] = 0.f;
-                for (int pc = c_first; pc <= c_last; ++pc) {
-                    const int ps = (sk_it0(total, pc, G) >= u_first) ? 0 : 1;   // the unit is pc's first segment
-                    const float* pp = p.part + ((size_t)pc * 2 + ps) * (kBM * NT);
-#pragma unroll
-                    for (int c = 0; c < NT; ++c)
-                        if (c < u.ncols) vals[c] += __ldcg(pp + c * kBM + row);
-                }
-            }
-            if (MODE == kModeDown) {
+            if (ph == 1) {
                 const int r = u.m * kBM + row;    // output feature
 #pragma unroll
                 for (int c = 0; c < NT; ++c) {
                     const bool valid = (p.regime == kRegimeDecode) ? (c < u.ncols && p.slot[c] == u.slot) : (c < u.ncols);
                     if (valid) p.rows_out[(size_t)(u.brow0 + c) * p.d + r] = vals[c];
+                }
+                if (p.regime == kRegimeDecode && p.y) {
+                    // y block m is complete once every valid pair's row block m is written
+                    bool last = false;
+                    if (!count_arrival(p.ycnt + u.m, upairs[u.key], pairs_total_sh, last)) break;
+                    if (last) {
+                        for (int t = 0; t < p.T; ++t) {
+                            float yv = 0.f;
+                            for (int j = 0; j < p.k; ++j) {
+                                const int pr = t * p.k + j, s = p.slot[pr];
+                                if (s < 0 || s >= p.num_slots) continue;
+                                yv = fmaf(p.w[pr], __ldcg(p.rows_out + (size_t)pr * p.d + r), yv);
+                            }
+                            p.y[(size_t)t * p.d + r] = f32_to_bf16(yv);
+                        }
+                    }
                 }
             } else {
                 // rows 2i' = gate, 2i'+1 = up of output i' = row/2 within the tile (i = 64m + i')
@@ -650,25 +725,30 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
                     uint32_t scales[kTerms];
                     warp_quantize32(hbuf[c * 64 + 32 * b + lane], lane, codes, scales);
                     const int i0 = u.m * 64 + 32 * b, kb = i0 / kKB, j = (i0 % kKB) / 32;
-                    if (lane == 0) {
-                        auto write_row = [&](int htile, int hrow) {
+                    auto write_row = [&](int htile, int hrow) {
+                        if (lane < kTerms) {
+                            // lane t writes term t (the codes of every term sit in lane 0)
+                            uint4 cv = codes[0];
+                            uint32_t sv = scales[0];
 #pragma unroll
-                            for (int t = 0; t < kTerms; ++t) {
-                                *reinterpret_cast<uint4*>(p.hq + act_code_off(htile, kb, t, hrow, j, p.h_nt, KBf)) = codes[t];
-                                p.hsf[act_scale_off(htile, kb, t, hrow, j, p.h_nt, KBf)] = (uint8_t)scales[t];
-                            }
-                        };
-                        if (p.regime == kRegimeDecode) {
-                            // column c = token; h for every pair (c, jj) routed to this slot
-                            if (c < p.T)
-                                for (int jj = 0; jj < p.k; ++jj)
-                                    if (p.slot[c * p.k + jj] == u.slot) write_row(0, c * p.k + jj);
-                        } else if (c < u.ncols) {
-                            write_row(u.btile, c);
+                            for (int t = 1; t < kTerms; ++t)
+                                if (lane == t) { cv = codes[t]; sv = scales[t]; }
+                            *reinterpret_cast<uint4*>(p.hq + act_code_off(htile, kb, lane, hrow, j, NT, KBf)) = cv;
+                            p.hsf[act_scale_off(htile, kb, lane, hrow, j, NT, KBf)] = (uint8_t)sv;
                         }
+                    };
+                    if (p.regime == kRegimeDecode) {
+                        // column c = token; h for every pair (c, jj) routed to this slot
+                        if (c < p.T)
+                            for (int jj = 0; jj < p.k; ++jj)
+                                if (p.slot[c * p.k + jj] == u.slot) write_row(0, c * p.k + jj);
+                    } else if (c < u.ncols) {
+                        write_row(u.btile, c);
                     }
                 }
-                // hand-off 2: hbuf may be overwritten by the next unit
+                // the h rows are read by the async proxy (bulk copies) of other CTAs
+                fence_proxy_async();
+                // hand-off 2: hbuf may be overwritten by the next unit; h of this unit is written
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&epibar[1]));
                 if (!mbar_wait(smem_u32(&epibar[1]), ephase, abortp)) {
@@ -676,6 +756,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
                     break;
                 }
                 ephase ^= 1u;
+                if (ew == 0 && lane == 0) {
+                    __threadfence();
+                    atomicAdd(p.ready + u.key, 1);
+                }
             }
         }
     }
@@ -685,54 +769,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_gemm_kernel(GemmParams p
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
-// y[t] = bf16( sum_j w[t,j] rows[t*k + j] ) in ascending j, skipping pairs without a valid slot.
-__global__ void decode_combine_kernel(int T, int d, int k, int num_slots, const float* __restrict__ rows,
-                                      const int32_t* __restrict__ slot, const float* __restrict__ w, uint16_t* y) {
-    const int vec = d / 4;
-    for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < T * vec; idx += gridDim.x * blockDim.x) {
-        const int t = idx / vec, c4 = idx % vec;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            const int pr = t * k + j, s = slot[pr];
-            if (s < 0 || s >= num_slots) continue;
-            const float wj = w[pr];
-            const float4 z = reinterpret_cast<const float4*>(rows + (size_t)pr * d)[c4];
-            acc.x = fmaf(wj, z.x, acc.x);
-            acc.y = fmaf(wj, z.y, acc.y);
-            acc.z = fmaf(wj, z.z, acc.z);
-            acc.w = fmaf(wj, z.w, acc.w);
-        }
-        const uint32_t lo = (uint32_t)f32_to_bf16(acc.x) | ((uint32_t)f32_to_bf16(acc.y) << 16);
-        const uint32_t hi = (uint32_t)f32_to_bf16(acc.z) | ((uint32_t)f32_to_bf16(acc.w) << 16);
-        reinterpret_cast<uint2*>(y + (size_t)t * d)[c4] = make_uint2(lo, hi);
-    }
-}
-
 // ------------------------------------------------------------------ host side
 
-template <int NT, int MODE>
-static int launch_gemm(const GemmParams& p, int grid, cudaStream_t st) {
-    using C = GemmCfg<NT>;
-    if (cudaFuncSetAttribute(mxf4_gemm_kernel<NT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes) !=
-        cudaSuccess)
-        return MOE_ERR_LAUNCH;
-    mxf4_gemm_kernel<NT, MODE><<<grid, kThreadsGemm, C::kBytes, st>>>(p);
-    note_launch(1);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
-}
-
-template <int MODE>
-static int launch_gemm_nt(int NT, const GemmParams& p, int grid, cudaStream_t st) {
-    switch (NT) {
-        case 16: return launch_gemm<16, MODE>(p, grid, st);
-        case 32: return launch_gemm<32, MODE>(p, grid, st);
-        case 64: return launch_gemm<64, MODE>(p, grid, st);
-        default: return MOE_ERR_LAUNCH;
-    }
-}
-
-constexpr int kPrefillNT = 32;
-constexpr int kMaxNT = 64;
+constexpr int kMaxGemmCtas = 160;
 
 // Capacity of the activation tile buffers for T tokens: decode uses one tile of up to kMaxNT
 // rows; the prefill plan needs at most ceil(T*k/NT) + min(E, T*k) tiles of kPrefillNT rows.
@@ -750,23 +789,20 @@ static size_t act_sf_blocks(const moe_dims* m, int T) {      // 1 KB scale block
     const size_t dec = (kTerms * kMaxNT + 127) / 128;
     return b > dec ? b : dec;
 }
-
-constexpr int kMaxGemmCtas = 256;
-
-// Units of either GEMM for T tokens: weight tiles (2f/128 or d/128) x activation tiles.
-static size_t max_units(const moe_dims* m, int T) {
-    const size_t mt = (size_t)(2 * m->f > m->d ? 2 * m->f : m->d) / kBM;
-    return (act_tiles(m, T) > (size_t)kMaxNT ? act_tiles(m, T) : (size_t)kMaxNT) * mt;
+// keys (decode: slot ordinals; prefill: tiles) and units of either phase
+static size_t max_keys(const moe_dims* m, int T) {
+    return act_tiles(m, T) > (size_t)kMaxNT ? act_tiles(m, T) : (size_t)kMaxNT;
 }
 
 struct TcBuffers {
     uint8_t *xq, *xsf, *hq, *hsf;
-    float* part;           // [kMaxGemmCtas][2][128][kMaxNT]
-    int32_t* ctr;          // [2][max_units]: gate/up, down
-    size_t nctr;           // max_units
+    int32_t* zero;         // counters cleared by the quantiser: work, ready[nkeys], ycnt[d/128]
+    size_t nkeys, nzero;
     float* rows;
     int32_t* plan;
 };
+
+static size_t counters_of(const moe_dims* m, int T) { return 1 + max_keys(m, T) + m->d / kBM; }
 
 static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& L) {
     TcBuffers b;
@@ -776,9 +812,9 @@ static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& 
     b.xsf = reinterpret_cast<uint8_t*>(o); o += align256(sfb * (m->d / kKB) * 1024);
     b.hq = reinterpret_cast<uint8_t*>(o);  o += align256(rows * kTerms * m->f / 2);
     b.hsf = reinterpret_cast<uint8_t*>(o); o += align256(sfb * (m->f / kKB) * 1024);
-    b.part = reinterpret_cast<float*>(o);  o += align256((size_t)kMaxGemmCtas * 2 * kBM * kMaxNT * 4);
-    b.nctr = max_units(m, T);
-    b.ctr = reinterpret_cast<int32_t*>(o); o += align256(2 * b.nctr * 4);
+    b.nkeys = max_keys(m, T);
+    b.nzero = counters_of(m, T);
+    b.zero = reinterpret_cast<int32_t*>(o); o += align256(b.nzero * 4);
     b.rows = reinterpret_cast<float*>(o);
     b.plan = reinterpret_cast<int32_t*>(ws + L.active);
     return b;
@@ -788,8 +824,26 @@ size_t tc_workspace_bytes(const moe_dims* m, int T) {
     const size_t R = (size_t)(T > 0 ? T : 1) * m->top_k;
     const size_t rows = act_rows(m, T), sfb = act_sf_blocks(m, T);
     return align256(rows * kTerms * m->d / 2) + align256(sfb * (m->d / kKB) * 1024) + align256(rows * kTerms * m->f / 2) +
-           align256(sfb * (m->f / kKB) * 1024) + align256((size_t)kMaxGemmCtas * 2 * kBM * kMaxNT * 4) +
-           align256(2 * max_units(m, T) * 4) + align256(R * m->d * 4);
+           align256(sfb * (m->f / kKB) * 1024) + align256(counters_of(m, T) * 4) + align256(R * m->d * 4);
+}
+
+template <int NT>
+static int launch_ffn(const FfnParams& p, int grid, cudaStream_t st) {
+    using C = GemmCfg<NT>;
+    if (cudaFuncSetAttribute(mxf4_ffn_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
+    mxf4_ffn_kernel<NT><<<grid, kThreadsGemm, C::kBytes, st>>>(p);
+    note_launch(1);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
+static int launch_ffn_nt(int NT, const FfnParams& p, int grid, cudaStream_t st) {
+    switch (NT) {
+        case 16: return launch_ffn<16>(p, grid, st);
+        case 32: return launch_ffn<32>(p, grid, st);
+        case 64: return launch_ffn<64>(p, grid, st);
+        default: return MOE_ERR_LAUNCH;
+    }
 }
 
 static int nt_for(int cols) { return cols <= 16 ? 16 : cols <= 32 ? 32 : 64; }
@@ -797,90 +851,76 @@ static int nt_for(int cols) { return cols <= 16 ? 16 : cols <= 32 ? 32 : 64; }
 bool tc_supported(const moe_dims* m) { return m->d % kKB == 0 && m->f % kKB == 0; }
 bool tc_decode_supported(const moe_dims* m, int T) { return tc_supported(m) && T >= 1 && T * m->top_k <= kMaxNT; }
 
-static GemmParams base_params(const moe_dims* m, const moe_arena* ar, int T, const int32_t* slot, int32_t* status) {
-    GemmParams p{};
+static FfnParams ffn_params(const moe_dims* m, const moe_arena* ar, int T, const int32_t* slot, int32_t* status,
+                            const TcBuffers& b) {
+    FfnParams p{};
+    const SlotLayout SL = slot_layout(m->d, m->f);
     p.T = T; p.k = m->top_k; p.E = m->num_experts; p.num_slots = ar->num_slots;
     p.slot = slot; p.arena = reinterpret_cast<const uint8_t*>(ar->base); p.slot_bytes = ar->slot_bytes;
     p.f = m->f; p.d = m->d; p.status = status;
+    PhaseParams& g = p.ph[0];
+    g.kblocks = m->d / kKB; g.mtiles = 2 * m->f / kBM;
+    g.a_code_off = SL.gu_q; g.a_sf_off = SL.gu_s;
+    g.b_q = b.xq; g.b_sf = b.xsf;
+    PhaseParams& dn = p.ph[1];
+    dn.kblocks = m->f / kKB; dn.mtiles = m->d / kBM;
+    dn.a_code_off = SL.dn_q; dn.a_sf_off = SL.dn_s;
+    dn.b_q = b.hq; dn.b_sf = b.hsf;
+    p.hq = b.hq; p.hsf = b.hsf;
+    p.work = b.zero;
+    p.ready = b.zero + 1;
+    p.ycnt = b.zero + 1 + b.nkeys;
     return p;
 }
 
-static GemmParams with_split(GemmParams p, const TcBuffers& b, int which) {
-    p.part = b.part;
-    p.ctr = b.ctr + (size_t)which * b.nctr;
-    return p;
-}
-
-// Decode regime: quantise x into one tile, gate/up GEMM (SwiGLU, h quantised per (token, j)
-// pair into one tile), down GEMM (one fp32 row per pair), fixed-order combine into y.
+// Decode regime: x quantised into one tile of NT rows, then one FFN launch (gate/up with
+// SwiGLU and h quantised per (token, j) pair, down to one fp32 row per pair, fixed-order
+// combine into y).
 int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                      const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
                      int num_sms) {
     if (T == 0) return MOE_OK;
     TcBuffers b = tc_buffers(m, T, ws, L);
-    const int d = m->d, f = m->f, k = m->top_k, R = T * k;
-    const SlotLayout SL = slot_layout(d, f);
-    const int nt1 = nt_for(T), nt2 = nt_for(R);
-    const int qwarps = nt1 * (d / 32);
-    quantize_tiles_kernel<<<(qwarps + 7) / 8, 256, 0, st>>>(x, nullptr, nullptr, nullptr, m->num_experts, k, T, d, nt1,
-                                                          b.xq, b.xsf, b.ctr, (int)(2 * b.nctr));
+    const int d = m->d, k = m->top_k, R = T * k;
+    const int NT = nt_for(R);
+    const int qwarps = NT * (d / 32);
+    quantize_tiles_kernel<<<(qwarps + 7) / 8, 256, 0, st>>>(x, nullptr, nullptr, nullptr, m->num_experts, k, T, d, NT,
+                                                          b.xq, b.xsf, b.zero, (int)b.nzero);
     note_launch(1);
-    GemmParams p = base_params(m, ar, T, slot, status);
-    p.mode = kModeGateUp; p.regime = kRegimeDecode;
-    p.K = d; p.kblocks = d / kKB; p.mtiles = 2 * f / kBM;
-    p.decode_cols = T;
-    p.a_code_off = SL.gu_q; p.a_sf_off = SL.gu_s;
-    p.b_q = b.xq; p.b_sf = b.xsf;
-    p.hq = b.hq; p.hsf = b.hsf; p.h_nt = nt2;
+    FfnParams p = ffn_params(m, ar, T, slot, status, b);
+    p.regime = kRegimeDecode;
+    p.w = w;
+    p.ph[0].decode_cols = T;
+    p.ph[1].decode_cols = R;
+    p.rows_out = b.rows;
+    p.y = y;
     const int grid = num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas;
-    int rc = launch_gemm_nt<kModeGateUp>(nt1, with_split(p, b, 0), grid, st);
-    if (rc) return rc;
-    GemmParams q = p;
-    q.mode = kModeDown; q.K = f; q.kblocks = f / kKB; q.mtiles = d / kBM;
-    q.decode_cols = R;
-    q.a_code_off = SL.dn_q; q.a_sf_off = SL.dn_s;
-    q.b_q = b.hq; q.b_sf = b.hsf; q.rows_out = b.rows;
-    rc = launch_gemm_nt<kModeDown>(nt2, with_split(q, b, 1), grid, st);
-    if (rc) return rc;
-    decode_combine_kernel<<<(T * (d / 4) + 255) / 256, 256, 0, st>>>(T, d, k, ar->num_slots, b.rows, slot, w, y);
-    note_launch(1);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+    return launch_ffn_nt(NT, p, grid, st);
 }
 
 __global__ void plan_kernel(int E, int n, const int32_t* offsets, int32_t* plan, int32_t* status, int tile_rows);
 
-// Prefill regime: x rows quantised into the plan's tiles (grouped by expert), gate/up GEMM
-// per (group, weight tile, row tile) with SwiGLU + h quantisation into the same tiles, down
-// GEMM to per-row fp32 outputs; the caller's combine sums them in fixed order.
+// Prefill regime: x rows quantised into the plan's tiles (grouped by expert), then one FFN
+// launch (gate/up per (group, weight tile, row tile) with SwiGLU + h quantisation into the same
+// tiles, down to per-row fp32 outputs); the caller's combine sums them in fixed order.
 int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                       const int32_t* offsets, const int32_t* row_src, float* rows_out, int32_t* status, char* ws,
                       const WsLayout& L, cudaStream_t st, int num_sms) {
     if (T == 0) return MOE_OK;
     TcBuffers b = tc_buffers(m, T, ws, L);
-    const int d = m->d, f = m->f, k = m->top_k, n = T * k;
-    const SlotLayout SL = slot_layout(d, f);
+    const int d = m->d, k = m->top_k, n = T * k;
     plan_kernel<<<1, 32, 0, st>>>(m->num_experts, n, offsets, b.plan, status, kPrefillNT);
     const long qwarps = (long)act_tiles(m, T) * kPrefillNT * (d / 32);
     const long qblocks = (qwarps + 7) / 8;
     quantize_tiles_kernel<<<(int)(qblocks > 16L * num_sms ? 16L * num_sms : qblocks), 256, 0, st>>>(
-        x, row_src, b.plan, offsets, m->num_experts, k, T, d, kPrefillNT, b.xq, b.xsf, b.ctr, (int)(2 * b.nctr));
+        x, row_src, b.plan, offsets, m->num_experts, k, T, d, kPrefillNT, b.xq, b.xsf, b.zero, (int)b.nzero);
     note_launch(2);
-    GemmParams p = base_params(m, ar, T, slot, status);
-    p.mode = kModeGateUp; p.regime = kRegimePrefill;
-    p.K = d; p.kblocks = d / kKB; p.mtiles = 2 * f / kBM;
+    FfnParams p = ffn_params(m, ar, T, slot, status, b);
+    p.regime = kRegimePrefill;
     p.plan = b.plan; p.offsets = offsets; p.row_src = row_src;
-    p.a_code_off = SL.gu_q; p.a_sf_off = SL.gu_s;
-    p.b_q = b.xq; p.b_sf = b.xsf;
-    p.hq = b.hq; p.hsf = b.hsf; p.h_nt = kPrefillNT;
     p.rows_out = rows_out;
     const int grid = num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas;
-    int rc = launch_gemm_nt<kModeGateUp>(kPrefillNT, with_split(p, b, 0), grid, st);
-    if (rc) return rc;
-    GemmParams q = p;
-    q.mode = kModeDown; q.K = f; q.kblocks = f / kKB; q.mtiles = d / kBM;
-    q.a_code_off = SL.dn_q; q.a_sf_off = SL.dn_s;
-    q.b_q = b.hq; q.b_sf = b.hsf;
-    return launch_gemm_nt<kModeDown>(kPrefillNT, with_split(q, b, 1), grid, st);
+    return launch_ffn_nt(kPrefillNT, p, grid, st);
 }
 
 }  // namespace fp4moe
