@@ -207,7 +207,11 @@ __global__ void quantize_tiles_kernel(const uint16_t* __restrict__ x, const int3
                                       int T, int d, int NT, uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
                                       int32_t* __restrict__ zero, int nzero) {
     const int lane = threadIdx.x & 31;
-    // the GEMMs' per-unit arrival counters start at zero
+    // launched early behind the previous kernel: nothing it wrote is read before it completes;
+    // the FFN kernel may launch at once (it waits for this kernel in turn)
+    pdl_trigger();
+    pdl_wait();
+    // the FFN kernel's counters start at zero
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += gridDim.x * blockDim.x) zero[i] = 0;
     const int nblk = d / 32, KB = d / kKB;
     const int ntiles = plan ? plan[1] : 1;
@@ -424,6 +428,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    // everything above overlaps the previous kernel; its outputs are read from here on
+    pdl_wait();
     // decode: the unique valid slots, in order of first appearance, are the keys
     if (p.regime == kRegimeDecode) {
         const int n = p.T * p.k;   // <= kMaxNT, checked on the host
@@ -495,7 +501,43 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 UnitInfo u;
                 const bool ok = unit_info<NT>(p, P, ph ? unit - n0 : unit, uslots, u);
                 const uint8_t* sbase = p.arena + (int64_t)(ok ? u.slot : 0) * p.slot_bytes;
+                // A down unit whose key is not ready yet gets its weight copies issued into every
+                // free stage; the h copies of those stages follow once the key is ready.
+                bool have_b = !(ph == 1 && ok && u.key != ready_key);
+                int pend_n = 0, pend_kb0 = 0, pend_stage0 = 0;
+                auto issue_b = [&](int kb, int stg) {
+                    const uint32_t sb = smem_u32(stage_base + stg * C::kStage);
+                    const uint32_t bar = smem_u32(&full[stg]);
+                    const int64_t btile = (int64_t)u.btile * P.kblocks + kb;
+                    bulk_g2s(sb + C::kA, P.b_q + btile * C::kB, C::kB, bar);
+                    bulk_g2s(sb + C::kA + C::kB + C::kSFA, P.b_sf + btile * C::kSFB, C::kSFB, bar);
+                };
+                auto flush = [&]() {
+                    for (int i = 0; i < pend_n; ++i) issue_b(pend_kb0 + i, (pend_stage0 + i) % C::kStages);
+                    pend_n = 0;
+                };
+                auto key_ready = [&](bool block) -> bool {
+                    // h rows of this key: every gate/up unit of the key has written them
+                    unsigned spins = 0;
+                    while (ld_acquire(p.ready + u.key) < p.ph[0].mtiles) {
+                        if (!block) return false;
+                        if (++spins > kSpinLimit || *abortp) {
+                            atomicOr(p.status, MOE_STATUS_TIMEOUT);
+                            *abortp = 1;
+                            break;   // the copies still go out, so that every stage's barrier completes
+                        }
+                        __nanosleep(64);
+                    }
+                    fence_proxy_async();
+                    ready_key = u.key;
+                    have_b = true;
+                    return true;
+                };
                 for (int kb = 0; kb < P.kblocks; ++kb) {
+                    if (pend_n == C::kStages) {   // the next stage still waits for its h copy
+                        key_ready(true);
+                        flush();
+                    }
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abortp)) {
                         atomicOr(p.status, MOE_STATUS_TIMEOUT);
                         *abortp = 1;
@@ -504,30 +546,23 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     const uint32_t st = smem_u32(stage_base + stage * C::kStage);
                     const uint32_t bar = smem_u32(&full[stage]);
                     const int64_t atile = (int64_t)u.m * P.kblocks + kb;
-                    const int64_t btile = (int64_t)u.btile * P.kblocks + kb;
                     mbar_expect_tx(bar, C::kStage);
                     bulk_g2s(st, sbase + P.a_code_off + atile * kTileCodeBytes, C::kA, bar);
                     bulk_g2s(st + C::kA + C::kB, sbase + P.a_sf_off + atile * kTileScaleBytes, C::kSFA, bar);
-                    if (ph == 1 && ok && u.key != ready_key) {
-                        // h rows of this key: every gate/up unit of the key has written them
-                        unsigned spins = 0;
-                        while (ld_acquire(p.ready + u.key) < p.ph[0].mtiles) {
-                            if (++spins > kSpinLimit || *abortp) {
-                                atomicOr(p.status, MOE_STATUS_TIMEOUT);
-                                *abortp = 1;
-                                break;
-                            }
-                            __nanosleep(32);
-                        }
-                        fence_proxy_async();
-                        ready_key = u.key;
+                    if (!have_b && key_ready(false)) flush();
+                    if (have_b) {
+                        issue_b(kb, stage);
+                    } else {
+                        if (pend_n == 0) { pend_kb0 = kb; pend_stage0 = stage; }
+                        ++pend_n;
                     }
-                    // (issued even after a timeout so that the stage's barrier completes)
-                    bulk_g2s(st + C::kA, P.b_q + btile * C::kB, C::kB, bar);
-                    bulk_g2s(st + C::kA + C::kB + C::kSFA, P.b_sf + btile * C::kSFB, C::kSFB, bar);
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                }
+                if (pend_n) {
+                    key_ready(true);
+                    flush();
                 }
             }
             // every issued copy lands before the CTA may exit (bounded)
@@ -832,9 +867,10 @@ static int launch_ffn(const FfnParams& p, int grid, cudaStream_t st) {
     using C = GemmCfg<NT>;
     if (cudaFuncSetAttribute(mxf4_ffn_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes) != cudaSuccess)
         return MOE_ERR_LAUNCH;
-    mxf4_ffn_kernel<NT><<<grid, kThreadsGemm, C::kBytes, st>>>(p);
+    if (launch_pdl(mxf4_ffn_kernel<NT>, dim3(grid), dim3(kThreadsGemm), (size_t)C::kBytes, st, p) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
     note_launch(1);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+    return MOE_OK;
 }
 
 static int launch_ffn_nt(int NT, const FfnParams& p, int grid, cudaStream_t st) {
@@ -884,8 +920,10 @@ int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16
     const int d = m->d, k = m->top_k, R = T * k;
     const int NT = nt_for(R);
     const int qwarps = NT * (d / 32);
-    quantize_tiles_kernel<<<(qwarps + 7) / 8, 256, 0, st>>>(x, nullptr, nullptr, nullptr, m->num_experts, k, T, d, NT,
-                                                          b.xq, b.xsf, b.zero, (int)b.nzero);
+    if (launch_pdl(quantize_tiles_kernel, dim3((qwarps + 7) / 8), dim3(256), 0, st, x, (const int32_t*)nullptr,
+                   (const int32_t*)nullptr, (const int32_t*)nullptr, m->num_experts, k, T, d, NT, b.xq, b.xsf, b.zero,
+                   (int)b.nzero) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
     note_launch(1);
     FfnParams p = ffn_params(m, ar, T, slot, status, b);
     p.regime = kRegimeDecode;

@@ -11,11 +11,13 @@
 //
 // How the device reaches the exact set without computing every exact logit:
 //  1. a fast logit D with an error bound delta, |D - exact| <= delta:
-//     decode (T <= 16): each lane sums its bf16 products (exact in fp32) with TwoSum
-//       compensation (Ogita, Rump, Oishi, "Accurate sum and dot product", SIAM J. Sci.
-//       Comput. 26(6), 2005, Sum2), the lanes' (sum, compensation) pairs are added in fp64:
-//       delta = (gamma_(c-1) + gamma_m^2 + 2^-49) * sum|x_k w_k| + d 2^-147, with c products
-//       per plain FMA chunk and m chunks per lane (a few 1e-9 at d = 5120);
+//     decode (T <= 16): each lane sums its bf16 products (exact in fp32) in chunks of c
+//       products, the chunks with TwoSum compensation (Ogita, Rump, Oishi, "Accurate sum and
+//       dot product", SIAM J. Sci. Comput. 26(6), 2005, Sum2) along 8/c independent chains of
+//       m = d/256 chunks; chains and lanes are then added as (sum, compensation) pairs with
+//       TwoSum in fp32:
+//       delta = (gamma_(c-1) + gamma_m^2 + 2^-34) * sum|x_k w_k| * (1 + 2^-9) + d 2^-147,
+//       the 2^-34 term covering the pair additions (a few 1e-9 at d = 5120);
 //     prefill: fp32 FMA chains with at most L roundings on any path,
 //       delta = gamma_L * ||x|| ||w|| (Cauchy-Schwarz), inflated by 2^-10 for the norms;
 //  2. [D - delta, D + delta] rounded outward to fp32 holds l32; through the monotone
@@ -47,8 +49,7 @@ struct RouteArgs {
     float* xnorm;      // [T]   (prefill bound)
     float* wnorm;      // [E]   (prefill bound)
     unsigned* counter;
-    float bound_coef;  // prefill: gamma_L * (1 + 2^-10)
-    double g1, g2;     // decode: gamma_(c-1) and gamma_m^2 (fp32 unit roundoff)
+    float bound_coef;  // prefill: gamma_L * (1 + 2^-10); decode: gamma_(c-1) + gamma_m^2 + 2^-34
 };
 
 // ------------------------------------------------------------------ exact logit (Kulisch)
@@ -141,11 +142,11 @@ __device__ __forceinline__ float sigmoid_exact32(float l32) {
     return __double2float_rn(1.0 / (1.0 + exp(-(double)l32)));
 }
 
-// Key record of expert e from a point logit and an fp32 interval [lo, hi] holding l32.
-__device__ __forceinline__ float4 make_key(const RouteArgs& a, int e, float lf, float lo, float hi) {
+// Key record of expert e from a point logit and an fp32 interval [lo, hi] holding l32
+// (table entry tb and bias b of the expert passed in).
+__device__ __forceinline__ float4 make_key(int tb, float b, float lf, float lo, float hi) {
     const float NEG_INF = -__int_as_float(0x7f800000);
-    if (a.table[e] < 0) return make_float4(NEG_INF, NEG_INF, NEG_INF, -1.0f);
-    const float b = a.bias ? a.bias[e] : 0.0f;
+    if (tb < 0) return make_float4(NEG_INF, NEG_INF, NEG_INF, -1.0f);
     const float margin = 1.0f / 2097152.0f;   // 2^-21
     const float sv = sigmoid_fast(lf);
     return make_float4(sv + b, __fadd_rd(__fsub_rd(sigmoid_fast(lo), margin), b),
@@ -170,65 +171,90 @@ __device__ __forceinline__ void warp_best(float& k, int& e) {
     }
 }
 
-// One warp selects the experts of token t from its key records.  EPL = experts per lane
-// (E <= 32 * EPL); expert e = lane + 32 m.
-template <int EPL>
-__device__ void select_token(const RouteArgs& a, int t, int lane) {
+// Shared-memory bytes of one selecting warp: E key records, E exact keys and 64 words for
+// the chosen experts.
+__host__ __device__ inline size_t select_smem_per_warp(int E) { return ((size_t)E * 20 + 256 + 15) / 16 * 16; }
+
+// Order-preserving map of a float key to uint32 (every non-NaN key maps above 0, so 0 means
+// "no candidate"), and its inverse.
+__device__ __forceinline__ uint32_t key_order(float k) {
+    const uint32_t u = __float_as_uint(k);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+
+// One warp selects the experts of token t.  rec (E records), exk (E floats) and out (64
+// words) are this warp's shared memory; lane l owns experts e = l + 32 m (m < ceil(E/32) <=
+// 32), bit m of its masks.  A top-k round is two warp reductions (largest key, then lowest
+// id among equal keys); only the winning lane rescans its experts.
+__device__ __noinline__ void select_token(const RouteArgs& a, int t, int lane, float4* rec, float* exk, int* out) {
     const float NEG_INF = -__int_as_float(0x7f800000);
-    const float4* krow = a.keys + (size_t)t * a.E;
-    float4 kr[EPL];
+    const int E = a.E, EPL = (E + 31) >> 5;
+    const float4* krow = a.keys + (size_t)t * E;
+    uint32_t valid = 0, picked = 0, best_u = 0;
+    int best_m = -1;
+    for (int m0 = 0; m0 < EPL; m0 += 4) {
+        float4 v[4];
 #pragma unroll
-    for (int m = 0; m < EPL; ++m) {
-        const int e = lane + 32 * m;
-        kr[m] = (e < a.E) ? __ldcg(krow + e) : make_float4(NEG_INF, NEG_INF, NEG_INF, -1.0f);
-    }
-    float sv[EPL], exk[EPL];
-    uint32_t valid = 0, picked = 0;
+        for (int u = 0; u < 4; ++u) {
+            const int e = lane + 32 * (m0 + u);
+            v[u] = (m0 + u < EPL && e < E) ? __ldcg(krow + e) : make_float4(NEG_INF, NEG_INF, NEG_INF, -1.0f);
+        }
 #pragma unroll
-    for (int m = 0; m < EPL; ++m) {
-        sv[m] = kr[m].w;
-        exk[m] = NEG_INF;
-        if (kr[m].w >= 0.0f) valid |= 1u << m;
+        for (int u = 0; u < 4; ++u) {
+            const int m = m0 + u, e = lane + 32 * m;
+            if (m < EPL && e < E) {
+                rec[e] = v[u];
+                if (v[u].w >= 0.0f) {
+                    valid |= 1u << m;
+                    const uint32_t ku = key_order(v[u].x);
+                    if (ku > best_u) { best_u = ku; best_m = m; }
+                }
+            }
+        }
     }
-    // S = top-k by point estimate
+    __syncwarp();
+    // S = top-k by point estimate (key desc, id asc)
     int nsel = 0;
     for (int j = 0; j < a.k; ++j) {
-        float bk = NEG_INF;
-        int be = -1;
-#pragma unroll
-        for (int m = 0; m < EPL; ++m)
-            if (((valid & ~picked) >> m) & 1u)
-                if (better(kr[m].x, lane + 32 * m, bk, be)) { bk = kr[m].x; be = lane + 32 * m; }
-        warp_best(bk, be);
-        if (be < 0) break;
-        if ((be & 31) == lane) picked |= 1u << (be >> 5);
+        const uint32_t M = __reduce_max_sync(0xffffffffu, best_u);
+        if (M == 0) break;
+        const uint32_t win = __reduce_min_sync(0xffffffffu, best_u == M ? (uint32_t)(lane + 32 * best_m) : 0xFFFFFFFFu);
+        if ((int)(win & 31) == lane) {
+            picked |= 1u << (win >> 5);
+            best_u = 0;
+            best_m = -1;
+            for (uint32_t r = valid & ~picked; r; r &= r - 1) {
+                const int m = __ffs(r) - 1;
+                const uint32_t ku = key_order(rec[lane + 32 * m].x);
+                if (ku > best_u) { best_u = ku; best_m = m; }
+            }
+        }
         ++nsel;
     }
     if (nsel < a.k && lane == 0) atomicOr(a.status, MOE_STATUS_FEW_RESIDENT);
     // interval thresholds
     float min_lo_in = __int_as_float(0x7f800000), max_hi_out = NEG_INF;
-#pragma unroll
-    for (int m = 0; m < EPL; ++m) {
-        if ((picked >> m) & 1u) min_lo_in = fminf(min_lo_in, kr[m].y);
-        else if ((valid >> m) & 1u) max_hi_out = fmaxf(max_hi_out, kr[m].z);
+    for (uint32_t r = valid; r; r &= r - 1) {
+        const int m = __ffs(r) - 1, e = lane + 32 * m;
+        if ((picked >> m) & 1u) min_lo_in = fminf(min_lo_in, rec[e].y);
+        else max_hi_out = fmaxf(max_hi_out, rec[e].z);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        min_lo_in = fminf(min_lo_in, __shfl_xor_sync(0xffffffffu, min_lo_in, o));
-        max_hi_out = fmaxf(max_hi_out, __shfl_xor_sync(0xffffffffu, max_hi_out, o));
-    }
+    min_lo_in = key_value(__reduce_min_sync(0xffffffffu, key_order(min_lo_in)));
+    max_hi_out = key_value(__reduce_max_sync(0xffffffffu, key_order(max_hi_out)));
     uint32_t certain = 0, uncertain = 0;
-#pragma unroll
-    for (int m = 0; m < EPL; ++m) {
-        bool p = (picked >> m) & 1u, v = (valid >> m) & 1u;
-        if (p && kr[m].y > max_hi_out) certain |= 1u << m;
-        else if (p || (v && kr[m].z >= min_lo_in)) uncertain |= 1u << m;
+    for (uint32_t r = valid; r; r &= r - 1) {
+        const int m = __ffs(r) - 1, e = lane + 32 * m;
+        const bool pk = (picked >> m) & 1u;
+        if (pk && rec[e].y > max_hi_out) certain |= 1u << m;
+        else if (pk || rec[e].z >= min_lo_in) uncertain |= 1u << m;
     }
-    uint32_t final_mask = certain, exact_done = 0;
+    uint32_t final_mask = certain;
     const uint16_t* xt = a.x + (size_t)t * a.d;
     // exact scores (and keys) of the experts in `mask`, one expert at a time by the whole warp
     auto exact_scores = [&](uint32_t mask) {
-#pragma unroll
         for (int m = 0; m < EPL; ++m) {
             uint32_t bal = __ballot_sync(0xffffffffu, (mask >> m) & 1u);
             while (bal) {
@@ -237,91 +263,80 @@ __device__ void select_token(const RouteArgs& a, int t, int lane) {
                 const int e = src + 32 * m;
                 const float s32 = sigmoid_exact32(exact_dot_bf16_warp(xt, a.wr + (size_t)e * a.d, a.d, lane));
                 if (lane == src) {
-                    exk[m] = __fadd_rn(s32, a.bias ? a.bias[e] : 0.0f);
-                    sv[m] = s32;
+                    exk[e] = __fadd_rn(s32, a.bias ? a.bias[e] : 0.0f);
+                    rec[e].w = s32;
                 }
             }
         }
-        exact_done |= mask;
+        __syncwarp();
     };
-    if (warp_sum(__popc(uncertain)) > 0) {
-        const int need = nsel - warp_sum(__popc(certain));
+    if (__any_sync(0xffffffffu, uncertain != 0)) {
+        const int need = nsel - __reduce_add_sync(0xffffffffu, (uint32_t)__popc(certain));
         exact_scores(uncertain);
         uint32_t chosen = 0;
         for (int j = 0; j < need; ++j) {
             float bk = NEG_INF;
             int be = -1;
-#pragma unroll
-            for (int m = 0; m < EPL; ++m)
-                if (((uncertain & ~chosen) >> m) & 1u)
-                    if (better(exk[m], lane + 32 * m, bk, be)) { bk = exk[m]; be = lane + 32 * m; }
-            warp_best(bk, be);
-            if (be < 0) break;
-            if ((be & 31) == lane) chosen |= 1u << (be >> 5);
+            for (uint32_t r = uncertain & ~chosen; r; r &= r - 1) {
+                const int e = lane + 32 * (__ffs(r) - 1);
+                if (be < 0 || exk[e] > bk) { bk = exk[e]; be = e; }
+            }
+            // key desc, id asc over the warp (candidates without a key carry id 0x7FFFFFFF)
+            const uint32_t M = __reduce_max_sync(0xffffffffu, be < 0 ? 0u : key_order(bk));
+            if (M == 0) break;
+            const uint32_t win =
+                __reduce_min_sync(0xffffffffu, (be >= 0 && key_order(bk) == M) ? (uint32_t)be : 0xFFFFFFFFu);
+            if ((int)(win & 31) == lane) chosen |= 1u << (win >> 5);
         }
         final_mask |= chosen;
     }
     // weights: a chosen expert whose key interval is wider than 1e-5 of its score gets its
     // score from the exact logit, so every score has relative error below 1e-5
     uint32_t wide = 0;
-#pragma unroll
-    for (int m = 0; m < EPL; ++m)
-        if (((final_mask & ~exact_done) >> m) & 1u)
-            if (kr[m].z - kr[m].y > 1e-5f * sv[m]) wide |= 1u << m;
-    if (__any_sync(0xffffffffu, wide != 0)) exact_scores(wide);
-    // outputs in ascending expert id: e = lane + 32 m, so m outer, lane inner
-    int32_t slot[EPL];
-#pragma unroll
-    for (int m = 0; m < EPL; ++m) slot[m] = ((final_mask >> m) & 1u) ? a.table[lane + 32 * m] : -1;
-    float sum = 0.0f;
-#pragma unroll
-    for (int m = 0; m < EPL; ++m) {
-        uint32_t bal = __ballot_sync(0xffffffffu, (final_mask >> m) & 1u);
-        while (bal) {
-            const int src = __ffs(bal) - 1;
-            bal &= bal - 1;
-            sum += __shfl_sync(0xffffffffu, sv[m], src);
-        }
+    for (uint32_t r = final_mask & ~uncertain; r; r &= r - 1) {
+        const int m = __ffs(r) - 1, e = lane + 32 * m;
+        if (rec[e].z - rec[e].y > 1e-5f * rec[e].w) wide |= 1u << m;
     }
-    int pos = 0;
+    if (__any_sync(0xffffffffu, wide != 0)) exact_scores(wide);
+    // chosen experts in ascending id (m outer, lane inner) into out[0..n); weight sum in that order
+    int n = 0;
+    const uint32_t below = (1u << lane) - 1u;
+    for (int m = 0; m < EPL; ++m) {
+        const uint32_t bal = __ballot_sync(0xffffffffu, (final_mask >> m) & 1u);
+        if ((final_mask >> m) & 1u) out[n + __popc(bal & below)] = lane + 32 * m;
+        n += __popc(bal);
+    }
+    __syncwarp();
+    float sum = 0.0f;
+    if (lane == 0)
+        for (int i = 0; i < n; ++i) sum += rec[out[i]].w;
+    sum = __shfl_sync(0xffffffffu, sum, 0);
     int32_t* ids = a.ids + (size_t)t * a.k;
     float* wo = a.w + (size_t)t * a.k;
     int32_t* so = a.slots + (size_t)t * a.k;
-#pragma unroll
-    for (int m = 0; m < EPL; ++m) {
-        const uint32_t bal = __ballot_sync(0xffffffffu, (final_mask >> m) & 1u);
-        if ((final_mask >> m) & 1u) {
-            const int idx = pos + __popc(bal & ((1u << lane) - 1u));
-            ids[idx] = lane + 32 * m;
-            wo[idx] = (sum > 0.0f) ? __fdiv_rn(sv[m], sum) : 0.0f;
-            so[idx] = slot[m];
+    for (int j = lane; j < a.k; j += 32) {
+        if (j < n) {
+            const int e = out[j];
+            ids[j] = e;
+            wo[j] = (sum > 0.0f) ? __fdiv_rn(rec[e].w, sum) : 0.0f;
+            so[j] = a.table[e];
+        } else {
+            ids[j] = -1;
+            wo[j] = 0.0f;
+            so[j] = -1;
         }
-        pos += __popc(bal);
     }
-    for (int j = pos + lane; j < a.k; j += 32) {
-        ids[j] = -1;
-        wo[j] = 0.0f;
-        so[j] = -1;
-    }
+    __syncwarp();
 }
 
-template <int EPL>
-__device__ void select_tokens_block(const RouteArgs& a, int t0, int tstep) {
+// Tokens t0, t0 + tstep, ... of one warp; `smem` holds the warp's selection arrays.
+__device__ __forceinline__ void select_tokens(const RouteArgs& a, int t0, int tstep, unsigned char* smem) {
     const int lane = threadIdx.x & 31;
-    for (int t = t0; t < a.T; t += tstep) select_token<EPL>(a, t, lane);
+    float4* rec = reinterpret_cast<float4*>(smem);
+    float* exk = reinterpret_cast<float*>(smem + (size_t)a.E * 16);
+    int* out = reinterpret_cast<int*>(smem + (size_t)a.E * 20);
+    for (int t = t0; t < a.T; t += tstep) select_token(a, t, lane, rec, exk, out);
 }
-
-#define FP4MOE_EPL_DISPATCH(E, ...)                                   \
-    do {                                                              \
-        int epl_ = ((E) + 31) / 32;                                   \
-        if (epl_ <= 2) { constexpr int EPL = 2; __VA_ARGS__; }        \
-        else if (epl_ <= 4) { constexpr int EPL = 4; __VA_ARGS__; }   \
-        else if (epl_ <= 8) { constexpr int EPL = 8; __VA_ARGS__; }   \
-        else if (epl_ <= 12) { constexpr int EPL = 12; __VA_ARGS__; } \
-        else if (epl_ <= 16) { constexpr int EPL = 16; __VA_ARGS__; } \
-        else if (epl_ <= 24) { constexpr int EPL = 24; __VA_ARGS__; } \
-        else { constexpr int EPL = 32; __VA_ARGS__; }                 \
-    } while (0)
 
 // ------------------------------------------------------------------ decode: one warp per expert
 
@@ -336,18 +351,23 @@ constexpr int kDecodeWarps = 4;
 constexpr int kDecodeVec = 20;              // weight vectors (8 bf16) per lane in flight
 constexpr size_t kDecodeSmemMax = 200 * 1024;
 
-// Key records for T <= TB tokens; x rows staged in shared memory.  Lane l of the warp of
-// expert e owns vectors l, l+32, ...; per token it keeps (s, c) of a compensated sum of
-// plain FMA chunks of CH products, and sum|x w|.  The last block to finish selects.
+// Key records for T <= TB tokens; x rows staged in shared memory (reused afterwards by the
+// selection).  Lane l of the warp of expert e owns vectors l, l+32, ...; per token it keeps
+// 8/CH compensated sums (s, c) -- one per plain FMA chunk of CH products of a vector, so the
+// chains are independent -- and sum|x w|.  The last block to finish selects.
 template <int TB, int CH>
 __global__ void __launch_bounds__(kDecodeWarps * 32) route_decode_kernel(RouteArgs a) {
+    constexpr int NCH = 8 / CH;
     extern __shared__ uint4 smem_u4[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.T, d = a.d, E = a.E, nvec = d / 8;
     const int gw = blockIdx.x * kDecodeWarps + warp, nw = gridDim.x * kDecodeWarps;
+    pdl_trigger();   // the next kernel may launch now; it waits for this one before reading anything
     // the first batch of this warp's weights is in flight while x is staged
     uint4 wv[kDecodeVec];
     int e = gw;
+    int tb = -1;
+    float bias_e = 0.0f;
     if (e < E) {
         const uint4* wrow = reinterpret_cast<const uint4*>(a.wr + (size_t)e * d);
 #pragma unroll
@@ -355,14 +375,36 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) route_decode_kernel(RouteAr
             const int c = lane + 32 * b;
             wv[b] = (c < nvec) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
         }
+        tb = a.table[e];
+        bias_e = a.bias ? a.bias[e] : 0.0f;
     }
-    for (int i = tid; i < T * nvec; i += blockDim.x) smem_u4[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+    {
+        const uint4* xg = reinterpret_cast<const uint4*>(a.x);
+        const int n = T * nvec;
+        for (int i0 = tid; i0 < n; i0 += 4 * blockDim.x) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * blockDim.x;
+                if (i < n) v[u] = __ldg(xg + i);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * blockDim.x;
+                if (i < n) smem_u4[i] = v[u];
+            }
+        }
+    }
     __syncthreads();
     for (; e < E; e += nw) {
         const uint4* wrow = reinterpret_cast<const uint4*>(a.wr + (size_t)e * d);
-        float s[TB], c[TB], A[TB];
+        float s[TB][NCH], c[TB][NCH], A[TB];
 #pragma unroll
-        for (int t = 0; t < TB; ++t) s[t] = c[t] = A[t] = 0.f;
+        for (int t = 0; t < TB; ++t) {
+            A[t] = 0.f;
+#pragma unroll
+            for (int q = 0; q < NCH; ++q) s[t][q] = c[t][q] = 0.f;
+        }
         for (int c0 = 0; c0 < nvec; c0 += 32 * kDecodeVec) {
             if (c0 > 0) {
 #pragma unroll
@@ -384,36 +426,56 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) route_decode_kernel(RouteAr
                     const float x8[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
                                          bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
 #pragma unroll
-                    for (int i0 = 0; i0 < 8; i0 += CH) {
-                        float q = __fmul_rn(x8[i0], w8[i0]);
+                    for (int q = 0; q < NCH; ++q) {
+                        const int i0 = q * CH;
+                        float qs = __fmul_rn(x8[i0], w8[i0]);
 #pragma unroll
-                        for (int i = i0 + 1; i < i0 + CH; ++i) q = __fmaf_rn(x8[i], w8[i], q);
+                        for (int i = i0 + 1; i < i0 + CH; ++i) qs = __fmaf_rn(x8[i], w8[i], qs);
                         float err;
-                        two_sum(s[t], q, s[t], err);
-                        c[t] = __fadd_rn(c[t], err);
-#pragma unroll
-                        for (int i = i0; i < i0 + CH; ++i) A[t] = __fmaf_rn(fabsf(x8[i]), fabsf(w8[i]), A[t]);
+                        two_sum(s[t][q], qs, s[t][q], err);
+                        c[t][q] = __fadd_rn(c[t][q], err);
                     }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) A[t] = __fmaf_rn(fabsf(x8[i]), fabsf(w8[i]), A[t]);
                 }
             }
         }
-        // per token: D = sum over lanes of (s + c) in fp64, Asum = sum|x w|; lane t keeps token t
-        double myD = 0.0, myA = 0.0;
+        // per token: (S, C) = sum over chains and lanes of (s + c) as TwoSum pairs, As =
+        // sum|x w| (rounded up across lanes); every lane ends with the same values, lane t
+        // keeps token t
+        float myS = 0.f, myC = 0.f, myA = 0.f;
 #pragma unroll
         for (int t = 0; t < TB; ++t) {
             if (t >= T) break;
-            const double D = warp_sum((double)s[t] + (double)c[t]);
-            const double As = warp_sum((double)A[t]);
-            if (lane == t) { myD = D; myA = As; }
+            float S = s[t][0], Cc = c[t][0];
+#pragma unroll
+            for (int q = 1; q < NCH; ++q) {
+                float err;
+                two_sum(S, s[t][q], S, err);
+                Cc = __fadd_rn(Cc, __fadd_rn(c[t][q], err));
+            }
+            float As = A[t];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float S2 = __shfl_xor_sync(0xffffffffu, S, o), C2 = __shfl_xor_sync(0xffffffffu, Cc, o);
+                float err;
+                two_sum(S, S2, S, err);
+                Cc = __fadd_rn(__fadd_rn(Cc, C2), err);
+                As = __fadd_ru(As, __shfl_xor_sync(0xffffffffu, As, o));
+            }
+            if (lane == t) { myS = S; myC = Cc; myA = As; }
         }
         if (lane < T) {
-            // |D - exact| <= (g1 + g2 + 2^-49) * sum|x w| * (1 + 2^-9) + d * 2^-147
-            const double coef = __dadd_ru(__dadd_ru(a.g1, a.g2), 1.7763568394002505e-15);
-            double delta = __dmul_ru(__dmul_ru(coef, myA), 1.001953125);
-            delta = __dadd_ru(delta, (double)d * 5.605193857299268e-45);
-            const float lo = __double2float_rd(__dsub_rd(myD, delta));
-            const float hi = __double2float_ru(__dadd_ru(myD, delta));
-            a.keys[(size_t)lane * E + e] = make_key(a, e, __double2float_rn(myD), lo, hi);
+            // |S + C - exact| <= coef * sum|x w| * (1 + 2^-9) + d * 2^-147
+            float delta = __fmul_ru(__fmul_ru(a.bound_coef, myA), 1.001953125f);
+            delta = __fadd_ru(delta, (float)d * 5.605193857299268e-45f);
+            const float lo = __fadd_rd(myS, __fsub_rd(myC, delta));
+            const float hi = __fadd_ru(myS, __fadd_ru(myC, delta));
+            a.keys[(size_t)lane * E + e] = make_key(tb, bias_e, __fadd_rn(myS, myC), lo, hi);
+        }
+        if (e + nw < E) {
+            tb = a.table[e + nw];
+            bias_e = a.bias ? a.bias[e + nw] : 0.0f;
         }
     }
     // completion ticket: the last block to arrive selects for every token
@@ -427,7 +489,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) route_decode_kernel(RouteAr
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    FP4MOE_EPL_DISPATCH(E, select_tokens_block<EPL>(a, warp, kDecodeWarps));
+    select_tokens(a, warp, kDecodeWarps,
+                  reinterpret_cast<unsigned char*>(smem_u4) + (size_t)warp * select_smem_per_warp(E));
     __syncthreads();
     if (tid == 0) atomicExch(a.counter, 0u);
 }
@@ -517,15 +580,17 @@ __global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
             const float l = tot[i][j];
             float delta = fmaf(a.bound_coef * xn, __ldg(a.wnorm + e), 7.5e-37f);
             delta = __fmul_ru(delta, 1.0f + 1.0f / 1048576.0f);
-            a.keys[(size_t)t * a.E + e] = make_key(a, e, l, __fsub_rd(l, delta), __fadd_ru(l, delta));
+            a.keys[(size_t)t * a.E + e] =
+                make_key(a.table[e], a.bias ? a.bias[e] : 0.0f, l, __fsub_rd(l, delta), __fadd_ru(l, delta));
         }
     }
 }
 
-template <int EPL>
 __global__ void __launch_bounds__(128) route_select_kernel(RouteArgs a) {
+    extern __shared__ unsigned char sel_smem[];
+    const int warp = threadIdx.x >> 5;
     const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
-    select_tokens_block<EPL>(a, gw, nw);
+    select_tokens(a, gw, nw, sel_smem + (size_t)warp * select_smem_per_warp(a.E));
 }
 
 // ------------------------------------------------------------------ host side
@@ -540,14 +605,16 @@ static float gamma_coef(int L) { return (float)(gamma32(L) * (1.0 + 1.0 / 1024.0
 
 template <int TB, int CH>
 static int launch_decode_tb(RouteArgs a, cudaStream_t st) {
-    const size_t smem = (size_t)a.T * a.d * 2;
+    size_t smem = (size_t)a.T * a.d * 2;
+    const size_t sel = kDecodeWarps * select_smem_per_warp(a.E);
+    if (sel > smem) smem = sel;
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(route_decode_kernel<TB, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
         return MOE_ERR_LAUNCH;
-    const int m = a.d / 32 / CH;   // compensated steps per lane
-    a.g1 = gamma32(CH - 1);
-    a.g2 = gamma32(m) * gamma32(m);
+    const int m = a.d / 256;    // compensated steps per chain and lane
+    const double coef = gamma32(CH - 1) + gamma32(m) * gamma32(m) + 1.0 / 17179869184.0;   // + 2^-34
+    a.bound_coef = (float)(coef * (1.0 + 1.0 / 4096.0));                                   // rounded up
     const int blocks = (a.E + kDecodeWarps - 1) / kDecodeWarps;
     route_decode_kernel<TB, CH><<<blocks, kDecodeWarps * 32, smem, st>>>(a);
     note_launch(1);
@@ -571,7 +638,11 @@ static int launch_route_args(RouteArgs& a, cudaStream_t st) {
     dim3 grid((a.E + kTileE - 1) / kTileE, (a.T + kTileT - 1) / kTileT);
     route_tiled_kernel<<<grid, 256, 0, st>>>(a);
     const int sel_blocks = (a.T + 3) / 4;
-    FP4MOE_EPL_DISPATCH(a.E, route_select_kernel<EPL><<<sel_blocks, 128, 0, st>>>(a));
+    const size_t sel = 4 * select_smem_per_warp(a.E);
+    if (sel > 48 * 1024 &&
+        cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
+    route_select_kernel<<<sel_blocks, 128, sel, st>>>(a);
     note_launch(3);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }

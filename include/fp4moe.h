@@ -29,6 +29,11 @@
  *  - Device-side conditions are OR-ed into *dev_status (an int32 the caller zeroes and reads
  *    after its own synchronisation): MOE_STATUS_* bits below.
  *  - Calls on different streams are independent when given different workspaces.
+ *  - Some kernels are launched with programmatic dependent launch: they may become resident
+ *    while the previous kernel on `stream` still runs, but read nothing before that kernel
+ *    has completed, so stream order keeps its usual meaning.
+ *  - After a call that set MOE_STATUS_TIMEOUT the workspace must be re-initialised
+ *    (moe_workspace_init) before its next use.
  */
 #ifndef FP4MOE_H
 #define FP4MOE_H
@@ -147,7 +152,13 @@ int moe_permute(const moe_dims* dims, int32_t T, const int32_t* topk_ids, int32_
  * (group_offsets/row_src/row_dst from moe_permute of the same topk_ids).
  * flags = MOE_FUSE_COMBINE: writes y bf16 [T, d] (rows_out may be NULL).
  * flags = 0: writes rows_out fp32 [T*k, d] (row r = z for row_src[r], unweighted); y unused.
- * Slots outside [0, num_slots) set MOE_STATUS_BAD_SLOT and contribute zero. */
+ * Slots outside [0, num_slots) set MOE_STATUS_BAD_SLOT and contribute zero.
+ * Decode (T <= 16 with MOE_FUSE_COMBINE) needs only the routing outputs; the permutation
+ * arguments may be NULL there.  The tensor-core path (the default) feeds x and h to the MMA
+ * as a sum of four MXFP4 terms each (e2m1 codes, UE8M0 scale per 32 elements, every term
+ * quantising the previous terms' residual); its expert outputs match exact fp4 x bf16
+ * products to about 1e-4 relative before the bf16 rounding of y.  The tensor-core path takes
+ * decode calls with T*k <= 64; other decode calls use the CUDA-core kernels. */
 int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, const uint16_t* x,
                        const int32_t* topk_ids, const int32_t* topk_slot, const float* topk_w,
                        const int32_t* group_offsets, const int32_t* row_src, const int32_t* row_dst,
