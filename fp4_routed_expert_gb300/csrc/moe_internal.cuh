@@ -72,6 +72,12 @@ inline bool dims_ok(const moe_dims* m) {
            m->top_k <= kMaxTopK && m->top_k <= m->num_experts && m->d <= 65536 && m->f <= 65536;
 }
 
+// Counters inside the counter section (zeroed by moe_workspace_init; every user leaves them
+// zero again): the decode FFN kernel's work list, x-ready, exit ticket, per-key readiness
+// (kMaxDecodeKeys) and per-block y counts (d/128 <= 512).
+enum { kCtrRoute = 0, kCtrFfnWork = 64, kCtrFfnXReady = 65, kCtrFfnExit = 66, kCtrFfnReady = 128,
+       kCtrFfnY = 256, kCounterWords = 1024 };
+
 // Workspace sections, each 256-byte aligned.  The persistent counters come first so that
 // their offset is the same for every token count; the other sections are per call.
 struct WsLayout {
@@ -97,7 +103,7 @@ inline WsLayout ws_layout(const moe_dims* m, int T_max) {
     WsLayout w;
     size_t o = 0;
     size_t T = (size_t)(T_max > 0 ? T_max : 1), E = (size_t)m->num_experts, k = (size_t)m->top_k;
-    w.counter = o; o = align256(o + 4 * 64);     // first: its offset must not depend on T
+    w.counter = o; o = align256(o + 4 * kCounterWords);   // first: its offset must not depend on T
     w.keys = o;    o = align256(o + 16 * T * E);
     w.xnorm = o;   o = align256(o + 4 * T);
     w.wnorm = o;   o = align256(o + 4 * E);
@@ -110,8 +116,6 @@ inline WsLayout ws_layout(const moe_dims* m, int T_max) {
     return w;
 }
 
-// Counters inside the counter section.
-enum { kCtrRoute = 0, kCtrDecodeUp = 1 };
 
 // ---------------------------------------------------------------------------- device helpers
 
@@ -165,6 +169,43 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// mbarrier and bulk-copy wrappers (PTX).  Every wait is bounded by kSpinLimit polls.
+constexpr unsigned kSpinLimit = 1u << 25;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(done)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return done != 0;
+}
+// Bounded wait: false after kSpinLimit polls or once another warp has aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    for (unsigned i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if ((i & 1023u) == 1023u && *abort_flag) return false;
+    }
+    return false;
+}
+// Contiguous global->shared bulk copy completing on an mbarrier (16-byte aligned, size a
+// multiple of 16).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 template <typename T>
 __device__ __forceinline__ T warp_sum(T v) {
 #pragma unroll

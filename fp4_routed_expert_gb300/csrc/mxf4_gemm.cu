@@ -34,7 +34,6 @@ constexpr int kBM = 128;              // weight rows per tile
 constexpr int kKB = 256;              // K elements per stage
 constexpr int kKBytes = 128;          // code bytes per row per stage
 constexpr int kThreadsGemm = 6 * 32;
-constexpr unsigned kSpinLimit = 1u << 25;
 constexpr int kTmemCols = 512;
 constexpr int kSfRing = 2;
 constexpr int kPrefillNT = 32;           // activation rows per tile (prefill)
@@ -45,40 +44,6 @@ enum { kRegimeDecode = 0, kRegimePrefill = 1 };
 
 // ------------------------------------------------------------------ PTX wrappers
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-                 : "=r"(done)
-                 : "r"(bar), "r"(parity)
-                 : "memory");
-    return done != 0;
-}
-// Bounded wait: false after kSpinLimit polls or once another warp has aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    for (unsigned i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try(bar, parity)) return true;
-        if ((i & 1023u) == 1023u && *abort_flag) return false;
-    }
-    return false;
-}
-// Contiguous global->shared bulk copy completing on an mbarrier (16-byte aligned, size a
-// multiple of 16).
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -287,6 +252,11 @@ struct FfnParams {
     int32_t* work;                   // next unit to hand out (zero at launch)
     int32_t* ready;                  // phase 0 units finished, per key (decode: slot ordinal; prefill: tile)
     int32_t* ycnt;                   // decode: pair rows finished per 128-feature block of y
+    // decode: x is quantised by this kernel into ph[0].b_q / b_sf (NT-row tile), CTAs counted
+    // in xready; the last CTA to exit (exit ticket) clears every counter for the next call
+    const uint16_t* x_src;
+    int32_t* xready;
+    int32_t* exit_ctr;
 };
 
 // Work list: units [0, n0) are gate/up units, [n0, n0 + n1) down units, n_i = n_keys x
@@ -483,6 +453,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
         // ---------------- producer: takes units, four contiguous bulk copies per stage
         if (lane == 0) {
             int stage = 0, ready_key = -1;
+            bool x_ok = (p.x_src == nullptr);
             uint32_t phase = 0, issued = 0, issued_parity = 0;   // per-stage bit masks
             while (true) {
                 int unit = *abortp ? -1 : atomicAdd(p.work, 1);
@@ -501,9 +472,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 UnitInfo u;
                 const bool ok = unit_info<NT>(p, P, ph ? unit - n0 : unit, uslots, u);
                 const uint8_t* sbase = p.arena + (int64_t)(ok ? u.slot : 0) * p.slot_bytes;
-                // A down unit whose key is not ready yet gets its weight copies issued into every
-                // free stage; the h copies of those stages follow once the key is ready.
-                bool have_b = !(ph == 1 && ok && u.key != ready_key);
+                // A unit whose activations are not ready yet (gate/up: x still being quantised by
+                // the CTAs; down: h of its key) gets its weight copies issued into every free
+                // stage; the activation copies of those stages follow once they are ready.
+                bool have_b = (ph == 0) ? x_ok : !(ok && u.key != ready_key);
                 int pend_n = 0, pend_kb0 = 0, pend_stage0 = 0;
                 auto issue_b = [&](int kb, int stg) {
                     const uint32_t sb = smem_u32(stage_base + stg * C::kStage);
@@ -517,9 +489,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     pend_n = 0;
                 };
                 auto key_ready = [&](bool block) -> bool {
-                    // h rows of this key: every gate/up unit of the key has written them
+                    // gate/up: every CTA has quantised its share of x; down: every gate/up unit
+                    // of the key has written its h rows
+                    const int32_t* flag = (ph == 0) ? p.xready : p.ready + u.key;
+                    const int target = (ph == 0) ? (int)gridDim.x : p.ph[0].mtiles;
                     unsigned spins = 0;
-                    while (ld_acquire(p.ready + u.key) < p.ph[0].mtiles) {
+                    while (ld_acquire(flag) < target) {
                         if (!block) return false;
                         if (++spins > kSpinLimit || *abortp) {
                             atomicOr(p.status, MOE_STATUS_TIMEOUT);
@@ -529,7 +504,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                         __nanosleep(64);
                     }
                     fence_proxy_async();
-                    ready_key = u.key;
+                    if (ph == 0) x_ok = true;
+                    else ready_key = u.key;
                     have_b = true;
                     return true;
                 };
@@ -671,6 +647,39 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
             last = ok1 && fix_last;
             return ok1;
         };
+        if (p.x_src) {
+            // x -> kTerms MXFP4 terms in the NT-row activation tile, one warp per (row,
+            // 32-element block); rows >= T are zero.  Then count this CTA in xready.
+            const int nblk = p.d / 32, KBd = p.d / kKB;
+            const int total = NT * nblk;
+            for (int job = blockIdx.x * 4 + ew; job < total; job += gridDim.x * 4) {
+                const int r = job / nblk, b = job % nblk, kb = b / 8, j = b % 8;
+                uint8_t* q = const_cast<uint8_t*>(p.ph[0].b_q);
+                uint8_t* sf = const_cast<uint8_t*>(p.ph[0].b_sf);
+                if (r >= p.T) {
+                    if (lane < kTerms) {
+                        *reinterpret_cast<uint4*>(q + act_code_off(0, kb, lane, r, j, NT, KBd)) = make_uint4(0, 0, 0, 0);
+                        sf[act_scale_off(0, kb, lane, r, j, NT, KBd)] = 0;
+                    }
+                    continue;
+                }
+                uint4 codes[kTerms];
+                uint32_t scales[kTerms];
+                warp_quantize32(bf16_to_f32(p.x_src[(size_t)r * p.d + 32 * b + lane]), lane, codes, scales);
+                if (lane < kTerms) {
+                    uint4 cv = codes[0];
+                    uint32_t sv = scales[0];
+#pragma unroll
+                    for (int t = 1; t < kTerms; ++t)
+                        if (lane == t) { cv = codes[t]; sv = scales[t]; }
+                    *reinterpret_cast<uint4*>(q + act_code_off(0, kb, lane, r, j, NT, KBd)) = cv;
+                    sf[act_scale_off(0, kb, lane, r, j, NT, KBd)] = (uint8_t)sv;
+                }
+            }
+            fence_proxy_async();   // read by the async proxy (bulk copies) of every CTA
+            bool unused;
+            count_arrival(p.xready, 1, (int)gridDim.x, unused);
+        }
         while (true) {
             int unit = -1;
             if (mbar_wait(smem_u32(&uqfull[qi]), qphase, abortp)) unit = uq[qi];
@@ -802,6 +811,25 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     __syncthreads();
     tc_fence_after();
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    if (p.exit_ctr) {
+        // the last CTA to leave clears the counters for the next call
+        __shared__ int last_cta;
+        if (tid == 0) {
+            __threadfence();
+            last_cta = (atomicAdd(p.exit_ctr, 1) == (int)gridDim.x - 1);
+        }
+        __syncthreads();
+        if (last_cta) {
+            __threadfence();
+            for (int i = tid; i < n_keys; i += blockDim.x) p.ready[i] = 0;
+            for (int i = tid; i < p.d / kBM; i += blockDim.x) p.ycnt[i] = 0;
+            if (tid == 0) {
+                *p.work = 0;
+                *p.xready = 0;
+                *p.exit_ctr = 0;
+            }
+        }
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -909,24 +937,25 @@ static FfnParams ffn_params(const moe_dims* m, const moe_arena* ar, int T, const
     return p;
 }
 
-// Decode regime: x quantised into one tile of NT rows, then one FFN launch (gate/up with
-// SwiGLU and h quantised per (token, j) pair, down to one fp32 row per pair, fixed-order
-// combine into y).
+// Decode regime: one FFN launch (x quantised by the CTAs into one tile of NT rows, gate/up
+// with SwiGLU and h quantised per (token, j) pair, down to one fp32 row per pair,
+// fixed-order combine into y).
 int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                      const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
                      int num_sms) {
     if (T == 0) return MOE_OK;
     TcBuffers b = tc_buffers(m, T, ws, L);
-    const int d = m->d, k = m->top_k, R = T * k;
+    const int k = m->top_k, R = T * k;
     const int NT = nt_for(R);
-    const int qwarps = NT * (d / 32);
-    if (launch_pdl(quantize_tiles_kernel, dim3((qwarps + 7) / 8), dim3(256), 0, st, x, (const int32_t*)nullptr,
-                   (const int32_t*)nullptr, (const int32_t*)nullptr, m->num_experts, k, T, d, NT, b.xq, b.xsf, b.zero,
-                   (int)b.nzero) != cudaSuccess)
-        return MOE_ERR_LAUNCH;
-    note_launch(1);
     FfnParams p = ffn_params(m, ar, T, slot, status, b);
     p.regime = kRegimeDecode;
+    int32_t* ctr = reinterpret_cast<int32_t*>(ws + L.counter);
+    p.work = ctr + kCtrFfnWork;
+    p.xready = ctr + kCtrFfnXReady;
+    p.exit_ctr = ctr + kCtrFfnExit;
+    p.ready = ctr + kCtrFfnReady;
+    p.ycnt = ctr + kCtrFfnY;
+    p.x_src = x;
     p.w = w;
     p.ph[0].decode_cols = T;
     p.ph[1].decode_cols = R;

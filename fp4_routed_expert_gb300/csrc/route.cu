@@ -329,13 +329,183 @@ __device__ __noinline__ void select_token(const RouteArgs& a, int t, int lane, f
     __syncwarp();
 }
 
-// Tokens t0, t0 + tstep, ... of one warp; `smem` holds the warp's selection arrays.
-__device__ __forceinline__ void select_tokens(const RouteArgs& a, int t0, int tstep, unsigned char* smem) {
-    const int lane = threadIdx.x & 31;
-    float4* rec = reinterpret_cast<float4*>(smem);
-    float* exk = reinterpret_cast<float*>(smem + (size_t)a.E * 16);
-    int* out = reinterpret_cast<int*>(smem + (size_t)a.E * 20);
-    for (int t = t0; t < a.T; t += tstep) select_token(a, t, lane, rec, exk, out);
+// One block of 128 threads per token.  Thread i holds experts i, i+128, ... (at most 8).
+// Each warp finds the top-k of its 256.. experts by k rounds of two warp reductions (largest
+// key, then lowest id among equal keys; only the owner of the winner rescans its experts),
+// warp 0 merges the four lists the same way, and every thread checks its experts against
+// the certification thresholds.  A token with an uncertain or wide expert is handed whole to
+// select_token (warp 0).
+constexpr int kSelThreads = 128, kSelItems = 8;   // E <= 1024
+
+__global__ void __launch_bounds__(kSelThreads) route_select_kernel(RouteArgs a) {
+    extern __shared__ unsigned char sel_smem[];   // select_token's arrays (warp 0)
+    __shared__ float4 items[kSelItems][kSelThreads];
+    __shared__ uint32_t c_u[4][32];
+    __shared__ int c_e[4][32];
+    __shared__ float c_s[4][32];
+    __shared__ int S_e[32];
+    __shared__ float S_s[32];
+    __shared__ int S_sorted[32];
+    __shared__ int S_n;
+    __shared__ uint32_t inS[32];                  // bitmap over experts
+    __shared__ uint32_t red_lo[4], red_hi[4];
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = a.E, k = a.k;
+    pdl_trigger();
+    pdl_wait();   // the key records of the logit kernel
+    for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+        const float4* krow = a.keys + (size_t)t * E;
+        {
+            float4 r[kSelItems];
+#pragma unroll
+            for (int i = 0; i < kSelItems; ++i) {
+                const int e = tid + kSelThreads * i;
+                r[i] = (e < E) ? __ldcg(krow + e) : make_float4(NEG_INF, NEG_INF, NEG_INF, -1.0f);
+            }
+#pragma unroll
+            for (int i = 0; i < kSelItems; ++i) items[i][tid] = r[i];
+        }
+        __syncwarp();   // a round's winner's score is read by the lane that records it
+        if (tid < 32) inS[tid] = 0;
+        uint32_t valid = 0;
+#pragma unroll 1
+        for (int i = 0; i < kSelItems; ++i)
+            if (items[i][tid].w >= 0.0f) valid |= 1u << i;
+        // ---- per-warp top-k
+        uint32_t picked = 0, bu = 0;
+        int bi = -1;
+        auto local_best = [&]() {
+            bu = 0;
+            bi = -1;
+#pragma unroll 1
+            for (uint32_t rr = valid & ~picked; rr; rr &= rr - 1) {
+                const int i = __ffs(rr) - 1;
+                const uint32_t ku = key_order(items[i][tid].x);
+                if (ku > bu) { bu = ku; bi = i; }
+            }
+        };
+        local_best();
+        uint32_t my_u = 0;
+        int my_e = -1, nsel = 0;
+        float my_s = 0.f;
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+            const uint32_t M = __reduce_max_sync(0xffffffffu, bu);
+            if (M == 0) break;
+            const uint32_t win = __reduce_min_sync(0xffffffffu, bu == M ? (uint32_t)(tid + kSelThreads * bi) : 0xFFFFFFFFu);
+            if (lane == j) { my_u = M; my_e = (int)win; my_s = items[win / kSelThreads][win % kSelThreads].w; }
+            if ((int)(win % kSelThreads) == tid) {
+                picked |= 1u << bi;
+                local_best();
+            }
+            ++nsel;
+        }
+        c_u[warp][lane] = lane < nsel ? my_u : 0u;
+        c_e[warp][lane] = my_e;
+        c_s[warp][lane] = my_s;
+        __syncthreads();
+        // ---- warp 0 merges: lane l holds candidate l of every warp
+        if (warp == 0) {
+            uint32_t taken = 0;
+            int n = 0;
+#pragma unroll 1
+            for (int j = 0; j < k; ++j) {
+                uint32_t lb = 0;
+                int lq = -1, le = 0x7FFFFFFF;
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t cu = c_u[q][lane];
+                    const int ce = c_e[q][lane];
+                    if (!((taken >> q) & 1u) && cu != 0 && (cu > lb || (cu == lb && ce < le))) { lb = cu; lq = q; le = ce; }
+                }
+                const uint32_t M = __reduce_max_sync(0xffffffffu, lb);
+                if (M == 0) break;
+                const uint32_t win = __reduce_min_sync(0xffffffffu, (lb == M && lq >= 0) ? (uint32_t)le : 0xFFFFFFFFu);
+                if (lb == M && lq >= 0 && (uint32_t)le == win) {
+                    taken |= 1u << lq;
+                    S_e[j] = (int)win;
+                    S_s[j] = c_s[lq][lane];
+                    atomicOr(&inS[win >> 5], 1u << (win & 31));
+                }
+                ++n;
+            }
+            if (lane == 0) S_n = n;
+        }
+        __syncthreads();
+        const int n = S_n;
+        if (n < k && tid == 0) atomicOr(a.status, MOE_STATUS_FEW_RESIDENT);
+        // ---- thresholds: min klo over S, max khi over the other valid experts
+        float lo_in = __int_as_float(0x7f800000), hi_out = NEG_INF;
+        uint32_t inmask = 0;
+#pragma unroll 1
+        for (uint32_t rr = valid; rr; rr &= rr - 1) {
+            const int i = __ffs(rr) - 1, e = tid + kSelThreads * i;
+            const float4 v = items[i][tid];
+            if ((inS[e >> 5] >> (e & 31)) & 1u) { inmask |= 1u << i; lo_in = fminf(lo_in, v.y); }
+            else hi_out = fmaxf(hi_out, v.z);
+        }
+        uint32_t wlo = __reduce_min_sync(0xffffffffu, key_order(lo_in));
+        uint32_t whi = __reduce_max_sync(0xffffffffu, key_order(hi_out));
+        if (lane == 0) { red_lo[warp] = wlo; red_hi[warp] = whi; }
+        __syncthreads();
+        wlo = min(min(red_lo[0], red_lo[1]), min(red_lo[2], red_lo[3]));
+        whi = max(max(red_hi[0], red_hi[1]), max(red_hi[2], red_hi[3]));
+        const float min_lo_in = key_value(wlo), max_hi_out = key_value(whi);
+        // every chosen expert certain, no other expert overlapping, every weight narrow?
+        bool doubt = false;
+#pragma unroll 1
+        for (uint32_t rr = valid; rr; rr &= rr - 1) {
+            const int i = __ffs(rr) - 1;
+            const float4 v = items[i][tid];
+            if ((inmask >> i) & 1u) {
+                if (!(v.y > max_hi_out)) doubt = true;
+                if (v.z - v.y > 1e-5f * v.w) doubt = true;
+            } else if (v.z >= min_lo_in) {
+                doubt = true;
+            }
+        }
+        if (__syncthreads_or(doubt)) {
+            if (warp == 0) {
+                float4* rec = reinterpret_cast<float4*>(sel_smem);
+                float* exk = reinterpret_cast<float*>(sel_smem + (size_t)E * 16);
+                int* out = reinterpret_cast<int*>(sel_smem + (size_t)E * 20);
+                select_token(a, t, lane, rec, exk, out);
+            }
+            __syncthreads();
+            continue;
+        }
+        // ---- outputs: S in ascending id, weights s / sum(s) with the sum in that order
+        if (warp == 0) {
+            if (lane < n) {
+                const int e = S_e[lane];
+                int rank = 0;
+                for (int i = 0; i < n; ++i) rank += (S_e[i] < e);
+                S_sorted[rank] = lane;
+            }
+            __syncwarp();
+            float sum = 0.0f;
+            if (lane == 0)
+                for (int i = 0; i < n; ++i) sum += S_s[S_sorted[i]];
+            sum = __shfl_sync(0xffffffffu, sum, 0);
+            int32_t* ids = a.ids + (size_t)t * k;
+            float* wo = a.w + (size_t)t * k;
+            int32_t* so = a.slots + (size_t)t * k;
+            for (int j = lane; j < k; j += 32) {
+                if (j < n) {
+                    const int c = S_sorted[j], e = S_e[c];
+                    ids[j] = e;
+                    wo[j] = (sum > 0.0f) ? __fdiv_rn(S_s[c], sum) : 0.0f;
+                    so[j] = a.table[e];
+                } else {
+                    ids[j] = -1;
+                    wo[j] = 0.0f;
+                    so[j] = -1;
+                }
+            }
+        }
+        __syncthreads();
+    }
 }
 
 // ------------------------------------------------------------------ decode: one warp per expert
@@ -348,81 +518,68 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& err) 
 }
 
 constexpr int kDecodeWarps = 4;
-constexpr int kDecodeVec = 20;              // weight vectors (8 bf16) per lane in flight
 constexpr size_t kDecodeSmemMax = 200 * 1024;
 
-// Key records for T <= TB tokens; x rows staged in shared memory (reused afterwards by the
-// selection).  Lane l of the warp of expert e owns vectors l, l+32, ...; per token it keeps
-// 8/CH compensated sums (s, c) -- one per plain FMA chunk of CH products of a vector, so the
-// chains are independent -- and sum|x w|.  The last block to finish selects.
-template <int TB, int CH>
+__host__ __device__ inline size_t decode_smem_bytes(int T, int d) {
+    return (size_t)(kDecodeWarps + T) * d * 2 + 16;   // W rows, x rows, one mbarrier
+}
+
+// Key records for T <= 16 tokens.  A block takes kDecodeWarps experts per round: their router
+// rows and (once) the tokens' rows arrive in shared memory by bulk copies, then warp w works
+// on expert e0 + w, one token at a time.  Lane l owns vectors l, l+32, ...; per token it
+// keeps 8/CH compensated sums (s, c) -- one per plain FMA chunk of CH products of a vector, so
+// the chains are independent -- and sum|x w|.  The loops are kept short: this code runs once
+// per call and is seldom in the instruction cache.  The selection kernel follows.
+template <int CH>
 __global__ void __launch_bounds__(kDecodeWarps * 32) route_decode_kernel(RouteArgs a) {
     constexpr int NCH = 8 / CH;
-    extern __shared__ uint4 smem_u4[];
+    extern __shared__ __align__(16) unsigned char dsm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.T, d = a.d, E = a.E, nvec = d / 8;
-    const int gw = blockIdx.x * kDecodeWarps + warp, nw = gridDim.x * kDecodeWarps;
+    uint16_t* ws = reinterpret_cast<uint16_t*>(dsm);
+    const uint16_t* xs = ws + (size_t)kDecodeWarps * d;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(dsm + (size_t)(kDecodeWarps + T) * d * 2);
+    __shared__ int abort_flag;
     pdl_trigger();   // the next kernel may launch now; it waits for this one before reading anything
-    // the first batch of this warp's weights is in flight while x is staged
-    uint4 wv[kDecodeVec];
-    int e = gw;
-    int tb = -1;
-    float bias_e = 0.0f;
-    if (e < E) {
-        const uint4* wrow = reinterpret_cast<const uint4*>(a.wr + (size_t)e * d);
-#pragma unroll
-        for (int b = 0; b < kDecodeVec; ++b) {
-            const int c = lane + 32 * b;
-            wv[b] = (c < nvec) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
-        }
-        tb = a.table[e];
-        bias_e = a.bias ? a.bias[e] : 0.0f;
-    }
-    {
-        const uint4* xg = reinterpret_cast<const uint4*>(a.x);
-        const int n = T * nvec;
-        for (int i0 = tid; i0 < n; i0 += 4 * blockDim.x) {
-            uint4 v[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = i0 + u * blockDim.x;
-                if (i < n) v[u] = __ldg(xg + i);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = i0 + u * blockDim.x;
-                if (i < n) smem_u4[i] = v[u];
-            }
-        }
+    if (tid == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    for (; e < E; e += nw) {
-        const uint4* wrow = reinterpret_cast<const uint4*>(a.wr + (size_t)e * d);
-        float s[TB][NCH], c[TB][NCH], A[TB];
-#pragma unroll
-        for (int t = 0; t < TB; ++t) {
-            A[t] = 0.f;
-#pragma unroll
-            for (int q = 0; q < NCH; ++q) s[t][q] = c[t][q] = 0.f;
+    uint32_t phase = 0;
+    for (int e0 = blockIdx.x * kDecodeWarps; e0 < E; e0 += gridDim.x * kDecodeWarps) {
+        const int nw = min(kDecodeWarps, E - e0);
+        if (tid == 0) {
+            const bool first = (e0 == (int)blockIdx.x * kDecodeWarps);
+            const uint32_t rowb = (uint32_t)d * 2;
+            mbar_expect_tx(smem_u32(bar), rowb * nw + (first ? rowb * T : 0u));
+            if (first) bulk_g2s(smem_u32(xs), a.x, rowb * T, smem_u32(bar));
+            for (int w = 0; w < nw; ++w) bulk_g2s(smem_u32(ws + (size_t)w * d), a.wr + (size_t)(e0 + w) * d, rowb, smem_u32(bar));
         }
-        for (int c0 = 0; c0 < nvec; c0 += 32 * kDecodeVec) {
-            if (c0 > 0) {
-#pragma unroll
-                for (int b = 0; b < kDecodeVec; ++b) {
-                    const int cv = c0 + lane + 32 * b;
-                    wv[b] = (cv < nvec) ? __ldg(wrow + cv) : make_uint4(0, 0, 0, 0);
-                }
+        const int e = e0 + warp;
+        const int tb = (e < E) ? a.table[e] : -1;
+        const float bias_e = (e < E && a.bias) ? a.bias[e] : 0.0f;
+        // bounded wait; the copies are waited for (again bounded) even after a timeout
+        if (!mbar_wait(smem_u32(bar), phase, &abort_flag)) {
+            if (tid == 0) atomicOr(a.status, MOE_STATUS_TIMEOUT);
+            for (unsigned i = 0; i < kSpinLimit && !mbar_try(smem_u32(bar), phase); ++i) {
             }
+        }
+        phase ^= 1u;
+        if (e < E) {
+            const uint4* wrow = reinterpret_cast<const uint4*>(ws + (size_t)warp * d);
+            float myS = 0.f, myC = 0.f, myA = 0.f;
+            for (int t = 0; t < T; ++t) {
+                const uint4* xrow = reinterpret_cast<const uint4*>(xs + (size_t)t * d);
+                float s[NCH], c[NCH], A = 0.f;
 #pragma unroll
-            for (int b = 0; b < kDecodeVec; ++b) {
-                const int cv = c0 + lane + 32 * b;
-                if (cv >= nvec) break;
-                const float w8[8] = {bf16_lo(wv[b].x), bf16_hi(wv[b].x), bf16_lo(wv[b].y), bf16_hi(wv[b].y),
-                                     bf16_lo(wv[b].z), bf16_hi(wv[b].z), bf16_lo(wv[b].w), bf16_hi(wv[b].w)};
-#pragma unroll
-                for (int t = 0; t < TB; ++t) {
-                    if (t >= T) break;
-                    const uint4 xv = smem_u4[(size_t)t * nvec + cv];
+                for (int q = 0; q < NCH; ++q) s[q] = c[q] = 0.f;
+#pragma unroll 2
+                for (int cv = lane; cv < nvec; cv += 32) {
+                    const uint4 wv = wrow[cv], xv = xrow[cv];
+                    const float w8[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
+                                         bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
                     const float x8[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
                                          bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
 #pragma unroll
@@ -432,67 +589,42 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) route_decode_kernel(RouteAr
 #pragma unroll
                         for (int i = i0 + 1; i < i0 + CH; ++i) qs = __fmaf_rn(x8[i], w8[i], qs);
                         float err;
-                        two_sum(s[t][q], qs, s[t][q], err);
-                        c[t][q] = __fadd_rn(c[t][q], err);
+                        two_sum(s[q], qs, s[q], err);
+                        c[q] = __fadd_rn(c[q], err);
                     }
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) A[t] = __fmaf_rn(fabsf(x8[i]), fabsf(w8[i]), A[t]);
+                    for (int i = 0; i < 8; ++i) A = __fmaf_rn(fabsf(x8[i]), fabsf(w8[i]), A);
                 }
+                // (S, C) = sum over chains and lanes of (s + c) as TwoSum pairs, A = sum|x w|
+                // rounded up across lanes; every lane ends with the same values
+                float S = s[0], Cc = c[0];
+#pragma unroll
+                for (int q = 1; q < NCH; ++q) {
+                    float err;
+                    two_sum(S, s[q], S, err);
+                    Cc = __fadd_rn(Cc, __fadd_rn(c[q], err));
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float S2 = __shfl_xor_sync(0xffffffffu, S, o), C2 = __shfl_xor_sync(0xffffffffu, Cc, o);
+                    float err;
+                    two_sum(S, S2, S, err);
+                    Cc = __fadd_rn(__fadd_rn(Cc, C2), err);
+                    A = __fadd_ru(A, __shfl_xor_sync(0xffffffffu, A, o));
+                }
+                if (lane == t) { myS = S; myC = Cc; myA = A; }
+            }
+            if (lane < T) {
+                // |S + C - exact| <= coef * sum|x w| * (1 + 2^-9) + d * 2^-147
+                float delta = __fmul_ru(__fmul_ru(a.bound_coef, myA), 1.001953125f);
+                delta = __fadd_ru(delta, (float)d * 5.605193857299268e-45f);
+                const float lo = __fadd_rd(myS, __fsub_rd(myC, delta));
+                const float hi = __fadd_ru(myS, __fadd_ru(myC, delta));
+                a.keys[(size_t)lane * E + e] = make_key(tb, bias_e, __fadd_rn(myS, myC), lo, hi);
             }
         }
-        // per token: (S, C) = sum over chains and lanes of (s + c) as TwoSum pairs, As =
-        // sum|x w| (rounded up across lanes); every lane ends with the same values, lane t
-        // keeps token t
-        float myS = 0.f, myC = 0.f, myA = 0.f;
-#pragma unroll
-        for (int t = 0; t < TB; ++t) {
-            if (t >= T) break;
-            float S = s[t][0], Cc = c[t][0];
-#pragma unroll
-            for (int q = 1; q < NCH; ++q) {
-                float err;
-                two_sum(S, s[t][q], S, err);
-                Cc = __fadd_rn(Cc, __fadd_rn(c[t][q], err));
-            }
-            float As = A[t];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float S2 = __shfl_xor_sync(0xffffffffu, S, o), C2 = __shfl_xor_sync(0xffffffffu, Cc, o);
-                float err;
-                two_sum(S, S2, S, err);
-                Cc = __fadd_rn(__fadd_rn(Cc, C2), err);
-                As = __fadd_ru(As, __shfl_xor_sync(0xffffffffu, As, o));
-            }
-            if (lane == t) { myS = S; myC = Cc; myA = As; }
-        }
-        if (lane < T) {
-            // |S + C - exact| <= coef * sum|x w| * (1 + 2^-9) + d * 2^-147
-            float delta = __fmul_ru(__fmul_ru(a.bound_coef, myA), 1.001953125f);
-            delta = __fadd_ru(delta, (float)d * 5.605193857299268e-45f);
-            const float lo = __fadd_rd(myS, __fsub_rd(myC, delta));
-            const float hi = __fadd_ru(myS, __fadd_ru(myC, delta));
-            a.keys[(size_t)lane * E + e] = make_key(tb, bias_e, __fadd_rn(myS, myC), lo, hi);
-        }
-        if (e + nw < E) {
-            tb = a.table[e + nw];
-            bias_e = a.bias ? a.bias[e + nw] : 0.0f;
-        }
+        __syncthreads();   // the next round's copies overwrite the router rows
     }
-    // completion ticket: the last block to arrive selects for every token
-    __shared__ int is_last;
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        const unsigned tk = atomicAdd(a.counter, 1u);
-        is_last = (tk == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
-    select_tokens(a, warp, kDecodeWarps,
-                  reinterpret_cast<unsigned char*>(smem_u4) + (size_t)warp * select_smem_per_warp(E));
-    __syncthreads();
-    if (tid == 0) atomicExch(a.counter, 0u);
 }
 
 // ------------------------------------------------------------------ large T: tiled logits
@@ -586,13 +718,6 @@ __global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
     }
 }
 
-__global__ void __launch_bounds__(128) route_select_kernel(RouteArgs a) {
-    extern __shared__ unsigned char sel_smem[];
-    const int warp = threadIdx.x >> 5;
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
-    select_tokens(a, gw, nw, sel_smem + (size_t)warp * select_smem_per_warp(a.E));
-}
-
 // ------------------------------------------------------------------ host side
 
 // gamma_n = n u / (1 - n u), u = 2^-24
@@ -603,48 +728,52 @@ static double gamma32(int n) {
 
 static float gamma_coef(int L) { return (float)(gamma32(L) * (1.0 + 1.0 / 1024.0)); }
 
-template <int TB, int CH>
-static int launch_decode_tb(RouteArgs a, cudaStream_t st) {
-    size_t smem = (size_t)a.T * a.d * 2;
-    const size_t sel = kDecodeWarps * select_smem_per_warp(a.E);
-    if (sel > smem) smem = sel;
+// Selection: one block per token, launched behind the key-record kernel.
+static int launch_select(const RouteArgs& a, cudaStream_t st) {
+    const size_t sel = select_smem_per_warp(a.E);
+    if (sel > 48 * 1024 &&
+        cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
+    const int grid = a.T < 4096 ? a.T : 4096;
+    if (launch_pdl(route_select_kernel, dim3(grid), dim3(kSelThreads), sel, st, a) != cudaSuccess) return MOE_ERR_LAUNCH;
+    note_launch(1);
+    return MOE_OK;
+}
+
+template <int CH>
+static int launch_decode_ch(RouteArgs a, cudaStream_t st, int num_sms) {
+    const size_t smem = decode_smem_bytes(a.T, a.d);
     if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(route_decode_kernel<TB, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
+        cudaFuncSetAttribute(route_decode_kernel<CH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MOE_ERR_LAUNCH;
     const int m = a.d / 256;    // compensated steps per chain and lane
     const double coef = gamma32(CH - 1) + gamma32(m) * gamma32(m) + 1.0 / 17179869184.0;   // + 2^-34
     a.bound_coef = (float)(coef * (1.0 + 1.0 / 4096.0));                                   // rounded up
-    const int blocks = (a.E + kDecodeWarps - 1) / kDecodeWarps;
-    route_decode_kernel<TB, CH><<<blocks, kDecodeWarps * 32, smem, st>>>(a);
+    int blocks = (a.E + kDecodeWarps - 1) / kDecodeWarps;
+    if (num_sms > 0 && blocks > num_sms) blocks = num_sms;
+    route_decode_kernel<CH><<<blocks, kDecodeWarps * 32, smem, st>>>(a);
     note_launch(1);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_LAUNCH;
+    return launch_select(a, st);
 }
 
 // Router launches for RouteArgs with every pointer set: the decode kernel when the tokens'
 // rows fit in shared memory, else norms -> tiled logits -> selection.
-static int launch_route_args(RouteArgs& a, cudaStream_t st) {
+static int launch_route_args(RouteArgs& a, cudaStream_t st, int num_sms) {
     if (a.T == 0) return MOE_OK;
-    if (a.T <= kDecodeMaxT && (size_t)a.T * a.d * 2 <= kDecodeSmemMax) {
-        if (a.T == 1) return launch_decode_tb<1, 1>(a, st);
-        if (a.T == 2) return launch_decode_tb<2, 1>(a, st);
-        if (a.T <= 4) return launch_decode_tb<4, 2>(a, st);
-        if (a.T <= 8) return launch_decode_tb<8, 4>(a, st);
-        return launch_decode_tb<16, 4>(a, st);
+    if (a.T <= kDecodeMaxT && decode_smem_bytes(a.T, a.d) <= kDecodeSmemMax) {
+        if (a.T <= 2) return launch_decode_ch<1>(a, st, num_sms);
+        if (a.T <= 4) return launch_decode_ch<2>(a, st, num_sms);
+        return launch_decode_ch<4>(a, st, num_sms);
     }
     a.bound_coef = gamma_coef(kChunkK + (a.d + kChunkK - 1) / kChunkK + 1);
     const int rows = a.T + a.E;
     route_norms_kernel<<<(rows + 7) / 8, 256, 0, st>>>(a);
     dim3 grid((a.E + kTileE - 1) / kTileE, (a.T + kTileT - 1) / kTileT);
     route_tiled_kernel<<<grid, 256, 0, st>>>(a);
-    const int sel_blocks = (a.T + 3) / 4;
-    const size_t sel = 4 * select_smem_per_warp(a.E);
-    if (sel > 48 * 1024 &&
-        cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel) != cudaSuccess)
-        return MOE_ERR_LAUNCH;
-    route_select_kernel<<<sel_blocks, 128, sel, st>>>(a);
-    note_launch(3);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+    note_launch(2);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_LAUNCH;
+    return launch_select(a, st);
 }
 
 int launch_route(const moe_dims* m, int T, const uint16_t* x, const uint16_t* wr, const float* bias,
@@ -658,8 +787,7 @@ int launch_route(const moe_dims* m, int T, const uint16_t* x, const uint16_t* wr
     a.xnorm = reinterpret_cast<float*>(ws + L.xnorm);
     a.wnorm = reinterpret_cast<float*>(ws + L.wnorm);
     a.counter = reinterpret_cast<unsigned*>(ws + L.counter) + kCtrRoute;
-    (void)num_sms;
-    return launch_route_args(a, st);
+    return launch_route_args(a, st, num_sms);
 }
 
 }  // namespace fp4moe
@@ -716,8 +844,6 @@ extern "C" int moe_route_topk_noalloc(const moe_dims* dims, int32_t T, const uin
         base = static_cast<unsigned char*>(g_route_scratch_addr[dev]);
     }
     cudaStream_t st = (cudaStream_t)stream;
-    // the completion ticket must start at zero
-    if (cudaMemsetAsync(base, 0, kStaticCounterBytes, st) != cudaSuccess) return MOE_ERR_LAUNCH;
     RouteArgs a{};
     a.T = T; a.d = dims->d; a.E = dims->num_experts; a.k = dims->top_k;
     a.x = x; a.wr = w_router; a.bias = score_bias; a.table = expert_to_slot;
@@ -726,5 +852,7 @@ extern "C" int moe_route_topk_noalloc(const moe_dims* dims, int32_t T, const uin
     a.keys = reinterpret_cast<float4*>(base + kStaticCounterBytes);
     a.xnorm = reinterpret_cast<float*>(base + kStaticCounterBytes + kStaticKeyBytes);
     a.wnorm = reinterpret_cast<float*>(base + kStaticCounterBytes + kStaticKeyBytes + kStaticXnormBytes);
-    return launch_route_args(a, st);
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_LAUNCH;
+    return launch_route_args(a, st, sms);
 }

@@ -129,14 +129,13 @@ int moe_route_topk(const moe_dims* dims, int32_t T, const uint16_t* x, const uin
  * a serving loop that must not allocate between steps.  The pages have no counterpart to
  * this entry point; it computes exactly what moe_route_topk computes.
  * Limits: 0 <= T <= 16 (larger T returns MOE_ERR_TOKENS before anything is enqueued) and the
- * dims limits above.  Its scratch (fast logits, norms and a completion ticket, about 69 KB)
+ * dims limits above.  Its scratch (key records and norms, about 260 KB)
  * is a static device array inside this library, held by every GPU that loads the library
  * until the process exits.  It allocates nothing and calls no allocating routine.
  * The first call on each device looks up the array's device address with that device
- * current; make that first call before any stream capture.  Every call clears the ticket
- * (an asynchronous memset on `stream`) and overwrites the rest of the array: calls whose
- * execution overlaps on the GPU -- on different streams, or from different threads --
- * race on the shared array and must be serialised by the caller. */
+ * current; make that first call before any stream capture.  Every call overwrites the
+ * array: calls whose execution overlaps on the GPU -- on different streams, or from
+ * different threads -- race on the shared array and must be serialised by the caller. */
 int moe_route_topk_noalloc(const moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* w_router,
                            const float* score_bias, const int32_t* expert_to_slot, int32_t* topk_ids,
                            float* topk_w, int32_t* topk_slot, int32_t* dev_status, void* stream);
