@@ -51,6 +51,29 @@ def env_rank():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+FFN_SOURCES = ("fp4_routed_expert_gb300/csrc/mxf4_gemm.cu", "fp4_routed_expert_gb300/csrc/moe_internal.cuh")
+TRAFFIC_PROFILE = "profiles/expert_ffn_decode_T1_d5120_f2304_E384_k6.md"
+
+
+def ffn_traffic():
+    """DRAM bytes per FFN launch from the committed ncu capture, if it was taken on the current
+    kernel source (digest of its files), else None."""
+    import hashlib
+    h = hashlib.sha256()
+    try:
+        for f in FFN_SOURCES:
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        text = open(os.path.join(ROOT, TRAFFIC_PROFILE)).read()
+    except OSError:
+        return None
+    for line in text.splitlines():
+        if line.startswith("traffic-record:"):
+            fields = dict(kv.split("=", 1) for kv in line.split()[1:])
+            if fields.get("digest") == h.hexdigest()[:16]:
+                return int(fields["dram_bytes_per_launch"])
+    return None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -280,7 +303,7 @@ def run_ours(args, rank, world, local_rank):
             "config": dict(CONFIG, parallelism="replicas" if world > 1 else "single GPU"),
             "roofline": {"bound": "hbm", "kernel": "mxf4_ffn_kernel (expert FFN: gate/up + SwiGLU + down + combine, T=1)",
                          "achieved": round(achieved, 1) if achieved else None, "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4) if achieved else None, "traffic": None,
+                         "frac": round(achieved / peak, 4) if achieved else None, "traffic": ffn_traffic(),
                          "bytes_per_launch": FFN_BYTES, "launch_ms": round(k_ms, 5) if k_ms else None,
                          "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured" else "fallback 6.8 TB/s"},
             "layer_roofline": {"bytes_per_token": ALG_BYTES_PER_TOKEN,

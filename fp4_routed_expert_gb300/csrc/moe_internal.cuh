@@ -73,9 +73,9 @@ inline bool dims_ok(const moe_dims* m) {
 }
 
 // Counters inside the counter section (zeroed by moe_workspace_init; every user leaves them
-// zero again): the decode FFN kernel's work list, x-ready, exit ticket, per-key readiness
+// zero again): the decode FFN kernel's work list, x jobs and x-ready, exit ticket, per-key readiness
 // (kMaxDecodeKeys) and per-block y counts (d/128 <= 512).
-enum { kCtrRoute = 0, kCtrFfnWork = 64, kCtrFfnXReady = 65, kCtrFfnExit = 66, kCtrFfnReady = 128,
+enum { kCtrRoute = 0, kCtrFfnWork = 64, kCtrFfnXReady = 65, kCtrFfnExit = 66, kCtrFfnXJob = 67, kCtrFfnReady = 128,
        kCtrFfnY = 256, kCounterWords = 1024 };
 
 // Workspace sections, each 256-byte aligned.  The persistent counters come first so that

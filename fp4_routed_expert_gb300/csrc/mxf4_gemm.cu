@@ -252,10 +252,12 @@ struct FfnParams {
     int32_t* work;                   // next unit to hand out (zero at launch)
     int32_t* ready;                  // phase 0 units finished, per key (decode: slot ordinal; prefill: tile)
     int32_t* ycnt;                   // decode: pair rows finished per 128-feature block of y
-    // decode: x is quantised by this kernel into ph[0].b_q / b_sf (NT-row tile), CTAs counted
-    // in xready; the last CTA to exit (exit ticket) clears every counter for the next call
+    // decode: x is quantised by this kernel into ph[0].b_q / b_sf (rows 0..T-1 of the NT-row
+    // tile; the padding rows only feed discarded columns); the last CTA to exit (exit ticket)
+    // clears every counter for the next call
     const uint16_t* x_src;
-    int32_t* xready;
+    int32_t* xjob;                   // decode: next x job (row, 32-element block) to hand out
+    int32_t* xready;                 // decode: x jobs finished
     int32_t* exit_ctr;
 };
 
@@ -363,6 +365,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     uint64_t* fixbar = epibar + 2;               // [2] arrival-count hand-offs
     uint64_t* uqfull = fixbar + 2;               // [kUQ] unit id written
     uint64_t* uqempty = uqfull + kUQ;            // [kUQ] unit id read by the MMA and epilogue warps
+    uint64_t* setupbar = uqempty + kUQ;          // keys of this call known
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     __shared__ int n_keys_sh, pairs_total_sh;
@@ -370,6 +373,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     __shared__ int wcount[8];
     __shared__ int uslots[kMaxNT];
     __shared__ int upairs[kMaxNT];
+    __shared__ int sslot[kMaxNT];                // decode: the routing outputs of the T*k pairs
+    __shared__ float sw[kMaxNT];
     __shared__ int uq[kUQ];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -390,6 +395,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
             mbar_init(smem_u32(&uqfull[i]), 1);
             mbar_init(smem_u32(&uqempty[i]), 5);
         }
+        mbar_init(smem_u32(setupbar), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -398,50 +404,97 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // everything above overlaps the previous kernel; its outputs are read from here on
-    pdl_wait();
-    // decode: the unique valid slots, in order of first appearance, are the keys
-    if (p.regime == kRegimeDecode) {
-        const int n = p.T * p.k;   // <= kMaxNT, checked on the host
-        int s = -1;
-        bool first = false;
-        if (tid < n) {
-            s = p.slot[tid];
-            const bool ok = s >= 0 && s < p.num_slots;
-            if (s >= p.num_slots && blockIdx.x == 0) atomicOr(p.status, MOE_STATUS_BAD_SLOT);
-            first = ok;
-            for (int j = 0; j < tid && first; ++j)
-                if (p.slot[j] == s) first = false;
-        }
-        const unsigned bal = __ballot_sync(0xffffffffu, first);
-        if (lane == 0) wcount[warp] = __popc(bal);
-        __syncthreads();
-        int off = 0;
-        for (int w = 0; w < warp; ++w) off += wcount[w];
-        if (first) {
-            int np = 0;
-            for (int j = 0; j < n; ++j) np += (p.slot[j] == s);
-            uslots[off + __popc(bal & ((1u << lane) - 1u))] = s;
-            upairs[off + __popc(bal & ((1u << lane) - 1u))] = np;
-        }
-        if (tid == 0) {
-            int tot = 0, pairs = 0;
-            for (int w = 0; w < kThreadsGemm / 32; ++w) tot += wcount[w];
-            for (int j = 0; j < n; ++j) pairs += (p.slot[j] >= 0 && p.slot[j] < p.num_slots);
-            n_keys_sh = tot;
-            pairs_total_sh = pairs;
-        }
-    } else if (tid == 0) {
-        n_keys_sh = p.plan[1];
-        pairs_total_sh = 0;
-    }
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();   // barriers initialised, TMEM address published
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
-    const int n_keys = n_keys_sh;
-    const int n0 = n_keys * p.ph[0].mtiles, n_all = n0 + n_keys * p.ph[1].mtiles;
     volatile int* abortp = &abort_flag;
+    // Decode: x -> kTerms MXFP4 terms, one warp per (row < T, 32-element block), jobs taken
+    // from a global counter so that the CTAs resident first do them all.  This runs before the
+    // wait below: x is an input of this call, and the kernel that may still be running (the
+    // router's) does not write it.
+    if (p.x_src && warp >= 2) {
+        const int nblk = p.d / 32, KBd = p.d / kKB, total = p.T * nblk;
+        uint8_t* q = const_cast<uint8_t*>(p.ph[0].b_q);
+        uint8_t* sf = const_cast<uint8_t*>(p.ph[0].b_sf);
+        while (true) {
+            int job = 0;
+            if (lane == 0) job = atomicAdd(p.xjob, 1);
+            job = __shfl_sync(0xffffffffu, job, 0);
+            if (job >= total) break;
+            const int r = job / nblk, b = job % nblk, kb = b / 8, j = b % 8;
+            uint4 codes[kTerms];
+            uint32_t scales[kTerms];
+            warp_quantize32(bf16_to_f32(p.x_src[(size_t)r * p.d + 32 * b + lane]), lane, codes, scales);
+            if (lane < kTerms) {
+                uint4 cv = codes[0];
+                uint32_t sv = scales[0];
+#pragma unroll
+                for (int t = 1; t < kTerms; ++t)
+                    if (lane == t) { cv = codes[t]; sv = scales[t]; }
+                *reinterpret_cast<uint4*>(q + act_code_off(0, kb, lane, r, j, NT, KBd)) = cv;
+                sf[act_scale_off(0, kb, lane, r, j, NT, KBd)] = (uint8_t)sv;
+            }
+            fence_proxy_async();   // read by the async proxy (bulk copies) of every CTA
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence();
+                atomicAdd(p.xready, 1);
+            }
+        }
+    }
+    // everything above overlaps the previous kernel; its outputs are read from here on
+    pdl_wait();
+    if (warp == 0) {
+        // decode: the unique valid slots, in order of first appearance, are the keys
+        if (p.regime == kRegimeDecode) {
+            const int n = p.T * p.k;   // <= kMaxNT = 64, checked on the host
+            for (int i = lane; i < n; i += 32) {
+                sslot[i] = p.slot[i];
+                sw[i] = p.w ? p.w[i] : 0.f;
+            }
+            __syncwarp();
+            int ord = 0, pairs = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = lane + 32 * h;
+                int s = -1, np = 0;
+                bool first = false;
+                if (i < n) {
+                    s = sslot[i];
+                    const bool ok = s >= 0 && s < p.num_slots;
+                    if (s >= p.num_slots && blockIdx.x == 0) atomicOr(p.status, MOE_STATUS_BAD_SLOT);
+                    pairs += ok;
+                    first = ok;
+                    for (int jj = 0; jj < i && first; ++jj)
+                        if (sslot[jj] == s) first = false;
+                    if (first)
+                        for (int jj = 0; jj < n; ++jj) np += (sslot[jj] == s);
+                }
+                const unsigned bal = __ballot_sync(0xffffffffu, first);
+                if (first) {
+                    uslots[ord + __popc(bal & ((1u << lane) - 1u))] = s;
+                    upairs[ord + __popc(bal & ((1u << lane) - 1u))] = np;
+                }
+                ord += __popc(bal);
+            }
+            pairs = __reduce_add_sync(0xffffffffu, (uint32_t)pairs);
+            if (lane == 0) {
+                n_keys_sh = ord;
+                pairs_total_sh = pairs;
+            }
+        } else if (lane == 0) {
+            n_keys_sh = p.plan[1];
+            pairs_total_sh = 0;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(setupbar));
+    }
+    if (!mbar_wait(smem_u32(setupbar), 0, abortp)) {
+        if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
+    }
+    const int n_keys = *abortp ? 0 : n_keys_sh;
+    const int n0 = n_keys * p.ph[0].mtiles, n_all = n0 + n_keys * p.ph[1].mtiles;
     // decode with no valid pair: y is zero
     if (p.regime == kRegimeDecode && p.y && n_keys == 0 && blockIdx.x == 0)
         for (int i = tid; i < p.T * p.d; i += blockDim.x) p.y[i] = 0;
@@ -489,10 +542,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     pend_n = 0;
                 };
                 auto key_ready = [&](bool block) -> bool {
-                    // gate/up: every CTA has quantised its share of x; down: every gate/up unit
-                    // of the key has written its h rows
+                    // gate/up: every x job is done; down: every gate/up unit of the key has
+                    // written its h rows
                     const int32_t* flag = (ph == 0) ? p.xready : p.ready + u.key;
-                    const int target = (ph == 0) ? (int)gridDim.x : p.ph[0].mtiles;
+                    const int target = (ph == 0) ? p.T * (p.d / 32) : p.ph[0].mtiles;
                     unsigned spins = 0;
                     while (ld_acquire(flag) < target) {
                         if (!block) return false;
@@ -647,39 +700,6 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
             last = ok1 && fix_last;
             return ok1;
         };
-        if (p.x_src) {
-            // x -> kTerms MXFP4 terms in the NT-row activation tile, one warp per (row,
-            // 32-element block); rows >= T are zero.  Then count this CTA in xready.
-            const int nblk = p.d / 32, KBd = p.d / kKB;
-            const int total = NT * nblk;
-            for (int job = blockIdx.x * 4 + ew; job < total; job += gridDim.x * 4) {
-                const int r = job / nblk, b = job % nblk, kb = b / 8, j = b % 8;
-                uint8_t* q = const_cast<uint8_t*>(p.ph[0].b_q);
-                uint8_t* sf = const_cast<uint8_t*>(p.ph[0].b_sf);
-                if (r >= p.T) {
-                    if (lane < kTerms) {
-                        *reinterpret_cast<uint4*>(q + act_code_off(0, kb, lane, r, j, NT, KBd)) = make_uint4(0, 0, 0, 0);
-                        sf[act_scale_off(0, kb, lane, r, j, NT, KBd)] = 0;
-                    }
-                    continue;
-                }
-                uint4 codes[kTerms];
-                uint32_t scales[kTerms];
-                warp_quantize32(bf16_to_f32(p.x_src[(size_t)r * p.d + 32 * b + lane]), lane, codes, scales);
-                if (lane < kTerms) {
-                    uint4 cv = codes[0];
-                    uint32_t sv = scales[0];
-#pragma unroll
-                    for (int t = 1; t < kTerms; ++t)
-                        if (lane == t) { cv = codes[t]; sv = scales[t]; }
-                    *reinterpret_cast<uint4*>(q + act_code_off(0, kb, lane, r, j, NT, KBd)) = cv;
-                    sf[act_scale_off(0, kb, lane, r, j, NT, KBd)] = (uint8_t)sv;
-                }
-            }
-            fence_proxy_async();   // read by the async proxy (bulk copies) of every CTA
-            bool unused;
-            count_arrival(p.xready, 1, (int)gridDim.x, unused);
-        }
         while (true) {
             int unit = -1;
             if (mbar_wait(smem_u32(&uqfull[qi]), qphase, abortp)) unit = uq[qi];
@@ -725,7 +745,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 const int r = u.m * kBM + row;    // output feature
 #pragma unroll
                 for (int c = 0; c < NT; ++c) {
-                    const bool valid = (p.regime == kRegimeDecode) ? (c < u.ncols && p.slot[c] == u.slot) : (c < u.ncols);
+                    const bool valid = (p.regime == kRegimeDecode) ? (c < u.ncols && sslot[c] == u.slot) : (c < u.ncols);
                     if (valid) p.rows_out[(size_t)(u.brow0 + c) * p.d + r] = vals[c];
                 }
                 if (p.regime == kRegimeDecode && p.y) {
@@ -736,9 +756,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                         for (int t = 0; t < p.T; ++t) {
                             float yv = 0.f;
                             for (int j = 0; j < p.k; ++j) {
-                                const int pr = t * p.k + j, s = p.slot[pr];
+                                const int pr = t * p.k + j, s = sslot[pr];
                                 if (s < 0 || s >= p.num_slots) continue;
-                                yv = fmaf(p.w[pr], __ldcg(p.rows_out + (size_t)pr * p.d + r), yv);
+                                yv = fmaf(sw[pr], __ldcg(p.rows_out + (size_t)pr * p.d + r), yv);
                             }
                             p.y[(size_t)t * p.d + r] = f32_to_bf16(yv);
                         }
@@ -785,7 +805,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                         // column c = token; h for every pair (c, jj) routed to this slot
                         if (c < p.T)
                             for (int jj = 0; jj < p.k; ++jj)
-                                if (p.slot[c * p.k + jj] == u.slot) write_row(0, c * p.k + jj);
+                                if (sslot[c * p.k + jj] == u.slot) write_row(0, c * p.k + jj);
                     } else if (c < u.ncols) {
                         write_row(u.btile, c);
                     }
@@ -825,6 +845,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
             for (int i = tid; i < p.d / kBM; i += blockDim.x) p.ycnt[i] = 0;
             if (tid == 0) {
                 *p.work = 0;
+                *p.xjob = 0;
                 *p.xready = 0;
                 *p.exit_ctr = 0;
             }
@@ -952,6 +973,7 @@ int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16
     int32_t* ctr = reinterpret_cast<int32_t*>(ws + L.counter);
     p.work = ctr + kCtrFfnWork;
     p.xready = ctr + kCtrFfnXReady;
+    p.xjob = ctr + kCtrFfnXJob;
     p.exit_ctr = ctr + kCtrFfnExit;
     p.ready = ctr + kCtrFfnReady;
     p.ycnt = ctr + kCtrFfnY;

@@ -329,184 +329,132 @@ __device__ __noinline__ void select_token(const RouteArgs& a, int t, int lane, f
     __syncwarp();
 }
 
-// One block of 128 threads per token.  Thread i holds experts i, i+128, ... (at most 8).
-// Each warp finds the top-k of its 256.. experts by k rounds of two warp reductions (largest
-// key, then lowest id among equal keys; only the owner of the winner rescans its experts),
-// warp 0 merges the four lists the same way, and every thread checks its experts against
-// the certification thresholds.  A token with an uncertain or wide expert is handed whole to
-// select_token (warp 0).
-constexpr int kSelThreads = 128, kSelItems = 8;   // E <= 1024
+// One warp per token.  Lane l holds the key records of experts l + 32 m (m < EPL) in
+// registers; a top-k round is two warp reductions (largest key, then lowest id among equal
+// keys) and a register rescan by the winning lane.  The chosen set is final when every chosen
+// expert's key interval lies above every other expert's and every chosen score is narrow;
+// otherwise the token goes whole to select_token (same warp).  E <= 32 * EPL.
+constexpr int kSelWarps = 4;
 
-__global__ void __launch_bounds__(kSelThreads) route_select_kernel(RouteArgs a) {
-    extern __shared__ unsigned char sel_smem[];   // select_token's arrays (warp 0)
-    __shared__ float4 items[kSelItems][kSelThreads];
-    __shared__ uint32_t c_u[4][32];
-    __shared__ int c_e[4][32];
-    __shared__ float c_s[4][32];
-    __shared__ int S_e[32];
-    __shared__ float S_s[32];
-    __shared__ int S_sorted[32];
-    __shared__ int S_n;
-    __shared__ uint32_t inS[32];                  // bitmap over experts
-    __shared__ uint32_t red_lo[4], red_hi[4];
+template <int EPL>
+__global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(RouteArgs a) {
+    extern __shared__ unsigned char sel_smem[];   // per warp: select_token's arrays
     const float NEG_INF = -__int_as_float(0x7f800000);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int E = a.E, k = a.k;
+    unsigned char* wsm = sel_smem + (size_t)warp * select_smem_per_warp(E);
+    float4* rec = reinterpret_cast<float4*>(wsm);
+    float* exk = reinterpret_cast<float*>(wsm + (size_t)E * 16);
+    int* out = reinterpret_cast<int*>(wsm + (size_t)E * 20);   // 64 words: ranks' scores
     pdl_trigger();
     pdl_wait();   // the key records of the logit kernel
-    for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+    for (int t = blockIdx.x * kSelWarps + warp; t < a.T; t += gridDim.x * kSelWarps) {
         const float4* krow = a.keys + (size_t)t * E;
-        {
-            float4 r[kSelItems];
+        float4 r[EPL];
 #pragma unroll
-            for (int i = 0; i < kSelItems; ++i) {
-                const int e = tid + kSelThreads * i;
-                r[i] = (e < E) ? __ldcg(krow + e) : make_float4(NEG_INF, NEG_INF, NEG_INF, -1.0f);
-            }
-#pragma unroll
-            for (int i = 0; i < kSelItems; ++i) items[i][tid] = r[i];
+        for (int m = 0; m < EPL; ++m) {
+            const int e = lane + 32 * m;
+            r[m] = (e < E) ? __ldcg(krow + e) : make_float4(NEG_INF, NEG_INF, NEG_INF, -1.0f);
         }
-        __syncwarp();   // a round's winner's score is read by the lane that records it
-        if (tid < 32) inS[tid] = 0;
-        uint32_t valid = 0;
-#pragma unroll 1
-        for (int i = 0; i < kSelItems; ++i)
-            if (items[i][tid].w >= 0.0f) valid |= 1u << i;
-        // ---- per-warp top-k
-        uint32_t picked = 0, bu = 0;
-        int bi = -1;
-        auto local_best = [&]() {
-            bu = 0;
-            bi = -1;
-#pragma unroll 1
-            for (uint32_t rr = valid & ~picked; rr; rr &= rr - 1) {
-                const int i = __ffs(rr) - 1;
-                const uint32_t ku = key_order(items[i][tid].x);
-                if (ku > bu) { bu = ku; bi = i; }
+        uint32_t valid = 0, picked = 0, bu = 0;
+        int bm = 0;
+#pragma unroll
+        for (int m = 0; m < EPL; ++m)
+            if (r[m].w >= 0.0f) {
+                valid |= 1u << m;
+                const uint32_t ku = key_order(r[m].x);
+                if (ku > bu) { bu = ku; bm = m; }
             }
-        };
-        local_best();
-        uint32_t my_u = 0;
-        int my_e = -1, nsel = 0;
-        float my_s = 0.f;
-#pragma unroll 1
+        int n = 0;
         for (int j = 0; j < k; ++j) {
             const uint32_t M = __reduce_max_sync(0xffffffffu, bu);
             if (M == 0) break;
-            const uint32_t win = __reduce_min_sync(0xffffffffu, bu == M ? (uint32_t)(tid + kSelThreads * bi) : 0xFFFFFFFFu);
-            if (lane == j) { my_u = M; my_e = (int)win; my_s = items[win / kSelThreads][win % kSelThreads].w; }
-            if ((int)(win % kSelThreads) == tid) {
-                picked |= 1u << bi;
-                local_best();
+            const uint32_t win = __reduce_min_sync(0xffffffffu, bu == M ? (uint32_t)(lane + 32 * bm) : 0xFFFFFFFFu);
+            if ((int)(win & 31) == lane) {
+                picked |= 1u << (win >> 5);
+                bu = 0;
+#pragma unroll
+                for (int m = 0; m < EPL; ++m)
+                    if (((valid & ~picked) >> m) & 1u) {
+                        const uint32_t ku = key_order(r[m].x);
+                        if (ku > bu) { bu = ku; bm = m; }
+                    }
             }
-            ++nsel;
+            ++n;
         }
-        c_u[warp][lane] = lane < nsel ? my_u : 0u;
-        c_e[warp][lane] = my_e;
-        c_s[warp][lane] = my_s;
-        __syncthreads();
-        // ---- warp 0 merges: lane l holds candidate l of every warp
-        if (warp == 0) {
-            uint32_t taken = 0;
-            int n = 0;
-#pragma unroll 1
-            for (int j = 0; j < k; ++j) {
-                uint32_t lb = 0;
-                int lq = -1, le = 0x7FFFFFFF;
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t cu = c_u[q][lane];
-                    const int ce = c_e[q][lane];
-                    if (!((taken >> q) & 1u) && cu != 0 && (cu > lb || (cu == lb && ce < le))) { lb = cu; lq = q; le = ce; }
-                }
-                const uint32_t M = __reduce_max_sync(0xffffffffu, lb);
-                if (M == 0) break;
-                const uint32_t win = __reduce_min_sync(0xffffffffu, (lb == M && lq >= 0) ? (uint32_t)le : 0xFFFFFFFFu);
-                if (lb == M && lq >= 0 && (uint32_t)le == win) {
-                    taken |= 1u << lq;
-                    S_e[j] = (int)win;
-                    S_s[j] = c_s[lq][lane];
-                    atomicOr(&inS[win >> 5], 1u << (win & 31));
-                }
-                ++n;
-            }
-            if (lane == 0) S_n = n;
-        }
-        __syncthreads();
-        const int n = S_n;
-        if (n < k && tid == 0) atomicOr(a.status, MOE_STATUS_FEW_RESIDENT);
-        // ---- thresholds: min klo over S, max khi over the other valid experts
+        if (n < k && lane == 0) atomicOr(a.status, MOE_STATUS_FEW_RESIDENT);
+        // certification thresholds: min klo over the chosen, max khi over the rest
         float lo_in = __int_as_float(0x7f800000), hi_out = NEG_INF;
-        uint32_t inmask = 0;
-#pragma unroll 1
-        for (uint32_t rr = valid; rr; rr &= rr - 1) {
-            const int i = __ffs(rr) - 1, e = tid + kSelThreads * i;
-            const float4 v = items[i][tid];
-            if ((inS[e >> 5] >> (e & 31)) & 1u) { inmask |= 1u << i; lo_in = fminf(lo_in, v.y); }
-            else hi_out = fmaxf(hi_out, v.z);
+#pragma unroll
+        for (int m = 0; m < EPL; ++m) {
+            if ((picked >> m) & 1u) lo_in = fminf(lo_in, r[m].y);
+            else if ((valid >> m) & 1u) hi_out = fmaxf(hi_out, r[m].z);
         }
-        uint32_t wlo = __reduce_min_sync(0xffffffffu, key_order(lo_in));
-        uint32_t whi = __reduce_max_sync(0xffffffffu, key_order(hi_out));
-        if (lane == 0) { red_lo[warp] = wlo; red_hi[warp] = whi; }
-        __syncthreads();
-        wlo = min(min(red_lo[0], red_lo[1]), min(red_lo[2], red_lo[3]));
-        whi = max(max(red_hi[0], red_hi[1]), max(red_hi[2], red_hi[3]));
-        const float min_lo_in = key_value(wlo), max_hi_out = key_value(whi);
-        // every chosen expert certain, no other expert overlapping, every weight narrow?
+        const float min_lo_in = key_value(__reduce_min_sync(0xffffffffu, key_order(lo_in)));
+        const float max_hi_out = key_value(__reduce_max_sync(0xffffffffu, key_order(hi_out)));
         bool doubt = false;
-#pragma unroll 1
-        for (uint32_t rr = valid; rr; rr &= rr - 1) {
-            const int i = __ffs(rr) - 1;
-            const float4 v = items[i][tid];
-            if ((inmask >> i) & 1u) {
-                if (!(v.y > max_hi_out)) doubt = true;
-                if (v.z - v.y > 1e-5f * v.w) doubt = true;
-            } else if (v.z >= min_lo_in) {
+#pragma unroll
+        for (int m = 0; m < EPL; ++m) {
+            if ((picked >> m) & 1u) {
+                if (!(r[m].y > max_hi_out) || r[m].z - r[m].y > 1e-5f * r[m].w) doubt = true;
+            } else if (((valid >> m) & 1u) && r[m].z >= min_lo_in) {
                 doubt = true;
             }
         }
-        if (__syncthreads_or(doubt)) {
-            if (warp == 0) {
-                float4* rec = reinterpret_cast<float4*>(sel_smem);
-                float* exk = reinterpret_cast<float*>(sel_smem + (size_t)E * 16);
-                int* out = reinterpret_cast<int*>(sel_smem + (size_t)E * 20);
-                select_token(a, t, lane, rec, exk, out);
-            }
-            __syncthreads();
+        if (__any_sync(0xffffffffu, doubt)) {
+            select_token(a, t, lane, rec, exk, out);
             continue;
         }
-        // ---- outputs: S in ascending id, weights s / sum(s) with the sum in that order
-        if (warp == 0) {
-            if (lane < n) {
-                const int e = S_e[lane];
-                int rank = 0;
-                for (int i = 0; i < n; ++i) rank += (S_e[i] < e);
-                S_sorted[rank] = lane;
+        // outputs in ascending id (m outer, lane inner); weight sum in that order
+        float* osc = reinterpret_cast<float*>(out);
+        int* oid = out + 32;
+        const uint32_t below = (1u << lane) - 1u;
+        int base = 0;
+#pragma unroll
+        for (int m = 0; m < EPL; ++m) {
+            const uint32_t bal = __ballot_sync(0xffffffffu, (picked >> m) & 1u);
+            if ((picked >> m) & 1u) {
+                const int rank = base + __popc(bal & below);
+                osc[rank] = r[m].w;
+                oid[rank] = lane + 32 * m;
             }
-            __syncwarp();
-            float sum = 0.0f;
-            if (lane == 0)
-                for (int i = 0; i < n; ++i) sum += S_s[S_sorted[i]];
-            sum = __shfl_sync(0xffffffffu, sum, 0);
-            int32_t* ids = a.ids + (size_t)t * k;
-            float* wo = a.w + (size_t)t * k;
-            int32_t* so = a.slots + (size_t)t * k;
-            for (int j = lane; j < k; j += 32) {
-                if (j < n) {
-                    const int c = S_sorted[j], e = S_e[c];
-                    ids[j] = e;
-                    wo[j] = (sum > 0.0f) ? __fdiv_rn(S_s[c], sum) : 0.0f;
-                    so[j] = a.table[e];
-                } else {
-                    ids[j] = -1;
-                    wo[j] = 0.0f;
-                    so[j] = -1;
-                }
+            base += __popc(bal);
+        }
+        __syncwarp();
+        float sum = 0.0f;
+        if (lane == 0)
+            for (int i = 0; i < n; ++i) sum += osc[i];
+        sum = __shfl_sync(0xffffffffu, sum, 0);
+        int32_t* ids = a.ids + (size_t)t * k;
+        float* wo = a.w + (size_t)t * k;
+        int32_t* so = a.slots + (size_t)t * k;
+        for (int j = lane; j < k; j += 32) {
+            if (j < n) {
+                const int e = oid[j];
+                ids[j] = e;
+                wo[j] = (sum > 0.0f) ? __fdiv_rn(osc[j], sum) : 0.0f;
+                so[j] = a.table[e];
+            } else {
+                ids[j] = -1;
+                wo[j] = 0.0f;
+                so[j] = -1;
             }
         }
-        __syncthreads();
+        __syncwarp();
     }
 }
+
+#define FP4MOE_EPL_DISPATCH(E, ...)                                   \
+    do {                                                              \
+        const int epl_ = ((E) + 31) / 32;                             \
+        if (epl_ <= 2) { constexpr int EPL = 2; __VA_ARGS__; }        \
+        else if (epl_ <= 4) { constexpr int EPL = 4; __VA_ARGS__; }   \
+        else if (epl_ <= 8) { constexpr int EPL = 8; __VA_ARGS__; }   \
+        else if (epl_ <= 12) { constexpr int EPL = 12; __VA_ARGS__; } \
+        else if (epl_ <= 16) { constexpr int EPL = 16; __VA_ARGS__; } \
+        else if (epl_ <= 24) { constexpr int EPL = 24; __VA_ARGS__; } \
+        else { constexpr int EPL = 32; __VA_ARGS__; }                 \
+    } while (0)
 
 // ------------------------------------------------------------------ decode: one warp per expert
 
@@ -728,16 +676,23 @@ static double gamma32(int n) {
 
 static float gamma_coef(int L) { return (float)(gamma32(L) * (1.0 + 1.0 / 1024.0)); }
 
-// Selection: one block per token, launched behind the key-record kernel.
-static int launch_select(const RouteArgs& a, cudaStream_t st) {
-    const size_t sel = select_smem_per_warp(a.E);
+// Selection: one warp per token, launched behind the key-record kernel.
+template <int EPL>
+static int launch_select_epl(const RouteArgs& a, cudaStream_t st) {
+    const size_t sel = kSelWarps * select_smem_per_warp(a.E);
     if (sel > 48 * 1024 &&
-        cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel) != cudaSuccess)
+        cudaFuncSetAttribute(route_select_kernel<EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sel) != cudaSuccess)
         return MOE_ERR_LAUNCH;
-    const int grid = a.T < 4096 ? a.T : 4096;
-    if (launch_pdl(route_select_kernel, dim3(grid), dim3(kSelThreads), sel, st, a) != cudaSuccess) return MOE_ERR_LAUNCH;
+    int grid = (a.T + kSelWarps - 1) / kSelWarps;
+    if (grid > 4096) grid = 4096;
+    if (launch_pdl(route_select_kernel<EPL>, dim3(grid), dim3(kSelWarps * 32), sel, st, a) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
     note_launch(1);
     return MOE_OK;
+}
+static int launch_select(const RouteArgs& a, cudaStream_t st) {
+    FP4MOE_EPL_DISPATCH(a.E, return launch_select_epl<EPL>(a, st));
+    return MOE_ERR_LAUNCH;
 }
 
 template <int CH>
