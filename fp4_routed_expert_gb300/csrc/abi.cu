@@ -109,7 +109,7 @@ int moe_workspace_init(const moe_dims* dims, void* ws, size_t ws_bytes, void* st
     WsLayout L;
     int rc = check_ws(dims, 0, ws, ws_bytes, &L);
     if (rc) return rc;
-    cudaError_t e = cudaMemsetAsync(static_cast<char*>(ws) + L.counter, 0, 4 * kCounterWords, (cudaStream_t)stream);
+    cudaError_t e = cudaMemsetAsync(static_cast<char*>(ws) + L.counter, 0, 4 * counter_words(dims), (cudaStream_t)stream);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 

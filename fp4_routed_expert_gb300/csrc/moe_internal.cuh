@@ -77,6 +77,7 @@ inline bool dims_ok(const moe_dims* m) {
 // (kMaxDecodeKeys) and per-block y counts (d/128 <= 512).
 enum { kCtrRoute = 0, kCtrFfnWork = 64, kCtrFfnXReady = 65, kCtrFfnExit = 66, kCtrFfnXJob = 67, kCtrFfnReady = 128,
        kCtrFfnY = 256, kCounterWords = 1024 };
+inline size_t counter_words(const moe_dims*) { return kCounterWords; }
 
 // Workspace sections, each 256-byte aligned.  The persistent counters come first so that
 // their offset is the same for every token count; the other sections are per call.
@@ -103,7 +104,7 @@ inline WsLayout ws_layout(const moe_dims* m, int T_max) {
     WsLayout w;
     size_t o = 0;
     size_t T = (size_t)(T_max > 0 ? T_max : 1), E = (size_t)m->num_experts, k = (size_t)m->top_k;
-    w.counter = o; o = align256(o + 4 * kCounterWords);   // first: its offset must not depend on T
+    w.counter = o; o = align256(o + 4 * counter_words(m));   // first: its offset must not depend on T
     w.keys = o;    o = align256(o + 16 * T * E);
     w.xnorm = o;   o = align256(o + 4 * T);
     w.wnorm = o;   o = align256(o + 4 * E);

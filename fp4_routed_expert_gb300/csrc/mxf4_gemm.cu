@@ -700,18 +700,29 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
             last = ok1 && fix_last;
             return ok1;
         };
+        // Two warm-up passes first (a gate/up unit, then a down unit of key 0) with every global
+        // write, atomic and hand-off disabled: they run the epilogue's instructions once while
+        // the warps would idle anyway, so the first real units do not fetch them cold.  They
+        // read TMEM (allocated, contents unused) and write only this warp's rows of hbuf.
+        int warm = (n_keys > 0) ? 2 : 0;
         while (true) {
+            const bool dry = warm > 0;
             int unit = -1;
-            if (mbar_wait(smem_u32(&uqfull[qi]), qphase, abortp)) unit = uq[qi];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&uqempty[qi]));
-            if (++qi == kUQ) { qi = 0; qphase ^= 1u; }
+            if (dry) {
+                unit = (warm == 2) ? 0 : n0;
+                --warm;
+            } else {
+                if (mbar_wait(smem_u32(&uqfull[qi]), qphase, abortp)) unit = uq[qi];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&uqempty[qi]));
+                if (++qi == kUQ) { qi = 0; qphase ^= 1u; }
+            }
             if (unit < 0) break;
             const int ph = unit < n0 ? 0 : 1;
             const PhaseParams& P = p.ph[ph];
             UnitInfo u;
             const bool ok = unit_info<NT>(p, P, ph ? unit - n0 : unit, uslots, u);
-            if (!mbar_wait(smem_u32(&tfull[acc]), aphase, abortp)) {
+            if (!dry && !mbar_wait(smem_u32(&tfull[acc]), aphase, abortp)) {
                 if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
                 break;
             }
@@ -738,20 +749,22 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
-            if (++acc == C::kDbuf) { acc = 0; aphase ^= 1u; }
+            if (!dry) {
+                if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+                if (++acc == C::kDbuf) { acc = 0; aphase ^= 1u; }
+            }
             if (!ok) continue;
             if (ph == 1) {
                 const int r = u.m * kBM + row;    // output feature
 #pragma unroll
                 for (int c = 0; c < NT; ++c) {
                     const bool valid = (p.regime == kRegimeDecode) ? (c < u.ncols && sslot[c] == u.slot) : (c < u.ncols);
-                    if (valid) p.rows_out[(size_t)(u.brow0 + c) * p.d + r] = vals[c];
+                    if (valid && !dry) p.rows_out[(size_t)(u.brow0 + c) * p.d + r] = vals[c];
                 }
                 if (p.regime == kRegimeDecode && p.y) {
                     // y block m is complete once every valid pair's row block m is written
-                    bool last = false;
-                    if (!count_arrival(p.ycnt + u.m, upairs[u.key], pairs_total_sh, last)) break;
+                    bool last = dry;
+                    if (!dry && !count_arrival(p.ycnt + u.m, upairs[u.key], pairs_total_sh, last)) break;
                     if (last) {
                         for (int t = 0; t < p.T; ++t) {
                             float yv = 0.f;
@@ -760,7 +773,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                                 if (s < 0 || s >= p.num_slots) continue;
                                 yv = fmaf(sw[pr], __ldcg(p.rows_out + (size_t)pr * p.d + r), yv);
                             }
-                            p.y[(size_t)t * p.d + r] = f32_to_bf16(yv);
+                            if (!dry) p.y[(size_t)t * p.d + r] = f32_to_bf16(yv);
                         }
                     }
                 }
@@ -777,10 +790,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 }
                 // hand-off 1: every warp's h values are in hbuf
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&epibar[0]));
-                if (!mbar_wait(smem_u32(&epibar[0]), ephase, abortp)) {
-                    if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
-                    break;
+                if (!dry) {
+                    if (lane == 0) mbar_arrive(smem_u32(&epibar[0]));
+                    if (!mbar_wait(smem_u32(&epibar[0]), ephase, abortp)) {
+                        if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
+                        break;
+                    }
                 }
                 // quantise, one warp per job = (column c, block b of 32 outputs i0 = 64m + 32b)
                 for (int job = ew; job < u.ncols * 2; job += 4) {
@@ -790,7 +805,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     warp_quantize32(hbuf[c * 64 + 32 * b + lane], lane, codes, scales);
                     const int i0 = u.m * 64 + 32 * b, kb = i0 / kKB, j = (i0 % kKB) / 32;
                     auto write_row = [&](int htile, int hrow) {
-                        if (lane < kTerms) {
+                        if (lane < kTerms && !dry) {
                             // lane t writes term t (the codes of every term sit in lane 0)
                             uint4 cv = codes[0];
                             uint32_t sv = scales[0];
@@ -814,6 +829,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 fence_proxy_async();
                 // hand-off 2: hbuf may be overwritten by the next unit; h of this unit is written
                 __syncwarp();
+                if (dry) continue;
                 if (lane == 0) mbar_arrive(smem_u32(&epibar[1]));
                 if (!mbar_wait(smem_u32(&epibar[1]), ephase, abortp)) {
                     if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
