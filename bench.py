@@ -47,6 +47,21 @@ CONFIG = {"workload": "decode T=1, one MoE layer, d=5120 f=2304 E=384 top-k=6, 3
           "tokens_per_step": TOKENS, "l2": "inputs larger than L2 (7.22 GB arena), no flush"}
 
 
+def max_over_ranks(v: float, dist=None, device=None) -> float:
+    """The slowest rank's time: all-reduce MAX over the process group (identity without one)."""
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's step time."""
+    return world * units_per_rank / (ms_per_step / 1e3)
+
+
 def env_rank():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
@@ -261,13 +276,9 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     clk = clocks.stop()
-    total_ms = ev0.elapsed_time(ev1)
-    if dist:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(ev0.elapsed_time(ev1), dist, device)
     ms_per_step = total_ms / args.steps
-    value = world * TOKENS / (ms_per_step / 1e3)
+    value = job_throughput(TOKENS, world, ms_per_step)
     # end-to-end through the public API with host buffers: pinned x in, y out, every step
     x_host = torch.empty((TOKENS, D), dtype=torch.bfloat16, pin_memory=True)
     x_host.copy_(w["x"].cpu())
@@ -282,11 +293,7 @@ def run_ours(args, rank, world, local_rank):
             y_host.copy_(w["y"], non_blocking=True)
         e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, device)
     status = int(w["layer"].status.item())
     peaks, peak_kind = measured_peaks()
     out = None
@@ -309,13 +316,73 @@ def run_ours(args, rank, world, local_rank):
             "layer_roofline": {"bytes_per_token": ALG_BYTES_PER_TOKEN,
                                "achieved_gbs": round(ALG_BYTES_PER_TOKEN * value / world / 1e9, 1),
                                "frac": round(ALG_BYTES_PER_TOKEN * value / world / 1e9 / peak, 4)},
-            "e2e": {"value": round(world * TOKENS / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+            "e2e": {"value": round(job_throughput(TOKENS, world, e2e_ms), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": TOKENS * D * 2, "d2h_bytes_per_step": TOKENS * D * 2},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "device_status": status,
         }
     return out, w
+
+
+# ---------------------------------------------------------------------------- prefill chunk
+
+PREFILL_T = 4096
+PREFILL_BIAS = (1.2, 0.04)   # Zipf s, beta of the per-expert score bias
+
+
+def run_prefill(w, args, device):
+    """One prefill chunk at the pages' shape: T=4096 tokens of N(0,1) bf16, Zipf(1.2)-skewed
+    score bias, every expert resident; route -> permute -> expert FFN -> combine, graph-replayed.
+    Returns the measurement object added to the JSON line."""
+    import torch
+    from fp4_routed_expert_gb300.layer import MoeLayer
+    from synth import tensors as syn
+    T = PREFILL_T
+    xb = syn.activations(0, 0, T, D, stream=9)
+    bias = torch.from_numpy(syn.zipf_score_bias(0, 0, E, *PREFILL_BIAS)).to(device)
+    x = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).to(device).view(torch.bfloat16)
+    layer = MoeLayer(D, F, E, K, T, w["arena"], device)
+    y = torch.empty((T, D), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        layer.route(x, w["wr"], w["tab"], bias)
+        layer.experts(x, fused_prefill=True, y=y)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        layer.route(x, w["wr"], w["tab"], bias)
+        layer.experts(x, fused_prefill=True, y=y)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    ids = layer.ids[:T].cpu().numpy()
+    used = int(np.unique(ids[ids >= 0]).size)
+    peaks, kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    fp4 = float(peaks["bf16_tflops"]) * (13.5 / 2.25)   # FP4 dense peak = measured bf16 x nominal ratio
+    bytes_ = used * EXPERT_BYTES + ROUTER_BYTES + 2 * T * D * 2
+    flops = 6.0 * T * K * D * F                          # gate, up, down: 2 flops per multiply-add
+    return {"workload": "prefill chunk T=%d, d=%d f=%d E=%d top-k=%d, Zipf(s=%.1f, beta=%.2f) score bias, all experts "
+                        "resident; route + permute + expert FFN + combine" % (T, D, F, E, K, *PREFILL_BIAS),
+            "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_chunk": round(ms, 4),
+            "experts_used": used, "status": int(layer.status.item()),
+            "roofline_hbm": {"bound": "hbm", "achieved": round(bytes_ / (ms * 1e-3) / 1e9, 1), "peak": hbm,
+                             "unit": "GB/s", "frac": round(bytes_ / (ms * 1e-3) / 1e9 / hbm, 4), "bytes": bytes_},
+            "roofline_fp4": {"bound": "tensor", "achieved": round(flops / (ms * 1e-3) / 1e12, 2), "peak": round(fp4, 1),
+                             "unit": "TFLOP/s", "frac": round(flops / (ms * 1e-3) / 1e12 / fp4, 4),
+                             "peak_source": "measured bf16 x 6 (nominal fp4/bf16 dense ratio)" if kind == "measured"
+                             else "fallback bf16 x 6"}}
 
 
 # ---------------------------------------------------------------------------- oracle timing
@@ -388,6 +455,7 @@ def main():
     ap.add_argument("--experts", type=int, default=384,
                     help="experts resident in the arena (profiling runs use fewer; the metric is defined at 384)")
     ap.add_argument("--tokens", type=int, default=1000, help="tokens per step")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-chunk measurement")
     args = ap.parse_args()
     global E, TOKENS, ROUTER_BYTES, ALG_BYTES_PER_TOKEN
     E, TOKENS = args.experts, args.tokens
@@ -405,6 +473,9 @@ def main():
     import fp4_routed_expert_gb300 as moe
     moe.lib()
     out, w = run_ours(args, rank, world, local_rank)
+    if rank == 0 and out is not None and not args.no_prefill and E == 384:
+        import torch
+        out["prefill"] = run_prefill(w, args, torch.device("cuda", local_rank))
     if rank == 0 and out is not None:
         if not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline_block()

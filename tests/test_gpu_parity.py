@@ -278,3 +278,30 @@ def test_full_shape_prefill_sampled_tokens(full_decode, cuda_cores):
     x = syn.activations(0, 0, T, 5120, stream=5)
     got = run_layer(wl, x, bias=bias, cuda_cores=cuda_cores)
     check_tokens(wl, x, got, [0, 1, 255, 511], bias=bias)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["rows_then_combine", "fused_combine"])
+def test_config3_prefill_chunk_T4096(full_decode, fused):
+    """The prefill chunk at the pages' shape (T = 4096, Zipf(1.2) bias, every expert resident):
+    ids and slots of sampled tokens against the oracle router, the whole permutation against
+    the oracle's permutation of the returned ids (bit for bit), sampled outputs against the
+    oracle layer, and the skew the workload is meant to have (some experts get no token)."""
+    wl = full_decode
+    T = 4096
+    bias = syn.zipf_score_bias(0, 0, 384, 1.2, 0.04)
+    x = syn.activations(0, 0, T, 5120, stream=9)
+    got = run_layer(wl, x, bias=bias, fused_prefill=fused)
+    ids = got["ids"]
+    assert got["status"] == 0
+    counts = np.bincount(ids[ids >= 0], minlength=wl.E)
+    assert (counts == 0).sum() >= 1 and counts.max() > 6 * T / wl.E
+    perm = oracle.permute(ids, wl.E)
+    np.testing.assert_array_equal(got["offsets"], perm["offsets"])
+    n = perm["rows"]
+    np.testing.assert_array_equal(got["row_src"][:n], perm["row_src"])
+    np.testing.assert_array_equal(got["row_dst"], perm["row_dst"])
+    check_tokens(wl, x, got, [0, 1, 2047, 4095], bias=bias)
+    sample = np.random.default_rng(3).choice(T, 48, replace=False)
+    r = oracle.route_topk(x[sample], wl.wr, bias, wl.table, wl.k)
+    np.testing.assert_array_equal(ids[sample], r["ids"])
+    np.testing.assert_array_equal(got["slots"][sample], r["slots"])
