@@ -89,24 +89,65 @@ __global__ void permute_tail_kernel(int n, int E, const int32_t* offsets, int32_
 
 // Validates group_offsets (monotone in [0, n]) and lists the non-empty groups with the
 // prefix of their tile counts (tile_rows rows per tile).  plan = [n_active, total_tiles, e_0.., tile_start_0..]
-__global__ void plan_kernel(int E, int n, const int32_t* offsets, int32_t* plan, int32_t* status, int tile_rows) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
-    int na = 0, tiles = 0, prev = 0;
-    bool bad = offsets[0] != 0;
-    for (int e = 0; e < E; ++e) {
-        int o0 = offsets[e], o1 = offsets[e + 1];
-        if (o0 < prev || o1 < o0 || o1 > n) { bad = true; break; }
-        prev = o0;
-        if (o1 > o0) {
-            plan[2 + na] = e;
-            plan[2 + E + na] = tiles;
-            tiles += (o1 - o0 + tile_rows - 1) / tile_rows;
-            ++na;
-        }
+// One block of 1024 threads, thread e = expert e (E <= 1024): block-wide exclusive scans of
+// "has rows" and "tiles of tile_rows rows" give each non-empty expert its group index and first
+// tile; every group writes its record and its tiles' entries of tile_group.  Offsets that are
+// not a valid group partition of n rows (or more tiles than max_tiles) give an empty plan and
+// MOE_STATUS_BAD_SLOT.
+__global__ void __launch_bounds__(1024) plan_kernel(int E, int n, const int32_t* __restrict__ offsets,
+                                                    const int32_t* __restrict__ row_src, const int32_t* __restrict__ slot,
+                                                    int nrows, int32_t* plan, int32_t* status, int tile_rows, int max_tiles) {
+    __shared__ int wa[32], wt[32];
+    __shared__ int bad_sh;
+    const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+    if (e == 0) bad_sh = (offsets[0] != 0);
+    __syncthreads();
+    int o0 = 0, o1 = 0, act = 0, nt = 0;
+    if (e < E) {
+        o0 = offsets[e];
+        o1 = offsets[e + 1];
+        if (o1 < o0 || o1 > n) bad_sh = 1;
+        act = o1 > o0;
+        nt = act ? (o1 - o0 + tile_rows - 1) / tile_rows : 0;
     }
-    if (bad) { na = 0; tiles = 0; atomicOr(status, MOE_STATUS_BAD_SLOT); }
-    plan[0] = na;
-    plan[1] = tiles;
+    // inclusive warp scans, then the warp totals
+    int sa = act, st = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int ya = __shfl_up_sync(0xffffffffu, sa, o), yt = __shfl_up_sync(0xffffffffu, st, o);
+        if (lane >= o) { sa += ya; st += yt; }
+    }
+    if (lane == 31) { wa[warp] = sa; wt[warp] = st; }
+    __syncthreads();
+    if (warp == 0) {
+        int a = wa[lane], t = wt[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ya = __shfl_up_sync(0xffffffffu, a, o), yt = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) { a += ya; t += yt; }
+        }
+        wa[lane] = a;   // inclusive over warps
+        wt[lane] = t;
+    }
+    __syncthreads();
+    const int g = sa - act + (warp > 0 ? wa[warp - 1] : 0);       // exclusive
+    const int ts = st - nt + (warp > 0 ? wt[warp - 1] : 0);
+    const int na = wa[31], tiles = wt[31];
+    const bool bad = bad_sh || tiles > max_tiles;
+    if (!bad && act) {
+        plan[2 + g] = e;
+        plan[2 + E + g] = ts;
+        const int src = row_src[o0];
+        const int sl = (src >= 0 && src < nrows) ? slot[src] : -1;
+        reinterpret_cast<int4*>(plan + plan_grec_off(E))[g] = make_int4(o0, o1, sl, ts);
+        int32_t* tg = plan + plan_tile_group_off(E);
+        for (int t = ts; t < ts + nt; ++t) tg[t] = g;
+    }
+    if (e == 0) {
+        plan[0] = bad ? 0 : na;
+        plan[1] = bad ? 0 : tiles;
+        if (bad) atomicOr(status, MOE_STATUS_BAD_SLOT);
+    }
 }
 
 // ---------------------------------------------------------------------------- grouped GEMM
@@ -332,7 +373,8 @@ int launch_prefill_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint
     a.rows = rows_out;
     a.status = status;
     if (T == 0) return MOE_OK;
-    plan_kernel<<<1, 32, 0, st>>>(a.E, a.n, offsets, reinterpret_cast<int32_t*>(ws + L.active), status, kBT);
+    plan_kernel<<<1, 1024, 0, st>>>(a.E, a.n, offsets, row_src, slot, a.n, reinterpret_cast<int32_t*>(ws + L.active),
+                                    status, kBT, (int)act_tiles(m, T));
     int blocks = 4 * num_sms;
     grouped_gemm_kernel<false><<<blocks, 256, 0, st>>>(a);
     grouped_gemm_kernel<true><<<blocks, 256, 0, st>>>(a);

@@ -79,6 +79,20 @@ enum { kCtrRoute = 0, kCtrFfnWork = 64, kCtrFfnXReady = 65, kCtrFfnExit = 66, kC
        kCtrFfnY = 256, kCounterWords = 1024 };
 inline size_t counter_words(const moe_dims*) { return kCounterWords; }
 
+// Prefill activation tiles: kPrefillNT permuted rows each (tensor-core path).  The plan of a
+// prefill call (written by plan_kernel) describes the expert groups and their tiles:
+//   int32 [0] n_active, [1] tiles, [2, 2+E) expert of group g, [2+E, 2+2E) first tile of g,
+//   int4  grec[E] at plan_grec_off(E): {first row, end row, arena slot, first tile} of g,
+//   int32 tile_group[max_tiles] at plan_tile_group_off(E): the group of each tile.
+constexpr int kPrefillNT = 32;
+inline size_t act_tiles(const moe_dims* m, int T) {
+    const size_t n = (size_t)(T > 0 ? T : 1) * m->top_k;
+    const size_t t = (n + kPrefillNT - 1) / kPrefillNT + (n < (size_t)m->num_experts ? n : (size_t)m->num_experts);
+    return t > 1 ? t : 1;
+}
+__host__ __device__ inline int plan_grec_off(int E) { return (2 + 2 * E + 3) / 4 * 4; }
+__host__ __device__ inline int plan_tile_group_off(int E) { return plan_grec_off(E) + 4 * E; }
+
 // Workspace sections, each 256-byte aligned.  The persistent counters come first so that
 // their offset is the same for every token count; the other sections are per call.
 struct WsLayout {
@@ -86,7 +100,7 @@ struct WsLayout {
     size_t xnorm;       // fp32 [T_max]      ||x_t||_2
     size_t wnorm;       // fp32 [E]          ||W_r[e]||_2
     size_t counter;     // uint32 [64]       completion tickets (zeroed once, self-resetting)
-    size_t active;      // int32 [2 + 2E]    group plan: n_active, tiles, expert ids, tile prefix
+    size_t active;      // prefill group plan (see plan_grec_off / plan_tile_group_off)
     size_t h;           // fp32 [T_max*k, f] SwiGLU output per (token, j) pair or permuted row
     size_t rows;        // fp32 [T_max*k, d] per-row expert outputs (prefill with fused combine)
     size_t tc;          // tensor-core path: quantised activations, quantised h, per-row outputs
@@ -108,7 +122,7 @@ inline WsLayout ws_layout(const moe_dims* m, int T_max) {
     w.keys = o;    o = align256(o + 16 * T * E);
     w.xnorm = o;   o = align256(o + 4 * T);
     w.wnorm = o;   o = align256(o + 4 * E);
-    w.active = o;  o = align256(o + 4 * (2 + 2 * E));
+    w.active = o;  o = align256(o + 4 * ((size_t)plan_tile_group_off((int)E) + act_tiles(m, (int)T)));
     w.h = o;       o = align256(o + 4 * T * k * (size_t)m->f);
     w.rows = o;
     if (T_max > kDecodeMaxT) o = align256(o + 4 * T * k * (size_t)m->d);

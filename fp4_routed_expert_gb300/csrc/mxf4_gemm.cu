@@ -35,9 +35,8 @@ constexpr int kKB = 256;              // K elements per stage
 constexpr int kKBytes = 128;          // code bytes per row per stage
 constexpr int kThreadsGemm = 6 * 32;
 constexpr int kTmemCols = 512;
-constexpr int kSfRing = 2;
-constexpr int kPrefillNT = 32;           // activation rows per tile (prefill)
-constexpr int kMaxNT = 64;               // activation rows per tile (decode: T*k pairs)               // scale buffers in TMEM (tcgen05.cp and MMAs run in issue order)
+constexpr int kSfRing = 2;                // scale buffers in TMEM (tcgen05.cp and MMAs run in issue order)
+constexpr int kMaxNT = 64;               // activation rows per tile (decode: T*k pairs)
 
 enum { kModeGateUp = 0, kModeDown = 1 };
 enum { kRegimeDecode = 0, kRegimePrefill = 1 };
@@ -140,6 +139,43 @@ __device__ __forceinline__ void warp_quantize32(float v, int lane, uint4* codes 
     }
 }
 
+// The same quantisation by one thread for the 32 values v (registers): the code words of term
+// t in w[t][0..3] (element i in word i/8, nibble i%8), its scale byte in sc[t].
+__device__ __forceinline__ void thread_quantize32(float (&v)[32], uint32_t (&w)[kTerms][4], uint32_t (&sc)[kTerms]) {
+#pragma unroll
+    for (int t = 0; t < kTerms; ++t) {
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        int e = -127;
+        const uint32_t u = __float_as_uint(amax);
+        if ((u >> 23) != 0u) {
+            const int e0 = (int)((u >> 23) & 0xFF) - 127;
+            const float m = __uint_as_float((u & 0x007FFFFFu) | 0x3F800000u);
+            e = (m <= 1.5f) ? e0 - 2 : e0 - 1;
+        }
+        e = max(-127, min(127, e));
+        sc[t] = (uint32_t)(e + 127);
+        const float inv = (e >= -126 && e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : 0.f;
+        const float scl = (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[t][k] = 0u;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float q = v[i] * inv;
+            const uint32_t c = e2m1_mag_code(fminf(fabsf(q), 6.0f));
+            const float val = e2m1_mag_value(c) * scl;
+            const bool neg = q < 0.f && c;
+            v[i] -= neg ? -val : val;
+            w[t][i >> 3] |= (c | (neg ? 8u : 0u)) << (4 * (i & 7));
+        }
+    }
+}
+
+// Padded index of h value i (0..63) of column c in the gate/up epilogue's shared tile: the
+// 32-value blocks start 33 words apart, so threads reading one block each hit distinct banks.
+__device__ __forceinline__ int hidx(int c, int i) { return c * 66 + (i >> 5) * 33 + (i & 31); }
+
 // Activation operands are kept in tiles: tile (t, kb) holds the kTerms x NT rows of B
 // (row r' = term*NT + row, codes pre-swizzled, 128 bytes per row) and their scale atoms,
 // 1 KB per 128 rows of r'.
@@ -152,26 +188,15 @@ __device__ __forceinline__ int64_t act_scale_off(int tile, int kb, int term, int
     return (((int64_t)tile * KB + kb) * blocks + (rr >> 7)) * 1024 + (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
 }
 
-// Group g of the plan holding tile `tile` (plan = [n_active, tiles, e_0.., tile_start_0..]).
-__device__ __forceinline__ int plan_group_of_tile(const int32_t* plan, int E, int tile) {
-    int lo = 0, hi = plan[0] - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (plan[2 + E + mid] <= tile) lo = mid; else hi = mid - 1;
-    }
-    return lo;
-}
-
-// Activations -> kTerms MXFP4 terms in tile layout, one warp per (tile, row, 32-element
-// block); also clears `nzero` counters for the GEMMs that follow.  Decode (plan == NULL): one tile, row r holds token r (rows >= T are zero).
-// Prefill: the plan's tiles; row r of tile t of group g holds permuted row
-// offsets[e_g] + NT*(t - tile_start_g) + r, i.e. token row_src[n]/k (rows past the group's
-// end are zero).
-__global__ void quantize_tiles_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row_src,
-                                      const int32_t* __restrict__ plan, const int32_t* __restrict__ offsets, int E, int k,
-                                      int T, int d, int NT, uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                      int32_t* __restrict__ zero, int nzero) {
-    const int lane = threadIdx.x & 31;
+// Prefill activations -> kTerms MXFP4 terms in tile layout, one thread per (tile, row,
+// 32-element block): row r of tile t of group g holds permuted row first_row_g + NT*(t -
+// first_tile_g) + r, i.e. token row_src[n]/k; rows past the group's end are zero.  Also
+// clears `nzero` counters for the FFN kernel that follows.
+__global__ void __launch_bounds__(256) quantize_tiles_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row_src,
+                                                             const int32_t* __restrict__ plan, int E, int k, int T, int d,
+                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                                             int32_t* __restrict__ zero, int nzero) {
+    constexpr int NT = kPrefillNT;
     // launched early behind the previous kernel: nothing it wrote is read before it completes;
     // the FFN kernel may launch at once (it waits for this kernel in turn)
     pdl_trigger();
@@ -179,43 +204,48 @@ __global__ void quantize_tiles_kernel(const uint16_t* __restrict__ x, const int3
     // the FFN kernel's counters start at zero
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += gridDim.x * blockDim.x) zero[i] = 0;
     const int nblk = d / 32, KB = d / kKB;
-    const int ntiles = plan ? plan[1] : 1;
-    const long total = (long)ntiles * NT * nblk;
-    const long gw = (blockIdx.x * (long)blockDim.x + threadIdx.x) >> 5, nw = ((long)gridDim.x * blockDim.x) >> 5;
-    for (long idx = gw; idx < total; idx += nw) {
+    const long total = (long)plan[1] * NT * nblk;
+    const int32_t* tgroup = plan + plan_tile_group_off(E);
+    const int4* grec = reinterpret_cast<const int4*>(plan + plan_grec_off(E));
+    for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
         const int b = (int)(idx % nblk);
         const int r = (int)((idx / nblk) % NT);
         const int tile = (int)(idx / ((long)nblk * NT));
+        const int4 gr = grec[tgroup[tile]];   // first row, end row, slot, first tile
+        const int n = gr.x + NT * (tile - gr.w) + r;
         int tok = -1;
-        if (!plan) {
-            tok = (r < T) ? r : -1;
-        } else {
-            const int g = plan_group_of_tile(plan, E, tile);
-            const int e = plan[2 + g];
-            const int n = offsets[e] + NT * (tile - plan[2 + E + g]) + r;
-            if (n < offsets[e + 1]) {
-                const int s = row_src[n];
-                tok = (s >= 0 && s < T * k) ? s / k : -1;
-            }
+        if (n < gr.y) {
+            const int s = row_src[n];
+            tok = (s >= 0 && s < T * k) ? s / k : -1;
         }
         const int kb = b / 8, j = b % 8;
+        uint32_t wds[kTerms][4], scl[kTerms];
         if (tok < 0) {                                       // padding row: zero codes, zero scale
-            if (lane < kTerms) {
-                *reinterpret_cast<uint4*>(q + act_code_off(tile, kb, lane, r, j, NT, KB)) = make_uint4(0, 0, 0, 0);
-                sf[act_scale_off(tile, kb, lane, r, j, NT, KB)] = 0;
-            }
-            continue;
-        }
-        const float v = bf16_to_f32(x[(size_t)tok * d + 32 * b + lane]);
-        uint4 codes[kTerms];
-        uint32_t scales[kTerms];
-        warp_quantize32(v, lane, codes, scales);
-        if (lane == 0) {
 #pragma unroll
             for (int t = 0; t < kTerms; ++t) {
-                *reinterpret_cast<uint4*>(q + act_code_off(tile, kb, t, r, j, NT, KB)) = codes[t];
-                sf[act_scale_off(tile, kb, t, r, j, NT, KB)] = (uint8_t)scales[t];
+                scl[t] = 0;
+                wds[t][0] = wds[t][1] = wds[t][2] = wds[t][3] = 0;
             }
+        } else {
+            const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * d + 32 * b);
+            float v[32];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint4 w4 = __ldg(src + u);
+                const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    v[8 * u + 2 * h] = bf16_lo(ww[h]);
+                    v[8 * u + 2 * h + 1] = bf16_hi(ww[h]);
+                }
+            }
+            thread_quantize32(v, wds, scl);
+        }
+#pragma unroll
+        for (int t = 0; t < kTerms; ++t) {
+            *reinterpret_cast<uint4*>(q + act_code_off(tile, kb, t, r, j, NT, KB)) =
+                make_uint4(wds[t][0], wds[t][1], wds[t][2], wds[t][3]);
+            sf[act_scale_off(tile, kb, t, r, j, NT, KB)] = (uint8_t)scl[t];
         }
     }
 }
@@ -237,7 +267,9 @@ struct FfnParams {
     int T, k, E, num_slots;
     const int32_t* slot;             // [T*k]
     const float* w;                  // [T*k] routing weights (decode combine)
-    const int32_t* plan;             // prefill: [n_active, tiles, e_0.., tile_start_0..] (NT-row tiles)
+    const int32_t* plan;             // prefill: the plan (see plan_grec_off / plan_tile_group_off)
+    const int32_t* tile_group;       // prefill: group of each tile
+    const int4* grec;                // prefill: {first row, end row, slot, first tile} per group
     const int32_t* offsets;
     const int32_t* row_src;
     const uint8_t* arena;
@@ -276,8 +308,8 @@ struct GemmCfg {
     static constexpr int kRows = kTerms * NT;
     static constexpr int kGroups = kRows > 128 ? kRows / 128 : 1;
     static constexpr int kN = kRows > 128 ? 128 : kRows;
-    static constexpr int kAcc = kRows <= 128 ? 2 : 1;
-    static constexpr int kDbuf = kRows <= 64 ? 2 : 1;
+    static constexpr int kAcc = kRows <= 64 ? 2 : 1;                    // short chains only at small N
+    static constexpr int kDbuf = 2 * kAcc * kRows <= 256 ? 2 : 1;
     static_assert(kDbuf * kAcc * kRows <= 256, "accumulators exceed their TMEM columns");
     static constexpr int kSfCols = 8 + 8 * kGroups;          // scale columns per stage (A + B)
     static constexpr int kA = kBM * kKBytes;                 // 16 KB
@@ -285,7 +317,7 @@ struct GemmCfg {
     static constexpr int kSFA = 1024;
     static constexpr int kSFB = kGroups * 1024;
     static constexpr int kStage = kA + kB + kSFA + kSFB;     // a multiple of 1024
-    static constexpr int kH = NT * 64 * 4;                   // gate/up epilogue h tile
+    static constexpr int kH = NT * 66 * 4;                   // gate/up epilogue h tile (padded rows)
     static constexpr int kBudget = 224 * 1024;               // dynamic smem (static use stays below 1 KB)
     static constexpr int kFit = (kBudget - kH - 2048) / kStage;
     static constexpr int kStages = kFit > 8 ? 8 : kFit;
@@ -314,25 +346,18 @@ __device__ __forceinline__ bool unit_info(const FfnParams& p, const PhaseParams&
         u.ncols = P.decode_cols;
         return true;
     }
-    // prefill: unit = tile_start[g]*mtiles + m*ntiles_g + ntile (tiles sharing weights adjacent)
-    const int E = p.E, na = p.plan[0];
-    int lo = 0, hi = na - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (p.plan[2 + E + mid] * P.mtiles <= unit) lo = mid; else hi = mid - 1;
-    }
-    const int g = lo, e = p.plan[2 + g];
-    const int o0 = p.offsets[e], o1 = p.offsets[e + 1];
-    const int ntiles = (o1 - o0 + NT - 1) / NT;
-    const int local = unit - p.plan[2 + E + g] * P.mtiles;
+    // prefill: unit = first_tile_g*mtiles + m*ntiles_g + ntile (tiles sharing weights adjacent),
+    // so unit / mtiles is a tile of group g
+    const int4 gr = p.grec[p.tile_group[unit / P.mtiles]];   // first row, end row, slot, first tile
+    const int ntiles = (gr.y - gr.x + NT - 1) / NT;
+    const int local = unit - gr.w * P.mtiles;
     u.m = local / ntiles;
     const int nt = local % ntiles;
-    u.btile = p.plan[2 + E + g] + nt;
+    u.btile = gr.w + nt;
     u.key = u.btile;
-    u.brow0 = o0 + nt * NT;
-    u.ncols = min(NT, o1 - u.brow0);
-    const int src = p.row_src[o0];
-    u.slot = (src >= 0 && src < p.T * p.k) ? p.slot[src] : -1;
+    u.brow0 = gr.x + nt * NT;
+    u.ncols = min(NT, gr.y - u.brow0);
+    u.slot = gr.z;
     return u.slot >= 0 && u.slot < p.num_slots;
 }
 
@@ -785,7 +810,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     const float partner = __shfl_xor_sync(0xffffffffu, vals[c], 1);
                     if ((lane & 1) == 0) {
                         const float g = vals[c];
-                        hbuf[c * 64 + (row >> 1)] = g / (1.0f + expf(-g)) * partner;
+                        hbuf[hidx(c, row >> 1)] = g / (1.0f + expf(-g)) * partner;
                     }
                 }
                 // hand-off 1: every warp's h values are in hbuf
@@ -797,12 +822,40 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                         break;
                     }
                 }
-                // quantise, one warp per job = (column c, block b of 32 outputs i0 = 64m + 32b)
-                for (int job = ew; job < u.ncols * 2; job += 4) {
+                // quantise; a job is (column c, block b of 32 outputs i0 = 64m + 32b).  Many
+                // jobs: one thread each; few: one warp each (shuffles, shorter latency)
+                if (u.ncols * 2 > 8) {
+                    const int job = ew * 32 + lane;
+                    if (job < u.ncols * 2) {
+                        const int c = job >> 1, b = job & 1;
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = hbuf[hidx(c, 32 * b + i)];
+                        uint32_t wds[kTerms][4], scl[kTerms];
+                        thread_quantize32(v, wds, scl);
+                        const int i0 = u.m * 64 + 32 * b, kb = i0 / kKB, j = (i0 % kKB) / 32;
+                        auto write_row_t = [&](int htile, int hrow) {
+                            if (dry) return;
+#pragma unroll
+                            for (int t = 0; t < kTerms; ++t) {
+                                *reinterpret_cast<uint4*>(p.hq + act_code_off(htile, kb, t, hrow, j, NT, KBf)) =
+                                    make_uint4(wds[t][0], wds[t][1], wds[t][2], wds[t][3]);
+                                p.hsf[act_scale_off(htile, kb, t, hrow, j, NT, KBf)] = (uint8_t)scl[t];
+                            }
+                        };
+                        if (p.regime == kRegimeDecode) {
+                            if (c < p.T)
+                                for (int jj = 0; jj < p.k; ++jj)
+                                    if (sslot[c * p.k + jj] == u.slot) write_row_t(0, c * p.k + jj);
+                        } else {
+                            write_row_t(u.btile, c);
+                        }
+                    }
+                } else for (int job = ew; job < u.ncols * 2; job += 4) {
                     const int c = job >> 1, b = job & 1;
                     uint4 codes[kTerms];
                     uint32_t scales[kTerms];
-                    warp_quantize32(hbuf[c * 64 + 32 * b + lane], lane, codes, scales);
+                    warp_quantize32(hbuf[hidx(c, 32 * b + lane)], lane, codes, scales);
                     const int i0 = u.m * 64 + 32 * b, kb = i0 / kKB, j = (i0 % kKB) / 32;
                     auto write_row = [&](int htile, int hrow) {
                         if (lane < kTerms && !dry) {
@@ -874,12 +927,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
 constexpr int kMaxGemmCtas = 160;
 
 // Capacity of the activation tile buffers for T tokens: decode uses one tile of up to kMaxNT
-// rows; the prefill plan needs at most ceil(T*k/NT) + min(E, T*k) tiles of kPrefillNT rows.
-static size_t act_tiles(const moe_dims* m, int T) {
-    const size_t n = (size_t)(T > 0 ? T : 1) * m->top_k;
-    const size_t t = (n + kPrefillNT - 1) / kPrefillNT + (n < (size_t)m->num_experts ? n : (size_t)m->num_experts);
-    return t > 1 ? t : 1;
-}
+// rows; the prefill plan needs at most act_tiles(m, T) tiles of kPrefillNT rows.
 static size_t act_rows(const moe_dims* m, int T) {
     const size_t r = act_tiles(m, T) * kPrefillNT;
     return r > (size_t)kMaxNT ? r : (size_t)kMaxNT;
@@ -1003,7 +1051,8 @@ int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16
     return launch_ffn_nt(NT, p, grid, st);
 }
 
-__global__ void plan_kernel(int E, int n, const int32_t* offsets, int32_t* plan, int32_t* status, int tile_rows);
+__global__ void plan_kernel(int E, int n, const int32_t* offsets, const int32_t* row_src, const int32_t* slot,
+                            int nrows, int32_t* plan, int32_t* status, int tile_rows, int max_tiles);
 
 // Prefill regime: x rows quantised into the plan's tiles (grouped by expert), then one FFN
 // launch (gate/up per (group, weight tile, row tile) with SwiGLU + h quantisation into the same
@@ -1014,15 +1063,18 @@ int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint1
     if (T == 0) return MOE_OK;
     TcBuffers b = tc_buffers(m, T, ws, L);
     const int d = m->d, k = m->top_k, n = T * k;
-    plan_kernel<<<1, 32, 0, st>>>(m->num_experts, n, offsets, b.plan, status, kPrefillNT);
-    const long qwarps = (long)act_tiles(m, T) * kPrefillNT * (d / 32);
-    const long qblocks = (qwarps + 7) / 8;
-    quantize_tiles_kernel<<<(int)(qblocks > 16L * num_sms ? 16L * num_sms : qblocks), 256, 0, st>>>(
-        x, row_src, b.plan, offsets, m->num_experts, k, T, d, kPrefillNT, b.xq, b.xsf, b.zero, (int)b.nzero);
+    plan_kernel<<<1, 1024, 0, st>>>(m->num_experts, n, offsets, row_src, slot, n, b.plan, status, kPrefillNT,
+                                    (int)act_tiles(m, T));
+    const long qjobs = (long)act_tiles(m, T) * kPrefillNT * (d / 32);
+    const long qblocks = (qjobs + 255) / 256;
+    quantize_tiles_kernel<<<(int)(qblocks > 8L * num_sms ? 8L * num_sms : qblocks), 256, 0, st>>>(
+        x, row_src, b.plan, m->num_experts, k, T, d, b.xq, b.xsf, b.zero, (int)b.nzero);
     note_launch(2);
     FfnParams p = ffn_params(m, ar, T, slot, status, b);
     p.regime = kRegimePrefill;
     p.plan = b.plan; p.offsets = offsets; p.row_src = row_src;
+    p.tile_group = b.plan + plan_tile_group_off(m->num_experts);
+    p.grec = reinterpret_cast<const int4*>(b.plan + plan_grec_off(m->num_experts));
     p.rows_out = rows_out;
     const int grid = num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas;
     return launch_ffn_nt(kPrefillNT, p, grid, st);
