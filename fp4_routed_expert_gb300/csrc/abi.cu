@@ -127,10 +127,10 @@ int moe_pack_expert(const moe_dims* dims, const uint8_t* gate_q, const uint8_t* 
     SlotLayout L = slot_layout(d, f);
     uint8_t* base = static_cast<uint8_t*>(arena->base) + (int64_t)slot * arena->slot_bytes;
     int sms = num_sms_of_current_device();
-    pack_codes_kernel<<<2 * sms, 256, 0, st>>>(gate_q, up_q, base + L.gu_q, 2 * f, d);
-    pack_scales_kernel<<<sms, 256, 0, st>>>(gate_s, up_s, base + L.gu_s, 2 * f, d);
-    pack_codes_kernel<<<2 * sms, 256, 0, st>>>(down_q, nullptr, base + L.dn_q, d, f);
-    pack_scales_kernel<<<sms, 256, 0, st>>>(down_s, nullptr, base + L.dn_s, d, f);
+    pack_codes_kernel<<<2 * sms, 256, 0, st>>>(gate_q, up_q, base + L.gu, 2 * f, d);
+    pack_scales_kernel<<<sms, 256, 0, st>>>(gate_s, up_s, base + L.gu, 2 * f, d);
+    pack_codes_kernel<<<2 * sms, 256, 0, st>>>(down_q, nullptr, base + L.dn, d, f);
+    pack_scales_kernel<<<sms, 256, 0, st>>>(down_s, nullptr, base + L.dn, d, f);
     note_launch(4);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_LAUNCH;
     return MOE_OK;

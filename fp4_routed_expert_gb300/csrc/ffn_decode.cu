@@ -146,8 +146,8 @@ __global__ void __launch_bounds__(256) decode_gateup_kernel(DecodeArgs a) {
     for (int it = gw; it < items; it += nw) {
         const int u = it / f, i = it % f;
         const uint8_t* base = a.arena + (int64_t)uniq_slot[u] * a.slot_bytes;
-        const uint8_t* cq = base + a.L.gu_q;   // gate row 2i, up row 2i+1 of the tiled matrix
-        const uint8_t* cs = base + a.L.gu_s;
+        const uint8_t* cq = base + a.L.gu;   // gate row 2i, up row 2i+1 of the tiled matrix
+        const uint8_t* cs = base + a.L.gu;
         float accg[XT], accu[XT];
 #pragma unroll
         for (int q = 0; q < XT; ++q) accg[q] = accu[q] = 0.f;
@@ -228,8 +228,8 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
                 int s = a.slot[pair];
                 if (s < 0 || s >= a.num_slots) continue;   // group-uniform: same pair for the warp
                 const uint8_t* base = a.arena + (int64_t)s * a.slot_bytes;
-                const uint8_t* dq = base + a.L.dn_q;
-                const uint8_t* ds = base + a.L.dn_s;
+                const uint8_t* dq = base + a.L.dn;
+                const uint8_t* ds = base + a.L.dn;
                 const int p = pexp[j];
                 float acc = 0.f;
                 for (int c0 = l8; c0 < nchunk; c0 += 8 * 9) {

@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(256) grouped_gemm_kernel(GroupedArgs a) {
         const bool slot_ok = s >= 0 && s < a.num_slots;
         if (!slot_ok && tid == 0 && rt == 0) atomicOr(a.status, MOE_STATUS_BAD_SLOT);
         const uint8_t* base = a.arena + (slot_ok ? (int64_t)s * a.slot_bytes : 0);
-        const uint8_t* wq = base + (DOWN ? a.L.dn_q : a.L.gu_q);
-        const uint8_t* wsb = base + (DOWN ? a.L.dn_s : a.L.gu_s);
+        const uint8_t* wq = base + (DOWN ? a.L.dn : a.L.gu);
+        const uint8_t* wsb = base + (DOWN ? a.L.dn : a.L.gu);
         float acc[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)

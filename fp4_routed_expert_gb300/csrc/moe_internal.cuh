@@ -33,37 +33,41 @@ constexpr int kTileRows = 128;      // rows per arena tile
 constexpr int kTileK = 256;         // K elements per arena tile
 constexpr int kTileCodeBytes = 16384;
 constexpr int kTileScaleBytes = 1024;
+constexpr int kTileBytes = kTileCodeBytes + kTileScaleBytes;   // a tile: its codes, then its scale atoms
 
+// A slot holds two matrices, gate/up (2f rows interleaved gate/up, K = d) and then down
+// (d rows, K = f), each as tiles of 128 rows x 256 K elements in (row tile, K tile) order.
+// A tile is 16 KB of codes (pre-swizzled for SWIZZLE_128B) followed by its 1 KB of scale
+// atoms, so one contiguous copy brings a tile, or a run of tiles along K, with its scales.
 struct SlotLayout {
-    int64_t gu_q, gu_s, dn_q, dn_s, bytes;
+    int64_t gu, dn, bytes;   // matrix offsets inside the slot, slot size
 };
 
 __host__ __device__ inline SlotLayout slot_layout(int d, int f) {
     SlotLayout L;
-    int64_t fd = (int64_t)f * d;
-    L.gu_q = 0;
-    L.gu_s = fd;
-    L.dn_q = fd + fd / 16;
-    L.dn_s = L.dn_q + fd / 2;
-    int64_t end = L.dn_s + fd / 32;
+    const int64_t fd = (int64_t)f * d;
+    L.gu = 0;
+    L.dn = (fd / 16384) * kTileBytes;                  // (2f/128) x (d/256) tiles
+    const int64_t end = L.dn + (fd / 32768) * kTileBytes;   // (d/128) x (f/256) tiles
     L.bytes = (end + 1023) / 1024 * 1024;
     return L;
 }
 
-// Offset, inside a matrix's code region, of 16-byte chunk `chunk` (K elements 32*chunk..+31)
-// of matrix row `row`, for a matrix with reduction length K.
+// Offset, from a matrix's start, of 16-byte code chunk `chunk` (K elements 32*chunk..+31) of
+// matrix row `row`, for a matrix with reduction length K.
 __host__ __device__ inline int64_t code_chunk_off(int row, int chunk, int K) {
     const int64_t tile = (int64_t)(row / kTileRows) * (K / kTileK) + chunk / 8;
     const int r = row % kTileRows;
-    return tile * kTileCodeBytes + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
+    return tile * kTileBytes + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
 }
 
-// Offset, inside a matrix's scale region, of the scale byte of K block `kb` (32 elements)
-// of matrix row `row`.
+// Offset, from a matrix's start, of the scale byte of K block `kb` (32 elements) of matrix
+// row `row`: in the tile's scale atoms (32-row atoms of 16 bytes per row, two atoms per 128
+// rows' 8 blocks, the layout tcgen05.cp 32x128b.warpx4 reads).
 __host__ __device__ inline int64_t scale_off(int row, int kb, int K) {
     const int64_t tile = (int64_t)(row / kTileRows) * (K / kTileK) + kb / 8;
     const int r = row % kTileRows, j = kb & 7;
-    return tile * kTileScaleBytes + (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
+    return tile * kTileBytes + kTileCodeBytes + (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
 }
 
 inline bool dims_ok(const moe_dims* m) {

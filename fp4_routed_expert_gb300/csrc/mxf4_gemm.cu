@@ -10,13 +10,15 @@
 // quantising the residual left by q_1..q_(i-1)); the MMA accumulates every term into the same
 // fp32 accumulator, so D = W . x up to the residual after kTerms terms.
 //
-// Every operand sits in global memory in 16 KB code tiles (128 rows x 256 K elements,
-// pre-swizzled for SWIZZLE_128B) and 1 KB scale-atom tiles, so each pipeline stage is four
-// contiguous bulk copies (cp.async.bulk) into shared memory.
+// Every operand sits in global memory in blocks of 256 K elements that carry their codes
+// (128-byte rows pre-swizzled for SWIZZLE_128B) followed by their scale atoms, and the blocks
+// of one row tile are consecutive along K.  A pipeline stage spans kKPS such K blocks and is
+// two contiguous bulk copies (cp.async.bulk), weights and activations: a bulk copy costs the
+// SM's copy engine a fixed time on top of its bytes, so few large copies stream fastest.
 //
 // One persistent kernel, one CTA per SM, 6 warps:
-//   warp 0  producer: bulk copies of the weight tile, its scale atoms, the kTerms activation
-//           tiles (NT rows) and their scale atoms per 256-element K block
+//   warp 0  producer: per stage one bulk copy of the weight tiles (codes + scale atoms) and
+//           one of the activation blocks (kTerms x NT rows + scale atoms)
 //   warp 1  MMA issuer (one lane): tcgen05.cp of the scale atoms, 4 x kTerms MMAs per
 //           K block, tcgen05.commit to release smem stages and publish accumulators
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (double-buffered in TMEM), then
@@ -31,7 +33,7 @@ namespace fp4moe {
 
 constexpr int kTerms = 4;
 constexpr int kBM = 128;              // weight rows per tile
-constexpr int kKB = 256;              // K elements per stage
+constexpr int kKB = 256;              // K elements per K block
 constexpr int kKBytes = 128;          // code bytes per row per stage
 constexpr int kThreadsGemm = 6 * 32;
 constexpr int kTmemCols = 512;
@@ -176,16 +178,18 @@ __device__ __forceinline__ void thread_quantize32(float (&v)[32], uint32_t (&w)[
 // 32-value blocks start 33 words apart, so threads reading one block each hit distinct banks.
 __device__ __forceinline__ int hidx(int c, int i) { return c * 66 + (i >> 5) * 33 + (i & 31); }
 
-// Activation operands are kept in tiles: tile (t, kb) holds the kTerms x NT rows of B
-// (row r' = term*NT + row, codes pre-swizzled, 128 bytes per row) and their scale atoms,
-// 1 KB per 128 rows of r'.
+// Activation operands are kept in blocks: block (tile t, K block kb) holds the kTerms x NT
+// rows of B (row r' = term*NT + row, codes pre-swizzled, 128 bytes per row) followed by their
+// scale atoms, 1 KB per 128 rows of r'; the KB blocks of a tile are consecutive.
+__host__ __device__ constexpr int act_block_bytes(int NT) { return kTerms * NT * 128 + (kTerms * NT + 127) / 128 * 1024; }
 __device__ __forceinline__ int64_t act_code_off(int tile, int kb, int term, int row, int chunk, int NT, int KB) {
-    return (((int64_t)tile * KB + kb) * kTerms + term) * NT * 128 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+    return ((int64_t)tile * KB + kb) * act_block_bytes(NT) + (term * NT + row) * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 __device__ __forceinline__ int64_t act_scale_off(int tile, int kb, int term, int row, int j /*0..7*/, int NT, int KB) {
-    const int rr = term * NT + row, blocks = (kTerms * NT + 127) / 128;
+    const int rr = term * NT + row;
     const int r = rr & 127;
-    return (((int64_t)tile * KB + kb) * blocks + (rr >> 7)) * 1024 + (j >> 2) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
+    return ((int64_t)tile * KB + kb) * act_block_bytes(NT) + kTerms * NT * 128 + (rr >> 7) * 1024 + (j >> 2) * 512 +
+           (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
 }
 
 // Prefill activations -> kTerms MXFP4 terms in tile layout, one thread per (tile, row,
@@ -194,8 +198,7 @@ __device__ __forceinline__ int64_t act_scale_off(int tile, int kb, int term, int
 // clears `nzero` counters for the FFN kernel that follows.
 __global__ void __launch_bounds__(256) quantize_tiles_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row_src,
                                                              const int32_t* __restrict__ plan, int E, int k, int T, int d,
-                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                             int32_t* __restrict__ zero, int nzero) {
+                                                             uint8_t* __restrict__ q, int32_t* __restrict__ zero, int nzero) {
     constexpr int NT = kPrefillNT;
     // launched early behind the previous kernel: nothing it wrote is read before it completes;
     // the FFN kernel may launch at once (it waits for this kernel in turn)
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(256) quantize_tiles_kernel(const uint16_t* __r
         for (int t = 0; t < kTerms; ++t) {
             *reinterpret_cast<uint4*>(q + act_code_off(tile, kb, t, r, j, NT, KB)) =
                 make_uint4(wds[t][0], wds[t][1], wds[t][2], wds[t][3]);
-            sf[act_scale_off(tile, kb, t, r, j, NT, KB)] = (uint8_t)scl[t];
+            q[act_scale_off(tile, kb, t, r, j, NT, KB)] = (uint8_t)scl[t];
         }
     }
 }
@@ -256,9 +259,8 @@ __global__ void __launch_bounds__(256) quantize_tiles_kernel(const uint16_t* __r
 // (phase 1, K = f, weight rows d).
 struct PhaseParams {
     int kblocks, mtiles;             // K / 256, weight rows / 128
-    int64_t a_code_off, a_sf_off;    // weight matrix regions inside a slot
-    const uint8_t* b_q;              // activation tiles (codes)
-    const uint8_t* b_sf;             // activation tiles (scale atoms)
+    int64_t a_off;                   // the weight matrix inside a slot
+    const uint8_t* b;                // activation blocks
     int decode_cols;                 // decode: valid columns (B rows) of every unit
 };
 
@@ -275,8 +277,7 @@ struct FfnParams {
     const uint8_t* arena;
     int64_t slot_bytes;
     PhaseParams ph[2];
-    uint8_t* hq;                     // h tiles written by phase 0, read by phase 1 (codes)
-    uint8_t* hsf;                    // h tiles (scale atoms)
+    uint8_t* h;                      // h blocks written by phase 0, read by phase 1
     int f, d;
     float* rows_out;                 // phase 1 output rows [rows][d] (fp32)
     uint16_t* y;                     // decode: combined output [T][d] (bf16)
@@ -311,12 +312,13 @@ struct GemmCfg {
     static constexpr int kAcc = kRows <= 64 ? 2 : 1;                    // short chains only at small N
     static constexpr int kDbuf = 2 * kAcc * kRows <= 256 ? 2 : 1;
     static_assert(kDbuf * kAcc * kRows <= 256, "accumulators exceed their TMEM columns");
-    static constexpr int kSfCols = 8 + 8 * kGroups;          // scale columns per stage (A + B)
-    static constexpr int kA = kBM * kKBytes;                 // 16 KB
-    static constexpr int kB = kRows * kKBytes;
-    static constexpr int kSFA = 1024;
-    static constexpr int kSFB = kGroups * 1024;
-    static constexpr int kStage = kA + kB + kSFA + kSFB;     // a multiple of 1024
+    static constexpr int kSfCols = 8 + 8 * kGroups;          // scale columns per K block (A + B)
+    static constexpr int kBCodes = kRows * kKBytes;          // activation codes per K block
+    static constexpr int kBBlk = act_block_bytes(NT);        // activation block (codes + atoms)
+    static constexpr int kKPS = 2;                           // K blocks per stage
+    // stage: kKPS weight tiles (kTileBytes each), then kKPS activation blocks; every operand
+    // start is a multiple of 1024 bytes
+    static constexpr int kStage = kKPS * (kTileBytes + kBBlk);
     static constexpr int kH = NT * 66 * 4;                   // gate/up epilogue h tile (padded rows)
     static constexpr int kBudget = 224 * 1024;               // dynamic smem (static use stays below 1 KB)
     static constexpr int kFit = (kBudget - kH - 2048) / kStage;
@@ -395,7 +397,6 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     __shared__ int abort_flag;
     __shared__ int n_keys_sh, pairs_total_sh;
     __shared__ int fix_last;
-    __shared__ int wcount[8];
     __shared__ int uslots[kMaxNT];
     __shared__ int upairs[kMaxNT];
     __shared__ int sslot[kMaxNT];                // decode: the routing outputs of the T*k pairs
@@ -440,8 +441,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     // router's) does not write it.
     if (p.x_src && warp >= 2) {
         const int nblk = p.d / 32, KBd = p.d / kKB, total = p.T * nblk;
-        uint8_t* q = const_cast<uint8_t*>(p.ph[0].b_q);
-        uint8_t* sf = const_cast<uint8_t*>(p.ph[0].b_sf);
+        uint8_t* q = const_cast<uint8_t*>(p.ph[0].b);
         while (true) {
             int job = 0;
             if (lane == 0) job = atomicAdd(p.xjob, 1);
@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 for (int t = 1; t < kTerms; ++t)
                     if (lane == t) { cv = codes[t]; sv = scales[t]; }
                 *reinterpret_cast<uint4*>(q + act_code_off(0, kb, lane, r, j, NT, KBd)) = cv;
-                sf[act_scale_off(0, kb, lane, r, j, NT, KBd)] = (uint8_t)sv;
+                q[act_scale_off(0, kb, lane, r, j, NT, KBd)] = (uint8_t)sv;
             }
             fence_proxy_async();   // read by the async proxy (bulk copies) of every CTA
             __syncwarp();
@@ -554,16 +554,17 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 // the CTAs; down: h of its key) gets its weight copies issued into every free
                 // stage; the activation copies of those stages follow once they are ready.
                 bool have_b = (ph == 0) ? x_ok : !(ok && u.key != ready_key);
-                int pend_n = 0, pend_kb0 = 0, pend_stage0 = 0;
-                auto issue_b = [&](int kb, int stg) {
-                    const uint32_t sb = smem_u32(stage_base + stg * C::kStage);
-                    const uint32_t bar = smem_u32(&full[stg]);
-                    const int64_t btile = (int64_t)u.btile * P.kblocks + kb;
-                    bulk_g2s(sb + C::kA, P.b_q + btile * C::kB, C::kB, bar);
-                    bulk_g2s(sb + C::kA + C::kB + C::kSFA, P.b_sf + btile * C::kSFB, C::kSFB, bar);
+                const int nst = (P.kblocks + C::kKPS - 1) / C::kKPS;   // stages of this unit
+                int pend_n = 0, pend_s0 = 0, pend_stage0 = 0;
+                // activation blocks of stage s of the unit (K blocks kKPS*s ..) into smem stage stg
+                auto issue_b = [&](int s, int stg) {
+                    const int kb = s * C::kKPS, nkb = min(C::kKPS, P.kblocks - kb);
+                    const int64_t blk = (int64_t)u.btile * P.kblocks + kb;
+                    bulk_g2s(smem_u32(stage_base + stg * C::kStage + C::kKPS * kTileBytes), P.b + blk * C::kBBlk,
+                             nkb * C::kBBlk, smem_u32(&full[stg]));
                 };
                 auto flush = [&]() {
-                    for (int i = 0; i < pend_n; ++i) issue_b(pend_kb0 + i, (pend_stage0 + i) % C::kStages);
+                    for (int i = 0; i < pend_n; ++i) issue_b(pend_s0 + i, (pend_stage0 + i) % C::kStages);
                     pend_n = 0;
                 };
                 auto key_ready = [&](bool block) -> bool {
@@ -587,7 +588,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     have_b = true;
                     return true;
                 };
-                for (int kb = 0; kb < P.kblocks; ++kb) {
+                for (int s = 0; s < nst; ++s) {
                     if (pend_n == C::kStages) {   // the next stage still waits for its h copy
                         key_ready(true);
                         flush();
@@ -599,15 +600,15 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     }
                     const uint32_t st = smem_u32(stage_base + stage * C::kStage);
                     const uint32_t bar = smem_u32(&full[stage]);
+                    const int kb = s * C::kKPS, nkb = min(C::kKPS, P.kblocks - kb);
                     const int64_t atile = (int64_t)u.m * P.kblocks + kb;
-                    mbar_expect_tx(bar, C::kStage);
-                    bulk_g2s(st, sbase + P.a_code_off + atile * kTileCodeBytes, C::kA, bar);
-                    bulk_g2s(st + C::kA + C::kB, sbase + P.a_sf_off + atile * kTileScaleBytes, C::kSFA, bar);
+                    mbar_expect_tx(bar, nkb * (kTileBytes + C::kBBlk));
+                    bulk_g2s(st, sbase + P.a_off + atile * kTileBytes, nkb * kTileBytes, bar);
                     if (!have_b && key_ready(false)) flush();
                     if (have_b) {
-                        issue_b(kb, stage);
+                        issue_b(s, stage);
                     } else {
-                        if (pend_n == 0) { pend_kb0 = kb; pend_stage0 = stage; }
+                        if (pend_n == 0) { pend_s0 = s; pend_stage0 = stage; }
                         ++pend_n;
                     }
                     issued |= 1u << stage;
@@ -648,7 +649,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 tc_fence_after();
                 const uint32_t dset = tmem + acc * C::kAcc * C::kRows;
                 bool failed = false;
-                for (int kb = 0; kb < KB; ++kb) {
+                const int nst = (KB + C::kKPS - 1) / C::kKPS;
+                for (int s = 0; s < nst; ++s) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abortp)) {
                         atomicOr(p.status, MOE_STATUS_TIMEOUT);
                         *abortp = 1;
@@ -657,31 +659,37 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     }
                     tc_fence_after();
                     uint8_t* st = stage_base + stage * C::kStage;
-                    const uint32_t sa = smem_u32(st), sb = smem_u32(st + C::kA);
-                    const uint32_t ssfa = smem_u32(st + C::kA + C::kB), ssfb = ssfa + C::kSFA;
-                    const uint32_t sfcol = tmem + 256 + sfring * C::kSfCols;
-                    tc_cp_sf(sfcol + 0, desc_sf(ssfa));
-                    tc_cp_sf(sfcol + 4, desc_sf(ssfa + 512));
+                    const int nkb = min(C::kKPS, KB - s * C::kKPS);
 #pragma unroll
-                    for (int g = 0; g < C::kGroups; ++g) {
-                        tc_cp_sf(sfcol + 8 + 8 * g, desc_sf(ssfb + g * 1024));
-                        tc_cp_sf(sfcol + 8 + 8 * g + 4, desc_sf(ssfb + g * 1024 + 512));
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int a = j % C::kAcc;
-                        const uint64_t ad = desc_sw128(sa + 32 * j);
-                        const uint32_t accumulate = (kb > 0 || j >= C::kAcc) ? 1u : 0u;
+                    for (int i = 0; i < C::kKPS; ++i) {
+                        if (i >= nkb) break;
+                        const uint32_t sa = smem_u32(st + i * kTileBytes);
+                        const uint32_t sb = smem_u32(st + C::kKPS * kTileBytes + i * C::kBBlk);
+                        const uint32_t ssfa = sa + kTileCodeBytes, ssfb = sb + C::kBCodes;
+                        const uint32_t sfcol = tmem + 256 + sfring * C::kSfCols;
+                        tc_cp_sf(sfcol + 0, desc_sf(ssfa));
+                        tc_cp_sf(sfcol + 4, desc_sf(ssfa + 512));
 #pragma unroll
                         for (int g = 0; g < C::kGroups; ++g) {
-                            const uint64_t bd = desc_sw128(sb + g * 128 * kKBytes + 32 * j);
-                            mma_mxf4(dset + a * C::kRows + g * 128, ad, bd, (j & 1) ? idesc_hi : idesc_lo,
-                                     sfcol + 4 * (j >> 1), sfcol + 8 + 8 * g + 4 * (j >> 1), accumulate);
+                            tc_cp_sf(sfcol + 8 + 8 * g, desc_sf(ssfb + g * 1024));
+                            tc_cp_sf(sfcol + 8 + 8 * g + 4, desc_sf(ssfb + g * 1024 + 512));
                         }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int a = j % C::kAcc;
+                            const uint64_t ad = desc_sw128(sa + 32 * j);
+                            const uint32_t accumulate = (s > 0 || i > 0 || j >= C::kAcc) ? 1u : 0u;
+#pragma unroll
+                            for (int g = 0; g < C::kGroups; ++g) {
+                                const uint64_t bd = desc_sw128(sb + g * 128 * kKBytes + 32 * j);
+                                mma_mxf4(dset + a * C::kRows + g * 128, ad, bd, (j & 1) ? idesc_hi : idesc_lo,
+                                         sfcol + 4 * (j >> 1), sfcol + 8 + 8 * g + 4 * (j >> 1), accumulate);
+                            }
+                        }
+                        sfring = (sfring + 1) % kSfRing;
                     }
                     tc_commit(smem_u32(&empty[stage]));
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-                    sfring = (sfring + 1) % kSfRing;
                 }
                 if (failed) break;
                 tc_commit(smem_u32(&tfull[acc]));
@@ -838,9 +846,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                             if (dry) return;
 #pragma unroll
                             for (int t = 0; t < kTerms; ++t) {
-                                *reinterpret_cast<uint4*>(p.hq + act_code_off(htile, kb, t, hrow, j, NT, KBf)) =
+                                *reinterpret_cast<uint4*>(p.h + act_code_off(htile, kb, t, hrow, j, NT, KBf)) =
                                     make_uint4(wds[t][0], wds[t][1], wds[t][2], wds[t][3]);
-                                p.hsf[act_scale_off(htile, kb, t, hrow, j, NT, KBf)] = (uint8_t)scl[t];
+                                p.h[act_scale_off(htile, kb, t, hrow, j, NT, KBf)] = (uint8_t)scl[t];
                             }
                         };
                         if (p.regime == kRegimeDecode) {
@@ -865,8 +873,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
 #pragma unroll
                             for (int t = 1; t < kTerms; ++t)
                                 if (lane == t) { cv = codes[t]; sv = scales[t]; }
-                            *reinterpret_cast<uint4*>(p.hq + act_code_off(htile, kb, lane, hrow, j, NT, KBf)) = cv;
-                            p.hsf[act_scale_off(htile, kb, lane, hrow, j, NT, KBf)] = (uint8_t)sv;
+                            *reinterpret_cast<uint4*>(p.h + act_code_off(htile, kb, lane, hrow, j, NT, KBf)) = cv;
+                            p.h[act_scale_off(htile, kb, lane, hrow, j, NT, KBf)] = (uint8_t)sv;
                         }
                     };
                     if (p.regime == kRegimeDecode) {
@@ -926,16 +934,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
 
 constexpr int kMaxGemmCtas = 160;
 
-// Capacity of the activation tile buffers for T tokens: decode uses one tile of up to kMaxNT
-// rows; the prefill plan needs at most act_tiles(m, T) tiles of kPrefillNT rows.
-static size_t act_rows(const moe_dims* m, int T) {
-    const size_t r = act_tiles(m, T) * kPrefillNT;
-    return r > (size_t)kMaxNT ? r : (size_t)kMaxNT;
-}
-static size_t act_sf_blocks(const moe_dims* m, int T) {      // 1 KB scale blocks per K block
-    const size_t b = act_tiles(m, T) * ((kTerms * kPrefillNT + 127) / 128);
-    const size_t dec = (kTerms * kMaxNT + 127) / 128;
-    return b > dec ? b : dec;
+// Capacity of an activation buffer (x or h, reduction length K) for T tokens: decode uses one
+// tile of up to kMaxNT rows; the prefill plan needs at most act_tiles(m, T) tiles of
+// kPrefillNT rows; a tile is K/256 blocks of act_block_bytes(NT).
+static size_t act_bytes(const moe_dims* m, int T, int K) {
+    const size_t dec = (size_t)act_block_bytes(kMaxNT), pre = act_tiles(m, T) * (size_t)act_block_bytes(kPrefillNT);
+    return (size_t)(K / kKB) * (dec > pre ? dec : pre);
 }
 // keys (decode: slot ordinals; prefill: tiles) and units of either phase
 static size_t max_keys(const moe_dims* m, int T) {
@@ -943,7 +947,7 @@ static size_t max_keys(const moe_dims* m, int T) {
 }
 
 struct TcBuffers {
-    uint8_t *xq, *xsf, *hq, *hsf;
+    uint8_t *x, *h;        // activation blocks of x (K = d) and h (K = f)
     int32_t* zero;         // counters cleared by the quantiser: work, ready[nkeys], ycnt[d/128]
     size_t nkeys, nzero;
     float* rows;
@@ -954,12 +958,9 @@ static size_t counters_of(const moe_dims* m, int T) { return 1 + max_keys(m, T) 
 
 static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& L) {
     TcBuffers b;
-    const size_t rows = act_rows(m, T), sfb = act_sf_blocks(m, T);
     char* o = ws + L.tc;
-    b.xq = reinterpret_cast<uint8_t*>(o);  o += align256(rows * kTerms * m->d / 2);
-    b.xsf = reinterpret_cast<uint8_t*>(o); o += align256(sfb * (m->d / kKB) * 1024);
-    b.hq = reinterpret_cast<uint8_t*>(o);  o += align256(rows * kTerms * m->f / 2);
-    b.hsf = reinterpret_cast<uint8_t*>(o); o += align256(sfb * (m->f / kKB) * 1024);
+    b.x = reinterpret_cast<uint8_t*>(o); o += align256(act_bytes(m, T, m->d));
+    b.h = reinterpret_cast<uint8_t*>(o); o += align256(act_bytes(m, T, m->f));
     b.nkeys = max_keys(m, T);
     b.nzero = counters_of(m, T);
     b.zero = reinterpret_cast<int32_t*>(o); o += align256(b.nzero * 4);
@@ -970,9 +971,8 @@ static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& 
 
 size_t tc_workspace_bytes(const moe_dims* m, int T) {
     const size_t R = (size_t)(T > 0 ? T : 1) * m->top_k;
-    const size_t rows = act_rows(m, T), sfb = act_sf_blocks(m, T);
-    return align256(rows * kTerms * m->d / 2) + align256(sfb * (m->d / kKB) * 1024) + align256(rows * kTerms * m->f / 2) +
-           align256(sfb * (m->f / kKB) * 1024) + align256(counters_of(m, T) * 4) + align256(R * m->d * 4);
+    return align256(act_bytes(m, T, m->d)) + align256(act_bytes(m, T, m->f)) + align256(counters_of(m, T) * 4) +
+           align256(R * m->d * 4);
 }
 
 template <int NT>
@@ -1009,13 +1009,13 @@ static FfnParams ffn_params(const moe_dims* m, const moe_arena* ar, int T, const
     p.f = m->f; p.d = m->d; p.status = status;
     PhaseParams& g = p.ph[0];
     g.kblocks = m->d / kKB; g.mtiles = 2 * m->f / kBM;
-    g.a_code_off = SL.gu_q; g.a_sf_off = SL.gu_s;
-    g.b_q = b.xq; g.b_sf = b.xsf;
+    g.a_off = SL.gu;
+    g.b = b.x;
     PhaseParams& dn = p.ph[1];
     dn.kblocks = m->f / kKB; dn.mtiles = m->d / kBM;
-    dn.a_code_off = SL.dn_q; dn.a_sf_off = SL.dn_s;
-    dn.b_q = b.hq; dn.b_sf = b.hsf;
-    p.hq = b.hq; p.hsf = b.hsf;
+    dn.a_off = SL.dn;
+    dn.b = b.h;
+    p.h = b.h;
     p.work = b.zero;
     p.ready = b.zero + 1;
     p.ycnt = b.zero + 1 + b.nkeys;
@@ -1068,7 +1068,7 @@ int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint1
     const long qjobs = (long)act_tiles(m, T) * kPrefillNT * (d / 32);
     const long qblocks = (qjobs + 255) / 256;
     quantize_tiles_kernel<<<(int)(qblocks > 8L * num_sms ? 8L * num_sms : qblocks), 256, 0, st>>>(
-        x, row_src, b.plan, m->num_experts, k, T, d, b.xq, b.xsf, b.zero, (int)b.nzero);
+        x, row_src, b.plan, m->num_experts, k, T, d, b.x, b.zero, (int)b.nzero);
     note_launch(2);
     FfnParams p = ffn_params(m, ar, T, slot, status, b);
     p.regime = kRegimePrefill;
