@@ -76,19 +76,30 @@ __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-// Asynchronous 32x32b.x16 load: the registers are valid only after tc_wait_ld16 on them (the
-// wait takes them as operands, so no use can be scheduled before it).
-__device__ __forceinline__ void tc_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+// Asynchronous 32x32b.x16 / .x8 loads: the registers are valid only after tc_wait_ld on them
+// (the wait takes them as operands, so no use can be scheduled before it).
+__device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
           "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
-__device__ __forceinline__ void tc_wait_ld16(uint32_t (&r)[16]) {
+__device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
                    "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+__device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[8]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
                  :
                  : "memory");
 }
@@ -320,7 +331,8 @@ struct GemmCfg {
     // start is a multiple of 1024 bytes
     static constexpr int kStage = kKPS * (kTileBytes + kBBlk);
     static constexpr int kH = NT * 66 * 4;                   // gate/up epilogue h tile (padded rows)
-    static constexpr int kBudget = 224 * 1024;               // dynamic smem (static use stays below 1 KB)
+    static constexpr int kLdW = NT < 16 ? NT : 16;           // accumulator columns per tcgen05.ld
+    static constexpr int kBudget = 226 * 1024;               // dynamic smem (static use stays below 1.1 KB)
     static constexpr int kFit = (kBudget - kH - 2048) / kStage;
     static constexpr int kStages = kFit > 8 ? 8 : kFit;
     static constexpr int kBytes = kStages * kStage + kH + 1024 /*barriers*/ + 1024 /*alignment*/;
@@ -768,16 +780,16 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
 #pragma unroll
             for (int a = 0; a < C::kAcc; ++a)
 #pragma unroll
-                for (int c0 = 0; c0 < NT; c0 += 16) {
+                for (int c0 = 0; c0 < NT; c0 += C::kLdW) {
                     if (c0 >= u.ncols) break;        // warp-uniform: columns past ncols are padding
-                    uint32_t tmp[kTerms][16];
+                    uint32_t tmp[kTerms][C::kLdW];
 #pragma unroll
-                    for (int t = 0; t < kTerms; ++t) tc_ld16_issue(lanebase + a * C::kRows + t * NT + c0, tmp[t]);
+                    for (int t = 0; t < kTerms; ++t) tc_ld_issue(lanebase + a * C::kRows + t * NT + c0, tmp[t]);
 #pragma unroll
                     for (int t = 0; t < kTerms; ++t) {
-                        tc_wait_ld16(tmp[t]);
+                        tc_wait_ld(tmp[t]);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) vals[c0 + i] += __uint_as_float(tmp[t][i]);
+                        for (int i = 0; i < C::kLdW; ++i) vals[c0 + i] += __uint_as_float(tmp[t][i]);
                     }
                 }
             tc_fence_before();
@@ -988,6 +1000,7 @@ static int launch_ffn(const FfnParams& p, int grid, cudaStream_t st) {
 
 static int launch_ffn_nt(int NT, const FfnParams& p, int grid, cudaStream_t st) {
     switch (NT) {
+        case 8: return launch_ffn<8>(p, grid, st);
         case 16: return launch_ffn<16>(p, grid, st);
         case 32: return launch_ffn<32>(p, grid, st);
         case 64: return launch_ffn<64>(p, grid, st);
@@ -995,7 +1008,7 @@ static int launch_ffn_nt(int NT, const FfnParams& p, int grid, cudaStream_t st) 
     }
 }
 
-static int nt_for(int cols) { return cols <= 16 ? 16 : cols <= 32 ? 32 : 64; }
+static int nt_for(int cols) { return cols <= 8 ? 8 : cols <= 16 ? 16 : cols <= 32 ? 32 : 64; }
 
 bool tc_supported(const moe_dims* m) { return m->d % kKB == 0 && m->f % kKB == 0; }
 bool tc_decode_supported(const moe_dims* m, int T) { return tc_supported(m) && T >= 1 && T * m->top_k <= kMaxNT; }

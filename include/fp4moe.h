@@ -30,8 +30,11 @@
  *    after its own synchronisation): MOE_STATUS_* bits below.
  *  - Calls on different streams are independent when given different workspaces.
  *  - Some kernels are launched with programmatic dependent launch: they may become resident
- *    while the previous kernel on `stream` still runs, but read nothing before that kernel
- *    has completed, so stream order keeps its usual meaning.
+ *    while the previous kernel on `stream` still runs.  Before that kernel has completed they
+ *    read exactly one input, which the kernel enqueued immediately before the call must
+ *    therefore not write: x of moe_expert_ffn_fp4 on the tensor-core decode path (the router
+ *    call that normally precedes it does not).  Every other input, every output and the
+ *    workspace are touched only after it has completed.
  *  - After a call that set MOE_STATUS_TIMEOUT the workspace must be re-initialised
  *    (moe_workspace_init) before its next use.
  */

@@ -97,6 +97,49 @@ def test_tiny_layer_matches_oracle(tiny):
     assert row_rel_err(got["y"], ref["y"]).max() <= TOL
 
 
+def oracle_with_routing(wl, x_bits, r):
+    """Oracle layer output for tokens x_bits under the given routing (ids, slots, weights)."""
+    cache, ys = {}, []
+    for t in range(x_bits.shape[0]):
+        z = np.zeros((wl.k, wl.d))
+        for j in range(wl.k):
+            s = int(r["slots"][t, j])
+            if s < 0:
+                continue
+            if s not in cache:
+                cache[s] = wl.expert_tensors(s)
+            _, z[j] = oracle.expert_ffn(x_bits[t], cache[s])
+        ys.append(oracle.combine(z, r["weights"][t]))
+    return np.stack(ys)
+
+
+def test_back_to_back_calls_share_one_workspace(tiny):
+    """Router and expert calls enqueued back to back on one stream and one workspace with no
+    host synchronisation: a launch may start while the one before it still runs, and must
+    neither disturb it nor see its state.  FFN after FFN (other activations, same routing),
+    router after FFN and FFN after router, each output against the oracle."""
+    T = 3
+    xs = [syn.activations(0, 40 + i, T, 512) for i in range(2)]
+    layer = MoeLayer(tiny.d, tiny.f, tiny.E, tiny.k, T, tiny.arena)
+    xt = [bits_to_torch(x, DEV) for x in xs]
+    wr = bits_to_torch(tiny.wr, DEV)
+    tab = torch.from_numpy(tiny.table).to(DEV)
+    outs = []
+    layer.route(xt[0], wr, tab)
+    for rep in range(4):                      # four FFN calls in a row on the first routing
+        outs.append((0, rep % 2, layer.experts(xt[rep % 2], y=torch.empty((T, tiny.d), dtype=torch.bfloat16, device=DEV))))
+    layer.route(xt[1], wr, tab)
+    outs.append((1, 1, layer.experts(xt[1], y=torch.empty((T, tiny.d), dtype=torch.bfloat16, device=DEV))))
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    routes = [oracle.route_topk(x, tiny.wr, None, tiny.table, tiny.k) for x in xs]
+    np.testing.assert_array_equal(layer.ids[:T].cpu().numpy(), routes[1]["ids"])
+    for ri, xi, y in outs:
+        ref = oracle_with_routing(tiny, xs[xi], routes[ri])
+        err = row_rel_err(y.float().cpu().numpy(), ref)
+        assert err.max() <= TOL, (ri, xi, err)
+
+
 @pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor_cores", "cuda_cores"])
 @pytest.mark.parametrize("T", [1, 3, 16, 17, 100])
 def test_tiny_shapes_decode_and_prefill(tiny, T, cuda_cores):
