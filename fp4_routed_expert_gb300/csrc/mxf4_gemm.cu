@@ -123,11 +123,9 @@ __device__ __forceinline__ void warp_quantize32(float v, int lane, uint4* codes 
                                                 uint32_t* scales /*[kTerms]*/) {
 #pragma unroll
     for (int t = 0; t < kTerms; ++t) {
-        float amax = fabsf(v);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        // max |v| over the warp: magnitudes order like their bit patterns as unsigned integers
+        const uint32_t u = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
         int e = -127;
-        const uint32_t u = __float_as_uint(amax);
         if ((u >> 23) != 0u) {                                   // normal amax; subnormal residuals are dropped
             const int e0 = (int)((u >> 23) & 0xFF) - 127;        // floor(log2 amax)
             const float m = __uint_as_float((u & 0x007FFFFFu) | 0x3F800000u);   // amax / 2^e0 in [1, 2)
@@ -380,6 +378,14 @@ __device__ __forceinline__ int ld_acquire(const int32_t* a) {
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
     return v;
 }
+__device__ __forceinline__ int atom_add_acq_rel(int32_t* a, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void red_add_release(int32_t* a, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // The whole expert FFN in one persistent launch (one CTA per SM, every CTA resident).  The
@@ -474,10 +480,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
             }
             fence_proxy_async();   // read by the async proxy (bulk copies) of every CTA
             __syncwarp();
-            if (lane == 0) {
-                __threadfence();
-                atomicAdd(p.xready, 1);
-            }
+            if (lane == 0) red_add_release(p.xready, 1);
         }
     }
     // everything above overlaps the previous kernel; its outputs are read from here on
@@ -727,9 +730,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 if (lane == 0) {
                     int l = 0;
                     if (okw) {
-                        __threadfence();
-                        l = (atomicAdd(counter, add) + add == target);
-                        __threadfence();
+                        l = (atom_add_acq_rel(counter, add) + add == target);
                     } else {
                         atomicOr(p.status, MOE_STATUS_TIMEOUT);
                         *abortp = 1;
@@ -909,10 +910,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     break;
                 }
                 ephase ^= 1u;
-                if (ew == 0 && lane == 0) {
-                    __threadfence();
-                    atomicAdd(p.ready + u.key, 1);
-                }
+                if (ew == 0 && lane == 0) red_add_release(p.ready + u.key, 1);
             }
         }
     }

@@ -153,6 +153,21 @@ def test_tiny_shapes_decode_and_prefill(tiny, T, cuda_cores):
         np.testing.assert_array_equal(got["row_dst"], p["row_dst"])
 
 
+@pytest.fixture(scope="module")
+def small_multistage():
+    # d = 1024, f = 768: gate/up units of 4 K blocks (two pipeline stages), down units of 3 K
+    # blocks (a full and a half stage, cut into two parts by the decode schedule)
+    return make_workload(1024, 768, 16, 4, seed=5, scale=(-9, -5))
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 17, 40])
+def test_small_multistage_shape(small_multistage, T):
+    x = syn.activations(5, 0, T, 1024)
+    got = run_layer(small_multistage, x)
+    assert got["status"] == 0
+    check_tokens(small_multistage, x, got, list(range(T)))
+
+
 @pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor_cores", "cuda_cores"])
 def test_prefill_fused_combine_matches_unfused(tiny, cuda_cores):
     x = syn.activations(0, 0, 40, 512, stream=2)
