@@ -171,9 +171,9 @@ __device__ __forceinline__ void warp_best(float& k, int& e) {
     }
 }
 
-// Shared-memory bytes of one selecting warp: E key records, E exact keys and 64 words for
-// the chosen experts.
-__host__ __device__ inline size_t select_smem_per_warp(int E) { return ((size_t)E * 20 + 256 + 15) / 16 * 16; }
+// Shared-memory bytes of one selecting warp: E key records, E exact keys and 96 words for
+// the chosen experts (scores, ids, slots).
+__host__ __device__ inline size_t select_smem_per_warp(int E) { return ((size_t)E * 20 + 384 + 15) / 16 * 16; }
 
 // Order-preserving map of a float key to uint32 (every non-NaN key maps above 0, so 0 means
 // "no candidate"), and its inverse.
@@ -345,16 +345,19 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(RouteArgs 
     unsigned char* wsm = sel_smem + (size_t)warp * select_smem_per_warp(E);
     float4* rec = reinterpret_cast<float4*>(wsm);
     float* exk = reinterpret_cast<float*>(wsm + (size_t)E * 16);
-    int* out = reinterpret_cast<int*>(wsm + (size_t)E * 20);   // 64 words: ranks' scores
+    int* out = reinterpret_cast<int*>(wsm + (size_t)E * 20);   // 96 words: ranks' scores, ids, slots
     pdl_trigger();
     pdl_wait();   // the key records of the logit kernel
     for (int t = blockIdx.x * kSelWarps + warp; t < a.T; t += gridDim.x * kSelWarps) {
         const float4* krow = a.keys + (size_t)t * E;
+        // key records and slot-table entries of experts lane + 32 m, loaded together
         float4 r[EPL];
+        int tb[EPL];
 #pragma unroll
         for (int m = 0; m < EPL; ++m) {
             const int e = lane + 32 * m;
             r[m] = (e < E) ? __ldcg(krow + e) : make_float4(NEG_INF, NEG_INF, NEG_INF, -1.0f);
+            tb[m] = (e < E) ? __ldg(a.table + e) : -1;
         }
         uint32_t valid = 0, picked = 0, bu = 0;
         int bm = 0;
@@ -408,6 +411,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(RouteArgs 
         // outputs in ascending id (m outer, lane inner); weight sum in that order
         float* osc = reinterpret_cast<float*>(out);
         int* oid = out + 32;
+        int* osl = out + 64;
         const uint32_t below = (1u << lane) - 1u;
         int base = 0;
 #pragma unroll
@@ -417,6 +421,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(RouteArgs 
                 const int rank = base + __popc(bal & below);
                 osc[rank] = r[m].w;
                 oid[rank] = lane + 32 * m;
+                osl[rank] = tb[m];
             }
             base += __popc(bal);
         }
@@ -430,10 +435,9 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(RouteArgs 
         int32_t* so = a.slots + (size_t)t * k;
         for (int j = lane; j < k; j += 32) {
             if (j < n) {
-                const int e = oid[j];
-                ids[j] = e;
+                ids[j] = oid[j];
                 wo[j] = (sum > 0.0f) ? __fdiv_rn(osc[j], sum) : 0.0f;
-                so[j] = a.table[e];
+                so[j] = osl[j];
             } else {
                 ids[j] = -1;
                 wo[j] = 0.0f;
@@ -503,7 +507,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) route_decode_kernel(RouteAr
             const uint32_t rowb = (uint32_t)d * 2;
             mbar_expect_tx(smem_u32(bar), rowb * nw + (first ? rowb * T : 0u));
             if (first) bulk_g2s(smem_u32(xs), a.x, rowb * T, smem_u32(bar));
-            for (int w = 0; w < nw; ++w) bulk_g2s(smem_u32(ws + (size_t)w * d), a.wr + (size_t)(e0 + w) * d, rowb, smem_u32(bar));
+            // the block's router rows are consecutive: one copy (a bulk copy costs a fixed time
+            // on top of its bytes)
+            bulk_g2s(smem_u32(ws), a.wr + (size_t)e0 * d, rowb * nw, smem_u32(bar));
         }
         const int e = e0 + warp;
         const int tb = (e < E) ? a.table[e] : -1;
