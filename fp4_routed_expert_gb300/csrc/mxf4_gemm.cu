@@ -293,7 +293,7 @@ struct FfnParams {
     int32_t* status;
     int32_t* work;                   // next unit to hand out (zero at launch)
     int32_t* ready;                  // phase 0 units finished, per key (decode: slot ordinal; prefill: tile)
-    int32_t* ycnt;                   // decode: pair rows finished per 128-feature block of y
+    int32_t* ycnt;                   // decode: pair rows finished per 32 features of y
     // decode: x is quantised by this kernel into ph[0].b_q / b_sf (rows 0..T-1 of the NT-row
     // tile; the padding rows only feed discarded columns); the last CTA to exit (exit ticket)
     // clears every counter for the next call
@@ -392,8 +392,8 @@ __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.
 // producer takes units from the work list; a down unit needs the h rows of its key (decode:
 // its slot; prefill: its tile) from every gate/up unit of that key, so the producer issues the
 // unit's first weight copy, then waits (bounded) for the key's count of finished gate/up units
-// before issuing the h copy.  Decode also combines: the last down unit to finish a
-// 128-feature block of y sums the token's pair rows in ascending j.
+// before issuing the h copy.  Decode also combines: the warp of the last down unit to write a
+// run of 32 features of y sums the token's pair rows there in ascending j.
 template <int NT>
 __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) {
     using C = GemmCfg<NT>;
@@ -808,9 +808,15 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     if (valid && !dry) p.rows_out[(size_t)(u.brow0 + c) * p.d + r] = vals[c];
                 }
                 if (p.regime == kRegimeDecode && p.y) {
-                    // y block m is complete once every valid pair's row block m is written
+                    // y rows [128m + 32q, +32) are complete once every valid pair's rows there are
+                    // written: one counter per 32 features, one arrival per warp
                     bool last = dry;
-                    if (!dry && !count_arrival(p.ycnt + u.m, upairs[u.key], pairs_total_sh, last)) break;
+                    if (!dry) {
+                        __syncwarp();
+                        int l = 0;
+                        if (lane == 0) l = (atom_add_acq_rel(p.ycnt + u.m * 4 + q, upairs[u.key]) + upairs[u.key] == pairs_total_sh);
+                        last = __shfl_sync(0xffffffffu, l, 0) != 0;
+                    }
                     if (last) {
                         for (int t = 0; t < p.T; ++t) {
                             float yv = 0.f;
@@ -921,15 +927,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     if (p.exit_ctr) {
         // the last CTA to leave clears the counters for the next call
         __shared__ int last_cta;
-        if (tid == 0) {
-            __threadfence();
-            last_cta = (atomicAdd(p.exit_ctr, 1) == (int)gridDim.x - 1);
-        }
+        if (tid == 0) last_cta = (atom_add_acq_rel(p.exit_ctr, 1) == (int)gridDim.x - 1);
         __syncthreads();
         if (last_cta) {
-            __threadfence();
             for (int i = tid; i < n_keys; i += blockDim.x) p.ready[i] = 0;
-            for (int i = tid; i < p.d / kBM; i += blockDim.x) p.ycnt[i] = 0;
+            for (int i = tid; i < p.d / 32; i += blockDim.x) p.ycnt[i] = 0;
             if (tid == 0) {
                 *p.work = 0;
                 *p.xjob = 0;
@@ -958,13 +960,13 @@ static size_t max_keys(const moe_dims* m, int T) {
 
 struct TcBuffers {
     uint8_t *x, *h;        // activation blocks of x (K = d) and h (K = f)
-    int32_t* zero;         // counters cleared by the quantiser: work, ready[nkeys], ycnt[d/128]
+    int32_t* zero;         // counters cleared by the quantiser: work, ready[nkeys], ycnt[d/32]
     size_t nkeys, nzero;
     float* rows;
     int32_t* plan;
 };
 
-static size_t counters_of(const moe_dims* m, int T) { return 1 + max_keys(m, T) + m->d / kBM; }
+static size_t counters_of(const moe_dims* m, int T) { return 1 + max_keys(m, T) + m->d / 32; }
 
 static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& L) {
     TcBuffers b;
