@@ -456,6 +456,8 @@ def main():
                     help="experts resident in the arena (profiling runs use fewer; the metric is defined at 384)")
     ap.add_argument("--tokens", type=int, default=1000, help="tokens per step")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-chunk measurement")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="measure only the prefill chunk (profiling runs; with --experts the arena holds fewer experts)")
     args = ap.parse_args()
     global E, TOKENS, ROUTER_BYTES, ALG_BYTES_PER_TOKEN
     E, TOKENS = args.experts, args.tokens
@@ -464,6 +466,8 @@ def main():
     if E != 384 or TOKENS != 1000:
         CONFIG["workload"] = "PROFILING VARIANT (not the metric's workload): E=%d experts, %d tokens per step" % (E, TOKENS)
         CONFIG["tokens_per_step"] = TOKENS
+        CONFIG["l2"] = "arena of %.2f GB (each call streams 6 experts, 112.8 MB, more than L2), no flush" % (
+            E * EXPERT_BYTES / 1e9)
     rank, world, local_rank = env_rank()
     if args.impl == "reference":
         out = run_reference(args, rank, world)
@@ -472,6 +476,15 @@ def main():
         return 0
     import fp4_routed_expert_gb300 as moe
     moe.lib()
+    if args.prefill_only:
+        if rank == 0:
+            import torch
+            torch.cuda.set_device(local_rank)
+            dev = torch.device("cuda", local_rank)
+            out = {"metric": "prefill chunk tokens/s", "impl": "ours", "config": dict(CONFIG),
+                   "prefill": run_prefill(build_workload(dev), args, dev)}
+            print(json.dumps(out), flush=True)
+        return 0
     out, w = run_ours(args, rank, world, local_rank)
     if rank == 0 and out is not None and not args.no_prefill and E == 384:
         import torch
