@@ -453,6 +453,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
     volatile int* abortp = &abort_flag;
+    // Decode: the producer claims its first unit now, before the wait below.  The work list is
+    // a counter that the previous call left at zero (the kernel before this one started after
+    // that call completed, exactly as for the x jobs); what the unit means is known only after
+    // the wait.  Prefill's counter is cleared by the kernel before this one, so it claims later.
+    int pre_unit = -2;
+    if (warp == 0 && lane == 0 && p.regime == kRegimeDecode) pre_unit = atomicAdd(p.work, 1);
     // Decode: x -> kTerms MXFP4 terms, one warp per (row < T, 32-element block), jobs taken
     // from a global counter so that the CTAs resident first do them all.  This runs before the
     // wait below: x is an input of this call, and the kernel that may still be running (the
@@ -549,7 +555,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
             bool x_ok = (p.x_src == nullptr);
             uint32_t phase = 0, issued = 0, issued_parity = 0;   // per-stage bit masks
             while (true) {
-                int unit = *abortp ? -1 : atomicAdd(p.work, 1);
+                int unit;
+                if (pre_unit != -2) {
+                    unit = *abortp ? -1 : pre_unit;
+                    pre_unit = -2;
+                } else {
+                    unit = *abortp ? -1 : atomicAdd(p.work, 1);
+                }
                 if (unit >= n_all) unit = -1;
                 if (!mbar_wait(smem_u32(&uqempty[qi]), qphase ^ 1u, abortp)) {
                     atomicOr(p.status, MOE_STATUS_TIMEOUT);
