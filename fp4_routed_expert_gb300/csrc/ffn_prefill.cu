@@ -88,7 +88,8 @@ __global__ void permute_tail_kernel(int n, int E, const int32_t* offsets, int32_
 // ---------------------------------------------------------------------------- plan
 
 // Validates group_offsets (monotone in [0, n]) and lists the non-empty groups with the
-// prefix of their tile counts (tile_rows rows per tile).  plan = [n_active, total_tiles, e_0.., tile_start_0..]
+// prefix of their tile counts (tile_rows rows per tile), and the tile row of every pair.
+// plan = [n_active, total_tiles, e_0.., tile_start_0..] (layout: see plan_pair_off)
 // One block of 1024 threads, thread e = expert e (E <= 1024): block-wide exclusive scans of
 // "has rows" and "tiles of tile_rows rows" give each non-empty expert its group index and first
 // tile; every group writes its record and its tiles' entries of tile_group.  Offsets that are
@@ -147,6 +148,28 @@ __global__ void __launch_bounds__(1024) plan_kernel(int E, int n, const int32_t*
         plan[0] = bad ? 0 : na;
         plan[1] = bad ? 0 : tiles;
         if (bad) atomicOr(status, MOE_STATUS_BAD_SLOT);
+    }
+    // pair s -> tile row: permuted row i of expert e (offsets[e] <= i < offsets[e + 1]) sits in
+    // row i - offsets[e] of the expert's tiles, which start at tile_start: the linear tile row
+    // is tile_start * tile_rows + i - offsets[e]
+    __shared__ int so0[kMaxExperts], sts[kMaxExperts];
+    int32_t* prow = plan + plan_pair_off(E, max_tiles);
+    if (e < E) {
+        so0[e] = o0;
+        sts[e] = ts;
+    }
+    for (int i = e; i < nrows; i += blockDim.x) prow[i] = -1;
+    __syncthreads();
+    if (bad || E < 1) return;
+    const int rows_end = offsets[E];
+    for (int i = e; i < rows_end && i < nrows; i += blockDim.x) {
+        int lo = 0, hi = E - 1;   // the last expert whose rows start at or before i
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (so0[mid] <= i) lo = mid; else hi = mid - 1;
+        }
+        const int src = row_src[i];
+        if (src >= 0 && src < nrows) prow[src] = sts[lo] * tile_rows + (i - so0[lo]);
     }
 }
 

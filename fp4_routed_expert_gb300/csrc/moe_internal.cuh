@@ -87,7 +87,9 @@ inline size_t counter_words(const moe_dims*) { return kCounterWords; }
 // prefill call (written by plan_kernel) describes the expert groups and their tiles:
 //   int32 [0] n_active, [1] tiles, [2, 2+E) expert of group g, [2+E, 2+2E) first tile of g,
 //   int4  grec[E] at plan_grec_off(E): {first row, end row, arena slot, first tile} of g,
-//   int32 tile_group[max_tiles] at plan_tile_group_off(E): the group of each tile.
+//   int32 tile_group[max_tiles] at plan_tile_group_off(E): the group of each tile,
+//   int32 pair_row[n] at plan_pair_off(E, max_tiles): the tile row of pair t*k + j
+//         (tile * tile_rows + row), -1 for a pair that has no row.
 constexpr int kPrefillNT = 32;
 inline size_t act_tiles(const moe_dims* m, int T) {
     const size_t n = (size_t)(T > 0 ? T : 1) * m->top_k;
@@ -96,6 +98,7 @@ inline size_t act_tiles(const moe_dims* m, int T) {
 }
 __host__ __device__ inline int plan_grec_off(int E) { return (2 + 2 * E + 3) / 4 * 4; }
 __host__ __device__ inline int plan_tile_group_off(int E) { return plan_grec_off(E) + 4 * E; }
+__host__ __device__ inline int plan_pair_off(int E, int max_tiles) { return plan_tile_group_off(E) + max_tiles; }
 
 // Workspace sections, each 256-byte aligned.  The persistent counters come first so that
 // their offset is the same for every token count; the other sections are per call.
@@ -126,7 +129,7 @@ inline WsLayout ws_layout(const moe_dims* m, int T_max) {
     w.keys = o;    o = align256(o + 16 * T * E);
     w.xnorm = o;   o = align256(o + 4 * T);
     w.wnorm = o;   o = align256(o + 4 * E);
-    w.active = o;  o = align256(o + 4 * ((size_t)plan_tile_group_off((int)E) + act_tiles(m, (int)T)));
+    w.active = o;  o = align256(o + 4 * ((size_t)plan_tile_group_off((int)E) + act_tiles(m, (int)T) + T * k));
     w.h = o;       o = align256(o + 4 * T * k * (size_t)m->f);
     w.rows = o;
     if (T_max > kDecodeMaxT) o = align256(o + 4 * T * k * (size_t)m->d);

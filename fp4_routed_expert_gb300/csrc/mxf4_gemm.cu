@@ -201,13 +201,14 @@ __device__ __forceinline__ int64_t act_scale_off(int tile, int kb, int term, int
            (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
 }
 
-// Prefill activations -> kTerms MXFP4 terms in tile layout, one thread per (tile, row,
-// 32-element block): row r of tile t of group g holds permuted row first_row_g + NT*(t -
-// first_tile_g) + r, i.e. token row_src[n]/k; rows past the group's end are zero.  Also
-// clears `nzero` counters for the FFN kernel that follows.
-__global__ void __launch_bounds__(256) quantize_tiles_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row_src,
-                                                             const int32_t* __restrict__ plan, int E, int k, int T, int d,
-                                                             uint8_t* __restrict__ q, int32_t* __restrict__ zero, int nzero) {
+// Prefill activations -> kTerms MXFP4 terms in tile layout, one thread per (token t, 32-element
+// block b): the block is quantised once and written into the tile row of each of the token's k
+// pairs (pair_row, from the plan).  Rows of a tile past its group's end are never written: they
+// feed only accumulator columns that the epilogues discard.  Also clears `nzero` counters for
+// the FFN kernel that follows.
+__global__ void __launch_bounds__(256) quantize_tiles_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pair_row,
+                                                             int k, int T, int d, uint8_t* __restrict__ q,
+                                                             int32_t* __restrict__ zero, int nzero) {
     constexpr int NT = kPrefillNT;
     // launched early behind the previous kernel: nothing it wrote is read before it completes;
     // the FFN kernel may launch at once (it waits for this kernel in turn)
@@ -216,48 +217,35 @@ __global__ void __launch_bounds__(256) quantize_tiles_kernel(const uint16_t* __r
     // the FFN kernel's counters start at zero
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += gridDim.x * blockDim.x) zero[i] = 0;
     const int nblk = d / 32, KB = d / kKB;
-    const long total = (long)plan[1] * NT * nblk;
-    const int32_t* tgroup = plan + plan_tile_group_off(E);
-    const int4* grec = reinterpret_cast<const int4*>(plan + plan_grec_off(E));
+    const long total = (long)T * nblk;
     for (long idx = blockIdx.x * (long)blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
         const int b = (int)(idx % nblk);
-        const int r = (int)((idx / nblk) % NT);
-        const int tile = (int)(idx / ((long)nblk * NT));
-        const int4 gr = grec[tgroup[tile]];   // first row, end row, slot, first tile
-        const int n = gr.x + NT * (tile - gr.w) + r;
-        int tok = -1;
-        if (n < gr.y) {
-            const int s = row_src[n];
-            tok = (s >= 0 && s < T * k) ? s / k : -1;
+        const int t = (int)(idx / nblk);
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + 32 * b);
+        float v[32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint4 w4 = __ldg(src + u);
+            const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                v[8 * u + 2 * h] = bf16_lo(ww[h]);
+                v[8 * u + 2 * h + 1] = bf16_hi(ww[h]);
+            }
         }
-        const int kb = b / 8, j = b % 8;
         uint32_t wds[kTerms][4], scl[kTerms];
-        if (tok < 0) {                                       // padding row: zero codes, zero scale
+        thread_quantize32(v, wds, scl);
+        const int kb = b / 8, j = b % 8;
+        for (int jj = 0; jj < k; ++jj) {
+            const int lin = __ldg(pair_row + (size_t)t * k + jj);
+            if (lin < 0) continue;
+            const int tile = lin / NT, r = lin % NT;
 #pragma unroll
-            for (int t = 0; t < kTerms; ++t) {
-                scl[t] = 0;
-                wds[t][0] = wds[t][1] = wds[t][2] = wds[t][3] = 0;
+            for (int tt = 0; tt < kTerms; ++tt) {
+                *reinterpret_cast<uint4*>(q + act_code_off(tile, kb, tt, r, j, NT, KB)) =
+                    make_uint4(wds[tt][0], wds[tt][1], wds[tt][2], wds[tt][3]);
+                q[act_scale_off(tile, kb, tt, r, j, NT, KB)] = (uint8_t)scl[tt];
             }
-        } else {
-            const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)tok * d + 32 * b);
-            float v[32];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint4 w4 = __ldg(src + u);
-                const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    v[8 * u + 2 * h] = bf16_lo(ww[h]);
-                    v[8 * u + 2 * h + 1] = bf16_hi(ww[h]);
-                }
-            }
-            thread_quantize32(v, wds, scl);
-        }
-#pragma unroll
-        for (int t = 0; t < kTerms; ++t) {
-            *reinterpret_cast<uint4*>(q + act_code_off(tile, kb, t, r, j, NT, KB)) =
-                make_uint4(wds[t][0], wds[t][1], wds[t][2], wds[t][3]);
-            q[act_scale_off(tile, kb, t, r, j, NT, KB)] = (uint8_t)scl[t];
         }
     }
 }
@@ -1088,12 +1076,12 @@ int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint1
     if (T == 0) return MOE_OK;
     TcBuffers b = tc_buffers(m, T, ws, L);
     const int d = m->d, k = m->top_k, n = T * k;
-    plan_kernel<<<1, 1024, 0, st>>>(m->num_experts, n, offsets, row_src, slot, n, b.plan, status, kPrefillNT,
-                                    (int)act_tiles(m, T));
-    const long qjobs = (long)act_tiles(m, T) * kPrefillNT * (d / 32);
+    const int max_tiles = (int)act_tiles(m, T);
+    plan_kernel<<<1, 1024, 0, st>>>(m->num_experts, n, offsets, row_src, slot, n, b.plan, status, kPrefillNT, max_tiles);
+    const long qjobs = (long)T * (d / 32);
     const long qblocks = (qjobs + 255) / 256;
     quantize_tiles_kernel<<<(int)(qblocks > 8L * num_sms ? 8L * num_sms : qblocks), 256, 0, st>>>(
-        x, row_src, b.plan, m->num_experts, k, T, d, b.x, b.zero, (int)b.nzero);
+        x, b.plan + plan_pair_off(m->num_experts, max_tiles), k, T, d, b.x, b.zero, (int)b.nzero);
     note_launch(2);
     FfnParams p = ffn_params(m, ar, T, slot, status, b);
     p.regime = kRegimePrefill;
