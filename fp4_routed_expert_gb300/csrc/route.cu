@@ -50,6 +50,7 @@ struct RouteArgs {
     float* wnorm;      // [E]   (prefill bound)
     unsigned* counter;
     float bound_coef;  // prefill: gamma_L * (1 + 2^-10); decode: gamma_(c-1) + gamma_m^2 + 2^-34
+    float refine_coef; // the decode bound for chunks of one product (selection's refinement)
 };
 
 // ------------------------------------------------------------------ exact logit (Kulisch)
@@ -151,6 +152,60 @@ __device__ __forceinline__ float4 make_key(int tb, float b, float lf, float lo, 
     const float sv = sigmoid_fast(lf);
     return make_float4(sv + b, __fadd_rd(__fsub_rd(sigmoid_fast(lo), margin), b),
                        __fadd_ru(__fadd_ru(sigmoid_fast(hi), margin), b), sv);
+}
+
+// TwoSum (Knuth): s + err == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& err) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+// Key record of (token x, expert row w) by the decode kernel's compensated dot product with
+// chunks of one product (lane l: vectors l, l+32, ..., eight TwoSum chains, then chains and
+// lanes added as (sum, compensation) pairs), read from global memory by a whole warp; every
+// lane returns the record.  coef is that kernel's bound for one-product chunks.
+__device__ __noinline__ float4 refine_key_warp(const uint16_t* __restrict__ x, const uint16_t* __restrict__ w, int d,
+                                               int lane, float coef, int tb, float bias) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x);
+    const uint4* wr = reinterpret_cast<const uint4*>(w);
+    float s[8], c[8], A = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s[q] = c[q] = 0.f;
+    for (int cv = lane; cv < d / 8; cv += 32) {
+        const uint4 wv = __ldg(wr + cv), xv = __ldg(xr + cv);
+        const float w8[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
+                             bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
+        const float x8[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
+                             bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float err;
+            two_sum(s[q], __fmul_rn(x8[q], w8[q]), s[q], err);   // bf16 x bf16 products are exact in fp32
+            c[q] = __fadd_rn(c[q], err);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) A = __fmaf_rn(fabsf(x8[i]), fabsf(w8[i]), A);
+    }
+    float S = s[0], C = c[0];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) {
+        float err;
+        two_sum(S, s[q], S, err);
+        C = __fadd_rn(C, __fadd_rn(c[q], err));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float S2 = __shfl_xor_sync(0xffffffffu, S, o), C2 = __shfl_xor_sync(0xffffffffu, C, o);
+        float err;
+        two_sum(S, S2, S, err);
+        C = __fadd_rn(__fadd_rn(C, C2), err);
+        A = __fadd_ru(A, __shfl_xor_sync(0xffffffffu, A, o));
+    }
+    // |S + C - exact| <= coef * sum|x w| * (1 + 2^-9) + d * 2^-147
+    float delta = __fmul_ru(__fmul_ru(coef, A), 1.001953125f);
+    delta = __fadd_ru(delta, (float)d * 5.605193857299268e-45f);
+    return make_key(tb, bias, __fadd_rn(S, C), __fadd_rd(S, __fsub_rd(C, delta)), __fadd_ru(S, __fadd_ru(C, delta)));
 }
 
 // ------------------------------------------------------------------ certified selection
@@ -395,18 +450,47 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(RouteArgs 
         }
         const float min_lo_in = key_value(__reduce_min_sync(0xffffffffu, key_order(lo_in)));
         const float max_hi_out = key_value(__reduce_max_sync(0xffffffffu, key_order(hi_out)));
-        bool doubt = false;
+        bool doubt = false, order_doubt = false;
 #pragma unroll
         for (int m = 0; m < EPL; ++m) {
             if ((picked >> m) & 1u) {
-                if (!(r[m].y > max_hi_out) || r[m].z - r[m].y > 1e-5f * r[m].w) doubt = true;
+                if (!(r[m].y > max_hi_out)) order_doubt = true;
+                else if (r[m].z - r[m].y > 1e-5f * r[m].w) doubt = true;
             } else if (((valid >> m) & 1u) && r[m].z >= min_lo_in) {
-                doubt = true;
+                order_doubt = true;
             }
         }
-        if (__any_sync(0xffffffffu, doubt)) {
-            select_token(a, t, lane, rec, exk, out);
-            continue;
+        if (__any_sync(0xffffffffu, doubt || order_doubt)) {
+            // Refinement: when the chosen set is certain and only some chosen scores are wide
+            // (the tiled logits' bound), the chosen experts' records are recomputed with the
+            // compensated dot product; if every chosen interval is then narrow and still above
+            // every other expert's, the token is done without exact logits.
+            bool resolved = false;
+            if (!__any_sync(0xffffffffu, order_doubt) && a.refine_coef > 0.0f) {
+                const uint16_t* xt = a.x + (size_t)t * a.d;
+                bool still = false;
+#pragma unroll
+                for (int m = 0; m < EPL; ++m) {
+                    uint32_t bal = __ballot_sync(0xffffffffu, (picked >> m) & 1u);
+                    while (bal) {
+                        const int src = __ffs(bal) - 1;
+                        bal &= bal - 1;
+                        const int e = src + 32 * m;
+                        const float be = a.bias ? a.bias[e] : 0.0f;
+                        const int tbe = __shfl_sync(0xffffffffu, tb[m], src);
+                        const float4 nr = refine_key_warp(xt, a.wr + (size_t)e * a.d, a.d, lane, a.refine_coef, tbe, be);
+                        if (lane == src) {
+                            r[m] = nr;
+                            if (!(nr.y > max_hi_out) || nr.z - nr.y > 1e-5f * nr.w) still = true;
+                        }
+                    }
+                }
+                resolved = !__any_sync(0xffffffffu, still);
+            }
+            if (!resolved) {
+                select_token(a, t, lane, rec, exk, out);
+                continue;
+            }
         }
         // outputs in ascending id (m outer, lane inner); weight sum in that order
         float* osc = reinterpret_cast<float*>(out);
@@ -461,13 +545,6 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(RouteArgs 
     } while (0)
 
 // ------------------------------------------------------------------ decode: one warp per expert
-
-// TwoSum (Knuth): s + err == a + b exactly.
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& err) {
-    s = __fadd_rn(a, b);
-    const float bb = __fsub_rn(s, a);
-    err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
 
 constexpr int kDecodeWarps = 4;
 constexpr size_t kDecodeSmemMax = 200 * 1024;
@@ -722,6 +799,11 @@ static int launch_decode_ch(RouteArgs a, cudaStream_t st, int num_sms) {
 // rows fit in shared memory, else norms -> tiled logits -> selection.
 static int launch_route_args(RouteArgs& a, cudaStream_t st, int num_sms) {
     if (a.T == 0) return MOE_OK;
+    {
+        const int m = a.d / 256;   // the decode bound for one-product chunks (selection's refinement)
+        const double coef = gamma32(0) + gamma32(m) * gamma32(m) + 1.0 / 17179869184.0;
+        a.refine_coef = (float)(coef * (1.0 + 1.0 / 4096.0));
+    }
     if (a.T <= kDecodeMaxT && decode_smem_bytes(a.T, a.d) <= kDecodeSmemMax) {
         if (a.T <= 2) return launch_decode_ch<1>(a, st, num_sms);
         if (a.T <= 4) return launch_decode_ch<2>(a, st, num_sms);
