@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     uint32_t qphase = 0;
 
     if (warp == 0) {
-        // ---------------- producer: takes units, four contiguous bulk copies per stage
+        // ---------------- producer: takes units, two contiguous bulk copies per stage
         if (lane == 0) {
             int stage = 0, ready_key = -1;
             bool x_ok = (p.x_src == nullptr);
