@@ -78,9 +78,9 @@ inline bool dims_ok(const moe_dims* m) {
 
 // Counters inside the counter section (zeroed by moe_workspace_init; every user leaves them
 // zero again): the decode FFN kernel's work list, x jobs and x-ready, exit ticket, per-key readiness
-// (kMaxDecodeKeys) and y counts per 32 output features (d/32 <= 2048).
+// (256 decode keys) and y counts per 32 output features (d/32 <= 2048).
 enum { kCtrRoute = 0, kCtrFfnWork = 64, kCtrFfnXReady = 65, kCtrFfnExit = 66, kCtrFfnXJob = 67, kCtrFfnReady = 128,
-       kCtrFfnY = 256, kCounterWords = 2304 };
+       kCtrFfnY = 384, kCounterWords = 2432 };
 inline size_t counter_words(const moe_dims*) { return kCounterWords; }
 
 // Prefill activation tiles: kPrefillNT permuted rows each (tensor-core path).  The plan of a

@@ -38,7 +38,8 @@ constexpr int kKBytes = 128;          // code bytes per row per stage
 constexpr int kThreadsGemm = 6 * 32;
 constexpr int kTmemCols = 512;
 constexpr int kSfRing = 2;                // scale buffers in TMEM (tcgen05.cp and MMAs run in issue order)
-constexpr int kMaxNT = 64;               // activation rows per tile (decode: T*k pairs)
+constexpr int kDecodeNT = 16;             // decode tile rows at most: the tokens of x; a key's pairs of h
+constexpr int kMaxDecodePairs = 128;      // decode calls on the tensor cores: T*k <= 128
 
 enum { kModeGateUp = 0, kModeDown = 1 };
 enum { kRegimeDecode = 0, kRegimePrefill = 1 };
@@ -258,7 +259,6 @@ struct PhaseParams {
     int kblocks, mtiles;             // K / 256, weight rows / 128
     int64_t a_off;                   // the weight matrix inside a slot
     const uint8_t* b;                // activation blocks
-    int decode_cols;                 // decode: valid columns (B rows) of every unit
 };
 
 struct FfnParams {
@@ -318,7 +318,7 @@ struct GemmCfg {
     static constexpr int kStage = kKPS * (kTileBytes + kBBlk);
     static constexpr int kH = NT * 66 * 4;                   // gate/up epilogue h tile (padded rows)
     static constexpr int kLdW = NT < 16 ? NT : 16;           // accumulator columns per tcgen05.ld
-    static constexpr int kBudget = 226 * 1024;               // dynamic smem (static use stays below 1.1 KB)
+    static constexpr int kBudget = 226 * 1024;               // dynamic smem (static use stays below 2 KB)
     static constexpr int kFit = (kBudget - kH - 2048) / kStage;
     static constexpr int kStages = kFit > 8 ? 8 : kFit;
     static constexpr int kBytes = kStages * kStage + kH + 1024 /*barriers*/ + 1024 /*alignment*/;
@@ -335,15 +335,16 @@ struct UnitInfo {
 };
 
 template <int NT>
-__device__ __forceinline__ bool unit_info(const FfnParams& p, const PhaseParams& P, int unit, const int* uslots,
-                                          UnitInfo& u) {
+__device__ __forceinline__ bool unit_info(const FfnParams& p, const PhaseParams& P, int ph, int unit, const int* kslot,
+                                          const int* kinfo, UnitInfo& u) {
     if (p.regime == kRegimeDecode) {
+        // gate/up: the x tile, one column per token; down: the key's own h tile
         u.m = unit % P.mtiles;
         u.key = unit / P.mtiles;
-        u.slot = uslots[u.key];
-        u.btile = 0;
+        u.slot = kslot[u.key];
+        u.btile = ph ? u.key : 0;
         u.brow0 = 0;
-        u.ncols = P.decode_cols;
+        u.ncols = ph ? (kinfo[u.key] & 0xFFFF) : p.T;
         return true;
     }
     // prefill: unit = first_tile_g*mtiles + m*ntiles_g + ntile (tiles sharing weights adjacent),
@@ -403,10 +404,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     __shared__ int abort_flag;
     __shared__ int n_keys_sh, pairs_total_sh;
     __shared__ int fix_last;
-    __shared__ int uslots[kMaxNT];
-    __shared__ int upairs[kMaxNT];
-    __shared__ int sslot[kMaxNT];                // decode: the routing outputs of the T*k pairs
-    __shared__ float sw[kMaxNT];
+    // decode: the routing outputs of the T*k pairs and the keys.  A key is a slot's pairs, in
+    // order of appearance, in chunks of at most NT: the chunk's h rows are one tile.
+    __shared__ int pinfo[kMaxDecodePairs];       // pair -> key << 5 | row in the key's tile, -1: none
+    __shared__ int kslot[kMaxDecodePairs];       // key -> slot
+    __shared__ int kinfo[kMaxDecodePairs];       // key -> first kplist index << 16 | pairs
+    __shared__ short kplist[kMaxDecodePairs];    // the pairs of each key in row order
     __shared__ int uq[kUQ];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -480,42 +483,119 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     // everything above overlaps the previous kernel; its outputs are read from here on
     pdl_wait();
     if (warp == 0) {
-        // decode: the unique valid slots, in order of first appearance, are the keys
+        // decode: keys in order of their first pair (a slot's first appearance, then every
+        // NT-th); one warp, pair i on lane i mod 32
         if (p.regime == kRegimeDecode) {
-            const int n = p.T * p.k;   // <= kMaxNT = 64, checked on the host
-            for (int i = lane; i < n; i += 32) {
-                sslot[i] = p.slot[i];
-                sw[i] = p.w ? p.w[i] : 0.f;
-            }
-            __syncwarp();
-            int ord = 0, pairs = 0;
+            const int n = p.T * p.k;   // <= kMaxDecodePairs, checked on the host
+            if (n <= 32) {
+                // one pair per lane, in registers: a slot's pairs are found by one match, a
+                // pair's occurrence is the count of its slot's lanes below it
+                const unsigned below = (1u << lane) - 1u;
+                const int s = lane < n ? p.slot[lane] : -1;
+                const bool ok = lane < n && s >= 0 && s < p.num_slots;
+                if (lane < n && s >= p.num_slots && blockIdx.x == 0) atomicOr(p.status, MOE_STATUS_BAD_SLOT);
+                const unsigned peers = __match_any_sync(0xffffffffu, ok ? s : -1 - lane);
+                const int occ = __popc(peers & below), tot = __popc(peers);
+                const bool start = ok && (occ % NT) == 0;
+                const unsigned bal = __ballot_sync(0xffffffffu, start);
+                const int mykey = start ? __popc(bal & below) : 0;
+                // the lane that starts this pair's key: the (occ0 + 1)-th lane of its slot
+                const int src = (ok && !start) ? (int)__fns(peers, 0, occ - occ % NT + 1) : lane;
+                const int key = __shfl_sync(0xffffffffu, mykey, src);
+                // first kplist index of each key: exclusive scan of the key sizes, key order =
+                // lane order of the starting pairs
+                const int csize = start ? min(NT, tot - occ) : 0;
+                int inc = csize;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int i = lane + 32 * h;
-                int s = -1, np = 0;
-                bool first = false;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += y;
+                }
+                const int base = __shfl_sync(0xffffffffu, inc - csize, src);
+                if (lane < n) pinfo[lane] = ok ? ((key << 5) | (occ % NT)) : -1;
+                if (start) {
+                    kslot[mykey] = s;
+                    kinfo[mykey] = (base << 16) | csize;
+                }
+                if (ok) kplist[base + occ % NT] = (short)lane;
+                const unsigned okbal = __ballot_sync(0xffffffffu, ok);
+                if (lane == 0) {
+                    n_keys_sh = __popc(bal);
+                    pairs_total_sh = __popc(okbal);
+                }
+            } else {
+            int* sslot = reinterpret_cast<int*>(hbuf);   // the slots, during the setup only
+            for (int i = lane; i < n; i += 32) sslot[i] = p.slot[i];
+            __syncwarp();
+            // occurrence of each pair's slot among the pairs before it (kept in kplist for
+            // now); a pair whose occurrence is a multiple of NT starts a key
+            int ord = 0, pairs = 0;
+            for (int i0 = 0; i0 < n; i0 += 32) {
+                const int i = i0 + lane;
+                int s = -1, occ = 0, tot = 0;
+                bool ok = false;
                 if (i < n) {
                     s = sslot[i];
-                    const bool ok = s >= 0 && s < p.num_slots;
+                    ok = s >= 0 && s < p.num_slots;
                     if (s >= p.num_slots && blockIdx.x == 0) atomicOr(p.status, MOE_STATUS_BAD_SLOT);
-                    pairs += ok;
-                    first = ok;
-                    for (int jj = 0; jj < i && first; ++jj)
-                        if (sslot[jj] == s) first = false;
-                    if (first)
-                        for (int jj = 0; jj < n; ++jj) np += (sslot[jj] == s);
+                    if (ok) {
+                        for (int j = 0; j < n; ++j) {
+                            const bool same = sslot[j] == s;
+                            occ += (same && j < i);
+                            tot += same;
+                        }
+                    }
+                    kplist[i] = (short)occ;
+                    pinfo[i] = -1;
                 }
-                const unsigned bal = __ballot_sync(0xffffffffu, first);
-                if (first) {
-                    uslots[ord + __popc(bal & ((1u << lane) - 1u))] = s;
-                    upairs[ord + __popc(bal & ((1u << lane) - 1u))] = np;
+                pairs += ok;
+                const bool start = ok && (occ % NT) == 0;
+                const unsigned bal = __ballot_sync(0xffffffffu, start);
+                if (start) {
+                    const int key = ord + __popc(bal & ((1u << lane) - 1u));
+                    pinfo[i] = key << 5;
+                    kslot[key] = s;
+                    kinfo[key] = min(NT, tot - occ);   // pairs of the key (first index later)
                 }
                 ord += __popc(bal);
+            }
+            __syncwarp();
+            // the other pairs join the key started by their chunk's first pair
+            for (int i = lane; i < n; i += 32) {
+                const int s = sslot[i], occ = kplist[i];
+                if (s < 0 || s >= p.num_slots || (occ % NT) == 0) continue;
+                const int occ0 = occ - occ % NT;
+                for (int j = 0; j < i; ++j)
+                    if (sslot[j] == s && kplist[j] == occ0) {
+                        pinfo[i] = (pinfo[j] & ~31) | (occ % NT);
+                        break;
+                    }
+            }
+            __syncwarp();
+            // each key's first index in kplist: exclusive prefix sum of the key sizes
+            int carry = 0;
+            for (int k0 = 0; k0 < ord; k0 += 32) {
+                const int kk = k0 + lane;
+                const int cnt = kk < ord ? kinfo[kk] : 0;
+                int inc = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += y;
+                }
+                if (kk < ord) kinfo[kk] = ((carry + inc - cnt) << 16) | cnt;
+                carry += __shfl_sync(0xffffffffu, inc, 31);
+            }
+            __syncwarp();
+            for (int i = lane; i < n; i += 32) {
+                const int pi = pinfo[i];
+                if (pi >= 0) kplist[(kinfo[pi >> 5] >> 16) + (pi & 31)] = (short)i;
             }
             pairs = __reduce_add_sync(0xffffffffu, (uint32_t)pairs);
             if (lane == 0) {
                 n_keys_sh = ord;
                 pairs_total_sh = pairs;
+            }
             }
         } else if (lane == 0) {
             n_keys_sh = p.plan[1];
@@ -563,7 +643,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 const int ph = unit < n0 ? 0 : 1;
                 const PhaseParams& P = p.ph[ph];
                 UnitInfo u;
-                const bool ok = unit_info<NT>(p, P, ph ? unit - n0 : unit, uslots, u);
+                const bool ok = unit_info<NT>(p, P, ph, ph ? unit - n0 : unit, kslot, kinfo, u);
                 const uint8_t* sbase = p.arena + (int64_t)(ok ? u.slot : 0) * p.slot_bytes;
                 // A unit whose activations are not ready yet (gate/up: x still being quantised by
                 // the CTAs; down: h of its key) gets its weight copies issued into every free
@@ -767,7 +847,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
             const int ph = unit < n0 ? 0 : 1;
             const PhaseParams& P = p.ph[ph];
             UnitInfo u;
-            const bool ok = unit_info<NT>(p, P, ph ? unit - n0 : unit, uslots, u);
+            const bool ok = unit_info<NT>(p, P, ph, ph ? unit - n0 : unit, kslot, kinfo, u);
             if (!dry && !mbar_wait(smem_u32(&tfull[acc]), aphase, abortp)) {
                 if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
                 break;
@@ -804,8 +884,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 const int r = u.m * kBM + row;    // output feature
 #pragma unroll
                 for (int c = 0; c < NT; ++c) {
-                    const bool valid = (p.regime == kRegimeDecode) ? (c < u.ncols && sslot[c] == u.slot) : (c < u.ncols);
-                    if (valid && !dry) p.rows_out[(size_t)(u.brow0 + c) * p.d + r] = vals[c];
+                    if (c >= u.ncols || dry) continue;
+                    // decode: column c is row c of the key's tile, i.e. its c-th pair
+                    const int row_out = (p.regime == kRegimeDecode) ? kplist[(kinfo[u.key] >> 16) + c] : u.brow0 + c;
+                    p.rows_out[(size_t)row_out * p.d + r] = vals[c];
                 }
                 if (p.regime == kRegimeDecode && p.y) {
                     // y rows [128m + 32q, +32) are complete once every valid pair's rows there are
@@ -814,16 +896,16 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     if (!dry) {
                         __syncwarp();
                         int l = 0;
-                        if (lane == 0) l = (atom_add_acq_rel(p.ycnt + u.m * 4 + q, upairs[u.key]) + upairs[u.key] == pairs_total_sh);
+                        if (lane == 0) l = (atom_add_acq_rel(p.ycnt + u.m * 4 + q, u.ncols) + u.ncols == pairs_total_sh);
                         last = __shfl_sync(0xffffffffu, l, 0) != 0;
                     }
                     if (last) {
                         for (int t = 0; t < p.T; ++t) {
                             float yv = 0.f;
                             for (int j = 0; j < p.k; ++j) {
-                                const int pr = t * p.k + j, s = sslot[pr];
-                                if (s < 0 || s >= p.num_slots) continue;
-                                yv = fmaf(sw[pr], __ldcg(p.rows_out + (size_t)pr * p.d + r), yv);
+                                const int pr = t * p.k + j;
+                                if (pinfo[pr] < 0) continue;   // no valid slot
+                                yv = fmaf(__ldg(p.w + pr), __ldcg(p.rows_out + (size_t)pr * p.d + r), yv);
                             }
                             if (!dry) p.y[(size_t)t * p.d + r] = f32_to_bf16(yv);
                         }
@@ -871,9 +953,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                             }
                         };
                         if (p.regime == kRegimeDecode) {
+                            // token c's pairs of this key: row (pinfo & 31) of the key's h tile
                             if (c < p.T)
-                                for (int jj = 0; jj < p.k; ++jj)
-                                    if (sslot[c * p.k + jj] == u.slot) write_row_t(0, c * p.k + jj);
+                                for (int jj = 0; jj < p.k; ++jj) {
+                                    const int pi = pinfo[c * p.k + jj];
+                                    if (pi >= 0 && (pi >> 5) == u.key) write_row_t(u.key, pi & 31);
+                                }
                         } else {
                             write_row_t(u.btile, c);
                         }
@@ -897,10 +982,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                         }
                     };
                     if (p.regime == kRegimeDecode) {
-                        // column c = token; h for every pair (c, jj) routed to this slot
+                        // column c = token; its pairs of this key: row (pinfo & 31) of the key's h tile
                         if (c < p.T)
-                            for (int jj = 0; jj < p.k; ++jj)
-                                if (sslot[c * p.k + jj] == u.slot) write_row(0, c * p.k + jj);
+                            for (int jj = 0; jj < p.k; ++jj) {
+                                const int pi = pinfo[c * p.k + jj];
+                                if (pi >= 0 && (pi >> 5) == u.key) write_row(u.key, pi & 31);
+                            }
                     } else if (c < u.ncols) {
                         write_row(u.btile, c);
                     }
@@ -946,16 +1033,23 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
 
 constexpr int kMaxGemmCtas = 160;
 
-// Capacity of an activation buffer (x or h, reduction length K) for T tokens: decode uses one
-// tile of up to kMaxNT rows; the prefill plan needs at most act_tiles(m, T) tiles of
-// kPrefillNT rows; a tile is K/256 blocks of act_block_bytes(NT).
-static size_t act_bytes(const moe_dims* m, int T, int K) {
-    const size_t dec = (size_t)act_block_bytes(kMaxNT), pre = act_tiles(m, T) * (size_t)act_block_bytes(kPrefillNT);
+// Decode keys for T tokens: at most one per pair (a slot's pairs in chunks of kDecodeNT).
+static size_t decode_keys(const moe_dims* m, int T) {
+    const size_t n = (size_t)(T > 0 ? T : 1) * m->top_k;
+    return n < (size_t)kMaxDecodePairs ? n : (size_t)kMaxDecodePairs;
+}
+// Capacity of an activation buffer (reduction length K) for T tokens, in tiles of K/256 blocks:
+// decode x is one tile of kDecodeNT rows and decode h one such tile per key; the prefill plan
+// needs at most act_tiles(m, T) tiles of kPrefillNT rows.
+static size_t act_bytes(const moe_dims* m, int T, int K, size_t decode_tiles) {
+    const size_t dec = decode_tiles * act_block_bytes(kDecodeNT), pre = act_tiles(m, T) * (size_t)act_block_bytes(kPrefillNT);
     return (size_t)(K / kKB) * (dec > pre ? dec : pre);
 }
-// keys (decode: slot ordinals; prefill: tiles) and units of either phase
+static size_t act_bytes_x(const moe_dims* m, int T) { return act_bytes(m, T, m->d, 1); }
+static size_t act_bytes_h(const moe_dims* m, int T) { return act_bytes(m, T, m->f, decode_keys(m, T)); }
+// keys (decode: slot chunks; prefill: tiles) and units of either phase
 static size_t max_keys(const moe_dims* m, int T) {
-    return act_tiles(m, T) > (size_t)kMaxNT ? act_tiles(m, T) : (size_t)kMaxNT;
+    return act_tiles(m, T) > decode_keys(m, T) ? act_tiles(m, T) : decode_keys(m, T);
 }
 
 struct TcBuffers {
@@ -971,8 +1065,8 @@ static size_t counters_of(const moe_dims* m, int T) { return 1 + max_keys(m, T) 
 static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& L) {
     TcBuffers b;
     char* o = ws + L.tc;
-    b.x = reinterpret_cast<uint8_t*>(o); o += align256(act_bytes(m, T, m->d));
-    b.h = reinterpret_cast<uint8_t*>(o); o += align256(act_bytes(m, T, m->f));
+    b.x = reinterpret_cast<uint8_t*>(o); o += align256(act_bytes_x(m, T));
+    b.h = reinterpret_cast<uint8_t*>(o); o += align256(act_bytes_h(m, T));
     b.nkeys = max_keys(m, T);
     b.nzero = counters_of(m, T);
     b.zero = reinterpret_cast<int32_t*>(o); o += align256(b.nzero * 4);
@@ -983,7 +1077,7 @@ static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& 
 
 size_t tc_workspace_bytes(const moe_dims* m, int T) {
     const size_t R = (size_t)(T > 0 ? T : 1) * m->top_k;
-    return align256(act_bytes(m, T, m->d)) + align256(act_bytes(m, T, m->f)) + align256(counters_of(m, T) * 4) +
+    return align256(act_bytes_x(m, T)) + align256(act_bytes_h(m, T)) + align256(counters_of(m, T) * 4) +
            align256(R * m->d * 4);
 }
 
@@ -1003,15 +1097,15 @@ static int launch_ffn_nt(int NT, const FfnParams& p, int grid, cudaStream_t st) 
         case 8: return launch_ffn<8>(p, grid, st);
         case 16: return launch_ffn<16>(p, grid, st);
         case 32: return launch_ffn<32>(p, grid, st);
-        case 64: return launch_ffn<64>(p, grid, st);
         default: return MOE_ERR_LAUNCH;
     }
 }
 
-static int nt_for(int cols) { return cols <= 8 ? 8 : cols <= 16 ? 16 : cols <= 32 ? 32 : 64; }
 
 bool tc_supported(const moe_dims* m) { return m->d % kKB == 0 && m->f % kKB == 0; }
-bool tc_decode_supported(const moe_dims* m, int T) { return tc_supported(m) && T >= 1 && T * m->top_k <= kMaxNT; }
+bool tc_decode_supported(const moe_dims* m, int T) {
+    return tc_supported(m) && T >= 1 && T <= kDecodeNT && T * m->top_k <= kMaxDecodePairs;
+}
 
 static FfnParams ffn_params(const moe_dims* m, const moe_arena* ar, int T, const int32_t* slot, int32_t* status,
                             const TcBuffers& b) {
@@ -1035,16 +1129,16 @@ static FfnParams ffn_params(const moe_dims* m, const moe_arena* ar, int T, const
     return p;
 }
 
-// Decode regime: one FFN launch (x quantised by the CTAs into one tile of NT rows, gate/up
-// with SwiGLU and h quantised per (token, j) pair, down to one fp32 row per pair,
-// fixed-order combine into y).
+// Decode regime: one FFN launch (x quantised by the CTAs into one tile of kDecodeNT rows,
+// gate/up with SwiGLU and h quantised per (token, j) pair into its key's tile, down to one fp32
+// row per pair, fixed-order combine into y).  A token's arithmetic does not depend on the
+// other tokens of the call: every column of an MMA is its own dot product, the accumulator
+// chains (two per unit) and every epilogue step are per column.
 int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                      const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
                      int num_sms) {
     if (T == 0) return MOE_OK;
     TcBuffers b = tc_buffers(m, T, ws, L);
-    const int k = m->top_k, R = T * k;
-    const int NT = nt_for(R);
     FfnParams p = ffn_params(m, ar, T, slot, status, b);
     p.regime = kRegimeDecode;
     int32_t* ctr = reinterpret_cast<int32_t*>(ws + L.counter);
@@ -1056,12 +1150,12 @@ int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16
     p.ycnt = ctr + kCtrFfnY;
     p.x_src = x;
     p.w = w;
-    p.ph[0].decode_cols = T;
-    p.ph[1].decode_cols = R;
     p.rows_out = b.rows;
     p.y = y;
     const int grid = num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas;
-    return launch_ffn_nt(NT, p, grid, st);
+    // 8-row tiles up to T = 8 (five pipeline stages), 16 beyond: an MMA's columns do not
+    // depend on each other, so a token's results are the same with either
+    return launch_ffn_nt(T <= 8 ? 8 : kDecodeNT, p, grid, st);
 }
 
 __global__ void plan_kernel(int E, int n, const int32_t* offsets, const int32_t* row_src, const int32_t* slot,

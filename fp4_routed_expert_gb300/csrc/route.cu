@@ -11,8 +11,9 @@
 //
 // How the device reaches the exact set without computing every exact logit:
 //  1. a fast logit D with an error bound delta, |D - exact| <= delta:
-//     decode (T <= 16): each lane sums its bf16 products (exact in fp32) in chunks of c
-//       products, the chunks with TwoSum compensation (Ogita, Rump, Oishi, "Accurate sum and
+//     decode (T <= 16): each lane sums its bf16 products (exact in fp32) in chunks of c = 1
+//       product (the kernel takes any c; one keeps a token's arithmetic independent of T),
+//       the chunks with TwoSum compensation (Ogita, Rump, Oishi, "Accurate sum and
 //       dot product", SIAM J. Sci. Comput. 26(6), 2005, Sum2) along 8/c independent chains of
 //       m = d/256 chunks; chains and lanes are then added as (sum, compensation) pairs with
 //       TwoSum in fp32:
@@ -805,9 +806,9 @@ static int launch_route_args(RouteArgs& a, cudaStream_t st, int num_sms) {
         a.refine_coef = (float)(coef * (1.0 + 1.0 / 4096.0));
     }
     if (a.T <= kDecodeMaxT && decode_smem_bytes(a.T, a.d) <= kDecodeSmemMax) {
-        if (a.T <= 2) return launch_decode_ch<1>(a, st, num_sms);
-        if (a.T <= 4) return launch_decode_ch<2>(a, st, num_sms);
-        return launch_decode_ch<4>(a, st, num_sms);
+        // chunks of one product for every T: a token's logits are then the same arithmetic
+        // whatever the other tokens of the call (verify rows equal their decode calls)
+        return launch_decode_ch<1>(a, st, num_sms);
     }
     a.bound_coef = gamma_coef(kChunkK + (a.d + kChunkK - 1) / kChunkK + 1);
     const int rows = a.T + a.E;

@@ -328,6 +328,39 @@ def test_full_shape_verify_T16(full_decode, cuda_cores):
     check_tokens(wl, x, got, [0, 7, 15])
 
 
+def assert_rows_equal_single_calls(wl, x, cuda_cores):
+    """Each row of one call on all of x equals the call on that token alone, bit for bit."""
+    big = run_layer(wl, x, cuda_cores=cuda_cores)
+    assert big["status"] == 0
+    for t in range(x.shape[0]):
+        one = run_layer(wl, x[t:t + 1], cuda_cores=cuda_cores)
+        assert one["status"] == 0
+        np.testing.assert_array_equal(one["ids"][0], big["ids"][t])
+        np.testing.assert_array_equal(one["slots"][0], big["slots"][t])
+        assert one["w"][0].tobytes() == big["w"][t].tobytes(), t
+        assert one["y"][0].tobytes() == big["y"][t].tobytes(), t   # fp32 view of the bf16 row
+    return big
+
+
+@pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor_cores", "cuda_cores"])
+def test_verify_rows_equal_decode_calls(full_decode, cuda_cores):
+    """DSpark verify: every row of a T=16 call reproduces the T=1 decode call on that token bit
+    for bit (routing and output), including a token that appears twice."""
+    x = syn.activations(0, 0, 16, 5120, stream=11).copy()
+    x[9] = x[2]
+    assert_rows_equal_single_calls(full_decode, x, cuda_cores)
+
+
+def test_slots_shared_by_experts_and_split_keys():
+    """16 experts on 3 slots: a token may route two of its experts to one slot, and at T=16 a
+    slot collects more than 16 pairs, so its pairs form several keys.  Output against the
+    oracle, and rows against single-token calls bit for bit."""
+    wl = make_workload(1024, 768, 16, 4, seed=7, scale=(-9, -5), table=np.arange(16) % 3)
+    x = syn.activations(7, 0, 16, 1024)
+    big = assert_rows_equal_single_calls(wl, x, False)
+    check_tokens(wl, x, big, list(range(16)))
+
+
 @pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor_cores", "cuda_cores"])
 def test_full_shape_prefill_sampled_tokens(full_decode, cuda_cores):
     wl = full_decode
