@@ -160,7 +160,9 @@ int moe_permute(const moe_dims* dims, int32_t T, const int32_t* topk_ids, int32_
  * as a sum of four MXFP4 terms each (e2m1 codes, UE8M0 scale per 32 elements, every term
  * quantising the previous terms' residual); its expert outputs match exact fp4 x bf16
  * products to about 1e-4 relative before the bf16 rounding of y.  The tensor-core path takes
- * decode calls with T*k <= 64; other decode calls use the CUDA-core kernels. */
+ * decode calls with T*k <= 128; other decode calls use the CUDA-core kernels.  In either
+ * kernel family a decode call's row t is bit-identical to the T = 1 call on token t alone
+ * (with the same routing), so multi-row verification reproduces single-token decoding. */
 int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, const uint16_t* x,
                        const int32_t* topk_ids, const int32_t* topk_slot, const float* topk_w,
                        const int32_t* group_offsets, const int32_t* row_src, const int32_t* row_dst,
