@@ -18,7 +18,8 @@ from . import build as _build
 __all__ = [
     "MoeError", "moe_dims", "moe_arena", "lib", "moe_slot_bytes", "moe_workspace_bytes",
     "moe_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_route_topk_noalloc", "moe_permute",
-    "moe_expert_ffn_fp4", "moe_combine", "moe_status_str", "moe_kernel_launches", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
+    "moe_expert_ffn_fp4", "moe_combine", "moe_split_waves", "moe_gather_experts", "moe_status_str",
+    "moe_kernel_launches", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
     "MOE_STATUS_FEW_RESIDENT", "MOE_STATUS_BAD_SLOT", "MOE_STATUS_TIMEOUT", "DECODE_MAX_T",
 ]
 
@@ -57,6 +58,8 @@ _SIG = {
     "moe_permute": (ctypes.c_int, [_P, _I] + [_P] * 5 + [ctypes.c_size_t, _P]),
     "moe_expert_ffn_fp4": (ctypes.c_int, [_P, _P, _I] + [_P] * 7 + [_I] + [_P] * 4 + [ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [_P, _I] + [_P] * 5),
+    "moe_split_waves": (ctypes.c_int, [_P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
+    "moe_gather_experts": (ctypes.c_int, [_P, _P, _P, _I] + [_P] * 6),
     "moe_route_topk_noalloc": (ctypes.c_int, [_P, _I] + [_P] * 9),
     "moe_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_kernel_launches": (ctypes.c_uint64, []),
@@ -165,6 +168,22 @@ def moe_expert_ffn_fp4(dims, arena: moe_arena, T, x, topk_ids, topk_slot, topk_w
 def moe_combine(dims, T, rows, row_dst, topk_w, y, stream=None):
     _check("moe_combine", lib().moe_combine(
         ctypes.byref(_dims(dims)), int(T), _ptr(rows), _ptr(row_dst), _ptr(topk_w), _ptr(y), _stream(stream)))
+
+
+def moe_split_waves(dims, T, topk_ids, topk_slot, resident_expert, num_slots, slot_wave1, slot_wave2, missing,
+                    n_missing, stream=None):
+    _check("moe_split_waves", lib().moe_split_waves(
+        ctypes.byref(_dims(dims)), int(T), _ptr(topk_ids), _ptr(topk_slot), _ptr(resident_expert), int(num_slots),
+        _ptr(slot_wave1), _ptr(slot_wave2), _ptr(missing), _ptr(n_missing), _stream(stream)))
+
+
+def moe_gather_experts(dims, arena, store_ptr, n_store, missing, n_missing, expert_to_slot, resident_expert,
+                       dev_status, stream=None):
+    """store_ptr: int device-accessible address of the slot images (device memory, or pinned
+    host memory mapped into the device)."""
+    _check("moe_gather_experts", lib().moe_gather_experts(
+        ctypes.byref(_dims(dims)), ctypes.byref(arena), ctypes.c_void_p(int(store_ptr)), int(n_store), _ptr(missing),
+        _ptr(n_missing), _ptr(expert_to_slot), _ptr(resident_expert), _ptr(dev_status), _stream(stream)))
 
 
 from .layer import MoeLayer  # noqa: E402  (device buffers + the four calls in order)

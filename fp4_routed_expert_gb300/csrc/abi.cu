@@ -29,6 +29,12 @@ bool tc_decode_supported(const moe_dims* m, int T);
 int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                      const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
                      int num_sms);
+int launch_split_waves(const moe_dims* m, int T, const int32_t* ids, const int32_t* slot, const int32_t* resident_expert,
+                       int num_slots, int32_t* wave1, int32_t* wave2, int32_t* missing, int32_t* n_missing,
+                       cudaStream_t st);
+int launch_gather_experts(const moe_arena* ar, const uint8_t* store, int n_store, const int32_t* missing,
+                          const int32_t* n_missing, const int32_t* expert_to_slot, int32_t* resident_expert,
+                          int32_t* status, cudaStream_t st, int num_sms);
 int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                       const int32_t* offsets, const int32_t* row_src, float* rows_out, int32_t* status, char* ws,
                       const WsLayout& L, cudaStream_t st, int num_sms);
@@ -197,6 +203,31 @@ int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, 
         rc = launch_prefill_ffn(dims, arena, T, x, topk_slot, group_offsets, row_src, rows, dev_status, w, L, st, sms);
     if (rc || !fused) return rc;
     return launch_combine(dims, T, rows, row_dst, topk_w, y, st, sms);
+}
+
+int moe_split_waves(const moe_dims* dims, int32_t T, const int32_t* topk_ids, const int32_t* topk_slot,
+                    const int32_t* resident_expert, int32_t num_slots, int32_t* slot_wave1, int32_t* slot_wave2,
+                    int32_t* missing, int32_t* n_missing, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (T < 0) return MOE_ERR_TOKENS;
+    if (num_slots <= 0) return MOE_ERR_ARENA;
+    if (!topk_ids || !topk_slot || !resident_expert || !slot_wave1 || !slot_wave2 || !missing || !n_missing)
+        return MOE_ERR_NULL;
+    return launch_split_waves(dims, T, topk_ids, topk_slot, resident_expert, num_slots, slot_wave1, slot_wave2, missing,
+                              n_missing, (cudaStream_t)stream);
+}
+
+int moe_gather_experts(const moe_dims* dims, const moe_arena* arena, const void* store, int32_t n_store,
+                       const int32_t* missing, const int32_t* n_missing, const int32_t* expert_to_slot,
+                       int32_t* resident_expert, int32_t* dev_status, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    int rc = check_arena(dims, arena);
+    if (rc) return rc;
+    if (!store || !missing || !n_missing || !expert_to_slot || !resident_expert || !dev_status) return MOE_ERR_NULL;
+    if (n_store <= 0) return MOE_ERR_DIMS;
+    if (!aligned16(store)) return MOE_ERR_ALIGN;
+    return launch_gather_experts(arena, static_cast<const uint8_t*>(store), n_store, missing, n_missing, expert_to_slot,
+                                 resident_expert, dev_status, (cudaStream_t)stream, num_sms_of_current_device());
 }
 
 int moe_combine(const moe_dims* dims, int32_t T, const float* rows, const int32_t* row_dst, const float* topk_w,

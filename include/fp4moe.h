@@ -174,6 +174,38 @@ int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, 
 int moe_combine(const moe_dims* dims, int32_t T, const float* rows, const int32_t* row_dst,
                 const float* topk_w, uint16_t* y, void* stream);
 
+/* Partial residency (the two-wave routed MoE; "DeepSeek-V4.1-Flash on a single NVIDIA DGX
+ * Spark", 30 September follow-up: compute the experts on hand before the top-up read and the
+ * rest after it, bit-exact because every (token, slot) row is written once and the slot sum is
+ * a separate fixed-order kernel; 28 September follow-up: a GPU-driven expert gather).
+ *
+ * The routing is made with the table of destination slots (expert_to_slot: where each expert
+ * lives when resident; missing experts must have distinct slots).  resident_expert int32
+ * [num_slots] (device) says which expert each slot holds now (-1: none).
+ *
+ * moe_split_waves: for the T*k pairs, slot_wave1 = the pair's slot if that slot holds the
+ * pair's expert now, else -1; slot_wave2 = the pair's slot otherwise, else -1 (pairs without a
+ * valid slot are -1 in both).  missing int32 [T*k] receives the distinct experts of wave 2 in
+ * ascending id and *n_missing (device int32) their count.  One kernel; all device memory.
+ *
+ * moe_gather_experts: copies, for each of the *n_missing experts e in missing, the slot image
+ * at store + e * slot_bytes (n_store images; moe_pack_expert's layout, e.g. packed into a slot
+ * and copied out) into slot expert_to_slot[e] of the arena, and sets resident_expert of that
+ * slot to e.  store is any device-accessible address: device memory, or pinned host memory
+ * mapped into the device (the kernel reads it directly; no copy is issued by the host).
+ * 16-byte aligned.  An expert with no valid slot sets MOE_STATUS_BAD_SLOT and is skipped.
+ *
+ * Two waves: split; moe_expert_ffn_fp4 (flags 0) with slot_wave1 into rows; gather; the same
+ * call with slot_wave2 into the same rows (each row is written by one of the two calls); then
+ * moe_combine.  The result equals the one-wave call (all experts resident, same routing) bit
+ * for bit. */
+int moe_split_waves(const moe_dims* dims, int32_t T, const int32_t* topk_ids, const int32_t* topk_slot,
+                    const int32_t* resident_expert, int32_t num_slots, int32_t* slot_wave1, int32_t* slot_wave2,
+                    int32_t* missing, int32_t* n_missing, void* stream);
+int moe_gather_experts(const moe_dims* dims, const moe_arena* arena, const void* store, int32_t n_store,
+                       const int32_t* missing, const int32_t* n_missing, const int32_t* expert_to_slot,
+                       int32_t* resident_expert, int32_t* dev_status, void* stream);
+
 /* Number of kernels this library has enqueued in this process so far (every entry point
  * above counts the kernels it launches).  A call captured into a CUDA graph counts once, at
  * capture, so the difference across a capture is the kernel count of one graph replay.

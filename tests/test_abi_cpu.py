@@ -54,5 +54,11 @@ def test_host_argument_errors_return_before_any_launch():
     assert L.moe_expert_ffn_fp4(ctypes.byref(good), ctypes.byref(ar), 1, fake, fake, fake, fake, None, None, None, 7,
                                 None, fake, fake, fake, 1 << 30, None) == -6
     assert L.moe_pack_expert(ctypes.byref(good), fake, fake, fake, fake, fake, fake, ctypes.byref(ar), 9, None) == -5
+    assert L.moe_split_waves(ctypes.byref(good), 1, fake, fake, fake, 0, fake, fake, fake, fake, None) == -5
+    assert L.moe_split_waves(ctypes.byref(good), 1, fake, None, fake, 4, fake, fake, fake, fake, None) == -1
+    ar = moe.moe_arena(1 << 20, moe.moe_slot_bytes(good), 4)
+    assert L.moe_gather_experts(ctypes.byref(good), ctypes.byref(ar), P((1 << 20) + 8), 16, fake, fake, fake, fake, fake,
+                                None) == -8
+    assert L.moe_gather_experts(ctypes.byref(good), ctypes.byref(ar), fake, 16, fake, None, fake, fake, fake, None) == -1
     assert moe.moe_status_str(-4) == "workspace too small"
     assert moe.moe_kernel_launches() == launched      # every rejected call launched nothing

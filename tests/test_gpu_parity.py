@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import fp4_routed_expert_gb300 as moe
-from fp4_routed_expert_gb300.layer import MoeLayer
+from fp4_routed_expert_gb300.layer import Arena, MoeLayer
 import oracle
 from synth import gpu as sgpu
 from synth import tensors as syn
@@ -359,6 +359,82 @@ def test_slots_shared_by_experts_and_split_keys():
     x = syn.activations(7, 0, 16, 1024)
     big = assert_rows_equal_single_calls(wl, x, False)
     check_tokens(wl, x, big, list(range(16)))
+
+
+def host_device_pointer(t):
+    """Device address of pinned host tensor t (cudaHostGetDevicePointer)."""
+    import ctypes
+    rt = None
+    for name in ("libcudart.so.13", "libcudart.so"):
+        try:
+            rt = ctypes.CDLL(name)
+            break
+        except OSError:
+            pass
+    if rt is None:
+        return t.data_ptr()   # unified addressing: the host address is the device address
+    dp = ctypes.c_void_p()
+    assert rt.cudaHostGetDevicePointer(ctypes.byref(dp), ctypes.c_void_p(t.data_ptr()), 0) == 0
+    return dp.value
+
+
+@pytest.mark.parametrize("T", [3, 40])
+def test_two_wave_moe_equals_one_wave(T):
+    """Partial residency (NEXT-2): with half the experts on hand, wave 1 computes their rows,
+    one kernel gathers the missing experts from pinned host memory into their slots, wave 2
+    computes the rest, and the fixed-order combine gives the one-wave result bit for bit."""
+    d, f, E, k = 1024, 768, 16, 4
+    full = make_workload(d, f, E, k, seed=21, scale=(-9, -5))        # identity table: slot e = expert e
+    dims = moe.moe_dims(d, f, E, k)
+    sb = moe.moe_slot_bytes(dims)
+    store = torch.empty(E * sb, dtype=torch.uint8, pin_memory=True)  # every expert's slot image
+    store.copy_(full.arena.buf[:E * sb].cpu())
+    part = Arena(dims, E, DEV)
+    part.buf.zero_()
+    resident = torch.full((E,), -1, dtype=torch.int32, device=DEV)
+    for e in (0, 2, 3, 5, 7, 8, 11, 13):
+        part.buf[e * sb:(e + 1) * sb].copy_(full.arena.buf[e * sb:(e + 1) * sb])
+        resident[e] = e
+    x_bits = syn.activations(21, 0, T, d)
+    x = bits_to_torch(x_bits, DEV)
+    wr = bits_to_torch(full.wr, DEV)
+    tab = torch.from_numpy(full.table).to(DEV)
+    layer = MoeLayer(d, f, E, k, T, part)
+    layer.route(x, wr, tab)
+    n = T * k
+    moe.moe_permute(dims, T, layer.ids, layer.offsets, layer.row_src, layer.row_dst, layer.ws)
+    w1, w2, missing = (torch.empty(n, dtype=torch.int32, device=DEV) for _ in range(3))
+    n_missing = torch.zeros(1, dtype=torch.int32, device=DEV)
+    moe.moe_split_waves(dims, T, layer.ids, layer.slots, resident, E, w1, w2, missing, n_missing)
+    rows = torch.full((n, d), float("nan"), dtype=torch.float32, device=DEV)
+    ffn = lambda arena, slots, out: moe.moe_expert_ffn_fp4(
+        dims, arena.c, T, x, layer.ids, slots, layer.w, layer.offsets, layer.row_src, layer.row_dst, 0, out, None,
+        layer.status, layer.ws)
+    ffn(part, w1, rows)
+    moe.moe_gather_experts(dims, part.c, host_device_pointer(store), E, missing, n_missing, tab, resident, layer.status)
+    ffn(part, w2, rows)
+    y2 = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    moe.moe_combine(dims, T, rows, layer.row_dst, layer.w, y2)
+    rows1 = torch.empty_like(rows)
+    ffn(full.arena, layer.slots, rows1)
+    y1 = torch.empty_like(y2)
+    moe.moe_combine(dims, T, rows1, layer.row_dst, layer.w, y1)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    ids = layer.ids[:T].cpu().numpy()
+    want = sorted(set(int(e) for e in ids.ravel() if e >= 0) - {0, 2, 3, 5, 7, 8, 11, 13})
+    assert int(n_missing.item()) == len(want) and missing[:len(want)].cpu().tolist() == want
+    w1h, w2h, slots = w1.cpu().numpy(), w2.cpu().numpy(), layer.slots[:T].cpu().numpy().ravel()
+    assert ((w1h >= 0) != (w2h >= 0)).all() and (np.maximum(w1h, w2h) == slots).all()
+    for e in want:                                                   # gathered images and residency
+        assert torch.equal(part.buf[e * sb:(e + 1) * sb], full.arena.buf[e * sb:(e + 1) * sb]), e
+        assert int(resident[e].item()) == e
+    valid = layer.row_src[:n].cpu().numpy() >= 0
+    assert torch.equal(rows[torch.from_numpy(valid).to(DEV)].view(torch.int32),
+                       rows1[torch.from_numpy(valid).to(DEV)].view(torch.int32))
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    check_tokens(full, x_bits, dict(ids=ids, slots=layer.slots[:T].cpu().numpy(), w=layer.w[:T].cpu().numpy(),
+                                    y=y2.float().cpu().numpy()), list(range(min(T, 8))))
 
 
 @pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor_cores", "cuda_cores"])
