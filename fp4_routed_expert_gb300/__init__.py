@@ -18,7 +18,7 @@ from . import build as _build
 __all__ = [
     "MoeError", "moe_dims", "moe_arena", "lib", "moe_slot_bytes", "moe_workspace_bytes",
     "moe_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_route_topk_noalloc", "moe_permute",
-    "moe_expert_ffn_fp4", "moe_combine", "moe_split_waves", "moe_gather_experts", "moe_status_str",
+    "moe_expert_ffn_fp4", "moe_combine", "moe_residency_bias", "moe_split_waves", "moe_gather_experts", "moe_status_str",
     "moe_kernel_launches", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
     "MOE_STATUS_FEW_RESIDENT", "MOE_STATUS_BAD_SLOT", "MOE_STATUS_TIMEOUT", "DECODE_MAX_T",
 ]
@@ -58,6 +58,7 @@ _SIG = {
     "moe_permute": (ctypes.c_int, [_P, _I] + [_P] * 5 + [ctypes.c_size_t, _P]),
     "moe_expert_ffn_fp4": (ctypes.c_int, [_P, _P, _I] + [_P] * 7 + [_I] + [_P] * 4 + [ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [_P, _I] + [_P] * 5),
+    "moe_residency_bias": (ctypes.c_int, [_P, _P, _P, _P, _I, ctypes.c_float, _P, _P]),
     "moe_split_waves": (ctypes.c_int, [_P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
     "moe_gather_experts": (ctypes.c_int, [_P, _P, _P, _I] + [_P] * 6),
     "moe_route_topk_noalloc": (ctypes.c_int, [_P, _I] + [_P] * 9),
@@ -168,6 +169,12 @@ def moe_expert_ffn_fp4(dims, arena: moe_arena, T, x, topk_ids, topk_slot, topk_w
 def moe_combine(dims, T, rows, row_dst, topk_w, y, stream=None):
     _check("moe_combine", lib().moe_combine(
         ctypes.byref(_dims(dims)), int(T), _ptr(rows), _ptr(row_dst), _ptr(topk_w), _ptr(y), _stream(stream)))
+
+
+def moe_residency_bias(dims, score_bias, expert_to_slot, resident_expert, num_slots, lam, bias_out, stream=None):
+    _check("moe_residency_bias", lib().moe_residency_bias(
+        ctypes.byref(_dims(dims)), _ptr(score_bias), _ptr(expert_to_slot), _ptr(resident_expert), int(num_slots),
+        float(lam), _ptr(bias_out), _stream(stream)))
 
 
 def moe_split_waves(dims, T, topk_ids, topk_slot, resident_expert, num_slots, slot_wave1, slot_wave2, missing,

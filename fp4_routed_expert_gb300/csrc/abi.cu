@@ -29,6 +29,8 @@ bool tc_decode_supported(const moe_dims* m, int T);
 int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                      const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
                      int num_sms);
+int launch_residency_bias(const moe_dims* m, const int32_t* expert_to_slot, const int32_t* resident_expert,
+                          int num_slots, const float* bias, float lambda, float* bias_out, cudaStream_t st);
 int launch_split_waves(const moe_dims* m, int T, const int32_t* ids, const int32_t* slot, const int32_t* resident_expert,
                        int num_slots, int32_t* wave1, int32_t* wave2, int32_t* missing, int32_t* n_missing,
                        cudaStream_t st);
@@ -203,6 +205,16 @@ int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, 
         rc = launch_prefill_ffn(dims, arena, T, x, topk_slot, group_offsets, row_src, rows, dev_status, w, L, st, sms);
     if (rc || !fused) return rc;
     return launch_combine(dims, T, rows, row_dst, topk_w, y, st, sms);
+}
+
+int moe_residency_bias(const moe_dims* dims, const float* score_bias, const int32_t* expert_to_slot,
+                       const int32_t* resident_expert, int32_t num_slots, float lambda, float* bias_out, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (num_slots <= 0) return MOE_ERR_ARENA;
+    if (!(lambda >= 0.0f) || !(lambda < 3.0e38f)) return MOE_ERR_DIMS;   // finite, >= 0 (NaN fails both)
+    if (!expert_to_slot || !resident_expert || !bias_out) return MOE_ERR_NULL;
+    return launch_residency_bias(dims, expert_to_slot, resident_expert, num_slots, score_bias, lambda, bias_out,
+                                 (cudaStream_t)stream);
 }
 
 int moe_split_waves(const moe_dims* dims, int32_t T, const int32_t* topk_ids, const int32_t* topk_slot,

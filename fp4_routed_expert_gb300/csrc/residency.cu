@@ -95,6 +95,30 @@ __global__ void __launch_bounds__(256) gather_experts_kernel(const uint8_t* __re
     }
 }
 
+// Cache-conditional routing ("DeepSeek-V4.1-Flash on a single NVIDIA DGX Spark", Conventions
+// and the expert-cache document list it as an approved approximation, after "Mixture of
+// Cache-Conditional Experts", arXiv 2412.00099): instead of the hard mask of non-resident
+// experts, a resident expert's selection key gets a bonus lambda.  bias_out[e] = bias[e] +
+// lambda if expert e sits in its slot now, else bias[e].
+__global__ void residency_bias_kernel(int E, const int32_t* __restrict__ expert_to_slot,
+                                      const int32_t* __restrict__ resident_expert, int num_slots,
+                                      const float* __restrict__ bias, float lambda, float* __restrict__ bias_out) {
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+        const int s = expert_to_slot[e];
+        const bool on_hand = s >= 0 && s < num_slots && resident_expert[s] == e;
+        const float b = bias ? bias[e] : 0.0f;
+        bias_out[e] = on_hand ? __fadd_rn(b, lambda) : b;
+    }
+}
+
+int launch_residency_bias(const moe_dims* m, const int32_t* expert_to_slot, const int32_t* resident_expert,
+                          int num_slots, const float* bias, float lambda, float* bias_out, cudaStream_t st) {
+    residency_bias_kernel<<<(m->num_experts + 255) / 256, 256, 0, st>>>(m->num_experts, expert_to_slot, resident_expert,
+                                                                        num_slots, bias, lambda, bias_out);
+    note_launch(1);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
 int launch_split_waves(const moe_dims* m, int T, const int32_t* ids, const int32_t* slot, const int32_t* resident_expert,
                        int num_slots, int32_t* wave1, int32_t* wave2, int32_t* missing, int32_t* n_missing,
                        cudaStream_t st) {

@@ -199,6 +199,18 @@ int moe_combine(const moe_dims* dims, int32_t T, const float* rows, const int32_
  * call with slot_wave2 into the same rows (each row is written by one of the two calls); then
  * moe_combine.  The result equals the one-wave call (all experts resident, same routing) bit
  * for bit. */
+/* Cache-conditional routing (NEXT-4; the pages list it as an approved approximation after
+ * "Mixture of Cache-Conditional Experts", arXiv 2412.00099; they give no formula, the reading
+ * here is an additive bonus): instead of masking non-resident experts (expert_to_slot = -1),
+ * route with every expert's destination slot and this bias:
+ *   bias_out[e] = score_bias[e] (0 if score_bias is NULL) + lambda   if slot expert_to_slot[e]
+ *                 holds e now (resident_expert), else score_bias[e].
+ * Selection keys become s_e + bias_out[e]; weights stay s_j / sum s.  lambda = 0 is the exact
+ * routing; a lambda above the spread of the keys gives the hard mask whenever k experts are
+ * resident.  lambda must be finite and >= 0 (else MOE_ERR_DIMS).  One kernel, E entries. */
+int moe_residency_bias(const moe_dims* dims, const float* score_bias, const int32_t* expert_to_slot,
+                       const int32_t* resident_expert, int32_t num_slots, float lambda, float* bias_out,
+                       void* stream);
 int moe_split_waves(const moe_dims* dims, int32_t T, const int32_t* topk_ids, const int32_t* topk_slot,
                     const int32_t* resident_expert, int32_t num_slots, int32_t* slot_wave1, int32_t* slot_wave2,
                     int32_t* missing, int32_t* n_missing, void* stream);

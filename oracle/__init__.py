@@ -10,6 +10,7 @@ Parity status per function (what pins it is in tests/test_oracle_pins.py):
   exact fp32 router logit        pinned (exact rational arithmetic, hand-made midpoints)
   router score                   pinned (multi-precision sigmoid, special values)
   route_topk                     pinned (hand-worked examples in tests/golden/)
+  residency_bias                 pinned (hand-worked values, brute-force routing limits)
   permute                        pinned (brute force and invariants)
   expert_ffn / combine / layer   pinned (closed forms, independent fp64 re-derivation)
   residual_rmsnorm               pinned (independent fp64 re-derivation)
@@ -49,6 +50,8 @@ def lib():
         L.oracle_dot_bf16_rn32.argtypes = [P, P, i32, P]
         L.oracle_router_score.restype = ctypes.c_float
         L.oracle_router_score.argtypes = [ctypes.c_float]
+        L.oracle_residency_bias.restype = None
+        L.oracle_residency_bias.argtypes = [i32, P, P, P, i32, ctypes.c_float, P]
         L.oracle_route_topk.restype = i32
         L.oracle_route_topk.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
         L.oracle_permute.restype = i32
@@ -122,6 +125,16 @@ def route_topk(x_bits, w_router_bits, bias, expert_to_slot, k, want_logits=False
     out = dict(ids=ids, weights=w, slots=slots, status=int(st))
     if want_logits:
         out["logits"], out["scores"] = lg, sc
+    return out
+
+
+def residency_bias(bias, expert_to_slot, resident_expert, lam):
+    """Cache-conditional routing bias: bias + lam (fp32) for experts resident in their slot."""
+    tab = _c(expert_to_slot, np.int32)
+    res = _c(resident_expert, np.int32)
+    b = None if bias is None else _c(bias, np.float32)
+    out = np.zeros(tab.shape[0], np.float32)
+    lib().oracle_residency_bias(tab.shape[0], _p(b), _p(tab), _p(res), res.shape[0], ctypes.c_float(lam), _p(out))
     return out
 
 

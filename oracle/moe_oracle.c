@@ -178,6 +178,25 @@ float oracle_router_score(float logit) {
     return (float)(1.0 / (1.0 + exp(-(double)logit)));
 }
 
+/* ---- cache-conditional routing bias ------------------------------------------------ */
+
+/* "DeepSeek-V4.1-Flash on a single NVIDIA DGX Spark", Conventions and the expert-cache
+ * document: cache-conditional routing (after arXiv 2412.00099) is an approved approximation
+ * that favours experts already resident instead of masking the others.  The pages give no
+ * formula; the reading taken: a bonus lambda added to a resident expert's selection bias,
+ *   out[e] = bias[e] + lambda (one fp32 rounding)  if slot expert_to_slot[e] holds e now,
+ *   out[e] = bias[e]                               otherwise (bias NULL means 0).
+ * Routing then uses every expert's destination slot and this bias: keys s + out[e]. */
+void oracle_residency_bias(int E, const float* bias, const int32_t* expert_to_slot,
+                           const int32_t* resident_expert, int num_slots, float lambda, float* out) {
+    for (int e = 0; e < E; ++e) {
+        float b = bias ? bias[e] : 0.0f;
+        int s = expert_to_slot[e];
+        int on_hand = s >= 0 && s < num_slots && resident_expert[s] == e;
+        out[e] = on_hand ? b + lambda : b;
+    }
+}
+
 /* ---- router: score, mask, top-k, renormalise, slot lookup -------------------------- */
 
 /* For each token t: key[e] = s[e] + bias[e] in fp32 (bias NULL means 0) for experts with

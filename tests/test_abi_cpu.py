@@ -60,5 +60,11 @@ def test_host_argument_errors_return_before_any_launch():
     assert L.moe_gather_experts(ctypes.byref(good), ctypes.byref(ar), P((1 << 20) + 8), 16, fake, fake, fake, fake, fake,
                                 None) == -8
     assert L.moe_gather_experts(ctypes.byref(good), ctypes.byref(ar), fake, 16, fake, None, fake, fake, fake, None) == -1
+    f32 = ctypes.c_float
+    assert L.moe_residency_bias(ctypes.byref(good), None, fake, fake, 0, f32(0.1), fake, None) == -5
+    assert L.moe_residency_bias(ctypes.byref(good), None, fake, None, 4, f32(0.1), fake, None) == -1
+    assert L.moe_residency_bias(ctypes.byref(good), None, fake, fake, 4, f32(-0.1), fake, None) == -2
+    assert L.moe_residency_bias(ctypes.byref(good), None, fake, fake, 4, f32(float("nan")), fake, None) == -2
+    assert L.moe_residency_bias(ctypes.byref(good), None, fake, fake, 4, f32(float("inf")), fake, None) == -2
     assert moe.moe_status_str(-4) == "workspace too small"
     assert moe.moe_kernel_launches() == launched      # every rejected call launched nothing

@@ -437,6 +437,64 @@ def test_two_wave_moe_equals_one_wave(T):
                                     y=y2.float().cpu().numpy()), list(range(min(T, 8))))
 
 
+@pytest.mark.parametrize("T", [3, 40])
+def test_cache_conditional_routing_two_waves(T):
+    """Cache-conditional routing (NEXT-4) on a partly resident arena: moe_residency_bias gives
+    the oracle's bias bit for bit, the router never masks (every expert keeps its slot), it
+    picks resident experts more often than exact routing yet still picks some missing ones, and
+    the two-wave layer (wave 1, gather, wave 2, fixed-order combine) matches the oracle layer
+    routed with the same bias."""
+    d, f, E, k, lam = 1024, 768, 16, 4, 0.05
+    on = (1, 4, 6, 9, 10, 14)
+    full = make_workload(d, f, E, k, seed=23, scale=(-9, -5))        # identity table
+    dims = moe.moe_dims(d, f, E, k)
+    sb = moe.moe_slot_bytes(dims)
+    store = torch.empty(E * sb, dtype=torch.uint8, pin_memory=True)
+    store.copy_(full.arena.buf[:E * sb].cpu())
+    part = Arena(dims, E, DEV)
+    part.buf.zero_()
+    resident = torch.full((E,), -1, dtype=torch.int32, device=DEV)
+    for e in on:
+        part.buf[e * sb:(e + 1) * sb].copy_(full.arena.buf[e * sb:(e + 1) * sb])
+        resident[e] = e
+    res_host = resident.cpu().numpy()
+    tab = torch.from_numpy(full.table).to(DEV)
+    base = syn.zipf_score_bias(0, 0, E, 1.2, 0.01)
+    bias = torch.empty(E, dtype=torch.float32, device=DEV)
+    moe.moe_residency_bias(dims, torch.from_numpy(base).to(DEV), tab, resident, E, lam, bias)
+    x_bits = syn.activations(23, 0, T, d)
+    x = bits_to_torch(x_bits, DEV)
+    layer = MoeLayer(d, f, E, k, T, part)
+    layer.route(x, bits_to_torch(full.wr, DEV), tab, bias)
+    n = T * k
+    moe.moe_permute(dims, T, layer.ids, layer.offsets, layer.row_src, layer.row_dst, layer.ws)
+    w1, w2, missing = (torch.empty(n, dtype=torch.int32, device=DEV) for _ in range(3))
+    n_missing = torch.zeros(1, dtype=torch.int32, device=DEV)
+    moe.moe_split_waves(dims, T, layer.ids, layer.slots, resident, E, w1, w2, missing, n_missing)
+    rows = torch.full((n, d), float("nan"), dtype=torch.float32, device=DEV)
+    ffn = lambda slots: moe.moe_expert_ffn_fp4(
+        dims, part.c, T, x, layer.ids, slots, layer.w, layer.offsets, layer.row_src, layer.row_dst, 0, rows, None,
+        layer.status, layer.ws)
+    ffn(w1)
+    moe.moe_gather_experts(dims, part.c, host_device_pointer(store), E, missing, n_missing, tab, resident, layer.status)
+    ffn(w2)
+    y = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    moe.moe_combine(dims, T, rows, layer.row_dst, layer.w, y)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    want_bias = oracle.residency_bias(base, full.table, res_host, lam)
+    np.testing.assert_array_equal(bias.cpu().numpy().view(np.int32), want_bias.view(np.int32))
+    ids = layer.ids[:T].cpu().numpy()
+    exact = oracle.route_topk(x_bits, full.wr, base, full.table, k)
+    share = lambda a: np.isin(a, on).mean()
+    assert share(ids) > share(exact["ids"]) and share(ids) < 1.0, (share(ids), share(exact["ids"]))
+    got = dict(ids=ids, slots=layer.slots[:T].cpu().numpy(), w=layer.w[:T].cpu().numpy(), y=y.float().cpu().numpy())
+    r = oracle.route_topk(x_bits, full.wr, want_bias, full.table, k)
+    np.testing.assert_array_equal(got["ids"], r["ids"])
+    np.testing.assert_array_equal(got["slots"], r["slots"])
+    check_tokens(full, x_bits, got, list(range(min(T, 8))), bias=want_bias)
+
+
 @pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor_cores", "cuda_cores"])
 def test_full_shape_prefill_sampled_tokens(full_decode, cuda_cores):
     wl = full_decode

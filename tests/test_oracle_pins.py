@@ -474,3 +474,83 @@ def test_expert_size_matches_the_pages():
     n = int(g["experts_total"])
     assert round(n * b / 1e9, 1) == float(g["bytes_total_gb"])
     assert round(n * 3 * d * f / 1e9, 1) == float(g["weights_total_billion"])
+
+
+# ----------------------------------------------------------------- cache-conditional routing
+
+def test_residency_bias_hand_worked():
+    """Hand values: slots 0..3 hold experts 4, 1, -, 2, so experts 1, 2 and 4 are resident;
+    expert 0 maps to slot 3 (which holds 2), expert 3 has no slot, expert 5 points outside the
+    slot range."""
+    tab = np.array([3, 1, 3, -1, 0, 7], np.int32)
+    res = np.array([4, 1, -1, 2], np.int32)
+    bias = np.array([0.25, -0.5, 0.125, 1.0, 1.0, 0.0], np.float32)
+    got = oracle.residency_bias(bias, tab, res, 0.5)
+    assert got.tolist() == [0.25, 0.0, 0.625, 1.0, 1.5, 0.0]
+    # one fp32 rounding: 1 + 2^-25 rounds back to 1, 1 + 3*2^-24 rounds to 1 + 2^-22
+    got = oracle.residency_bias(bias, tab, res, 2.0 ** -25)
+    assert got[4] == np.float32(1.0) and got[1] == np.float32(-0.5 + 2.0 ** -25)
+    got = oracle.residency_bias(bias, tab, res, 3 * 2.0 ** -24)
+    assert got[4] == np.float32(1.0 + 2.0 ** -22)
+    assert oracle.residency_bias(None, tab, res, 0.5).tolist() == [0.0, 0.5, 0.5, 0.0, 0.5, 0.0]
+
+
+def _brute_route(x, wr, bias, k):
+    """Top-k by python sort of (-(s + bias) in fp32, id) over every expert, weights s / sum."""
+    T, E = x.shape[0], wr.shape[0]
+    ids, ws = [], []
+    for t in range(T):
+        s = [np.float32(1.0 / (1.0 + math.exp(-float(round_fraction_to_f32(
+            sum((bf16_exact(int(a)) * bf16_exact(int(b)) for a, b in zip(x[t], wr[e])), Fraction(0)))))))
+            for e in range(E)]
+        keys = sorted((-float(np.float32(s[e] + bias[e])), e) for e in range(E))
+        chosen = sorted(e for _, e in keys[:k])
+        tot = np.float32(0)
+        for e in chosen:
+            tot = np.float32(tot + s[e])
+        ids.append(chosen)
+        ws.append([np.float32(s[e] / tot) for e in chosen])
+    return np.array(ids, np.int32), np.array(ws, np.float32)
+
+
+def test_cache_conditional_routing_limits():
+    """Soft residency bias on tiny random routers: it never masks (every expert keeps its slot),
+    lambda = 0 is the exact routing, a large lambda picks only resident experts (the hard mask's
+    choice when the masked keys are separated), and a moderate lambda still lets a strong
+    non-resident expert through; every case matches a brute-force restatement."""
+    rng = np.random.default_rng(12)
+    T, d, E, k = 4, 64, 12, 3
+    saw_nonresident = 0
+    for trial in range(12):
+        x = syn.f32_to_bf16_bits(rng.normal(size=(T, d)).astype(np.float32))
+        wr = syn.f32_to_bf16_bits((rng.normal(size=(E, d)) * 0.08).astype(np.float32))
+        tab = rng.permutation(E).astype(np.int32)
+        res = np.full(E, -1, np.int32)
+        on = rng.choice(E, 5, replace=False)
+        res[tab[on]] = on
+        bias = (rng.normal(size=E) * 0.02).astype(np.float32) if trial % 2 else None
+        b0 = np.zeros(E, np.float32) if bias is None else bias
+        exact = oracle.route_topk(x, wr, bias, tab, k)
+        for lam in (0.0, 0.03, 1.0):
+            rb = oracle.residency_bias(bias, tab, res, lam)
+            r = oracle.route_topk(x, wr, rb, tab, k)
+            assert r["status"] == 0
+            ids, ws = _brute_route(x, wr, rb, k)
+            np.testing.assert_array_equal(r["ids"], ids)
+            np.testing.assert_array_equal(r["weights"], ws)
+            np.testing.assert_array_equal(r["slots"], tab[r["ids"]])
+            if lam == 0.0:
+                np.testing.assert_array_equal(r["ids"], exact["ids"])
+                np.testing.assert_array_equal(r["weights"], exact["weights"])
+            if lam == 1.0:
+                assert np.isin(r["ids"], on).all()
+                masked_tab = np.where(np.isin(np.arange(E), on), tab, -1).astype(np.int32)
+                m = oracle.route_topk(x, wr, bias, masked_tab, k, want_logits=True)
+                for t in range(T):
+                    kv = np.sort((m["scores"][t] + b0)[on])[::-1]
+                    if kv[k - 1] - kv[k] > 2.0 ** -20:
+                        np.testing.assert_array_equal(r["ids"][t], m["ids"][t])
+                        np.testing.assert_array_equal(r["weights"][t], m["weights"][t])
+            if lam == 0.03:
+                saw_nonresident += int((~np.isin(r["ids"], on)).sum())
+    assert saw_nonresident > 0
