@@ -11,6 +11,8 @@ Parity status per function (what pins it is in tests/test_oracle_pins.py):
   router score                   pinned (multi-precision sigmoid, special values)
   route_topk                     pinned (hand-worked examples in tests/golden/)
   residency_bias                 pinned (hand-worked values, brute-force routing limits)
+  cb3_pack_row / cb3_expert_ffn  pinned (exhaustive partitions in exact rationals, lossless
+                                 rows, FP4 FFN on lossless experts)
   permute                        pinned (brute force and invariants)
   expert_ffn / combine / layer   pinned (closed forms, independent fp64 re-derivation)
   residual_rmsnorm               pinned (independent fp64 re-derivation)
@@ -52,6 +54,10 @@ def lib():
         L.oracle_router_score.argtypes = [ctypes.c_float]
         L.oracle_residency_bias.restype = None
         L.oracle_residency_bias.argtypes = [i32, P, P, P, i32, ctypes.c_float, P]
+        L.oracle_cb3_pack_row.restype = i32
+        L.oracle_cb3_pack_row.argtypes = [i32, P, P, P, P]
+        L.oracle_cb3_expert_ffn.restype = None
+        L.oracle_cb3_expert_ffn.argtypes = [i32, i32] + [P] * 9
         L.oracle_route_topk.restype = i32
         L.oracle_route_topk.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
         L.oracle_permute.restype = i32
@@ -158,6 +164,47 @@ def expert_ffn(x_bits, ex: dict):
     h = np.zeros(f, np.float64)
     z = np.zeros(d, np.float64)
     lib().oracle_expert_ffn(d, f, _p(x), *[_p(a) for a in arrs], _p(h), _p(z))
+    return h, z
+
+
+def cb3_pack_row(q_row, s_row):
+    """One FP4 row (packed codes, UE8M0 scales) -> (levels uint16 bf16 bits [8], idx uint8 [K],
+    number of distinct values)."""
+    q = _c(q_row, np.uint8)
+    sc = _c(s_row, np.uint8)
+    K = q.size * 2
+    cb = np.zeros(8, np.uint16)
+    idx = np.zeros(K, np.uint8)
+    n = lib().oracle_cb3_pack_row(K, _p(q), _p(sc), _p(cb), _p(idx))
+    return cb, idx, int(n)
+
+
+def cb3_pack_expert(ex: dict):
+    """Canonical FP4 expert tensors -> dict of cb3 levels [rows, 8] and indices [rows, K] for
+    the gate, up and down matrices."""
+    out = {}
+    for m in ("gate", "up", "down"):
+        q, sc = _c(ex[m + "_q"], np.uint8), _c(ex[m + "_s"], np.uint8)
+        R, K = q.shape[0], q.shape[1] * 2
+        cb = np.zeros((R, 8), np.uint16)
+        idx = np.zeros((R, K), np.uint8)
+        for r in range(R):
+            cb[r], idx[r], _ = cb3_pack_row(q[r], sc[r])
+        out[m + "_cb"], out[m + "_idx"] = cb, idx
+    return out
+
+
+def cb3_expert_ffn(x_bits, cx: dict):
+    """One cb3 expert (cb3_pack_expert's dict) on one token; returns (h [f], z [d]) in fp64."""
+    x = _c(x_bits, np.uint16)
+    d = x.size
+    f = cx["gate_cb"].shape[0]
+    arrs = []
+    for m in ("gate", "up", "down"):
+        arrs += [_c(cx[m + "_cb"], np.uint16), _c(cx[m + "_idx"], np.uint8)]
+    h = np.zeros(f, np.float64)
+    z = np.zeros(d, np.float64)
+    lib().oracle_cb3_expert_ffn(d, f, _p(x), *[_p(a) for a in arrs], _p(h), _p(z))
     return h, z
 
 

@@ -316,6 +316,132 @@ void oracle_expert_ffn(int d, int f, const uint16_t* x, const uint8_t* gate_q,
     if (!h_out) free(h);
 }
 
+/* ---- cb3: a 3-bit per-row codebook packed from the FP4 experts --------------------- */
+
+/* "DeepSeek-V4.1-Flash on a single NVIDIA DGX Spark", section "The numbers": the resident
+ * experts can be held in a 3-bit per-row codebook packed from the checkpoint's own FP4
+ * experts (an approximation of the model).  The pages give no packing rule; the reading
+ * taken: each matrix row gets 8 bf16 levels and every weight a 3-bit index, and the levels
+ * are the ones that minimise the row's squared error against its FP4 values -- the optimal
+ * 1-D 8-means of the row.  Its clusters are contiguous runs of the sorted distinct values
+ * (Fisher 1958), so it is found exactly by dynamic programming over split points:
+ *   u_0 < ... < u_{n-1} the distinct values, c_i their counts; prefix sums in ascending
+ *   order N_i = sum c, S_i = sum c*u, Q_i = sum (c*u)*u;
+ *   cost(a, b) = (Q_b - Q_a) - (S_b - S_a)^2 / (N_b - N_a)   (squared error of [a, b));
+ *   D_1(i) = cost(0, i);  D_g(i) = min over m in [g-1, i) of D_{g-1}(m) + cost(m, i),
+ *   the smallest m on ties; G = min(8, n) clusters, traced back from D_G(n).
+ * Level g = bf16(mean of cluster g) = bf16((S_b - S_a) / (N_b - N_a)), one rounding; levels
+ * past G are 0; a weight's index is its cluster.  Every step is fp64 in the order written. */
+static int cmp_double(const void* a, const void* b) {
+    double x = *(const double*)a, y = *(const double*)b;
+    return (x > y) - (x < y);
+}
+
+static double cb3_cost(const double* N, const double* S, const double* Q, int a, int b) {
+    double s1 = S[b] - S[a];
+    double s2 = Q[b] - Q[a];
+    double nn = N[b] - N[a];
+    return s2 - (s1 * s1) / nn;
+}
+
+/* One FP4 row of K weights -> 8 bf16 levels (cb) and K indices (idx).  Returns n, the number
+ * of distinct values in the row (-0 and +0 are one value). */
+int oracle_cb3_pack_row(int K, const uint8_t* qrow, const uint8_t* srow, uint16_t* cb, uint8_t* idx) {
+    double* v = (double*)malloc(sizeof(double) * (size_t)K);
+    double* u = (double*)malloc(sizeof(double) * (size_t)K);
+    double* cnt = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int k = 0; k < K; ++k) {
+        v[k] = oracle_weight_at(qrow, srow, k);
+        if (v[k] == 0.0) v[k] = 0.0;                  /* -0 joins +0 */
+    }
+    memcpy(u, v, sizeof(double) * (size_t)K);
+    qsort(u, (size_t)K, sizeof(double), cmp_double);
+    int n = 0;
+    for (int k = 0; k < K; ++k) {
+        if (n > 0 && u[n - 1] == u[k]) { cnt[n - 1] += 1.0; continue; }
+        u[n] = u[k];
+        cnt[n] = 1.0;
+        ++n;
+    }
+    double* N = (double*)calloc((size_t)n + 1, sizeof(double));
+    double* S = (double*)calloc((size_t)n + 1, sizeof(double));
+    double* Q = (double*)calloc((size_t)n + 1, sizeof(double));
+    for (int i = 0; i < n; ++i) {
+        double cu = cnt[i] * u[i];
+        N[i + 1] = N[i] + cnt[i];
+        S[i + 1] = S[i] + cu;
+        Q[i + 1] = Q[i] + cu * u[i];
+    }
+    int G = n < 8 ? n : 8;
+    double* D = (double*)malloc(sizeof(double) * (size_t)(G + 1) * (size_t)(n + 1));
+    int* split = (int*)malloc(sizeof(int) * (size_t)(G + 1) * (size_t)(n + 1));
+#define DD(g, i) D[(size_t)(g) * (size_t)(n + 1) + (size_t)(i)]
+#define SP(g, i) split[(size_t)(g) * (size_t)(n + 1) + (size_t)(i)]
+    for (int i = 1; i <= n; ++i) { DD(1, i) = cb3_cost(N, S, Q, 0, i); SP(1, i) = 0; }
+    for (int g = 2; g <= G; ++g)
+        for (int i = g; i <= n; ++i) {
+            int best = -1;
+            double bv = 0.0;
+            for (int m = g - 1; m < i; ++m) {
+                double c = DD(g - 1, m) + cb3_cost(N, S, Q, m, i);
+                if (best < 0 || c < bv) { best = m; bv = c; }
+            }
+            DD(g, i) = bv;
+            SP(g, i) = best;
+        }
+    int* start = (int*)malloc(sizeof(int) * 9);
+    int b = n;
+    for (int g = G; g >= 1; --g) {
+        int a = SP(g, b);
+        start[g - 1] = a;
+        cb[g - 1] = oracle_bf16_from_double((S[b] - S[a]) / (N[b] - N[a]));
+        b = a;
+    }
+    start[G] = n;
+    for (int g = G; g < 8; ++g) cb[g] = 0;
+    for (int k = 0; k < K; ++k) {
+        int lo = 0, hi = n - 1;                        /* v[k] is u[lo] after the search */
+        while (lo < hi) {
+            int mid = (lo + hi) / 2;
+            if (u[mid] < v[k]) lo = mid + 1; else hi = mid;
+        }
+        int g = 0;
+        while (g + 1 < G && start[g + 1] <= lo) ++g;
+        idx[k] = (uint8_t)g;
+    }
+#undef DD
+#undef SP
+    free(v); free(u); free(cnt); free(N); free(S); free(Q); free(D); free(split); free(start);
+    return n;
+}
+
+/* The SwiGLU expert FFN of oracle_expert_ffn with cb3 weights: W[r, k] = bf16 level
+ * cb[r*8 + idx[r*K + k]] of row r (gate and up rows K = d, down rows K = f). */
+void oracle_cb3_expert_ffn(int d, int f, const uint16_t* x, const uint16_t* cb_gate,
+                           const uint8_t* idx_gate, const uint16_t* cb_up, const uint8_t* idx_up,
+                           const uint16_t* cb_down, const uint8_t* idx_down, double* h_out,
+                           double* z_out) {
+    double* h = h_out ? h_out : (double*)malloc(sizeof(double) * (size_t)f);
+    double* xd = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int k = 0; k < d; ++k) xd[k] = oracle_bf16_value(x[k]);
+    for (int i = 0; i < f; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int k = 0; k < d; ++k) {
+            g += xd[k] * oracle_bf16_value(cb_gate[(size_t)i * 8 + idx_gate[(size_t)i * d + k]]);
+            u += xd[k] * oracle_bf16_value(cb_up[(size_t)i * 8 + idx_up[(size_t)i * d + k]]);
+        }
+        h[i] = g / (1.0 + exp(-g)) * u;
+    }
+    for (int r = 0; r < d; ++r) {
+        double z = 0.0;
+        for (int i = 0; i < f; ++i)
+            z += oracle_bf16_value(cb_down[(size_t)r * 8 + idx_down[(size_t)r * f + i]]) * h[i];
+        z_out[r] = z;
+    }
+    free(xd);
+    if (!h_out) free(h);
+}
+
 /* ---- combine: y = sum_j w_j z_j in ascending j (= ascending expert id) ------------- */
 
 void oracle_combine(int d, int k, const double* z, const float* w, double* y) {

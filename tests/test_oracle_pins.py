@@ -554,3 +554,156 @@ def test_cache_conditional_routing_limits():
             if lam == 0.03:
                 saw_nonresident += int((~np.isin(r["ids"], on)).sum())
     assert saw_nonresident > 0
+
+
+# ----------------------------------------------------------------------------- cb3 codec
+
+E2M1_CODE = {0.0: 0, 0.5: 1, 1.0: 2, 1.5: 3, 2.0: 4, 3.0: 5, 4.0: 6, 6.0: 7}
+
+
+def _fp4_row(values, scale_bytes):
+    """Pack K values (each an e2m1 value times its block's 2^(b-127)) into codes + scales."""
+    K = len(values)
+    q = np.zeros(K // 2, np.uint8)
+    for k, v in enumerate(values):
+        m = abs(v) / 2.0 ** (int(scale_bytes[k // 32]) - 127)
+        c = E2M1_CODE[m] | (8 if v < 0 else 0)
+        q[k // 2] |= c << (4 * (k % 2))
+    return q, np.asarray(scale_bytes, np.uint8)
+
+
+def _levels(cb):
+    return [oracle.bf16_value(int(b)) for b in cb]
+
+
+SIGNED_E2M1 = [0.0] + [sg * m for m in (0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0) for sg in (1.0, -1.0)]
+
+
+def test_cb3_lossless_rows():
+    """A row with at most 8 distinct values is reproduced exactly: its levels are those values,
+    ascending, then zeros."""
+    rng = np.random.default_rng(31)
+    for trial in range(20):
+        nv = int(rng.integers(1, 9))
+        vals = [float(v) for v in rng.choice(SIGNED_E2M1, nv, replace=False)]
+        b = int(rng.integers(100, 140))
+        row = [v * 2.0 ** (b - 127) for v in rng.choice(vals, 64)]
+        q, s = _fp4_row(row, [b, b])
+        cb, idx, n = oracle.cb3_pack_row(q, s)
+        distinct = sorted(set(row))
+        assert n == len(distinct)
+        lv = _levels(cb)
+        assert lv[:n] == distinct and all(v == 0.0 for v in lv[n:])
+        assert [lv[i] for i in idx] == row
+
+
+def test_cb3_equal_cost_tie_goes_to_the_earlier_split():
+    """Nine equally spaced values (-4..4), 32 of each: every merge of two neighbours costs the
+    same (16); the smallest split point on ties merges the top pair, 3 and 4 -> 3.5."""
+    vals = [-4.0, -3.0, -2.0, -1.0, 0.0, 1.0, 2.0, 3.0, 4.0]
+    row = [v for v in vals for _ in range(32)]
+    q, s = _fp4_row(row, [127] * 9)
+    cb, idx, n = oracle.cb3_pack_row(q, s)
+    assert n == 9
+    assert _levels(cb) == [-4.0, -3.0, -2.0, -1.0, 0.0, 1.0, 2.0, 3.5]
+    assert idx.tolist() == [min(i // 32, 7) for i in range(288)]
+
+
+def _set_partitions(n, blocks):
+    """Every partition of range(n) into exactly `blocks` non-empty sets (restricted growth)."""
+    a = [0] * n
+
+    def rec(i, m):
+        if i == n:
+            if m == blocks:
+                yield list(a)
+            return
+        if blocks - m > n - i:
+            return
+        for v in range(min(m + 1, blocks)):
+            a[i] = v
+            yield from rec(i + 1, max(m, v + 1))
+
+    yield from rec(0, 0)
+
+
+def test_cb3_optimal_among_all_partitions():
+    """Rows with 9 or 10 distinct values and uneven counts: the oracle's clusters reach the
+    least squared error over every partition of the distinct values into 8 sets (not only
+    contiguous ones), computed in exact rationals; each level is bf16 of its cluster's exact
+    mean and the levels ascend."""
+    rng = np.random.default_rng(32)
+    for trial in range(8):
+        nd = 9 + trial % 2
+        vals = [float(v) for v in rng.choice(SIGNED_E2M1, nd, replace=False)]
+        row = vals + [float(v) for v in rng.choice(vals, 64 - nd, p=rng.dirichlet(np.ones(nd)))]
+        rng.shuffle(row)
+        q, s = _fp4_row(row, [127, 127])
+        cb, idx, n = oracle.cb3_pack_row(q, s)
+        u = sorted(set(row))
+        assert n == len(u) == nd
+        cnt = {v: row.count(v) for v in u}
+
+        def sse(groups):
+            tot = Fraction(0)
+            for g in groups:
+                c = sum(cnt[v] for v in g)
+                mean = sum(Fraction(v) * cnt[v] for v in g) / c
+                tot += sum(cnt[v] * (Fraction(v) - mean) ** 2 for v in g)
+            return tot
+
+        best = min(sse([[u[i] for i in range(n) if p[i] == b] for b in range(8)]) for p in _set_partitions(n, 8))
+        got_groups = [sorted({row[k] for k in range(64) if idx[k] == g}) for g in range(8)]
+        assert all(got_groups), got_groups
+        assert sum(len(g) for g in got_groups) == n         # every value in exactly one cluster
+        assert sse(got_groups) == best
+        lv = _levels(cb)
+        assert lv == sorted(lv)
+        for g, grp in enumerate(got_groups):
+            mean = sum(Fraction(v) * cnt[v] for v in grp) / sum(cnt[v] for v in grp)
+            assert lv[g] == round_fraction_to_bf16(mean), (g, grp)
+
+
+def round_fraction_to_bf16(v: Fraction) -> float:
+    """Nearest bf16 to an exact rational, ties to even (normal range)."""
+    if v == 0:
+        return 0.0
+    sgn = -1 if v < 0 else 1
+    a = abs(v)
+    e = math.floor(math.log2(a))
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (e - 7)
+    r = a / quantum
+    fl = math.floor(r)
+    rem = r - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sgn * float(fl * quantum)
+
+
+def test_cb3_ffn_equals_fp4_ffn_on_lossless_expert():
+    """An expert whose rows hold at most 8 distinct values packs losslessly, so the cb3 FFN
+    equals the FP4 FFN exactly (same products, same order)."""
+    rng = np.random.default_rng(33)
+    d, f = 64, 32
+    ex = {}
+    for m, (R, K) in (("gate", (f, d)), ("up", (f, d)), ("down", (d, f))):
+        qs, ss = [], []
+        for r in range(R):
+            b = int(rng.integers(122, 128))
+            mags = rng.choice([0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], 4, replace=False)
+            vals = [float(v) * 2.0 ** (b - 127) for v in np.concatenate([mags, -mags])]
+            q, s = _fp4_row([float(v) for v in rng.choice(vals, K)], [b] * (K // 32))
+            qs.append(q)
+            ss.append(s)
+        ex[m + "_q"], ex[m + "_s"] = np.stack(qs), np.stack(ss)
+    cx = oracle.cb3_pack_expert(ex)
+    for t in range(3):
+        x = syn.f32_to_bf16_bits(rng.normal(size=d).astype(np.float32))
+        h1, z1 = oracle.expert_ffn(x, ex)
+        h2, z2 = oracle.cb3_expert_ffn(x, cx)
+        np.testing.assert_array_equal(h1, h2)
+        np.testing.assert_array_equal(z1, z2)
