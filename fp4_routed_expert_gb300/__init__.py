@@ -19,6 +19,7 @@ __all__ = [
     "MoeError", "moe_dims", "moe_arena", "lib", "moe_slot_bytes", "moe_workspace_bytes",
     "moe_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_route_topk_noalloc", "moe_permute",
     "moe_expert_ffn_fp4", "moe_combine", "moe_residency_bias", "moe_split_waves", "moe_gather_experts", "moe_status_str",
+    "moe_cb3_slot_bytes", "moe_pack_cb3", "moe_expert_ffn_cb3", "MOE_STATUS_CB3_ROW",
     "moe_kernel_launches", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
     "MOE_STATUS_FEW_RESIDENT", "MOE_STATUS_BAD_SLOT", "MOE_STATUS_TIMEOUT", "DECODE_MAX_T",
 ]
@@ -28,6 +29,7 @@ MOE_FFN_CUDA_CORES = 2
 MOE_STATUS_FEW_RESIDENT = 1
 MOE_STATUS_BAD_SLOT = 2
 MOE_STATUS_TIMEOUT = 4
+MOE_STATUS_CB3_ROW = 8
 DECODE_MAX_T = 16
 
 
@@ -59,6 +61,9 @@ _SIG = {
     "moe_expert_ffn_fp4": (ctypes.c_int, [_P, _P, _I] + [_P] * 7 + [_I] + [_P] * 4 + [ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [_P, _I] + [_P] * 5),
     "moe_residency_bias": (ctypes.c_int, [_P, _P, _P, _P, _I, ctypes.c_float, _P, _P]),
+    "moe_cb3_slot_bytes": (ctypes.c_int64, [_P]),
+    "moe_pack_cb3": (ctypes.c_int, [_P, _P, _I, _P, _I, _P, _P]),
+    "moe_expert_ffn_cb3": (ctypes.c_int, [_P, _P, _I] + [_P] * 6 + [ctypes.c_size_t, _P]),
     "moe_split_waves": (ctypes.c_int, [_P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
     "moe_gather_experts": (ctypes.c_int, [_P, _P, _P, _I] + [_P] * 6),
     "moe_route_topk_noalloc": (ctypes.c_int, [_P, _I] + [_P] * 9),
@@ -175,6 +180,21 @@ def moe_residency_bias(dims, score_bias, expert_to_slot, resident_expert, num_sl
     _check("moe_residency_bias", lib().moe_residency_bias(
         ctypes.byref(_dims(dims)), _ptr(score_bias), _ptr(expert_to_slot), _ptr(resident_expert), int(num_slots),
         float(lam), _ptr(bias_out), _stream(stream)))
+
+
+def moe_cb3_slot_bytes(dims) -> int:
+    return int(lib().moe_cb3_slot_bytes(ctypes.byref(_dims(dims))))
+
+
+def moe_pack_cb3(dims, fp4_arena, fp4_slot, cb3_arena, cb3_slot, status, stream=None):
+    _check("moe_pack_cb3", lib().moe_pack_cb3(ctypes.byref(_dims(dims)), ctypes.byref(fp4_arena), int(fp4_slot),
+                                              ctypes.byref(cb3_arena), int(cb3_slot), _ptr(status), _stream(stream)))
+
+
+def moe_expert_ffn_cb3(dims, cb3_arena, T, x, topk_slot, topk_w, y, status, ws, stream=None):
+    _check("moe_expert_ffn_cb3", lib().moe_expert_ffn_cb3(
+        ctypes.byref(_dims(dims)), ctypes.byref(cb3_arena), int(T), _ptr(x), _ptr(topk_slot), _ptr(topk_w), _ptr(y),
+        _ptr(status), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_split_waves(dims, T, topk_ids, topk_slot, resident_expert, num_slots, slot_wave1, slot_wave2, missing,

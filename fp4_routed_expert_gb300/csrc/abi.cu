@@ -25,6 +25,11 @@ int launch_prefill_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint
 int launch_combine(const moe_dims* m, int T, const float* rows, const int32_t* row_dst, const float* w,
                    uint16_t* y, cudaStream_t st, int num_sms);
 bool tc_supported(const moe_dims* m);
+int64_t cb3_slot_bytes(int d, int f);
+int launch_pack_cb3(const moe_dims* m, const uint8_t* src_slot, uint8_t* dst_slot, int32_t* status, cudaStream_t st);
+int launch_cb3_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
+                   const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
+                   int num_sms);
 bool tc_decode_supported(const moe_dims* m, int T);
 int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                      const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
@@ -89,10 +94,11 @@ static int check_ws(const moe_dims* m, int T, void* ws, size_t ws_bytes, WsLayou
     return MOE_OK;
 }
 
-static int check_arena(const moe_dims* m, const moe_arena* ar) {
+static int check_arena(const moe_dims* m, const moe_arena* ar, bool cb3 = false) {
     if (!ar || !ar->base) return MOE_ERR_NULL;
     if ((reinterpret_cast<uintptr_t>(ar->base) & 1023u) != 0) return MOE_ERR_ARENA;
-    if (ar->slot_bytes != slot_layout(m->d, m->f).bytes || ar->num_slots <= 0) return MOE_ERR_ARENA;
+    const int64_t want = cb3 ? cb3_slot_bytes(m->d, m->f) : slot_layout(m->d, m->f).bytes;
+    if (ar->slot_bytes != want || ar->num_slots <= 0) return MOE_ERR_ARENA;
     return MOE_OK;
 }
 
@@ -249,6 +255,42 @@ int moe_combine(const moe_dims* dims, int32_t T, const float* rows, const int32_
     if (T > 0 && (!rows || !row_dst || !topk_w || !y)) return MOE_ERR_NULL;
     if (T > 0 && (!aligned16(rows) || !aligned16(y))) return MOE_ERR_ALIGN;
     return launch_combine(dims, T, rows, row_dst, topk_w, y, (cudaStream_t)stream, num_sms_of_current_device());
+}
+
+int64_t moe_cb3_slot_bytes(const moe_dims* dims) {
+    if (!dims_ok(dims)) return -1;
+    return cb3_slot_bytes(dims->d, dims->f);
+}
+
+int moe_pack_cb3(const moe_dims* dims, const moe_arena* fp4_arena, int32_t fp4_slot, const moe_arena* cb3_arena,
+                 int32_t cb3_slot, int32_t* dev_status, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    int rc = check_arena(dims, fp4_arena);
+    if (rc) return rc;
+    rc = check_arena(dims, cb3_arena, true);
+    if (rc) return rc;
+    if (!dev_status) return MOE_ERR_NULL;
+    if (fp4_slot < 0 || fp4_slot >= fp4_arena->num_slots || cb3_slot < 0 || cb3_slot >= cb3_arena->num_slots)
+        return MOE_ERR_ARENA;
+    const uint8_t* src = static_cast<const uint8_t*>(fp4_arena->base) + (int64_t)fp4_slot * fp4_arena->slot_bytes;
+    uint8_t* dst = static_cast<uint8_t*>(cb3_arena->base) + (int64_t)cb3_slot * cb3_arena->slot_bytes;
+    return launch_pack_cb3(dims, src, dst, dev_status, (cudaStream_t)stream);
+}
+
+int moe_expert_ffn_cb3(const moe_dims* dims, const moe_arena* cb3_arena, int32_t T, const uint16_t* x,
+                       const int32_t* topk_slot, const float* topk_w, uint16_t* y, int32_t* dev_status, void* ws,
+                       size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (T < 0 || T > kDecodeMaxT) return MOE_ERR_TOKENS;
+    int rc = check_arena(dims, cb3_arena, true);
+    if (rc) return rc;
+    if (!x || !topk_slot || !topk_w || !y || !dev_status) return MOE_ERR_NULL;
+    if (!aligned16(x)) return MOE_ERR_ALIGN;
+    WsLayout L;
+    rc = check_ws(dims, T, ws, ws_bytes, &L);
+    if (rc) return rc;
+    return launch_cb3_ffn(dims, cb3_arena, T, x, topk_slot, topk_w, y, dev_status, static_cast<char*>(ws), L,
+                          (cudaStream_t)stream, num_sms_of_current_device());
 }
 
 uint64_t moe_kernel_launches(void) { return fp4moe::g_kernel_launches.load(std::memory_order_relaxed); }

@@ -4,8 +4,9 @@ from __future__ import annotations
 
 import torch
 
-from . import (DECODE_MAX_T, MOE_FFN_CUDA_CORES, MOE_FUSE_COMBINE, moe_arena, moe_dims, moe_expert_ffn_fp4, moe_pack_expert,
-               moe_permute, moe_route_topk, moe_slot_bytes, moe_workspace_bytes, moe_workspace_init)
+from . import (DECODE_MAX_T, MOE_FFN_CUDA_CORES, MOE_FUSE_COMBINE, moe_arena, moe_cb3_slot_bytes, moe_dims,
+               moe_expert_ffn_cb3, moe_expert_ffn_fp4, moe_pack_cb3, moe_pack_expert, moe_permute, moe_route_topk,
+               moe_slot_bytes, moe_workspace_bytes, moe_workspace_init)
 
 
 def aligned_empty(nbytes: int, align: int = 1024, device=None) -> torch.Tensor:
@@ -32,6 +33,23 @@ class Arena:
                         self.c, slot, stream)
 
 
+class Cb3Arena:
+    """Resident expert slots in the cb3 format (3-bit per-row codebook), packed on the device
+    from FP4 slots."""
+
+    def __init__(self, dims: moe_dims, num_slots: int, device=None):
+        self.dims = dims
+        self.slot_bytes = moe_cb3_slot_bytes(dims)
+        if self.slot_bytes <= 0:
+            raise ValueError("unsupported dims")
+        self.buf = aligned_empty(self.slot_bytes * num_slots, 1024, device)
+        self.c = moe_arena(self.buf.data_ptr(), self.slot_bytes, num_slots)
+        self.num_slots = num_slots
+
+    def pack_from(self, fp4: Arena, fp4_slot: int, slot: int, status, stream=None):
+        moe_pack_cb3(self.dims, fp4.c, fp4_slot, self.c, slot, status, stream)
+
+
 class MoeLayer:
     """Buffers for up to T_max tokens and the call sequence of one layer.
 
@@ -56,6 +74,14 @@ class MoeLayer:
         self.row_dst = torch.empty(n, dtype=torch.int32, device=dev)
         self.rows = torch.empty((n, d), dtype=torch.float32, device=dev) if T_max > DECODE_MAX_T else None
         self.y = torch.empty((max(T_max, 1), d), dtype=torch.bfloat16, device=dev)
+
+    def experts_cb3(self, cb3: Cb3Arena, x, T=None, stream=None, y=None):
+        """Expert FFN + combine on cb3 experts (decode and verify, T <= 16); the routing's slots
+        index the cb3 arena."""
+        T = x.shape[0] if T is None else T
+        y = self.y if y is None else y
+        moe_expert_ffn_cb3(self.dims, cb3.c, T, x, self.slots, self.w, y, self.status, self.ws, stream)
+        return y
 
     def route(self, x, w_router, table, bias=None, T=None, stream=None):
         T = x.shape[0] if T is None else T

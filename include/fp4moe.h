@@ -81,6 +81,8 @@ enum {
 #define MOE_STATUS_FEW_RESIDENT 1  /* a token had fewer than top_k resident experts */
 #define MOE_STATUS_BAD_SLOT 2      /* a slot id outside [0, num_slots): that term was skipped */
 #define MOE_STATUS_TIMEOUT 4       /* a bounded device wait gave up */
+#define MOE_STATUS_CB3_ROW 8       /* moe_pack_cb3: a row with more than 256 distinct values or a
+                                      NaN scale; its levels and indices were written as zero */
 
 /* Flags of moe_expert_ffn_fp4. */
 #define MOE_FUSE_COMBINE 1         /* write y directly (fixed-order combine fused in) */
@@ -217,6 +219,36 @@ int moe_split_waves(const moe_dims* dims, int32_t T, const int32_t* topk_ids, co
 int moe_gather_experts(const moe_dims* dims, const moe_arena* arena, const void* store, int32_t n_store,
                        const int32_t* missing, const int32_t* n_missing, const int32_t* expert_to_slot,
                        int32_t* resident_expert, int32_t* dev_status, void* stream);
+
+/* cb3 expert format (NEXT-3; "DeepSeek-V4.1-Flash on a single NVIDIA DGX Spark", section "The
+ * numbers": resident experts in a 3-bit per-row codebook packed from the checkpoint's own FP4
+ * experts).  An approximation of the model that trades accuracy for capacity: 13.4 MB per
+ * expert instead of 18.8 MB at d=5120, f=2304.  Every matrix row (gate, up: K = d; down:
+ * K = f) holds 8 bf16 levels and a 3-bit index per weight.  The pages give no packing rule;
+ * the one used: the levels are the optimal 1-D 8-means of the row's FP4 values (clusters are
+ * contiguous runs of the sorted distinct values, exact dynamic programming over the split
+ * points in fp64, ties to the smaller split), each level its cluster's mean rounded once to
+ * bf16, and a weight's index is its cluster.  A row with at most 8 distinct values is exact.
+ * The slot layout is private to this library (moe_pack_cb3 is its only writer).
+ *
+ * moe_cb3_slot_bytes: bytes per cb3 slot (a multiple of 1024), or -1 for unsupported dims.
+ *
+ * moe_pack_cb3: packs the FP4 expert in slot fp4_slot of fp4_arena (moe_pack_expert's layout)
+ * into slot cb3_slot of cb3_arena (slot_bytes = moe_cb3_slot_bytes).  One kernel, one block
+ * per row.  A row with more than 256 distinct values or a NaN scale sets MOE_STATUS_CB3_ROW.
+ *
+ * moe_expert_ffn_cb3: a5-a6 on cb3 experts for 0 <= T <= 16 tokens (decode and multi-token
+ * verify; larger T returns MOE_ERR_TOKENS): h = silu(W_gate x) * (W_up x), y[t] = bf16(sum_j
+ * w_j W_down h_j) in ascending j, CUDA cores, fp32 accumulation (level x x products are exact
+ * in fp32).  Same routing inputs as the decode call of moe_expert_ffn_fp4 (topk_slot,
+ * topk_w [T, k]); uses the workspace of moe_workspace_bytes(dims, T).  Row t equals the T = 1
+ * call on token t bit for bit.  Slots outside [0, num_slots) set MOE_STATUS_BAD_SLOT. */
+int64_t moe_cb3_slot_bytes(const moe_dims* dims);
+int moe_pack_cb3(const moe_dims* dims, const moe_arena* fp4_arena, int32_t fp4_slot, const moe_arena* cb3_arena,
+                 int32_t cb3_slot, int32_t* dev_status, void* stream);
+int moe_expert_ffn_cb3(const moe_dims* dims, const moe_arena* cb3_arena, int32_t T, const uint16_t* x,
+                       const int32_t* topk_slot, const float* topk_w, uint16_t* y, int32_t* dev_status, void* ws,
+                       size_t ws_bytes, void* stream);
 
 /* Number of kernels this library has enqueued in this process so far (every entry point
  * above counts the kernels it launches).  A call captured into a CUDA graph counts once, at

@@ -56,6 +56,8 @@ def lib():
         L.oracle_residency_bias.argtypes = [i32, P, P, P, i32, ctypes.c_float, P]
         L.oracle_cb3_pack_row.restype = i32
         L.oracle_cb3_pack_row.argtypes = [i32, P, P, P, P]
+        L.oracle_cb3_pack_matrix.restype = None
+        L.oracle_cb3_pack_matrix.argtypes = [i32, i32, P, P, P, P]
         L.oracle_cb3_expert_ffn.restype = None
         L.oracle_cb3_expert_ffn.argtypes = [i32, i32] + [P] * 9
         L.oracle_route_topk.restype = i32
@@ -188,8 +190,7 @@ def cb3_pack_expert(ex: dict):
         R, K = q.shape[0], q.shape[1] * 2
         cb = np.zeros((R, 8), np.uint16)
         idx = np.zeros((R, K), np.uint8)
-        for r in range(R):
-            cb[r], idx[r], _ = cb3_pack_row(q[r], sc[r])
+        lib().oracle_cb3_pack_matrix(R, K, _p(q), _p(sc), _p(cb), _p(idx))
         out[m + "_cb"], out[m + "_idx"] = cb, idx
     return out
 

@@ -415,6 +415,14 @@ int oracle_cb3_pack_row(int K, const uint8_t* qrow, const uint8_t* srow, uint16_
     return n;
 }
 
+/* oracle_cb3_pack_row for each of the R rows of a canonical FP4 matrix (codes [R, K/2],
+ * scales [R, K/32]): levels [R, 8], indices [R, K]. */
+void oracle_cb3_pack_matrix(int R, int K, const uint8_t* q, const uint8_t* s, uint16_t* cb, uint8_t* idx) {
+    for (int r = 0; r < R; ++r)
+        oracle_cb3_pack_row(K, q + (size_t)r * (K / 2), s + (size_t)r * (K / 32), cb + (size_t)r * 8,
+                            idx + (size_t)r * K);
+}
+
 /* The SwiGLU expert FFN of oracle_expert_ffn with cb3 weights: W[r, k] = bf16 level
  * cb[r*8 + idx[r*K + k]] of row r (gate and up rows K = d, down rows K = f). */
 void oracle_cb3_expert_ffn(int d, int f, const uint16_t* x, const uint16_t* cb_gate,

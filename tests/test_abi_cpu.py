@@ -33,6 +33,10 @@ def test_slot_bytes_and_workspace():
     assert moe.moe_workspace_bytes((5120, 2304, 384, 6), 1) > 0
     assert moe.moe_workspace_bytes((5120, 2304, 384, 6), 4096) > moe.moe_workspace_bytes((5120, 2304, 384, 6), 16)
     assert moe.moe_workspace_bytes((5120, 2304, 2000, 6), 1) == 0
+    # cb3: 16 bytes of levels per row (2f + d rows) + 3 bits per weight, rounded up to 1 KB
+    assert moe.moe_cb3_slot_bytes((5120, 2304, 384, 6)) == 13_426_688
+    assert moe.moe_cb3_slot_bytes((512, 256, 16, 2)) == 163_840
+    assert moe.moe_cb3_slot_bytes((500, 256, 16, 2)) == -1
 
 
 def test_host_argument_errors_return_before_any_launch():
@@ -66,5 +70,20 @@ def test_host_argument_errors_return_before_any_launch():
     assert L.moe_residency_bias(ctypes.byref(good), None, fake, fake, 4, f32(-0.1), fake, None) == -2
     assert L.moe_residency_bias(ctypes.byref(good), None, fake, fake, 4, f32(float("nan")), fake, None) == -2
     assert L.moe_residency_bias(ctypes.byref(good), None, fake, fake, 4, f32(float("inf")), fake, None) == -2
+    fp4_ar = moe.moe_arena(1 << 20, moe.moe_slot_bytes(good), 4)
+    cb3_ar = moe.moe_arena(1 << 20, moe.moe_cb3_slot_bytes(good), 4)
+    assert L.moe_pack_cb3(ctypes.byref(good), ctypes.byref(fp4_ar), 0, ctypes.byref(fp4_ar), 0, fake, None) == -5
+    assert L.moe_pack_cb3(ctypes.byref(good), ctypes.byref(fp4_ar), 4, ctypes.byref(cb3_ar), 0, fake, None) == -5
+    assert L.moe_pack_cb3(ctypes.byref(good), ctypes.byref(fp4_ar), 0, ctypes.byref(cb3_ar), -1, fake, None) == -5
+    assert L.moe_pack_cb3(ctypes.byref(good), ctypes.byref(fp4_ar), 0, ctypes.byref(cb3_ar), 0, None, None) == -1
+    assert L.moe_pack_cb3(ctypes.byref(bad), ctypes.byref(fp4_ar), 0, ctypes.byref(cb3_ar), 0, fake, None) == -2
+    assert L.moe_expert_ffn_cb3(ctypes.byref(good), ctypes.byref(cb3_ar), 17, fake, fake, fake, fake, fake, fake,
+                                1 << 30, None) == -3
+    assert L.moe_expert_ffn_cb3(ctypes.byref(good), ctypes.byref(fp4_ar), 1, fake, fake, fake, fake, fake, fake,
+                                1 << 30, None) == -5
+    assert L.moe_expert_ffn_cb3(ctypes.byref(good), ctypes.byref(cb3_ar), 1, fake, fake, fake, None, fake, fake,
+                                1 << 30, None) == -1
+    assert L.moe_expert_ffn_cb3(ctypes.byref(good), ctypes.byref(cb3_ar), 1, fake, fake, fake, fake, fake, fake,
+                                16, None) == -4
     assert moe.moe_status_str(-4) == "workspace too small"
     assert moe.moe_kernel_launches() == launched      # every rejected call launched nothing
