@@ -26,6 +26,7 @@ int launch_combine(const moe_dims* m, int T, const float* rows, const int32_t* r
                    uint16_t* y, cudaStream_t st, int num_sms);
 bool tc_supported(const moe_dims* m);
 int64_t cb3_slot_bytes(int d, int f);
+bool cb3_ffn_supported(const moe_dims* m);
 int launch_pack_cb3(const moe_dims* m, const uint8_t* src_slot, uint8_t* dst_slot, int32_t* status, cudaStream_t st);
 int launch_cb3_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                    const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
@@ -281,6 +282,7 @@ int moe_expert_ffn_cb3(const moe_dims* dims, const moe_arena* cb3_arena, int32_t
                        const int32_t* topk_slot, const float* topk_w, uint16_t* y, int32_t* dev_status, void* ws,
                        size_t ws_bytes, void* stream) {
     if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (!cb3_ffn_supported(dims)) return MOE_ERR_DIMS;
     if (T < 0 || T > kDecodeMaxT) return MOE_ERR_TOKENS;
     int rc = check_arena(dims, cb3_arena, true);
     if (rc) return rc;

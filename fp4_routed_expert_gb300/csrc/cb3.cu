@@ -241,14 +241,35 @@ __global__ void __launch_bounds__(256) cb3_pack_kernel(const uint8_t* __restrict
 
 // ---------------------------------------------------------------------------- FFN
 
-// Row decoding.  The 8 levels of a row as byte tables for prmt: lo[0..1] hold the low bytes
-// of levels 0-3 and 4-7, hi[0..1] the high bytes.
+// Work split.  A warp owns a whole output (gate/up: one h element of one pair; down: 2 rows of
+// one pair's z) and adds its lanes' sums by a butterfly.  Gate/up: lane l owns the 32-element
+// groups l, l+32, ... of the row, in that order; the token is staged in shared memory as bf16
+// and bf16 levels multiply bf16 activations with fma.rn.f32.bf16 (exact products, fp32 sums).
+// Down: lane l owns the 8-element quarters l, l+32, ... (f/8 is a multiple of 32, so every
+// lane has the same count, and the quarter's position in its group is l % 4 for all of them);
+// h (fp32) is read from shared memory.  The order of every sum is fixed by the shapes alone,
+// so a token's results do not depend on the other tokens of the call.  z rows go to the
+// workspace and a last kernel forms y = sum_j w_j z_j in ascending j.
+
+constexpr int kCb3MaxGL = 8;       // gate/up: groups per lane (d <= 8192)
+constexpr int kCb3MaxQL = 9;       // down: quarters per lane (f <= 2304)
+constexpr int kCb3DnRows = 2;      // output rows per down item
+
+__host__ __device__ constexpr int cb3_padded(int n) { return n + n / 8; }
+
+// Levels of a row as byte tables for prmt: lo0/lo1 hold the low bytes of levels 0-3 / 4-7,
+// hi0/hi1 their high bytes.
 struct Cb3Levels {
     uint32_t lo0, lo1, hi0, hi1;
 };
 
-__device__ __forceinline__ Cb3Levels cb3_levels(const uint8_t* p) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+// The levels of row r of a batch whose 16-byte level records lanes 0.. hold (lane r has row r).
+__device__ __forceinline__ Cb3Levels cb3_levels_from(const uint4& mine, int r) {
+    uint4 v;
+    v.x = __shfl_sync(0xffffffffu, mine.x, r);
+    v.y = __shfl_sync(0xffffffffu, mine.y, r);
+    v.z = __shfl_sync(0xffffffffu, mine.z, r);
+    v.w = __shfl_sync(0xffffffffu, mine.w, r);
     Cb3Levels l;
     l.lo0 = __byte_perm(v.x, v.y, 0x6420);
     l.hi0 = __byte_perm(v.x, v.y, 0x7531);
@@ -259,21 +280,51 @@ __device__ __forceinline__ Cb3Levels cb3_levels(const uint8_t* p) {
 
 // Nibble selectors of quarter Q (elements 8Q..8Q+7) of a group from its A, B, Z words.
 template <int Q>
-__device__ __forceinline__ uint32_t cb3_nibbles(uint32_t A, uint32_t B, uint32_t Z) {
+__device__ __forceinline__ uint32_t cb3_nibbles(const uint32_t* g) {
+    const uint32_t A = g[0], B = g[1], Z = g[2];
     if (Q == 0) return (A & 0x33333333u) | (Z & 0x44444444u);
     if (Q == 1) return ((A >> 2) & 0x33333333u) | ((Z >> 1) & 0x44444444u);
     if (Q == 2) return (B & 0x33333333u) | ((Z << 2) & 0x44444444u);
     return ((B >> 2) & 0x33333333u) | ((Z << 1) & 0x44444444u);
 }
 
-// The 8 weights (fp32) selected by the 8 nibbles of N.
-__device__ __forceinline__ void cb3_weights8(const Cb3Levels& l, uint32_t N, float* w) {
+// The 8 weights selected by the 8 nibbles of N, as four bf16 pairs (elements 2i, 2i+1).
+__device__ __forceinline__ void cb3_pairs8(const Cb3Levels& l, uint32_t N, uint32_t* e) {
     const uint32_t la = __byte_perm(l.lo0, l.lo1, N), ha = __byte_perm(l.hi0, l.hi1, N);
     const uint32_t lb = __byte_perm(l.lo0, l.lo1, N >> 16), hb = __byte_perm(l.hi0, l.hi1, N >> 16);
-    const uint32_t e01 = __byte_perm(la, ha, 0x5140), e23 = __byte_perm(la, ha, 0x7362);
-    const uint32_t e45 = __byte_perm(lb, hb, 0x5140), e67 = __byte_perm(lb, hb, 0x7362);
-    w[0] = bf16_lo(e01); w[1] = bf16_hi(e01); w[2] = bf16_lo(e23); w[3] = bf16_hi(e23);
-    w[4] = bf16_lo(e45); w[5] = bf16_hi(e45); w[6] = bf16_lo(e67); w[7] = bf16_hi(e67);
+    e[0] = __byte_perm(la, ha, 0x5140);
+    e[1] = __byte_perm(la, ha, 0x7362);
+    e[2] = __byte_perm(lb, hb, 0x5140);
+    e[3] = __byte_perm(lb, hb, 0x7362);
+}
+
+// s + w.lo * x.lo, then + w.hi * x.hi: bf16 operands, exact products, fp32 accumulation.
+__device__ __forceinline__ float fma2_bf16(uint32_t w, uint32_t x, float s) {
+    asm("{ .reg .b16 wl, wh, xl, xh;\n"
+        "  mov.b32 {wl, wh}, %1;\n"
+        "  mov.b32 {xl, xh}, %2;\n"
+        "  fma.rn.f32.bf16 %0, wl, xl, %0;\n"
+        "  fma.rn.f32.bf16 %0, wh, xh, %0;\n}"
+        : "+f"(s)
+        : "r"(w), "r"(x));
+    return s;
+}
+
+template <int Q>
+__device__ __forceinline__ float cb3_quarter_bf16(const Cb3Levels& l, const uint32_t* g, const uint32_t* x, float s) {
+    uint32_t e[4];
+    cb3_pairs8(l, cb3_nibbles<Q>(g), e);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s = fma2_bf16(e[i], x[4 * Q + i], s);
+    return s;
+}
+
+// One group (index words g[3]) against 32 bf16 activations (16 pairs x[]), elements in order.
+__device__ __forceinline__ float cb3_dot_bf16(const Cb3Levels& l, const uint32_t* g, const uint32_t* x, float s) {
+    s = cb3_quarter_bf16<0>(l, g, x, s);
+    s = cb3_quarter_bf16<1>(l, g, x, s);
+    s = cb3_quarter_bf16<2>(l, g, x, s);
+    return cb3_quarter_bf16<3>(l, g, x, s);
 }
 
 __device__ __forceinline__ uint32_t ldg_nc_u32(const uint32_t* p) {
@@ -282,13 +333,9 @@ __device__ __forceinline__ uint32_t ldg_nc_u32(const uint32_t* p) {
     return v;
 }
 
-constexpr int kCb3XT = 8;   // tokens per pass of the gate/up kernel
-
-__host__ __device__ constexpr int cb3_padded(int n) { return n + n / 8; }
-
 struct Cb3Args {
     int T, d, f, k, num_slots;
-    int t0, tn;
+    int t;                      // token of the gate/up launch
     const uint16_t* x;
     const int32_t* slot;        // [T, k]
     const float* w;             // [T, k]
@@ -296,163 +343,158 @@ struct Cb3Args {
     int64_t slot_bytes;
     Cb3Layout C;
     float* h;                   // [T*k, f]
+    float* z;                   // [T*k, d]
     uint16_t* y;                // [T, d]
     int32_t* status;
 };
 
-// Dot of one 32-element group of a row with staged activations a (36-float stride per group:
-// 32 values then 4 pad), accumulated into acc[0..nq) for the nq tokens at a + tok_off[q].
-template <int XT>
-__device__ __forceinline__ void cb3_group_dot(const Cb3Levels& l, uint32_t A, uint32_t B, uint32_t Z, const float* a,
-                                              const int* tok_off, int nq, float* acc) {
-    float wv[8];
-#pragma unroll
-    for (int Q = 0; Q < 4; ++Q) {
-        const uint32_t N = Q == 0 ? cb3_nibbles<0>(A, B, Z) : Q == 1 ? cb3_nibbles<1>(A, B, Z)
-                         : Q == 2 ? cb3_nibbles<2>(A, B, Z) : cb3_nibbles<3>(A, B, Z);
-        cb3_weights8(l, N, wv);
-#pragma unroll
-        for (int q = 0; q < XT; ++q) {
-            if (q >= nq) break;
-            const float4* a4 = reinterpret_cast<const float4*>(a + tok_off[q] + 8 * Q);
-            const float4 p = a4[0], r = a4[1];
-            float s = acc[q];
-            s = fmaf(wv[0], p.x, s); s = fmaf(wv[1], p.y, s); s = fmaf(wv[2], p.z, s); s = fmaf(wv[3], p.w, s);
-            s = fmaf(wv[4], r.x, s); s = fmaf(wv[5], r.y, s); s = fmaf(wv[6], r.z, s); s = fmaf(wv[7], r.w, s);
-            acc[q] = s;
-        }
-    }
-}
-
-// Gate/up + SwiGLU.  Items are (unique slot u, output i); a warp reads gate row i and up row
-// i of slot u (lane owns groups lane, lane+32, ...) and reduces for every token of this pass
-// routed to u.  Shared memory: the pass's tokens as fp32 [tn][cb3_padded(d)].
-template <int XT>
-__global__ void __launch_bounds__(256) cb3_gateup_kernel(Cb3Args a) {
-    extern __shared__ float xs[];
-    __shared__ int uniq_slot[kCb3XT * kMaxTopK];
-    __shared__ int mem_cnt[kCb3XT * kMaxTopK];
-    __shared__ int mem_pair[kCb3XT * kMaxTopK][kCb3XT];
-    __shared__ int n_uniq;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d = a.d, f = a.f, k = a.k, tn = a.tn;
-    if (tid == 0) {
-        int nu = 0;
-        for (int q = 0; q < tn * k; ++q) {
-            const int p = a.t0 * k + q;
-            const int s = a.slot[p];
-            if (s < 0) continue;
-            if (s >= a.num_slots) { if (blockIdx.x == 0) atomicOr(a.status, MOE_STATUS_BAD_SLOT); continue; }
-            int u = 0;
-            while (u < nu && !(uniq_slot[u] == s && mem_cnt[u] < XT)) ++u;
-            if (u == nu) { uniq_slot[nu] = s; mem_cnt[nu] = 0; ++nu; }
-            mem_pair[u][mem_cnt[u]++] = p;
-        }
-        n_uniq = nu;
-    }
-    for (int t = 0; t < tn; ++t) {
-        const uint16_t* xt = a.x + (size_t)(a.t0 + t) * d;
-        for (int i = tid; i < d; i += blockDim.x) xs[(size_t)t * cb3_padded(d) + i + 4 * (i >> 5)] = bf16_to_f32(xt[i]);
-    }
+// Gate/up + SwiGLU for token a.t: items are (j, i) -- output i of the token's pair j; the warp
+// decodes gate row i and up row i of the pair's slot.  The token sits in shared memory as bf16,
+// 32-element groups 80 bytes apart (64 bytes + 16 of padding: conflict-free 16-byte reads
+// when consecutive lanes read consecutive groups).
+template <int GL>
+__global__ void __launch_bounds__(128) cb3_gateup_kernel(Cb3Args a) {
+    extern __shared__ uint4 xs4[];                        // [nc][5]: 4 data + 1 pad
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int d = a.d, f = a.f, k = a.k, nc = d / 32;
+    const uint4* xg = reinterpret_cast<const uint4*>(a.x + (size_t)a.t * d);
+    for (int v = tid; v < nc * 4; v += blockDim.x) xs4[(v >> 2) * 5 + (v & 3)] = __ldg(xg + v);
     __syncthreads();
-    const int nu = n_uniq, nc = d / 32;
-    const int gw = blockIdx.x * (blockDim.x >> 5) + warp, nw = gridDim.x * (blockDim.x >> 5);
-    for (int it = gw; it < nu * f; it += nw) {
-        const int u = it / f, i = it % f;
-        const uint8_t* base = a.arena + (int64_t)uniq_slot[u] * a.slot_bytes;
-        const Cb3Levels lg = cb3_levels(base + 16 * (int64_t)i), lu = cb3_levels(base + 16 * (int64_t)(f + i));
-        const uint32_t* ig = reinterpret_cast<const uint32_t*>(base + a.C.gate + (int64_t)i * (3 * d / 8));
-        const uint32_t* iu = reinterpret_cast<const uint32_t*>(base + a.C.up + (int64_t)i * (3 * d / 8));
-        const int nmem = mem_cnt[u];
-        int tok_off[XT];
+    const int gw = (blockIdx.x * blockDim.x + tid) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
+    for (int it = gw; it < k * f; it += nw) {
+        const int j = it / f, i = it % f, pair = a.t * k + j;
+        const int s = a.slot[pair];
+        if (s < 0 || s >= a.num_slots) {
+            if (s >= a.num_slots && i == 0 && lane == 0) atomicOr(a.status, MOE_STATUS_BAD_SLOT);
+            continue;
+        }
+        const uint8_t* base = a.arena + (int64_t)s * a.slot_bytes;
+        const uint4 lvmine = lane < 2 ? __ldg(reinterpret_cast<const uint4*>(base + 16 * (int64_t)(lane ? f + i : i)))
+                                      : make_uint4(0, 0, 0, 0);
+        const uint32_t* pg = reinterpret_cast<const uint32_t*>(base + a.C.gate + (int64_t)i * (3 * d / 8));
+        const uint32_t* pu = reinterpret_cast<const uint32_t*>(base + a.C.up + (int64_t)i * (3 * d / 8));
+        uint32_t wg[GL][3], wu[GL][3];
 #pragma unroll
-        for (int q = 0; q < XT; ++q) tok_off[q] = q < nmem ? (mem_pair[u][q] / k - a.t0) * cb3_padded(d) : 0;
-        float accg[XT], accu[XT];
+        for (int g = 0; g < GL; ++g) {
+            const int c = lane + 32 * g;
+            if (c < nc) {
 #pragma unroll
-        for (int q = 0; q < XT; ++q) accg[q] = accu[q] = 0.f;
-        for (int c0 = lane; c0 < nc; c0 += 32 * 4) {
-            uint32_t g3[4][3], u3[4][3];
+                for (int q = 0; q < 3; ++q) { wg[g][q] = ldg_nc_u32(pg + q * nc + c); wu[g][q] = ldg_nc_u32(pu + q * nc + c); }
+            }
+        }
+        const Cb3Levels lg = cb3_levels_from(lvmine, 0), lu = cb3_levels_from(lvmine, 1);
+        float accg = 0.f, accu = 0.f;
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int c = c0 + 32 * b;
-                if (c < nc) {
+        for (int g = 0; g < GL; ++g) {
+            const int c = lane + 32 * g;
+            if (c < nc) {
+                uint32_t xr[16];
 #pragma unroll
-                    for (int r = 0; r < 3; ++r) { g3[b][r] = ldg_nc_u32(ig + r * nc + c); u3[b][r] = ldg_nc_u32(iu + r * nc + c); }
+                for (int v = 0; v < 4; ++v) {
+                    const uint4 q = xs4[c * 5 + v];
+                    xr[4 * v] = q.x; xr[4 * v + 1] = q.y; xr[4 * v + 2] = q.z; xr[4 * v + 3] = q.w;
                 }
-            }
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int c = c0 + 32 * b;
-                if (c >= nc) break;
-                const float* xa = xs + 36 * c;
-                cb3_group_dot<XT>(lg, g3[b][0], g3[b][1], g3[b][2], xa, tok_off, nmem, accg);
-                cb3_group_dot<XT>(lu, u3[b][0], u3[b][1], u3[b][2], xa, tok_off, nmem, accu);
+                accg = cb3_dot_bf16(lg, wg[g], xr, accg);
+                accu = cb3_dot_bf16(lu, wu[g], xr, accu);
             }
         }
-#pragma unroll
-        for (int q = 0; q < XT; ++q) {
-            if (q >= nmem) break;
-            const float g = warp_sum(accg[q]), uu = warp_sum(accu[q]);
-            if (lane == 0) a.h[(size_t)mem_pair[u][q] * f + i] = g / (1.0f + expf(-g)) * uu;
-        }
+        const float gs = warp_sum(accg), us = warp_sum(accu);
+        if (lane == 0) a.h[(size_t)pair * f + i] = gs / (1.0f + expf(-gs)) * us;
     }
 }
 
-// Down + fixed-order combine.  Each warp owns 4 output rows (8 lanes per row; lane owns
-// groups l8, l8+8, ...); for each token the k pairs are visited in ascending j.  Shared
-// memory: the token's k vectors h [k][cb3_padded(f)].
+// Down: for each token the block stages the token's k vectors h [k][cb3_padded(f)]; items are
+// (j, 2 output rows) and write z rows of the pair.  Lane l owns quarters l + 32m (m < QL,
+// QL = f/256); its quarter position Q = l % 4 is the same in every group.
+template <int QL>
 __global__ void __launch_bounds__(256) cb3_down_kernel(Cb3Args a) {
     extern __shared__ float hs[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d = a.d, f = a.f, k = a.k;
-    const int l8 = lane & 7, grp = lane >> 3;
-    const int nc = f / 32;
-    const int r = blockIdx.x * ((blockDim.x >> 5) * 4) + warp * 4 + grp;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int d = a.d, f = a.f, k = a.k, nc = f / 32;
+    const int gw = (blockIdx.x * blockDim.x + tid) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
+    const int nb = d / kCb3DnRows;
+    const int Q = lane & 3;
+    const int wsel = (Q >> 1) * nc;                       // A (quarters 0, 1) or B (2, 3)
+    const uint32_t ash = 2u * (Q & 1), zrot = Q == 0 ? 0u : Q == 1 ? 31u : Q == 2 ? 2u : 1u;
     for (int t = 0; t < a.T; ++t) {
         __syncthreads();
-        for (int j = 0; j < k; ++j) {
-            const int pair = t * k + j;
+        // stage the token's h rows with asynchronous 16-byte copies (all in flight at once)
+        for (int e = tid; e < k * (f / 4); e += blockDim.x) {
+            const int j = e / (f / 4), i = (e % (f / 4)) * 4, pair = t * k + j;
             const int s = a.slot[pair];
-            const bool ok = s >= 0 && s < a.num_slots;
-            const float* hp = a.h + (size_t)pair * f;
-            for (int i = tid; i < f; i += blockDim.x) hs[(size_t)j * cb3_padded(f) + i + 4 * (i >> 5)] = ok ? __ldcg(hp + i) : 0.f;
+            float* dst = hs + (size_t)j * cb3_padded(f) + i + 4 * (i >> 5);
+            if (s >= 0 && s < a.num_slots) {
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(a.h + (size_t)pair * f + i)
+                             : "memory");
+            } else {
+                *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
         __syncthreads();
-        if (r >= d) continue;
-        float y = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const int pair = t * k + j;
+        for (int it = gw; it < k * nb; it += nw) {
+            const int j = it / nb, r0 = (it % nb) * kCb3DnRows, pair = t * k + j;
             const int s = a.slot[pair];
-            if (s < 0 || s >= a.num_slots) continue;      // the same pair for the whole warp
+            if (s < 0 || s >= a.num_slots) continue;
             const uint8_t* base = a.arena + (int64_t)s * a.slot_bytes;
-            const Cb3Levels l = cb3_levels(base + 16 * (int64_t)(2 * f + r));
-            const uint32_t* ix = reinterpret_cast<const uint32_t*>(base + a.C.down + (int64_t)r * (3 * f / 8));
-            const float* hj = hs + (size_t)j * cb3_padded(f);
-            const int tok0[1] = {0};
-            float acc = 0.f;
-            for (int c0 = l8; c0 < nc; c0 += 8 * 3) {
-                uint32_t w3[3][3];
+            const uint4 lvmine = lane < kCb3DnRows
+                ? __ldg(reinterpret_cast<const uint4*>(base + 16 * (int64_t)(2 * f + r0 + lane))) : make_uint4(0, 0, 0, 0);
+            uint32_t wab[kCb3DnRows][QL], wz[kCb3DnRows][QL];
 #pragma unroll
-                for (int b = 0; b < 3; ++b) {
-                    const int c = c0 + 8 * b;
-                    if (c < nc) {
+            for (int r = 0; r < kCb3DnRows; ++r) {
+                const uint32_t* p = reinterpret_cast<const uint32_t*>(base + a.C.down + (int64_t)(r0 + r) * (3 * f / 8));
 #pragma unroll
-                        for (int q = 0; q < 3; ++q) w3[b][q] = ldg_nc_u32(ix + q * nc + c);
-                    }
-                }
-#pragma unroll
-                for (int b = 0; b < 3; ++b) {
-                    const int c = c0 + 8 * b;
-                    if (c >= nc) break;
-                    cb3_group_dot<1>(l, w3[b][0], w3[b][1], w3[b][2], hj + 36 * c, tok0, 1, &acc);
+                for (int m = 0; m < QL; ++m) {
+                    const int c = (lane + 32 * m) >> 2;
+                    wab[r][m] = ldg_nc_u32(p + wsel + c);
+                    wz[r][m] = ldg_nc_u32(p + 2 * nc + c);
                 }
             }
-            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            y = fmaf(a.w[pair], acc, y);
+            const float* hj = hs + (size_t)j * cb3_padded(f) + 8 * Q;
+            Cb3Levels l[kCb3DnRows];
+            float acc[kCb3DnRows];
+#pragma unroll
+            for (int r = 0; r < kCb3DnRows; ++r) { l[r] = cb3_levels_from(lvmine, r); acc[r] = 0.f; }
+#pragma unroll
+            for (int m = 0; m < QL; ++m) {
+                const int c = (lane + 32 * m) >> 2;
+                const float4 p = reinterpret_cast<const float4*>(hj + 36 * c)[0];
+                const float4 q = reinterpret_cast<const float4*>(hj + 36 * c)[1];
+#pragma unroll
+                for (int r = 0; r < kCb3DnRows; ++r) {
+                    const uint32_t N =
+                        ((wab[r][m] >> ash) & 0x33333333u) | (__funnelshift_l(wz[r][m], wz[r][m], zrot) & 0x44444444u);
+                    uint32_t e[4];
+                    cb3_pairs8(l[r], N, e);
+                    float v = acc[r];
+                    v = fmaf(bf16_lo(e[0]), p.x, v); v = fmaf(bf16_hi(e[0]), p.y, v);
+                    v = fmaf(bf16_lo(e[1]), p.z, v); v = fmaf(bf16_hi(e[1]), p.w, v);
+                    v = fmaf(bf16_lo(e[2]), q.x, v); v = fmaf(bf16_hi(e[2]), q.y, v);
+                    v = fmaf(bf16_lo(e[3]), q.z, v); v = fmaf(bf16_hi(e[3]), q.w, v);
+                    acc[r] = v;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kCb3DnRows; ++r) {
+                const float v = warp_sum(acc[r]);
+                if (lane == 0) a.z[(size_t)pair * d + r0 + r] = v;
+            }
         }
-        if (l8 == 0) a.y[(size_t)t * d + r] = f32_to_bf16(y);
+    }
+}
+
+// y[t, r] = bf16(sum_j w_j z_j[r]) over the pairs with a valid slot, ascending j.
+__global__ void __launch_bounds__(256) cb3_combine_kernel(Cb3Args a) {
+    const int d = a.d, k = a.k;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < a.T * d; e += gridDim.x * blockDim.x) {
+        const int t = e / d, r = e % d;
+        float y = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const int s = a.slot[t * k + j];
+            if (s < 0 || s >= a.num_slots) continue;
+            y = fmaf(a.w[t * k + j], __ldcg(a.z + (size_t)(t * k + j) * d + r), y);
+        }
+        a.y[e] = f32_to_bf16(y);
     }
 }
 
@@ -466,13 +508,19 @@ int launch_pack_cb3(const moe_dims* m, const uint8_t* src_slot, uint8_t* dst_slo
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
-template <int XT>
-static int launch_cb3_gateup(const Cb3Args& a, size_t smem, int blocks, cudaStream_t st) {
+bool cb3_ffn_supported(const moe_dims* m) { return m->d <= 1024 * kCb3MaxGL && m->f <= 256 * kCb3MaxQL; }
+
+template <int GL>
+static void launch_gateup_gl(const Cb3Args& a, int blocks, cudaStream_t st) {
+    cb3_gateup_kernel<GL><<<blocks, 128, (size_t)(a.d / 32) * 80, st>>>(a);
+}
+
+template <int GL>
+static int launch_down_gl(const Cb3Args& a, size_t smem, int blocks, cudaStream_t st) {
     if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(cb3_gateup_kernel<XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        cudaFuncSetAttribute(cb3_down_kernel<GL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MOE_ERR_LAUNCH;
-    cb3_gateup_kernel<XT><<<blocks, 256, smem, st>>>(a);
-    note_launch(1);
+    cb3_down_kernel<GL><<<blocks, 256, smem, st>>>(a);
     return MOE_OK;
 }
 
@@ -487,24 +535,44 @@ int launch_cb3_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t
     a.slot_bytes = ar->slot_bytes;
     a.C = cb3_layout(m->d, m->f);
     a.h = reinterpret_cast<float*>(ws + L.h);
+    a.z = reinterpret_cast<float*>(ws + L.rows);
     a.y = y; a.status = status;
-    for (int t0 = 0; t0 < T; t0 += kCb3XT) {
-        a.t0 = t0;
-        a.tn = (T - t0 < kCb3XT) ? T - t0 : kCb3XT;
-        const size_t smem = (size_t)a.tn * cb3_padded(m->d) * 4;
-        const int blocks = 2 * num_sms;
-        int rc;
-        if (a.tn == 1) rc = launch_cb3_gateup<1>(a, smem, blocks, st);
-        else if (a.tn == 2) rc = launch_cb3_gateup<2>(a, smem, blocks, st);
-        else if (a.tn <= 4) rc = launch_cb3_gateup<4>(a, smem, blocks, st);
-        else rc = launch_cb3_gateup<8>(a, smem, blocks, st);
-        if (rc) return rc;
+    const int glu = (m->d / 32 + 31) / 32, qld = m->f / 256;
+    const int items = m->top_k * m->f;
+    const int gblocks = (items / 4 < 8 * num_sms) ? (items + 3) / 4 : 8 * num_sms;
+    for (int t = 0; t < T; ++t) {          // one launch per token: the T = 1 kernel, exactly
+        a.t = t;
+        switch (glu) {
+            case 1: launch_gateup_gl<1>(a, gblocks, st); break;
+            case 2: launch_gateup_gl<2>(a, gblocks, st); break;
+            case 3: launch_gateup_gl<3>(a, gblocks, st); break;
+            case 4: launch_gateup_gl<4>(a, gblocks, st); break;
+            case 5: launch_gateup_gl<5>(a, gblocks, st); break;
+            case 6: launch_gateup_gl<6>(a, gblocks, st); break;
+            case 7: launch_gateup_gl<7>(a, gblocks, st); break;
+            default: launch_gateup_gl<8>(a, gblocks, st); break;
+        }
+        note_launch(1);
     }
-    const size_t smem2 = (size_t)m->top_k * cb3_padded(m->f) * 4;
-    if (smem2 > 48 * 1024 &&
-        cudaFuncSetAttribute(cb3_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2) != cudaSuccess)
-        return MOE_ERR_LAUNCH;
-    cb3_down_kernel<<<(m->d + 31) / 32, 256, smem2, st>>>(a);
+    const size_t smem = (size_t)m->top_k * cb3_padded(m->f) * 4;
+    const int dn_items = m->top_k * (m->d / kCb3DnRows);
+    const int dblocks = (dn_items / 8 < 2 * num_sms) ? (dn_items + 7) / 8 : 2 * num_sms;
+    int rc;
+    switch (qld) {
+        case 1: rc = launch_down_gl<1>(a, smem, dblocks, st); break;
+        case 2: rc = launch_down_gl<2>(a, smem, dblocks, st); break;
+        case 3: rc = launch_down_gl<3>(a, smem, dblocks, st); break;
+        case 4: rc = launch_down_gl<4>(a, smem, dblocks, st); break;
+        case 5: rc = launch_down_gl<5>(a, smem, dblocks, st); break;
+        case 6: rc = launch_down_gl<6>(a, smem, dblocks, st); break;
+        case 7: rc = launch_down_gl<7>(a, smem, dblocks, st); break;
+        case 8: rc = launch_down_gl<8>(a, smem, dblocks, st); break;
+        case 9: rc = launch_down_gl<9>(a, smem, dblocks, st); break;
+        default: return MOE_ERR_DIMS;
+    }
+    if (rc) return rc;
+    note_launch(1);
+    cb3_combine_kernel<<<(T * m->d + 255) / 256 < 2 * num_sms ? (T * m->d + 255) / 256 : 2 * num_sms, 256, 0, st>>>(a);
     note_launch(1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }

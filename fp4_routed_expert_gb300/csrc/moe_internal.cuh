@@ -109,7 +109,7 @@ struct WsLayout {
     size_t counter;     // uint32 [64]       completion tickets (zeroed once, self-resetting)
     size_t active;      // prefill group plan (see plan_grec_off / plan_tile_group_off)
     size_t h;           // fp32 [T_max*k, f] SwiGLU output per (token, j) pair or permuted row
-    size_t rows;        // fp32 [T_max*k, d] per-row expert outputs (prefill with fused combine)
+    size_t rows;        // fp32 [T_max*k, d] per-row expert outputs (prefill with fused combine; cb3 z rows)
     size_t tc;          // tensor-core path: quantised activations, quantised h, per-row outputs
     size_t total;
 };
@@ -131,8 +131,7 @@ inline WsLayout ws_layout(const moe_dims* m, int T_max) {
     w.wnorm = o;   o = align256(o + 4 * E);
     w.active = o;  o = align256(o + 4 * ((size_t)plan_tile_group_off((int)E) + act_tiles(m, (int)T) + T * k));
     w.h = o;       o = align256(o + 4 * T * k * (size_t)m->f);
-    w.rows = o;
-    if (T_max > kDecodeMaxT) o = align256(o + 4 * T * k * (size_t)m->d);
+    w.rows = o;    o = align256(o + 4 * T * k * (size_t)m->d);
     w.tc = o;      o = align256(o + tc_workspace_bytes(m, (int)T));
     w.total = o;
     return w;
