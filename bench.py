@@ -13,7 +13,8 @@ than L2, so no L2 flush is inserted between steps.
 For N > 1 (torchrun, one process per GPU) every rank runs an independent replica of the
 layer (the path has no exchange step); value = all ranks' tokens / the slowest rank's time.
 --impl reference times the CPU oracle (plain C, one host core) on a bounded sample of the
-same workload.
+same workload.  Two more measurements ride on the same line (rank 0): "prefill" (one T=4096
+chunk) and "cb3" (the decode workload with the experts in the 3-bit codebook format).
 """
 from __future__ import annotations
 
@@ -385,6 +386,90 @@ def run_prefill(w, args, device):
                              else "fallback bf16 x 6"}}
 
 
+# ---------------------------------------------------------------------------- cb3 experts
+
+CB3_SLOT_BYTES = 13_426_688
+SM_COUNT, SM_MAX_MHZ, FP32_LANES_PER_SM = 152, 2070, 128
+
+
+def run_cb3(w, args, device):
+    """The same decode workload with the experts in the cb3 format (3-bit per-row codebook,
+    packed on the device from the FP4 arena): route + cb3 expert FFN per token, graph-replayed,
+    events around every 10th token's FFN.  Also the output's distance from the FP4 layer on
+    the same tokens (the approximation's cost).  Returns the object added to the JSON line."""
+    import torch
+    import fp4_routed_expert_gb300 as moe
+    from fp4_routed_expert_gb300.layer import Cb3Arena
+    dims = moe.moe_dims(D, F, E, K)
+    cb = Cb3Arena(dims, E, device)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    t0 = time.perf_counter()
+    for s_ in range(E):
+        cb.pack_from(w["arena"], s_, s_, st)
+    torch.cuda.synchronize()
+    pack_s = time.perf_counter() - t0
+    layer = w["layer"]
+    y = torch.empty_like(w["y"])
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        for i in range(4):
+            layer.route(w["x"][i:i + 1], w["wr"], w["tab"], None, T=1)
+            layer.experts_cb3(cb, w["x"][i:i + 1], T=1, y=y[i:i + 1])
+    torch.cuda.synchronize()
+    rt = CudaRt()
+    probes = []
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        h = torch.cuda.current_stream().cuda_stream
+        for i in range(TOKENS):
+            layer.route(w["x"][i:i + 1], w["wr"], w["tab"], None, T=1)
+            probe = rt.ok() and i % 10 == 5
+            if probe:
+                a, b = rt.event(), rt.event()
+                rt.record_external(a, h)
+            layer.experts_cb3(cb, w["x"][i:i + 1], T=1, y=y[i:i + 1])
+            if probe:
+                rt.record_external(b, h)
+                probes.append((a, b))
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    k_ms = [rt.elapsed_ms(a, b) for a, b in probes]
+    k_ms = statistics.mean([v for v in k_ms if v is not None]) if k_ms else None
+    # distance from the FP4 layer (w["y"] holds the FP4 path's outputs for the same tokens)
+    yc, yf = y.float(), w["y"].float()
+    rel = ((yc - yf).abs().amax(dim=1) / yf.abs().amax(dim=1).clamp_min(1e-30)).cpu().numpy()
+    peaks, kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    prods = 3 * K * D * F                                  # weight x activation products per token
+    peak_alu = SM_COUNT * FP32_LANES_PER_SM * SM_MAX_MHZ * 1e6 / 1e12
+    bytes_ = K * CB3_SLOT_BYTES + 2 * D * 2
+    out = {"workload": "decode T=1 as above, experts in the cb3 format (8 bf16 levels per row, 3-bit indices; "
+                       "%d B per expert, %.1f%% of FP4)" % (CB3_SLOT_BYTES, 100.0 * CB3_SLOT_BYTES / EXPERT_BYTES),
+           "value": round(TOKENS / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+           "pack_s": round(pack_s, 3), "experts_packed": E, "status": int(st.item()) | int(layer.status.item()),
+           "vs_fp4_row_rel_err": {"median": float(np.median(rel)), "max": float(rel.max())}}
+    if k_ms:
+        out["ffn_launch_ms"] = round(k_ms, 5)
+        out["roofline_alu"] = {"bound": "alu", "achieved": round(prods / (k_ms * 1e-3) / 1e12, 3), "peak": round(peak_alu, 2),
+                               "unit": "T weight-products/s", "frac": round(prods / (k_ms * 1e-3) / 1e12 / peak_alu, 4),
+                               "peak_source": "152 SMs x 128 FP32 lanes x 2070 MHz: one instruction per product"}
+        out["roofline_hbm"] = {"bound": "hbm", "achieved": round(bytes_ / (k_ms * 1e-3) / 1e9, 1), "peak": hbm,
+                               "unit": "GB/s", "frac": round(bytes_ / (k_ms * 1e-3) / 1e9 / hbm, 4), "bytes": bytes_}
+    del cb
+    return out
+
+
 # ---------------------------------------------------------------------------- oracle timing
 
 def oracle_sample(n_tokens, time_budget_s=None, x_bits=None, wr_bits=None, table=None):
@@ -456,6 +541,10 @@ def main():
                     help="experts resident in the arena (profiling runs use fewer; the metric is defined at 384)")
     ap.add_argument("--tokens", type=int, default=1000, help="tokens per step")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-chunk measurement")
+    ap.add_argument("--no-cb3", action="store_true", help="skip the cb3-format decode measurement")
+    ap.add_argument("--cb3-only", action="store_true",
+                    help="measure only the cb3-format decode leg (profiling runs; the FP4 layer runs once, eagerly, "
+                         "for the comparison)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="measure only the prefill chunk (profiling runs; with --experts the arena holds fewer experts)")
     args = ap.parse_args()
@@ -485,10 +574,24 @@ def main():
                    "prefill": run_prefill(build_workload(dev), args, dev)}
             print(json.dumps(out), flush=True)
         return 0
+    if args.cb3_only:
+        if rank == 0:
+            import torch
+            torch.cuda.set_device(local_rank)
+            dev = torch.device("cuda", local_rank)
+            w = build_workload(dev)
+            for i in range(TOKENS):
+                token_calls(w, i)
+            out = {"metric": "cb3 decode tokens/s", "impl": "ours", "config": dict(CONFIG), "cb3": run_cb3(w, args, dev)}
+            print(json.dumps(out), flush=True)
+        return 0
     out, w = run_ours(args, rank, world, local_rank)
     if rank == 0 and out is not None and not args.no_prefill and E == 384:
         import torch
         out["prefill"] = run_prefill(w, args, torch.device("cuda", local_rank))
+    if rank == 0 and out is not None and not args.no_cb3 and E == 384:
+        import torch
+        out["cb3"] = run_cb3(w, args, torch.device("cuda", local_rank))
     if rank == 0 and out is not None:
         if not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline_block()

@@ -201,9 +201,10 @@ int moe_combine(const moe_dims* dims, int32_t T, const float* rows, const int32_
  * call with slot_wave2 into the same rows (each row is written by one of the two calls); then
  * moe_combine.  The result equals the one-wave call (all experts resident, same routing) bit
  * for bit. */
-/* Cache-conditional routing (NEXT-4; the pages list it as an approved approximation after
- * "Mixture of Cache-Conditional Experts", arXiv 2412.00099; they give no formula, the reading
- * here is an additive bonus): instead of masking non-resident experts (expert_to_slot = -1),
+/* Cache-conditional routing ("DeepSeek-V4.1-Flash on a single NVIDIA DGX Spark", Conventions,
+ * and the expert-cache notes list it as an approved approximation, after "Mixture of
+ * Cache-Conditional Experts", arXiv 2412.00099; they give no formula, the reading here is an
+ * additive bonus): instead of masking non-resident experts (expert_to_slot = -1),
  * route with every expert's destination slot and this bias:
  *   bias_out[e] = score_bias[e] (0 if score_bias is NULL) + lambda   if slot expert_to_slot[e]
  *                 holds e now (resident_expert), else score_bias[e].
@@ -220,7 +221,7 @@ int moe_gather_experts(const moe_dims* dims, const moe_arena* arena, const void*
                        const int32_t* missing, const int32_t* n_missing, const int32_t* expert_to_slot,
                        int32_t* resident_expert, int32_t* dev_status, void* stream);
 
-/* cb3 expert format (NEXT-3; "DeepSeek-V4.1-Flash on a single NVIDIA DGX Spark", section "The
+/* cb3 expert format ("DeepSeek-V4.1-Flash on a single NVIDIA DGX Spark", section "The
  * numbers": resident experts in a 3-bit per-row codebook packed from the checkpoint's own FP4
  * experts).  An approximation of the model that trades accuracy for capacity: 13.4 MB per
  * expert instead of 18.8 MB at d=5120, f=2304.  Every matrix row (gate, up: K = d; down:

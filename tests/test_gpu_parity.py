@@ -380,7 +380,7 @@ def host_device_pointer(t):
 
 @pytest.mark.parametrize("T", [3, 40])
 def test_two_wave_moe_equals_one_wave(T):
-    """Partial residency (NEXT-2): with half the experts on hand, wave 1 computes their rows,
+    """Partial residency: with half the experts on hand, wave 1 computes their rows,
     one kernel gathers the missing experts from pinned host memory into their slots, wave 2
     computes the rest, and the fixed-order combine gives the one-wave result bit for bit."""
     d, f, E, k = 1024, 768, 16, 4
@@ -439,7 +439,7 @@ def test_two_wave_moe_equals_one_wave(T):
 
 @pytest.mark.parametrize("T", [3, 40])
 def test_cache_conditional_routing_two_waves(T):
-    """Cache-conditional routing (NEXT-4) on a partly resident arena: moe_residency_bias gives
+    """Cache-conditional routing on a partly resident arena: moe_residency_bias gives
     the oracle's bias bit for bit, the router never masks (every expert keeps its slot), it
     picks resident experts more often than exact routing yet still picks some missing ones, and
     the two-wave layer (wave 1, gather, wave 2, fixed-order combine) matches the oracle layer
