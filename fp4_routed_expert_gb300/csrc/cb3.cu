@@ -430,26 +430,38 @@ __global__ void __launch_bounds__(256) cb3_down_kernel(Cb3Args a) {
                 *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-        __syncthreads();
-        for (int it = gw; it < k * nb; it += nw) {
-            const int j = it / nb, r0 = (it % nb) * kCb3DnRows, pair = t * k + j;
-            const int s = a.slot[pair];
-            if (s < 0 || s >= a.num_slots) continue;
-            const uint8_t* base = a.arena + (int64_t)s * a.slot_bytes;
-            const uint4 lvmine = lane < kCb3DnRows
-                ? __ldg(reinterpret_cast<const uint4*>(base + 16 * (int64_t)(2 * f + r0 + lane))) : make_uint4(0, 0, 0, 0);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        // the first item's index words are requested before the wait for h, so the two
+        // latencies overlap; every thread passes the barrier once per token
+        bool staged = false;
+        for (int it = gw;; it += nw) {
+            const bool have = it < k * nb;
+            const int j = have ? it / nb : 0, r0 = have ? (it % nb) * kCb3DnRows : 0, pair = t * k + j;
+            const int s = have ? a.slot[pair] : -1;
+            const bool valid = s >= 0 && s < a.num_slots;
+            const uint8_t* base = a.arena + (int64_t)(valid ? s : 0) * a.slot_bytes;
+            uint4 lvmine = make_uint4(0, 0, 0, 0);
             uint32_t wab[kCb3DnRows][QL], wz[kCb3DnRows][QL];
+            if (valid) {
+                if (lane < kCb3DnRows) lvmine = __ldg(reinterpret_cast<const uint4*>(base + 16 * (int64_t)(2 * f + r0 + lane)));
 #pragma unroll
-            for (int r = 0; r < kCb3DnRows; ++r) {
-                const uint32_t* p = reinterpret_cast<const uint32_t*>(base + a.C.down + (int64_t)(r0 + r) * (3 * f / 8));
+                for (int r = 0; r < kCb3DnRows; ++r) {
+                    const uint32_t* p = reinterpret_cast<const uint32_t*>(base + a.C.down + (int64_t)(r0 + r) * (3 * f / 8));
 #pragma unroll
-                for (int m = 0; m < QL; ++m) {
-                    const int c = (lane + 32 * m) >> 2;
-                    wab[r][m] = ldg_nc_u32(p + wsel + c);
-                    wz[r][m] = ldg_nc_u32(p + 2 * nc + c);
+                    for (int m = 0; m < QL; ++m) {
+                        const int c = (lane + 32 * m) >> 2;
+                        wab[r][m] = ldg_nc_u32(p + wsel + c);
+                        wz[r][m] = ldg_nc_u32(p + 2 * nc + c);
+                    }
                 }
             }
+            if (!staged) {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+                __syncthreads();
+                staged = true;
+            }
+            if (!have) break;
+            if (!valid) continue;
             const float* hj = hs + (size_t)j * cb3_padded(f) + 8 * Q;
             Cb3Levels l[kCb3DnRows];
             float acc[kCb3DnRows];
