@@ -332,9 +332,11 @@ PREFILL_T = 4096
 PREFILL_BIAS = (1.2, 0.04)   # Zipf s, beta of the per-expert score bias
 
 
-def run_prefill(w, args, device):
+def run_prefill(w, args, device, resident=None):
     """One prefill chunk at the pages' shape: T=4096 tokens of N(0,1) bf16, Zipf(1.2)-skewed
     score bias, every expert resident; route -> permute -> expert FFN -> combine, graph-replayed.
+    resident = n keeps only the first n experts routable (the rest masked): the diagnostic
+    compute-bound case (n = 12: about 2,048 tokens per expert, above the ridge point).
     Returns the measurement object added to the JSON line."""
     import torch
     from fp4_routed_expert_gb300.layer import MoeLayer
@@ -345,14 +347,19 @@ def run_prefill(w, args, device):
     x = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).to(device).view(torch.bfloat16)
     layer = MoeLayer(D, F, E, K, T, w["arena"], device)
     y = torch.empty((T, D), dtype=torch.bfloat16, device=device)
+    tab = w["tab"]
+    if resident is not None:
+        keep = np.full(E, -1, np.int32)
+        keep[:resident] = w["table"][:resident]
+        tab = torch.from_numpy(keep).to(device)
     stream = torch.cuda.Stream(device)
     with torch.cuda.stream(stream):
-        layer.route(x, w["wr"], w["tab"], bias)
+        layer.route(x, w["wr"], tab, bias)
         layer.experts(x, fused_prefill=True, y=y)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        layer.route(x, w["wr"], w["tab"], bias)
+        layer.route(x, w["wr"], tab, bias)
         layer.experts(x, fused_prefill=True, y=y)
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -374,8 +381,11 @@ def run_prefill(w, args, device):
     fp4 = float(peaks["bf16_tflops"]) * (13.5 / 2.25)   # FP4 dense peak = measured bf16 x nominal ratio
     bytes_ = used * EXPERT_BYTES + ROUTER_BYTES + 2 * T * D * 2
     flops = 6.0 * T * K * D * F                          # gate, up, down: 2 flops per multiply-add
-    return {"workload": "prefill chunk T=%d, d=%d f=%d E=%d top-k=%d, Zipf(s=%.1f, beta=%.2f) score bias, all experts "
-                        "resident; route + permute + expert FFN + combine" % (T, D, F, E, K, *PREFILL_BIAS),
+    what = ("all experts resident" if resident is None else
+            "DIAGNOSTIC (not a workload of the pages): only experts 0..%d routable, ~%d tokens per expert"
+            % (resident - 1, T * K // resident))
+    return {"workload": "prefill chunk T=%d, d=%d f=%d E=%d top-k=%d, Zipf(s=%.1f, beta=%.2f) score bias, %s; "
+                        "route + permute + expert FFN + combine" % (T, D, F, E, K, *PREFILL_BIAS, what),
             "value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_chunk": round(ms, 4),
             "experts_used": used, "status": int(layer.status.item()),
             "roofline_hbm": {"bound": "hbm", "achieved": round(bytes_ / (ms * 1e-3) / 1e9, 1), "peak": hbm,
@@ -611,6 +621,7 @@ def main():
     if rank == 0 and out is not None and not args.no_prefill and E == 384:
         import torch
         out["prefill"] = run_prefill(w, args, torch.device("cuda", local_rank))
+        out["prefill_diagnostic_12_experts"] = run_prefill(w, args, torch.device("cuda", local_rank), resident=12)
     if rank == 0 and out is not None and not args.no_cb3 and E == 384:
         import torch
         out["cb3"] = run_cb3(w, args, torch.device("cuda", local_rank))
