@@ -247,15 +247,14 @@ __global__ void __launch_bounds__(256) cb3_pack_kernel(const uint8_t* __restrict
 // and bf16 levels multiply bf16 activations with fma.rn.f32.bf16 (exact products, fp32 sums).
 // Down: lane l owns the 8-element quarters l, l+32, ... (f/8 is a multiple of 32, so every
 // lane has the same count, and the quarter's position in its group is l % 4 for all of them);
-// h (fp32) is read from shared memory.  The order of every sum is fixed by the shapes alone,
+// h is rounded once to bf16 when the gate/up kernel writes it, staged in shared memory, and
+// multiplied the same way.  The order of every sum is fixed by the shapes alone,
 // so a token's results do not depend on the other tokens of the call.  z rows go to the
 // workspace and a last kernel forms y = sum_j w_j z_j in ascending j.
 
 constexpr int kCb3MaxGL = 8;       // gate/up: groups per lane (d <= 8192)
 constexpr int kCb3MaxQL = 9;       // down: quarters per lane (f <= 2304)
 constexpr int kCb3DnRows = 2;      // output rows per down item
-
-__host__ __device__ constexpr int cb3_padded(int n) { return n + n / 8; }
 
 // Levels of a row as byte tables for prmt: lo0/lo1 hold the low bytes of levels 0-3 / 4-7,
 // hi0/hi1 their high bytes.
@@ -342,7 +341,7 @@ struct Cb3Args {
     const uint8_t* arena;
     int64_t slot_bytes;
     Cb3Layout C;
-    float* h;                   // [T*k, f]
+    uint16_t* h;                // [T*k, f] bf16
     float* z;                   // [T*k, d]
     uint16_t* y;                // [T, d]
     int32_t* status;
@@ -399,16 +398,16 @@ __global__ void __launch_bounds__(128) cb3_gateup_kernel(Cb3Args a) {
             }
         }
         const float gs = warp_sum(accg), us = warp_sum(accu);
-        if (lane == 0) a.h[(size_t)pair * f + i] = gs / (1.0f + expf(-gs)) * us;
+        if (lane == 0) a.h[(size_t)pair * f + i] = f32_to_bf16(gs / (1.0f + expf(-gs)) * us);
     }
 }
 
-// Down: for each token the block stages the token's k vectors h [k][cb3_padded(f)]; items are
+// Down: for each token the block stages the token's k vectors h [k][f] (bf16); items are
 // (j, 2 output rows) and write z rows of the pair.  Lane l owns quarters l + 32m (m < QL,
 // QL = f/256); its quarter position Q = l % 4 is the same in every group.
 template <int QL>
 __global__ void __launch_bounds__(256) cb3_down_kernel(Cb3Args a) {
-    extern __shared__ float hs[];
+    extern __shared__ uint4 hs4[];                        // [k][f/8]: 8 bf16 per entry
     const int tid = threadIdx.x, lane = tid & 31;
     const int d = a.d, f = a.f, k = a.k, nc = f / 32;
     const int gw = (blockIdx.x * blockDim.x + tid) >> 5, nw = (gridDim.x * blockDim.x) >> 5;
@@ -419,15 +418,15 @@ __global__ void __launch_bounds__(256) cb3_down_kernel(Cb3Args a) {
     for (int t = 0; t < a.T; ++t) {
         __syncthreads();
         // stage the token's h rows with asynchronous 16-byte copies (all in flight at once)
-        for (int e = tid; e < k * (f / 4); e += blockDim.x) {
-            const int j = e / (f / 4), i = (e % (f / 4)) * 4, pair = t * k + j;
+        for (int e = tid; e < k * (f / 8); e += blockDim.x) {
+            const int j = e / (f / 8), i = (e % (f / 8)) * 8, pair = t * k + j;
             const int s = a.slot[pair];
-            float* dst = hs + (size_t)j * cb3_padded(f) + i + 4 * (i >> 5);
+            uint4* dst = hs4 + e;
             if (s >= 0 && s < a.num_slots) {
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(a.h + (size_t)pair * f + i)
                              : "memory");
             } else {
-                *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *dst = make_uint4(0, 0, 0, 0);
             }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
@@ -462,7 +461,9 @@ __global__ void __launch_bounds__(256) cb3_down_kernel(Cb3Args a) {
             }
             if (!have) break;
             if (!valid) continue;
-            const float* hj = hs + (size_t)j * cb3_padded(f) + 8 * Q;
+            // quarter (c, Q) of h_j: 16 bytes at entry 4c + Q; 8 consecutive lanes read 128
+            // consecutive bytes (no bank conflict)
+            const uint4* hj = hs4 + (size_t)j * (f / 8) + Q;
             Cb3Levels l[kCb3DnRows];
             float acc[kCb3DnRows];
 #pragma unroll
@@ -470,8 +471,7 @@ __global__ void __launch_bounds__(256) cb3_down_kernel(Cb3Args a) {
 #pragma unroll
             for (int m = 0; m < QL; ++m) {
                 const int c = (lane + 32 * m) >> 2;
-                const float4 p = reinterpret_cast<const float4*>(hj + 36 * c)[0];
-                const float4 q = reinterpret_cast<const float4*>(hj + 36 * c)[1];
+                const uint4 hq = hj[4 * c];
 #pragma unroll
                 for (int r = 0; r < kCb3DnRows; ++r) {
                     const uint32_t N =
@@ -479,10 +479,10 @@ __global__ void __launch_bounds__(256) cb3_down_kernel(Cb3Args a) {
                     uint32_t e[4];
                     cb3_pairs8(l[r], N, e);
                     float v = acc[r];
-                    v = fmaf(bf16_lo(e[0]), p.x, v); v = fmaf(bf16_hi(e[0]), p.y, v);
-                    v = fmaf(bf16_lo(e[1]), p.z, v); v = fmaf(bf16_hi(e[1]), p.w, v);
-                    v = fmaf(bf16_lo(e[2]), q.x, v); v = fmaf(bf16_hi(e[2]), q.y, v);
-                    v = fmaf(bf16_lo(e[3]), q.z, v); v = fmaf(bf16_hi(e[3]), q.w, v);
+                    v = fma2_bf16(e[0], hq.x, v);
+                    v = fma2_bf16(e[1], hq.y, v);
+                    v = fma2_bf16(e[2], hq.z, v);
+                    v = fma2_bf16(e[3], hq.w, v);
                     acc[r] = v;
                 }
             }
@@ -546,7 +546,7 @@ int launch_cb3_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t
     a.arena = reinterpret_cast<const uint8_t*>(ar->base);
     a.slot_bytes = ar->slot_bytes;
     a.C = cb3_layout(m->d, m->f);
-    a.h = reinterpret_cast<float*>(ws + L.h);
+    a.h = reinterpret_cast<uint16_t*>(ws + L.h);
     a.z = reinterpret_cast<float*>(ws + L.rows);
     a.y = y; a.status = status;
     const int glu = (m->d / 32 + 31) / 32, qld = m->f / 256;
@@ -566,7 +566,7 @@ int launch_cb3_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t
         }
         note_launch(1);
     }
-    const size_t smem = (size_t)m->top_k * cb3_padded(m->f) * 4;
+    const size_t smem = (size_t)m->top_k * m->f * 2;
     const int dn_items = m->top_k * (m->d / kCb3DnRows);
     const int dblocks = (dn_items / 8 < 2 * num_sms) ? (dn_items + 7) / 8 : 2 * num_sms;
     int rc;
