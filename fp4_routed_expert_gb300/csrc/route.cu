@@ -655,7 +655,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) route_decode_kernel(RouteAr
                 a.keys[(size_t)lane * E + e] = make_key(tb, bias_e, __fadd_rn(myS, myC), lo, hi);
             }
         }
-        __syncthreads();   // the next round's copies overwrite the router rows
+        __syncthreads();   // the next iteration's copies overwrite the router rows
     }
 }
 
