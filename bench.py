@@ -502,10 +502,10 @@ def oracle_sample(n_tokens, time_budget_s=None, x_bits=None, wr_bits=None, table
     done = 0
     for t in range(n_tokens):
         rr = oracle.route_topk(x_bits[t:t + 1], wr_bits, None, table, K)
-        z = np.zeros((K, D))
+        z = np.zeros((K, D), np.float32)
         for j in range(K):
-            _, z[j] = oracle.expert_ffn(x_bits[t], cache[int(rr["slots"][0, j])])
-        oracle.combine(z, rr["weights"][0])
+            _, z[j] = oracle.expert_ffn_f32(x_bits[t], cache[int(rr["slots"][0, j])])
+        oracle.combine_f32(z, rr["weights"][0])
         done += 1
         if time_budget_s and time.perf_counter() - t0 > time_budget_s:
             break

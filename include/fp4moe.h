@@ -112,7 +112,10 @@ int moe_pack_expert(const moe_dims* dims, const uint8_t* gate_q, const uint8_t* 
                     const uint8_t* up_q, const uint8_t* up_s, const uint8_t* down_q,
                     const uint8_t* down_s, const moe_arena* arena, int32_t slot, void* stream);
 
-/* a1-a3: router scoring, top-k selection and slot lookup for T tokens.
+/* a1-a3: router scoring, top-k selection and slot lookup for T tokens ("Start the expert
+ * reads before the GPU is done", 28 September follow-up: each layer's router runs on the GPU
+ * and its chosen expert ids -- read back through the router mailbox there -- decide which
+ * experts are read and computed; here they stay on the device as topk_slot).
  *   x              bf16 [T, d]
  *   w_router       bf16 [E, d]
  *   score_bias     fp32 [E] added to the score for selection only, or NULL
@@ -138,7 +141,9 @@ int moe_route_topk(const moe_dims* dims, int32_t T, const uint16_t* x, const uin
  * is a static device array inside this library, held by every GPU that loads the library
  * until the process exits.  It allocates nothing and calls no allocating routine.
  * The first call on each device looks up the array's device address with that device
- * current; make that first call before any stream capture.  Every call overwrites the
+ * current; make that first call before any stream capture.  That address is kept for the life
+ * of the process, so this entry point must not be called on a device after cudaDeviceReset
+ * there (the reset unloads the library's device code and its array with it).  Every call overwrites the
  * array: calls whose execution overlaps on the GPU -- on different streams, or from
  * different threads -- race on the shared array and must be serialised by the caller. */
 int moe_route_topk_noalloc(const moe_dims* dims, int32_t T, const uint16_t* x, const uint16_t* w_router,
@@ -146,9 +151,13 @@ int moe_route_topk_noalloc(const moe_dims* dims, int32_t T, const uint16_t* x, c
                            float* topk_w, int32_t* topk_slot, int32_t* dev_status, void* stream);
 
 /* a4: stable grouping of the T*k (token, j) rows by expert id (tokens ascending inside a
- * group).  group_offsets int32 [E+1] (group e = rows [off[e], off[e+1]), off[E] = rows
- * with a valid id), row_src int32 [T*k] (row r came from t*k + j; entries >= off[E] are
- * -1), row_dst int32 [T*k] (the inverse; -1 for id -1). */
+ * group), so that every (token, slot) row has one place and is written once ("Start the
+ * expert reads before the GPU is done", 30 September follow-up).
+ *   group_offsets int32 [E+1]: group e = rows [off[e], off[e+1]); off[E] = rows with a valid id
+ *   row_src int32 [T*k]: row r came from pair t*k + j; entries >= off[E] are -1
+ *   row_dst int32 [T*k]: the inverse; -1 for id -1
+ * The activations are not gathered here: the expert call reads x through row_src and encodes
+ * its own tensor-core operand (so this call takes no x and writes no A operand). */
 int moe_permute(const moe_dims* dims, int32_t T, const int32_t* topk_ids, int32_t* group_offsets,
                 int32_t* row_src, int32_t* row_dst, void* ws, size_t ws_bytes, void* stream);
 
@@ -176,10 +185,11 @@ int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, 
 int moe_combine(const moe_dims* dims, int32_t T, const float* rows, const int32_t* row_dst,
                 const float* topk_w, uint16_t* y, void* stream);
 
-/* Partial residency (the two-wave routed MoE; "DeepSeek-V4.1-Flash on a single NVIDIA DGX
- * Spark", 30 September follow-up: compute the experts on hand before the top-up read and the
+/* Partial residency (the two-wave routed MoE; "Start the expert reads before the GPU is
+ * done", 30 September follow-up: compute the experts on hand before the top-up read and the
  * rest after it, bit-exact because every (token, slot) row is written once and the slot sum is
- * a separate fixed-order kernel; 28 September follow-up: a GPU-driven expert gather).
+ * a separate fixed-order kernel; same page, 28 September follow-up: a GPU-driven expert gather
+ * that removes the per-layer command buffers, proposed there as the next step).
  *
  * The routing is made with the table of destination slots (expert_to_slot: where each expert
  * lives when resident; missing experts must have distinct slots).  resident_expert int32

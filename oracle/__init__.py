@@ -14,7 +14,11 @@ Parity status per function (what pins it is in tests/test_oracle_pins.py):
   cb3_pack_row / cb3_expert_ffn  pinned (exhaustive partitions in exact rationals, lossless
                                  rows, FP4 FFN on lossless experts)
   permute                        pinned (brute force and invariants)
-  expert_ffn / combine / layer   pinned (closed forms, independent fp64 re-derivation)
+  expert_ffn_f32 / combine_f32   pinned (fp32 closed forms with exact sums, an independent
+    / layer (fp32, the reference)  numpy float32 sequential re-derivation, agreement with the
+                                 fp64 statement within the fp32 summation bound)
+  expert_ffn / combine (fp64)    pinned (closed forms, independent fp64 re-derivation); kept as
+                                 a cross-check of the fp32 statement
   residual_rmsnorm               pinned (independent fp64 re-derivation)
 """
 from __future__ import annotations
@@ -68,6 +72,14 @@ def lib():
         L.oracle_expert_ffn.argtypes = [i32, i32, P, P, P, P, P, P, P, P, P]
         L.oracle_combine.restype = None
         L.oracle_combine.argtypes = [i32, i32, P, P, P]
+        L.oracle_expert_ffn_f32.restype = None
+        L.oracle_expert_ffn_f32.argtypes = [i32, i32, P, P, P, P, P, P, P, P, P]
+        L.oracle_combine_f32.restype = None
+        L.oracle_combine_f32.argtypes = [i32, i32, P, P, P]
+        L.oracle_weight_at_f32.restype = ctypes.c_float
+        L.oracle_weight_at_f32.argtypes = [P, P, i32]
+        L.oracle_moe_layer_f32.restype = i32
+        L.oracle_moe_layer_f32.argtypes = [i32] * 6 + [P] * 15
         L.oracle_moe_layer.restype = i32
         L.oracle_moe_layer.argtypes = [i32] * 6 + [P] * 15
         L.oracle_residual_rmsnorm.restype = None
@@ -156,8 +168,39 @@ def permute(ids, E):
     return dict(offsets=offsets, row_src=row_src[:n].copy(), row_dst=row_dst, rows=int(n))
 
 
+def expert_ffn_f32(x_bits, ex: dict):
+    """One expert on one token in fp32, every sum in index order (the reference statement);
+    returns (h [f], z [d]) as float32."""
+    x = _c(x_bits, np.uint16)
+    d = x.size
+    gq = _c(ex["gate_q"], np.uint8)
+    f = gq.shape[0]
+    arrs = [gq] + [_c(ex[n], np.uint8) for n in ("gate_s", "up_q", "up_s", "down_q", "down_s")]
+    h = np.zeros(f, np.float32)
+    z = np.zeros(d, np.float32)
+    lib().oracle_expert_ffn_f32(d, f, _p(x), *[_p(a) for a in arrs], _p(h), _p(z))
+    return h, z
+
+
+def combine_f32(z, w):
+    """y = sum_j w_j z_j in fp32, j ascending."""
+    z = _c(z, np.float32)
+    w = _c(w, np.float32)
+    k, d = z.shape
+    y = np.zeros(d, np.float32)
+    lib().oracle_combine_f32(d, k, _p(z), _p(w), _p(y))
+    return y
+
+
+def weight_at_f32(q_row, s_row, k: int) -> np.float32:
+    q = _c(q_row, np.uint8)
+    sc = _c(s_row, np.uint8)
+    return np.float32(lib().oracle_weight_at_f32(_p(q), _p(sc), int(k)))
+
+
 def expert_ffn(x_bits, ex: dict):
-    """One expert (canonical tensors dict) on one token; returns (h [f], z [d]) in fp64."""
+    """One expert (canonical tensors dict) on one token; returns (h [f], z [d]) in fp64
+    (the cross-check statement; expert_ffn_f32 is the reference)."""
     x = _c(x_bits, np.uint16)
     d = x.size
     gq = _c(ex["gate_q"], np.uint8)
@@ -218,8 +261,10 @@ def combine(z, w):
     return y
 
 
-def moe_layer(x_bits, w_router_bits, bias, expert_to_slot, k, slot_tensors: dict):
-    """Whole layer with every slot's canonical tensors stacked as [num_slots, ...]."""
+def moe_layer(x_bits, w_router_bits, bias, expert_to_slot, k, slot_tensors: dict, precision: str = "f32"):
+    """Whole layer with every slot's canonical tensors stacked as [num_slots, ...].
+    precision "f32" (the reference statement) or "f64" (the cross-check); y is returned as
+    float64 either way (exact conversion of the fp32 result)."""
     x = _c(x_bits, np.uint16)
     wr = _c(w_router_bits, np.uint16)
     T, d = x.shape
@@ -232,10 +277,18 @@ def moe_layer(x_bits, w_router_bits, bias, expert_to_slot, k, slot_tensors: dict
     ids = np.zeros((T, k), np.int32)
     w = np.zeros((T, k), np.float32)
     slots = np.zeros((T, k), np.int32)
-    y = np.zeros((T, d), np.float64)
     yb = np.zeros((T, d), np.uint16)
-    st = lib().oracle_moe_layer(T, d, f, E, k, S, _p(x), _p(wr), _p(b), _p(tab),
-                                *[_p(a) for a in arrs], _p(ids), _p(w), _p(slots), _p(y), _p(yb))
+    if precision == "f32":
+        y = np.zeros((T, d), np.float32)
+        st = lib().oracle_moe_layer_f32(T, d, f, E, k, S, _p(x), _p(wr), _p(b), _p(tab),
+                                        *[_p(a) for a in arrs], _p(ids), _p(w), _p(slots), _p(y), _p(yb))
+        y = y.astype(np.float64)
+    elif precision == "f64":
+        y = np.zeros((T, d), np.float64)
+        st = lib().oracle_moe_layer(T, d, f, E, k, S, _p(x), _p(wr), _p(b), _p(tab),
+                                    *[_p(a) for a in arrs], _p(ids), _p(w), _p(slots), _p(y), _p(yb))
+    else:
+        raise ValueError("precision must be 'f32' or 'f64'")
     return dict(ids=ids, weights=w, slots=slots, y=y, y_bf16=yb, status=int(st))
 
 

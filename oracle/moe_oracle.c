@@ -25,7 +25,11 @@
  *  - the router logit is the exact dot product rounded once to fp32 (order independent);
  *    s = fp32(1 / (1 + exp(-logit))) evaluated in double.
  *  - expert FFN = SwiGLU: h = silu(W_gate x) * (W_up x), z = W_down h; y = sum_j w_j z_j.
- *    All FFN arithmetic here is fp64 (every product is exact in fp64).
+ *    The reference statement is fp32 (the checkpoint is served with fp32 matmuls): every
+ *    weight w = code * 2^(b-127) and every product float(x) * w is exact in fp32, and each
+ *    sum is one plain fp32 accumulation in index order (oracle_expert_ffn_f32,
+ *    oracle_combine_f32).  An fp64 statement of the same steps (oracle_expert_ffn,
+ *    oracle_combine) is kept beside it as a cross-check.
  *  - code 2i of a row is the low nibble of byte i; scale byte b means 2^(b-127);
  *    b = 255 is not a number.
  */
@@ -316,6 +320,70 @@ void oracle_expert_ffn(int d, int f, const uint16_t* x, const uint8_t* gate_q,
     if (!h_out) free(h);
 }
 
+/* ---- the same FFN in fp32, the reference statement -------------------------------- */
+
+/* Weight k of a packed row as fp32: code * 2^(b-127), exact (b = 0 gives a subnormal). */
+float oracle_weight_at_f32(const uint8_t* qrow, const uint8_t* srow, int k) {
+    return (float)oracle_e2m1_value(oracle_code_at(qrow, k)) * ldexpf(1.0f, (int)srow[k / 32] - 127);
+}
+
+/* bfloat16 bit pattern -> fp32 (exact). */
+static float bf16_f32(uint16_t bits) { return (float)oracle_bf16_value(bits); }
+
+/* One expert on one token, every step in fp32 and in index order:
+ *   g_i = sum_{k=0..d-1} x_k * Wg[i,k]   u_i likewise       (products exact, sums rounded)
+ *   h_i = (g_i / (1 + expf(-g_i))) * u_i                     (libm expf)
+ *   z_r = sum_{i=0..f-1} Wd[r,i] * h_i                       (products and sums rounded)
+ * Built with -ffp-contract=off, so no multiply-add is fused. */
+void oracle_expert_ffn_f32(int d, int f, const uint16_t* x, const uint8_t* gate_q,
+                           const uint8_t* gate_s, const uint8_t* up_q, const uint8_t* up_s,
+                           const uint8_t* down_q, const uint8_t* down_s, float* h_out,
+                           float* z_out) {
+    float* h = h_out ? h_out : (float*)malloc(sizeof(float) * (size_t)f);
+    float* xf = (float*)malloc(sizeof(float) * (size_t)d);
+    for (int k = 0; k < d; ++k) xf[k] = bf16_f32(x[k]);
+    for (int i = 0; i < f; ++i) {
+        const uint8_t* gq = gate_q + (size_t)i * (d / 2);
+        const uint8_t* gs = gate_s + (size_t)i * (d / 32);
+        const uint8_t* uq = up_q + (size_t)i * (d / 2);
+        const uint8_t* us = up_s + (size_t)i * (d / 32);
+        float g = 0.0f, u = 0.0f;
+        for (int k = 0; k < d; ++k) {
+            float pg = xf[k] * oracle_weight_at_f32(gq, gs, k);
+            float pu = xf[k] * oracle_weight_at_f32(uq, us, k);
+            g = g + pg;
+            u = u + pu;
+        }
+        float den = 1.0f + expf(-g);
+        float sg = g / den;
+        h[i] = sg * u;
+    }
+    for (int r = 0; r < d; ++r) {
+        const uint8_t* dq = down_q + (size_t)r * (f / 2);
+        const uint8_t* ds = down_s + (size_t)r * (f / 32);
+        float z = 0.0f;
+        for (int i = 0; i < f; ++i) {
+            float p = oracle_weight_at_f32(dq, ds, i) * h[i];
+            z = z + p;
+        }
+        z_out[r] = z;
+    }
+    free(xf);
+    if (!h_out) free(h);
+}
+
+/* y_r = sum_{j=0..k-1} w_j * z_j[r] in fp32, j ascending (= ascending expert id). */
+void oracle_combine_f32(int d, int k, const float* z, const float* w, float* y) {
+    for (int r = 0; r < d; ++r) {
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            float p = w[j] * z[(size_t)j * d + r];
+            acc = acc + p;
+        }
+        y[r] = acc;
+    }
+}
+
 /* ---- cb3: a 3-bit per-row codebook packed from the FP4 experts --------------------- */
 
 /* "DeepSeek-V4.1-Flash on a single NVIDIA DGX Spark", section "The numbers": the resident
@@ -491,6 +559,38 @@ int oracle_moe_layer(int T, int d, int f, int E, int k, int num_slots, const uin
         oracle_combine(d, k, z, weights + (size_t)t * k, y + (size_t)t * d);
         if (y_bf16)
             for (int r = 0; r < d; ++r) y_bf16[(size_t)t * d + r] = oracle_bf16_from_double(y[(size_t)t * d + r]);
+    }
+    free(z);
+    return status;
+}
+
+/* The whole layer with the fp32 FFN and combine: y [T,d] fp32 (before the bf16 rounding),
+ * y_bf16 optional; otherwise as oracle_moe_layer. */
+int oracle_moe_layer_f32(int T, int d, int f, int E, int k, int num_slots, const uint16_t* x,
+                         const uint16_t* w_router, const float* bias, const int32_t* expert_to_slot,
+                         const uint8_t* gate_q, const uint8_t* gate_s, const uint8_t* up_q,
+                         const uint8_t* up_s, const uint8_t* down_q, const uint8_t* down_s,
+                         int32_t* ids, float* weights, int32_t* slots, float* y, uint16_t* y_bf16) {
+    int status = oracle_route_topk(T, d, E, k, x, w_router, bias, expert_to_slot, ids, weights,
+                                   slots, NULL, NULL);
+    size_t wq = (size_t)f * d / 2, ws = (size_t)f * d / 32;
+    float* z = (float*)calloc((size_t)k * d, sizeof(float));
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            int s = slots[t * k + j];
+            float* zj = z + (size_t)j * d;
+            if (s < 0 || s >= num_slots) {
+                if (s >= num_slots) status |= 2;
+                for (int r = 0; r < d; ++r) zj[r] = 0.0f;
+                continue;
+            }
+            oracle_expert_ffn_f32(d, f, x + (size_t)t * d, gate_q + s * wq, gate_s + s * ws,
+                                  up_q + s * wq, up_s + s * ws, down_q + s * wq, down_s + s * ws,
+                                  NULL, zj);
+        }
+        oracle_combine_f32(d, k, z, weights + (size_t)t * k, y + (size_t)t * d);
+        if (y_bf16)
+            for (int r = 0; r < d; ++r) y_bf16[(size_t)t * d + r] = oracle_bf16_from_double((double)y[(size_t)t * d + r]);
     }
     free(z);
     return status;

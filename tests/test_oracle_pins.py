@@ -393,6 +393,142 @@ def test_combine_fixed_order_and_one_hot():
     np.testing.assert_array_equal(y, want)
 
 
+# ----------------------------------------------------------------------------- FFN in fp32
+
+U32 = 2.0 ** -24     # unit roundoff of fp32
+
+
+def _exp_f32(v):
+    """exp(v) for a float32 v, computed in double and rounded once to float32 (libm's expf
+    may differ from this by one unit in the last place)."""
+    return np.float32(math.exp(float(v)))
+
+
+def _ffn_f32_numpy(x_bits, ex):
+    """The fp32 FFN re-derived here from the bit-field decode: products exact (checked), every
+    sum an explicit float32 accumulation in index order, vectorised over rows only."""
+    xf = syn.bf16_bits_to_f32(x_bits)
+    Wg = decode_matrix(ex["gate_q"], ex["gate_s"]).astype(np.float32)
+    Wu = decode_matrix(ex["up_q"], ex["up_s"]).astype(np.float32)
+    Wd = decode_matrix(ex["down_q"], ex["down_s"]).astype(np.float32)
+    Pg, Pu = (Wg * xf[None, :]), (Wu * xf[None, :])
+    assert np.array_equal(Pg.astype(np.float64), Wg.astype(np.float64) * xf.astype(np.float64)[None, :])  # exact
+    g = np.zeros(Wg.shape[0], np.float32)
+    u = np.zeros(Wg.shape[0], np.float32)
+    for k in range(Wg.shape[1]):
+        g = (g + Pg[:, k]).astype(np.float32)
+        u = (u + Pu[:, k]).astype(np.float32)
+    den = np.array([np.float32(1.0) + _exp_f32(-gi) for gi in g], np.float32)
+    h = ((g / den).astype(np.float32) * u).astype(np.float32)
+    z = np.zeros(Wd.shape[0], np.float32)
+    for i in range(Wd.shape[1]):
+        z = (z + (Wd[:, i] * h[i]).astype(np.float32)).astype(np.float32)
+    return g, u, h, z
+
+
+def test_ffn_f32_weights_are_exact():
+    """code * 2^(b-127) in fp32 equals the bit-field value for every code and scale byte where
+    that value is within the fp32 range, including b = 0 (the subnormal 2^-127), and is the
+    signed infinity beyond it (codes 2..6 at b = 254 exceed the largest fp32)."""
+    fmax = float(np.finfo(np.float32).max)
+    for b in range(0, 255):
+        for c in range(16):
+            q = np.array([c | (c << 4)], np.uint8)
+            s = np.array([b], np.uint8)
+            want = e2m1_from_bits(c) * 2.0 ** (b - 127)
+            if abs(want) > fmax:
+                want = math.copysign(math.inf, want)
+            assert float(oracle.weight_at_f32(q, s, 0)) == want
+            assert float(oracle.weight_at_f32(q, s, 1)) == want
+
+
+def test_ffn_f32_closed_form_all_ones():
+    """Every weight 1.0 and x a set of multiples of 2^-8 whose partial sums are exact in fp32:
+    g = u = S exactly; h = fp32 steps of silu(S) S; z = f copies of h summed in fp32."""
+    d, f = 64, 32
+    ex = {n: np.full(sh, 0x22 if n.endswith("_q") else 127, np.uint8)
+          for n, sh in syn.expert_tensor_shapes(d, f).items()}
+    rng = np.random.default_rng(16)
+    xv = rng.integers(-40, 41, d).astype(np.float32) / 256.0
+    x = syn.f32_to_bf16_bits(xv)
+    S = np.float32(np.sum(xv.astype(np.float64)))          # exact: |partial sums| < 2^5, step 2^-8
+    h, z = oracle.expert_ffn_f32(x, ex)
+    den = np.float32(np.float32(1.0) + _exp_f32(-S))
+    hs = np.float32(np.float32(S / den) * S)
+    np.testing.assert_allclose(h, hs, rtol=3 * U32)        # expf within an ulp of exp
+    zs = np.float32(0)
+    for _ in range(f):
+        zs = np.float32(zs + h[0])
+    assert np.all(h == h[0]) and np.all(z == zs)
+
+
+def test_ffn_f32_closed_form_diagonal():
+    """W_gate = I, W_up = 2I, W_down = I: z_i = h_i = fp32(fp32(x_i / (1 + expf(-x_i))) * 2x_i)."""
+    d = f = 32
+    def pack(codes):
+        return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    ex = {"gate_q": pack(np.eye(32, dtype=np.int64) * 2), "up_q": pack(np.eye(32, dtype=np.int64) * 4),
+          "down_q": pack(np.eye(32, dtype=np.int64) * 2)}
+    for n in ("gate_s", "up_s", "down_s"):
+        ex[n] = np.full((32, 1), 127, np.uint8)
+    xv = syn.bf16_bits_to_f32(syn.f32_to_bf16_bits(np.linspace(-3, 3, 32).astype(np.float32)))
+    x = syn.f32_to_bf16_bits(xv)
+    h, z = oracle.expert_ffn_f32(x, ex)
+    want = np.array([np.float32(np.float32(v / np.float32(np.float32(1) + _exp_f32(-v))) * np.float32(2 * v))
+                     for v in xv], np.float32)
+    np.testing.assert_allclose(h, want, rtol=3 * U32, atol=0)
+    np.testing.assert_array_equal(z, h)                     # one nonzero term per row: exact
+
+
+def test_ffn_f32_against_independent_numpy_float32():
+    rng = np.random.default_rng(17)
+    d, f = 128, 64
+    ex = _expert(rng, d, f)
+    x = syn.f32_to_bf16_bits(rng.normal(size=d).astype(np.float32))
+    h, z = oracle.expert_ffn_f32(x, ex)
+    g, u, hh, zz = _ffn_f32_numpy(x, ex)
+    # g and u are identical sequences of identical fp32 operations; h differs at most by the
+    # last-place difference between libm's expf and a correctly rounded exp, and z inherits it
+    np.testing.assert_allclose(h, hh, rtol=4 * U32, atol=4 * U32 * np.abs(hh).max())
+    np.testing.assert_allclose(z, zz, rtol=0, atol=16 * U32 * np.abs(zz).max())
+
+
+def test_ffn_f32_within_the_fp32_bound_of_the_fp64_statement():
+    """At the tiny workload's shape: |z32 - z64| stays inside a first-order bound of fp32
+    sequential summation (gamma_n = n u / (1 - n u) times the sums of absolute terms),
+    propagated through SwiGLU, with a factor 2 for the second-order terms."""
+    d, f = 512, 256
+    for e in (0, 5):
+        ex = syn.expert_tensors(0, 0, e, d, f, -8, -4)
+        x = syn.activations(0, 0, 1, d)[0]
+        h32, z32 = oracle.expert_ffn_f32(x, ex)
+        h64, z64 = oracle.expert_ffn(x, ex)
+        xv = bf16_to_f64(x)
+        Wg, Wu, Wd = (decode_matrix(ex[m + "_q"], ex[m + "_s"]) for m in ("gate", "up", "down"))
+        gam = lambda n: n * U32 / (1 - n * U32)
+        g, u = Wg @ xv, Wu @ xv
+        dg, du = gam(d) * (np.abs(Wg) @ np.abs(xv)), gam(d) * (np.abs(Wu) @ np.abs(xv))
+        sig = 1 / (1 + np.exp(-g))
+        dsilu = np.abs(sig * (1 + g * (1 - sig)))           # |silu'(g)|
+        dh = dsilu * dg * np.abs(u) + np.abs(g * sig) * du + 6 * U32 * np.abs(h64)
+        dz = np.abs(Wd) @ dh + gam(f + 1) * (np.abs(Wd) @ np.abs(h64))
+        assert np.all(np.abs(h32 - h64) <= 2 * dh), np.max(np.abs(h32 - h64) / dh)
+        assert np.all(np.abs(z32 - z64) <= 2 * dz), np.max(np.abs(z32 - z64) / dz)
+
+
+def test_combine_f32_one_hot_and_ascending_order():
+    rng = np.random.default_rng(18)
+    z = rng.normal(size=(3, 16)).astype(np.float32)
+    y = oracle.combine_f32(z, np.array([0.0, 1.0, 0.0], np.float32))
+    np.testing.assert_array_equal(y, z[1])
+    # order decides the value: in fp32, (1 + 2^24) - 2^24 = 0 (ascending j) while
+    # 1 + (2^24 - 2^24) = 1 (any order that pairs the large terms first)
+    z = np.array([[1.0], [2.0 ** 24], [-(2.0 ** 24)]], np.float32)
+    assert oracle.combine_f32(z, np.ones(3, np.float32))[0] == 0.0
+    z = np.array([[2.0 ** 24], [-(2.0 ** 24)], [1.0]], np.float32)
+    assert oracle.combine_f32(z, np.ones(3, np.float32))[0] == 1.0
+
+
 # ----------------------------------------------------------------------------- layer
 
 def _tiny_layer_inputs(seed=0):
@@ -408,8 +544,11 @@ def _tiny_layer_inputs(seed=0):
 
 def test_tiny_layer_against_independent_rederivation():
     d, f, E, k, T, x, wr, tab, experts, stacked = _tiny_layer_inputs()
-    r = oracle.moe_layer(x, wr, None, tab, k, stacked)
-    assert r["status"] == 0
+    r = oracle.moe_layer(x, wr, None, tab, k, stacked, precision="f64")
+    r32 = oracle.moe_layer(x, wr, None, tab, k, stacked)       # the fp32 reference statement
+    assert r["status"] == 0 and r32["status"] == 0
+    np.testing.assert_array_equal(r32["ids"], r["ids"])
+    np.testing.assert_array_equal(r32["weights"], r["weights"])
     for t in range(T):
         keys, s32 = [], {}
         for e in range(E):
@@ -431,6 +570,7 @@ def test_tiny_layer_against_independent_rederivation():
             hh = g * u / (1 + np.exp(-g))
             y += float(np.float32(s32[e] / tot)) * (decode_matrix(ex["down_q"], ex["down_s"]) @ hh)
         np.testing.assert_allclose(r["y"][t], y, rtol=1e-9, atol=1e-9 * np.abs(y).max())
+        assert np.abs(r32["y"][t] - y).max() <= 1e-5 * np.abs(y).max()
         # bf16 output is the one-step rounding of y
         yb = syn.bf16_bits_to_f32(r["y_bf16"][t]).astype(np.float64)
         assert np.all(np.abs(yb - r["y"][t]) <= np.abs(r["y"][t]) * 2.0 ** -8 + 1e-300)

@@ -65,3 +65,13 @@ def row_rel_err(y_gpu: np.ndarray, y_ref: np.ndarray) -> np.ndarray:
     num = np.abs(y_gpu - y_ref).max(axis=1)
     den = np.abs(y_ref).max(axis=1)
     return num / np.maximum(den, 1e-30)
+
+
+def elem_rel_err(y_gpu: np.ndarray, y_ref: np.ndarray, floor: float = 1e-3) -> np.ndarray:
+    """Per token row: max_i |y_gpu - y_ref| / max(|y_ref_i|, floor * max_i |y_ref|), the
+    elementwise relative error with a floor (reported beside the normwise row bound, which is
+    the one asserted: a plain elementwise ratio is unbounded where y_ref is near 0)."""
+    y_gpu = np.asarray(y_gpu, np.float64)
+    y_ref = np.asarray(y_ref, np.float64)
+    den = np.maximum(np.abs(y_ref), floor * np.abs(y_ref).max(axis=1, keepdims=True))
+    return (np.abs(y_gpu - y_ref) / np.maximum(den, 1e-30)).max(axis=1)
