@@ -20,7 +20,7 @@ __all__ = [
     "moe_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_route_topk_noalloc", "moe_permute",
     "moe_expert_ffn_fp4", "moe_combine", "moe_residency_bias", "moe_split_waves", "moe_gather_experts", "moe_status_str",
     "moe_cb3_slot_bytes", "moe_pack_cb3", "moe_expert_ffn_cb3", "MOE_STATUS_CB3_ROW",
-    "moe_kernel_launches", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
+    "moe_kernel_launches", "moe_workspace_set_wait_limit", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
     "MOE_STATUS_FEW_RESIDENT", "MOE_STATUS_BAD_SLOT", "MOE_STATUS_TIMEOUT", "DECODE_MAX_T",
 ]
 
@@ -55,6 +55,7 @@ _SIG = {
     "moe_slot_bytes": (ctypes.c_int64, [_P]),
     "moe_workspace_bytes": (ctypes.c_size_t, [_P, _I]),
     "moe_workspace_init": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P]),
+    "moe_workspace_set_wait_limit": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _I, _P]),
     "moe_pack_expert": (ctypes.c_int, [_P] * 8 + [_I, _P]),
     "moe_route_topk": (ctypes.c_int, [_P, _I] + [_P] * 9 + [ctypes.c_size_t, _P]),
     "moe_permute": (ctypes.c_int, [_P, _I] + [_P] * 5 + [ctypes.c_size_t, _P]),
@@ -133,6 +134,13 @@ def moe_workspace_bytes(dims, T_max: int) -> int:
 
 def moe_workspace_init(dims, ws, stream=None):
     _check("moe_workspace_init", lib().moe_workspace_init(ctypes.byref(_dims(dims)), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_workspace_set_wait_limit(dims, ws, polls: int, stream=None):
+    """Diagnostic: dependency waits of the expert kernels on this workspace give up after
+    `polls` polls (0 restores the default)."""
+    _check("moe_workspace_set_wait_limit", lib().moe_workspace_set_wait_limit(
+        ctypes.byref(_dims(dims)), _ptr(ws), ws.numel() * ws.element_size(), int(polls), _stream(stream)))
 
 
 def moe_pack_expert(dims, gate_q, gate_s, up_q, up_s, down_q, down_s, arena: moe_arena, slot: int, stream=None):

@@ -16,9 +16,9 @@ int launch_route(const moe_dims* m, int T, const uint16_t* x, const uint16_t* wr
                  char* ws, const WsLayout& L, cudaStream_t st, int num_sms);
 int launch_permute(const moe_dims* m, int T, const int32_t* ids, int32_t* offsets, int32_t* row_src,
                    int32_t* row_dst, cudaStream_t st);
-int launch_decode_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x,
-                      const int32_t* slot, const float* w, uint16_t* y, int32_t* status, char* ws,
-                      const WsLayout& L, cudaStream_t st, int num_sms);
+int launch_stream_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
+                      const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
+                      int num_sms);
 int launch_prefill_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                        const int32_t* offsets, const int32_t* row_src, float* rows_out, int32_t* status, char* ws,
                        const WsLayout& L, cudaStream_t st, int num_sms);
@@ -95,6 +95,8 @@ static int check_ws(const moe_dims* m, int T, void* ws, size_t ws_bytes, WsLayou
     return MOE_OK;
 }
 
+__global__ void set_word_kernel(int32_t* p, int32_t v) { *p = v; }
+
 static int check_arena(const moe_dims* m, const moe_arena* ar, bool cb3 = false) {
     if (!ar || !ar->base) return MOE_ERR_NULL;
     if ((reinterpret_cast<uintptr_t>(ar->base) & 1023u) != 0) return MOE_ERR_ARENA;
@@ -117,6 +119,18 @@ int64_t moe_slot_bytes(const moe_dims* dims) {
 size_t moe_workspace_bytes(const moe_dims* dims, int32_t T_max) {
     if (!dims_ok(dims) || T_max < 0) return 0;
     return ws_layout(dims, T_max).total;
+}
+
+int moe_workspace_set_wait_limit(const moe_dims* dims, void* ws, size_t ws_bytes, int32_t polls, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (polls < 0) return MOE_ERR_DIMS;
+    WsLayout L;
+    int rc = check_ws(dims, 0, ws, ws_bytes, &L);
+    if (rc) return rc;
+    set_word_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.counter) +
+                                                            kCtrWaitLimit, polls);
+    note_launch(1);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
 int moe_workspace_init(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream) {
@@ -200,7 +214,7 @@ int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, 
     if (T <= kDecodeMaxT && fused) {
         if (!cuda_cores && tc_decode_supported(dims, T))
             return launch_tc_decode(dims, arena, T, x, topk_slot, topk_w, y, dev_status, w, L, st, sms);
-        return launch_decode_ffn(dims, arena, T, x, topk_slot, topk_w, y, dev_status, w, L, st, sms);
+        return launch_stream_ffn(dims, arena, T, x, topk_slot, topk_w, y, dev_status, w, L, st, sms);
     }
     if (!group_offsets || !row_src || (fused && !row_dst)) return MOE_ERR_NULL;
     if (rows_out && !aligned16(rows_out)) return MOE_ERR_ALIGN;

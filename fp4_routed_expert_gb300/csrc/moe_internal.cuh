@@ -77,11 +77,18 @@ inline bool dims_ok(const moe_dims* m) {
 }
 
 // Counters inside the counter section (zeroed by moe_workspace_init; every user leaves them
-// zero again): the decode FFN kernel's work list, x jobs and x-ready, exit ticket, per-key readiness
-// (256 decode keys) and y counts per 32 output features (d/32 <= 2048).
-enum { kCtrRoute = 0, kCtrFfnWork = 64, kCtrFfnXReady = 65, kCtrFfnExit = 66, kCtrFfnXJob = 67, kCtrFfnReady = 128,
-       kCtrFfnY = 384, kCounterWords = 2432 };
-inline size_t counter_words(const moe_dims*) { return kCounterWords; }
+// zero again): the tensor-core FFN kernel's work list, x jobs and x-ready, exit ticket, per-key
+// readiness (256 decode keys) and y counts per 32 output features (d/32 <= 2048); the streaming
+// decode kernel's x jobs, x-ready and exit ticket; the wait limit (kCtrWaitLimit: 0 = the
+// default kSpinLimit polls, else the number of polls after which a wait on another CTA's
+// progress gives up -- set only by moe_workspace_set_wait_limit); then the streaming kernel's
+// h readiness per key (gate/up tiles whose h is written).
+enum { kCtrRoute = 0, kCtrFfnWork = 64, kCtrFfnXReady = 65, kCtrFfnExit = 66, kCtrFfnXJob = 67,
+       kCtrStrXJob = 69, kCtrStrXReady = 70, kCtrStrExit = 71, kCtrWaitLimit = 72,
+       kCtrFfnReady = 128, kCtrFfnY = 384, kCounterWords = 2432 };
+constexpr int kStreamMaxKeys = kDecodeMaxT * kMaxTopK;   // keys of a decode call: at most one per pair
+inline size_t stream_hcnt_off(const moe_dims*) { return kCounterWords; }
+inline size_t counter_words(const moe_dims* m) { return stream_hcnt_off(m) + kStreamMaxKeys; }
 
 // Prefill activation tiles: kPrefillNT permuted rows each (tensor-core path).  The plan of a
 // prefill call (written by plan_kernel) describes the expert groups and their tiles:
@@ -111,12 +118,14 @@ struct WsLayout {
     size_t h;           // fp32 [T_max*k, f] SwiGLU output per (token, j) pair or permuted row
     size_t rows;        // fp32 [T_max*k, d] per-row expert outputs (prefill with fused combine; cb3 z rows)
     size_t tc;          // tensor-core path: quantised activations, quantised h, per-row outputs
+    size_t stream;      // streaming decode path: x and h records, partial sums
     size_t total;
 };
 
 inline size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 size_t tc_workspace_bytes(const moe_dims* m, int T);   // mxf4_gemm.cu
+size_t stream_workspace_bytes(const moe_dims* m, int T);   // ffn_stream.cu
 
 // Adds n to the count of kernels this library has enqueued (abi.cu).
 void note_launch(int n);
@@ -133,6 +142,7 @@ inline WsLayout ws_layout(const moe_dims* m, int T_max) {
     w.h = o;       o = align256(o + 4 * T * k * (size_t)m->f);
     w.rows = o;    o = align256(o + 4 * T * k * (size_t)m->d);
     w.tc = o;      o = align256(o + tc_workspace_bytes(m, (int)T));
+    w.stream = o;  o = align256(o + stream_workspace_bytes(m, T_max > 0 ? T_max : 1));
     w.total = o;
     return w;
 }
@@ -207,6 +217,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(done)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return done != 0;
+}
+// Non-blocking probe (test_wait never suspends the thread; try_wait may, for a while).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile("{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
                  : "=r"(done)
                  : "r"(bar), "r"(parity)
                  : "memory");

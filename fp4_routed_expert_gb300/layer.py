@@ -90,7 +90,8 @@ class MoeLayer:
 
     def experts(self, x, T=None, fused_prefill=False, stream=None, y=None, cuda_cores=False):
         """Expert FFN + combine.  cuda_cores=True selects the CUDA-core kernels (exact fp4 x bf16
-        products); the default uses the tensor-core kernels where the shape allows."""
+        products: the streaming kernel in decode, grouped GEMMs in prefill); the default uses the
+        tensor-core kernels where the shape allows."""
         T = x.shape[0] if T is None else T
         y = self.y if y is None else y
         extra = MOE_FFN_CUDA_CORES if cuda_cores else 0

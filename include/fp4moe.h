@@ -32,9 +32,9 @@
  *  - Some kernels are launched with programmatic dependent launch: they may become resident
  *    while the previous kernel on `stream` still runs.  Before that kernel has completed they
  *    read exactly one input, which the kernel enqueued immediately before the call must
- *    therefore not write: x of moe_expert_ffn_fp4 on the tensor-core decode path (the router
- *    call that normally precedes it does not).  Every other input, every output and the
- *    workspace are touched only after it has completed.
+ *    therefore not write: x of a decode call of moe_expert_ffn_fp4 (the router call that
+ *    normally precedes it does not).  Every other input, every output and the workspace are
+ *    touched only after it has completed.
  *  - After a call that set MOE_STATUS_TIMEOUT the workspace must be re-initialised
  *    (moe_workspace_init) before its next use.
  */
@@ -86,8 +86,8 @@ enum {
 
 /* Flags of moe_expert_ffn_fp4. */
 #define MOE_FUSE_COMBINE 1         /* write y directly (fixed-order combine fused in) */
-#define MOE_FFN_CUDA_CORES 2       /* use the CUDA-core kernels (exact fp4 x bf16 products,
-                                      fp32 accumulation) instead of the tensor-core kernels */
+#define MOE_FFN_CUDA_CORES 2       /* use the CUDA-core kernels (exact fp4 x bf16 products, fp32
+                                      accumulation) instead of the tensor-core kernels */
 
 /* Bytes of one arena slot: 3*f*d/2 code bytes + 3*f*d/32 scale bytes, rounded up to
  * 1024 (18,800,640 at d=5120, f=2304).  Returns -1 for unsupported dims. */
@@ -99,8 +99,18 @@ int64_t moe_slot_bytes(const moe_dims* dims);
  * beyond what moe_workspace_init performs.  Returns 0 for unsupported dims. */
 size_t moe_workspace_bytes(const moe_dims* dims, int32_t T_max);
 
-/* Zero the workspace's persistent counters (once, after allocating it). */
+/* Zero the workspace's persistent counters (once, after allocating it).  This also restores
+ * the default wait limit. */
 int moe_workspace_init(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream);
+
+/* Diagnostic knob for the bounded waits: after this call, every wait of an expert kernel on
+ * another CTA's progress (x encoded, a key's h complete) through this workspace gives up after
+ * `polls` polls instead of the default (about a second), sets MOE_STATUS_TIMEOUT and lets the
+ * kernel drain its copies and return.  polls = 0 restores the default; so does
+ * moe_workspace_init.  Waits on a CTA's own copies keep the default limit.  It exists so that
+ * the timeout path can be exercised without a fault: a small limit makes a dependency wait run
+ * out.  Enqueued on `stream` (one one-thread kernel); polls < 0 returns MOE_ERR_DIMS. */
+int moe_workspace_set_wait_limit(const moe_dims* dims, void* ws, size_t ws_bytes, int32_t polls, void* stream);
 
 /* Pack one expert from the canonical (checkpoint) layout into arena slot `slot`.
  * Canonical layout, device pointers, two e2m1 codes per byte (element 2i in the low
@@ -167,12 +177,17 @@ int moe_permute(const moe_dims* dims, int32_t T, const int32_t* topk_ids, int32_
  * flags = 0: writes rows_out fp32 [T*k, d] (row r = z for row_src[r], unweighted); y unused.
  * Slots outside [0, num_slots) set MOE_STATUS_BAD_SLOT and contribute zero.
  * Decode (T <= 16 with MOE_FUSE_COMBINE) needs only the routing outputs; the permutation
- * arguments may be NULL there.  The tensor-core path (the default) feeds x and h to the MMA
- * as a sum of four MXFP4 terms each (e2m1 codes, UE8M0 scale per 32 elements, every term
- * quantising the previous terms' residual); its expert outputs match exact fp4 x bf16
- * products to about 1e-4 relative before the bf16 rounding of y.  The tensor-core path takes
- * decode calls with T*k <= 128; other decode calls use the CUDA-core kernels.  In either
- * kernel family a decode call's row t is bit-identical to the T = 1 call on token t alone
+ * arguments may be NULL there.
+ * Tensor cores (the default): tcgen05 block-scaled MMAs that feed x and h as a sum of four
+ * MXFP4 terms each (e2m1 codes, UE8M0 scale per 32 elements, every term quantising the previous
+ * terms' residual); expert outputs match exact fp4 x bf16 products to about 1e-4 relative
+ * before the bf16 rounding of y.  They take decode calls with T*k <= 128.
+ * CUDA cores (MOE_FFN_CUDA_CORES, and the other decode calls): decode streams every selected
+ * expert once through one persistent kernel (then a small combine kernel); every product fp4 x
+ * activation is exact in fp32 (x as f16 under a power-of-two scale per 32 elements, exact for
+ * bf16; h rounded once to f16 under the same kind of scale), sums in fp32 in an order fixed by
+ * the shapes.  Prefill runs grouped CUDA-core GEMMs with exact products.
+ * In every decode kernel a call's row t is bit-identical to the T = 1 call on token t alone
  * (with the same routing), so multi-row verification reproduces single-token decoding. */
 int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, const uint16_t* x,
                        const int32_t* topk_ids, const int32_t* topk_slot, const float* topk_w,

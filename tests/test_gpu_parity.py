@@ -19,6 +19,8 @@ DEV = "cuda"
 
 
 def run_layer(wl, x_bits, bias=None, fused_prefill=False, cuda_cores=False):
+    """cuda_cores=False: the tensor-core kernels (the default); True: the CUDA-core kernels
+    (decode: the streaming kernel and its combine; prefill: grouped GEMMs)."""
     T = x_bits.shape[0]
     layer = MoeLayer(wl.d, wl.f, wl.E, wl.k, max(T, 1), wl.arena)
     x = bits_to_torch(x_bits, DEV)

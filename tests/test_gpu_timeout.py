@@ -1,0 +1,53 @@
+"""Bounded waits: a dependency wait that runs out sets MOE_STATUS_TIMEOUT, the kernel drains
+its own copies and returns, and a workspace re-initialised afterwards serves a normal call.
+
+The wait is made to run out without any fault: moe_workspace_set_wait_limit makes every wait
+of the streaming decode kernel (the CUDA-core decode path) on another CTA's progress (x
+encoded, a key's h rows complete) give up after one poll, and in a small decode call the CTAs
+that take down units check their key's h count long before any gate/up tile has finished.  Waits on a CTA's own copies keep their default limit, so every copy
+that was issued lands before its CTA exits."""
+import numpy as np
+import pytest
+import torch
+
+import fp4_routed_expert_gb300 as moe
+from fp4_routed_expert_gb300.layer import MoeLayer
+from synth import tensors as syn
+
+from test_gpu_parity import oracle_with_routing
+from workloads import bits_to_torch, make_workload, row_rel_err
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return make_workload(512, 256, 16, 2, seed=0, scale=(-8, -4))
+
+
+def test_decode_dependency_wait_times_out_then_workspace_recovers(tiny):
+    T = 3
+    layer = MoeLayer(tiny.d, tiny.f, tiny.E, tiny.k, T, tiny.arena)
+    x_bits = syn.activations(0, 60, T, tiny.d)
+    x = bits_to_torch(x_bits, DEV)
+    wr = bits_to_torch(tiny.wr, DEV)
+    tab = torch.from_numpy(tiny.table).to(DEV)
+    layer.route(x, wr, tab)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    moe.moe_workspace_set_wait_limit(layer.dims, layer.ws, 1)
+    layer.experts(x, cuda_cores=True)
+    torch.cuda.synchronize()                      # the call returned
+    assert int(layer.status.item()) & moe.MOE_STATUS_TIMEOUT
+    # recovery: re-initialise the workspace (default limit again), route and run normally
+    moe.moe_workspace_init(layer.dims, layer.ws)
+    layer.status.zero_()
+    layer.route(x, wr, tab)
+    y = layer.experts(x, cuda_cores=True)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    r = dict(ids=layer.ids[:T].cpu().numpy(), slots=layer.slots[:T].cpu().numpy(), weights=layer.w[:T].cpu().numpy())
+    ref = oracle_with_routing(tiny, x_bits, r)
+    err = row_rel_err(y[:T].float().cpu().numpy(), ref)
+    assert err.max() <= 1e-2, err
