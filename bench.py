@@ -110,12 +110,13 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % gpu_index)
+        self.path = None
 
     def start(self):
+        import tempfile
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix="clocks_bench_%d_" % self.gpu, suffix=".csv")
+            self.f = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
@@ -133,7 +134,10 @@ class ClockSampler:
         self.f.close()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        with open(self.path) as fh:
+            lines = fh.readlines()
+        os.unlink(self.path)
+        for line in lines:
             p = [s.strip() for s in line.split(",")]
             if len(p) < 8:
                 continue
@@ -396,6 +400,285 @@ def run_prefill(w, args, device, resident=None):
                              else "fallback bf16 x 6"}}
 
 
+# ---------------------------------------------------------------------------- 40-layer keep-set workloads
+
+KS_DECODE_STEPS = 20          # fresh tokens (T=1) or verify batches (T=16) per replay
+LONG_T, LONG_CHUNKS = 8192, 4  # a 32,768-token sequence in four chunks
+LONG_BIAS = (1.1, 0.04)       # Zipf s, beta of the fresh per-layer score bias
+NORM_EPS = 1e-6
+
+
+def _probe_graph(stream, body, rt):
+    """Capture body(probe) into a graph; probe(name) returns a context that brackets the calls
+    inside it with external event record nodes.  Returns (graph, {name: [(a, b), ...]})."""
+    import contextlib
+    import torch
+    probes = {}
+
+    @contextlib.contextmanager
+    def probe(name, on=True):
+        if not (on and rt.ok()):
+            yield
+            return
+        h = torch.cuda.current_stream().cuda_stream
+        a, b = rt.event(), rt.event()
+        rt.record_external(a, h)
+        yield
+        rt.record_external(b, h)
+        probes.setdefault(name, []).append((a, b))
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        body(probe)
+    return g, probes
+
+
+def _probe_ms(rt, probes):
+    out = {}
+    for name, pairs in probes.items():
+        v = [rt.elapsed_ms(a, b) for a, b in pairs]
+        v = [x for x in v if x is not None]
+        if v:
+            out[name] = v
+    return out
+
+
+def _fractions(bytes_, flops, ms, peaks, kind):
+    hbm = float(peaks["hbm_gbs"])
+    fp4 = float(peaks["bf16_tflops"]) * (13.5 / 2.25)
+    gbs = bytes_ / (ms * 1e-3) / 1e9
+    tfs = flops / (ms * 1e-3) / 1e12
+    return ({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+             "bytes": int(bytes_), "peak_source": "%s hbm_gbs" % kind},
+            {"bound": "tensor", "achieved": round(tfs, 3), "peak": round(fp4, 1), "unit": "TFLOP/s",
+             "frac": round(tfs / fp4, 5), "flops": float(flops),
+             "peak_source": "%s bf16 x 6 (nominal fp4/bf16 dense ratio)" % kind})
+
+
+def run_keepset_decode(ks, T, args, device):
+    """One 40-layer decode (T=1) or DSpark-verify (T=16) step per fresh input, KS_DECODE_STEPS
+    of them per graph replay: each layer routes over its 154 resident experts (the rest masked),
+    runs the expert FFN with the combine fused, and the next layer's input is
+    bf16(RMSNorm(x + y)) computed on the device.  Distinct experts per layer (U) are counted
+    from an eager pass over the same inputs, which is also the warm-up."""
+    import torch
+    import fp4_routed_expert_gb300 as moe
+    from fp4_routed_expert_gb300.layer import MoeLayer
+    from synth import tensors as syn
+    from synth.keepset import LAYERS, KEEP, bits_to_device
+    S = KS_DECODE_STEPS
+    layer = MoeLayer(D, F, E, K, T, ks.arena, device)
+    xs = bits_to_device(syn.activations(0, 0, S * T, D, stream=15 if T == 1 else 16), device).view(S, T, D)
+    x = torch.empty((T, D), dtype=torch.bfloat16, device=device)
+    y = torch.empty((T, D), dtype=torch.bfloat16, device=device)
+    ids_log = torch.empty((S, LAYERS, T, K), dtype=torch.int32, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def step(s, probe=None, log=False):
+        x.copy_(xs[s])
+        for l in range(LAYERS):
+            on = probe is not None and s == S // 2
+            with (probe("route", on) if on else _null()):
+                layer.route(x, ks.wr[l], ks.tab_dev[l], None, T=T)
+            if log:
+                ids_log[s, l].copy_(layer.ids[:T])
+            with (probe("ffn", on) if on else _null()):
+                layer.experts(x, T=T, y=y)
+            with (probe("norm", on) if on else _null()):
+                moe.moe_residual_rmsnorm(T, D, x, y, NORM_EPS, x)
+
+    with torch.cuda.stream(stream):
+        for s in range(S):
+            step(s, log=True)
+    torch.cuda.synchronize()
+    ids = ids_log.cpu().numpy()
+    U = np.array([[np.unique(ids[s, l][ids[s, l] >= 0]).size for l in range(LAYERS)] for s in range(S)])
+    rt = CudaRt()
+    before = moe.moe_kernel_launches()
+    g, probes = _probe_graph(stream, lambda probe: [step(s, probe) for s in range(S)], rt)
+    launches = moe.moe_kernel_launches() - before
+    ms = _replay_ms(g, stream, args)
+    pk = _probe_ms(rt, probes)
+    status = int(layer.status.item())
+    peaks, kind = measured_peaks()
+    per_layer_io = 2 * T * D * 2 + KEEP * D * 2          # x in, y out, the resident router rows
+    bytes_ = float(U.sum()) * EXPERT_BYTES + S * LAYERS * per_layer_io
+    flops = 6.0 * S * LAYERS * T * K * D * F
+    hbm, fp4 = _fractions(bytes_, flops, ms, peaks, kind)
+    out = {"workload": "40-layer keep-set %s: d=%d f=%d E=%d (154 resident per layer, 6,160 slots, %.1f GB arena, "
+                       "Zipf(1.1) keep-sets, non-resident experts masked), top-k=%d, T=%d; %d fresh %s per replay, "
+                       "layers chained by bf16(RMSNorm(x + y)) on the device"
+                       % ("decode" if T == 1 else "DSpark verify", D, F, E, ks.arena.num_slots * EXPERT_BYTES / 1e9,
+                          K, T, S, "tokens" if T == 1 else "16-token batches"),
+           "value": round(S * T / (ms * 1e-3), 2), "unit": "tokens/s (through all 40 layers)",
+           "ms_per_step": round(ms / S, 4), "layer_tokens_per_s": round(S * T * LAYERS / (ms * 1e-3), 1),
+           "distinct_experts_per_layer": {"mean": round(float(U.mean()), 2), "min": int(U.min()), "max": int(U.max())},
+           "roofline_hbm": hbm, "roofline_fp4": fp4, "status": status, "gpu_launches_per_replay": launches,
+           "l2": "inputs larger than L2 (115.8 GB arena; each layer streams U experts), no flush"}
+    if "ffn" in pk:
+        s_mid = S // 2
+        fb = float(U[s_mid].sum()) * EXPERT_BYTES + LAYERS * 2 * T * D * 2
+        f_ms = sum(pk["ffn"])
+        out["ffn_roofline"] = {"bound": "hbm", "kernel": "expert FFN + fused combine (one call per layer)",
+                               "achieved": round(fb / (f_ms * 1e-3) / 1e9, 1), "peak": float(peaks["hbm_gbs"]),
+                               "unit": "GB/s", "frac": round(fb / (f_ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4),
+                               "launch_us_mean": round(1e3 * f_ms / len(pk["ffn"]), 2)}
+        out["breakdown_us_per_layer"] = {n: round(1e3 * statistics.mean(v), 2) for n, v in pk.items()}
+        out["breakdown_note"] = ("event-bracketed calls of the middle step of one replay: route = router + top-k + "
+                                 "slot lookup, ffn = expert FFN + combine, norm = the chaining step")
+    return out
+
+
+class _null:
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *a):
+        return False
+
+
+def _replay_ms(g, stream, args, reps=None):
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+    torch.cuda.synchronize()
+    reps = reps or max(3, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_long_prefill(ks, args, device):
+    """A 32,768-token sequence as four 8,192-token chunks through the 40 keep-set layers, a fresh
+    Zipf(1.1) score bias per layer, layers chained by bf16(RMSNorm(x + y)) on the device.  One
+    graph holds one chunk's 40 layers; a step copies each chunk's input in and replays it.  The
+    first pass (eager) logs the routing for U and warms up; a second graph with event probes
+    and the combine issued as its own call gives the per-call breakdown of one chunk."""
+    import torch
+    import fp4_routed_expert_gb300 as moe
+    from fp4_routed_expert_gb300.layer import MoeLayer
+    from synth import tensors as syn
+    from synth.keepset import LAYERS, KEEP, bits_to_device
+    T = LONG_T
+    layer = MoeLayer(D, F, E, K, T, ks.arena, device)
+    xs = [bits_to_device(syn.activations(0, 0, T, D, start_token=c * T, stream=13), device) for c in range(LONG_CHUNKS)]
+    bias = [torch.from_numpy(syn.zipf_score_bias(0, l, E, *LONG_BIAS)).to(device) for l in range(LAYERS)]
+    x = torch.empty((T, D), dtype=torch.bfloat16, device=device)
+    y = torch.empty((T, D), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.Stream(device)
+    U = np.zeros((LONG_CHUNKS, LAYERS), np.int64)
+    with torch.cuda.stream(stream):
+        for c in range(LONG_CHUNKS):
+            x.copy_(xs[c])
+            for l in range(LAYERS):
+                layer.route(x, ks.wr[l], ks.tab_dev[l], bias[l])
+                ids = layer.ids[:T].cpu().numpy()
+                U[c, l] = np.unique(ids[ids >= 0]).size
+                layer.experts(x, fused_prefill=True, y=y)
+                moe.moe_residual_rmsnorm(T, D, x, y, NORM_EPS, x)
+    torch.cuda.synchronize()
+
+    def chunk(probe):
+        for l in range(LAYERS):
+            layer.route(x, ks.wr[l], ks.tab_dev[l], bias[l])
+            layer.experts(x, fused_prefill=True, y=y)
+            moe.moe_residual_rmsnorm(T, D, x, y, NORM_EPS, x)
+
+    rt = CudaRt()
+    before = moe.moe_kernel_launches()
+    g, _ = _probe_graph(stream, chunk, rt)
+    launches = moe.moe_kernel_launches() - before
+    with torch.cuda.stream(stream):
+        for c in range(LONG_CHUNKS):       # warm replays
+            x.copy_(xs[c])
+            g.replay()
+    torch.cuda.synchronize()
+    reps = 1 if args.steps < 10 else 2
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(reps):
+            for c in range(LONG_CHUNKS):
+                x.copy_(xs[c])
+                g.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    status = int(layer.status.item())
+
+    # per-call breakdown of one chunk: the same kernels, the combine issued as its own call
+    def chunk_probed(probe):
+        for l in range(LAYERS):
+            with probe("route"):
+                layer.route(x, ks.wr[l], ks.tab_dev[l], bias[l])
+            with probe("permute"):
+                moe.moe_permute(layer.dims, T, layer.ids, layer.offsets, layer.row_src, layer.row_dst, layer.ws)
+            with probe("ffn (plan + A quantise + gate/up + down)"):
+                moe.moe_expert_ffn_fp4(layer.dims, layer.arena.c, T, x, layer.ids, layer.slots, layer.w,
+                                       layer.offsets, layer.row_src, layer.row_dst, 0, layer.rows, None,
+                                       layer.status, layer.ws)
+            with probe("combine"):
+                moe.moe_combine(layer.dims, T, layer.rows, layer.row_dst, layer.w, y)
+            with probe("norm"):
+                moe.moe_residual_rmsnorm(T, D, x, y, NORM_EPS, x)
+
+    g2, probes = _probe_graph(stream, chunk_probed, rt)
+    with torch.cuda.stream(stream):
+        x.copy_(xs[0])
+        g2.replay()
+        x.copy_(xs[0])
+        g2.replay()
+    torch.cuda.synchronize()
+    pk = _probe_ms(rt, probes)
+    peaks, kind = measured_peaks()
+    per_layer_io = 2 * T * D * 2 + KEEP * D * 2
+    bytes_ = float(U.sum()) * EXPERT_BYTES + LONG_CHUNKS * LAYERS * per_layer_io
+    flops = 6.0 * LONG_CHUNKS * LAYERS * T * K * D * F
+    hbm, fp4 = _fractions(bytes_, flops, ms, peaks, kind)
+    out = {"workload": "long prefill: 32,768 tokens as 4 x 8,192-token chunks through 40 keep-set layers (154 resident "
+                       "of 384 per layer, 6,160 slots), d=%d f=%d top-k=%d, fresh Zipf(s=%.1f, beta=%.2f) score bias "
+                       "per layer, layers chained by bf16(RMSNorm(x + y)) on the device; route + permute + expert FFN "
+                       "+ combine per chunk-layer" % (D, F, K, *LONG_BIAS),
+           "value": round(LONG_CHUNKS * T / (ms * 1e-3), 1), "unit": "tokens/s (through all 40 layers)",
+           "ms_per_sequence": round(ms, 3), "ms_per_chunk_layer": round(ms / (LONG_CHUNKS * LAYERS), 4),
+           "layer_tokens_per_s": round(LONG_CHUNKS * T * LAYERS / (ms * 1e-3), 1),
+           "distinct_experts_per_chunk_layer": {"mean": round(float(U.mean()), 2), "min": int(U.min()),
+                                                "max": int(U.max())},
+           "roofline_hbm": hbm, "roofline_fp4": fp4, "status": status, "gpu_launches_per_chunk": launches,
+           "timed": "%d pass(es) over the whole sequence after one eager and one graph warm-up pass" % reps}
+    if pk:
+        tot = sum(sum(v) for v in pk.values())
+        out["breakdown_ms_per_chunk"] = {n: round(sum(v), 3) for n, v in pk.items()}
+        out["breakdown_share"] = {n: round(sum(v) / tot, 4) for n, v in pk.items()}
+        out["breakdown_note"] = ("one chunk (40 layers) of a second graph with event probes around each call; "
+                                 "the combine runs as its own call there (the same kernel the fused call launches)")
+    return out
+
+
+def run_keepset(args, device):
+    import torch
+    from synth.keepset import KeepSetArena
+    t0 = time.perf_counter()
+    ks = KeepSetArena(device)
+    build_s = time.perf_counter() - t0
+    out = {"arena": {"slots": ks.arena.num_slots, "gb": round(ks.arena.num_slots * EXPERT_BYTES / 1e9, 2),
+                     "build_s": round(build_s, 1)}}
+    out["keepset_decode"] = run_keepset_decode(ks, 1, args, device)
+    out["keepset_verify"] = run_keepset_decode(ks, 16, args, device)
+    if not args.no_long_prefill:
+        out["long_prefill"] = run_long_prefill(ks, args, device)
+    ks.release()
+    del ks
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------------------- cb3 experts
 
 CB3_SLOT_BYTES = 13_426_688
@@ -533,13 +816,82 @@ def cpu_baseline_block():
         value = tokens / max(r[1] for r in res)
         sample = ("%d tokens on %d host cores, token-sharded (2 per process, the slowest process's time), "
                   "plus %d tokens on 1 core (%.4f tokens/s, %.1f s); full layer per token: exact router over 384 "
-                  "experts, 6 experts' SwiGLU FFN in fp64, combine; plain single-threaded C per process"
+                  "experts, 6 experts' SwiGLU FFN in sequential fp32, fixed-order combine; plain single-threaded C per process"
                   % (tokens, cores, n, single, el))
         return {"value": round(value, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
                 "single_core_value": round(single, 4)}
     except Exception as exc:   # the single-core figure still stands
         return {"value": round(single, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                 "sample": "%d tokens of the same workload on 1 core, %.1f s (sharded run failed: %s)" % (n, el, exc)}
+
+
+def _oracle_token_layer(x_row, seed_layer, table, bias):
+    """Time the oracle on one token through one layer (exact router over the 384 experts, the
+    chosen experts' fp32 SwiGLU FFNs, fixed-order combine); expert tensors are generated
+    beforehand, outside the timing.  Returns seconds."""
+    import oracle
+    from synth import tensors as syn
+    r = oracle.route_topk(x_row[None], _WR_CACHE.setdefault(seed_layer, syn.router_weight(0, seed_layer, E, D)),
+                          bias, table, K)
+    experts = {int(e): syn.expert_tensors(0, seed_layer, int(e), D, F, *SCALE) for e in r["ids"][0] if e >= 0}
+    t0 = time.perf_counter()
+    rr = oracle.route_topk(x_row[None], _WR_CACHE[seed_layer], bias, table, K)
+    z = np.zeros((K, D), np.float32)
+    for j in range(K):
+        e = int(rr["ids"][0, j])
+        if e >= 0:
+            _, z[j] = oracle.expert_ffn_f32(x_row, experts[e])
+    oracle.combine_f32(z, rr["weights"][0])
+    return time.perf_counter() - t0
+
+
+_WR_CACHE = {}
+
+
+def _oracle_configs_shard(i):
+    """One host core's sample for the multi-layer and prefill workloads (a spawned process):
+    one token-layer each of the keep-set decode, the T=4096 prefill chunk and the long
+    prefill, teacher-forced (each layer's input is a fresh synthetic token; the oracle's cost
+    does not depend on the values)."""
+    from synth import tensors as syn
+    from synth.keepset import KEEP, LAYERS, ZIPF_S
+    tabs = syn.keepset_slot_tables(0, LAYERS, E, KEEP, ZIPF_S)
+    l = (7 * i + 3) % LAYERS
+    out = {}
+    x = syn.activations(0, 0, 1, D, start_token=i, stream=15)
+    out["keepset"] = _oracle_token_layer(x[0], l, tabs[l], None)
+    x = syn.activations(0, 0, 1, D, start_token=(97 * i) % PREFILL_T, stream=9)
+    out["prefill"] = _oracle_token_layer(x[0], 0, syn.permuted_slot_table(0, 0, E),
+                                         syn.zipf_score_bias(0, 0, E, *PREFILL_BIAS))
+    c = i % LONG_CHUNKS
+    x = syn.activations(0, 0, 1, D, start_token=c * LONG_T + (131 * i) % LONG_T, stream=13)
+    out["long"] = _oracle_token_layer(x[0], l, tabs[l], syn.zipf_score_bias(0, l, E, *LONG_BIAS))
+    return out
+
+
+def config_cpu_baselines():
+    """The oracle's host throughput for the keep-set decode/verify, the prefill chunk and the
+    long prefill: every host core (spawned processes) times one token-layer of each; a
+    workload's rate is the sampled token-layers over the slowest process's time, divided by
+    the layers a token passes through.  The full workloads (20 steps x 40 layers, 4,096
+    tokens, 4 x 8,192 tokens x 40 layers) would take hours on the host: these figures are
+    linear extrapolations from the sample and say so."""
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(cores) as pool:
+        res = pool.map(_oracle_configs_shard, range(cores))
+    out = {}
+    for key, layers, name in (("keepset", 40, "keepset_decode"), ("prefill", 1, "prefill"), ("long", 40, "long_prefill")):
+        t = [r[key] for r in res]
+        rate = len(t) / max(t)                       # token-layers per second over all cores
+        out[name] = {"value": round(rate / layers, 5), "unit": "tokens/s (through all %d layer%s)"
+                     % (layers, "s" if layers > 1 else ""), "cores": cores, "kind": "oracle",
+                     "extrapolated": True,
+                     "sample": "%d token-layers, one per host core in parallel (median %.2f s each, slowest %.2f s); "
+                               "rate = token-layers / slowest time / %d layers, extrapolated linearly to the whole "
+                               "workload" % (len(t), statistics.median(t), max(t), layers)}
+    out["keepset_verify"] = dict(out["keepset_decode"])     # same per-token-layer work in the oracle
+    return out
 
 
 def run_reference(args, rank, world):
@@ -555,7 +907,7 @@ def run_reference(args, rank, world):
     tps = 1.0 / statistics.mean(times)
     return {"metric": METRIC, "value": round(tps, 4), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * per_step / tps, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle FFN), exact-then-fp32 router",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 (oracle FFN: sequential fp32 sums), exact-then-fp32 router",
             "data": "synthetic", "config": dict(CONFIG, parallelism="single host core"), "impl": "reference",
             "cpu_baseline": {"value": round(tps, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": "%d tokens per step of the same workload" % per_step},
@@ -574,6 +926,11 @@ def main():
     ap.add_argument("--tokens", type=int, default=1000, help="tokens per step")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-chunk measurement")
     ap.add_argument("--no-cb3", action="store_true", help="skip the cb3-format decode measurement")
+    ap.add_argument("--no-keepset", action="store_true",
+                    help="skip the 40-layer keep-set measurements (they need a 115.8 GB arena)")
+    ap.add_argument("--no-long-prefill", action="store_true", help="skip the 4 x 8,192-token long prefill")
+    ap.add_argument("--keepset-only", action="store_true",
+                    help="measure only the 40-layer keep-set workloads (profiling runs)")
     ap.add_argument("--cb3-only", action="store_true",
                     help="measure only the cb3-format decode leg (profiling runs; the FP4 layer runs once, eagerly, "
                          "for the comparison)")
@@ -606,6 +963,15 @@ def main():
                    "prefill": run_prefill(build_workload(dev), args, dev)}
             print(json.dumps(out), flush=True)
         return 0
+    if args.keepset_only:
+        if rank == 0:
+            import torch
+            torch.cuda.set_device(local_rank)
+            dev = torch.device("cuda", local_rank)
+            out = {"metric": "40-layer keep-set tokens/s", "impl": "ours"}
+            out.update(run_keepset(args, dev))
+            print(json.dumps(out), flush=True)
+        return 0
     if args.cb3_only:
         if rank == 0:
             import torch
@@ -625,9 +991,18 @@ def main():
     if rank == 0 and out is not None and not args.no_cb3 and E == 384:
         import torch
         out["cb3"] = run_cb3(w, args, torch.device("cuda", local_rank))
+    if rank == 0 and out is not None and not args.no_keepset and E == 384:
+        import torch
+        del w["arena"], w["layer"]
+        torch.cuda.empty_cache()
+        out.update(run_keepset(args, torch.device("cuda", local_rank)))
     if rank == 0 and out is not None:
         if not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline_block()
+            if E == 384:
+                for name, blk in config_cpu_baselines().items():
+                    if isinstance(out.get(name), dict):
+                        out[name]["cpu_baseline"] = blk
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -20,7 +20,7 @@ __all__ = [
     "moe_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_route_topk_noalloc", "moe_permute",
     "moe_expert_ffn_fp4", "moe_combine", "moe_residency_bias", "moe_split_waves", "moe_gather_experts", "moe_status_str",
     "moe_cb3_slot_bytes", "moe_pack_cb3", "moe_expert_ffn_cb3", "MOE_STATUS_CB3_ROW",
-    "moe_kernel_launches", "moe_workspace_set_wait_limit", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
+    "moe_kernel_launches", "moe_workspace_set_wait_limit", "moe_residual_rmsnorm", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
     "MOE_STATUS_FEW_RESIDENT", "MOE_STATUS_BAD_SLOT", "MOE_STATUS_TIMEOUT", "DECODE_MAX_T",
 ]
 
@@ -68,6 +68,7 @@ _SIG = {
     "moe_split_waves": (ctypes.c_int, [_P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
     "moe_gather_experts": (ctypes.c_int, [_P, _P, _P, _I] + [_P] * 6),
     "moe_route_topk_noalloc": (ctypes.c_int, [_P, _I] + [_P] * 9),
+    "moe_residual_rmsnorm": (ctypes.c_int, [_I, _I, _P, _P, _P, ctypes.c_float, _P, _P]),
     "moe_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_kernel_launches": (ctypes.c_uint64, []),
 }
@@ -177,6 +178,12 @@ def moe_expert_ffn_fp4(dims, arena: moe_arena, T, x, topk_ids, topk_slot, topk_w
         ctypes.byref(_dims(dims)), ctypes.byref(arena), int(T), _ptr(x), _ptr(topk_ids), _ptr(topk_slot),
         _ptr(topk_w), _ptr(group_offsets), _ptr(row_src), _ptr(row_dst), int(flags), _ptr(rows_out), _ptr(y),
         _ptr(dev_status), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_residual_rmsnorm(T, d, x, y, eps, x_next, stream=None):
+    """x_next = bf16(RMSNorm(x + y)) (unit weight), the chaining step of multi-layer workloads."""
+    _check("moe_residual_rmsnorm", lib().moe_residual_rmsnorm(int(T), int(d), _ptr(x), _ptr(y), ctypes.c_float(eps),
+                                                              _ptr(x_next), _stream(stream)))
 
 
 def moe_combine(dims, T, rows, row_dst, topk_w, y, stream=None):

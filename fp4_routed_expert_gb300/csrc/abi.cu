@@ -43,6 +43,7 @@ int launch_split_waves(const moe_dims* m, int T, const int32_t* ids, const int32
 int launch_gather_experts(const moe_arena* ar, const uint8_t* store, int n_store, const int32_t* missing,
                           const int32_t* n_missing, const int32_t* expert_to_slot, int32_t* resident_expert,
                           int32_t* status, cudaStream_t st, int num_sms);
+int launch_residual_rmsnorm(int T, int d, const uint16_t* x, const uint16_t* y, float eps, uint16_t* out, cudaStream_t st);
 int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                       const int32_t* offsets, const int32_t* row_src, float* rows_out, int32_t* status, char* ws,
                       const WsLayout& L, cudaStream_t st, int num_sms);
@@ -307,6 +308,15 @@ int moe_expert_ffn_cb3(const moe_dims* dims, const moe_arena* cb3_arena, int32_t
     if (rc) return rc;
     return launch_cb3_ffn(dims, cb3_arena, T, x, topk_slot, topk_w, y, dev_status, static_cast<char*>(ws), L,
                           (cudaStream_t)stream, num_sms_of_current_device());
+}
+
+int moe_residual_rmsnorm(int32_t T, int32_t d, const uint16_t* x, const uint16_t* y, float eps, uint16_t* x_next,
+                         void* stream) {
+    if (T < 0) return MOE_ERR_TOKENS;
+    if (d <= 0 || d > 65536) return MOE_ERR_DIMS;
+    if (!(eps >= 0.0f) || !(eps < 3.0e38f)) return MOE_ERR_DIMS;
+    if (T > 0 && (!x || !y || !x_next)) return MOE_ERR_NULL;
+    return launch_residual_rmsnorm(T, d, x, y, eps, x_next, (cudaStream_t)stream);
 }
 
 uint64_t moe_kernel_launches(void) { return fp4moe::g_kernel_launches.load(std::memory_order_relaxed); }

@@ -276,6 +276,13 @@ int moe_expert_ffn_cb3(const moe_dims* dims, const moe_arena* cb3_arena, int32_t
                        const int32_t* topk_slot, const float* topk_w, uint16_t* y, int32_t* dev_status, void* ws,
                        size_t ws_bytes, void* stream);
 
+/* Layer chaining for multi-layer workloads (a harness step, not part of the routed-expert
+ * layer): x_next[t] = bf16_RNE( v / sqrt(mean_i(v_i^2) + eps) ), v = x[t] + y[t] in fp32 (unit
+ * RMSNorm weight).  x, y, x_next bf16 [T, d]; x_next may alias x.  One kernel, one block per
+ * token.  eps must be finite and >= 0 (else MOE_ERR_DIMS); 1 <= d <= 65536. */
+int moe_residual_rmsnorm(int32_t T, int32_t d, const uint16_t* x, const uint16_t* y, float eps, uint16_t* x_next,
+                         void* stream);
+
 /* Number of kernels this library has enqueued in this process so far (every entry point
  * above counts the kernels it launches).  A call captured into a CUDA graph counts once, at
  * capture, so the difference across a capture is the kernel count of one graph replay.

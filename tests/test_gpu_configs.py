@@ -14,8 +14,8 @@ import torch
 import fp4_routed_expert_gb300 as moe
 from fp4_routed_expert_gb300.layer import Arena, MoeLayer
 import oracle
-from synth import gpu as sgpu
 from synth import tensors as syn
+from synth.keepset import D, E, F, K, KEEP, LAYERS, SCALE, KeepSetArena
 
 from workloads import bits_to_torch, elem_rel_err, row_rel_err
 
@@ -23,26 +23,12 @@ pytestmark = pytest.mark.gpu
 
 TOL = 1e-2
 DEV = "cuda"
-D, F, E, K, LAYERS, KEEP = 5120, 2304, 384, 6, 40, 154
-SCALE = (-10, -6)
 
 
-class KeepSet:
+class KeepSet(KeepSetArena):
     def __init__(self):
         torch.cuda.empty_cache()
-        self.tabs = syn.keepset_slot_tables(0, LAYERS, E, KEEP, 1.1)
-        self.dims = moe.moe_dims(D, F, E, K)
-        self.arena = Arena(self.dims, LAYERS * KEEP, DEV)
-        stage = sgpu.ExpertStaging(D, F, DEV)
-        for l in range(LAYERS):
-            for e in range(E):
-                s = int(self.tabs[l, e])
-                if s >= 0:
-                    self.arena.pack(s, stage.fill(0, l, e, *SCALE))
-        torch.cuda.synchronize()
-        self.wr_bits = [syn.router_weight(0, l, E, D) for l in range(LAYERS)]
-        self.wr = [bits_to_torch(b, DEV) for b in self.wr_bits]
-        self.tab_dev = [torch.from_numpy(np.ascontiguousarray(self.tabs[l])).to(DEV) for l in range(LAYERS)]
+        super().__init__(DEV)
 
     def oracle_layer(self, l, x_bits, tokens, bias=None):
         """Oracle routing (all given tokens) and outputs of the sampled tokens."""
