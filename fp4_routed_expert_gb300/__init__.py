@@ -68,7 +68,7 @@ _SIG = {
     "moe_split_waves": (ctypes.c_int, [_P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
     "moe_gather_experts": (ctypes.c_int, [_P, _P, _P, _I] + [_P] * 6),
     "moe_route_topk_noalloc": (ctypes.c_int, [_P, _I] + [_P] * 9),
-    "moe_residual_rmsnorm": (ctypes.c_int, [_I, _I, _P, _P, _P, ctypes.c_float, _P, _P]),
+    "moe_residual_rmsnorm": (ctypes.c_int, [_I, _I, _P, _P, ctypes.c_float, _P, _P]),
     "moe_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_kernel_launches": (ctypes.c_uint64, []),
 }
