@@ -468,7 +468,7 @@ def run_keepset_decode(ks, T, args, device):
     from synth.keepset import LAYERS, KEEP, bits_to_device
     S = KS_DECODE_STEPS
     layer = MoeLayer(D, F, E, K, T, ks.arena, device)
-    xs = bits_to_device(syn.activations(0, 0, S * T, D, stream=15 if T == 1 else 16), device).view(S, T, D)
+    xs = bits_to_device(syn.activations(0, 0, S * T, D, stream=15 if T == 1 else 14), device).view(S, T, D)
     x = torch.empty((T, D), dtype=torch.bfloat16, device=device)
     y = torch.empty((T, D), dtype=torch.bfloat16, device=device)
     ids_log = torch.empty((S, LAYERS, T, K), dtype=torch.int32, device=device)
