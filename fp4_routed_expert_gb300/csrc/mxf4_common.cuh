@@ -1,0 +1,236 @@
+// mxf4_common.cuh -- pieces shared by the tensor-core expert FFN kernels (sm_103a): tcgen05 /
+// TMEM wrappers, the MXFP4 multi-term quantisers of activations, the activation block layout
+// and the gpu-scope counter operations.
+#pragma once
+
+#include "moe_internal.cuh"
+
+namespace fp4moe {
+
+constexpr int kTerms = 4;
+constexpr int kBM = 128;              // weight rows per tile
+constexpr int kKB = 256;              // K elements per K block
+constexpr int kKBytes = 128;          // code bytes per row per stage
+constexpr int kThreadsGemm = 6 * 32;
+constexpr int kTmemCols = 512;
+constexpr int kSfRing = 2;                // scale buffers in TMEM (tcgen05.cp and MMAs run in issue order)
+constexpr int kDecodeNT = 16;             // decode tile rows at most: the tokens of x; a key's pairs of h
+constexpr int kMaxDecodePairs = kTcDecodeMaxKeys;   // decode calls on the tensor cores: T*k <= 128
+
+enum { kModeGateUp = 0, kModeDown = 1 };
+enum { kRegimeDecode = 0, kRegimePrefill = 1 };
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// K-major operand tile, 128-byte rows, SWIZZLE_128B, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t a) {
+    return (uint64_t)((a & 0x3FFFF) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Scale atom: 32 rows of 16 bytes, no swizzle, core matrices (8 rows) 128 bytes apart.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t a) {
+    return (uint64_t)((a & 0x3FFFF) >> 4) | ((uint64_t)(128 >> 4) << 32) | (1ull << 46);
+}
+// Instruction descriptor of kind::mxf4 (e2m1 x e2m1, UE8M0 scales, K-major A and B).
+// sf_id selects the first of the two scale bytes used by one K=64 MMA: 0 or 2.
+__device__ __forceinline__ uint32_t idesc_mxf4(int n, int sf_id) {
+    return ((uint32_t)(sf_id & 3) << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(kBM >> 4) << 24) | ((uint32_t)(sf_id & 3) << 29);
+}
+__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Asynchronous 32x32b.x16 / .x8 loads: the registers are valid only after tc_wait_ld on them
+// (the wait takes them as operands, so no use can be scheduled before it).
+__device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+__device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[8]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+                 :
+                 : "memory");
+}
+
+// ------------------------------------------------------------------ MXFP4 multi-term quantiser
+
+// Nearest e2m1 magnitude code of |v| <= 6 (0, .5, 1, 1.5, 2, 3, 4, 6).
+__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
+    return (a >= 0.25f) + (a >= 0.75f) + (a >= 1.25f) + (a >= 1.75f) + (a >= 2.5f) + (a >= 3.5f) + (a >= 5.0f);
+}
+__device__ __forceinline__ float e2m1_mag_value(uint32_t c) {
+    return c < 4 ? 0.5f * (float)c : (float)(1u << ((c >> 1) - 1)) * (1.0f + 0.5f * (float)(c & 1u));
+}
+
+// One warp quantises one 32-element block (lane i holds element i) into kTerms MXFP4
+// terms.  Term t takes the residual r left by terms 0..t-1: scale 2^e with e the smallest
+// integer such that max|r| <= 6 * 2^e (clamped to the UE8M0 range), codes = nearest e2m1
+// of r/2^e.  Lane 0 receives the 16 code bytes of every term in codes[t]; every lane
+// receives the scale bytes.
+__device__ __forceinline__ void warp_quantize32(float v, int lane, uint4* codes /*[kTerms], lane 0*/,
+                                                uint32_t* scales /*[kTerms]*/) {
+#pragma unroll
+    for (int t = 0; t < kTerms; ++t) {
+        // max |v| over the warp: magnitudes order like their bit patterns as unsigned integers
+        const uint32_t u = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
+        int e = -127;
+        if ((u >> 23) != 0u) {                                   // normal amax; subnormal residuals are dropped
+            const int e0 = (int)((u >> 23) & 0xFF) - 127;        // floor(log2 amax)
+            const float m = __uint_as_float((u & 0x007FFFFFu) | 0x3F800000u);   // amax / 2^e0 in [1, 2)
+            e = (m <= 1.5f) ? e0 - 2 : e0 - 1;                   // amax <= 6 * 2^e, minimal e
+        }
+        e = max(-127, min(127, e));
+        scales[t] = (uint32_t)(e + 127);
+        const float inv = (e >= -126 && e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : 0.f;   // 2^-e
+        const float sc = (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+        const float q = v * inv;
+        const uint32_t c = e2m1_mag_code(fminf(fabsf(q), 6.0f));
+        const float val = e2m1_mag_value(c) * sc;
+        const bool neg = q < 0.f && c;
+        v -= neg ? -val : val;
+        uint32_t nib = (c | (neg ? 8u : 0u)) << (4 * (lane & 7));
+        nib |= __shfl_xor_sync(0xffffffffu, nib, 1);
+        nib |= __shfl_xor_sync(0xffffffffu, nib, 2);
+        nib |= __shfl_xor_sync(0xffffffffu, nib, 4);              // lanes 8w.. hold word w
+        const uint32_t w1 = __shfl_sync(0xffffffffu, nib, 8), w2 = __shfl_sync(0xffffffffu, nib, 16),
+                       w3 = __shfl_sync(0xffffffffu, nib, 24);
+        codes[t] = make_uint4(nib, w1, w2, w3);
+    }
+}
+
+// The same quantisation by one thread for the 32 values v (registers): the code words of term
+// t in w[t][0..3] (element i in word i/8, nibble i%8), its scale byte in sc[t].
+__device__ __forceinline__ void thread_quantize32(float (&v)[32], uint32_t (&w)[kTerms][4], uint32_t (&sc)[kTerms]) {
+#pragma unroll
+    for (int t = 0; t < kTerms; ++t) {
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        int e = -127;
+        const uint32_t u = __float_as_uint(amax);
+        if ((u >> 23) != 0u) {
+            const int e0 = (int)((u >> 23) & 0xFF) - 127;
+            const float m = __uint_as_float((u & 0x007FFFFFu) | 0x3F800000u);
+            e = (m <= 1.5f) ? e0 - 2 : e0 - 1;
+        }
+        e = max(-127, min(127, e));
+        sc[t] = (uint32_t)(e + 127);
+        const float inv = (e >= -126 && e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : 0.f;
+        const float scl = (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) w[t][k] = 0u;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float q = v[i] * inv;
+            const uint32_t c = e2m1_mag_code(fminf(fabsf(q), 6.0f));
+            const float val = e2m1_mag_value(c) * scl;
+            const bool neg = q < 0.f && c;
+            v[i] -= neg ? -val : val;
+            w[t][i >> 3] |= (c | (neg ? 8u : 0u)) << (4 * (i & 7));
+        }
+    }
+}
+
+// The same quantisation by the 8 lanes of an octet (lanes 8o..8o+7 of a warp; lane s = lane & 7
+// holds elements 4s..4s+3 in v): the 32-bit code word w = s/2 of term t (elements 8w..8w+7)
+// lands in word[t] of the even lane s = 2w, every lane of the octet gets the scale bytes.  The
+// whole warp calls it (the shuffles stay inside each octet).
+__device__ __forceinline__ void octet_quantize32(float (&v)[4], int lane, uint32_t (&word)[kTerms],
+                                                 uint32_t (&sc)[kTerms]) {
+#pragma unroll
+    for (int t = 0; t < kTerms; ++t) {
+        uint32_t u = __float_as_uint(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+        u = max(u, __shfl_xor_sync(0xffffffffu, u, 1));
+        u = max(u, __shfl_xor_sync(0xffffffffu, u, 2));
+        u = max(u, __shfl_xor_sync(0xffffffffu, u, 4));
+        int e = -127;
+        if ((u >> 23) != 0u) {
+            const int e0 = (int)((u >> 23) & 0xFF) - 127;
+            const float m = __uint_as_float((u & 0x007FFFFFu) | 0x3F800000u);
+            e = (m <= 1.5f) ? e0 - 2 : e0 - 1;
+        }
+        e = max(-127, min(127, e));
+        sc[t] = (uint32_t)(e + 127);
+        const float inv = (e >= -126 && e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : 0.f;
+        const float scl = (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+        uint32_t half = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float q = v[i] * inv;
+            const uint32_t c = e2m1_mag_code(fminf(fabsf(q), 6.0f));
+            const float val = e2m1_mag_value(c) * scl;
+            const bool neg = q < 0.f && c;
+            v[i] -= neg ? -val : val;
+            half |= (c | (neg ? 8u : 0u)) << (4 * i);
+        }
+        // elements 4s..4s+3 are nibbles 4(s&1).. of word s/2
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, half, 1);
+        word[t] = (lane & 1) ? 0u : (half | (other << 16));
+    }
+}
+
+// Padded index of h value i (0..63) of column c in the gate/up epilogue's shared tile: the
+// 32-value blocks start 33 words apart, so threads reading one block each hit distinct banks.
+__device__ __forceinline__ int hidx(int c, int i) { return c * 66 + (i >> 5) * 33 + (i & 31); }
+
+// Activation operands are kept in blocks: block (tile t, K block kb) holds the kTerms x NT
+// rows of B (row r' = term*NT + row, codes pre-swizzled, 128 bytes per row) followed by their
+// scale atoms, 1 KB per 128 rows of r'; the KB blocks of a tile are consecutive.
+__host__ __device__ constexpr int act_block_bytes(int NT) { return kTerms * NT * 128 + (kTerms * NT + 127) / 128 * 1024; }
+__device__ __forceinline__ int64_t act_code_off(int tile, int kb, int term, int row, int chunk, int NT, int KB) {
+    return ((int64_t)tile * KB + kb) * act_block_bytes(NT) + (term * NT + row) * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+__device__ __forceinline__ int64_t act_scale_off(int tile, int kb, int term, int row, int j /*0..7*/, int NT, int KB) {
+    const int rr = term * NT + row;
+    const int r = rr & 127;
+    return ((int64_t)tile * KB + kb) * act_block_bytes(NT) + kTerms * NT * 128 + (rr >> 7) * 1024 + (j >> 2) * 512 +
+           (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
+}
+
+// ------------------------------------------------------------------ gpu-scope counters
+
+__device__ __forceinline__ int ld_acquire(const int32_t* a) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ int atom_add_acq_rel(int32_t* a, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void red_add_release(int32_t* a, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+}  // namespace fp4moe

@@ -27,180 +27,9 @@
 // Every wait is bounded; a timeout sets MOE_STATUS_TIMEOUT and the CTA drains and exits.
 #include <cuda.h>
 
-#include "moe_internal.cuh"
+#include "mxf4_common.cuh"
 
 namespace fp4moe {
-
-constexpr int kTerms = 4;
-constexpr int kBM = 128;              // weight rows per tile
-constexpr int kKB = 256;              // K elements per K block
-constexpr int kKBytes = 128;          // code bytes per row per stage
-constexpr int kThreadsGemm = 6 * 32;
-constexpr int kTmemCols = 512;
-constexpr int kSfRing = 2;                // scale buffers in TMEM (tcgen05.cp and MMAs run in issue order)
-constexpr int kDecodeNT = 16;             // decode tile rows at most: the tokens of x; a key's pairs of h
-constexpr int kMaxDecodePairs = 128;      // decode calls on the tensor cores: T*k <= 128
-
-enum { kModeGateUp = 0, kModeDown = 1 };
-enum { kRegimeDecode = 0, kRegimePrefill = 1 };
-
-// ------------------------------------------------------------------ PTX wrappers
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// K-major operand tile, 128-byte rows, SWIZZLE_128B, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t a) {
-    return (uint64_t)((a & 0x3FFFF) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
-// Scale atom: 32 rows of 16 bytes, no swizzle, core matrices (8 rows) 128 bytes apart.
-__device__ __forceinline__ uint64_t desc_sf(uint32_t a) {
-    return (uint64_t)((a & 0x3FFFF) >> 4) | ((uint64_t)(128 >> 4) << 32) | (1ull << 46);
-}
-// Instruction descriptor of kind::mxf4 (e2m1 x e2m1, UE8M0 scales, K-major A and B).
-// sf_id selects the first of the two scale bytes used by one K=64 MMA: 0 or 2.
-__device__ __forceinline__ uint32_t idesc_mxf4(int n, int sf_id) {
-    return ((uint32_t)(sf_id & 3) << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
-           ((uint32_t)(kBM >> 4) << 24) | ((uint32_t)(sf_id & 3) << 29);
-}
-__device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
-        "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-// Asynchronous 32x32b.x16 / .x8 loads: the registers are valid only after tc_wait_ld on them
-// (the wait takes them as operands, so no use can be scheduled before it).
-__device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[16]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-                 :
-                 : "memory");
-}
-__device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[8]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                 : "r"(taddr));
-}
-__device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[8]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
-                 :
-                 : "memory");
-}
-
-// ------------------------------------------------------------------ MXFP4 multi-term quantiser
-
-// Nearest e2m1 magnitude code of |v| <= 6 (0, .5, 1, 1.5, 2, 3, 4, 6).
-__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
-    return (a >= 0.25f) + (a >= 0.75f) + (a >= 1.25f) + (a >= 1.75f) + (a >= 2.5f) + (a >= 3.5f) + (a >= 5.0f);
-}
-__device__ __forceinline__ float e2m1_mag_value(uint32_t c) {
-    return c < 4 ? 0.5f * (float)c : (float)(1u << ((c >> 1) - 1)) * (1.0f + 0.5f * (float)(c & 1u));
-}
-
-// One warp quantises one 32-element block (lane i holds element i) into kTerms MXFP4
-// terms.  Term t takes the residual r left by terms 0..t-1: scale 2^e with e the smallest
-// integer such that max|r| <= 6 * 2^e (clamped to the UE8M0 range), codes = nearest e2m1
-// of r/2^e.  Lane 0 receives the 16 code bytes of every term in codes[t]; every lane
-// receives the scale bytes.
-__device__ __forceinline__ void warp_quantize32(float v, int lane, uint4* codes /*[kTerms], lane 0*/,
-                                                uint32_t* scales /*[kTerms]*/) {
-#pragma unroll
-    for (int t = 0; t < kTerms; ++t) {
-        // max |v| over the warp: magnitudes order like their bit patterns as unsigned integers
-        const uint32_t u = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
-        int e = -127;
-        if ((u >> 23) != 0u) {                                   // normal amax; subnormal residuals are dropped
-            const int e0 = (int)((u >> 23) & 0xFF) - 127;        // floor(log2 amax)
-            const float m = __uint_as_float((u & 0x007FFFFFu) | 0x3F800000u);   // amax / 2^e0 in [1, 2)
-            e = (m <= 1.5f) ? e0 - 2 : e0 - 1;                   // amax <= 6 * 2^e, minimal e
-        }
-        e = max(-127, min(127, e));
-        scales[t] = (uint32_t)(e + 127);
-        const float inv = (e >= -126 && e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : 0.f;   // 2^-e
-        const float sc = (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
-        const float q = v * inv;
-        const uint32_t c = e2m1_mag_code(fminf(fabsf(q), 6.0f));
-        const float val = e2m1_mag_value(c) * sc;
-        const bool neg = q < 0.f && c;
-        v -= neg ? -val : val;
-        uint32_t nib = (c | (neg ? 8u : 0u)) << (4 * (lane & 7));
-        nib |= __shfl_xor_sync(0xffffffffu, nib, 1);
-        nib |= __shfl_xor_sync(0xffffffffu, nib, 2);
-        nib |= __shfl_xor_sync(0xffffffffu, nib, 4);              // lanes 8w.. hold word w
-        const uint32_t w1 = __shfl_sync(0xffffffffu, nib, 8), w2 = __shfl_sync(0xffffffffu, nib, 16),
-                       w3 = __shfl_sync(0xffffffffu, nib, 24);
-        codes[t] = make_uint4(nib, w1, w2, w3);
-    }
-}
-
-// The same quantisation by one thread for the 32 values v (registers): the code words of term
-// t in w[t][0..3] (element i in word i/8, nibble i%8), its scale byte in sc[t].
-__device__ __forceinline__ void thread_quantize32(float (&v)[32], uint32_t (&w)[kTerms][4], uint32_t (&sc)[kTerms]) {
-#pragma unroll
-    for (int t = 0; t < kTerms; ++t) {
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        int e = -127;
-        const uint32_t u = __float_as_uint(amax);
-        if ((u >> 23) != 0u) {
-            const int e0 = (int)((u >> 23) & 0xFF) - 127;
-            const float m = __uint_as_float((u & 0x007FFFFFu) | 0x3F800000u);
-            e = (m <= 1.5f) ? e0 - 2 : e0 - 1;
-        }
-        e = max(-127, min(127, e));
-        sc[t] = (uint32_t)(e + 127);
-        const float inv = (e >= -126 && e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : 0.f;
-        const float scl = (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) w[t][k] = 0u;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float q = v[i] * inv;
-            const uint32_t c = e2m1_mag_code(fminf(fabsf(q), 6.0f));
-            const float val = e2m1_mag_value(c) * scl;
-            const bool neg = q < 0.f && c;
-            v[i] -= neg ? -val : val;
-            w[t][i >> 3] |= (c | (neg ? 8u : 0u)) << (4 * (i & 7));
-        }
-    }
-}
-
-// Padded index of h value i (0..63) of column c in the gate/up epilogue's shared tile: the
-// 32-value blocks start 33 words apart, so threads reading one block each hit distinct banks.
-__device__ __forceinline__ int hidx(int c, int i) { return c * 66 + (i >> 5) * 33 + (i & 31); }
-
-// Activation operands are kept in blocks: block (tile t, K block kb) holds the kTerms x NT
-// rows of B (row r' = term*NT + row, codes pre-swizzled, 128 bytes per row) followed by their
-// scale atoms, 1 KB per 128 rows of r'; the KB blocks of a tile are consecutive.
-__host__ __device__ constexpr int act_block_bytes(int NT) { return kTerms * NT * 128 + (kTerms * NT + 127) / 128 * 1024; }
-__device__ __forceinline__ int64_t act_code_off(int tile, int kb, int term, int row, int chunk, int NT, int KB) {
-    return ((int64_t)tile * KB + kb) * act_block_bytes(NT) + (term * NT + row) * 128 + (((chunk & 7) ^ (row & 7)) << 4);
-}
-__device__ __forceinline__ int64_t act_scale_off(int tile, int kb, int term, int row, int j /*0..7*/, int NT, int KB) {
-    const int rr = term * NT + row;
-    const int r = rr & 127;
-    return ((int64_t)tile * KB + kb) * act_block_bytes(NT) + kTerms * NT * 128 + (rr >> 7) * 1024 + (j >> 2) * 512 +
-           (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
-}
 
 // Prefill activations -> kTerms MXFP4 terms in tile layout, one thread per (token t, 32-element
 // block b): the block is quantised once and written into the tile row of each of the token's k
@@ -362,20 +191,6 @@ __device__ __forceinline__ bool unit_info(const FfnParams& p, const PhaseParams&
     return u.slot >= 0 && u.slot < p.num_slots;
 }
 
-__device__ __forceinline__ int ld_acquire(const int32_t* a) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
-    return v;
-}
-__device__ __forceinline__ int atom_add_acq_rel(int32_t* a, int v) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
-    return old;
-}
-__device__ __forceinline__ void red_add_release(int32_t* a, int v) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // The whole expert FFN in one persistent launch (one CTA per SM, every CTA resident).  The
 // producer takes units from the work list; a down unit needs the h rows of its key (decode:
@@ -729,6 +544,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
             int stage = 0, sfring = 0, acc = 0;
             uint32_t phase = 0, aphase = 0;
             const uint32_t idesc_lo = idesc_mxf4(C::kN, 0), idesc_hi = idesc_mxf4(C::kN, 2);
+            // Decode: every gate/up unit multiplies the same x tile, so the scale atoms of its K
+            // blocks are copied into TMEM once (by the CTA's first gate/up unit, into columns
+            // after the scale ring) when they fit there; later units only copy A scales.
+            const uint32_t xsf = tmem + 256 + kSfRing * C::kSfCols;
+            const bool xsf_fits = p.regime == kRegimeDecode &&
+                                  256 + kSfRing * C::kSfCols + p.ph[0].kblocks * 8 * C::kGroups <= kTmemCols;
+            bool xsf_done = false;
             while (true) {
                 int unit = -1;
                 if (mbar_wait(smem_u32(&uqfull[qi]), qphase, abortp)) unit = uq[qi];
@@ -736,6 +558,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                 if (++qi == kUQ) { qi = 0; qphase ^= 1u; }
                 if (unit < 0) break;
                 const int KB = p.ph[unit < n0 ? 0 : 1].kblocks;
+                const bool use_xsf = xsf_fits && unit < n0;
                 if (!mbar_wait(smem_u32(&tempty[acc]), aphase ^ 1u, abortp)) {
                     atomicOr(p.status, MOE_STATUS_TIMEOUT);
                     *abortp = 1;
@@ -762,12 +585,15 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                         const uint32_t sb = smem_u32(st + C::kKPS * kTileBytes + i * C::kBBlk);
                         const uint32_t ssfa = sa + kTileCodeBytes, ssfb = sb + C::kBCodes;
                         const uint32_t sfcol = tmem + 256 + sfring * C::kSfCols;
+                        const uint32_t sfb = use_xsf ? xsf + (s * C::kKPS + i) * 8 * C::kGroups : sfcol + 8;
                         tc_cp_sf(sfcol + 0, desc_sf(ssfa));
                         tc_cp_sf(sfcol + 4, desc_sf(ssfa + 512));
+                        if (!(use_xsf && xsf_done)) {
 #pragma unroll
-                        for (int g = 0; g < C::kGroups; ++g) {
-                            tc_cp_sf(sfcol + 8 + 8 * g, desc_sf(ssfb + g * 1024));
-                            tc_cp_sf(sfcol + 8 + 8 * g + 4, desc_sf(ssfb + g * 1024 + 512));
+                            for (int g = 0; g < C::kGroups; ++g) {
+                                tc_cp_sf(sfb + 8 * g, desc_sf(ssfb + g * 1024));
+                                tc_cp_sf(sfb + 8 * g + 4, desc_sf(ssfb + g * 1024 + 512));
+                            }
                         }
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -778,7 +604,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                             for (int g = 0; g < C::kGroups; ++g) {
                                 const uint64_t bd = desc_sw128(sb + g * 128 * kKBytes + 32 * j);
                                 mma_mxf4(dset + a * C::kRows + g * 128, ad, bd, (j & 1) ? idesc_hi : idesc_lo,
-                                         sfcol + 4 * (j >> 1), sfcol + 8 + 8 * g + 4 * (j >> 1), accumulate);
+                                         sfcol + 4 * (j >> 1), sfb + 8 * g + 4 * (j >> 1), accumulate);
                             }
                         }
                         sfring = (sfring + 1) % kSfRing;
@@ -787,6 +613,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (failed) break;
+                if (use_xsf) xsf_done = true;
                 tc_commit(smem_u32(&tfull[acc]));
                 if (++acc == C::kDbuf) { acc = 0; aphase ^= 1u; }
             }
@@ -931,54 +758,26 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                         break;
                     }
                 }
-                // quantise; a job is (column c, block b of 32 outputs i0 = 64m + 32b).  Many
-                // jobs: one thread each; few: one warp each (shuffles, shorter latency)
-                if (u.ncols * 2 > 8) {
-                    const int job = ew * 32 + lane;
-                    if (job < u.ncols * 2) {
-                        const int c = job >> 1, b = job & 1;
-                        float v[32];
+                // quantise; a job is (column c, block b of 32 outputs i0 = 64m + 32b), one
+                // octet of lanes each (16 octets over the four warps)
+                for (int base = 0; base < u.ncols * 2; base += 16) {
+                    const int job = base + ew * 4 + (lane >> 3), sl = lane & 7;
+                    const bool act = job < u.ncols * 2;
+                    const int c = act ? job >> 1 : 0, b = job & 1;
+                    float v[4];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = hbuf[hidx(c, 32 * b + i)];
-                        uint32_t wds[kTerms][4], scl[kTerms];
-                        thread_quantize32(v, wds, scl);
-                        const int i0 = u.m * 64 + 32 * b, kb = i0 / kKB, j = (i0 % kKB) / 32;
-                        auto write_row_t = [&](int htile, int hrow) {
-                            if (dry) return;
-#pragma unroll
-                            for (int t = 0; t < kTerms; ++t) {
-                                *reinterpret_cast<uint4*>(p.h + act_code_off(htile, kb, t, hrow, j, NT, KBf)) =
-                                    make_uint4(wds[t][0], wds[t][1], wds[t][2], wds[t][3]);
-                                p.h[act_scale_off(htile, kb, t, hrow, j, NT, KBf)] = (uint8_t)scl[t];
-                            }
-                        };
-                        if (p.regime == kRegimeDecode) {
-                            // token c's pairs of this key: row (pinfo & 31) of the key's h tile
-                            if (c < p.T)
-                                for (int jj = 0; jj < p.k; ++jj) {
-                                    const int pi = pinfo[c * p.k + jj];
-                                    if (pi >= 0 && (pi >> 5) == u.key) write_row_t(u.key, pi & 31);
-                                }
-                        } else {
-                            write_row_t(u.btile, c);
-                        }
-                    }
-                } else for (int job = ew; job < u.ncols * 2; job += 4) {
-                    const int c = job >> 1, b = job & 1;
-                    uint4 codes[kTerms];
-                    uint32_t scales[kTerms];
-                    warp_quantize32(hbuf[hidx(c, 32 * b + lane)], lane, codes, scales);
+                    for (int i = 0; i < 4; ++i) v[i] = act ? hbuf[hidx(c, 32 * b + 4 * sl + i)] : 0.f;
+                    uint32_t wd[kTerms], scl[kTerms];
+                    octet_quantize32(v, lane, wd, scl);
+                    if (!act || dry) continue;
                     const int i0 = u.m * 64 + 32 * b, kb = i0 / kKB, j = (i0 % kKB) / 32;
                     auto write_row = [&](int htile, int hrow) {
-                        if (lane < kTerms && !dry) {
-                            // lane t writes term t (the codes of every term sit in lane 0)
-                            uint4 cv = codes[0];
-                            uint32_t sv = scales[0];
 #pragma unroll
-                            for (int t = 1; t < kTerms; ++t)
-                                if (lane == t) { cv = codes[t]; sv = scales[t]; }
-                            *reinterpret_cast<uint4*>(p.h + act_code_off(htile, kb, lane, hrow, j, NT, KBf)) = cv;
-                            p.h[act_scale_off(htile, kb, lane, hrow, j, NT, KBf)] = (uint8_t)sv;
+                        for (int t = 0; t < kTerms; ++t) {
+                            if ((sl & 1) == 0)
+                                *reinterpret_cast<uint32_t*>(p.h + act_code_off(htile, kb, t, hrow, j, NT, KBf) + 2 * sl) =
+                                    wd[t];
+                            if (sl == 0) p.h[act_scale_off(htile, kb, t, hrow, j, NT, KBf)] = (uint8_t)scl[t];
                         }
                     };
                     if (p.regime == kRegimeDecode) {
@@ -988,7 +787,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                                 const int pi = pinfo[c * p.k + jj];
                                 if (pi >= 0 && (pi >> 5) == u.key) write_row(u.key, pi & 31);
                             }
-                    } else if (c < u.ncols) {
+                    } else {
                         write_row(u.btile, c);
                     }
                 }
@@ -1075,10 +874,29 @@ static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& 
     return b;
 }
 
+size_t dec_partial_bytes(const moe_dims* m, int T);   // ffn_decode_tc.cu
+
 size_t tc_workspace_bytes(const moe_dims* m, int T) {
     const size_t R = (size_t)(T > 0 ? T : 1) * m->top_k;
     return align256(act_bytes_x(m, T)) + align256(act_bytes_h(m, T)) + align256(counters_of(m, T) * 4) +
-           align256(R * m->d * 4);
+           align256(R * m->d * 4) + align256(dec_partial_bytes(m, T));
+}
+
+int launch_dec_tc(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
+                  const float* w, uint16_t* y, int32_t* status, uint8_t* xq, uint8_t* hq, float* partials,
+                  int32_t* ctr, const int32_t* wait_limit, cudaStream_t st, int num_sms);   // ffn_decode_tc.cu
+
+// Decode on the tensor cores with the split-K dataflow kernel: its activation tiles are the
+// tensor-core section's x and h buffers, its partial sums follow the per-row outputs.
+int launch_tc_decode_split(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
+                           const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
+                           int num_sms) {
+    TcBuffers b = tc_buffers(m, T, ws, L);
+    const size_t R = (size_t)(T > 0 ? T : 1) * m->top_k;
+    float* partials = reinterpret_cast<float*>(reinterpret_cast<char*>(b.rows) + align256(R * m->d * 4));
+    int32_t* ctr = reinterpret_cast<int32_t*>(ws + L.counter);
+    return launch_dec_tc(m, ar, T, x, slot, w, y, status, b.x, b.h, partials, ctr + dec_ctr_off(m), ctr + kCtrWaitLimit,
+                         st, num_sms);
 }
 
 template <int NT>

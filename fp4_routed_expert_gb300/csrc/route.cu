@@ -32,6 +32,8 @@
 //     exact score, so every weight is within 2e-5 (relative) of the exact one.
 // Each (token, expert) gets one 16-byte key record {point key, klo, khi, score}; score < 0
 // marks an expert that is not resident.
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace fp4moe {
@@ -385,152 +387,158 @@ __device__ __noinline__ void select_token(const RouteArgs& a, int t, int lane, f
     __syncwarp();
 }
 
-// One warp per token.  Lane l holds the key records of experts l + 32 m (m < EPL) in
-// registers; a top-k round is two warp reductions (largest key, then lowest id among equal
-// keys) and a register rescan by the winning lane.  The chosen set is final when every chosen
-// expert's key interval lies above every other expert's and every chosen score is narrow;
-// otherwise the token goes whole to select_token (same warp).  E <= 32 * EPL.
 constexpr int kSelWarps = 4;
 
+// The selection of token t by one warp (lane l holds the key records of experts l + 32 m,
+// m < EPL, in registers): a top-k round is two warp reductions (largest key, then lowest id
+// among equal keys) and a register rescan by the winning lane.  The chosen set is final when
+// every chosen expert's key interval lies above every other expert's and every chosen score
+// is narrow; otherwise the token goes whole to select_token (same warp).  E <= 32 * EPL.
+// rec, exk and out are this warp's select_token arrays in shared memory.
+template <int EPL>
+__device__ __forceinline__ void select_row(const RouteArgs& a, int t, int lane, float4* rec, float* exk, int* out) {
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const int E = a.E, k = a.k;
+    const float4* krow = a.keys + (size_t)t * E;
+    // key records and slot-table entries of experts lane + 32 m, loaded together
+    float4 r[EPL];
+    int tb[EPL];
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+        const int e = lane + 32 * m;
+        r[m] = (e < E) ? __ldcg(krow + e) : make_float4(NEG_INF, NEG_INF, NEG_INF, -1.0f);
+        tb[m] = (e < E) ? __ldg(a.table + e) : -1;
+    }
+    uint32_t valid = 0, picked = 0, bu = 0;
+    int bm = 0;
+#pragma unroll
+    for (int m = 0; m < EPL; ++m)
+        if (r[m].w >= 0.0f) {
+            valid |= 1u << m;
+            const uint32_t ku = key_order(r[m].x);
+            if (ku > bu) { bu = ku; bm = m; }
+        }
+    int n = 0;
+    for (int j = 0; j < k; ++j) {
+        const uint32_t M = __reduce_max_sync(0xffffffffu, bu);
+        if (M == 0) break;
+        const uint32_t win = __reduce_min_sync(0xffffffffu, bu == M ? (uint32_t)(lane + 32 * bm) : 0xFFFFFFFFu);
+        if ((int)(win & 31) == lane) {
+            picked |= 1u << (win >> 5);
+            bu = 0;
+#pragma unroll
+            for (int m = 0; m < EPL; ++m)
+                if (((valid & ~picked) >> m) & 1u) {
+                    const uint32_t ku = key_order(r[m].x);
+                    if (ku > bu) { bu = ku; bm = m; }
+                }
+        }
+        ++n;
+    }
+    if (n < k && lane == 0) atomicOr(a.status, MOE_STATUS_FEW_RESIDENT);
+    // certification thresholds: min klo over the chosen, max khi over the rest
+    float lo_in = __int_as_float(0x7f800000), hi_out = NEG_INF;
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+        if ((picked >> m) & 1u) lo_in = fminf(lo_in, r[m].y);
+        else if ((valid >> m) & 1u) hi_out = fmaxf(hi_out, r[m].z);
+    }
+    const float min_lo_in = key_value(__reduce_min_sync(0xffffffffu, key_order(lo_in)));
+    const float max_hi_out = key_value(__reduce_max_sync(0xffffffffu, key_order(hi_out)));
+    bool doubt = false, order_doubt = false;
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+        if ((picked >> m) & 1u) {
+            if (!(r[m].y > max_hi_out)) order_doubt = true;
+            else if (r[m].z - r[m].y > 1e-5f * r[m].w) doubt = true;
+        } else if (((valid >> m) & 1u) && r[m].z >= min_lo_in) {
+            order_doubt = true;
+        }
+    }
+    if (__any_sync(0xffffffffu, doubt || order_doubt)) {
+        // Refinement: when the chosen set is certain and only some chosen scores are wide
+        // (the tiled logits' bound), the chosen experts' records are recomputed with the
+        // compensated dot product; if every chosen interval is then narrow and still above
+        // every other expert's, the token is done without exact logits.
+        bool resolved = false;
+        if (!__any_sync(0xffffffffu, order_doubt) && a.refine_coef > 0.0f) {
+            const uint16_t* xt = a.x + (size_t)t * a.d;
+            bool still = false;
+#pragma unroll
+            for (int m = 0; m < EPL; ++m) {
+                uint32_t bal = __ballot_sync(0xffffffffu, (picked >> m) & 1u);
+                while (bal) {
+                    const int src = __ffs(bal) - 1;
+                    bal &= bal - 1;
+                    const int e = src + 32 * m;
+                    const float be = a.bias ? a.bias[e] : 0.0f;
+                    const int tbe = __shfl_sync(0xffffffffu, tb[m], src);
+                    const float4 nr = refine_key_warp(xt, a.wr + (size_t)e * a.d, a.d, lane, a.refine_coef, tbe, be);
+                    if (lane == src) {
+                        r[m] = nr;
+                        if (!(nr.y > max_hi_out) || nr.z - nr.y > 1e-5f * nr.w) still = true;
+                    }
+                }
+            }
+            resolved = !__any_sync(0xffffffffu, still);
+        }
+        if (!resolved) {
+            select_token(a, t, lane, rec, exk, out);
+            return;
+        }
+    }
+    // outputs in ascending id (m outer, lane inner); weight sum in that order
+    float* osc = reinterpret_cast<float*>(out);
+    int* oid = out + 32;
+    int* osl = out + 64;
+    const uint32_t below = (1u << lane) - 1u;
+    int base = 0;
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+        const uint32_t bal = __ballot_sync(0xffffffffu, (picked >> m) & 1u);
+        if ((picked >> m) & 1u) {
+            const int rank = base + __popc(bal & below);
+            osc[rank] = r[m].w;
+            oid[rank] = lane + 32 * m;
+            osl[rank] = tb[m];
+        }
+        base += __popc(bal);
+    }
+    __syncwarp();
+    float sum = 0.0f;
+    if (lane == 0)
+        for (int i = 0; i < n; ++i) sum += osc[i];
+    sum = __shfl_sync(0xffffffffu, sum, 0);
+    int32_t* ids = a.ids + (size_t)t * k;
+    float* wo = a.w + (size_t)t * k;
+    int32_t* so = a.slots + (size_t)t * k;
+    for (int j = lane; j < k; j += 32) {
+        if (j < n) {
+            ids[j] = oid[j];
+            wo[j] = (sum > 0.0f) ? __fdiv_rn(osc[j], sum) : 0.0f;
+            so[j] = osl[j];
+        } else {
+            ids[j] = -1;
+            wo[j] = 0.0f;
+            so[j] = -1;
+        }
+    }
+    __syncwarp();
+}
+
+// One warp per token, launched behind the key-record kernel of the tiled (large T) router.
 template <int EPL>
 __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(RouteArgs a) {
     extern __shared__ unsigned char sel_smem[];   // per warp: select_token's arrays
-    const float NEG_INF = -__int_as_float(0x7f800000);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int E = a.E, k = a.k;
-    unsigned char* wsm = sel_smem + (size_t)warp * select_smem_per_warp(E);
+    unsigned char* wsm = sel_smem + (size_t)warp * select_smem_per_warp(a.E);
     float4* rec = reinterpret_cast<float4*>(wsm);
-    float* exk = reinterpret_cast<float*>(wsm + (size_t)E * 16);
-    int* out = reinterpret_cast<int*>(wsm + (size_t)E * 20);   // 96 words: ranks' scores, ids, slots
+    float* exk = reinterpret_cast<float*>(wsm + (size_t)a.E * 16);
+    int* out = reinterpret_cast<int*>(wsm + (size_t)a.E * 20);   // 96 words: ranks' scores, ids, slots
     pdl_trigger();
     pdl_wait();   // the key records of the logit kernel
-    for (int t = blockIdx.x * kSelWarps + warp; t < a.T; t += gridDim.x * kSelWarps) {
-        const float4* krow = a.keys + (size_t)t * E;
-        // key records and slot-table entries of experts lane + 32 m, loaded together
-        float4 r[EPL];
-        int tb[EPL];
-#pragma unroll
-        for (int m = 0; m < EPL; ++m) {
-            const int e = lane + 32 * m;
-            r[m] = (e < E) ? __ldcg(krow + e) : make_float4(NEG_INF, NEG_INF, NEG_INF, -1.0f);
-            tb[m] = (e < E) ? __ldg(a.table + e) : -1;
-        }
-        uint32_t valid = 0, picked = 0, bu = 0;
-        int bm = 0;
-#pragma unroll
-        for (int m = 0; m < EPL; ++m)
-            if (r[m].w >= 0.0f) {
-                valid |= 1u << m;
-                const uint32_t ku = key_order(r[m].x);
-                if (ku > bu) { bu = ku; bm = m; }
-            }
-        int n = 0;
-        for (int j = 0; j < k; ++j) {
-            const uint32_t M = __reduce_max_sync(0xffffffffu, bu);
-            if (M == 0) break;
-            const uint32_t win = __reduce_min_sync(0xffffffffu, bu == M ? (uint32_t)(lane + 32 * bm) : 0xFFFFFFFFu);
-            if ((int)(win & 31) == lane) {
-                picked |= 1u << (win >> 5);
-                bu = 0;
-#pragma unroll
-                for (int m = 0; m < EPL; ++m)
-                    if (((valid & ~picked) >> m) & 1u) {
-                        const uint32_t ku = key_order(r[m].x);
-                        if (ku > bu) { bu = ku; bm = m; }
-                    }
-            }
-            ++n;
-        }
-        if (n < k && lane == 0) atomicOr(a.status, MOE_STATUS_FEW_RESIDENT);
-        // certification thresholds: min klo over the chosen, max khi over the rest
-        float lo_in = __int_as_float(0x7f800000), hi_out = NEG_INF;
-#pragma unroll
-        for (int m = 0; m < EPL; ++m) {
-            if ((picked >> m) & 1u) lo_in = fminf(lo_in, r[m].y);
-            else if ((valid >> m) & 1u) hi_out = fmaxf(hi_out, r[m].z);
-        }
-        const float min_lo_in = key_value(__reduce_min_sync(0xffffffffu, key_order(lo_in)));
-        const float max_hi_out = key_value(__reduce_max_sync(0xffffffffu, key_order(hi_out)));
-        bool doubt = false, order_doubt = false;
-#pragma unroll
-        for (int m = 0; m < EPL; ++m) {
-            if ((picked >> m) & 1u) {
-                if (!(r[m].y > max_hi_out)) order_doubt = true;
-                else if (r[m].z - r[m].y > 1e-5f * r[m].w) doubt = true;
-            } else if (((valid >> m) & 1u) && r[m].z >= min_lo_in) {
-                order_doubt = true;
-            }
-        }
-        if (__any_sync(0xffffffffu, doubt || order_doubt)) {
-            // Refinement: when the chosen set is certain and only some chosen scores are wide
-            // (the tiled logits' bound), the chosen experts' records are recomputed with the
-            // compensated dot product; if every chosen interval is then narrow and still above
-            // every other expert's, the token is done without exact logits.
-            bool resolved = false;
-            if (!__any_sync(0xffffffffu, order_doubt) && a.refine_coef > 0.0f) {
-                const uint16_t* xt = a.x + (size_t)t * a.d;
-                bool still = false;
-#pragma unroll
-                for (int m = 0; m < EPL; ++m) {
-                    uint32_t bal = __ballot_sync(0xffffffffu, (picked >> m) & 1u);
-                    while (bal) {
-                        const int src = __ffs(bal) - 1;
-                        bal &= bal - 1;
-                        const int e = src + 32 * m;
-                        const float be = a.bias ? a.bias[e] : 0.0f;
-                        const int tbe = __shfl_sync(0xffffffffu, tb[m], src);
-                        const float4 nr = refine_key_warp(xt, a.wr + (size_t)e * a.d, a.d, lane, a.refine_coef, tbe, be);
-                        if (lane == src) {
-                            r[m] = nr;
-                            if (!(nr.y > max_hi_out) || nr.z - nr.y > 1e-5f * nr.w) still = true;
-                        }
-                    }
-                }
-                resolved = !__any_sync(0xffffffffu, still);
-            }
-            if (!resolved) {
-                select_token(a, t, lane, rec, exk, out);
-                continue;
-            }
-        }
-        // outputs in ascending id (m outer, lane inner); weight sum in that order
-        float* osc = reinterpret_cast<float*>(out);
-        int* oid = out + 32;
-        int* osl = out + 64;
-        const uint32_t below = (1u << lane) - 1u;
-        int base = 0;
-#pragma unroll
-        for (int m = 0; m < EPL; ++m) {
-            const uint32_t bal = __ballot_sync(0xffffffffu, (picked >> m) & 1u);
-            if ((picked >> m) & 1u) {
-                const int rank = base + __popc(bal & below);
-                osc[rank] = r[m].w;
-                oid[rank] = lane + 32 * m;
-                osl[rank] = tb[m];
-            }
-            base += __popc(bal);
-        }
-        __syncwarp();
-        float sum = 0.0f;
-        if (lane == 0)
-            for (int i = 0; i < n; ++i) sum += osc[i];
-        sum = __shfl_sync(0xffffffffu, sum, 0);
-        int32_t* ids = a.ids + (size_t)t * k;
-        float* wo = a.w + (size_t)t * k;
-        int32_t* so = a.slots + (size_t)t * k;
-        for (int j = lane; j < k; j += 32) {
-            if (j < n) {
-                ids[j] = oid[j];
-                wo[j] = (sum > 0.0f) ? __fdiv_rn(osc[j], sum) : 0.0f;
-                so[j] = osl[j];
-            } else {
-                ids[j] = -1;
-                wo[j] = 0.0f;
-                so[j] = -1;
-            }
-        }
-        __syncwarp();
-    }
+    for (int t = blockIdx.x * kSelWarps + warp; t < a.T; t += gridDim.x * kSelWarps)
+        select_row<EPL>(a, t, lane, rec, exk, out);
 }
 
 #define FP4MOE_EPL_DISPATCH(E, ...)                                   \
@@ -547,24 +555,34 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(RouteArgs 
 
 // ------------------------------------------------------------------ decode: one warp per expert
 
-constexpr int kDecodeWarps = 4;
-constexpr size_t kDecodeSmemMax = 200 * 1024;
+constexpr int kDecodeWarps = 4;                 // experts per block and round
+constexpr int kDecodeGroups = 4;                // token groups at most (warps per expert)
+constexpr size_t kDecodeSmemMax = 226 * 1024;
 
 __host__ __device__ inline size_t decode_smem_bytes(int T, int d) {
     return (size_t)(kDecodeWarps + T) * d * 2 + 16;   // W rows, x rows, one mbarrier
 }
 
+// Number of token groups of a decode router launch: one warp per (expert, group).
+inline int decode_groups(int T) { return T < kDecodeGroups ? T : kDecodeGroups; }
+
 // Key records for T <= 16 tokens.  A block takes kDecodeWarps experts per round: their router
 // rows and (once) the tokens' rows arrive in shared memory by bulk copies, then warp w works
-// on expert e0 + w, one token at a time.  Lane l owns vectors l, l+32, ...; per token it
+// on expert e0 + w % kDecodeWarps for the tokens of group w / kDecodeWarps (blockDim.x / 128
+// groups of consecutive tokens), one token at a time; a token's arithmetic does not depend on
+// its group.  Lane l owns vectors l, l+32, ...; per token it
 // keeps 8/CH compensated sums (s, c) -- one per plain FMA chunk of CH products of a vector, so
 // the chains are independent -- and sum|x w|.  The loops are kept short: this code runs once
-// per call and is seldom in the instruction cache.  The selection kernel follows.
-template <int CH>
-__global__ void __launch_bounds__(kDecodeWarps * 32) route_decode_kernel(RouteArgs a) {
+// per call and is seldom in the instruction cache.  The last block to finish (a ticket on
+// a.counter, left at zero again) then selects every token's experts, one warp per token, in
+// its own shared memory.
+template <int CH, int EPL>
+__global__ void __launch_bounds__(kDecodeWarps * kDecodeGroups * 32) route_decode_kernel(RouteArgs a) {
     constexpr int NCH = 8 / CH;
     extern __shared__ __align__(16) unsigned char dsm[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = (tid >> 5) % kDecodeWarps, grp = (tid >> 5) / kDecodeWarps;
+    const int ngrp = blockDim.x / (32 * kDecodeWarps);
+    const int tpg = (a.T + ngrp - 1) / ngrp, t_lo = grp * tpg, t_hi = min(a.T, t_lo + tpg);
     const int T = a.T, d = a.d, E = a.E, nvec = d / 8;
     uint16_t* ws = reinterpret_cast<uint16_t*>(dsm);
     const uint16_t* xs = ws + (size_t)kDecodeWarps * d;
@@ -602,7 +620,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) route_decode_kernel(RouteAr
         if (e < E) {
             const uint4* wrow = reinterpret_cast<const uint4*>(ws + (size_t)warp * d);
             float myS = 0.f, myC = 0.f, myA = 0.f;
-            for (int t = 0; t < T; ++t) {
+            for (int t = t_lo; t < t_hi; ++t) {
                 const uint4* xrow = reinterpret_cast<const uint4*>(xs + (size_t)t * d);
                 float s[NCH], c[NCH], A = 0.f;
 #pragma unroll
@@ -644,19 +662,33 @@ __global__ void __launch_bounds__(kDecodeWarps * 32) route_decode_kernel(RouteAr
                     Cc = __fadd_rn(__fadd_rn(Cc, C2), err);
                     A = __fadd_ru(A, __shfl_xor_sync(0xffffffffu, A, o));
                 }
-                if (lane == t) { myS = S; myC = Cc; myA = A; }
+                if (lane == t - t_lo) { myS = S; myC = Cc; myA = A; }
             }
-            if (lane < T) {
+            if (lane < t_hi - t_lo) {
                 // |S + C - exact| <= coef * sum|x w| * (1 + 2^-9) + d * 2^-147
                 float delta = __fmul_ru(__fmul_ru(a.bound_coef, myA), 1.001953125f);
                 delta = __fadd_ru(delta, (float)d * 5.605193857299268e-45f);
                 const float lo = __fadd_rd(myS, __fsub_rd(myC, delta));
                 const float hi = __fadd_ru(myS, __fadd_ru(myC, delta));
-                a.keys[(size_t)lane * E + e] = make_key(tb, bias_e, __fadd_rn(myS, myC), lo, hi);
+                a.keys[(size_t)(t_lo + lane) * E + e] = make_key(tb, bias_e, __fadd_rn(myS, myC), lo, hi);
             }
         }
         __syncthreads();   // the next iteration's copies overwrite the router rows
     }
+    __shared__ int last_block;
+    __threadfence();   // this block's key records, before its ticket
+    __syncthreads();
+    if (tid == 0) last_block = (atomicAdd(a.counter, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!last_block) return;
+    __threadfence();
+    const int nsel = blockDim.x >> 5, wsel = tid >> 5;
+    unsigned char* wsm = dsm + (size_t)wsel * select_smem_per_warp(E);
+    float4* rec = reinterpret_cast<float4*>(wsm);
+    float* exk = reinterpret_cast<float*>(wsm + (size_t)E * 16);
+    int* out = reinterpret_cast<int*>(wsm + (size_t)E * 20);
+    for (int t = wsel; t < T; t += nsel) select_row<EPL>(a, t, lane, rec, exk, out);
+    if (tid == 0) *a.counter = 0u;
 }
 
 // ------------------------------------------------------------------ large T: tiled logits
@@ -779,21 +811,29 @@ static int launch_select(const RouteArgs& a, cudaStream_t st) {
     return MOE_ERR_LAUNCH;
 }
 
-template <int CH>
+// Dynamic shared memory of the decode router: the router rows and token rows of the logit
+// phase, or the selecting warps' arrays, whichever is larger.
+static size_t decode_route_smem(int T, int d, int E) {
+    const int sel_warps = std::min(kDecodeWarps * decode_groups(T), T);
+    return std::max(decode_smem_bytes(T, d), (size_t)sel_warps * select_smem_per_warp(E));
+}
+
+template <int CH, int EPL>
 static int launch_decode_ch(RouteArgs a, cudaStream_t st, int num_sms) {
-    const size_t smem = decode_smem_bytes(a.T, a.d);
+    const int threads = kDecodeWarps * 32 * decode_groups(a.T);
+    const size_t smem = decode_route_smem(a.T, a.d, a.E);
     if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(route_decode_kernel<CH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        cudaFuncSetAttribute(route_decode_kernel<CH, EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
         return MOE_ERR_LAUNCH;
     const int m = a.d / 256;    // compensated steps per chain and lane
     const double coef = gamma32(CH - 1) + gamma32(m) * gamma32(m) + 1.0 / 17179869184.0;   // + 2^-34
     a.bound_coef = (float)(coef * (1.0 + 1.0 / 4096.0));                                   // rounded up
     int blocks = (a.E + kDecodeWarps - 1) / kDecodeWarps;
     if (num_sms > 0 && blocks > num_sms) blocks = num_sms;
-    route_decode_kernel<CH><<<blocks, kDecodeWarps * 32, smem, st>>>(a);
+    route_decode_kernel<CH, EPL><<<blocks, threads, smem, st>>>(a);
     note_launch(1);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_LAUNCH;
-    return launch_select(a, st);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
 
 // Router launches for RouteArgs with every pointer set: the decode kernel when the tokens'
@@ -805,10 +845,11 @@ static int launch_route_args(RouteArgs& a, cudaStream_t st, int num_sms) {
         const double coef = gamma32(0) + gamma32(m) * gamma32(m) + 1.0 / 17179869184.0;
         a.refine_coef = (float)(coef * (1.0 + 1.0 / 4096.0));
     }
-    if (a.T <= kDecodeMaxT && decode_smem_bytes(a.T, a.d) <= kDecodeSmemMax) {
+    if (a.T <= kDecodeMaxT && decode_route_smem(a.T, a.d, a.E) <= kDecodeSmemMax) {
         // chunks of one product for every T: a token's logits are then the same arithmetic
         // whatever the other tokens of the call (verify rows equal their decode calls)
-        return launch_decode_ch<1>(a, st, num_sms);
+        FP4MOE_EPL_DISPATCH(a.E, return launch_decode_ch<1, EPL>(a, st, num_sms));
+        return MOE_ERR_LAUNCH;
     }
     a.bound_coef = gamma_coef(kChunkK + (a.d + kChunkK - 1) / kChunkK + 1);
     const int rows = a.T + a.E;

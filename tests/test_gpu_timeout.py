@@ -2,10 +2,11 @@
 its own copies and returns, and a workspace re-initialised afterwards serves a normal call.
 
 The wait is made to run out without any fault: moe_workspace_set_wait_limit makes every wait
-of the streaming decode kernel (the CUDA-core decode path) on another CTA's progress (x
-encoded, a key's h rows complete) give up after one poll, and in a small decode call the CTAs
-that take down units check their key's h count long before any gate/up tile has finished.  Waits on a CTA's own copies keep their default limit, so every copy
-that was issued lands before its CTA exits."""
+of the decode kernels (the tensor-core split-K kernel and the CUDA-core streaming kernel) on
+another CTA's progress (x encoded, a key's h rows complete) give up after one poll, and in a
+small decode call the CTAs that take down units check their key's h count long before any
+gate/up tile has finished.  Waits on a CTA's own copies and MMAs keep their default limit, so
+every copy that was issued lands, and every MMA completes, before its CTA exits."""
 import numpy as np
 import pytest
 import torch
@@ -26,7 +27,8 @@ def tiny():
     return make_workload(512, 256, 16, 2, seed=0, scale=(-8, -4))
 
 
-def test_decode_dependency_wait_times_out_then_workspace_recovers(tiny):
+@pytest.mark.parametrize("cuda_cores", [False, True], ids=["tensor_cores", "cuda_cores"])
+def test_decode_dependency_wait_times_out_then_workspace_recovers(tiny, cuda_cores):
     T = 3
     layer = MoeLayer(tiny.d, tiny.f, tiny.E, tiny.k, T, tiny.arena)
     x_bits = syn.activations(0, 60, T, tiny.d)
@@ -37,14 +39,14 @@ def test_decode_dependency_wait_times_out_then_workspace_recovers(tiny):
     torch.cuda.synchronize()
     assert int(layer.status.item()) == 0
     moe.moe_workspace_set_wait_limit(layer.dims, layer.ws, 1)
-    layer.experts(x, cuda_cores=True)
+    layer.experts(x, cuda_cores=cuda_cores)
     torch.cuda.synchronize()                      # the call returned
     assert int(layer.status.item()) & moe.MOE_STATUS_TIMEOUT
     # recovery: re-initialise the workspace (default limit again), route and run normally
     moe.moe_workspace_init(layer.dims, layer.ws)
     layer.status.zero_()
     layer.route(x, wr, tab)
-    y = layer.experts(x, cuda_cores=True)
+    y = layer.experts(x, cuda_cores=cuda_cores)
     torch.cuda.synchronize()
     assert int(layer.status.item()) == 0
     r = dict(ids=layer.ids[:T].cpu().numpy(), slots=layer.slots[:T].cpu().numpy(), weights=layer.w[:T].cpu().numpy())
