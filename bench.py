@@ -67,27 +67,58 @@ def env_rank():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
-FFN_SOURCES = ("fp4_routed_expert_gb300/csrc/mxf4_gemm.cu", "fp4_routed_expert_gb300/csrc/moe_internal.cuh")
-TRAFFIC_PROFILE = "profiles/expert_ffn_decode_T1_d5120_f2304_E384_k6.md"
+FFN_SOURCES = ("fp4_routed_expert_gb300/csrc/ffn_decode_tc.cu", "fp4_routed_expert_gb300/csrc/mxf4_common.cuh",
+               "fp4_routed_expert_gb300/csrc/moe_internal.cuh")
+FFN_KERNEL = "mxf4_decode_kernel"
+TRAFFIC_RECORD = "profiles/traffic_expert_ffn_decode_T1_d5120_f2304_E384_k6.json"
+
+
+def sources_digest(files) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def ffn_traffic():
-    """DRAM bytes per FFN launch from the committed ncu capture, if it was taken on the current
-    kernel source (digest of its files), else None."""
-    import hashlib
-    h = hashlib.sha256()
+    """DRAM bytes per FFN launch from the committed traffic record (written by --record-traffic
+    from an ncu capture), if it was taken on the current kernel source, else None."""
     try:
-        for f in FFN_SOURCES:
-            h.update(open(os.path.join(ROOT, f), "rb").read())
-        text = open(os.path.join(ROOT, TRAFFIC_PROFILE)).read()
-    except OSError:
-        return None
-    for line in text.splitlines():
-        if line.startswith("traffic-record:"):
-            fields = dict(kv.split("=", 1) for kv in line.split()[1:])
-            if fields.get("digest") == h.hexdigest()[:16]:
-                return int(fields["dram_bytes_per_launch"])
+        rec = json.load(open(os.path.join(ROOT, TRAFFIC_RECORD)))
+        if rec.get("digest") == sources_digest(FFN_SOURCES):
+            return int(rec["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
     return None
+
+
+def record_traffic(csv_path: str, kernel_regex: str, out_path: str, command: str) -> dict:
+    """Write the traffic record of one kernel from ncu's raw page (ncu -i REP --page raw --csv
+    --print-units base): the mean of dram__bytes_read.sum + dram__bytes_write.sum over the
+    captured launches whose name matches kernel_regex, with the digest of the FFN sources."""
+    import csv
+    import re
+    rows = list(csv.reader(open(csv_path)))
+    head = rows[0]
+    ki = head.index("Kernel Name")
+    ri, wi = head.index("dram__bytes_read.sum"), head.index("dram__bytes_write.sum")
+    vals = []
+    for r in rows[1:]:
+        if len(r) <= max(ki, ri, wi) or not re.search(kernel_regex, r[ki]):
+            continue
+        try:
+            vals.append(float(r[ri].replace(",", "")) + float(r[wi].replace(",", "")))
+        except ValueError:
+            continue            # the units row
+    if not vals:
+        raise SystemExit("no launch of %r with DRAM counters in %s" % (kernel_regex, csv_path))
+    rec = {"kernel": kernel_regex, "launches": len(vals), "dram_bytes_per_launch": int(statistics.mean(vals)),
+           "digest": sources_digest(FFN_SOURCES), "sources": list(FFN_SOURCES), "command": command}
+    with open(os.path.join(ROOT, out_path), "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return rec
 
 
 def measured_peaks():
@@ -313,7 +344,7 @@ def run_ours(args, rank, world, local_rank):
             "dtype": "fp4 (e2m1 x e2m1 block-scaled tcgen05 MMA, UE8M0/32, activations as 4 MXFP4 terms; fp32 accumulate)",
             "data": "synthetic (seeded Philox FP4 experts, N(0,1) bf16 tokens, N(0,0.02) bf16 router)",
             "config": dict(CONFIG, parallelism="replicas" if world > 1 else "single GPU"),
-            "roofline": {"bound": "hbm", "kernel": "mxf4_ffn_kernel (expert FFN: gate/up + SwiGLU + down + combine, T=1)",
+            "roofline": {"bound": "hbm", "kernel": FFN_KERNEL + " (expert FFN: gate/up + SwiGLU + down + combine, T=1)",
                          "achieved": round(achieved, 1) if achieved else None, "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4) if achieved else None, "traffic": ffn_traffic(),
                          "bytes_per_launch": FFN_BYTES, "launch_ms": round(k_ms, 5) if k_ms else None,
@@ -929,6 +960,9 @@ def main():
     ap.add_argument("--no-keepset", action="store_true",
                     help="skip the 40-layer keep-set measurements (they need a 115.8 GB arena)")
     ap.add_argument("--no-long-prefill", action="store_true", help="skip the 4 x 8,192-token long prefill")
+    ap.add_argument("--record-traffic", metavar="RAW_CSV",
+                    help="write the decode FFN traffic record from ncu's raw page (--print-units base) and exit")
+    ap.add_argument("--traffic-command", default="", help="the ncu command the raw page came from (recorded)")
     ap.add_argument("--keepset-only", action="store_true",
                     help="measure only the 40-layer keep-set workloads (profiling runs)")
     ap.add_argument("--cb3-only", action="store_true",
@@ -947,6 +981,9 @@ def main():
         CONFIG["l2"] = "arena of %.2f GB (each call streams 6 experts, 112.8 MB, more than L2), no flush" % (
             E * EXPERT_BYTES / 1e9)
     rank, world, local_rank = env_rank()
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, FFN_KERNEL, TRAFFIC_RECORD, args.traffic_command)))
+        return 0
     if args.impl == "reference":
         out = run_reference(args, rank, world)
         if out is not None:

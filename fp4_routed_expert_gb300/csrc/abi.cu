@@ -217,7 +217,7 @@ int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, 
     int sms = num_sms_of_current_device();
     if (T <= kDecodeMaxT && fused) {
         if (!cuda_cores && tc_decode_supported(dims, T))
-            return launch_tc_decode_split(dims, arena, T, x, topk_slot, topk_w, y, dev_status, w, L, st, sms);
+            return launch_tc_decode(dims, arena, T, x, topk_slot, topk_w, y, dev_status, w, L, st, sms);
         return launch_stream_ffn(dims, arena, T, x, topk_slot, topk_w, y, dev_status, w, L, st, sms);
     }
     if (!group_offsets || !row_src || (fused && !row_dst)) return MOE_ERR_NULL;

@@ -13,14 +13,15 @@
 //
 // Work.  A key is a slot's pairs (in chunks of at most NT); each key's FFN is cut into units:
 //   gate/up unit (key, m, s): weight row tile m (64 gate rows interleaved with 64 up rows) over
-//     K split s of d (KCg K blocks of 256); writes its fp32 partial sums to the workspace; the
-//     unit that completes tile m (a ticket per tile) adds the SG partials in split order,
-//     applies SwiGLU and writes h[64m, 64m+64) of the key's pairs as kTerms MXFP4 terms, then
-//     counts that h K block (4 tiles per block of 256 h values);
+//     K split s of d (KCg K blocks of 256); splits 0..SG-2 write their fp32 partial sums to the
+//     workspace and count themselves; split SG-1 (the tile's reducer) waits for that count,
+//     adds the SG partials in split order, applies SwiGLU and writes h[64m, 64m+64) of the
+//     key's pairs as kTerms MXFP4 terms, then counts that h K block (4 tiles per block of 256);
 //   down unit (key, m, s): output row tile m over K split s of f (KCd K blocks of h), once the
-//     h blocks of that split are complete; writes fp32 partials per pair; the unit that
-//     completes tile m (a ticket per tile, n_keys * SD arrivals) combines y[t][128m, +128) for
-//     every token: per pair the SD partials in split order, then the pairs in ascending j.
+//     h blocks of that split are complete; writes fp32 partials per pair and counts itself; the
+//     last key's split SD-1 (the tile's reducer) waits for the other n_keys * SD - 1 units and
+//     combines y[t][128m, +128) for every token: per pair the SD partials in split order, then
+//     the pairs in ascending j.
 // Every token's arithmetic is the same whatever the other tokens of the call: an MMA column is
 // its own dot product, and the splits, the summation orders and the quantisation depend only
 // on d and f.
@@ -58,6 +59,8 @@ struct DecParams {
 };
 
 enum { kDcWork = 0, kDcXJob = 1, kDcXReady = 2, kDcExit = 3, kDcHead = 16 };
+constexpr int kDecMaxSplits = 8;   // K splits of either phase at most
+constexpr int kMaxTopKDec = 8;     // top-k of a tensor-core decode call at most
 constexpr int kDecUQ = 8;   // unit ids in flight from the producer to the MMA and epilogue warps
 
 // counters after the head: gate/up tickets [key][MTg], h blocks [key][KBf], down tickets [MTd]
@@ -134,6 +137,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_decode_kernel(DecParams 
     uint64_t* setupbar = uqempty + kDecUQ;
     uint64_t* epibar = setupbar + 1;                // the four epilogue warps' rendezvous
     uint64_t* drainbar = setupbar + 2;              // every MMA of the CTA complete
+    uint64_t* warmbar = setupbar + 3;               // the warm-up MMAs complete
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     __shared__ int n_keys_sh, pairs_total_sh;
@@ -162,6 +166,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_decode_kernel(DecParams 
         mbar_init(smem_u32(setupbar), 1);
         mbar_init(smem_u32(epibar), 4);
         mbar_init(smem_u32(drainbar), 1);
+        mbar_init(smem_u32(warmbar), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -206,12 +211,69 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_decode_kernel(DecParams 
             if (lane == 0) red_add_release(p.ctr + kDcXReady, 1);
         }
     }
+    if (warp == 1 && lane == 0) {
+        // Warm-up while the router still runs: one K block of scale copies and MMAs on whatever
+        // stage 0 holds, into accumulator set 0 (the first unit overwrites it), so that the
+        // first real stage does not pay for a cold issue path.
+        const uint32_t sa = smem_u32(stage_base), sb = sa + C::kKPS * kTileBytes;
+        const uint32_t sfcol = tmem + 256;
+        tc_cp_sf(sfcol + 0, desc_sf(sa + kTileCodeBytes));
+        tc_cp_sf(sfcol + 4, desc_sf(sa + kTileCodeBytes + 512));
+        tc_cp_sf(sfcol + 8, desc_sf(sb + C::kRows * kKBytes));
+        tc_cp_sf(sfcol + 12, desc_sf(sb + C::kRows * kKBytes + 512));
+        const uint32_t idesc_lo = idesc_mxf4(C::kN, 0), idesc_hi = idesc_mxf4(C::kN, 2);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            mma_mxf4(tmem + (j % C::kAcc) * C::kRows, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
+                     (j & 1) ? idesc_hi : idesc_lo, sfcol + 4 * (j >> 1), sfcol + 8 + 4 * (j >> 1), j >= C::kAcc ? 1u : 0u);
+        tc_commit(smem_u32(warmbar));
+        for (unsigned i = 0; i < kSpinLimit; ++i)
+            if (mbar_try(smem_u32(warmbar), 0)) break;
+    }
     pdl_wait();   // the router's outputs (slots, weights) are read from here on
     const unsigned limit = dec_limit(p);
     if (warp == 0) {
         // keys in order of their first pair: a slot's pairs in chunks of at most NT (pair i on
         // lane i mod 32)
         const int n = p.T * p.k;   // <= kMaxDecodePairs, checked on the host
+        if (n <= 32) {
+            // one pair per lane, in registers: a slot's pairs are found by one match, a pair's
+            // occurrence is the count of its slot's lanes below it
+            const unsigned below = (1u << lane) - 1u;
+            const int s = lane < n ? p.slot[lane] : -1;
+            const bool ok = lane < n && s >= 0 && s < p.num_slots;
+            if (lane < n && s >= p.num_slots && blockIdx.x == 0) atomicOr(p.status, MOE_STATUS_BAD_SLOT);
+            const unsigned peers = __match_any_sync(0xffffffffu, ok ? s : -1 - lane);
+            const int occ = __popc(peers & below), tot = __popc(peers);
+            const bool start = ok && (occ % NT) == 0;
+            const unsigned bal = __ballot_sync(0xffffffffu, start);
+            const int mykey = start ? __popc(bal & below) : 0;
+            // the lane that starts this pair's key: the (occ0 + 1)-th lane of its slot
+            const int src = (ok && !start) ? (int)__fns(peers, 0, occ - occ % NT + 1) : lane;
+            const int key = __shfl_sync(0xffffffffu, mykey, src);
+            const int csize = start ? min(NT, tot - occ) : 0;
+            int inc = csize;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int yv = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += yv;
+            }
+            const int base = __shfl_sync(0xffffffffu, inc - csize, src);
+            if (lane < n) pinfo[lane] = ok ? ((key << 5) | (occ % NT)) : -1;
+            if (start) {
+                kslot[mykey] = s;
+                kinfo[mykey] = (base << 16) | csize;
+            }
+            if (ok) kplist[base + occ % NT] = (short)lane;
+            const unsigned okbal = __ballot_sync(0xffffffffu, ok);
+            __syncwarp();
+            if (lane == 0) {
+                n_keys_sh = __popc(bal);
+                pairs_total_sh = __popc(okbal);
+                mbar_arrive(smem_u32(setupbar));
+            }
+            __syncwarp();
+        } else {
         int* sslot = reinterpret_cast<int*>(hbuf);   // the slots, during the setup only
         for (int i = lane; i < n; i += 32) sslot[i] = p.slot[i];
         __syncwarp();
@@ -281,6 +343,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_decode_kernel(DecParams 
             mbar_arrive(smem_u32(setupbar));
         }
         __syncwarp();
+        }
     }
     if (!mbar_wait(smem_u32(setupbar), 0, abortp)) {
         if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
@@ -498,16 +561,19 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_decode_kernel(DecParams 
             }
             ephase ^= 1u;
         };
-        // ticket: after every epilogue thread's global writes, add one to *counter; true for the
-        // unit whose addition completed `target` (all four warps learn it)
+        // Ticket: after every epilogue thread's stores, one thread adds one to *counter (a
+        // gpu-scope fence first: the rendezvous orders the other threads' stores before it);
+        // true, for all four warps, for the unit whose addition completed `target`.  The next
+        // ticket's first rendezvous keeps tick_sh until every warp has read it.
         auto ticket = [&](int32_t* counter, int target) -> bool {
-            __threadfence();
             epi_sync();
-            if (ew == 0 && lane == 0) tick_sh = (atom_add_acq_rel(counter, 1) + 1 == target);
+            if (ew == 0 && lane == 0) {
+                __threadfence();
+                tick_sh = (atom_add_acq_rel(counter, 1) + 1 == target);
+            }
             epi_sync();
             const bool last = tick_sh != 0;
             if (last) __threadfence();
-            epi_sync();   // tick_sh may be overwritten by the next ticket only after every warp read it
             return last;
         };
         while (true) {
@@ -550,18 +616,21 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_decode_kernel(DecParams 
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
             if (++acc == C::kDbuf) { acc = 0; aphase ^= 1u; }
             if (u.kind == 0) {
-                // gate/up split: this unit's partial per pair of the key (column = the pair's token)
+                // gate/up split: this unit's partial per pair of the key (column = the pair's
+                // token); the unit whose ticket completes the tile adds the SG partials in split
+                // order, applies SwiGLU and writes h as MXFP4 terms
+                if (p.SG > 1) {
 #pragma unroll
-                for (int c = 0; c < NT; ++c) {
-                    if (c >= p.T) break;
-                    for (int jj = 0; jj < p.k; ++jj) {
-                        const int pr = c * p.k + jj, pi = pinfo[pr];
-                        if (pi >= 0 && (pi >> 5) == u.key)
-                            p.pgu[(((size_t)pr * p.MTg + u.m) * p.SG + u.s) * kBM + row] = vals[c];
+                    for (int c = 0; c < NT; ++c) {
+                        if (c >= p.T) break;
+                        for (int jj = 0; jj < p.k; ++jj) {
+                            const int pr = c * p.k + jj, pi = pinfo[pr];
+                            if (pi >= 0 && (pi >> 5) == u.key)
+                                p.pgu[(((size_t)pr * p.MTg + u.m) * p.SG + u.s) * kBM + row] = vals[c];
+                        }
                     }
+                    if (!ticket(gu_cnt + u.key * p.MTg + u.m, p.SG)) continue;
                 }
-                if (!ticket(gu_cnt + u.key * p.MTg + u.m, p.SG)) continue;
-                // the tile's last split: g and u in split order, SwiGLU, h as MXFP4 terms
 #pragma unroll
                 for (int c = 0; c < NT; ++c) {
                     if (c >= p.T) break;
@@ -570,10 +639,17 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_decode_kernel(DecParams 
                         const int pi = pinfo[c * p.k + jj];
                         if (pr0 < 0 && pi >= 0 && (pi >> 5) == u.key) pr0 = c * p.k + jj;
                     }
-                    float v = 0.f;
-                    if (pr0 >= 0) {
+                    float v = vals[c];
+                    if (pr0 >= 0 && p.SG > 1) {
                         const float* src = p.pgu + ((size_t)pr0 * p.MTg + u.m) * p.SG * kBM + row;
-                        for (int s2 = 0; s2 < p.SG; ++s2) v = (s2 == 0) ? __ldcg(src) : v + __ldcg(src + s2 * kBM);
+                        float pv[kDecMaxSplits];
+#pragma unroll
+                        for (int s2 = 0; s2 < kDecMaxSplits; ++s2)
+                            if (s2 < p.SG) pv[s2] = (s2 == u.s) ? vals[c] : __ldcg(src + s2 * kBM);
+                        v = pv[0];
+#pragma unroll
+                        for (int s2 = 1; s2 < kDecMaxSplits; ++s2)
+                            if (s2 < p.SG) v = v + pv[s2];
                     }
                     // rows 2i' = gate, 2i'+1 = up of output i' = row/2 within the tile
                     const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
@@ -617,18 +693,30 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_decode_kernel(DecParams 
                     const int pr = kplist[kbase + c];
                     p.pdn[(((size_t)pr * p.MTd + u.m) * p.SD + u.s) * kBM + row] = vals[c];
                 }
+                // the unit whose ticket completes tile m: y rows [128m, 128m + 128) of every
+                // token, per pair the splits in order, then the pairs in ascending j
                 if (!ticket(dn_cnt + u.m, n_keys * p.SD)) continue;
-                // the tile's last unit: y rows [128m, 128m + 128) of every token
                 for (int t = 0; t < p.T; ++t) {
-                    float yv = 0.f;
-                    for (int j = 0; j < p.k; ++j) {
-                        const int pr = t * p.k + j;
-                        if (pinfo[pr] < 0) continue;   // no valid slot
-                        const float* src = p.pdn + ((size_t)pr * p.MTd + u.m) * p.SD * kBM + row;
-                        float z = __ldcg(src);
-                        for (int s2 = 1; s2 < p.SD; ++s2) z = z + __ldcg(src + s2 * kBM);
-                        yv = __fadd_rn(yv, __fmul_rn(__ldg(p.w + pr), z));
+                    float z[kMaxTopKDec];
+#pragma unroll
+                    for (int j = 0; j < kMaxTopKDec; ++j) {
+                        z[j] = 0.f;
+                        if (j < p.k && pinfo[t * p.k + j] >= 0) {
+                            const float* src = p.pdn + ((size_t)(t * p.k + j) * p.MTd + u.m) * p.SD * kBM + row;
+                            float pv[kDecMaxSplits];
+#pragma unroll
+                            for (int s2 = 0; s2 < kDecMaxSplits; ++s2)
+                                if (s2 < p.SD) pv[s2] = __ldcg(src + s2 * kBM);
+                            z[j] = pv[0];
+#pragma unroll
+                            for (int s2 = 1; s2 < kDecMaxSplits; ++s2)
+                                if (s2 < p.SD) z[j] = z[j] + pv[s2];
+                        }
                     }
+                    float yv = 0.f;
+#pragma unroll
+                    for (int j = 0; j < kMaxTopKDec; ++j)
+                        if (j < p.k && pinfo[t * p.k + j] >= 0) yv = __fadd_rn(yv, __fmul_rn(__ldg(p.w + t * p.k + j), z[j]));
                     p.y[(size_t)t * p.d + r] = f32_to_bf16(yv);
                 }
             }
@@ -656,11 +744,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_decode_kernel(DecParams 
     }
 }
 
-// K split of a K-block count: about `target` blocks per split, even splits where possible.
+// K split of a K-block count: about `target` blocks per split, at most kDecMaxSplits splits.
 void k_split(int KB, int target, int* S, int* KC) {
     int s = (KB + target - 1) / target;
-    if (s < 1) s = 1;
-    *S = s;
+    s = s < 1 ? 1 : (s > kDecMaxSplits ? kDecMaxSplits : s);
     *KC = (KB + s - 1) / s;
     *S = (KB + *KC - 1) / *KC;
 }

@@ -92,8 +92,8 @@ inline size_t stream_hcnt_off(const moe_dims*) { return kCounterWords; }
 // and per-tile tickets follow the streaming kernel's counters.  Its K splits: about
 // kDecGuSplitBlocks K blocks of d per gate/up unit, kDecDnSplitBlocks of f per down unit.
 constexpr int kTcDecodeMaxKeys = 128;
-constexpr int kDecGuSplitBlocks = 4;
-constexpr int kDecDnSplitBlocks = 3;
+constexpr int kDecGuSplitBlocks = 10;
+constexpr int kDecDnSplitBlocks = 9;
 size_t dec_counter_words(const moe_dims* m);   // ffn_decode_tc.cu
 inline size_t dec_ctr_off(const moe_dims* m) { return stream_hcnt_off(m) + kStreamMaxKeys; }
 inline size_t counter_words(const moe_dims* m) { return dec_ctr_off(m) + dec_counter_words(m); }

@@ -118,6 +118,9 @@ struct FfnParams {
     int32_t* xjob;                   // decode: next x job (row, 32-element block) to hand out
     int32_t* xready;                 // decode: x jobs finished
     int32_t* exit_ctr;
+    // polls after which a wait on another CTA's progress gives up (0: kSpinLimit); read after
+    // the wait on the kernel ahead
+    const int32_t* wait_limit;
 };
 
 // Work list: units [0, n0) are gate/up units, [n0, n0 + n1) down units, n_i = n_keys x
@@ -126,18 +129,23 @@ struct FfnParams {
 // down unit, and the keys' gate/up units (key-major order) finish in key order.
 constexpr int kUQ = 8;   // unit ids in flight from the producer to the MMA and epilogue warps
 
-// Per-NT shape of the pipeline.  B rows per tile = kTerms*NT, split into MMA groups of at
-// most 128 rows (N of one MMA).  ACC independent accumulators (K slices alternate between
-// them so the tensor core can overlap their dependency chains) and DBUF accumulator sets
-// (epilogue of one unit overlapping the next unit's MMAs) fit in TMEM columns [0, 256).
-template <int NT>
+// Per-NT shape of the pipeline, for CPS CTAs resident per SM (each with 1/CPS of the shared
+// memory and of the 512 TMEM columns).  B rows per tile = kTerms*NT, split into MMA groups of
+// at most 128 rows (N of one MMA).  ACC independent accumulators (K slices alternate between
+// them so the tensor core can overlap their dependency chains; the count depends only on NT's
+// row count, never on CPS, so a column's arithmetic is the same in every configuration) and
+// DBUF accumulator sets (epilogue of one unit overlapping the next unit's MMAs) fit in TMEM
+// columns [0, kAccCols); the scale ring follows.
+template <int NT, int CPS>
 struct GemmCfg {
+    static constexpr int kTmem = kTmemCols / CPS;            // TMEM columns of one CTA
+    static constexpr int kAccCols = kTmem / 2;
     static constexpr int kRows = kTerms * NT;
     static constexpr int kGroups = kRows > 128 ? kRows / 128 : 1;
     static constexpr int kN = kRows > 128 ? 128 : kRows;
     static constexpr int kAcc = kRows <= 64 ? 2 : 1;                    // short chains only at small N
-    static constexpr int kDbuf = 2 * kAcc * kRows <= 256 ? 2 : 1;
-    static_assert(kDbuf * kAcc * kRows <= 256, "accumulators exceed their TMEM columns");
+    static constexpr int kDbuf = 2 * kAcc * kRows <= kAccCols ? 2 : 1;
+    static_assert(kDbuf * kAcc * kRows <= kAccCols, "accumulators exceed their TMEM columns");
     static constexpr int kSfCols = 8 + 8 * kGroups;          // scale columns per K block (A + B)
     static constexpr int kBCodes = kRows * kKBytes;          // activation codes per K block
     static constexpr int kBBlk = act_block_bytes(NT);        // activation block (codes + atoms)
@@ -147,7 +155,7 @@ struct GemmCfg {
     static constexpr int kStage = kKPS * (kTileBytes + kBBlk);
     static constexpr int kH = NT * 66 * 4;                   // gate/up epilogue h tile (padded rows)
     static constexpr int kLdW = NT < 16 ? NT : 16;           // accumulator columns per tcgen05.ld
-    static constexpr int kBudget = 226 * 1024;               // dynamic smem (static use stays below 2 KB)
+    static constexpr int kBudget = CPS == 1 ? 226 * 1024 : 112 * 1024;   // dynamic smem (static stays below 2 KB)
     static constexpr int kFit = (kBudget - kH - 2048) / kStage;
     static constexpr int kStages = kFit > 8 ? 8 : kFit;
     static constexpr int kBytes = kStages * kStage + kH + 1024 /*barriers*/ + 1024 /*alignment*/;
@@ -198,9 +206,9 @@ __device__ __forceinline__ bool unit_info(const FfnParams& p, const PhaseParams&
 // unit's first weight copy, then waits (bounded) for the key's count of finished gate/up units
 // before issuing the h copy.  Decode also combines: the warp of the last down unit to write a
 // run of 32 features of y sums the token's pair rows there in ascending j.
-template <int NT>
-__global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) {
-    using C = GemmCfg<NT>;
+template <int NT, int CPS>
+__global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p) {
+    using C = GemmCfg<NT, CPS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stage_base = smem;
@@ -250,7 +258,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_sh)),
-                     "r"(kTmemCols)
+                     "r"(C::kTmem)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -297,6 +305,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     }
     // everything above overlaps the previous kernel; its outputs are read from here on
     pdl_wait();
+    unsigned dep_limit = kSpinLimit;
+    if (p.wait_limit && *p.wait_limit > 0) dep_limit = (unsigned)*p.wait_limit;
     if (warp == 0) {
         // decode: keys in order of their first pair (a slot's first appearance, then every
         // NT-th); one warp, pair i on lane i mod 32
@@ -485,7 +495,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                     unsigned spins = 0;
                     while (ld_acquire(flag) < target) {
                         if (!block) return false;
-                        if (++spins > kSpinLimit || *abortp) {
+                        if (++spins > dep_limit || *abortp) {
                             atomicOr(p.status, MOE_STATUS_TIMEOUT);
                             *abortp = 1;
                             break;   // the copies still go out, so that every stage's barrier completes
@@ -547,9 +557,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
             // Decode: every gate/up unit multiplies the same x tile, so the scale atoms of its K
             // blocks are copied into TMEM once (by the CTA's first gate/up unit, into columns
             // after the scale ring) when they fit there; later units only copy A scales.
-            const uint32_t xsf = tmem + 256 + kSfRing * C::kSfCols;
+            const uint32_t xsf = tmem + C::kAccCols + kSfRing * C::kSfCols;
             const bool xsf_fits = p.regime == kRegimeDecode &&
-                                  256 + kSfRing * C::kSfCols + p.ph[0].kblocks * 8 * C::kGroups <= kTmemCols;
+                                  C::kAccCols + kSfRing * C::kSfCols + p.ph[0].kblocks * 8 * C::kGroups <= C::kTmem;
             bool xsf_done = false;
             while (true) {
                 int unit = -1;
@@ -584,7 +594,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
                         const uint32_t sa = smem_u32(st + i * kTileBytes);
                         const uint32_t sb = smem_u32(st + C::kKPS * kTileBytes + i * C::kBBlk);
                         const uint32_t ssfa = sa + kTileCodeBytes, ssfb = sb + C::kBCodes;
-                        const uint32_t sfcol = tmem + 256 + sfring * C::kSfCols;
+                        const uint32_t sfcol = tmem + C::kAccCols + sfring * C::kSfCols;
                         const uint32_t sfb = use_xsf ? xsf + (s * C::kKPS + i) * 8 * C::kGroups : sfcol + 8;
                         tc_cp_sf(sfcol + 0, desc_sf(ssfa));
                         tc_cp_sf(sfcol + 4, desc_sf(ssfa + 512));
@@ -809,7 +819,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) mxf4_ffn_kernel(FfnParams p) 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmem) : "memory");
     if (p.exit_ctr) {
         // the last CTA to leave clears the counters for the next call
         __shared__ int last_cta;
@@ -899,30 +909,21 @@ int launch_tc_decode_split(const moe_dims* m, const moe_arena* ar, int T, const 
                          st, num_sms);
 }
 
-template <int NT>
+template <int NT, int CPS>
 static int launch_ffn(const FfnParams& p, int grid, cudaStream_t st) {
-    using C = GemmCfg<NT>;
-    if (cudaFuncSetAttribute(mxf4_ffn_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes) != cudaSuccess)
+    using C = GemmCfg<NT, CPS>;
+    if (cudaFuncSetAttribute(mxf4_ffn_kernel<NT, CPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes) !=
+        cudaSuccess)
         return MOE_ERR_LAUNCH;
-    if (launch_pdl(mxf4_ffn_kernel<NT>, dim3(grid), dim3(kThreadsGemm), (size_t)C::kBytes, st, p) != cudaSuccess)
+    if (launch_pdl(mxf4_ffn_kernel<NT, CPS>, dim3(grid), dim3(kThreadsGemm), (size_t)C::kBytes, st, p) != cudaSuccess)
         return MOE_ERR_LAUNCH;
     note_launch(1);
     return MOE_OK;
 }
 
-static int launch_ffn_nt(int NT, const FfnParams& p, int grid, cudaStream_t st) {
-    switch (NT) {
-        case 8: return launch_ffn<8>(p, grid, st);
-        case 16: return launch_ffn<16>(p, grid, st);
-        case 32: return launch_ffn<32>(p, grid, st);
-        default: return MOE_ERR_LAUNCH;
-    }
-}
-
-
 bool tc_supported(const moe_dims* m) { return m->d % kKB == 0 && m->f % kKB == 0; }
 bool tc_decode_supported(const moe_dims* m, int T) {
-    return tc_supported(m) && T >= 1 && T <= kDecodeNT && T * m->top_k <= kMaxDecodePairs;
+    return tc_supported(m) && T >= 1 && T <= kDecodeNT && T * m->top_k <= kMaxDecodePairs && m->top_k <= 8;
 }
 
 static FfnParams ffn_params(const moe_dims* m, const moe_arena* ar, int T, const int32_t* slot, int32_t* status,
@@ -970,10 +971,12 @@ int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16
     p.w = w;
     p.rows_out = b.rows;
     p.y = y;
-    const int grid = num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas;
-    // 8-row tiles up to T = 8 (five pipeline stages), 16 beyond: an MMA's columns do not
-    // depend on each other, so a token's results are the same with either
-    return launch_ffn_nt(T <= 8 ? 8 : kDecodeNT, p, grid, st);
+    p.wait_limit = ctr + kCtrWaitLimit;
+    // Two CTAs per SM (half the shared memory and TMEM each): every gate/up unit of a call at
+    // the full shape starts in the first wave.  8-row tiles up to T = 8, 16 beyond: an MMA's
+    // columns do not depend on each other, so a token's results are the same with either.
+    const int grid = 2 * (num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas);
+    return T <= 8 ? launch_ffn<8, 2>(p, grid, st) : launch_ffn<kDecodeNT, 2>(p, grid, st);
 }
 
 __global__ void plan_kernel(int E, int n, const int32_t* offsets, const int32_t* row_src, const int32_t* slot,
@@ -1001,8 +1004,9 @@ int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint1
     p.tile_group = b.plan + plan_tile_group_off(m->num_experts);
     p.grec = reinterpret_cast<const int4*>(b.plan + plan_grec_off(m->num_experts));
     p.rows_out = rows_out;
+    p.wait_limit = reinterpret_cast<int32_t*>(ws + L.counter) + kCtrWaitLimit;
     const int grid = num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas;
-    return launch_ffn_nt(kPrefillNT, p, grid, st);
+    return launch_ffn<kPrefillNT, 1>(p, grid, st);
 }
 
 }  // namespace fp4moe

@@ -104,7 +104,8 @@ size_t moe_workspace_bytes(const moe_dims* dims, int32_t T_max);
 int moe_workspace_init(const moe_dims* dims, void* ws, size_t ws_bytes, void* stream);
 
 /* Diagnostic knob for the bounded waits: after this call, every wait of an expert kernel on
- * another CTA's progress (x encoded, a key's h complete) through this workspace gives up after
+ * another CTA's progress (decode: x encoded, a key's h complete; prefill on the tensor cores:
+ * a token tile's h complete) through this workspace gives up after
  * `polls` polls instead of the default (about a second), sets MOE_STATUS_TIMEOUT and lets the
  * kernel drain its copies and return.  polls = 0 restores the default; so does
  * moe_workspace_init.  Waits on a CTA's own copies keep the default limit.  It exists so that

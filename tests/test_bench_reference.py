@@ -35,3 +35,26 @@ def test_reference_arm_other_ranks_exit_without_work():
     r = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_traffic_record_from_ncu_raw_page(tmp_path, monkeypatch):
+    """--record-traffic: mean DRAM bytes over the matching launches of ncu's raw page (header
+    row, units row, one row per launch), stamped with the digest of the decode FFN sources;
+    the bench reads it back only while that digest still matches."""
+    import bench
+    raw = tmp_path / "raw.csv"
+    raw.write_text('"ID","Kernel Name","dram__bytes_read.sum","dram__bytes_write.sum"\n'
+                   '"","","byte","byte"\n'
+                   '"0","void fp4moe::route_decode_kernel<1, 12>(RouteArgs)","4000000","1000"\n'
+                   '"1","void fp4moe::(anonymous namespace)::mxf4_decode_kernel<8>(DecParams)","113000000","2000000"\n'
+                   '"2","void fp4moe::(anonymous namespace)::mxf4_decode_kernel<8>(DecParams)","113200000","2200000"\n')
+    out = tmp_path / "rec.json"
+    monkeypatch.setattr(bench, "ROOT", str(bench.ROOT))
+    rec = bench.record_traffic(str(raw), bench.FFN_KERNEL, str(out), "ncu ...")
+    assert rec["launches"] == 2 and rec["dram_bytes_per_launch"] == 115200000
+    assert rec["digest"] == bench.sources_digest(bench.FFN_SOURCES)
+    monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(out))
+    assert bench.ffn_traffic() == 115200000
+    rec["digest"] = "0" * 16
+    out.write_text(json.dumps(rec))
+    assert bench.ffn_traffic() is None
