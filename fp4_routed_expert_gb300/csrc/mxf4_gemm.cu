@@ -134,18 +134,19 @@ constexpr int kUQ = 8;   // unit ids in flight from the producer to the MMA and 
 // at most 128 rows (N of one MMA).  ACC independent accumulators (K slices alternate between
 // them so the tensor core can overlap their dependency chains; the count depends only on NT's
 // row count, never on CPS, so a column's arithmetic is the same in every configuration) and
-// DBUF accumulator sets (epilogue of one unit overlapping the next unit's MMAs) fit in TMEM
-// columns [0, kAccCols); the scale ring follows.
+// DBUF accumulator sets (epilogue of one unit overlapping the next unit's MMAs; one set with
+// two CTAs per SM, whose few units mostly wait for h anyway) fill TMEM columns [0, kAccCols);
+// the scale ring follows, then (decode) the x scales.
 template <int NT, int CPS>
 struct GemmCfg {
     static constexpr int kTmem = kTmemCols / CPS;            // TMEM columns of one CTA
-    static constexpr int kAccCols = kTmem / 2;
     static constexpr int kRows = kTerms * NT;
     static constexpr int kGroups = kRows > 128 ? kRows / 128 : 1;
     static constexpr int kN = kRows > 128 ? 128 : kRows;
     static constexpr int kAcc = kRows <= 64 ? 2 : 1;                    // short chains only at small N
-    static constexpr int kDbuf = 2 * kAcc * kRows <= kAccCols ? 2 : 1;
-    static_assert(kDbuf * kAcc * kRows <= kAccCols, "accumulators exceed their TMEM columns");
+    static constexpr int kDbuf = (CPS == 1 && 2 * kAcc * kRows <= 256) ? 2 : 1;
+    static constexpr int kAccCols = (kDbuf * kAcc * kRows + 31) / 32 * 32;
+    static_assert(kAccCols <= kTmem / 2, "accumulators exceed their TMEM columns");
     static constexpr int kSfCols = 8 + 8 * kGroups;          // scale columns per K block (A + B)
     static constexpr int kBCodes = kRows * kKBytes;          // activation codes per K block
     static constexpr int kBBlk = act_block_bytes(NT);        // activation block (codes + atoms)
@@ -768,28 +769,11 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
                         break;
                     }
                 }
-                // quantise; a job is (column c, block b of 32 outputs i0 = 64m + 32b), one
-                // octet of lanes each (16 octets over the four warps)
-                for (int base = 0; base < u.ncols * 2; base += 16) {
-                    const int job = base + ew * 4 + (lane >> 3), sl = lane & 7;
-                    const bool act = job < u.ncols * 2;
-                    const int c = act ? job >> 1 : 0, b = job & 1;
-                    float v[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) v[i] = act ? hbuf[hidx(c, 32 * b + 4 * sl + i)] : 0.f;
-                    uint32_t wd[kTerms], scl[kTerms];
-                    octet_quantize32(v, lane, wd, scl);
-                    if (!act || dry) continue;
-                    const int i0 = u.m * 64 + 32 * b, kb = i0 / kKB, j = (i0 % kKB) / 32;
-                    auto write_row = [&](int htile, int hrow) {
-#pragma unroll
-                        for (int t = 0; t < kTerms; ++t) {
-                            if ((sl & 1) == 0)
-                                *reinterpret_cast<uint32_t*>(p.h + act_code_off(htile, kb, t, hrow, j, NT, KBf) + 2 * sl) =
-                                    wd[t];
-                            if (sl == 0) p.h[act_scale_off(htile, kb, t, hrow, j, NT, KBf)] = (uint8_t)scl[t];
-                        }
-                    };
+                // quantise; a job is (column c, block b of 32 outputs i0 = 64m + 32b): few jobs
+                // (decode, T <= 4) one warp each -- the shortest latency for the h hand-off --
+                // else one octet of lanes each (16 octets over the four warps); both compute
+                // the same terms
+                auto h_rows = [&](int c, auto&& write_row) {
                     if (p.regime == kRegimeDecode) {
                         // column c = token; its pairs of this key: row (pinfo & 31) of the key's h tile
                         if (c < p.T)
@@ -799,6 +783,50 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
                             }
                     } else {
                         write_row(u.btile, c);
+                    }
+                };
+                if (u.ncols * 2 <= 8) {
+                    for (int job = ew; job < u.ncols * 2; job += 4) {
+                        const int c = job >> 1, b = job & 1;
+                        uint4 codes[kTerms];
+                        uint32_t scales[kTerms];
+                        warp_quantize32(hbuf[hidx(c, 32 * b + lane)], lane, codes, scales);
+                        if (dry) continue;
+                        const int i0 = u.m * 64 + 32 * b, kb = i0 / kKB, j = (i0 % kKB) / 32;
+                        h_rows(c, [&](int htile, int hrow) {
+                            if (lane < kTerms) {
+                                // lane t writes term t (the codes of every term sit in lane 0)
+                                uint4 cv = codes[0];
+                                uint32_t sv = scales[0];
+#pragma unroll
+                                for (int t = 1; t < kTerms; ++t)
+                                    if (lane == t) { cv = codes[t]; sv = scales[t]; }
+                                *reinterpret_cast<uint4*>(p.h + act_code_off(htile, kb, lane, hrow, j, NT, KBf)) = cv;
+                                p.h[act_scale_off(htile, kb, lane, hrow, j, NT, KBf)] = (uint8_t)sv;
+                            }
+                        });
+                    }
+                } else {
+                    for (int base = 0; base < u.ncols * 2; base += 16) {
+                        const int job = base + ew * 4 + (lane >> 3), sl = lane & 7;
+                        const bool act = job < u.ncols * 2;
+                        const int c = act ? job >> 1 : 0, b = job & 1;
+                        float v[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) v[i] = act ? hbuf[hidx(c, 32 * b + 4 * sl + i)] : 0.f;
+                        uint32_t wd[kTerms], scl[kTerms];
+                        octet_quantize32(v, lane, wd, scl);
+                        if (!act || dry) continue;
+                        const int i0 = u.m * 64 + 32 * b, kb = i0 / kKB, j = (i0 % kKB) / 32;
+                        h_rows(c, [&](int htile, int hrow) {
+#pragma unroll
+                            for (int t = 0; t < kTerms; ++t) {
+                                if ((sl & 1) == 0)
+                                    *reinterpret_cast<uint32_t*>(p.h + act_code_off(htile, kb, t, hrow, j, NT, KBf) +
+                                                                 2 * sl) = wd[t];
+                                if (sl == 0) p.h[act_scale_off(htile, kb, t, hrow, j, NT, KBf)] = (uint8_t)scl[t];
+                            }
+                        });
                     }
                 }
                 // the h rows are read by the async proxy (bulk copies) of other CTAs
