@@ -44,9 +44,6 @@ int launch_gather_experts(const moe_arena* ar, const uint8_t* store, int n_store
                           const int32_t* n_missing, const int32_t* expert_to_slot, int32_t* resident_expert,
                           int32_t* status, cudaStream_t st, int num_sms);
 int launch_residual_rmsnorm(int T, int d, const uint16_t* x, const uint16_t* y, float eps, uint16_t* out, cudaStream_t st);
-int launch_tc_decode_split(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
-                           const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
-                           int num_sms);
 int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                       const int32_t* offsets, const int32_t* row_src, float* rows_out, int32_t* status, char* ws,
                       const WsLayout& L, cudaStream_t st, int num_sms);

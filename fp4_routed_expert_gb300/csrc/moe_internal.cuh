@@ -88,15 +88,8 @@ enum { kCtrRoute = 0, kCtrFfnWork = 64, kCtrFfnXReady = 65, kCtrFfnExit = 66, kC
        kCtrFfnReady = 128, kCtrFfnY = 384, kCounterWords = 2432 };
 constexpr int kStreamMaxKeys = kDecodeMaxT * kMaxTopK;   // keys of a decode call: at most one per pair
 inline size_t stream_hcnt_off(const moe_dims*) { return kCounterWords; }
-// The tensor-core decode kernel (T*k <= kTcDecodeMaxKeys pairs): its work, x and exit counters
-// and per-tile tickets follow the streaming kernel's counters.  Its K splits: about
-// kDecGuSplitBlocks K blocks of d per gate/up unit, kDecDnSplitBlocks of f per down unit.
-constexpr int kTcDecodeMaxKeys = 128;
-constexpr int kDecGuSplitBlocks = 10;
-constexpr int kDecDnSplitBlocks = 9;
-size_t dec_counter_words(const moe_dims* m);   // ffn_decode_tc.cu
-inline size_t dec_ctr_off(const moe_dims* m) { return stream_hcnt_off(m) + kStreamMaxKeys; }
-inline size_t counter_words(const moe_dims* m) { return dec_ctr_off(m) + dec_counter_words(m); }
+constexpr int kTcDecodeMaxKeys = 128;   // pairs (T*k) of a decode call on the tensor cores at most
+inline size_t counter_words(const moe_dims* m) { return stream_hcnt_off(m) + kStreamMaxKeys; }
 
 // Prefill activation tiles: kPrefillNT permuted rows each (tensor-core path).  The plan of a
 // prefill call (written by plan_kernel) describes the expert groups and their tiles:

@@ -912,29 +912,10 @@ static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& 
     return b;
 }
 
-size_t dec_partial_bytes(const moe_dims* m, int T);   // ffn_decode_tc.cu
-
 size_t tc_workspace_bytes(const moe_dims* m, int T) {
     const size_t R = (size_t)(T > 0 ? T : 1) * m->top_k;
     return align256(act_bytes_x(m, T)) + align256(act_bytes_h(m, T)) + align256(counters_of(m, T) * 4) +
-           align256(R * m->d * 4) + align256(dec_partial_bytes(m, T));
-}
-
-int launch_dec_tc(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
-                  const float* w, uint16_t* y, int32_t* status, uint8_t* xq, uint8_t* hq, float* partials,
-                  int32_t* ctr, const int32_t* wait_limit, cudaStream_t st, int num_sms);   // ffn_decode_tc.cu
-
-// Decode on the tensor cores with the split-K dataflow kernel: its activation tiles are the
-// tensor-core section's x and h buffers, its partial sums follow the per-row outputs.
-int launch_tc_decode_split(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
-                           const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
-                           int num_sms) {
-    TcBuffers b = tc_buffers(m, T, ws, L);
-    const size_t R = (size_t)(T > 0 ? T : 1) * m->top_k;
-    float* partials = reinterpret_cast<float*>(reinterpret_cast<char*>(b.rows) + align256(R * m->d * 4));
-    int32_t* ctr = reinterpret_cast<int32_t*>(ws + L.counter);
-    return launch_dec_tc(m, ar, T, x, slot, w, y, status, b.x, b.h, partials, ctr + dec_ctr_off(m), ctr + kCtrWaitLimit,
-                         st, num_sms);
+           align256(R * m->d * 4);
 }
 
 template <int NT, int CPS>
