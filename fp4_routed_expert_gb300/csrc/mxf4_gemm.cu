@@ -140,23 +140,32 @@ constexpr int kUQ = 8;   // unit ids in flight from the producer to the MMA and 
 template <int NT, int CPS>
 struct GemmCfg {
     static constexpr int kTmem = kTmemCols / CPS;            // TMEM columns of one CTA
-    static constexpr int kRows = kTerms * NT;
-    static constexpr int kGroups = kRows > 128 ? kRows / 128 : 1;
-    static constexpr int kN = kRows > 128 ? 128 : kRows;
+    static constexpr int kRows = kTerms * NT;                // B rows = N of one MMA (<= 256)
+    static_assert(kRows <= 256 && kRows % 16 == 0, "one MMA covers every B row");
+    static constexpr int kN = kRows;
+    // B scales: one 32x128b copy per 128 B rows (group g) and half of a K block's eight
+    // 32-element blocks (jq); the MMA of K slice j reads from column base + kBsfQ * (j / 2) and,
+    // for B rows 128.., four columns further (the layout of one MMA with N > 128, checked on
+    // GB300 against a host product).  Wide tiles keep every base a multiple of 16 columns.
+    static constexpr int kSg = (kRows + 127) / 128;
+    static constexpr int kBsfQ = kSg == 1 ? 4 : 16;
+    static constexpr int kSfB = kSg == 1 ? 8 : 16;           // B scales' offset in a ring slot
+    static constexpr int kSfCols = kSfB + 2 * kBsfQ;         // scale columns per K block (A + B)
     static constexpr int kAcc = kRows <= 64 ? 2 : 1;                    // short chains only at small N
-    static constexpr int kDbuf = (CPS == 1 && 2 * kAcc * kRows <= 256) ? 2 : 1;
+    static constexpr int kDbuf = (CPS == 1 && 2 * kAcc * kRows + kSfRing * kSfCols <= kTmem) ? 2 : 1;
     static constexpr int kAccCols = (kDbuf * kAcc * kRows + 31) / 32 * 32;
-    static_assert(kAccCols <= kTmem / 2, "accumulators exceed their TMEM columns");
-    static constexpr int kSfCols = 8 + 8 * kGroups;          // scale columns per K block (A + B)
+    static_assert(kAccCols + kSfRing * kSfCols <= kTmem, "accumulators and scales exceed the TMEM columns");
     static constexpr int kBCodes = kRows * kKBytes;          // activation codes per K block
     static constexpr int kBBlk = act_block_bytes(NT);        // activation block (codes + atoms)
-    static constexpr int kKPS = 2;                           // K blocks per stage
+    static constexpr int kH = NT * 66 * 4;                   // gate/up epilogue h tile (padded rows)
+    static constexpr int kBudget = CPS == 1 ? 226 * 1024 : 112 * 1024;   // dynamic smem (static stays below 2 KB)
+    // K blocks per stage: two (fewer, larger copies) unless that leaves a one-CTA-per-SM
+    // pipeline fewer than three stages
+    static constexpr int kKPS = (CPS == 2 || (kBudget - kH - 2048) / (2 * (kTileBytes + kBBlk)) >= 3) ? 2 : 1;
     // stage: kKPS weight tiles (kTileBytes each), then kKPS activation blocks; every operand
     // start is a multiple of 1024 bytes
     static constexpr int kStage = kKPS * (kTileBytes + kBBlk);
-    static constexpr int kH = NT * 66 * 4;                   // gate/up epilogue h tile (padded rows)
     static constexpr int kLdW = NT < 16 ? NT : 16;           // accumulator columns per tcgen05.ld
-    static constexpr int kBudget = CPS == 1 ? 226 * 1024 : 112 * 1024;   // dynamic smem (static stays below 2 KB)
     static constexpr int kFit = (kBudget - kH - 2048) / kStage;
     static constexpr int kStages = kFit > 8 ? 8 : kFit;
     static constexpr int kBytes = kStages * kStage + kH + 1024 /*barriers*/ + 1024 /*alignment*/;
@@ -560,7 +569,7 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
             // after the scale ring) when they fit there; later units only copy A scales.
             const uint32_t xsf = tmem + C::kAccCols + kSfRing * C::kSfCols;
             const bool xsf_fits = p.regime == kRegimeDecode &&
-                                  C::kAccCols + kSfRing * C::kSfCols + p.ph[0].kblocks * 8 * C::kGroups <= C::kTmem;
+                                  C::kSg == 1 && C::kAccCols + kSfRing * C::kSfCols + p.ph[0].kblocks * 8 <= C::kTmem;
             bool xsf_done = false;
             while (true) {
                 int unit = -1;
@@ -596,27 +605,23 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
                         const uint32_t sb = smem_u32(st + C::kKPS * kTileBytes + i * C::kBBlk);
                         const uint32_t ssfa = sa + kTileCodeBytes, ssfb = sb + C::kBCodes;
                         const uint32_t sfcol = tmem + C::kAccCols + sfring * C::kSfCols;
-                        const uint32_t sfb = use_xsf ? xsf + (s * C::kKPS + i) * 8 * C::kGroups : sfcol + 8;
+                        const uint32_t sfb = use_xsf ? xsf + (s * C::kKPS + i) * 8 : sfcol + C::kSfB;
                         tc_cp_sf(sfcol + 0, desc_sf(ssfa));
                         tc_cp_sf(sfcol + 4, desc_sf(ssfa + 512));
                         if (!(use_xsf && xsf_done)) {
 #pragma unroll
-                            for (int g = 0; g < C::kGroups; ++g) {
-                                tc_cp_sf(sfb + 8 * g, desc_sf(ssfb + g * 1024));
-                                tc_cp_sf(sfb + 8 * g + 4, desc_sf(ssfb + g * 1024 + 512));
+                            for (int g = 0; g < C::kSg; ++g) {
+                                tc_cp_sf(sfb + 4 * g, desc_sf(ssfb + g * 1024));
+                                tc_cp_sf(sfb + C::kBsfQ + 4 * g, desc_sf(ssfb + g * 1024 + 512));
                             }
                         }
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const int a = j % C::kAcc;
-                            const uint64_t ad = desc_sw128(sa + 32 * j);
                             const uint32_t accumulate = (s > 0 || i > 0 || j >= C::kAcc) ? 1u : 0u;
-#pragma unroll
-                            for (int g = 0; g < C::kGroups; ++g) {
-                                const uint64_t bd = desc_sw128(sb + g * 128 * kKBytes + 32 * j);
-                                mma_mxf4(dset + a * C::kRows + g * 128, ad, bd, (j & 1) ? idesc_hi : idesc_lo,
-                                         sfcol + 4 * (j >> 1), sfb + 8 * g + 4 * (j >> 1), accumulate);
-                            }
+                            mma_mxf4(dset + a * C::kRows, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j),
+                                     (j & 1) ? idesc_hi : idesc_lo, sfcol + 4 * (j >> 1), sfb + C::kBsfQ * (j >> 1),
+                                     accumulate);
                         }
                         sfring = (sfring + 1) % kSfRing;
                     }
