@@ -98,7 +98,7 @@ inline size_t counter_words(const moe_dims* m) { return stream_hcnt_off(m) + kSt
 //   int32 tile_group[max_tiles] at plan_tile_group_off(E): the group of each tile,
 //   int32 pair_row[n] at plan_pair_off(E, max_tiles): the tile row of pair t*k + j
 //         (tile * tile_rows + row), -1 for a pair that has no row.
-constexpr int kPrefillNT = 48;
+constexpr int kPrefillNT = 64;
 inline size_t act_tiles(const moe_dims* m, int T) {
     const size_t n = (size_t)(T > 0 ? T : 1) * m->top_k;
     const size_t t = (n + kPrefillNT - 1) / kPrefillNT + (n < (size_t)m->num_experts ? n : (size_t)m->num_experts);
