@@ -712,61 +712,85 @@ __global__ void route_norms_kernel(RouteArgs a) {
     }
 }
 
-// 64 tokens x 64 experts per block, 4x4 per thread, K staged 32 at a time.  Each output is
-// accumulated in chunks of 256 products (fresh partial sums) added into a running total, so
-// every rounding path has at most 256 + ceil(d/256) roundings.  The epilogue turns each
-// logit into its key record with the Cauchy-Schwarz bound (norms computed beforehand).
-constexpr int kTileT = 64, kTileE = 64, kRouteTileK = 32, kChunkK = 256;
+// 128 tokens x 64 experts per block, 8 tokens x 4 experts per thread, K staged 32 at a time
+// (the next step's operands are loaded into registers while the current one is multiplied).
+// Each output is accumulated in chunks of 256 products (fresh partial sums, products in
+// ascending K) added into a running total, so every rounding path has at most 256 + ceil(d/256)
+// roundings.  The epilogue turns each logit into its key record with the Cauchy-Schwarz bound
+// (norms computed beforehand).
+constexpr int kTileT = 128, kTileE = 64, kRouteTileK = 32, kChunkK = 256;
 
-__global__ void __launch_bounds__(256) route_tiled_kernel(RouteArgs a) {
-    __shared__ float xs[kRouteTileK][kTileT + 4];
-    __shared__ float ws[kRouteTileK][kTileE + 4];
-    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+__global__ void __launch_bounds__(256, 2) route_tiled_kernel(RouteArgs a) {
+    __shared__ __align__(16) float xs[kRouteTileK][kTileT + 4];
+    __shared__ __align__(16) float ws[kRouteTileK][kTileE + 4];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.y * kTileT, e0 = blockIdx.x * kTileE;
-    float tot[4][4], part[4][4];
+    // loads: a warp takes 32 consecutive rows at one K offset, so its transposed stores hit
+    // distinct banks.  x: row 32 (w % 4) + lane, K offset 16 (w / 4), 16 values; W: row
+    // 32 (w % 2) + lane, K offset 8 (w / 2), 8 values.
+    const int xr = 32 * (warp & 3) + lane, xc = 16 * (warp >> 2);
+    const int wr = 32 * (warp & 1) + lane, wc = 8 * (warp >> 1);
+    const bool xok = t0 + xr < a.T, wok = e0 + wr < a.E;
+    const uint16_t* xp = a.x + (size_t)(t0 + xr) * a.d + xc;
+    const uint16_t* wp = a.wr + (size_t)(e0 + wr) * a.d + wc;
+    uint4 xv0, xv1, wv;
+    auto load = [&](int k0) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        xv0 = xok ? __ldg(reinterpret_cast<const uint4*>(xp + k0)) : z;
+        xv1 = xok ? __ldg(reinterpret_cast<const uint4*>(xp + k0 + 8)) : z;
+        wv = wok ? __ldg(reinterpret_cast<const uint4*>(wp + k0)) : z;
+    };
+    auto store = [&]() {
+        const uint32_t xw[8] = {xv0.x, xv0.y, xv0.z, xv0.w, xv1.x, xv1.y, xv1.z, xv1.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 8; ++i) {
+            xs[xc + 2 * i][xr] = bf16_lo(xw[i]);
+            xs[xc + 2 * i + 1][xr] = bf16_hi(xw[i]);
+        }
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ws[wc + 2 * i][wr] = bf16_lo(ww[i]);
+            ws[wc + 2 * i + 1][wr] = bf16_hi(ww[i]);
+        }
+    };
+    float tot[8][4], part[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) tot[i][j] = part[i][j] = 0.f;
+    load(0);
+    store();
+    __syncthreads();
     for (int k0 = 0; k0 < a.d; k0 += kRouteTileK) {
-        // 64 rows x 32 bf16 = 256 vectors of 8 per operand
-        {
-            const int r = tid >> 2, c = (tid & 3) * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (t0 + r < a.T) v = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + r) * a.d + k0 + c));
-            const float f8[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                                 bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) xs[c + i][r] = f8[i];
-            uint4 u = make_uint4(0, 0, 0, 0);
-            if (e0 + r < a.E) u = __ldg(reinterpret_cast<const uint4*>(a.wr + (size_t)(e0 + r) * a.d + k0 + c));
-            const float g8[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                                 bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ws[c + i][r] = g8[i];
-        }
-        __syncthreads();
+        const bool more = k0 + kRouteTileK < a.d;
+        if (more) load(k0 + kRouteTileK);
 #pragma unroll 8
         for (int kk = 0; kk < kRouteTileK; ++kk) {
-            const float4 xa = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
+            const float4 xa = *reinterpret_cast<const float4*>(&xs[kk][ty * 8]);
+            const float4 xb = *reinterpret_cast<const float4*>(&xs[kk][ty * 8 + 4]);
             const float4 wb = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
-            const float xv[4] = {xa.x, xa.y, xa.z, xa.w}, wv[4] = {wb.x, wb.y, wb.z, wb.w};
+            const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w}, wvv[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) part[i][j] = fmaf(xv[i], wv[j], part[i][j]);
+                for (int j = 0; j < 4; ++j) part[i][j] = fmaf(xv[i], wvv[j], part[i][j]);
         }
-        __syncthreads();
-        if (((k0 + kRouteTileK) % kChunkK) == 0 || k0 + kRouteTileK >= a.d) {
+        if (((k0 + kRouteTileK) % kChunkK) == 0 || !more) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) { tot[i][j] += part[i][j]; part[i][j] = 0.f; }
         }
+        __syncthreads();   // every thread is done with this step's tiles
+        if (more) {
+            store();
+            __syncthreads();
+        }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = t0 + ty * 4 + i;
+    for (int i = 0; i < 8; ++i) {
+        const int t = t0 + ty * 8 + i;
         if (t >= a.T) continue;
         const float xn = __ldg(a.xnorm + t);
 #pragma unroll
