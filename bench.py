@@ -411,6 +411,28 @@ def run_prefill(w, args, device, resident=None):
     ms = e0.elapsed_time(e1) / reps
     ids = layer.ids[:T].cpu().numpy()
     used = int(np.unique(ids[ids >= 0]).size)
+    # per-call breakdown: the same kernels in a second graph with event probes around each call
+    # (the combine issued as its own call, as the fused call launches it)
+    import fp4_routed_expert_gb300 as moe
+    rt = CudaRt()
+
+    def probed(probe):
+        with probe("route"):
+            layer.route(x, w["wr"], tab, bias)
+        with probe("permute"):
+            moe.moe_permute(layer.dims, T, layer.ids, layer.offsets, layer.row_src, layer.row_dst, layer.ws)
+        with probe("ffn (plan + A quantise + gate/up + down)"):
+            moe.moe_expert_ffn_fp4(layer.dims, layer.arena.c, T, x, layer.ids, layer.slots, layer.w, layer.offsets,
+                                   layer.row_src, layer.row_dst, 0, layer.rows, None, layer.status, layer.ws)
+        with probe("combine"):
+            moe.moe_combine(layer.dims, T, layer.rows, layer.row_dst, layer.w, y)
+
+    g2, probes = _probe_graph(stream, probed, rt)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g2.replay()
+    torch.cuda.synchronize()
+    pk = _probe_ms(rt, probes)
     peaks, kind = measured_peaks()
     hbm = float(peaks["hbm_gbs"])
     fp4 = float(peaks["bf16_tflops"]) * (13.5 / 2.25)   # FP4 dense peak = measured bf16 x nominal ratio
@@ -428,7 +450,10 @@ def run_prefill(w, args, device, resident=None):
             "roofline_fp4": {"bound": "tensor", "achieved": round(flops / (ms * 1e-3) / 1e12, 2), "peak": round(fp4, 1),
                              "unit": "TFLOP/s", "frac": round(flops / (ms * 1e-3) / 1e12 / fp4, 4),
                              "peak_source": "measured bf16 x 6 (nominal fp4/bf16 dense ratio)" if kind == "measured"
-                             else "fallback bf16 x 6"}}
+                             else "fallback bf16 x 6"},
+            "breakdown_ms": {n: round(statistics.mean(v), 4) for n, v in pk.items()},
+            "breakdown_note": "event-bracketed calls of one replay of a second graph (the combine as its own call); "
+                              "the ffn call's own kernels (plan, quantise, FFN) are split in the ncu launch list"}
 
 
 # ---------------------------------------------------------------------------- 40-layer keep-set workloads
@@ -970,6 +995,8 @@ def main():
                          "for the comparison)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="measure only the prefill chunk (profiling runs; with --experts the arena holds fewer experts)")
+    ap.add_argument("--prefill-resident", type=int, default=None,
+                    help="with --prefill-only: only the first N experts routable (the compute-bound diagnostic)")
     args = ap.parse_args()
     global E, TOKENS, ROUTER_BYTES, ALG_BYTES_PER_TOKEN
     E, TOKENS = args.experts, args.tokens
@@ -997,7 +1024,7 @@ def main():
             torch.cuda.set_device(local_rank)
             dev = torch.device("cuda", local_rank)
             out = {"metric": "prefill chunk tokens/s", "impl": "ours", "config": dict(CONFIG),
-                   "prefill": run_prefill(build_workload(dev), args, dev)}
+                   "prefill": run_prefill(build_workload(dev), args, dev, resident=args.prefill_resident)}
             print(json.dumps(out), flush=True)
         return 0
     if args.keepset_only:
