@@ -11,7 +11,7 @@ constexpr int kTerms = 4;
 constexpr int kBM = 128;              // weight rows per tile
 constexpr int kKB = 256;              // K elements per K block
 constexpr int kKBytes = 128;          // code bytes per row per stage
-constexpr int kThreadsGemm = 6 * 32;
+constexpr int kMaxEpiWarps = 8;                    // epilogue warps at most: two per TMEM lane quarter
 constexpr int kTmemCols = 512;
 constexpr int kSfRing = 2;                // scale buffers in TMEM (tcgen05.cp and MMAs run in issue order)
 constexpr int kDecodeNT = 16;             // decode tile rows at most: the tokens of x; a key's pairs of h
@@ -68,6 +68,14 @@ __device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[16]) {
                    "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
                  :
                  : "memory");
+}
+__device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[4]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]) : : "memory");
 }
 __device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[8]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"

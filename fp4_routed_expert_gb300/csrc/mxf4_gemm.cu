@@ -21,7 +21,7 @@
 //           one of the activation blocks (kTerms x NT rows + scale atoms)
 //   warp 1  MMA issuer (one lane): tcgen05.cp of the scale atoms, 4 x kTerms MMAs per
 //           K block, tcgen05.commit to release smem stages and publish accumulators
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator (double-buffered in TMEM), then
+//   warps 2..  epilogue (four, or eight over two column halves): tcgen05.ld of the accumulator, then
 //           gate/up: SwiGLU + requantisation of h into kTerms MXFP4 tiles for the down GEMM
 //           down:    fp32 rows for the fixed-order combine
 // Every wait is bounded; a timeout sets MOE_STATUS_TIMEOUT and the CTA drains and exits.
@@ -165,7 +165,14 @@ struct GemmCfg {
     // stage: kKPS weight tiles (kTileBytes each), then kKPS activation blocks; every operand
     // start is a multiple of 1024 bytes
     static constexpr int kStage = kKPS * (kTileBytes + kBBlk);
-    static constexpr int kLdW = NT < 16 ? NT : 16;           // accumulator columns per tcgen05.ld
+    // Epilogue warps: eight with one CTA per SM (two per TMEM lane quarter, each taking half of
+    // the columns: the wide prefill tiles' SwiGLU and quantisation need the issue slots), four
+    // with two CTAs per SM (a sub-partition's register file holds at most 4 x 32 threads x 128
+    // registers, and the decode epilogues are short).
+    static constexpr int kEpi = CPS == 1 ? 8 : 4;
+    static constexpr int kThreads = (2 + kEpi) * 32;
+    static constexpr int kNH = NT / (kEpi / 4);              // columns of one epilogue warp
+    static constexpr int kLdW = kNH < 16 ? kNH : 16;         // accumulator columns per tcgen05.ld
     static constexpr int kFit = (kBudget - kH - 2048) / kStage;
     static constexpr int kStages = kFit > 8 ? 8 : kFit;
     static constexpr int kBytes = kStages * kStage + kH + 1024 /*barriers*/ + 1024 /*alignment*/;
@@ -217,8 +224,9 @@ __device__ __forceinline__ bool unit_info(const FfnParams& p, const PhaseParams&
 // before issuing the h copy.  Decode also combines: the warp of the last down unit to write a
 // run of 32 features of y sums the token's pair rows there in ascending j.
 template <int NT, int CPS>
-__global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p) {
+__global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel(FfnParams p) {
     using C = GemmCfg<NT, CPS>;
+    static_assert(C::kThreads == (CPS == 1 ? 10 : 6) * 32 && C::kNH * (C::kEpi / 4) == NT, "epilogue warp layout");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stage_base = smem;
@@ -229,14 +237,12 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
     uint64_t* tfull = bars + 2 * C::kStages;     // [2] accumulator set ready
     uint64_t* tempty = tfull + 2;                // [2] accumulator set drained
     uint64_t* epibar = tempty + 2;               // [2] epilogue warps' h-tile hand-offs
-    uint64_t* fixbar = epibar + 2;               // [2] arrival-count hand-offs
-    uint64_t* uqfull = fixbar + 2;               // [kUQ] unit id written
+    uint64_t* uqfull = epibar + 2;               // [kUQ] unit id written
     uint64_t* uqempty = uqfull + kUQ;            // [kUQ] unit id read by the MMA and epilogue warps
     uint64_t* setupbar = uqempty + kUQ;          // keys of this call known
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     __shared__ int n_keys_sh, pairs_total_sh;
-    __shared__ int fix_last;
     // decode: the routing outputs of the T*k pairs and the keys.  A key is a slot's pairs, in
     // order of appearance, in chunks of at most NT: the chunk's h rows are one tile.
     __shared__ int pinfo[kMaxDecodePairs];       // pair -> key << 5 | row in the key's tile, -1: none
@@ -254,14 +260,12 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&tfull[a]), 1);
-            mbar_init(smem_u32(&tempty[a]), 4);
-            mbar_init(smem_u32(&epibar[a]), 4);
+            mbar_init(smem_u32(&tempty[a]), C::kEpi);
+            mbar_init(smem_u32(&epibar[a]), C::kEpi);
         }
-        mbar_init(smem_u32(&fixbar[0]), 4);
-        mbar_init(smem_u32(&fixbar[1]), 1);
         for (int i = 0; i < kUQ; ++i) {
             mbar_init(smem_u32(&uqfull[i]), 1);
-            mbar_init(smem_u32(&uqempty[i]), 5);
+            mbar_init(smem_u32(&uqempty[i]), 1 + C::kEpi);
         }
         mbar_init(smem_u32(setupbar), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -635,40 +639,15 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
             }
         }
     } else {
-        // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
+        // ---------------- epilogue (warps 2..9 -> TMEM lane quarters 2, 3, 0, 1, 2, 3, 0, 1; the
+        // first four take columns [0, NT/2), the other four [NT/2, NT))
         const int q = warp & 3;
         const int ew = warp - 2;
+        const int c_lo = (ew >> 2) * C::kNH;  // this warp's first column (two warps per quarter)
         const int row = q * 32 + lane;       // accumulator row = weight row within the tile
         int acc = 0;
-        uint32_t aphase = 0, ephase = 0, fphase = 0;
+        uint32_t aphase = 0, ephase = 0;
         const int KBf = p.f / kKB;
-        // All four warps together: add `add` to *counter after this CTA's global writes (one
-        // gpu-scope fence after the CTA hand-off); every warp learns whether that addition
-        // reached `target`.  False on a timeout.
-        auto count_arrival = [&](int32_t* counter, int add, int target, bool& last) -> bool {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&fixbar[0]));
-            if (ew == 0) {
-                const bool okw = mbar_wait(smem_u32(&fixbar[0]), fphase, abortp);
-                if (lane == 0) {
-                    int l = 0;
-                    if (okw) {
-                        l = (atom_add_acq_rel(counter, add) + add == target);
-                    } else {
-                        atomicOr(p.status, MOE_STATUS_TIMEOUT);
-                        *abortp = 1;
-                    }
-                    fix_last = l;
-                    mbar_arrive(smem_u32(&fixbar[1]));
-                }
-                __syncwarp();
-            }
-            const bool ok1 = mbar_wait(smem_u32(&fixbar[1]), fphase, abortp);
-            if (!ok1 && lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
-            fphase ^= 1u;
-            last = ok1 && fix_last;
-            return ok1;
-        };
         // Two warm-up passes first (a gate/up unit, then a down unit of key 0) with every global
         // write, atomic and hand-off disabled: they run the epilogue's instructions once while
         // the warps would idle anyway, so the first real units do not fetch them cold.  They
@@ -696,19 +675,21 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
                 break;
             }
             tc_fence_after();
-            // D[row][n] = sum over accumulators and terms of column (a*kRows + t*NT + n)
-            float vals[NT];
+            // D[row][n] = sum over accumulators and terms of column (a*kRows + t*NT + n); this
+            // warp's columns n = c_lo + cl
+            float vals[C::kNH];
 #pragma unroll
-            for (int c = 0; c < NT; ++c) vals[c] = 0.f;
+            for (int c = 0; c < C::kNH; ++c) vals[c] = 0.f;
             const uint32_t lanebase = tmem + ((uint32_t)(q * 32) << 16) + acc * C::kAcc * C::kRows;
 #pragma unroll
             for (int a = 0; a < C::kAcc; ++a)
 #pragma unroll
-                for (int c0 = 0; c0 < NT; c0 += C::kLdW) {
-                    if (c0 >= u.ncols) break;        // warp-uniform: columns past ncols are padding
+                for (int c0 = 0; c0 < C::kNH; c0 += C::kLdW) {
+                    if (c_lo + c0 >= u.ncols) break;   // warp-uniform: columns past ncols are padding
                     uint32_t tmp[kTerms][C::kLdW];
 #pragma unroll
-                    for (int t = 0; t < kTerms; ++t) tc_ld_issue(lanebase + a * C::kRows + t * NT + c0, tmp[t]);
+                    for (int t = 0; t < kTerms; ++t)
+                        tc_ld_issue(lanebase + a * C::kRows + t * NT + c_lo + c0, tmp[t]);
 #pragma unroll
                     for (int t = 0; t < kTerms; ++t) {
                         tc_wait_ld(tmp[t]);
@@ -726,20 +707,22 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
             if (ph == 1) {
                 const int r = u.m * kBM + row;    // output feature
 #pragma unroll
-                for (int c = 0; c < NT; ++c) {
+                for (int cl = 0; cl < C::kNH; ++cl) {
+                    const int c = c_lo + cl;
                     if (c >= u.ncols || dry) continue;
                     // decode: column c is row c of the key's tile, i.e. its c-th pair
                     const int row_out = (p.regime == kRegimeDecode) ? kplist[(kinfo[u.key] >> 16) + c] : u.brow0 + c;
-                    p.rows_out[(size_t)row_out * p.d + r] = vals[c];
+                    p.rows_out[(size_t)row_out * p.d + r] = vals[cl];
                 }
                 if (p.regime == kRegimeDecode && p.y) {
                     // y rows [128m + 32q, +32) are complete once every valid pair's rows there are
-                    // written: one counter per 32 features, one arrival per warp
+                    // written: one counter per 32 features, one arrival per warp with columns
                     bool last = dry;
-                    if (!dry) {
+                    const int mine = max(0, min(C::kNH, u.ncols - c_lo));
+                    if (!dry && mine > 0) {
                         __syncwarp();
                         int l = 0;
-                        if (lane == 0) l = (atom_add_acq_rel(p.ycnt + u.m * 4 + q, u.ncols) + u.ncols == pairs_total_sh);
+                        if (lane == 0) l = (atom_add_acq_rel(p.ycnt + u.m * 4 + q, mine) + mine == pairs_total_sh);
                         last = __shfl_sync(0xffffffffu, l, 0) != 0;
                     }
                     if (last) {
@@ -757,11 +740,12 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
             } else {
                 // rows 2i' = gate, 2i'+1 = up of output i' = row/2 within the tile (i = 64m + i')
 #pragma unroll
-                for (int c = 0; c < NT; ++c) {
+                for (int cl = 0; cl < C::kNH; ++cl) {
+                    const int c = c_lo + cl;
                     if (c >= u.ncols) break;
-                    const float partner = __shfl_xor_sync(0xffffffffu, vals[c], 1);
+                    const float partner = __shfl_xor_sync(0xffffffffu, vals[cl], 1);
                     if ((lane & 1) == 0) {
-                        const float g = vals[c];
+                        const float g = vals[cl];
                         hbuf[hidx(c, row >> 1)] = g / (1.0f + expf(-g)) * partner;
                     }
                 }
@@ -776,7 +760,7 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
                 }
                 // quantise; a job is (column c, block b of 32 outputs i0 = 64m + 32b): few jobs
                 // (decode, T <= 4) one warp each -- the shortest latency for the h hand-off --
-                // else one octet of lanes each (16 octets over the four warps); both compute
+                // else one octet of lanes each (32 octets over the eight warps); both compute
                 // the same terms
                 auto h_rows = [&](int c, auto&& write_row) {
                     if (p.regime == kRegimeDecode) {
@@ -791,7 +775,7 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
                     }
                 };
                 if (u.ncols * 2 <= 8) {
-                    for (int job = ew; job < u.ncols * 2; job += 4) {
+                    for (int job = ew; job < u.ncols * 2; job += C::kEpi) {
                         const int c = job >> 1, b = job & 1;
                         uint4 codes[kTerms];
                         uint32_t scales[kTerms];
@@ -812,7 +796,7 @@ __global__ void __launch_bounds__(kThreadsGemm, CPS) mxf4_ffn_kernel(FfnParams p
                         });
                     }
                 } else {
-                    for (int base = 0; base < u.ncols * 2; base += 16) {
+                    for (int base = 0; base < u.ncols * 2; base += 4 * C::kEpi) {
                         const int job = base + ew * 4 + (lane >> 3), sl = lane & 7;
                         const bool act = job < u.ncols * 2;
                         const int c = act ? job >> 1 : 0, b = job & 1;
@@ -929,7 +913,7 @@ static int launch_ffn(const FfnParams& p, int grid, cudaStream_t st) {
     if (cudaFuncSetAttribute(mxf4_ffn_kernel<NT, CPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes) !=
         cudaSuccess)
         return MOE_ERR_LAUNCH;
-    if (launch_pdl(mxf4_ffn_kernel<NT, CPS>, dim3(grid), dim3(kThreadsGemm), (size_t)C::kBytes, st, p) != cudaSuccess)
+    if (launch_pdl(mxf4_ffn_kernel<NT, CPS>, dim3(grid), dim3(C::kThreads), (size_t)C::kBytes, st, p) != cudaSuccess)
         return MOE_ERR_LAUNCH;
     note_launch(1);
     return MOE_OK;
