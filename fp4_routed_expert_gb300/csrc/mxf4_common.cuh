@@ -3,6 +3,8 @@
 // and the gpu-scope counter operations.
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include "moe_internal.cuh"
 
 namespace fp4moe {
@@ -91,47 +93,63 @@ __device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[8]) {
 
 // ------------------------------------------------------------------ MXFP4 multi-term quantiser
 
-// Nearest e2m1 magnitude code of |v| <= 6 (0, .5, 1, 1.5, 2, 3, 4, 6).
-__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
-    return (a >= 0.25f) + (a >= 0.75f) + (a >= 1.25f) + (a >= 1.75f) + (a >= 2.5f) + (a >= 3.5f) + (a >= 5.0f);
-}
-__device__ __forceinline__ float e2m1_mag_value(uint32_t c) {
-    return c < 4 ? 0.5f * (float)c : (float)(1u << ((c >> 1) - 1)) * (1.0f + 0.5f * (float)(c & 1u));
+// Term t of a 32-element block takes the residual r left by terms 0..t-1: scale 2^e with e the
+// smallest integer such that max|r| <= 6 * 2^e (clamped to the UE8M0 range; a block whose
+// residual maximum is subnormal or zero gets e = -127 and all-zero codes), codes = r / 2^e
+// rounded to the nearest e2m1 value (ties to even: the hardware conversion), and the next
+// residual is r minus the coded value (exact).  From the block maximum's bit pattern: the
+// scale byte, 2^-e (0 when e = -127) and 2^e.
+__device__ __forceinline__ void term_scale(uint32_t amax_bits, uint32_t& sc, float& inv, float& scl) {
+    int e = -127;
+    if ((amax_bits >> 23) != 0u) {                                   // normal amax
+        const int e0 = (int)((amax_bits >> 23) & 0xFF) - 127;        // floor(log2 amax)
+        const float m = __uint_as_float((amax_bits & 0x007FFFFFu) | 0x3F800000u);   // amax / 2^e0 in [1, 2)
+        e = (m <= 1.5f) ? e0 - 2 : e0 - 1;                           // amax <= 6 * 2^e, minimal e
+    }
+    e = max(-127, min(127, e));
+    sc = (uint32_t)(e + 127);
+    inv = (e >= -126 && e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : 0.f;   // 2^-e
+    scl = (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
-// One warp quantises one 32-element block (lane i holds element i) into kTerms MXFP4
-// terms.  Term t takes the residual r left by terms 0..t-1: scale 2^e with e the smallest
-// integer such that max|r| <= 6 * 2^e (clamped to the UE8M0 range), codes = nearest e2m1
-// of r/2^e.  Lane 0 receives the 16 code bytes of every term in codes[t]; every lane
-// receives the scale bytes.
-__device__ __forceinline__ void warp_quantize32(float v, int lane, uint4* codes /*[kTerms], lane 0*/,
+// Two values (|q| <= 6) -> one byte of e2m1 codes (lo in the low nibble), nearest with ties to
+// even, and the two coded values.
+__device__ __forceinline__ uint32_t e2m1x2_code(float lo, float hi, float& vlo, float& vhi) {
+    uint32_t byte, h2;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %2, %3;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, t;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(byte), "=r"(h2)
+        : "f"(hi), "f"(lo));
+    float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+    vlo = f.x;
+    vhi = f.y;
+    return byte;
+}
+
+// One warp quantises one 32-element block (lane i holds element i) into kTerms MXFP4 terms.
+// Every lane receives the 16 code bytes of every term in codes[t] and the scale bytes.
+__device__ __forceinline__ void warp_quantize32(float v, int lane, uint4* codes /*[kTerms]*/,
                                                 uint32_t* scales /*[kTerms]*/) {
 #pragma unroll
     for (int t = 0; t < kTerms; ++t) {
         // max |v| over the warp: magnitudes order like their bit patterns as unsigned integers
         const uint32_t u = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
-        int e = -127;
-        if ((u >> 23) != 0u) {                                   // normal amax; subnormal residuals are dropped
-            const int e0 = (int)((u >> 23) & 0xFF) - 127;        // floor(log2 amax)
-            const float m = __uint_as_float((u & 0x007FFFFFu) | 0x3F800000u);   // amax / 2^e0 in [1, 2)
-            e = (m <= 1.5f) ? e0 - 2 : e0 - 1;                   // amax <= 6 * 2^e, minimal e
-        }
-        e = max(-127, min(127, e));
-        scales[t] = (uint32_t)(e + 127);
-        const float inv = (e >= -126 && e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : 0.f;   // 2^-e
-        const float sc = (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
-        const float q = v * inv;
-        const uint32_t c = e2m1_mag_code(fminf(fabsf(q), 6.0f));
-        const float val = e2m1_mag_value(c) * sc;
-        const bool neg = q < 0.f && c;
-        v -= neg ? -val : val;
-        uint32_t nib = (c | (neg ? 8u : 0u)) << (4 * (lane & 7));
-        nib |= __shfl_xor_sync(0xffffffffu, nib, 1);
-        nib |= __shfl_xor_sync(0xffffffffu, nib, 2);
-        nib |= __shfl_xor_sync(0xffffffffu, nib, 4);              // lanes 8w.. hold word w
-        const uint32_t w1 = __shfl_sync(0xffffffffu, nib, 8), w2 = __shfl_sync(0xffffffffu, nib, 16),
-                       w3 = __shfl_sync(0xffffffffu, nib, 24);
-        codes[t] = make_uint4(nib, w1, w2, w3);
+        float inv, scl;
+        term_scale(u, scales[t], inv, scl);
+        // lanes 2i and 2i+1 code their pair together; the even lane holds the byte
+        const float q = v * inv, qn = __shfl_xor_sync(0xffffffffu, q, 1);
+        float vlo, vhi;
+        const uint32_t byte = e2m1x2_code((lane & 1) ? qn : q, (lane & 1) ? q : qn, vlo, vhi);
+        v -= ((lane & 1) ? vhi : vlo) * scl;
+        uint32_t w = (lane & 1) ? 0u : byte << (8 * ((lane >> 1) & 3));
+        w |= __shfl_xor_sync(0xffffffffu, w, 1);
+        w |= __shfl_xor_sync(0xffffffffu, w, 2);
+        w |= __shfl_xor_sync(0xffffffffu, w, 4);                     // lanes 8w..8w+7 hold word w
+        const uint32_t w1 = __shfl_sync(0xffffffffu, w, 8), w2 = __shfl_sync(0xffffffffu, w, 16),
+                       w3 = __shfl_sync(0xffffffffu, w, 24);
+        codes[t] = make_uint4(w, w1, w2, w3);
     }
 }
 
@@ -143,27 +161,17 @@ __device__ __forceinline__ void thread_quantize32(float (&v)[32], uint32_t (&w)[
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        int e = -127;
-        const uint32_t u = __float_as_uint(amax);
-        if ((u >> 23) != 0u) {
-            const int e0 = (int)((u >> 23) & 0xFF) - 127;
-            const float m = __uint_as_float((u & 0x007FFFFFu) | 0x3F800000u);
-            e = (m <= 1.5f) ? e0 - 2 : e0 - 1;
-        }
-        e = max(-127, min(127, e));
-        sc[t] = (uint32_t)(e + 127);
-        const float inv = (e >= -126 && e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : 0.f;
-        const float scl = (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
+        float inv, scl;
+        term_scale(__float_as_uint(amax), sc[t], inv, scl);
 #pragma unroll
         for (int k = 0; k < 4; ++k) w[t][k] = 0u;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float q = v[i] * inv;
-            const uint32_t c = e2m1_mag_code(fminf(fabsf(q), 6.0f));
-            const float val = e2m1_mag_value(c) * scl;
-            const bool neg = q < 0.f && c;
-            v[i] -= neg ? -val : val;
-            w[t][i >> 3] |= (c | (neg ? 8u : 0u)) << (4 * (i & 7));
+        for (int i = 0; i < 32; i += 2) {
+            float vlo, vhi;
+            const uint32_t byte = e2m1x2_code(v[i] * inv, v[i + 1] * inv, vlo, vhi);
+            v[i] -= vlo * scl;
+            v[i + 1] -= vhi * scl;
+            w[t][i >> 3] |= byte << (4 * (i & 7));
         }
     }
 }
@@ -180,27 +188,17 @@ __device__ __forceinline__ void octet_quantize32(float (&v)[4], int lane, uint32
         u = max(u, __shfl_xor_sync(0xffffffffu, u, 1));
         u = max(u, __shfl_xor_sync(0xffffffffu, u, 2));
         u = max(u, __shfl_xor_sync(0xffffffffu, u, 4));
-        int e = -127;
-        if ((u >> 23) != 0u) {
-            const int e0 = (int)((u >> 23) & 0xFF) - 127;
-            const float m = __uint_as_float((u & 0x007FFFFFu) | 0x3F800000u);
-            e = (m <= 1.5f) ? e0 - 2 : e0 - 1;
-        }
-        e = max(-127, min(127, e));
-        sc[t] = (uint32_t)(e + 127);
-        const float inv = (e >= -126 && e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : 0.f;
-        const float scl = (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
-        uint32_t half = 0u;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float q = v[i] * inv;
-            const uint32_t c = e2m1_mag_code(fminf(fabsf(q), 6.0f));
-            const float val = e2m1_mag_value(c) * scl;
-            const bool neg = q < 0.f && c;
-            v[i] -= neg ? -val : val;
-            half |= (c | (neg ? 8u : 0u)) << (4 * i);
-        }
+        float inv, scl;
+        term_scale(u, sc[t], inv, scl);
+        float a0, a1, b0, b1;
+        const uint32_t lo = e2m1x2_code(v[0] * inv, v[1] * inv, a0, a1);
+        const uint32_t hi = e2m1x2_code(v[2] * inv, v[3] * inv, b0, b1);
+        v[0] -= a0 * scl;
+        v[1] -= a1 * scl;
+        v[2] -= b0 * scl;
+        v[3] -= b1 * scl;
         // elements 4s..4s+3 are nibbles 4(s&1).. of word s/2
+        const uint32_t half = lo | (hi << 8);
         const uint32_t other = __shfl_xor_sync(0xffffffffu, half, 1);
         word[t] = (lane & 1) ? 0u : (half | (other << 16));
     }
