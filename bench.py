@@ -67,9 +67,9 @@ def env_rank():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
-FFN_SOURCES = ("fp4_routed_expert_gb300/csrc/mxf4_gemm.cu", "fp4_routed_expert_gb300/csrc/mxf4_common.cuh",
+FFN_SOURCES = ("fp4_routed_expert_gb300/csrc/mxf4_decode.cu", "fp4_routed_expert_gb300/csrc/mxf4_common.cuh",
                "fp4_routed_expert_gb300/csrc/moe_internal.cuh")
-FFN_KERNEL = "mxf4_ffn_kernel"
+FFN_KERNEL = "mxf4_decode_kernel"
 TRAFFIC_RECORD = "profiles/traffic_expert_ffn_decode_T1_d5120_f2304_E384_k6.json"
 
 

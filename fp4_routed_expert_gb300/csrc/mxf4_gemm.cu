@@ -325,117 +325,8 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
         // decode: keys in order of their first pair (a slot's first appearance, then every
         // NT-th); one warp, pair i on lane i mod 32
         if (p.regime == kRegimeDecode) {
-            const int n = p.T * p.k;   // <= kMaxDecodePairs, checked on the host
-            if (n <= 32) {
-                // one pair per lane, in registers: a slot's pairs are found by one match, a
-                // pair's occurrence is the count of its slot's lanes below it
-                const unsigned below = (1u << lane) - 1u;
-                const int s = lane < n ? p.slot[lane] : -1;
-                const bool ok = lane < n && s >= 0 && s < p.num_slots;
-                if (lane < n && s >= p.num_slots && blockIdx.x == 0) atomicOr(p.status, MOE_STATUS_BAD_SLOT);
-                const unsigned peers = __match_any_sync(0xffffffffu, ok ? s : -1 - lane);
-                const int occ = __popc(peers & below), tot = __popc(peers);
-                const bool start = ok && (occ % NT) == 0;
-                const unsigned bal = __ballot_sync(0xffffffffu, start);
-                const int mykey = start ? __popc(bal & below) : 0;
-                // the lane that starts this pair's key: the (occ0 + 1)-th lane of its slot
-                const int src = (ok && !start) ? (int)__fns(peers, 0, occ - occ % NT + 1) : lane;
-                const int key = __shfl_sync(0xffffffffu, mykey, src);
-                // first kplist index of each key: exclusive scan of the key sizes, key order =
-                // lane order of the starting pairs
-                const int csize = start ? min(NT, tot - occ) : 0;
-                int inc = csize;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, inc, o);
-                    if (lane >= o) inc += y;
-                }
-                const int base = __shfl_sync(0xffffffffu, inc - csize, src);
-                if (lane < n) pinfo[lane] = ok ? ((key << 5) | (occ % NT)) : -1;
-                if (start) {
-                    kslot[mykey] = s;
-                    kinfo[mykey] = (base << 16) | csize;
-                }
-                if (ok) kplist[base + occ % NT] = (short)lane;
-                const unsigned okbal = __ballot_sync(0xffffffffu, ok);
-                if (lane == 0) {
-                    n_keys_sh = __popc(bal);
-                    pairs_total_sh = __popc(okbal);
-                }
-            } else {
-            int* sslot = reinterpret_cast<int*>(hbuf);   // the slots, during the setup only
-            for (int i = lane; i < n; i += 32) sslot[i] = p.slot[i];
-            __syncwarp();
-            // occurrence of each pair's slot among the pairs before it (kept in kplist for
-            // now); a pair whose occurrence is a multiple of NT starts a key
-            int ord = 0, pairs = 0;
-            for (int i0 = 0; i0 < n; i0 += 32) {
-                const int i = i0 + lane;
-                int s = -1, occ = 0, tot = 0;
-                bool ok = false;
-                if (i < n) {
-                    s = sslot[i];
-                    ok = s >= 0 && s < p.num_slots;
-                    if (s >= p.num_slots && blockIdx.x == 0) atomicOr(p.status, MOE_STATUS_BAD_SLOT);
-                    if (ok) {
-                        for (int j = 0; j < n; ++j) {
-                            const bool same = sslot[j] == s;
-                            occ += (same && j < i);
-                            tot += same;
-                        }
-                    }
-                    kplist[i] = (short)occ;
-                    pinfo[i] = -1;
-                }
-                pairs += ok;
-                const bool start = ok && (occ % NT) == 0;
-                const unsigned bal = __ballot_sync(0xffffffffu, start);
-                if (start) {
-                    const int key = ord + __popc(bal & ((1u << lane) - 1u));
-                    pinfo[i] = key << 5;
-                    kslot[key] = s;
-                    kinfo[key] = min(NT, tot - occ);   // pairs of the key (first index later)
-                }
-                ord += __popc(bal);
-            }
-            __syncwarp();
-            // the other pairs join the key started by their chunk's first pair
-            for (int i = lane; i < n; i += 32) {
-                const int s = sslot[i], occ = kplist[i];
-                if (s < 0 || s >= p.num_slots || (occ % NT) == 0) continue;
-                const int occ0 = occ - occ % NT;
-                for (int j = 0; j < i; ++j)
-                    if (sslot[j] == s && kplist[j] == occ0) {
-                        pinfo[i] = (pinfo[j] & ~31) | (occ % NT);
-                        break;
-                    }
-            }
-            __syncwarp();
-            // each key's first index in kplist: exclusive prefix sum of the key sizes
-            int carry = 0;
-            for (int k0 = 0; k0 < ord; k0 += 32) {
-                const int kk = k0 + lane;
-                const int cnt = kk < ord ? kinfo[kk] : 0;
-                int inc = cnt;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, inc, o);
-                    if (lane >= o) inc += y;
-                }
-                if (kk < ord) kinfo[kk] = ((carry + inc - cnt) << 16) | cnt;
-                carry += __shfl_sync(0xffffffffu, inc, 31);
-            }
-            __syncwarp();
-            for (int i = lane; i < n; i += 32) {
-                const int pi = pinfo[i];
-                if (pi >= 0) kplist[(kinfo[pi >> 5] >> 16) + (pi & 31)] = (short)i;
-            }
-            pairs = __reduce_add_sync(0xffffffffu, (uint32_t)pairs);
-            if (lane == 0) {
-                n_keys_sh = ord;
-                pairs_total_sh = pairs;
-            }
-            }
+            decode_key_setup<NT>(p.slot, p.T * p.k, p.num_slots, p.status, blockIdx.x == 0, lane, pinfo, kslot, kinfo,
+                                 kplist, reinterpret_cast<int*>(hbuf), n_keys_sh, pairs_total_sh);
         } else if (lane == 0) {
             n_keys_sh = p.plan[1];
             pairs_total_sh = 0;
@@ -946,35 +837,19 @@ static FfnParams ffn_params(const moe_dims* m, const moe_arena* ar, int T, const
     return p;
 }
 
-// Decode regime: one FFN launch (x quantised by the CTAs into one tile of kDecodeNT rows,
-// gate/up with SwiGLU and h quantised per (token, j) pair into its key's tile, down to one fp32
-// row per pair, fixed-order combine into y).  A token's arithmetic does not depend on the
-// other tokens of the call: every column of an MMA is its own dot product, the accumulator
-// chains (two per unit) and every epilogue step are per column.
+// Decode regime (mxf4_decode.cu): one FFN launch with the weights as the MMAs' wide operand,
+// on this workspace's x and h tiles, per-pair rows and persistent counters.
+int launch_decode_wide(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
+                       const float* w, uint16_t* y, int32_t* status, uint8_t* xq, uint8_t* hq, float* rows,
+                       int32_t* ctr, cudaStream_t st, int num_sms);
+
 int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                      const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
                      int num_sms) {
     if (T == 0) return MOE_OK;
     TcBuffers b = tc_buffers(m, T, ws, L);
-    FfnParams p = ffn_params(m, ar, T, slot, status, b);
-    p.regime = kRegimeDecode;
-    int32_t* ctr = reinterpret_cast<int32_t*>(ws + L.counter);
-    p.work = ctr + kCtrFfnWork;
-    p.xready = ctr + kCtrFfnXReady;
-    p.xjob = ctr + kCtrFfnXJob;
-    p.exit_ctr = ctr + kCtrFfnExit;
-    p.ready = ctr + kCtrFfnReady;
-    p.ycnt = ctr + kCtrFfnY;
-    p.x_src = x;
-    p.w = w;
-    p.rows_out = b.rows;
-    p.y = y;
-    p.wait_limit = ctr + kCtrWaitLimit;
-    // Two CTAs per SM (half the shared memory and TMEM each): every gate/up unit of a call at
-    // the full shape starts in the first wave.  8-row tiles up to T = 8, 16 beyond: an MMA's
-    // columns do not depend on each other, so a token's results are the same with either.
-    const int grid = 2 * (num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas);
-    return T <= 8 ? launch_ffn<8, 2>(p, grid, st) : launch_ffn<kDecodeNT, 2>(p, grid, st);
+    return launch_decode_wide(m, ar, T, x, slot, w, y, status, b.x, b.h, b.rows,
+                              reinterpret_cast<int32_t*>(ws + L.counter), st, num_sms);
 }
 
 __global__ void plan_kernel(int E, int n, const int32_t* offsets, const int32_t* row_src, const int32_t* slot,

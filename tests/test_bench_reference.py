@@ -46,8 +46,8 @@ def test_traffic_record_from_ncu_raw_page(tmp_path, monkeypatch):
     raw.write_text('"ID","Kernel Name","dram__bytes_read.sum","dram__bytes_write.sum"\n'
                    '"","","byte","byte"\n'
                    '"0","void fp4moe::route_decode_kernel<1, 12>(RouteArgs)","4000000","1000"\n'
-                   '"1","void fp4moe::mxf4_ffn_kernel<8, 2>(fp4moe::FfnParams)","113000000","2000000"\n'
-                   '"2","void fp4moe::mxf4_ffn_kernel<8, 2>(fp4moe::FfnParams)","113200000","2200000"\n')
+                   '"1","void fp4moe::mxf4_decode_kernel<8>(fp4moe::DecParams)","113000000","2000000"\n'
+                   '"2","void fp4moe::mxf4_decode_kernel<8>(fp4moe::DecParams)","113200000","2200000"\n')
     out = tmp_path / "rec.json"
     monkeypatch.setattr(bench, "ROOT", str(bench.ROOT))
     rec = bench.record_traffic(str(raw), bench.FFN_KERNEL, str(out), "ncu ...")
