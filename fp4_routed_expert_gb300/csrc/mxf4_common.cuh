@@ -71,6 +71,16 @@ __device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[16]) {
                  :
                  : "memory");
 }
+// 16x256b.x4 (16 TMEM lanes, 32 columns): thread i receives, for column group g = 0..3,
+// r[4g], r[4g+1] = lane i/4, columns 8g + 2(i%4) + {0, 1}, and r[4g+2], r[4g+3] = lane 8 + i/4,
+// the same columns (checked on GB300 against 32x32b stores).
+__device__ __forceinline__ void tc_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
 __device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[4]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -350,22 +360,5 @@ __device__ void decode_key_setup(const int32_t* __restrict__ slot, int n, int nu
         }
     }
 }
-
-// ------------------------------------------------------------------ gpu-scope counters
-
-__device__ __forceinline__ int ld_acquire(const int32_t* a) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
-    return v;
-}
-__device__ __forceinline__ int atom_add_acq_rel(int32_t* a, int v) {
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
-    return old;
-}
-__device__ __forceinline__ void red_add_release(int32_t* a, int v) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 }  // namespace fp4moe

@@ -9,8 +9,9 @@
 // instruction for N = 32 and N = 256, so this kernel puts 256 weight rows on the N side of
 // every MMA and the activations (kTerms MXFP4 terms of at most 16 tokens: <= 64 of the 128
 // rows of M) on the other: one instruction moves twice the weight bytes of a 128-row weight
-// tile.  D[m][n] is then activation row m (token-major: row = token * kTerms + term) times
-// weight row n; the epilogue adds a token's kTerms lanes.
+// tile.  D[m][n] is then activation row m times weight row n, the rows of tokens 8q..8q+7
+// in TMEM lane quarter q, term-major inside it (row = 32 (token / 8) + 8 term + token % 8), so
+// that one 16x256b load pair hands each thread all kTerms rows of one token.
 //
 // A unit is one (key, 256 weight rows) pair over the whole K: gate/up (rows 2f interleaved
 // gate/up, K = d) and down (rows d, K = f).  The weights' two 128-row tiles of one K block are
@@ -29,14 +30,15 @@ constexpr int kDecUQ = 8;
 constexpr int kDecMaxK = 8;                       // top-k of a decode call on the tensor cores at most
 
 // Activation blocks of this kernel: block (tile t, K block kb) holds kTerms * NT rows of 128
-// code bytes, row r = token * kTerms + term (codes pre-swizzled for SWIZZLE_128B by r mod 8),
-// then two 512-byte scale atoms (32-element blocks 0-3 and 4-7 of the K block).
+// code bytes, row r = 32 (token / 8) + 8 term + token % 8 (codes pre-swizzled for SWIZZLE_128B
+// by r mod 8), then two 512-byte scale atoms (32-element blocks 0-3 and 4-7 of the K block).
+__device__ __forceinline__ int dact_row(int term, int row) { return 32 * (row >> 3) + 8 * term + (row & 7); }
 __device__ __forceinline__ int64_t dact_code_off(int tile, int kb, int term, int row, int chunk, int NT, int KB) {
-    const int r = row * kTerms + term;
+    const int r = dact_row(term, row);
     return ((int64_t)tile * KB + kb) * act_block_bytes(NT) + r * 128 + (((chunk & 7) ^ (r & 7)) << 4);
 }
 __device__ __forceinline__ int64_t dact_scale_off(int tile, int kb, int term, int row, int j /*0..7*/, int NT, int KB) {
-    const int r = row * kTerms + term;
+    const int r = dact_row(term, row);
     return ((int64_t)tile * KB + kb) * act_block_bytes(NT) + kTerms * NT * 128 + (j >> 2) * 512 + (r & 31) * 16 +
            (r >> 5) * 4 + (j & 3);
 }
@@ -93,12 +95,13 @@ struct DecCfg {
     static constexpr int kXsf = kRing + kSfRing * kSlot;
 };
 
+// 5-D tensor-map load into shared memory with an L2 cache policy.
 __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
-                                            uint32_t bar) {
+                                            uint32_t bar, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, "
-        "%6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar), "l"(policy)
         : "memory");
 }
 
@@ -246,6 +249,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
         if (lane == 0) {
             int stage = 0, ready_key = -1;
             bool x_ok = false;
+            // expert weights are read once per call: first out of L2, so that what every call
+            // reads (the router rows, x, the counters) stays there
+            const uint64_t wpol = l2_evict_first();
             uint32_t phase = 0, issued = 0, issued_parity = 0;   // per-stage bit masks
             bool first = true;
             while (true) {
@@ -313,8 +319,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
                     const uint32_t st = smem_u32(stage_base + stage * C::kStage);
                     const uint32_t bar = smem_u32(&full[stage]);
                     mbar_expect_tx(bar, C::kStage);
-                    tma_load_5d(st + C::kABlk, &p.wcodes[ph], 0, 0, s, 2 * um, slot, bar);
-                    tma_load_5d(st + C::kABlk + kWCodes, &p.wscales[ph], 0, kBM, s, 2 * um, slot, bar);
+                    tma_load_5d(st + C::kABlk, &p.wcodes[ph], 0, 0, s, 2 * um, slot, bar, wpol);
+                    tma_load_5d(st + C::kABlk + kWCodes, &p.wscales[ph], 0, kBM, s, 2 * um, slot, bar, wpol);
                     if (!have_b && key_ready(false)) flush();
                     if (have_b) {
                         issue_b(s, stage);
@@ -408,7 +414,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
         // 32q.., tokens or key rows 8q..8q+7) and columns [128 half, +128)
         const int q = warp & 3, ew = warp - 2, half = ew >> 2;
         const int arow = q * 8 + (lane >> 2);   // token (gate/up) or key row (down) of this lane
-        const int term = lane & 3;
+        const int cp = lane & 3;                 // its column pair within each group of 8
         uint32_t aphase = 0, ephase = 0;
         // Two warm-up passes first (gate/up unit 0, then down unit n0) with every global write,
         // atomic and hand-off skipped: the epilogue runs once per unit, and instructions fetched
@@ -443,61 +449,54 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
                 const uint32_t lanebase = tmem + ((uint32_t)(q * 32) << 16) + C::kAcc;
                 const int r0u = 256 * um + 128 * half;   // down: first output feature of this warp
                 const int pair = (ph == 1 && arow < ncols) ? kplist[(kinfo[key] >> 16) + arow] : 0;
-                // two 32-column chunks per round: their loads land together and their
-                // shuffle chains interleave
+                // Two 32-column chunks per round, each as two 16x256b loads (lanes 0-15: terms 0
+                // and 1, lanes 16-31: terms 2 and 3 of the quarter's eight rows): thread i gets
+                // all four terms of row 8q + i/4 for columns 8g + 2(i%4) + {0, 1}, g = 0..3, and
+                // sums them as (t0 + t1) + (t2 + t3).
 #pragma unroll 1
                 for (int cc = 0; cc < 4; cc += 2) {
-                    uint32_t rr[2][2][16];
+                    uint32_t ra[2][16], rb[2][16];
                     if (!dry) {
 #pragma unroll
                         for (int c2 = 0; c2 < 2; ++c2) {
-                            tc_ld_issue(lanebase + 128 * half + 32 * (cc + c2), rr[c2][0]);
-                            tc_ld_issue(lanebase + 128 * half + 32 * (cc + c2) + 16, rr[c2][1]);
+                            tc_ld16_issue(lanebase + 128 * half + 32 * (cc + c2), ra[c2]);
+                            tc_ld16_issue(lanebase + (16u << 16) + 128 * half + 32 * (cc + c2), rb[c2]);
                         }
 #pragma unroll
                         for (int c2 = 0; c2 < 2; ++c2) {
-                            tc_wait_ld(rr[c2][0]);
-                            tc_wait_ld(rr[c2][1]);
+                            tc_wait_ld(ra[c2]);
+                            tc_wait_ld(rb[c2]);
                         }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) rr[0][0][i] = rr[0][1][i] = rr[1][0][i] = rr[1][1][i] = 0u;
+                        for (int i = 0; i < 16; ++i) ra[0][i] = ra[1][i] = rb[0][i] = rb[1][i] = 0u;
                     }
 #pragma unroll
                     for (int c2 = 0; c2 < 2; ++c2) {
                         const int c = cc + c2;
-                        const uint32_t (&r0)[16] = rr[c2][0];
-                        const uint32_t (&r1)[16] = rr[c2][1];
-                        // Sum the kTerms lanes of a token (or key row) and scatter the 32 columns:
-                        // lane (row, term t) ends with columns 8t .. 8t+7, each the same sum
-                        // (v_t + v_t^2) + (v_t^1 + v_t^3) whichever lane owns it.
-                        float a[16], v[8];
-                        const bool hi2 = (term & 2) != 0, hi1 = (term & 1) != 0;
+                        float v[4][2];   // [column group g][column 2(i%4) + e]
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float lo = __uint_as_float(r0[i]), hi = __uint_as_float(r1[i]);
-                            a[i] = (hi2 ? hi : lo) + __shfl_xor_sync(0xffffffffu, hi2 ? lo : hi, 2);
-                        }
+                        for (int g = 0; g < 4; ++g)
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            v[i] = (hi1 ? a[8 + i] : a[i]) + __shfl_xor_sync(0xffffffffu, hi1 ? a[i] : a[8 + i], 1);
+                            for (int e = 0; e < 2; ++e)
+                                v[g][e] = (__uint_as_float(ra[c2][4 * g + e]) + __uint_as_float(ra[c2][4 * g + 2 + e])) +
+                                          (__uint_as_float(rb[c2][4 * g + e]) + __uint_as_float(rb[c2][4 * g + 2 + e]));
                         if (ph == 0) {
-                            // columns 2i (gate) and 2i+1 (up): h of output 128 um + 64 half + 16 c + 4 t + i
+                            // columns 8g + 2cp (gate) and + 1 (up): h of output 128 um + 64 half + 16 c + 4 g + cp
                             if (arow < p.T) {
-                                float hv[4];
+                                float* dst = hbuf + arow * 128 + 64 * half + 16 * c + cp;
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const float g = v[2 * i];
-                                    hv[i] = g * __frcp_rn(1.0f + __expf(-g)) * v[2 * i + 1];
+                                for (int g = 0; g < 4; ++g) {
+                                    const float gt = v[g][0];
+                                    dst[4 * g] = gt * __frcp_rn(1.0f + __expf(-gt)) * v[g][1];
                                 }
-                                *reinterpret_cast<float4*>(hbuf + arow * 128 + 64 * half + 16 * c + 4 * term) =
-                                    make_float4(hv[0], hv[1], hv[2], hv[3]);
                             }
                         } else if (arow < ncols && !dry) {
                             // column n = output feature 256 um + n of this key row's pair
-                            float4* dst = reinterpret_cast<float4*>(p.rows_out + (size_t)pair * p.d + r0u + 32 * c + 8 * term);
-                            dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-                            dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+                            float* dst = p.rows_out + (size_t)pair * p.d + r0u + 32 * c + 2 * cp;
+#pragma unroll
+                            for (int g = 0; g < 4; ++g)
+                                *reinterpret_cast<float2*>(dst + 8 * g) = make_float2(v[g][0], v[g][1]);
                         }
                     }
                 }

@@ -54,6 +54,7 @@ struct RouteArgs {
     unsigned* counter;
     float bound_coef;  // prefill: gamma_L * (1 + 2^-10); decode: gamma_(c-1) + gamma_m^2 + 2^-34
     float refine_coef; // the decode bound for chunks of one product (selection's refinement)
+    int dec_epb;       // decode: experts per block and round (1 .. kDecodeWarps)
 };
 
 // ------------------------------------------------------------------ exact logit (Kulisch)
@@ -555,38 +556,47 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(RouteArgs 
 
 // ------------------------------------------------------------------ decode: one warp per expert
 
-constexpr int kDecodeWarps = 4;                 // experts per block and round
-constexpr int kDecodeGroups = 4;                // token groups at most (warps per expert)
+constexpr int kDecodeWarps = 4;                 // experts per block and round at most
+constexpr int kDecodeKS = 4;                    // warps per (expert, token group): K in four parts
+constexpr int kDecodeThreads = 512;             // threads per block at most
 constexpr size_t kDecodeSmemMax = 226 * 1024;
 
-__host__ __device__ inline size_t decode_smem_bytes(int T, int d) {
-    return (size_t)(kDecodeWarps + T) * d * 2 + 16;   // W rows, x rows, one mbarrier
+__host__ __device__ inline size_t decode_smem_bytes(int T, int d, int epb) {
+    return (size_t)(epb + T) * d * 2 + 16;   // W rows, x rows, one mbarrier
 }
 
-// Number of token groups of a decode router launch: one warp per (expert, group).
-inline int decode_groups(int T) { return T < kDecodeGroups ? T : kDecodeGroups; }
+// Number of token groups of a decode router launch: kDecodeKS warps per (expert, group).
+inline int decode_groups(int T, int epb) {
+    const int g = kDecodeThreads / (32 * epb * kDecodeKS);
+    return T < g ? T : (g > 1 ? g : 1);
+}
 
-// Key records for T <= 16 tokens.  A block takes kDecodeWarps experts per round: their router
-// rows and (once) the tokens' rows arrive in shared memory by bulk copies, then warp w works
-// on expert e0 + w % kDecodeWarps for the tokens of group w / kDecodeWarps (blockDim.x / 128
-// groups of consecutive tokens), one token at a time; a token's arithmetic does not depend on
-// its group.  Lane l owns vectors l, l+32, ...; per token it
-// keeps 8/CH compensated sums (s, c) -- one per plain FMA chunk of CH products of a vector, so
-// the chains are independent -- and sum|x w|.  The loops are kept short: this code runs once
+// Key records for T <= 16 tokens.  A block takes EPB = a.dec_epb experts per round (the
+// fewest that spread the experts over the SMs): their router rows (kept in L2 between calls)
+// and (once) the tokens' rows arrive in shared memory by bulk copies, then warp w works on
+// expert e0 + w % EPB, quarter (w / EPB) % kDecodeKS of the K range, for the tokens of group
+// w / (EPB kDecodeKS), one token at a time; a token's arithmetic does not depend on its group
+// nor on EPB.  Lane l owns vectors l, l+32, ... of its quarter; per token it keeps 8/CH
+// compensated sums (s, c) -- one per plain FMA chunk of CH products of a vector, so the chains
+// are independent -- and sum|x w|; the quarters' (sum, compensation) pairs are then added in
+// quarter order like the lanes'.  The loops are kept short: this code runs once
 // per call and is seldom in the instruction cache.  The last block to finish (a ticket on
 // a.counter, left at zero again) then selects every token's experts, one warp per token, in
 // its own shared memory.
 template <int CH, int EPL>
-__global__ void __launch_bounds__(kDecodeWarps * kDecodeGroups * 32) route_decode_kernel(RouteArgs a) {
+__global__ void __launch_bounds__(kDecodeThreads) route_decode_kernel(RouteArgs a) {
     constexpr int NCH = 8 / CH;
     extern __shared__ __align__(16) unsigned char dsm[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = (tid >> 5) % kDecodeWarps, grp = (tid >> 5) / kDecodeWarps;
-    const int ngrp = blockDim.x / (32 * kDecodeWarps);
+    __shared__ float4 part[kDecodeWarps * kDecodeMaxT * kDecodeKS];   // (S, C, A) per expert, token, quarter
+    const int EPB = a.dec_epb;
+    const int tid = threadIdx.x, lane = tid & 31, wq = tid >> 5;
+    const int warp = wq % EPB, ks = (wq / EPB) % kDecodeKS, grp = wq / (EPB * kDecodeKS);
+    const int ngrp = blockDim.x / (32 * EPB * kDecodeKS);
     const int tpg = (a.T + ngrp - 1) / ngrp, t_lo = grp * tpg, t_hi = min(a.T, t_lo + tpg);
     const int T = a.T, d = a.d, E = a.E, nvec = d / 8;
     uint16_t* ws = reinterpret_cast<uint16_t*>(dsm);
-    const uint16_t* xs = ws + (size_t)kDecodeWarps * d;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(dsm + (size_t)(kDecodeWarps + T) * d * 2);
+    const uint16_t* xs = ws + (size_t)EPB * d;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(dsm + (size_t)(EPB + T) * d * 2);
     __shared__ int abort_flag;
     pdl_trigger();   // the next kernel may launch now; it waits for this one before reading anything
     if (tid == 0) {
@@ -596,16 +606,16 @@ __global__ void __launch_bounds__(kDecodeWarps * kDecodeGroups * 32) route_decod
     }
     __syncthreads();
     uint32_t phase = 0;
-    for (int e0 = blockIdx.x * kDecodeWarps; e0 < E; e0 += gridDim.x * kDecodeWarps) {
-        const int nw = min(kDecodeWarps, E - e0);
+    for (int e0 = blockIdx.x * EPB; e0 < E; e0 += gridDim.x * EPB) {
+        const int nw = min(EPB, E - e0);
         if (tid == 0) {
-            const bool first = (e0 == (int)blockIdx.x * kDecodeWarps);
+            const bool first = (e0 == (int)blockIdx.x * EPB);
             const uint32_t rowb = (uint32_t)d * 2;
             mbar_expect_tx(smem_u32(bar), rowb * nw + (first ? rowb * T : 0u));
             if (first) bulk_g2s(smem_u32(xs), a.x, rowb * T, smem_u32(bar));
             // the block's router rows are consecutive: one copy (a bulk copy costs a fixed time
             // on top of its bytes)
-            bulk_g2s(smem_u32(ws), a.wr + (size_t)e0 * d, rowb * nw, smem_u32(bar));
+            bulk_g2s_hint(smem_u32(ws), a.wr + (size_t)e0 * d, rowb * nw, smem_u32(bar), l2_evict_last());
         }
         const int e = e0 + warp;
         const int tb = (e < E) ? a.table[e] : -1;
@@ -619,14 +629,14 @@ __global__ void __launch_bounds__(kDecodeWarps * kDecodeGroups * 32) route_decod
         phase ^= 1u;
         if (e < E) {
             const uint4* wrow = reinterpret_cast<const uint4*>(ws + (size_t)warp * d);
-            float myS = 0.f, myC = 0.f, myA = 0.f;
+            const int qv = nvec / kDecodeKS, cv_lo = ks * qv, cv_hi = cv_lo + qv;
             for (int t = t_lo; t < t_hi; ++t) {
                 const uint4* xrow = reinterpret_cast<const uint4*>(xs + (size_t)t * d);
                 float s[NCH], c[NCH], A = 0.f;
 #pragma unroll
                 for (int q = 0; q < NCH; ++q) s[q] = c[q] = 0.f;
 #pragma unroll 2
-                for (int cv = lane; cv < nvec; cv += 32) {
+                for (int cv = cv_lo + lane; cv < cv_hi; cv += 32) {
                     const uint4 wv = wrow[cv], xv = xrow[cv];
                     const float w8[8] = {bf16_lo(wv.x), bf16_hi(wv.x), bf16_lo(wv.y), bf16_hi(wv.y),
                                          bf16_lo(wv.z), bf16_hi(wv.z), bf16_lo(wv.w), bf16_hi(wv.w)};
@@ -662,9 +672,21 @@ __global__ void __launch_bounds__(kDecodeWarps * kDecodeGroups * 32) route_decod
                     Cc = __fadd_rn(__fadd_rn(Cc, C2), err);
                     A = __fadd_ru(A, __shfl_xor_sync(0xffffffffu, A, o));
                 }
-                if (lane == t - t_lo) { myS = S; myC = Cc; myA = A; }
+                if (lane == 0) part[(warp * T + t) * kDecodeKS + ks] = make_float4(S, Cc, A, 0.f);
             }
-            if (lane < t_hi - t_lo) {
+        }
+        __syncthreads();   // every quarter's pair is in part
+        if (e < E && ks == 0 && lane < t_hi - t_lo) {
+            {
+                const float4* pp = part + (warp * T + t_lo + lane) * kDecodeKS;
+                float myS = pp[0].x, myC = pp[0].y, myA = pp[0].z;
+#pragma unroll
+                for (int k2 = 1; k2 < kDecodeKS; ++k2) {
+                    float err;
+                    two_sum(myS, pp[k2].x, myS, err);
+                    myC = __fadd_rn(__fadd_rn(myC, pp[k2].y), err);
+                    myA = __fadd_ru(myA, pp[k2].z);
+                }
                 // |S + C - exact| <= coef * sum|x w| * (1 + 2^-9) + d * 2^-147
                 float delta = __fmul_ru(__fmul_ru(a.bound_coef, myA), 1.001953125f);
                 delta = __fadd_ru(delta, (float)d * 5.605193857299268e-45f);
@@ -676,12 +698,12 @@ __global__ void __launch_bounds__(kDecodeWarps * kDecodeGroups * 32) route_decod
         __syncthreads();   // the next iteration's copies overwrite the router rows
     }
     __shared__ int last_block;
-    __threadfence();   // this block's key records, before its ticket
-    __syncthreads();
-    if (tid == 0) last_block = (atomicAdd(a.counter, 1u) == gridDim.x - 1);
+    __syncthreads();   // every key record of this block is written
+    // the ticket releases this block's records and acquires every earlier block's
+    if (tid == 0)
+        last_block = (atom_add_acq_rel(reinterpret_cast<int32_t*>(a.counter), 1) == (int)gridDim.x - 1);
     __syncthreads();
     if (!last_block) return;
-    __threadfence();
     const int nsel = blockDim.x >> 5, wsel = tid >> 5;
     unsigned char* wsm = dsm + (size_t)wsel * select_smem_per_warp(E);
     float4* rec = reinterpret_cast<float4*>(wsm);
@@ -837,15 +859,23 @@ static int launch_select(const RouteArgs& a, cudaStream_t st) {
 
 // Dynamic shared memory of the decode router: the router rows and token rows of the logit
 // phase, or the selecting warps' arrays, whichever is larger.
-static size_t decode_route_smem(int T, int d, int E) {
-    const int sel_warps = std::min(kDecodeWarps * decode_groups(T), T);
-    return std::max(decode_smem_bytes(T, d), (size_t)sel_warps * select_smem_per_warp(E));
+static size_t decode_route_smem(int T, int d, int E, int epb) {
+    const int sel_warps = std::min(epb * kDecodeKS * decode_groups(T, epb), T);
+    return std::max(decode_smem_bytes(T, d, epb), (size_t)sel_warps * select_smem_per_warp(E));
+}
+// Experts per decode-router block: the fewest (at most kDecodeWarps) that cover E with one
+// block per SM.
+static int decode_epb(int E, int num_sms) {
+    const int sms = num_sms > 0 ? num_sms : 1;
+    const int e = (E + sms - 1) / sms;
+    return e < 1 ? 1 : (e > kDecodeWarps ? kDecodeWarps : e);
 }
 
 template <int CH, int EPL>
 static int launch_decode_ch(RouteArgs a, cudaStream_t st, int num_sms) {
-    const int threads = kDecodeWarps * 32 * decode_groups(a.T);
-    const size_t smem = decode_route_smem(a.T, a.d, a.E);
+    a.dec_epb = decode_epb(a.E, num_sms);
+    const int threads = a.dec_epb * kDecodeKS * 32 * decode_groups(a.T, a.dec_epb);
+    const size_t smem = decode_route_smem(a.T, a.d, a.E, a.dec_epb);
     if (smem > 48 * 1024 &&
         cudaFuncSetAttribute(route_decode_kernel<CH, EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
@@ -853,7 +883,7 @@ static int launch_decode_ch(RouteArgs a, cudaStream_t st, int num_sms) {
     const int m = a.d / 256;    // compensated steps per chain and lane
     const double coef = gamma32(CH - 1) + gamma32(m) * gamma32(m) + 1.0 / 17179869184.0;   // + 2^-34
     a.bound_coef = (float)(coef * (1.0 + 1.0 / 4096.0));                                   // rounded up
-    int blocks = (a.E + kDecodeWarps - 1) / kDecodeWarps;
+    int blocks = (a.E + a.dec_epb - 1) / a.dec_epb;
     if (num_sms > 0 && blocks > num_sms) blocks = num_sms;
     route_decode_kernel<CH, EPL><<<blocks, threads, smem, st>>>(a);
     note_launch(1);
@@ -869,7 +899,7 @@ static int launch_route_args(RouteArgs& a, cudaStream_t st, int num_sms) {
         const double coef = gamma32(0) + gamma32(m) * gamma32(m) + 1.0 / 17179869184.0;
         a.refine_coef = (float)(coef * (1.0 + 1.0 / 4096.0));
     }
-    if (a.T <= kDecodeMaxT && decode_route_smem(a.T, a.d, a.E) <= kDecodeSmemMax) {
+    if (a.T <= kDecodeMaxT && decode_route_smem(a.T, a.d, a.E, decode_epb(a.E, num_sms)) <= kDecodeSmemMax) {
         // chunks of one product for every T: a token's logits are then the same arithmetic
         // whatever the other tokens of the call (verify rows equal their decode calls)
         FP4MOE_EPL_DISPATCH(a.E, return launch_decode_ch<1, EPL>(a, st, num_sms));
