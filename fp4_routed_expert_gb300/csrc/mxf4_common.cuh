@@ -1,6 +1,6 @@
 // mxf4_common.cuh -- pieces shared by the tensor-core expert FFN kernels (sm_103a): tcgen05 /
-// TMEM wrappers, the MXFP4 multi-term quantisers of activations, the activation block layout
-// and the gpu-scope counter operations.
+// TMEM wrappers, the MXFP4 multi-term quantisers of activations and the prefill activation
+// block layout.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -19,8 +19,6 @@ constexpr int kSfRing = 2;                // scale buffers in TMEM (tcgen05.cp a
 constexpr int kDecodeNT = 16;             // decode tile rows at most: the tokens of x; a key's pairs of h
 constexpr int kMaxDecodePairs = kTcDecodeMaxKeys;   // decode calls on the tensor cores: T*k <= 128
 
-enum { kModeGateUp = 0, kModeDown = 1 };
-enum { kRegimeDecode = 0, kRegimePrefill = 1 };
 
 // ------------------------------------------------------------------ PTX wrappers
 
@@ -235,130 +233,6 @@ __device__ __forceinline__ int64_t act_scale_off(int tile, int kb, int term, int
     const int r = rr & 127;
     return ((int64_t)tile * KB + kb) * act_block_bytes(NT) + kTerms * NT * 128 + (rr >> 7) * 1024 + (j >> 2) * 512 +
            (r & 31) * 16 + (r >> 5) * 4 + (j & 3);
-}
-
-// ------------------------------------------------------------------ decode keys
-
-// Decode keys of one call (one warp, pair i = t*k + j on lane i mod 32): a key is a slot's pairs,
-// in order of their appearance, in chunks of at most NT (the rows of one activation tile).
-//   pinfo[i]  = key << 5 | row of pair i in its key's tile, -1 for a pair without a valid slot
-//   kslot[key] = slot; kinfo[key] = first kplist index << 16 | pairs; kplist = pairs per key in row order
-// n_keys and pairs_total (valid pairs) are set on lane 0.  A slot outside [0, num_slots) sets
-// MOE_STATUS_BAD_SLOT (when report) and its pair is dropped.  scratch: n ints of shared memory.
-template <int NT>
-__device__ void decode_key_setup(const int32_t* __restrict__ slot, int n, int num_slots, int32_t* status, bool report,
-                                 int lane, int* pinfo, int* kslot, int* kinfo, short* kplist, int* scratch,
-                                 int& n_keys, int& pairs_total) {
-    if (n <= 32) {
-        // one pair per lane, in registers: a slot's pairs are found by one match, a
-        // pair's occurrence is the count of its slot's lanes below it
-        const unsigned below = (1u << lane) - 1u;
-        const int s = lane < n ? slot[lane] : -1;
-        const bool ok = lane < n && s >= 0 && s < num_slots;
-        if (lane < n && s >= num_slots && report) atomicOr(status, MOE_STATUS_BAD_SLOT);
-        const unsigned peers = __match_any_sync(0xffffffffu, ok ? s : -1 - lane);
-        const int occ = __popc(peers & below), tot = __popc(peers);
-        const bool start = ok && (occ % NT) == 0;
-        const unsigned bal = __ballot_sync(0xffffffffu, start);
-        const int mykey = start ? __popc(bal & below) : 0;
-        // the lane that starts this pair's key: the (occ0 + 1)-th lane of its slot
-        const int src = (ok && !start) ? (int)__fns(peers, 0, occ - occ % NT + 1) : lane;
-        const int key = __shfl_sync(0xffffffffu, mykey, src);
-        // first kplist index of each key: exclusive scan of the key sizes, key order =
-        // lane order of the starting pairs
-        const int csize = start ? min(NT, tot - occ) : 0;
-        int inc = csize;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += y;
-        }
-        const int base = __shfl_sync(0xffffffffu, inc - csize, src);
-        if (lane < n) pinfo[lane] = ok ? ((key << 5) | (occ % NT)) : -1;
-        if (start) {
-            kslot[mykey] = s;
-            kinfo[mykey] = (base << 16) | csize;
-        }
-        if (ok) kplist[base + occ % NT] = (short)lane;
-        const unsigned okbal = __ballot_sync(0xffffffffu, ok);
-        if (lane == 0) {
-            n_keys = __popc(bal);
-            pairs_total = __popc(okbal);
-        }
-    } else {
-        int* sslot = scratch;   // the slots, during the setup only
-        for (int i = lane; i < n; i += 32) sslot[i] = slot[i];
-        __syncwarp();
-        // occurrence of each pair's slot among the pairs before it (kept in kplist for
-        // now); a pair whose occurrence is a multiple of NT starts a key
-        int ord = 0, pairs = 0;
-        for (int i0 = 0; i0 < n; i0 += 32) {
-            const int i = i0 + lane;
-            int s = -1, occ = 0, tot = 0;
-            bool ok = false;
-            if (i < n) {
-                s = sslot[i];
-                ok = s >= 0 && s < num_slots;
-                if (s >= num_slots && report) atomicOr(status, MOE_STATUS_BAD_SLOT);
-                if (ok) {
-                    for (int j = 0; j < n; ++j) {
-                        const bool same = sslot[j] == s;
-                        occ += (same && j < i);
-                        tot += same;
-                    }
-                }
-                kplist[i] = (short)occ;
-                pinfo[i] = -1;
-            }
-            pairs += ok;
-            const bool start = ok && (occ % NT) == 0;
-            const unsigned bal = __ballot_sync(0xffffffffu, start);
-            if (start) {
-                const int key = ord + __popc(bal & ((1u << lane) - 1u));
-                pinfo[i] = key << 5;
-                kslot[key] = s;
-                kinfo[key] = min(NT, tot - occ);   // pairs of the key (first index later)
-            }
-            ord += __popc(bal);
-        }
-        __syncwarp();
-        // the other pairs join the key started by their chunk's first pair
-        for (int i = lane; i < n; i += 32) {
-            const int s = sslot[i], occ = kplist[i];
-            if (s < 0 || s >= num_slots || (occ % NT) == 0) continue;
-            const int occ0 = occ - occ % NT;
-            for (int j = 0; j < i; ++j)
-                if (sslot[j] == s && kplist[j] == occ0) {
-                    pinfo[i] = (pinfo[j] & ~31) | (occ % NT);
-                    break;
-                }
-        }
-        __syncwarp();
-        // each key's first index in kplist: exclusive prefix sum of the key sizes
-        int carry = 0;
-        for (int k0 = 0; k0 < ord; k0 += 32) {
-            const int kk = k0 + lane;
-            const int cnt = kk < ord ? kinfo[kk] : 0;
-            int inc = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += y;
-            }
-            if (kk < ord) kinfo[kk] = ((carry + inc - cnt) << 16) | cnt;
-            carry += __shfl_sync(0xffffffffu, inc, 31);
-        }
-        __syncwarp();
-        for (int i = lane; i < n; i += 32) {
-            const int pi = pinfo[i];
-            if (pi >= 0) kplist[(kinfo[pi >> 5] >> 16) + (pi & 31)] = (short)i;
-        }
-        pairs = __reduce_add_sync(0xffffffffu, (uint32_t)pairs);
-        if (lane == 0) {
-            n_keys = ord;
-            pairs_total = pairs;
-        }
-    }
 }
 
 }  // namespace fp4moe

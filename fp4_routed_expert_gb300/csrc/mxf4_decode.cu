@@ -25,7 +25,8 @@ namespace fp4moe {
 constexpr int kWRows = 256;                       // weight rows per unit (N of every MMA)
 constexpr int kWCodes = kWRows * kKBytes;         // 32 KB of codes per K block
 constexpr int kWScales = 2 * kTileScaleBytes;     // the two tiles' scale atoms
-constexpr int kDecThreads = 10 * 32;              // producer, MMA issuer, eight epilogue warps
+constexpr int kDecEpi = 16;                       // epilogue warps: four per TMEM lane quarter
+constexpr int kDecThreads = (2 + kDecEpi) * 32;   // producer, MMA issuer, epilogue warps
 constexpr int kDecUQ = 8;
 constexpr int kDecMaxK = 8;                       // top-k of a decode call on the tensor cores at most
 
@@ -68,6 +69,128 @@ struct DecParams {
     int32_t* exit_ctr;
     const int32_t* wait_limit;       // polls of a wait on another CTA (0: kSpinLimit)
 };
+
+// Decode keys of one call (one warp, pair i = t*k + j on lane i mod 32): a key is a slot's pairs,
+// in order of their appearance, in chunks of at most NT (the rows of one activation tile).
+//   pinfo[i]  = key << 5 | row of pair i in its key's tile, -1 for a pair without a valid slot
+//   kslot[key] = slot; kinfo[key] = first kplist index << 16 | pairs; kplist = pairs per key in row order
+// n_keys and pairs_total (valid pairs) are set on lane 0.  A slot outside [0, num_slots) sets
+// MOE_STATUS_BAD_SLOT (when report) and its pair is dropped.  scratch: n ints of shared memory.
+template <int NT>
+__device__ void decode_key_setup(const int32_t* __restrict__ slot, int n, int num_slots, int32_t* status, bool report,
+                                 int lane, int* pinfo, int* kslot, int* kinfo, short* kplist, int* scratch,
+                                 int& n_keys, int& pairs_total) {
+    if (n <= 32) {
+        // one pair per lane, in registers: a slot's pairs are found by one match, a
+        // pair's occurrence is the count of its slot's lanes below it
+        const unsigned below = (1u << lane) - 1u;
+        const int s = lane < n ? slot[lane] : -1;
+        const bool ok = lane < n && s >= 0 && s < num_slots;
+        if (lane < n && s >= num_slots && report) atomicOr(status, MOE_STATUS_BAD_SLOT);
+        const unsigned peers = __match_any_sync(0xffffffffu, ok ? s : -1 - lane);
+        const int occ = __popc(peers & below), tot = __popc(peers);
+        const bool start = ok && (occ % NT) == 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, start);
+        const int mykey = start ? __popc(bal & below) : 0;
+        // the lane that starts this pair's key: the (occ0 + 1)-th lane of its slot
+        const int src = (ok && !start) ? (int)__fns(peers, 0, occ - occ % NT + 1) : lane;
+        const int key = __shfl_sync(0xffffffffu, mykey, src);
+        // first kplist index of each key: exclusive scan of the key sizes, key order =
+        // lane order of the starting pairs
+        const int csize = start ? min(NT, tot - occ) : 0;
+        int inc = csize;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        const int base = __shfl_sync(0xffffffffu, inc - csize, src);
+        if (lane < n) pinfo[lane] = ok ? ((key << 5) | (occ % NT)) : -1;
+        if (start) {
+            kslot[mykey] = s;
+            kinfo[mykey] = (base << 16) | csize;
+        }
+        if (ok) kplist[base + occ % NT] = (short)lane;
+        const unsigned okbal = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0) {
+            n_keys = __popc(bal);
+            pairs_total = __popc(okbal);
+        }
+    } else {
+        int* sslot = scratch;   // the slots, during the setup only
+        for (int i = lane; i < n; i += 32) sslot[i] = slot[i];
+        __syncwarp();
+        // occurrence of each pair's slot among the pairs before it (kept in kplist for
+        // now); a pair whose occurrence is a multiple of NT starts a key
+        int ord = 0, pairs = 0;
+        for (int i0 = 0; i0 < n; i0 += 32) {
+            const int i = i0 + lane;
+            int s = -1, occ = 0, tot = 0;
+            bool ok = false;
+            if (i < n) {
+                s = sslot[i];
+                ok = s >= 0 && s < num_slots;
+                if (s >= num_slots && report) atomicOr(status, MOE_STATUS_BAD_SLOT);
+                if (ok) {
+                    for (int j = 0; j < n; ++j) {
+                        const bool same = sslot[j] == s;
+                        occ += (same && j < i);
+                        tot += same;
+                    }
+                }
+                kplist[i] = (short)occ;
+                pinfo[i] = -1;
+            }
+            pairs += ok;
+            const bool start = ok && (occ % NT) == 0;
+            const unsigned bal = __ballot_sync(0xffffffffu, start);
+            if (start) {
+                const int key = ord + __popc(bal & ((1u << lane) - 1u));
+                pinfo[i] = key << 5;
+                kslot[key] = s;
+                kinfo[key] = min(NT, tot - occ);   // pairs of the key (first index later)
+            }
+            ord += __popc(bal);
+        }
+        __syncwarp();
+        // the other pairs join the key started by their chunk's first pair
+        for (int i = lane; i < n; i += 32) {
+            const int s = sslot[i], occ = kplist[i];
+            if (s < 0 || s >= num_slots || (occ % NT) == 0) continue;
+            const int occ0 = occ - occ % NT;
+            for (int j = 0; j < i; ++j)
+                if (sslot[j] == s && kplist[j] == occ0) {
+                    pinfo[i] = (pinfo[j] & ~31) | (occ % NT);
+                    break;
+                }
+        }
+        __syncwarp();
+        // each key's first index in kplist: exclusive prefix sum of the key sizes
+        int carry = 0;
+        for (int k0 = 0; k0 < ord; k0 += 32) {
+            const int kk = k0 + lane;
+            const int cnt = kk < ord ? kinfo[kk] : 0;
+            int inc = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += y;
+            }
+            if (kk < ord) kinfo[kk] = ((carry + inc - cnt) << 16) | cnt;
+            carry += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        __syncwarp();
+        for (int i = lane; i < n; i += 32) {
+            const int pi = pinfo[i];
+            if (pi >= 0) kplist[(kinfo[pi >> 5] >> 16) + (pi & 31)] = (short)i;
+        }
+        pairs = __reduce_add_sync(0xffffffffu, (uint32_t)pairs);
+        if (lane == 0) {
+            n_keys = ord;
+            pairs_total = pairs;
+        }
+    }
+}
 
 // Shape for NT token rows (8 or 16): a stage is one K block: the activation block first (the
 // MMA reads A rows 0..127 from its start; rows past kTerms * NT fall on the weights and feed
@@ -146,7 +269,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
     __shared__ int uq[kDecUQ];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    constexpr int kEpi = 8;
+    constexpr int kEpi = kDecEpi;
     if (tid == 0) {
         abort_flag = 0;
         for (int s = 0; s < C::kStages; ++s) {
@@ -411,8 +534,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
         }
     } else {
         // ---------------- epilogue: warp w reads TMEM lane quarter w mod 4 (activation rows
-        // 32q.., tokens or key rows 8q..8q+7) and columns [128 half, +128)
-        const int q = warp & 3, ew = warp - 2, half = ew >> 2;
+        // 32q.., tokens or key rows 8q..8q+7) and columns [64 sl, +64), sl = (w - 2) / 4
+        const int q = warp & 3, ew = warp - 2, sl = ew >> 2;
         const int arow = q * 8 + (lane >> 2);   // token (gate/up) or key row (down) of this lane
         const int cp = lane & 3;                 // its column pair within each group of 8
         uint32_t aphase = 0, ephase = 0;
@@ -447,20 +570,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
             tc_fence_after();
             if (q < C::kQuarters) {
                 const uint32_t lanebase = tmem + ((uint32_t)(q * 32) << 16) + C::kAcc;
-                const int r0u = 256 * um + 128 * half;   // down: first output feature of this warp
+                const int r0u = 256 * um + 64 * sl;   // down: first output feature of this warp
                 const int pair = (ph == 1 && arow < ncols) ? kplist[(kinfo[key] >> 16) + arow] : 0;
-                // Two 32-column chunks per round, each as two 16x256b loads (lanes 0-15: terms 0
-                // and 1, lanes 16-31: terms 2 and 3 of the quarter's eight rows): thread i gets
-                // all four terms of row 8q + i/4 for columns 8g + 2(i%4) + {0, 1}, g = 0..3, and
-                // sums them as (t0 + t1) + (t2 + t3).
-#pragma unroll 1
-                for (int cc = 0; cc < 4; cc += 2) {
+                // The warp's two 32-column chunks, each as two 16x256b loads (lanes 0-15: terms 0
+                // and 1, lanes 16-31: terms 2 and 3 of the quarter's eight rows), all in flight
+                // together: thread i gets all four terms of row 8q + i/4 for columns
+                // 8g + 2(i%4) + {0, 1}, g = 0..3, and sums them as (t0 + t1) + (t2 + t3).
+                {
+                    constexpr int cc = 0;
                     uint32_t ra[2][16], rb[2][16];
                     if (!dry) {
 #pragma unroll
                         for (int c2 = 0; c2 < 2; ++c2) {
-                            tc_ld16_issue(lanebase + 128 * half + 32 * (cc + c2), ra[c2]);
-                            tc_ld16_issue(lanebase + (16u << 16) + 128 * half + 32 * (cc + c2), rb[c2]);
+                            tc_ld16_issue(lanebase + 64 * sl + 32 * c2, ra[c2]);
+                            tc_ld16_issue(lanebase + (16u << 16) + 64 * sl + 32 * c2, rb[c2]);
                         }
 #pragma unroll
                         for (int c2 = 0; c2 < 2; ++c2) {
@@ -482,9 +605,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
                                 v[g][e] = (__uint_as_float(ra[c2][4 * g + e]) + __uint_as_float(ra[c2][4 * g + 2 + e])) +
                                           (__uint_as_float(rb[c2][4 * g + e]) + __uint_as_float(rb[c2][4 * g + 2 + e]));
                         if (ph == 0) {
-                            // columns 8g + 2cp (gate) and + 1 (up): h of output 128 um + 64 half + 16 c + 4 g + cp
+                            // columns 8g + 2cp (gate) and + 1 (up): h of output 128 um + 32 sl + 16 c + 4 g + cp
                             if (arow < p.T) {
-                                float* dst = hbuf + arow * 128 + 64 * half + 16 * c + cp;
+                                float* dst = hbuf + arow * 128 + 32 * sl + 16 * c + cp;
 #pragma unroll
                                 for (int g = 0; g < 4; ++g) {
                                     const float gt = v[g][0];
@@ -503,32 +626,32 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
                 if (ph == 1) {
                     // Features [r0u + 32c, +32) of y are complete once every valid pair's rows
                     // there are written: one counter per 32 features, one arrival per warp with
-                    // its row count (lane c arrives for chunk c, all four in flight at once); the
+                    // its row count (lane c arrives for chunk c, both in flight at once); the
                     // warp that completes a chunk sums it in fixed order.
                     const int mine = max(0, min(8, ncols - 8 * q));
                     if (mine > 0) {
                         __syncwarp();
                         int l = dry;
-                        if (lane < 4 && !dry)
+                        if (lane < 2 && !dry)
                             l = (atom_add_acq_rel(p.ycnt + r0u / 32 + lane, mine) + mine == pairs_total_sh);
-                        const unsigned lastm = __ballot_sync(0xffffffffu, l) & 0xFu;
+                        const unsigned lastm = __ballot_sync(0xffffffffu, l) & 0x3u;
                         if (lastm) {
                             for (int t = 0; t < p.T; ++t) {
                                 // every load of the token first, then the sums in ascending j
-                                float rv[4][kDecMaxK], wv[kDecMaxK];
+                                float rv[2][kDecMaxK], wv[kDecMaxK];
 #pragma unroll
                                 for (int jj = 0; jj < kDecMaxK; ++jj) {
                                     const int pr = t * p.k + jj;
                                     const bool ok = jj < p.k && pinfo[pr] >= 0;
                                     wv[jj] = ok ? __ldg(p.w + pr) : 0.f;
 #pragma unroll
-                                    for (int c = 0; c < 4; ++c)
+                                    for (int c = 0; c < 2; ++c)
                                         rv[c][jj] = (ok && ((lastm >> c) & 1u))
                                                         ? __ldcg(p.rows_out + (size_t)pr * p.d + r0u + 32 * c + lane)
                                                         : 0.f;
                                 }
 #pragma unroll
-                                for (int c = 0; c < 4; ++c) {
+                                for (int c = 0; c < 2; ++c) {
                                     if (!((lastm >> c) & 1u)) continue;
                                     float yv = 0.f;
 #pragma unroll

@@ -1,6 +1,6 @@
-// mxf4_gemm.cu -- expert FFN on the 5th-generation tensor cores (sm_103a): grouped
-// block-scaled MXFP4 GEMMs with tcgen05.mma (kind::mxf4), TMEM accumulators, TMA operand
-// loads and fused epilogues.
+// mxf4_gemm.cu -- the prefill expert FFN on the 5th-generation tensor cores (sm_103a): grouped
+// block-scaled MXFP4 GEMMs with tcgen05.mma (kind::mxf4), TMEM accumulators, bulk-copy operand
+// loads and fused epilogues.  (The decode regime's kernel is in mxf4_decode.cu.)
 //
 // Operands.  A = expert weight rows straight from the slot arena: e2m1 codes and UE8M0
 // scales per 32 K elements, exactly the checkpoint's format ("DeepSeek-V4.1-Flash on a
@@ -8,7 +8,8 @@
 // B = activations, written by this library as a sum of kTerms MXFP4 tensors
 // (x ~ q_1 + q_2 + ..., each q_i e2m1 codes with its own UE8M0 scale per 32 elements, q_i
 // quantising the residual left by q_1..q_(i-1)); the MMA accumulates every term into the same
-// fp32 accumulator, so D = W . x up to the residual after kTerms terms.
+// fp32 accumulator, so D = W . x up to the residual after kTerms terms.  B's rows are the
+// expert-grouped permutation of the tokens in tiles of kPrefillNT rows (N = kTerms x 64 = 256).
 //
 // Every operand sits in global memory in blocks of 256 K elements that carry their codes
 // (128-byte rows pre-swizzled for SWIZZLE_128B) followed by their scale atoms, and the blocks
@@ -16,14 +17,14 @@
 // two contiguous bulk copies (cp.async.bulk), weights and activations: a bulk copy costs the
 // SM's copy engine a fixed time on top of its bytes, so few large copies stream fastest.
 //
-// One persistent kernel, one CTA per SM, 6 warps:
+// One persistent kernel, one CTA per SM, 10 warps:
 //   warp 0  producer: per stage one bulk copy of the weight tiles (codes + scale atoms) and
 //           one of the activation blocks (kTerms x NT rows + scale atoms)
-//   warp 1  MMA issuer (one lane): tcgen05.cp of the scale atoms, 4 x kTerms MMAs per
-//           K block, tcgen05.commit to release smem stages and publish accumulators
-//   warps 2..  epilogue (four, or eight over two column halves): tcgen05.ld of the accumulator, then
-//           gate/up: SwiGLU + requantisation of h into kTerms MXFP4 tiles for the down GEMM
-//           down:    fp32 rows for the fixed-order combine
+//   warp 1  MMA issuer (one lane): tcgen05.cp of the scale atoms, 4 MMAs per K block,
+//           tcgen05.commit to release smem stages and publish accumulators
+//   warps 2..9  epilogue (two per TMEM lane quarter over column halves): tcgen05.ld of the
+//           accumulator, then gate/up: SwiGLU + requantisation of h into kTerms MXFP4 tiles for
+//           the down GEMM; down: fp32 rows for the fixed-order combine
 // Every wait is bounded; a timeout sets MOE_STATUS_TIMEOUT and the CTA drains and exits.
 #include <cuda.h>
 
@@ -91,10 +92,8 @@ struct PhaseParams {
 };
 
 struct FfnParams {
-    int regime;
     int T, k, E, num_slots;
     const int32_t* slot;             // [T*k]
-    const float* w;                  // [T*k] routing weights (decode combine)
     const int32_t* plan;             // prefill: the plan (see plan_grec_off / plan_tile_group_off)
     const int32_t* tile_group;       // prefill: group of each tile
     const int4* grec;                // prefill: {first row, end row, slot, first tile} per group
@@ -106,40 +105,28 @@ struct FfnParams {
     uint8_t* h;                      // h blocks written by phase 0, read by phase 1
     int f, d;
     float* rows_out;                 // phase 1 output rows [rows][d] (fp32)
-    uint16_t* y;                     // decode: combined output [T][d] (bf16)
     int32_t* status;
     int32_t* work;                   // next unit to hand out (zero at launch)
-    int32_t* ready;                  // phase 0 units finished, per key (decode: slot ordinal; prefill: tile)
-    int32_t* ycnt;                   // decode: pair rows finished per 32 features of y
-    // decode: x is quantised by this kernel into ph[0].b_q / b_sf (rows 0..T-1 of the NT-row
-    // tile; the padding rows only feed discarded columns); the last CTA to exit (exit ticket)
-    // clears every counter for the next call
-    const uint16_t* x_src;
-    int32_t* xjob;                   // decode: next x job (row, 32-element block) to hand out
-    int32_t* xready;                 // decode: x jobs finished
-    int32_t* exit_ctr;
+    int32_t* ready;                  // phase 0 units finished, per activation tile
     // polls after which a wait on another CTA's progress gives up (0: kSpinLimit); read after
     // the wait on the kernel ahead
     const int32_t* wait_limit;
 };
 
-// Work list: units [0, n0) are gate/up units, [n0, n0 + n1) down units, n_i = n_keys x
-// weight tiles of phase i; a unit is one (key, weight tile) pair over the whole K.  CTAs take
-// units in that order from a global counter, so every gate/up unit is handed out before any
-// down unit, and the keys' gate/up units (key-major order) finish in key order.
+// Work list: units [0, n0) are gate/up units, [n0, n0 + n1) down units, n_i = tiles x weight
+// tiles of phase i; a unit is one (weight tile, activation tile) pair over the whole K, units
+// sharing weights adjacent.  CTAs take units in that order from a global counter, so every
+// gate/up unit is handed out before any down unit.
 constexpr int kUQ = 8;   // unit ids in flight from the producer to the MMA and epilogue warps
 
-// Per-NT shape of the pipeline, for CPS CTAs resident per SM (each with 1/CPS of the shared
-// memory and of the 512 TMEM columns).  B rows per tile = kTerms*NT, split into MMA groups of
-// at most 128 rows (N of one MMA).  ACC independent accumulators (K slices alternate between
-// them so the tensor core can overlap their dependency chains; the count depends only on NT's
-// row count, never on CPS, so a column's arithmetic is the same in every configuration) and
-// DBUF accumulator sets (epilogue of one unit overlapping the next unit's MMAs; one set with
-// two CTAs per SM, whose few units mostly wait for h anyway) fill TMEM columns [0, kAccCols);
-// the scale ring follows, then (decode) the x scales.
-template <int NT, int CPS>
+// Per-NT shape of the pipeline (one CTA per SM, the whole shared memory and 512 TMEM columns).
+// B rows per tile = kTerms*NT (N of one MMA, <= 256).  ACC independent accumulators (K slices
+// alternate between them so the tensor core can overlap their dependency chains; the count
+// depends only on the row count) and DBUF accumulator sets (epilogue of one unit overlapping
+// the next unit's MMAs) fill TMEM columns [0, kAccCols); the scale ring follows.
+template <int NT>
 struct GemmCfg {
-    static constexpr int kTmem = kTmemCols / CPS;            // TMEM columns of one CTA
+    static constexpr int kTmem = kTmemCols;                  // TMEM columns of the CTA
     static constexpr int kRows = kTerms * NT;                // B rows = N of one MMA (<= 256)
     static_assert(kRows <= 256 && kRows % 16 == 0, "one MMA covers every B row");
     static constexpr int kN = kRows;
@@ -151,25 +138,22 @@ struct GemmCfg {
     static constexpr int kBsfQ = kSg == 1 ? 4 : 16;
     static constexpr int kSfB = kSg == 1 ? 8 : 16;           // B scales' offset in a ring slot
     static constexpr int kSfCols = kSfB + 2 * kBsfQ;         // scale columns per K block (A + B)
-    static constexpr int kAcc = kRows <= 64 ? 2 : 1;                    // short chains only at small N
-    static constexpr int kDbuf = (CPS == 1 && 2 * kAcc * kRows + kSfRing * kSfCols <= kTmem) ? 2 : 1;
+    static constexpr int kAcc = kRows <= 64 ? 2 : 1;         // short chains only at small N
+    static constexpr int kDbuf = (2 * kAcc * kRows + kSfRing * kSfCols <= kTmem) ? 2 : 1;
     static constexpr int kAccCols = (kDbuf * kAcc * kRows + 31) / 32 * 32;
     static_assert(kAccCols + kSfRing * kSfCols <= kTmem, "accumulators and scales exceed the TMEM columns");
     static constexpr int kBCodes = kRows * kKBytes;          // activation codes per K block
     static constexpr int kBBlk = act_block_bytes(NT);        // activation block (codes + atoms)
     static constexpr int kH = NT * 66 * 4;                   // gate/up epilogue h tile (padded rows)
-    static constexpr int kBudget = CPS == 1 ? 226 * 1024 : 112 * 1024;   // dynamic smem (static stays below 2 KB)
-    // K blocks per stage: two (fewer, larger copies) unless that leaves a one-CTA-per-SM
-    // pipeline fewer than three stages
-    static constexpr int kKPS = (CPS == 2 || (kBudget - kH - 2048) / (2 * (kTileBytes + kBBlk)) >= 3) ? 2 : 1;
+    static constexpr int kBudget = 226 * 1024;               // dynamic smem (static stays below 2 KB)
+    // K blocks per stage: two (fewer, larger copies) unless that leaves fewer than three stages
+    static constexpr int kKPS = (kBudget - kH - 2048) / (2 * (kTileBytes + kBBlk)) >= 3 ? 2 : 1;
     // stage: kKPS weight tiles (kTileBytes each), then kKPS activation blocks; every operand
     // start is a multiple of 1024 bytes
     static constexpr int kStage = kKPS * (kTileBytes + kBBlk);
-    // Epilogue warps: eight with one CTA per SM (two per TMEM lane quarter, each taking half of
-    // the columns: the wide prefill tiles' SwiGLU and quantisation need the issue slots), four
-    // with two CTAs per SM (a sub-partition's register file holds at most 4 x 32 threads x 128
-    // registers, and the decode epilogues are short).
-    static constexpr int kEpi = CPS == 1 ? 8 : 4;
+    // Epilogue warps: eight, two per TMEM lane quarter, each taking half of the columns (the
+    // wide tiles' SwiGLU and quantisation need the issue slots).
+    static constexpr int kEpi = 8;
     static constexpr int kThreads = (2 + kEpi) * 32;
     static constexpr int kNH = NT / (kEpi / 4);              // columns of one epilogue warp
     static constexpr int kLdW = kNH < 16 ? kNH : 16;         // accumulator columns per tcgen05.ld
@@ -182,27 +166,16 @@ struct GemmCfg {
 struct UnitInfo {
     int slot;       // arena slot of the weights
     int m;          // weight row tile
-    int key;        // decode: slot ordinal; prefill: activation tile
+    int key;        // activation tile (its h readiness counter)
     int btile;      // activation tile
     int brow0;      // first B row (row index of the activation rows / outputs)
     int ncols;      // valid columns of D
 };
 
 template <int NT>
-__device__ __forceinline__ bool unit_info(const FfnParams& p, const PhaseParams& P, int ph, int unit, const int* kslot,
-                                          const int* kinfo, UnitInfo& u) {
-    if (p.regime == kRegimeDecode) {
-        // gate/up: the x tile, one column per token; down: the key's own h tile
-        u.m = unit % P.mtiles;
-        u.key = unit / P.mtiles;
-        u.slot = kslot[u.key];
-        u.btile = ph ? u.key : 0;
-        u.brow0 = 0;
-        u.ncols = ph ? (kinfo[u.key] & 0xFFFF) : p.T;
-        return true;
-    }
-    // prefill: unit = first_tile_g*mtiles + m*ntiles_g + ntile (tiles sharing weights adjacent),
-    // so unit / mtiles is a tile of group g
+__device__ __forceinline__ bool unit_info(const FfnParams& p, const PhaseParams& P, int unit, UnitInfo& u) {
+    // unit = first_tile_g*mtiles + m*ntiles_g + ntile (tiles sharing weights adjacent), so
+    // unit / mtiles is a tile of group g
     const int4 gr = p.grec[p.tile_group[unit / P.mtiles]];   // first row, end row, slot, first tile
     const int ntiles = (gr.y - gr.x + NT - 1) / NT;
     const int local = unit - gr.w * P.mtiles;
@@ -217,16 +190,15 @@ __device__ __forceinline__ bool unit_info(const FfnParams& p, const PhaseParams&
 }
 
 
-// The whole expert FFN in one persistent launch (one CTA per SM, every CTA resident).  The
-// producer takes units from the work list; a down unit needs the h rows of its key (decode:
-// its slot; prefill: its tile) from every gate/up unit of that key, so the producer issues the
-// unit's first weight copy, then waits (bounded) for the key's count of finished gate/up units
-// before issuing the h copy.  Decode also combines: the warp of the last down unit to write a
-// run of 32 features of y sums the token's pair rows there in ascending j.
-template <int NT, int CPS>
-__global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel(FfnParams p) {
-    using C = GemmCfg<NT, CPS>;
-    static_assert(C::kThreads == (CPS == 1 ? 10 : 6) * 32 && C::kNH * (C::kEpi / 4) == NT, "epilogue warp layout");
+// The whole expert FFN of a prefill call in one persistent launch (one CTA per SM, every CTA
+// resident).  The producer takes units from the work list; a down unit needs the h rows of its
+// activation tile from every gate/up unit of that tile, so the producer issues the unit's
+// weight copies, then waits (bounded) for the tile's count of finished gate/up units before
+// issuing the h copies.
+template <int NT>
+__global__ void __launch_bounds__(10 * 32, 1) mxf4_ffn_kernel(FfnParams p) {
+    using C = GemmCfg<NT>;
+    static_assert(C::kThreads == 10 * 32 && C::kNH * (C::kEpi / 4) == NT, "epilogue warp layout");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stage_base = smem;
@@ -239,16 +211,10 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
     uint64_t* epibar = tempty + 2;               // [2] epilogue warps' h-tile hand-offs
     uint64_t* uqfull = epibar + 2;               // [kUQ] unit id written
     uint64_t* uqempty = uqfull + kUQ;            // [kUQ] unit id read by the MMA and epilogue warps
-    uint64_t* setupbar = uqempty + kUQ;          // keys of this call known
+    uint64_t* setupbar = uqempty + kUQ;          // tile count of this call known
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
-    __shared__ int n_keys_sh, pairs_total_sh;
-    // decode: the routing outputs of the T*k pairs and the keys.  A key is a slot's pairs, in
-    // order of appearance, in chunks of at most NT: the chunk's h rows are one tile.
-    __shared__ int pinfo[kMaxDecodePairs];       // pair -> key << 5 | row in the key's tile, -1: none
-    __shared__ int kslot[kMaxDecodePairs];       // key -> slot
-    __shared__ int kinfo[kMaxDecodePairs];       // key -> first kplist index << 16 | pairs
-    __shared__ short kplist[kMaxDecodePairs];    // the pairs of each key in row order
+    __shared__ int n_keys_sh;
     __shared__ int uq[kUQ];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -281,67 +247,20 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
     volatile int* abortp = &abort_flag;
-    // Decode: the producer claims its first unit now, before the wait below.  The work list is
-    // a counter that the previous call left at zero (the kernel before this one started after
-    // that call completed, exactly as for the x jobs); what the unit means is known only after
-    // the wait.  Prefill's counter is cleared by the kernel before this one, so it claims later.
-    int pre_unit = -2;
-    if (warp == 0 && lane == 0 && p.regime == kRegimeDecode) pre_unit = atomicAdd(p.work, 1);
-    // Decode: x -> kTerms MXFP4 terms, one warp per (row < T, 32-element block), jobs taken
-    // from a global counter so that the CTAs resident first do them all.  This runs before the
-    // wait below: x is an input of this call, and the kernel that may still be running (the
-    // router's) does not write it.
-    if (p.x_src && warp >= 2) {
-        const int nblk = p.d / 32, KBd = p.d / kKB, total = p.T * nblk;
-        uint8_t* q = const_cast<uint8_t*>(p.ph[0].b);
-        while (true) {
-            int job = 0;
-            if (lane == 0) job = atomicAdd(p.xjob, 1);
-            job = __shfl_sync(0xffffffffu, job, 0);
-            if (job >= total) break;
-            const int r = job / nblk, b = job % nblk, kb = b / 8, j = b % 8;
-            uint4 codes[kTerms];
-            uint32_t scales[kTerms];
-            warp_quantize32(bf16_to_f32(p.x_src[(size_t)r * p.d + 32 * b + lane]), lane, codes, scales);
-            if (lane < kTerms) {
-                uint4 cv = codes[0];
-                uint32_t sv = scales[0];
-#pragma unroll
-                for (int t = 1; t < kTerms; ++t)
-                    if (lane == t) { cv = codes[t]; sv = scales[t]; }
-                *reinterpret_cast<uint4*>(q + act_code_off(0, kb, lane, r, j, NT, KBd)) = cv;
-                q[act_scale_off(0, kb, lane, r, j, NT, KBd)] = (uint8_t)sv;
-            }
-            fence_proxy_async();   // read by the async proxy (bulk copies) of every CTA
-            __syncwarp();
-            if (lane == 0) red_add_release(p.xready, 1);
-        }
-    }
     // everything above overlaps the previous kernel; its outputs are read from here on
     pdl_wait();
     unsigned dep_limit = kSpinLimit;
     if (p.wait_limit && *p.wait_limit > 0) dep_limit = (unsigned)*p.wait_limit;
-    if (warp == 0) {
-        // decode: keys in order of their first pair (a slot's first appearance, then every
-        // NT-th); one warp, pair i on lane i mod 32
-        if (p.regime == kRegimeDecode) {
-            decode_key_setup<NT>(p.slot, p.T * p.k, p.num_slots, p.status, blockIdx.x == 0, lane, pinfo, kslot, kinfo,
-                                 kplist, reinterpret_cast<int*>(hbuf), n_keys_sh, pairs_total_sh);
-        } else if (lane == 0) {
-            n_keys_sh = p.plan[1];
-            pairs_total_sh = 0;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(setupbar));
+    if (warp == 0 && lane == 0) {
+        n_keys_sh = p.plan[1];   // activation tiles of the plan
+        mbar_arrive(smem_u32(setupbar));
     }
     if (!mbar_wait(smem_u32(setupbar), 0, abortp)) {
         if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
     }
+    __syncwarp();
     const int n_keys = *abortp ? 0 : n_keys_sh;
     const int n0 = n_keys * p.ph[0].mtiles, n_all = n0 + n_keys * p.ph[1].mtiles;
-    // decode with no valid pair: y is zero
-    if (p.regime == kRegimeDecode && p.y && n_keys == 0 && blockIdx.x == 0)
-        for (int i = tid; i < p.T * p.d; i += blockDim.x) p.y[i] = 0;
     // position in the unit-id ring (same sequence for every role)
     int qi = 0;
     uint32_t qphase = 0;
@@ -350,16 +269,9 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
         // ---------------- producer: takes units, two contiguous bulk copies per stage
         if (lane == 0) {
             int stage = 0, ready_key = -1;
-            bool x_ok = (p.x_src == nullptr);
             uint32_t phase = 0, issued = 0, issued_parity = 0;   // per-stage bit masks
             while (true) {
-                int unit;
-                if (pre_unit != -2) {
-                    unit = *abortp ? -1 : pre_unit;
-                    pre_unit = -2;
-                } else {
-                    unit = *abortp ? -1 : atomicAdd(p.work, 1);
-                }
+                int unit = *abortp ? -1 : atomicAdd(p.work, 1);
                 if (unit >= n_all) unit = -1;
                 if (!mbar_wait(smem_u32(&uqempty[qi]), qphase ^ 1u, abortp)) {
                     atomicOr(p.status, MOE_STATUS_TIMEOUT);
@@ -373,12 +285,11 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
                 const int ph = unit < n0 ? 0 : 1;
                 const PhaseParams& P = p.ph[ph];
                 UnitInfo u;
-                const bool ok = unit_info<NT>(p, P, ph, ph ? unit - n0 : unit, kslot, kinfo, u);
+                const bool ok = unit_info<NT>(p, P, ph ? unit - n0 : unit, u);
                 const uint8_t* sbase = p.arena + (int64_t)(ok ? u.slot : 0) * p.slot_bytes;
-                // A unit whose activations are not ready yet (gate/up: x still being quantised by
-                // the CTAs; down: h of its key) gets its weight copies issued into every free
-                // stage; the activation copies of those stages follow once they are ready.
-                bool have_b = (ph == 0) ? x_ok : !(ok && u.key != ready_key);
+                // A down unit whose h is not ready yet gets its weight copies issued into every
+                // free stage; the h copies of those stages follow once it is ready.
+                bool have_b = (ph == 0) || !(ok && u.key != ready_key);
                 const int nst = (P.kblocks + C::kKPS - 1) / C::kKPS;   // stages of this unit
                 int pend_n = 0, pend_s0 = 0, pend_stage0 = 0;
                 // activation blocks of stage s of the unit (K blocks kKPS*s ..) into smem stage stg
@@ -393,10 +304,9 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
                     pend_n = 0;
                 };
                 auto key_ready = [&](bool block) -> bool {
-                    // gate/up: every x job is done; down: every gate/up unit of the key has
-                    // written its h rows
-                    const int32_t* flag = (ph == 0) ? p.xready : p.ready + u.key;
-                    const int target = (ph == 0) ? p.T * (p.d / 32) : p.ph[0].mtiles;
+                    // every gate/up unit of the activation tile has written its h rows
+                    const int32_t* flag = p.ready + u.key;
+                    const int target = p.ph[0].mtiles;
                     unsigned spins = 0;
                     while (ld_acquire(flag) < target) {
                         if (!block) return false;
@@ -408,8 +318,7 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
                         __nanosleep(64);
                     }
                     fence_proxy_async();
-                    if (ph == 0) x_ok = true;
-                    else ready_key = u.key;
+                    ready_key = u.key;
                     have_b = true;
                     return true;
                 };
@@ -459,13 +368,6 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
             int stage = 0, sfring = 0, acc = 0;
             uint32_t phase = 0, aphase = 0;
             const uint32_t idesc_lo = idesc_mxf4(C::kN, 0), idesc_hi = idesc_mxf4(C::kN, 2);
-            // Decode: every gate/up unit multiplies the same x tile, so the scale atoms of its K
-            // blocks are copied into TMEM once (by the CTA's first gate/up unit, into columns
-            // after the scale ring) when they fit there; later units only copy A scales.
-            const uint32_t xsf = tmem + C::kAccCols + kSfRing * C::kSfCols;
-            const bool xsf_fits = p.regime == kRegimeDecode &&
-                                  C::kSg == 1 && C::kAccCols + kSfRing * C::kSfCols + p.ph[0].kblocks * 8 <= C::kTmem;
-            bool xsf_done = false;
             while (true) {
                 int unit = -1;
                 if (mbar_wait(smem_u32(&uqfull[qi]), qphase, abortp)) unit = uq[qi];
@@ -473,7 +375,6 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
                 if (++qi == kUQ) { qi = 0; qphase ^= 1u; }
                 if (unit < 0) break;
                 const int KB = p.ph[unit < n0 ? 0 : 1].kblocks;
-                const bool use_xsf = xsf_fits && unit < n0;
                 if (!mbar_wait(smem_u32(&tempty[acc]), aphase ^ 1u, abortp)) {
                     atomicOr(p.status, MOE_STATUS_TIMEOUT);
                     *abortp = 1;
@@ -500,15 +401,13 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
                         const uint32_t sb = smem_u32(st + C::kKPS * kTileBytes + i * C::kBBlk);
                         const uint32_t ssfa = sa + kTileCodeBytes, ssfb = sb + C::kBCodes;
                         const uint32_t sfcol = tmem + C::kAccCols + sfring * C::kSfCols;
-                        const uint32_t sfb = use_xsf ? xsf + (s * C::kKPS + i) * 8 : sfcol + C::kSfB;
+                        const uint32_t sfb = sfcol + C::kSfB;
                         tc_cp_sf(sfcol + 0, desc_sf(ssfa));
                         tc_cp_sf(sfcol + 4, desc_sf(ssfa + 512));
-                        if (!(use_xsf && xsf_done)) {
 #pragma unroll
-                            for (int g = 0; g < C::kSg; ++g) {
-                                tc_cp_sf(sfb + 4 * g, desc_sf(ssfb + g * 1024));
-                                tc_cp_sf(sfb + C::kBsfQ + 4 * g, desc_sf(ssfb + g * 1024 + 512));
-                            }
+                        for (int g = 0; g < C::kSg; ++g) {
+                            tc_cp_sf(sfb + 4 * g, desc_sf(ssfb + g * 1024));
+                            tc_cp_sf(sfb + C::kBsfQ + 4 * g, desc_sf(ssfb + g * 1024 + 512));
                         }
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -524,7 +423,6 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
                 if (failed) break;
-                if (use_xsf) xsf_done = true;
                 tc_commit(smem_u32(&tfull[acc]));
                 if (++acc == C::kDbuf) { acc = 0; aphase ^= 1u; }
             }
@@ -539,7 +437,7 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
         int acc = 0;
         uint32_t aphase = 0, ephase = 0;
         const int KBf = p.f / kKB;
-        // Two warm-up passes first (a gate/up unit, then a down unit of key 0) with every global
+        // Two warm-up passes first (a gate/up unit, then a down unit of tile 0) with every global
         // write, atomic and hand-off disabled: they run the epilogue's instructions once while
         // the warps would idle anyway, so the first real units do not fetch them cold.  They
         // read TMEM (allocated, contents unused) and write only this warp's rows of hbuf.
@@ -560,11 +458,12 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
             const int ph = unit < n0 ? 0 : 1;
             const PhaseParams& P = p.ph[ph];
             UnitInfo u;
-            const bool ok = unit_info<NT>(p, P, ph, ph ? unit - n0 : unit, kslot, kinfo, u);
+            const bool ok = unit_info<NT>(p, P, ph ? unit - n0 : unit, u);
             if (!dry && !mbar_wait(smem_u32(&tfull[acc]), aphase, abortp)) {
                 if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
                 break;
             }
+            __syncwarp();
             tc_fence_after();
             // D[row][n] = sum over accumulators and terms of column (a*kRows + t*NT + n); this
             // warp's columns n = c_lo + cl
@@ -601,32 +500,7 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
                 for (int cl = 0; cl < C::kNH; ++cl) {
                     const int c = c_lo + cl;
                     if (c >= u.ncols || dry) continue;
-                    // decode: column c is row c of the key's tile, i.e. its c-th pair
-                    const int row_out = (p.regime == kRegimeDecode) ? kplist[(kinfo[u.key] >> 16) + c] : u.brow0 + c;
-                    p.rows_out[(size_t)row_out * p.d + r] = vals[cl];
-                }
-                if (p.regime == kRegimeDecode && p.y) {
-                    // y rows [128m + 32q, +32) are complete once every valid pair's rows there are
-                    // written: one counter per 32 features, one arrival per warp with columns
-                    bool last = dry;
-                    const int mine = max(0, min(C::kNH, u.ncols - c_lo));
-                    if (!dry && mine > 0) {
-                        __syncwarp();
-                        int l = 0;
-                        if (lane == 0) l = (atom_add_acq_rel(p.ycnt + u.m * 4 + q, mine) + mine == pairs_total_sh);
-                        last = __shfl_sync(0xffffffffu, l, 0) != 0;
-                    }
-                    if (last) {
-                        for (int t = 0; t < p.T; ++t) {
-                            float yv = 0.f;
-                            for (int j = 0; j < p.k; ++j) {
-                                const int pr = t * p.k + j;
-                                if (pinfo[pr] < 0) continue;   // no valid slot
-                                yv = fmaf(__ldg(p.w + pr), __ldcg(p.rows_out + (size_t)pr * p.d + r), yv);
-                            }
-                            if (!dry) p.y[(size_t)t * p.d + r] = f32_to_bf16(yv);
-                        }
-                    }
+                    p.rows_out[(size_t)(u.brow0 + c) * p.d + r] = vals[cl];
                 }
             } else {
                 // rows 2i' = gate, 2i'+1 = up of output i' = row/2 within the tile (i = 64m + i')
@@ -648,23 +522,13 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
                         if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
                         break;
                     }
+                    __syncwarp();
                 }
                 // quantise; a job is (column c, block b of 32 outputs i0 = 64m + 32b): few jobs
-                // (decode, T <= 4) one warp each -- the shortest latency for the h hand-off --
-                // else one octet of lanes each (32 octets over the eight warps); both compute
-                // the same terms
-                auto h_rows = [&](int c, auto&& write_row) {
-                    if (p.regime == kRegimeDecode) {
-                        // column c = token; its pairs of this key: row (pinfo & 31) of the key's h tile
-                        if (c < p.T)
-                            for (int jj = 0; jj < p.k; ++jj) {
-                                const int pi = pinfo[c * p.k + jj];
-                                if (pi >= 0 && (pi >> 5) == u.key) write_row(u.key, pi & 31);
-                            }
-                    } else {
-                        write_row(u.btile, c);
-                    }
-                };
+                // (a tile of at most 4 rows) one warp each, else one octet of lanes each (32
+                // octets over the eight warps); both compute the same terms, written to row c of
+                // the tile's h block
+                auto h_rows = [&](int c, auto&& write_row) { write_row(u.btile, c); };
                 if (u.ncols * 2 <= 8) {
                     for (int job = ew; job < u.ncols * 2; job += C::kEpi) {
                         const int c = job >> 1, b = job & 1;
@@ -728,22 +592,6 @@ __global__ void __launch_bounds__((CPS == 1 ? 10 : 6) * 32, CPS) mxf4_ffn_kernel
     __syncthreads();
     tc_fence_after();
     if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmem) : "memory");
-    if (p.exit_ctr) {
-        // the last CTA to leave clears the counters for the next call
-        __shared__ int last_cta;
-        if (tid == 0) last_cta = (atom_add_acq_rel(p.exit_ctr, 1) == (int)gridDim.x - 1);
-        __syncthreads();
-        if (last_cta) {
-            for (int i = tid; i < n_keys; i += blockDim.x) p.ready[i] = 0;
-            for (int i = tid; i < p.d / 32; i += blockDim.x) p.ycnt[i] = 0;
-            if (tid == 0) {
-                *p.work = 0;
-                *p.xjob = 0;
-                *p.xready = 0;
-                *p.exit_ctr = 0;
-            }
-        }
-    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -771,13 +619,13 @@ static size_t max_keys(const moe_dims* m, int T) {
 
 struct TcBuffers {
     uint8_t *x, *h;        // activation blocks of x (K = d) and h (K = f)
-    int32_t* zero;         // counters cleared by the quantiser: work, ready[nkeys], ycnt[d/32]
+    int32_t* zero;         // counters cleared by the quantiser: work, ready[nkeys]
     size_t nkeys, nzero;
     float* rows;
     int32_t* plan;
 };
 
-static size_t counters_of(const moe_dims* m, int T) { return 1 + max_keys(m, T) + m->d / 32; }
+static size_t counters_of(const moe_dims* m, int T) { return 1 + max_keys(m, T); }
 
 static TcBuffers tc_buffers(const moe_dims* m, int T, char* ws, const WsLayout& L) {
     TcBuffers b;
@@ -798,13 +646,12 @@ size_t tc_workspace_bytes(const moe_dims* m, int T) {
            align256(R * m->d * 4);
 }
 
-template <int NT, int CPS>
+template <int NT>
 static int launch_ffn(const FfnParams& p, int grid, cudaStream_t st) {
-    using C = GemmCfg<NT, CPS>;
-    if (cudaFuncSetAttribute(mxf4_ffn_kernel<NT, CPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes) !=
-        cudaSuccess)
+    using C = GemmCfg<NT>;
+    if (cudaFuncSetAttribute(mxf4_ffn_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes) != cudaSuccess)
         return MOE_ERR_LAUNCH;
-    if (launch_pdl(mxf4_ffn_kernel<NT, CPS>, dim3(grid), dim3(C::kThreads), (size_t)C::kBytes, st, p) != cudaSuccess)
+    if (launch_pdl(mxf4_ffn_kernel<NT>, dim3(grid), dim3(C::kThreads), (size_t)C::kBytes, st, p) != cudaSuccess)
         return MOE_ERR_LAUNCH;
     note_launch(1);
     return MOE_OK;
@@ -833,7 +680,6 @@ static FfnParams ffn_params(const moe_dims* m, const moe_arena* ar, int T, const
     p.h = b.h;
     p.work = b.zero;
     p.ready = b.zero + 1;
-    p.ycnt = b.zero + 1 + b.nkeys;
     return p;
 }
 
@@ -872,14 +718,13 @@ int launch_tc_prefill(const moe_dims* m, const moe_arena* ar, int T, const uint1
         x, b.plan + plan_pair_off(m->num_experts, max_tiles), k, T, d, b.x, b.zero, (int)b.nzero);
     note_launch(2);
     FfnParams p = ffn_params(m, ar, T, slot, status, b);
-    p.regime = kRegimePrefill;
     p.plan = b.plan; p.offsets = offsets; p.row_src = row_src;
     p.tile_group = b.plan + plan_tile_group_off(m->num_experts);
     p.grec = reinterpret_cast<const int4*>(b.plan + plan_grec_off(m->num_experts));
     p.rows_out = rows_out;
     p.wait_limit = reinterpret_cast<int32_t*>(ws + L.counter) + kCtrWaitLimit;
     const int grid = num_sms < kMaxGemmCtas ? num_sms : kMaxGemmCtas;
-    return launch_ffn<kPrefillNT, 1>(p, grid, st);
+    return launch_ffn<kPrefillNT>(p, grid, st);
 }
 
 }  // namespace fp4moe
