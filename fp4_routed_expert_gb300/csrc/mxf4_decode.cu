@@ -64,7 +64,6 @@ struct DecParams {
     int32_t* work;                   // next unit (zero at launch)
     int32_t* ready;                  // gate/up units finished per key
     int32_t* ycnt;                   // pair rows written per 32 features of y
-    int32_t* xjob;
     int32_t* xready;
     int32_t* exit_ctr;
     const int32_t* wait_limit;       // polls of a wait on another CTA (0: kSpinLimit)
@@ -258,7 +257,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
     uint64_t* epibar = tempty + 1;               // [2] h hand-offs between the epilogue warps
     uint64_t* uqfull = epibar + 2;               // [kDecUQ] unit id written
     uint64_t* uqempty = uqfull + kDecUQ;         // [kDecUQ] unit id read by the MMA and epilogue warps
-    uint64_t* setupbar = uqempty + kDecUQ;       // keys of this call known
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     __shared__ int n_keys_sh, pairs_total_sh;
@@ -284,7 +282,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
             mbar_init(smem_u32(&uqfull[i]), 1);
             mbar_init(smem_u32(&uqempty[i]), 1 + kEpi);
         }
-        mbar_init(smem_u32(setupbar), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -304,31 +301,41 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
     volatile int* abortp = &abort_flag;
     const int KBd = p.kblocks[0], KBf = p.kblocks[1];
 
-    // x -> kTerms MXFP4 terms (one warp per (token, 32-element block), jobs from a global
-    // counter).  x is an input of this call, so this overlaps the router.
+    // x -> kTerms MXFP4 terms, one epilogue thread per (token, 32-element block), the jobs
+    // dealt out by block (a few CTAs hold them all), each warp counting its finished jobs on
+    // xready.  This runs before the wait below: x is an input of this call, the kernel ahead
+    // (the router) does not write it, and the expert kernel of the previous call has completed
+    // before this one launched (the router lets it launch only after its own wait).
     if (warp >= 2) {
         const int nblk = p.d / 32, total = p.T * nblk;
-        while (true) {
-            int job = 0;
-            if (lane == 0) job = atomicAdd(p.xjob, 1);
-            job = __shfl_sync(0xffffffffu, job, 0);
-            if (job >= total) break;
-            const int r = job / nblk, b = job % nblk, kb = b / 8, j = b % 8;
-            uint4 codes[kTerms];
-            uint32_t scales[kTerms];
-            warp_quantize32(bf16_to_f32(p.x_src[(size_t)r * p.d + 32 * b + lane]), lane, codes, scales);
-            if (lane < kTerms) {
-                uint4 cv = codes[0];
-                uint32_t sv = scales[0];
+        for (int j0 = blockIdx.x * (kEpi * 32) + (warp - 2) * 32; j0 < total; j0 += gridDim.x * (kEpi * 32)) {
+            const int job = j0 + lane;
+            if (job < total) {
+                const int r = job / nblk, b = job % nblk, kb = b / 8, jb = b % 8;
+                const uint4* src = reinterpret_cast<const uint4*>(p.x_src + (size_t)r * p.d + 32 * b);
+                float v[32];
 #pragma unroll
-                for (int t = 1; t < kTerms; ++t)
-                    if (lane == t) { cv = codes[t]; sv = scales[t]; }
-                *reinterpret_cast<uint4*>(p.x + dact_code_off(0, kb, lane, r, j, NT, KBd)) = cv;
-                p.x[dact_scale_off(0, kb, lane, r, j, NT, KBd)] = (uint8_t)sv;
+                for (int u = 0; u < 4; ++u) {
+                    const uint4 w4 = src[u];
+                    const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        v[8 * u + 2 * h] = bf16_lo(ww[h]);
+                        v[8 * u + 2 * h + 1] = bf16_hi(ww[h]);
+                    }
+                }
+                uint32_t wd[kTerms][4], sc[kTerms];
+                thread_quantize32(v, wd, sc);
+#pragma unroll
+                for (int t = 0; t < kTerms; ++t) {
+                    *reinterpret_cast<uint4*>(p.x + dact_code_off(0, kb, t, r, jb, NT, KBd)) =
+                        make_uint4(wd[t][0], wd[t][1], wd[t][2], wd[t][3]);
+                    p.x[dact_scale_off(0, kb, t, r, jb, NT, KBd)] = (uint8_t)sc[t];
+                }
+                fence_proxy_async();   // read by the async proxy (bulk copies) of every CTA
             }
-            fence_proxy_async();   // read by the async proxy (bulk copies) of every CTA
             __syncwarp();
-            if (lane == 0) red_add_release(p.xready, 1);
+            if (lane == 0) red_add_release(p.xready, min(32, total - j0));
         }
     }
     // The setup below runs once per call right after the wait, on cold instructions: run it
@@ -344,23 +351,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
                              nk, np);
         __syncwarp();
     }
-    // the router's outputs are read from here on
+    // the router's outputs are read from here on; the next kernel (the next call's router)
+    // may launch now: before it waits for this kernel in turn it only stages its own weights
     pdl_wait();
+    pdl_trigger();
     unsigned dep_limit = kSpinLimit;
     if (p.wait_limit && *p.wait_limit > 0) dep_limit = (unsigned)*p.wait_limit;
-    if (warp == 0) {
+    if (warp == 0)
         decode_key_setup<NT>(p.slot, p.T * p.k, p.num_slots, p.status, blockIdx.x == 0, lane, pinfo, kslot, kinfo,
                              kplist, reinterpret_cast<int*>(hbuf), n_keys_sh, pairs_total_sh);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(setupbar));
-    }
-    if (!mbar_wait(smem_u32(setupbar), 0, abortp)) {
-        if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
-    }
-    // Every lane polls a barrier on its own and may leave the loop in a different round: the
-    // warp reconverges here (and after every such wait below) before its collective work.
-    __syncwarp();
-    const int n_keys = *abortp ? 0 : n_keys_sh;
+    // the keys are known; every role reads their count here, before any of them can abort
+    // on a later wait (the setup itself waits on nothing)
+    __syncthreads();
+    const int n_keys = n_keys_sh;
     const int n0 = n_keys * p.units[0], n_all = n0 + n_keys * p.units[1];
     if (n_keys == 0 && blockIdx.x == 0)   // no valid pair: y is zero
         for (int i = tid; i < p.T * p.d; i += blockDim.x) p.y[i] = 0;
@@ -741,7 +744,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
         for (int i = tid; i < p.d / 32; i += blockDim.x) p.ycnt[i] = 0;
         if (tid == 0) {
             *p.work = 0;
-            *p.xjob = 0;
             *p.xready = 0;
             *p.exit_ctr = 0;
         }
@@ -820,7 +822,6 @@ int launch_decode_wide(const moe_dims* m, const moe_arena* ar, int T, const uint
     p.slot = slot; p.w = w; p.x_src = x; p.x = xq; p.h = hq; p.rows_out = rows; p.y = y; p.status = status;
     p.work = ctr + kCtrFfnWork;
     p.xready = ctr + kCtrFfnXReady;
-    p.xjob = ctr + kCtrFfnXJob;
     p.exit_ctr = ctr + kCtrFfnExit;
     p.ready = ctr + kCtrFfnReady;
     p.ycnt = ctr + kCtrFfnY;

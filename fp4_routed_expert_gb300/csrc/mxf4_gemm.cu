@@ -211,7 +211,6 @@ __global__ void __launch_bounds__(10 * 32, 1) mxf4_ffn_kernel(FfnParams p) {
     uint64_t* epibar = tempty + 2;               // [2] epilogue warps' h-tile hand-offs
     uint64_t* uqfull = epibar + 2;               // [kUQ] unit id written
     uint64_t* uqempty = uqfull + kUQ;            // [kUQ] unit id read by the MMA and epilogue warps
-    uint64_t* setupbar = uqempty + kUQ;          // tile count of this call known
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_flag;
     __shared__ int n_keys_sh;
@@ -233,7 +232,6 @@ __global__ void __launch_bounds__(10 * 32, 1) mxf4_ffn_kernel(FfnParams p) {
             mbar_init(smem_u32(&uqfull[i]), 1);
             mbar_init(smem_u32(&uqempty[i]), 1 + C::kEpi);
         }
-        mbar_init(smem_u32(setupbar), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -251,15 +249,10 @@ __global__ void __launch_bounds__(10 * 32, 1) mxf4_ffn_kernel(FfnParams p) {
     pdl_wait();
     unsigned dep_limit = kSpinLimit;
     if (p.wait_limit && *p.wait_limit > 0) dep_limit = (unsigned)*p.wait_limit;
-    if (warp == 0 && lane == 0) {
-        n_keys_sh = p.plan[1];   // activation tiles of the plan
-        mbar_arrive(smem_u32(setupbar));
-    }
-    if (!mbar_wait(smem_u32(setupbar), 0, abortp)) {
-        if (lane == 0) { atomicOr(p.status, MOE_STATUS_TIMEOUT); *abortp = 1; }
-    }
-    __syncwarp();
-    const int n_keys = *abortp ? 0 : n_keys_sh;
+    if (tid == 0) n_keys_sh = p.plan[1];   // activation tiles of the plan
+    // every role reads the tile count here, before any of them can abort on a later wait
+    __syncthreads();
+    const int n_keys = n_keys_sh;
     const int n0 = n_keys * p.ph[0].mtiles, n_all = n0 + n_keys * p.ph[1].mtiles;
     // position in the unit-id ring (same sequence for every role)
     int qi = 0;

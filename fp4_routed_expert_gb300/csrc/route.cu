@@ -598,7 +598,6 @@ __global__ void __launch_bounds__(kDecodeThreads) route_decode_kernel(RouteArgs 
     const uint16_t* xs = ws + (size_t)EPB * d;
     uint64_t* bar = reinterpret_cast<uint64_t*>(dsm + (size_t)(EPB + T) * d * 2);
     __shared__ int abort_flag;
-    pdl_trigger();   // the next kernel may launch now; it waits for this one before reading anything
     if (tid == 0) {
         abort_flag = 0;
         mbar_init(smem_u32(bar), 1);
@@ -608,14 +607,23 @@ __global__ void __launch_bounds__(kDecodeThreads) route_decode_kernel(RouteArgs 
     uint32_t phase = 0;
     for (int e0 = blockIdx.x * EPB; e0 < E; e0 += gridDim.x * EPB) {
         const int nw = min(EPB, E - e0);
+        const bool first = (e0 == (int)blockIdx.x * EPB);
+        const uint32_t rowb = (uint32_t)d * 2;
         if (tid == 0) {
-            const bool first = (e0 == (int)blockIdx.x * EPB);
-            const uint32_t rowb = (uint32_t)d * 2;
             mbar_expect_tx(smem_u32(bar), rowb * nw + (first ? rowb * T : 0u));
-            if (first) bulk_g2s(smem_u32(xs), a.x, rowb * T, smem_u32(bar));
             // the block's router rows are consecutive: one copy (a bulk copy costs a fixed time
-            // on top of its bytes)
+            // on top of its bytes).  They are no kernel's output, so the first round's copy goes
+            // out before the wait below and overlaps the end of the kernel ahead.
             bulk_g2s_hint(smem_u32(ws), a.wr + (size_t)e0 * d, rowb * nw, smem_u32(bar), l2_evict_last());
+        }
+        if (first) {
+            // launched behind the previous kernel (programmatic dependent launch): x, the bias,
+            // the table and the outputs are touched only once it has completed; the next kernel
+            // (the expert kernel, which waits for this one before reading anything but x) may
+            // launch from then on
+            pdl_wait();
+            pdl_trigger();
+            if (tid == 0) bulk_g2s(smem_u32(xs), a.x, rowb * T, smem_u32(bar));
         }
         const int e = e0 + warp;
         const int tb = (e < E) ? a.table[e] : -1;
@@ -885,9 +893,10 @@ static int launch_decode_ch(RouteArgs a, cudaStream_t st, int num_sms) {
     a.bound_coef = (float)(coef * (1.0 + 1.0 / 4096.0));                                   // rounded up
     int blocks = (a.E + a.dec_epb - 1) / a.dec_epb;
     if (num_sms > 0 && blocks > num_sms) blocks = num_sms;
-    route_decode_kernel<CH, EPL><<<blocks, threads, smem, st>>>(a);
+    if (launch_pdl(route_decode_kernel<CH, EPL>, dim3(blocks), dim3(threads), smem, st, a) != cudaSuccess)
+        return MOE_ERR_LAUNCH;
     note_launch(1);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+    return MOE_OK;
 }
 
 // Router launches for RouteArgs with every pointer set: the decode kernel when the tokens'

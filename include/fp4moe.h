@@ -32,9 +32,9 @@
  *  - Some kernels are launched with programmatic dependent launch: they may become resident
  *    while the previous kernel on `stream` still runs.  Before that kernel has completed they
  *    read exactly one input, which the kernel enqueued immediately before the call must
- *    therefore not write: x of a decode call of moe_expert_ffn_fp4 (the router call that
- *    normally precedes it does not).  Every other input, every output and the workspace are
- *    touched only after it has completed.
+ *    therefore not write: w_router of a decode-size routing call (T <= 16), whose rows are
+ *    staged while the previous call's expert kernel finishes.  Every other input, every
+ *    output and the workspace are touched only after it has completed.
  *  - After a call that set MOE_STATUS_TIMEOUT the workspace must be re-initialised
  *    (moe_workspace_init) before its next use.
  */
