@@ -611,23 +611,15 @@ __global__ void __launch_bounds__(kDecodeThreads) route_decode_kernel(RouteArgs 
         const uint32_t rowb = (uint32_t)d * 2;
         if (tid == 0) {
             mbar_expect_tx(smem_u32(bar), rowb * nw + (first ? rowb * T : 0u));
-            // the block's router rows are consecutive: one copy (a bulk copy costs a fixed time
-            // on top of its bytes).  They are no kernel's output, so the first round's copy goes
-            // out before the wait below and overlaps the end of the kernel ahead.
+            // Launched behind the previous kernel (programmatic dependent launch), the logit
+            // phase reads only the router rows (one copy: a bulk copy costs a fixed time on top
+            // of its bytes) and x, which the kernel ahead does not write (the header's
+            // contract); so it overlaps the end of that kernel.  The bias, the table, the
+            // ticket and every output are touched only after the wait below.
+            if (first) bulk_g2s(smem_u32(xs), a.x, rowb * T, smem_u32(bar));
             bulk_g2s_hint(smem_u32(ws), a.wr + (size_t)e0 * d, rowb * nw, smem_u32(bar), l2_evict_last());
         }
-        if (first) {
-            // launched behind the previous kernel (programmatic dependent launch): x, the bias,
-            // the table and the outputs are touched only once it has completed; the next kernel
-            // (the expert kernel, which waits for this one before reading anything but x) may
-            // launch from then on
-            pdl_wait();
-            pdl_trigger();
-            if (tid == 0) bulk_g2s(smem_u32(xs), a.x, rowb * T, smem_u32(bar));
-        }
         const int e = e0 + warp;
-        const int tb = (e < E) ? a.table[e] : -1;
-        const float bias_e = (e < E && a.bias) ? a.bias[e] : 0.0f;
         // bounded wait; the copies are waited for (again bounded) even after a timeout
         if (!mbar_wait(smem_u32(bar), phase, &abort_flag)) {
             if (tid == 0) atomicOr(a.status, MOE_STATUS_TIMEOUT);
@@ -684,6 +676,14 @@ __global__ void __launch_bounds__(kDecodeThreads) route_decode_kernel(RouteArgs 
             }
         }
         __syncthreads();   // every quarter's pair is in part
+        if (first) {
+            // the kernel ahead has completed from here on; the next kernel (the expert kernel,
+            // which waits for this one before reading anything but x) may launch
+            pdl_wait();
+            pdl_trigger();
+        }
+        const int tb = (e < E) ? a.table[e] : -1;
+        const float bias_e = (e < E && a.bias) ? a.bias[e] : 0.0f;
         if (e < E && ks == 0 && lane < t_hi - t_lo) {
             {
                 const float4* pp = part + (warp * T + t_lo + lane) * kDecodeKS;

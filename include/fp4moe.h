@@ -31,10 +31,13 @@
  *  - Calls on different streams are independent when given different workspaces.
  *  - Some kernels are launched with programmatic dependent launch: they may become resident
  *    while the previous kernel on `stream` still runs.  Before that kernel has completed they
- *    read exactly one input, which the kernel enqueued immediately before the call must
- *    therefore not write: w_router of a decode-size routing call (T <= 16), whose rows are
- *    staged while the previous call's expert kernel finishes.  Every other input, every
- *    output and the workspace are touched only after it has completed.
+ *    read only these inputs, which the kernel enqueued immediately before the call must
+ *    therefore not write: x and w_router of a decode-size routing call (T <= 16), whose
+ *    logits are computed while the previous call's expert kernel finishes, and x of a decode
+ *    call of moe_expert_ffn_fp4.  Every other input, every output and the workspace are
+ *    touched only after it has completed.  (A kernel that never signals an early launch --
+ *    a plain CUDA kernel, or this library's residual/RMSNorm step -- completes before the
+ *    next one starts, so x written by such a kernel is safe.)
  *  - After a call that set MOE_STATUS_TIMEOUT the workspace must be re-initialised
  *    (moe_workspace_init) before its next use.
  */
