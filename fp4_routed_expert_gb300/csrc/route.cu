@@ -396,6 +396,29 @@ constexpr int kSelWarps = 4;
 // every chosen expert's key interval lies above every other expert's and every chosen score
 // is narrow; otherwise the token goes whole to select_token (same warp).  E <= 32 * EPL.
 // rec, exk and out are this warp's select_token arrays in shared memory.
+// Largest key order among this lane's experts m with bit m of `mask` set (0 when none), ties
+// to the lower m (the lower expert id): a pairwise tree, a few dependent steps instead of EPL.
+template <int EPL>
+__device__ __forceinline__ void lane_best(const uint32_t (&ko)[EPL], uint32_t mask, uint32_t& bu, int& bm) {
+    uint32_t v[EPL];
+    int ix[EPL];
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+        v[m] = ((mask >> m) & 1u) ? ko[m] : 0u;
+        ix[m] = m;
+    }
+#pragma unroll
+    for (int w = 1; w < EPL; w *= 2)
+#pragma unroll
+        for (int m = 0; m + w < EPL; m += 2 * w)
+            if (v[m + w] > v[m]) {   // strict: on equal keys the lower index stays
+                v[m] = v[m + w];
+                ix[m] = ix[m + w];
+            }
+    bu = v[0];
+    bm = ix[0];
+}
+
 template <int EPL>
 __device__ __forceinline__ void select_row(const RouteArgs& a, int t, int lane, float4* rec, float* exk, int* out) {
     const float NEG_INF = -__int_as_float(0x7f800000);
@@ -411,14 +434,14 @@ __device__ __forceinline__ void select_row(const RouteArgs& a, int t, int lane, 
         tb[m] = (e < E) ? __ldg(a.table + e) : -1;
     }
     uint32_t valid = 0, picked = 0, bu = 0;
+    uint32_t ko[EPL];
     int bm = 0;
 #pragma unroll
-    for (int m = 0; m < EPL; ++m)
-        if (r[m].w >= 0.0f) {
-            valid |= 1u << m;
-            const uint32_t ku = key_order(r[m].x);
-            if (ku > bu) { bu = ku; bm = m; }
-        }
+    for (int m = 0; m < EPL; ++m) {
+        if (r[m].w >= 0.0f) valid |= 1u << m;
+        ko[m] = key_order(r[m].x);
+    }
+    lane_best<EPL>(ko, valid, bu, bm);
     int n = 0;
     for (int j = 0; j < k; ++j) {
         const uint32_t M = __reduce_max_sync(0xffffffffu, bu);
@@ -426,13 +449,7 @@ __device__ __forceinline__ void select_row(const RouteArgs& a, int t, int lane, 
         const uint32_t win = __reduce_min_sync(0xffffffffu, bu == M ? (uint32_t)(lane + 32 * bm) : 0xFFFFFFFFu);
         if ((int)(win & 31) == lane) {
             picked |= 1u << (win >> 5);
-            bu = 0;
-#pragma unroll
-            for (int m = 0; m < EPL; ++m)
-                if (((valid & ~picked) >> m) & 1u) {
-                    const uint32_t ku = key_order(r[m].x);
-                    if (ku > bu) { bu = ku; bm = m; }
-                }
+            lane_best<EPL>(ko, valid & ~picked, bu, bm);
         }
         ++n;
     }
