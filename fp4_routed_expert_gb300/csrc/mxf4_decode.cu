@@ -27,7 +27,7 @@ constexpr int kWCodes = kWRows * kKBytes;         // 32 KB of codes per K block
 constexpr int kWScales = 2 * kTileScaleBytes;     // the two tiles' scale atoms
 constexpr int kDecEpi = 16;                       // epilogue warps: four per TMEM lane quarter
 constexpr int kDecThreads = (2 + kDecEpi) * 32;   // producer, MMA issuer, epilogue warps
-constexpr int kDecUQ = 8;
+constexpr int kDecUQ = 8;                         // unit ids in flight from the producer to the other warps
 constexpr int kDecMaxK = 8;                       // top-k of a decode call on the tensor cores at most
 
 // Activation blocks of this kernel: block (tile t, K block kb) holds kTerms * NT rows of 128
@@ -233,10 +233,11 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
 //           bulk copy of the activation block (x, or the key's h once every gate/up unit of
 //           the key has written it)
 //   warp 1  MMA issuer (one lane): scale atoms into TMEM, 4 MMAs of N = 256 per K block
-//   warps 2..9 epilogue: the warps on the TMEM lane quarters that hold activation rows read
-//           the accumulator (each warp 128 of the 256 columns), add the kTerms lanes of a
-//           token, then gate/up: SwiGLU into shared memory and kTerms-term MXFP4 encoding of h
-//           (one warp per 32-element block) into each pair's row of its key's h tile;
+//   warps 2..17 epilogue, four per TMEM lane quarter: the warps on the quarters that hold
+//           activation rows read the accumulator (each warp 64 of the 256 columns, by
+//           16x256b loads that hand a thread every term of one token), add the terms, then
+//           gate/up: SwiGLU into shared memory, and one thread per (token, 32-element block)
+//           encodes h into kTerms MXFP4 terms in each pair's row of its key's h tile;
 //           down: fp32 rows per pair, and the fixed-order combine of every 32 features of y
 //           by the warp that completes them
 // x is encoded by the CTAs before the wait on the router.  Every wait is bounded; a timeout
