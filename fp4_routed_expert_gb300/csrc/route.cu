@@ -759,46 +759,44 @@ __global__ void route_norms_kernel(RouteArgs a) {
     }
 }
 
-// 128 tokens x 64 experts per block, 8 tokens x 4 experts per thread, K staged 32 at a time
-// (the next step's operands are loaded into registers while the current one is multiplied).
+// 64 tokens x 64 experts per block of 128 threads (four resident per SM, so that a grid of a
+// few hundred tiles spreads evenly over the SMs), 8 tokens x 4 experts per thread, K staged 32
+// at a time (the next step's operands are loaded into registers while the current one is
+// multiplied).
 // Each output is accumulated in chunks of 256 products (fresh partial sums, products in
 // ascending K) added into a running total, so every rounding path has at most 256 + ceil(d/256)
 // roundings.  The epilogue turns each logit into its key record with the Cauchy-Schwarz bound
 // (norms computed beforehand).
-constexpr int kTileT = 128, kTileE = 64, kRouteTileK = 32, kChunkK = 256;
+constexpr int kTileT = 64, kTileE = 64, kRouteTileK = 32, kChunkK = 256, kTiledThreads = 128;
 
-__global__ void __launch_bounds__(256, 2) route_tiled_kernel(RouteArgs a) {
+__global__ void __launch_bounds__(kTiledThreads, 4) route_tiled_kernel(RouteArgs a) {
     __shared__ __align__(16) float xs[kRouteTileK][kTileT + 4];
     __shared__ __align__(16) float ws[kRouteTileK][kTileE + 4];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.y * kTileT, e0 = blockIdx.x * kTileE;
     // loads: a warp takes 32 consecutive rows at one K offset, so its transposed stores hit
-    // distinct banks.  x: row 32 (w % 4) + lane, K offset 16 (w / 4), 16 values; W: row
-    // 32 (w % 2) + lane, K offset 8 (w / 2), 8 values.
-    const int xr = 32 * (warp & 3) + lane, xc = 16 * (warp >> 2);
-    const int wr = 32 * (warp & 1) + lane, wc = 8 * (warp >> 1);
-    const bool xok = t0 + xr < a.T, wok = e0 + wr < a.E;
+    // distinct banks.  x and W alike: row 32 (w % 2) + lane, K offset 16 (w / 2), 16 values.
+    const int xr = 32 * (warp & 1) + lane, xc = 16 * (warp >> 1);
+    const bool xok = t0 + xr < a.T, wok = e0 + xr < a.E;
     const uint16_t* xp = a.x + (size_t)(t0 + xr) * a.d + xc;
-    const uint16_t* wp = a.wr + (size_t)(e0 + wr) * a.d + wc;
-    uint4 xv0, xv1, wv;
+    const uint16_t* wp = a.wr + (size_t)(e0 + xr) * a.d + xc;
+    uint4 xv0, xv1, wv0, wv1;
     auto load = [&](int k0) {
         const uint4 z = make_uint4(0, 0, 0, 0);
         xv0 = xok ? __ldg(reinterpret_cast<const uint4*>(xp + k0)) : z;
         xv1 = xok ? __ldg(reinterpret_cast<const uint4*>(xp + k0 + 8)) : z;
-        wv = wok ? __ldg(reinterpret_cast<const uint4*>(wp + k0)) : z;
+        wv0 = wok ? __ldg(reinterpret_cast<const uint4*>(wp + k0)) : z;
+        wv1 = wok ? __ldg(reinterpret_cast<const uint4*>(wp + k0 + 8)) : z;
     };
     auto store = [&]() {
         const uint32_t xw[8] = {xv0.x, xv0.y, xv0.z, xv0.w, xv1.x, xv1.y, xv1.z, xv1.w};
+        const uint32_t ww[8] = {wv0.x, wv0.y, wv0.z, wv0.w, wv1.x, wv1.y, wv1.z, wv1.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             xs[xc + 2 * i][xr] = bf16_lo(xw[i]);
             xs[xc + 2 * i + 1][xr] = bf16_hi(xw[i]);
-        }
-        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            ws[wc + 2 * i][wr] = bf16_lo(ww[i]);
-            ws[wc + 2 * i + 1][wr] = bf16_hi(ww[i]);
+            ws[xc + 2 * i][xr] = bf16_lo(ww[i]);
+            ws[xc + 2 * i + 1][xr] = bf16_hi(ww[i]);
         }
     };
     float tot[8][4], part[8][4];
@@ -935,7 +933,7 @@ static int launch_route_args(RouteArgs& a, cudaStream_t st, int num_sms) {
     const int rows = a.T + a.E;
     route_norms_kernel<<<(rows + 7) / 8, 256, 0, st>>>(a);
     dim3 grid((a.E + kTileE - 1) / kTileE, (a.T + kTileT - 1) / kTileT);
-    route_tiled_kernel<<<grid, 256, 0, st>>>(a);
+    route_tiled_kernel<<<grid, kTiledThreads, 0, st>>>(a);
     note_launch(2);
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_LAUNCH;
     return launch_select(a, st);
