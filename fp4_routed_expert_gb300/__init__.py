@@ -18,7 +18,7 @@ from . import build as _build
 __all__ = [
     "MoeError", "moe_dims", "moe_arena", "lib", "moe_slot_bytes", "moe_workspace_bytes",
     "moe_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_route_topk_noalloc", "moe_permute",
-    "moe_expert_ffn_fp4", "moe_combine", "moe_residency_bias", "moe_split_waves", "moe_gather_experts", "moe_status_str",
+    "moe_expert_ffn_fp4", "moe_layer_decode_fp4", "moe_combine", "moe_residency_bias", "moe_split_waves", "moe_gather_experts", "moe_status_str",
     "moe_cb3_slot_bytes", "moe_pack_cb3", "moe_expert_ffn_cb3", "MOE_STATUS_CB3_ROW",
     "moe_kernel_launches", "moe_workspace_set_wait_limit", "moe_residual_rmsnorm", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
     "MOE_STATUS_FEW_RESIDENT", "MOE_STATUS_BAD_SLOT", "MOE_STATUS_TIMEOUT", "DECODE_MAX_T",
@@ -60,6 +60,7 @@ _SIG = {
     "moe_route_topk": (ctypes.c_int, [_P, _I] + [_P] * 9 + [ctypes.c_size_t, _P]),
     "moe_permute": (ctypes.c_int, [_P, _I] + [_P] * 5 + [ctypes.c_size_t, _P]),
     "moe_expert_ffn_fp4": (ctypes.c_int, [_P, _P, _I] + [_P] * 7 + [_I] + [_P] * 4 + [ctypes.c_size_t, _P]),
+    "moe_layer_decode_fp4": (ctypes.c_int, [_P, _P, _I] + [_P] * 10 + [ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [_P, _I] + [_P] * 5),
     "moe_residency_bias": (ctypes.c_int, [_P, _P, _P, _P, _I, ctypes.c_float, _P, _P]),
     "moe_cb3_slot_bytes": (ctypes.c_int64, [_P]),
@@ -178,6 +179,14 @@ def moe_expert_ffn_fp4(dims, arena: moe_arena, T, x, topk_ids, topk_slot, topk_w
         ctypes.byref(_dims(dims)), ctypes.byref(arena), int(T), _ptr(x), _ptr(topk_ids), _ptr(topk_slot),
         _ptr(topk_w), _ptr(group_offsets), _ptr(row_src), _ptr(row_dst), int(flags), _ptr(rows_out), _ptr(y),
         _ptr(dev_status), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_layer_decode_fp4(dims, arena: moe_arena, T, x, w_router, score_bias, expert_to_slot, topk_ids, topk_w,
+                         topk_slot, y, dev_status, ws, stream=None):
+    _check("moe_layer_decode_fp4", lib().moe_layer_decode_fp4(
+        ctypes.byref(_dims(dims)), ctypes.byref(arena), int(T), _ptr(x), _ptr(w_router), _ptr(score_bias),
+        _ptr(expert_to_slot), _ptr(topk_ids), _ptr(topk_w), _ptr(topk_slot), _ptr(y), _ptr(dev_status), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_residual_rmsnorm(T, d, x, y, eps, x_next, stream=None):

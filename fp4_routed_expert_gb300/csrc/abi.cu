@@ -4,7 +4,7 @@
 #include <atomic>
 #include <cstdio>
 
-#include "moe_internal.cuh"
+#include "route_select.cuh"
 
 namespace fp4moe {
 
@@ -34,7 +34,7 @@ int launch_cb3_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t
 bool tc_decode_supported(const moe_dims* m, int T);
 int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                      const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
-                     int num_sms);
+                     int num_sms, const RouteArgs* ra = nullptr, int route_blocks = 0);
 int launch_residency_bias(const moe_dims* m, const int32_t* expert_to_slot, const int32_t* resident_expert,
                           int num_slots, const float* bias, float lambda, float* bias_out, cudaStream_t st);
 int launch_split_waves(const moe_dims* m, int T, const int32_t* ids, const int32_t* slot, const int32_t* resident_expert,
@@ -227,6 +227,42 @@ int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, 
         rc = launch_prefill_ffn(dims, arena, T, x, topk_slot, group_offsets, row_src, rows, dev_status, w, L, st, sms);
     if (rc || !fused) return rc;
     return launch_combine(dims, T, rows, row_dst, topk_w, y, st, sms);
+}
+
+int moe_layer_decode_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, const uint16_t* x,
+                         const uint16_t* w_router, const float* score_bias, const int32_t* expert_to_slot,
+                         int32_t* topk_ids, float* topk_w, int32_t* topk_slot, uint16_t* y, int32_t* dev_status,
+                         void* ws, size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (T < 0 || T > kDecodeMaxT) return MOE_ERR_TOKENS;
+    int rc = check_arena(dims, arena);
+    if (rc) return rc;
+    if (!x || !w_router || !expert_to_slot || !topk_ids || !topk_w || !topk_slot || !y || !dev_status)
+        return MOE_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w_router)) return MOE_ERR_ALIGN;
+    WsLayout L;
+    rc = check_ws(dims, T, ws, ws_bytes, &L);
+    if (rc) return rc;
+    if (T == 0) return MOE_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    char* w = static_cast<char*>(ws);
+    const int sms = num_sms_of_current_device();
+    const bool tc = tc_decode_supported(dims, T);
+    if (tc) {
+        // router kernel with its records handed to the expert kernel, which selects
+        RouteArgs ra{};
+        int blocks = 0;
+        rc = launch_route_handoff(dims, T, x, w_router, score_bias, expert_to_slot, topk_ids, topk_w, topk_slot,
+                                  dev_status, w, L, st, sms, &ra, &blocks);
+        if (rc == MOE_OK)
+            return launch_tc_decode(dims, arena, T, x, topk_slot, topk_w, y, dev_status, w, L, st, sms, &ra, blocks);
+        if (rc != 1) return rc;
+    }
+    rc = launch_route(dims, T, x, w_router, score_bias, expert_to_slot, topk_ids, topk_w, topk_slot, dev_status, w,
+                      L, st, sms);
+    if (rc) return rc;
+    if (tc) return launch_tc_decode(dims, arena, T, x, topk_slot, topk_w, y, dev_status, w, L, st, sms);
+    return launch_stream_ffn(dims, arena, T, x, topk_slot, topk_w, y, dev_status, w, L, st, sms);
 }
 
 int moe_residency_bias(const moe_dims* dims, const float* score_bias, const int32_t* expert_to_slot,

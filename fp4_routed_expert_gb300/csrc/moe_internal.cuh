@@ -110,6 +110,8 @@ __host__ __device__ inline int plan_pair_off(int E, int max_tiles) { return plan
 
 // Workspace sections, each 256-byte aligned.  The persistent counters come first so that
 // their offset is the same for every token count; the other sections are per call.
+struct RouteArgs;   // router launch arguments (route_select.cuh)
+
 struct WsLayout {
     size_t keys;        // float4 [T_max, E] router key records {key, key lo, key hi, score}
     size_t xnorm;       // fp32 [T_max]      ||x_t||_2

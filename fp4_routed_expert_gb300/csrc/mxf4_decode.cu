@@ -19,6 +19,7 @@
 #include <cuda.h>
 
 #include "mxf4_common.cuh"
+#include "route_select.cuh"
 
 namespace fp4moe {
 
@@ -67,7 +68,25 @@ struct DecParams {
     int32_t* xready;
     int32_t* exit_ctr;
     const int32_t* wait_limit;       // polls of a wait on another CTA (0: kSpinLimit)
+    // Selection handed over by the routing call (sel_epl 4 or 12, the experts per lane of a
+    // selecting warp; 0: slot and w are the routing call's outputs): its key records, one
+    // release per router block on ra.counter (route_blocks in all); this kernel selects and
+    // CTA 0 writes ra.ids, ra.w and ra.slots.
+    RouteArgs ra;
+    int route_blocks;
+    int sel_epl;
 };
+
+// Selecting warps' arrays in the stage buffers (free until the producer starts): one
+// select_smem_per_warp(kHandoffMaxExperts) region per token, then the chosen slots and ids.
+constexpr int kSelWarpBytes = (int)select_smem_per_warp(kHandoffMaxExperts);
+constexpr int kSelSlotOff = kDecodeMaxT * kSelWarpBytes;
+constexpr int kSelIdOff = kSelSlotOff + kMaxDecodePairs * 4;
+
+template <int EPL>
+__device__ __forceinline__ void dec_select(const RouteArgs& a, int t, int lane, float4* rec, float* exk, int* out, SelOut o) {
+    select_row<EPL>(a, t, lane, rec, exk, out, o);
+}
 
 // Decode keys of one call (one warp, pair i = t*k + j on lane i mod 32): a key is a slot's pairs,
 // in order of their appearance, in chunks of at most NT (the rows of one activation tile).
@@ -266,6 +285,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
     __shared__ int kinfo[kMaxDecodePairs];
     __shared__ short kplist[kMaxDecodePairs];
     __shared__ int uq[kDecUQ];
+    __shared__ int sel_ok_sh;
+    static_assert(2 * C::kStages + 4 + 2 * kDecUQ <= 64, "the barriers fit below the routing weights");
+    float* selw = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512);   // [T*k] routing weights
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int kEpi = kDecEpi;
@@ -352,14 +374,73 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
                              nk, np);
         __syncwarp();
     }
-    // the router's outputs are read from here on; the next kernel (the next call's router)
-    // may launch now: before it waits for this kernel in turn it only stages its own weights
-    pdl_wait();
-    pdl_trigger();
     unsigned dep_limit = kSpinLimit;
-    if (p.wait_limit && *p.wait_limit > 0) dep_limit = (unsigned)*p.wait_limit;
+    const int npairs = p.T * p.k;
+    const int32_t* setup_slot = p.slot;
+    if (p.sel_epl) {
+        // The routing call handed its key records over.  The next kernel may launch now (it
+        // waits for this one before it writes anything this kernel reads); warps 2 .. T + 1
+        // select one token each once every router block has released its records, and CTA 0
+        // writes the routing outputs.
+        pdl_trigger();
+        {
+            const int wl = ld_acquire(p.wait_limit);
+            if (wl > 0) dep_limit = (unsigned)wl;
+        }
+        int32_t* sel_slot = reinterpret_cast<int32_t*>(stage_base + kSelSlotOff);
+        int32_t* sel_id = reinterpret_cast<int32_t*>(stage_base + kSelIdOff);
+        const int t = warp - 2;
+        if (t >= 0 && t < p.T) {
+            if (t == 0 && lane == 0) {
+                int ok = 0;
+                for (unsigned i = 0; i < dep_limit; ++i)
+                    if (ld_acquire(reinterpret_cast<const int32_t*>(p.ra.counter)) >= p.route_blocks) {
+                        ok = 1;
+                        break;
+                    }
+                if (!ok) {
+                    atomicOr(p.status, MOE_STATUS_TIMEOUT);
+                    *abortp = 1;
+                }
+                sel_ok_sh = ok;
+            }
+            __syncwarp();
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * p.T) : "memory");   // the selecting warps
+            const SelOut o{sel_id + t * p.k, selw + t * p.k, sel_slot + t * p.k, blockIdx.x == 0 ? p.status : nullptr};
+            if (sel_ok_sh) {
+                uint8_t* wsm = stage_base + (size_t)t * kSelWarpBytes;
+                float4* rec = reinterpret_cast<float4*>(wsm);
+                float* exk = reinterpret_cast<float*>(wsm + (size_t)p.ra.E * 16);
+                int* out = reinterpret_cast<int*>(wsm + (size_t)p.ra.E * 20);
+                if (p.sel_epl == 4) dec_select<4>(p.ra, t, lane, rec, exk, out, o);
+                else dec_select<12>(p.ra, t, lane, rec, exk, out, o);
+            } else {
+                for (int j = lane; j < p.k; j += 32) {
+                    o.ids[j] = -1;
+                    o.w[j] = 0.0f;
+                    o.slots[j] = -1;
+                }
+            }
+        }
+        __syncthreads();
+        if (blockIdx.x == 0)
+            for (int i = tid; i < npairs; i += blockDim.x) {
+                p.ra.ids[i] = sel_id[i];
+                p.ra.w[i] = selw[i];
+                p.ra.slots[i] = sel_slot[i];
+            }
+        setup_slot = sel_slot;
+    } else {
+        // the router's outputs are read from here on; the next kernel (the next call's router)
+        // may launch now: before it waits for this kernel in turn it only stages its own weights
+        pdl_wait();
+        pdl_trigger();
+        if (p.wait_limit && *p.wait_limit > 0) dep_limit = (unsigned)*p.wait_limit;
+        if (warp == 1)
+            for (int i = lane; i < npairs; i += 32) selw[i] = p.w[i];
+    }
     if (warp == 0)
-        decode_key_setup<NT>(p.slot, p.T * p.k, p.num_slots, p.status, blockIdx.x == 0, lane, pinfo, kslot, kinfo,
+        decode_key_setup<NT>(setup_slot, npairs, p.num_slots, p.status, blockIdx.x == 0, lane, pinfo, kslot, kinfo,
                              kplist, reinterpret_cast<int*>(hbuf), n_keys_sh, pairs_total_sh);
     // the keys are known; every role reads their count here, before any of them can abort
     // on a later wait (the setup itself waits on nothing)
@@ -647,7 +728,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
                                 for (int jj = 0; jj < kDecMaxK; ++jj) {
                                     const int pr = t * p.k + jj;
                                     const bool ok = jj < p.k && pinfo[pr] >= 0;
-                                    wv[jj] = ok ? __ldg(p.w + pr) : 0.f;
+                                    wv[jj] = ok ? selw[pr] : 0.f;
 #pragma unroll
                                     for (int c = 0; c < 2; ++c)
                                         rv[c][jj] = (ok && ((lastm >> c) & 1u))
@@ -732,6 +813,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
             if (ew == 0 && lane == 0) red_add_release(p.ready + key, 1);
         }
     }
+    if (p.sel_epl) pdl_wait();   // a call that selects completes after its routing call
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -747,6 +829,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
             *p.work = 0;
             *p.xready = 0;
             *p.exit_ctr = 0;
+            if (p.sel_epl) *reinterpret_cast<int32_t*>(p.ra.counter) = 0;
         }
     }
 }
@@ -809,9 +892,10 @@ static int launch_dec(const DecParams& p, int grid, cudaStream_t st) {
 // one token never mix with another's, so a token's results are the same with either.
 int launch_decode_wide(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                        const float* w, uint16_t* y, int32_t* status, uint8_t* xq, uint8_t* hq, float* rows,
-                       int32_t* ctr, cudaStream_t st, int num_sms) {
+                       int32_t* ctr, cudaStream_t st, int num_sms, const RouteArgs* ra, int route_blocks) {
     if (T == 0) return MOE_OK;
     if (m->top_k > kDecMaxK || T > kDecodeNT) return MOE_ERR_DIMS;
+    if (ra && (ra->E > kHandoffMaxExperts || ra->T != T || ra->k != m->top_k || route_blocks < 1)) return MOE_ERR_DIMS;
     DecParams p{};
     const SlotLayout SL = slot_layout(m->d, m->f);
     if (!weight_maps(&p.wcodes[0], &p.wscales[0], ar, SL.gu, m->d / kKB, 2 * m->f / kBM) ||
@@ -827,6 +911,11 @@ int launch_decode_wide(const moe_dims* m, const moe_arena* ar, int T, const uint
     p.ready = ctr + kCtrFfnReady;
     p.ycnt = ctr + kCtrFfnY;
     p.wait_limit = ctr + kCtrWaitLimit;
+    if (ra) {
+        p.ra = *ra;
+        p.route_blocks = route_blocks;
+        p.sel_epl = ra->E <= 128 ? 4 : 12;
+    }
     const int grid = num_sms < 256 ? num_sms : 256;
     return T <= 8 ? launch_dec<8>(p, grid, st) : launch_dec<kDecodeNT>(p, grid, st);
 }

@@ -680,15 +680,15 @@ static FfnParams ffn_params(const moe_dims* m, const moe_arena* ar, int T, const
 // on this workspace's x and h tiles, per-pair rows and persistent counters.
 int launch_decode_wide(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                        const float* w, uint16_t* y, int32_t* status, uint8_t* xq, uint8_t* hq, float* rows,
-                       int32_t* ctr, cudaStream_t st, int num_sms);
+                       int32_t* ctr, cudaStream_t st, int num_sms, const RouteArgs* ra, int route_blocks);
 
 int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                      const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
-                     int num_sms) {
+                     int num_sms, const RouteArgs* ra, int route_blocks) {
     if (T == 0) return MOE_OK;
     TcBuffers b = tc_buffers(m, T, ws, L);
     return launch_decode_wide(m, ar, T, x, slot, w, y, status, b.x, b.h, b.rows,
-                              reinterpret_cast<int32_t*>(ws + L.counter), st, num_sms);
+                              reinterpret_cast<int32_t*>(ws + L.counter), st, num_sms, ra, route_blocks);
 }
 
 __global__ void plan_kernel(int E, int n, const int32_t* offsets, const int32_t* row_src, const int32_t* slot,

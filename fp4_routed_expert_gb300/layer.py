@@ -5,8 +5,8 @@ from __future__ import annotations
 import torch
 
 from . import (DECODE_MAX_T, MOE_FFN_CUDA_CORES, MOE_FUSE_COMBINE, moe_arena, moe_cb3_slot_bytes, moe_dims,
-               moe_expert_ffn_cb3, moe_expert_ffn_fp4, moe_pack_cb3, moe_pack_expert, moe_permute, moe_route_topk,
-               moe_slot_bytes, moe_workspace_bytes, moe_workspace_init)
+               moe_expert_ffn_cb3, moe_expert_ffn_fp4, moe_layer_decode_fp4, moe_pack_cb3, moe_pack_expert,
+               moe_permute, moe_route_topk, moe_slot_bytes, moe_workspace_bytes, moe_workspace_init)
 
 
 def aligned_empty(nbytes: int, align: int = 1024, device=None) -> torch.Tensor:
@@ -109,6 +109,15 @@ class MoeLayer:
             moe_expert_ffn_fp4(self.dims, self.arena.c, T, x, self.ids, self.slots, self.w, self.offsets,
                                self.row_src, self.row_dst, extra, self.rows, None, self.status, self.ws, stream)
             moe_combine(self.dims, T, self.rows, self.row_dst, self.w, y, stream)
+        return y
+
+    def decode(self, x, w_router, table, bias=None, T=None, stream=None, y=None):
+        """Routing, expert FFN and combine of a decode call (T <= 16) in one request
+        (moe_layer_decode_fp4): the same outputs as route() then experts()."""
+        T = x.shape[0] if T is None else T
+        y = self.y if y is None else y
+        moe_layer_decode_fp4(self.dims, self.arena.c, T, x, w_router, bias, table, self.ids, self.w, self.slots, y,
+                             self.status, self.ws, stream)
         return y
 
     def forward(self, x, w_router, table, bias=None, stream=None, y=None, cuda_cores=False):

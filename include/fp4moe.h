@@ -34,7 +34,7 @@
  *    read only these inputs, which the kernel enqueued immediately before the call must
  *    therefore not write: x and w_router of a decode-size routing call (T <= 16), whose
  *    logits are computed while the previous call's expert kernel finishes, and x of a decode
- *    call of moe_expert_ffn_fp4.  Every other input, every output and the workspace are
+ *    call of moe_expert_ffn_fp4 or moe_layer_decode_fp4 (which also reads w_router early).  Every other input, every output and the workspace are
  *    touched only after it has completed.  (A kernel that never signals an early launch --
  *    a plain CUDA kernel, or this library's residual/RMSNorm step -- completes before the
  *    next one starts, so x written by such a kernel is safe.)
@@ -198,6 +198,23 @@ int moe_expert_ffn_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, 
                        const int32_t* group_offsets, const int32_t* row_src, const int32_t* row_dst,
                        int32_t flags, float* rows_out, uint16_t* y, int32_t* dev_status, void* ws,
                        size_t ws_bytes, void* stream);
+
+/* a1-a3 and a5-a6 of a decode call in one request: the outputs (topk_ids, topk_w, topk_slot,
+ * y) are bit for bit those of moe_route_topk followed by moe_expert_ffn_fp4 with
+ * MOE_FUSE_COMBINE on the same stream and workspace.  0 <= T <= 16 (larger T returns
+ * MOE_ERR_TOKENS); arguments as in those two calls.  On the tensor-core path with at most 384
+ * experts the router kernel writes only its key records and the expert kernel selects from
+ * them itself (one warp per token in every CTA; CTA 0 writes the routing outputs), so the
+ * expert reads start without waiting for a separate selection to complete: the boundary
+ * between the router's result and the expert reads ("Start the expert reads before the GPU is
+ * done", 28 September follow-up: the wait on the router mailbox and the boundaries between a
+ * layer's command buffers) becomes a counter inside the GPU.  Other calls run the two steps as
+ * separate launches.  The routing outputs are written while the expert kernel runs: read them
+ * after this call completes. */
+int moe_layer_decode_fp4(const moe_dims* dims, const moe_arena* arena, int32_t T, const uint16_t* x,
+                         const uint16_t* w_router, const float* score_bias, const int32_t* expert_to_slot,
+                         int32_t* topk_ids, float* topk_w, int32_t* topk_slot, uint16_t* y,
+                         int32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
 
 /* a6 (unfused): y[t] = bf16( sum_j topk_w[t,j] * rows[row_dst[t*k+j]] ) in ascending j,
  * skipping row_dst = -1.  rows fp32 [T*k, d]. */

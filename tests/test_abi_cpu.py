@@ -85,5 +85,17 @@ def test_host_argument_errors_return_before_any_launch():
                                 1 << 30, None) == -1
     assert L.moe_expert_ffn_cb3(ctypes.byref(good), ctypes.byref(cb3_ar), 1, fake, fake, fake, fake, fake, fake,
                                 16, None) == -4
+    lay = L.moe_layer_decode_fp4
+    ok_ar = moe.moe_arena(1 << 20, moe.moe_slot_bytes(good), 4)
+    bad_ar = moe.moe_arena(1 << 20, 12345, 4)
+    args = lambda d, ar, T, x=fake, y=fake, wsb=1 << 30: (ctypes.byref(d), ctypes.byref(ar), T, x, fake, None, fake,
+                                                        fake, fake, fake, y, fake, fake, wsb, None)
+    assert lay(*args(bad, ok_ar, 1)) == -2
+    assert lay(*args(good, ok_ar, 17)) == -3                  # decode only: T <= 16
+    assert lay(*args(good, ok_ar, -1)) == -3
+    assert lay(*args(good, bad_ar, 1)) == -5
+    assert lay(*args(good, ok_ar, 1, y=None)) == -1
+    assert lay(*args(good, ok_ar, 1, x=P((1 << 20) + 2))) == -8
+    assert lay(*args(good, ok_ar, 1, wsb=16)) == -4
     assert moe.moe_status_str(-4) == "workspace too small"
     assert moe.moe_kernel_launches() == launched      # every rejected call launched nothing
