@@ -373,15 +373,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
         decode_key_setup<NT>(dummy, n, 1, p.status, false, lane, pinfo, kslot, kinfo, kplist, dummy + kMaxDecodePairs,
                              nk, np);
         __syncwarp();
+        // a call that selects here sets up its keys in warp 2: it waits for this warm-up (barrier 2)
+        if (p.sel_epl) asm volatile("bar.arrive 2, 64;" ::: "memory");
     }
     unsigned dep_limit = kSpinLimit;
     const int npairs = p.T * p.k;
-    const int32_t* setup_slot = p.slot;
     if (p.sel_epl) {
         // The routing call handed its key records over.  The next kernel may launch now (it
         // waits for this one before it writes anything this kernel reads); warps 2 .. T + 1
-        // select one token each once every router block has released its records, and CTA 0
-        // writes the routing outputs.
+        // select one token each once every router block has released its records (CTA 0 also
+        // writes the routing outputs), then warp 2 sets up the keys.
         pdl_trigger();
         {
             const int wl = ld_acquire(p.wait_limit);
@@ -421,15 +422,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
                     o.slots[j] = -1;
                 }
             }
+            __syncwarp();
+            if (blockIdx.x == 0)
+                for (int j = lane; j < p.k; j += 32) {
+                    p.ra.ids[t * p.k + j] = o.ids[j];
+                    p.ra.w[t * p.k + j] = o.w[j];
+                    p.ra.slots[t * p.k + j] = o.slots[j];
+                }
+            // the keys, by the first selecting warp once every token is selected
+            if (p.T > 1) asm volatile("bar.sync 1, %0;" ::"r"(32 * p.T) : "memory");
+            if (t == 0) asm volatile("bar.sync 2, 64;" ::: "memory");   // warp 0's warm-up is done
+            if (t == 0)
+                decode_key_setup<NT>(sel_slot, npairs, p.num_slots, p.status, blockIdx.x == 0, lane, pinfo, kslot,
+                                     kinfo, kplist, reinterpret_cast<int*>(hbuf), n_keys_sh, pairs_total_sh);
         }
-        __syncthreads();
-        if (blockIdx.x == 0)
-            for (int i = tid; i < npairs; i += blockDim.x) {
-                p.ra.ids[i] = sel_id[i];
-                p.ra.w[i] = selw[i];
-                p.ra.slots[i] = sel_slot[i];
-            }
-        setup_slot = sel_slot;
     } else {
         // the router's outputs are read from here on; the next kernel (the next call's router)
         // may launch now: before it waits for this kernel in turn it only stages its own weights
@@ -438,10 +444,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
         if (p.wait_limit && *p.wait_limit > 0) dep_limit = (unsigned)*p.wait_limit;
         if (warp == 1)
             for (int i = lane; i < npairs; i += 32) selw[i] = p.w[i];
+        if (warp == 0)
+            decode_key_setup<NT>(p.slot, npairs, p.num_slots, p.status, blockIdx.x == 0, lane, pinfo, kslot, kinfo,
+                                 kplist, reinterpret_cast<int*>(hbuf), n_keys_sh, pairs_total_sh);
     }
-    if (warp == 0)
-        decode_key_setup<NT>(setup_slot, npairs, p.num_slots, p.status, blockIdx.x == 0, lane, pinfo, kslot, kinfo,
-                             kplist, reinterpret_cast<int*>(hbuf), n_keys_sh, pairs_total_sh);
     // the keys are known; every role reads their count here, before any of them can abort
     // on a later wait (the setup itself waits on nothing)
     __syncthreads();

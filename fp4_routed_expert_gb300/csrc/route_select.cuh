@@ -374,8 +374,9 @@ inline __device__ __noinline__ void select_token(const RouteArgs& a, int t, int 
 }
 
 // The selection of token t by one warp (lane l holds the key records of experts l + 32 m,
-// m < EPL, in registers): a top-k round is two warp reductions (largest key, then lowest id
-// among equal keys) and a register rescan by the winning lane.  The chosen set is final when
+// m < EPL, in registers): a top-k round is a warp reduction (largest key) and a ballot of
+// the lanes holding it (a second reduction, lowest id, only when several do); the winning
+// lane promotes its second candidate and rescans its registers.  The chosen set is final when
 // every chosen expert's key interval lies above every other expert's and every chosen score
 // is narrow; otherwise the token goes whole to select_token (same warp).  E <= 32 * EPL.
 // rec, exk and out are this warp's select_token arrays in shared memory.
@@ -426,25 +427,51 @@ __device__ __forceinline__ void select_row(const RouteArgs& a, int t, int lane, 
         ko[m] = key_order(r[m].x);
     }
     lane_best<EPL>(ko, valid, bu, bm);
+    // Each lane also keeps its second candidate: a winning lane promotes it at once and
+    // rescans for the next one just after the following round's reduction is issued, so that
+    // the rescan overlaps the reduction instead of preceding it.
+    uint32_t bu2;
+    int bm2;
+    lane_best<EPL>(ko, valid & ~(1u << bm), bu2, bm2);
+    bool refill = false;
     int n = 0;
     for (int j = 0; j < k; ++j) {
         const uint32_t M = __reduce_max_sync(0xffffffffu, bu);
+        if (refill) {
+            lane_best<EPL>(ko, valid & ~picked & ~(1u << bm), bu2, bm2);
+            refill = false;
+        }
         if (M == 0) break;
-        const uint32_t win = __reduce_min_sync(0xffffffffu, bu == M ? (uint32_t)(lane + 32 * bm) : 0xFFFFFFFFu);
-        if ((int)(win & 31) == lane) {
-            picked |= 1u << (win >> 5);
-            lane_best<EPL>(ko, valid & ~picked, bu, bm);
+        // the winner: the one lane holding M, else the lowest expert id among those that do
+        const uint32_t hold = __ballot_sync(0xffffffffu, bu == M);
+        int wl = __ffs(hold) - 1;
+        if (hold & (hold - 1u))
+            wl = (int)(__reduce_min_sync(0xffffffffu, bu == M ? (uint32_t)(lane + 32 * bm) : 0xFFFFFFFFu) & 31u);
+        if (lane == wl) {
+            picked |= 1u << bm;
+            bu = bu2;
+            bm = bm2;
+            refill = true;
         }
         ++n;
     }
     if (n < k && lane == 0 && o.status) atomicOr(o.status, MOE_STATUS_FEW_RESIDENT);
-    // certification thresholds: min klo over the chosen, max khi over the rest
-    float lo_in = __int_as_float(0x7f800000), hi_out = NEG_INF;
+    // certification thresholds: min klo over the chosen, max khi over the rest (pairwise trees)
+    float lov[EPL], hiv[EPL];
 #pragma unroll
     for (int m = 0; m < EPL; ++m) {
-        if ((picked >> m) & 1u) lo_in = fminf(lo_in, r[m].y);
-        else if ((valid >> m) & 1u) hi_out = fmaxf(hi_out, r[m].z);
+        const bool pk = (picked >> m) & 1u;
+        lov[m] = pk ? r[m].y : __int_as_float(0x7f800000);
+        hiv[m] = (!pk && ((valid >> m) & 1u)) ? r[m].z : NEG_INF;
     }
+#pragma unroll
+    for (int w = 1; w < EPL; w *= 2)
+#pragma unroll
+        for (int m = 0; m + w < EPL; m += 2 * w) {
+            lov[m] = fminf(lov[m], lov[m + w]);
+            hiv[m] = fmaxf(hiv[m], hiv[m + w]);
+        }
+    const float lo_in = lov[0], hi_out = hiv[0];
     const float min_lo_in = key_value(__reduce_min_sync(0xffffffffu, key_order(lo_in)));
     const float max_hi_out = key_value(__reduce_max_sync(0xffffffffu, key_order(hi_out)));
     bool doubt = false, order_doubt = false;
@@ -509,7 +536,14 @@ __device__ __forceinline__ void select_row(const RouteArgs& a, int t, int lane, 
     __syncwarp();
     float sum = 0.0f;
     if (lane == 0)
-        for (int i = 0; i < n; ++i) sum += osc[i];
+        for (int i0 = 0; i0 < n; i0 += 8) {   // the loads of 8 scores together, then their sum in order
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = (i0 + i < n) ? osc[i0 + i] : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i0 + i < n) sum += v[i];
+        }
     sum = __shfl_sync(0xffffffffu, sum, 0);
     int32_t* ids = o.ids;
     float* wo = o.w;
