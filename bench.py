@@ -68,7 +68,7 @@ def env_rank():
 
 
 FFN_SOURCES = ("fp4_routed_expert_gb300/csrc/mxf4_decode.cu", "fp4_routed_expert_gb300/csrc/mxf4_common.cuh",
-               "fp4_routed_expert_gb300/csrc/moe_internal.cuh")
+               "fp4_routed_expert_gb300/csrc/moe_internal.cuh", "fp4_routed_expert_gb300/csrc/route_select.cuh")
 FFN_KERNEL = "mxf4_decode_kernel"
 TRAFFIC_RECORD = "profiles/traffic_expert_ffn_decode_T1_d5120_f2304_E384_k6.json"
 
