@@ -249,6 +249,11 @@ __device__ __forceinline__ int ld_acquire(const int32_t* a) {
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
     return v;
 }
+__device__ __forceinline__ int ld_relaxed(const int32_t* a) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
 __device__ __forceinline__ int atom_add_acq_rel(int32_t* a, int v) {
     int old;
     asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");

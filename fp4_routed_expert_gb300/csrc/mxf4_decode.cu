@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
     __shared__ int kinfo[kMaxDecodePairs];
     __shared__ short kplist[kMaxDecodePairs];
     __shared__ int uq[kDecUQ];
-    __shared__ int sel_ok_sh;
+    __shared__ int sel_ok_sh, wait_limit_sh;
     static_assert(2 * C::kStages + 4 + 2 * kDecUQ <= 64, "the barriers fit below the routing weights");
     float* selw = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512);   // [T*k] routing weights
 
@@ -384,26 +384,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
         // select one token each once every router block has released its records (CTA 0 also
         // writes the routing outputs), then warp 2 sets up the keys.
         pdl_trigger();
-        {
-            const int wl = ld_acquire(p.wait_limit);
-            if (wl > 0) dep_limit = (unsigned)wl;
-        }
         int32_t* sel_slot = reinterpret_cast<int32_t*>(stage_base + kSelSlotOff);
         int32_t* sel_id = reinterpret_cast<int32_t*>(stage_base + kSelIdOff);
         const int t = warp - 2;
         if (t >= 0 && t < p.T) {
             if (t == 0 && lane == 0) {
-                int ok = 0;
-                for (unsigned i = 0; i < dep_limit; ++i)
-                    if (ld_acquire(reinterpret_cast<const int32_t*>(p.ra.counter)) >= p.route_blocks) {
-                        ok = 1;
-                        break;
-                    }
+                // the wait limit and the first poll in flight together
+                const int wl = ld_relaxed(p.wait_limit);
+                int ok = ld_acquire(reinterpret_cast<const int32_t*>(p.ra.counter)) >= p.route_blocks;
+                const unsigned lim = wl > 0 ? (unsigned)wl : kSpinLimit;
+                for (unsigned i = 1; !ok && i < lim; ++i)
+                    ok = ld_acquire(reinterpret_cast<const int32_t*>(p.ra.counter)) >= p.route_blocks;
                 if (!ok) {
                     atomicOr(p.status, MOE_STATUS_TIMEOUT);
                     *abortp = 1;
                 }
                 sel_ok_sh = ok;
+                wait_limit_sh = wl;
             }
             __syncwarp();
             asm volatile("bar.sync 1, %0;" ::"r"(32 * p.T) : "memory");   // the selecting warps
@@ -451,6 +448,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
     // the keys are known; every role reads their count here, before any of them can abort
     // on a later wait (the setup itself waits on nothing)
     __syncthreads();
+    if (p.sel_epl && wait_limit_sh > 0) dep_limit = (unsigned)wait_limit_sh;
     const int n_keys = n_keys_sh;
     const int n0 = n_keys * p.units[0], n_all = n0 + n_keys * p.units[1];
     if (n_keys == 0 && blockIdx.x == 0)   // no valid pair: y is zero
