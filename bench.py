@@ -545,17 +545,16 @@ def run_keepset_decode(ks, T, args, device):
         x.copy_(xs[s])
         for l in range(LAYERS):
             on = probe is not None and s == S // 2
-            if on or log:
-                # the probed step (and the eager pass that logs the ids) runs routing and
-                # experts as separate calls, so that events can bracket each
-                with (probe("route", on) if on else _null()):
-                    layer.route(x, ks.wr[l], ks.tab_dev[l], None, T=T)
-                if log:
-                    ids_log[s, l].copy_(layer.ids[:T])
-                with (probe("ffn", on) if on else _null()):
-                    layer.experts(x, T=T, y=y)
-            else:
-                layer.decode(x, ks.wr[l], ks.tab_dev[l], None, T=T, y=y)
+            # routing and experts as two calls: between layers the RMSNorm step (a plain
+            # launch) ends the overlap of consecutive calls, and then the router's last block
+            # selecting while the expert kernel's CTAs start measured faster than every CTA
+            # selecting (the single request of moe_layer_decode_fp4)
+            with (probe("route", on) if on else _null()):
+                layer.route(x, ks.wr[l], ks.tab_dev[l], None, T=T)
+            if log:
+                ids_log[s, l].copy_(layer.ids[:T])
+            with (probe("ffn", on) if on else _null()):
+                layer.experts(x, T=T, y=y)
             with (probe("norm", on) if on else _null()):
                 moe.moe_residual_rmsnorm(T, D, x, y, NORM_EPS, x)
 
