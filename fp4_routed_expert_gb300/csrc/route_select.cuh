@@ -335,11 +335,30 @@ inline __device__ __noinline__ void select_token(const RouteArgs& a, int t, int 
         final_mask |= chosen;
     }
     // weights: a chosen expert whose key interval is wider than 1e-5 of its score gets its
-    // score from the exact logit, so every score has relative error below 1e-5
+    // record recomputed with the compensated dot product (the refinement of select_row), and
+    // if that interval is still wide, its score from the exact logit, so every score has
+    // relative error below 1e-5
     uint32_t wide = 0;
     for (uint32_t r = final_mask & ~uncertain; r; r &= r - 1) {
         const int m = __ffs(r) - 1, e = lane + 32 * m;
         if (rec[e].z - rec[e].y > 1e-5f * rec[e].w) wide |= 1u << m;
+    }
+    if (a.refine_coef > 0.0f && __any_sync(0xffffffffu, wide != 0)) {
+        for (int m = 0; m < EPL; ++m) {
+            uint32_t bal = __ballot_sync(0xffffffffu, (wide >> m) & 1u);
+            while (bal) {
+                const int src = __ffs(bal) - 1;
+                bal &= bal - 1;
+                const int e = src + 32 * m;
+                const float be = a.bias ? a.bias[e] : 0.0f;
+                const float4 nr = refine_key_warp(xt, a.wr + (size_t)e * a.d, a.d, lane, a.refine_coef, a.table[e], be);
+                if (lane == src && !(nr.z - nr.y > 1e-5f * nr.w)) {
+                    rec[e] = nr;
+                    wide &= ~(1u << m);
+                }
+            }
+        }
+        __syncwarp();
     }
     if (__any_sync(0xffffffffu, wide != 0)) exact_scores(wide);
     // chosen experts in ascending id (m outer, lane inner) into out[0..n); weight sum in that order
