@@ -55,6 +55,32 @@ def test_decode_dependency_wait_times_out_then_workspace_recovers(tiny, cuda_cor
     assert err.max() <= 1e-2, err
 
 
+def test_single_request_decode_wait_times_out_then_workspace_recovers(tiny):
+    """The same through moe_layer_decode_fp4, whose expert kernel also waits for the router's
+    key records (one poll of the router's counter, then the key hand-offs): the call returns
+    with MOE_STATUS_TIMEOUT, and after moe_workspace_init the next single request equals the
+    oracle."""
+    T = 3
+    layer = MoeLayer(tiny.d, tiny.f, tiny.E, tiny.k, T, tiny.arena)
+    x_bits = syn.activations(0, 62, T, tiny.d)
+    x = bits_to_torch(x_bits, DEV)
+    wr = bits_to_torch(tiny.wr, DEV)
+    tab = torch.from_numpy(tiny.table).to(DEV)
+    moe.moe_workspace_set_wait_limit(layer.dims, layer.ws, 1)
+    layer.decode(x, wr, tab)
+    torch.cuda.synchronize()                      # the call returned
+    assert int(layer.status.item()) & moe.MOE_STATUS_TIMEOUT
+    moe.moe_workspace_init(layer.dims, layer.ws)
+    layer.status.zero_()
+    y = layer.decode(x, wr, tab)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    r = dict(ids=layer.ids[:T].cpu().numpy(), slots=layer.slots[:T].cpu().numpy(), weights=layer.w[:T].cpu().numpy())
+    ref = oracle_with_routing(tiny, x_bits, r)
+    err = row_rel_err(y[:T].float().cpu().numpy(), ref)
+    assert err.max() <= 1e-2, err
+
+
 def test_prefill_dependency_wait_times_out_then_workspace_recovers(tiny):
     """The same on the tensor-core prefill path (T = 40 > 16: permuted rows in token tiles; a
     down unit waits for every gate/up unit of its tile)."""
