@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) mxf4_decode_kernel(const __gri
                                  kplist, reinterpret_cast<int*>(hbuf), n_keys_sh, pairs_total_sh);
     }
     // the keys are known; every role reads their count here, before any of them can abort
-    // on a later wait (the setup itself waits on nothing)
+    // on a later wait (a selecting CTA whose poll gave up set every slot to -1: no keys)
     __syncthreads();
     if (p.sel_epl && wait_limit_sh > 0) dep_limit = (unsigned)wait_limit_sh;
     const int n_keys = n_keys_sh;
