@@ -19,7 +19,7 @@ __all__ = [
     "MoeError", "moe_dims", "moe_arena", "lib", "moe_slot_bytes", "moe_workspace_bytes",
     "moe_workspace_init", "moe_pack_expert", "moe_route_topk", "moe_route_topk_noalloc", "moe_permute",
     "moe_expert_ffn_fp4", "moe_layer_decode_fp4", "moe_combine", "moe_residency_bias", "moe_split_waves", "moe_gather_experts", "moe_status_str",
-    "moe_cb3_slot_bytes", "moe_pack_cb3", "moe_expert_ffn_cb3", "MOE_STATUS_CB3_ROW",
+    "moe_cb3_slot_bytes", "moe_pack_cb3", "moe_expert_ffn_cb3", "moe_expert_ffn_cb3_rows", "MOE_STATUS_CB3_ROW",
     "moe_kernel_launches", "moe_workspace_set_wait_limit", "moe_residual_rmsnorm", "MOE_FUSE_COMBINE", "MOE_FFN_CUDA_CORES",
     "MOE_STATUS_FEW_RESIDENT", "MOE_STATUS_BAD_SLOT", "MOE_STATUS_TIMEOUT", "DECODE_MAX_T",
 ]
@@ -66,6 +66,7 @@ _SIG = {
     "moe_cb3_slot_bytes": (ctypes.c_int64, [_P]),
     "moe_pack_cb3": (ctypes.c_int, [_P, _P, _I, _P, _I, _P, _P]),
     "moe_expert_ffn_cb3": (ctypes.c_int, [_P, _P, _I] + [_P] * 6 + [ctypes.c_size_t, _P]),
+    "moe_expert_ffn_cb3_rows": (ctypes.c_int, [_P, _P, _I] + [_P] * 6 + [ctypes.c_size_t, _P]),
     "moe_split_waves": (ctypes.c_int, [_P, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
     "moe_gather_experts": (ctypes.c_int, [_P, _P, _P, _I] + [_P] * 6),
     "moe_route_topk_noalloc": (ctypes.c_int, [_P, _I] + [_P] * 9),
@@ -219,6 +220,13 @@ def moe_expert_ffn_cb3(dims, cb3_arena, T, x, topk_slot, topk_w, y, status, ws, 
     _check("moe_expert_ffn_cb3", lib().moe_expert_ffn_cb3(
         ctypes.byref(_dims(dims)), ctypes.byref(cb3_arena), int(T), _ptr(x), _ptr(topk_slot), _ptr(topk_w), _ptr(y),
         _ptr(status), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_expert_ffn_cb3_rows(dims, cb3_arena, T, x, topk_slot, row_dst, rows_out, status, ws, stream=None):
+    """moe_expert_ffn_cb3 without the combine: pair (t, j) into row row_dst[t*k + j] of rows_out."""
+    _check("moe_expert_ffn_cb3_rows", lib().moe_expert_ffn_cb3_rows(
+        ctypes.byref(_dims(dims)), ctypes.byref(cb3_arena), int(T), _ptr(x), _ptr(topk_slot), _ptr(row_dst),
+        _ptr(rows_out), _ptr(status), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_split_waves(dims, T, topk_ids, topk_slot, resident_expert, num_slots, slot_wave1, slot_wave2, missing,

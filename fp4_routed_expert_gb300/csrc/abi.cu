@@ -30,7 +30,7 @@ bool cb3_ffn_supported(const moe_dims* m);
 int launch_pack_cb3(const moe_dims* m, const uint8_t* src_slot, uint8_t* dst_slot, int32_t* status, cudaStream_t st);
 int launch_cb3_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                    const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
-                   int num_sms);
+                   int num_sms, const int32_t* row_dst = nullptr, float* rows_out = nullptr);
 bool tc_decode_supported(const moe_dims* m, int T);
 int launch_tc_decode(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                      const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
@@ -292,6 +292,7 @@ int moe_gather_experts(const moe_dims* dims, const moe_arena* arena, const void*
                        int32_t* resident_expert, int32_t* dev_status, void* stream) {
     if (!dims_ok(dims)) return MOE_ERR_DIMS;
     int rc = check_arena(dims, arena);
+    if (rc == MOE_ERR_ARENA) rc = check_arena(dims, arena, true);   // a cb3 arena: images of its format
     if (rc) return rc;
     if (!store || !missing || !n_missing || !expert_to_slot || !resident_expert || !dev_status) return MOE_ERR_NULL;
     if (n_store <= 0) return MOE_ERR_DIMS;
@@ -344,6 +345,23 @@ int moe_expert_ffn_cb3(const moe_dims* dims, const moe_arena* cb3_arena, int32_t
     if (rc) return rc;
     return launch_cb3_ffn(dims, cb3_arena, T, x, topk_slot, topk_w, y, dev_status, static_cast<char*>(ws), L,
                           (cudaStream_t)stream, num_sms_of_current_device());
+}
+
+int moe_expert_ffn_cb3_rows(const moe_dims* dims, const moe_arena* cb3_arena, int32_t T, const uint16_t* x,
+                            const int32_t* topk_slot, const int32_t* row_dst, float* rows_out, int32_t* dev_status,
+                            void* ws, size_t ws_bytes, void* stream) {
+    if (!dims_ok(dims)) return MOE_ERR_DIMS;
+    if (!cb3_ffn_supported(dims)) return MOE_ERR_DIMS;
+    if (T < 0 || T > kDecodeMaxT) return MOE_ERR_TOKENS;
+    int rc = check_arena(dims, cb3_arena, true);
+    if (rc) return rc;
+    if (!x || !topk_slot || !row_dst || !rows_out || !dev_status) return MOE_ERR_NULL;
+    if (!aligned16(x)) return MOE_ERR_ALIGN;
+    WsLayout L;
+    rc = check_ws(dims, T, ws, ws_bytes, &L);
+    if (rc) return rc;
+    return launch_cb3_ffn(dims, cb3_arena, T, x, topk_slot, nullptr, nullptr, dev_status, static_cast<char*>(ws), L,
+                          (cudaStream_t)stream, num_sms_of_current_device(), row_dst, rows_out);
 }
 
 int moe_residual_rmsnorm(int32_t T, int32_t d, const uint16_t* x, const uint16_t* y, float eps, uint16_t* x_next,

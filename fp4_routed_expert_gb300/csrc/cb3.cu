@@ -342,7 +342,9 @@ struct Cb3Args {
     int64_t slot_bytes;
     Cb3Layout C;
     uint16_t* h;                // [T*k, f] bf16
-    float* z;                   // [T*k, d]
+    float* z;                   // [T*k, d]: row t*k + j is pair (t, j)
+    const int32_t* row_dst;     // rows output instead (null: z, then the combine into y):
+    float* rows_out;            // pair (t, j) into row row_dst[t*k + j], skipped when < 0
     uint16_t* y;                // [T, d]
     int32_t* status;
 };
@@ -461,6 +463,9 @@ __global__ void __launch_bounds__(256) cb3_down_kernel(Cb3Args a) {
             }
             if (!have) break;
             if (!valid) continue;
+            const int zrow = a.row_dst ? a.row_dst[pair] : pair;
+            if (zrow < 0) continue;
+            float* zr = (a.row_dst ? a.rows_out : a.z) + (size_t)zrow * d;
             // quarter (c, Q) of h_j: 16 bytes at entry 4c + Q; 8 consecutive lanes read 128
             // consecutive bytes (no bank conflict)
             const uint4* hj = hs4 + (size_t)j * (f / 8) + Q;
@@ -489,7 +494,7 @@ __global__ void __launch_bounds__(256) cb3_down_kernel(Cb3Args a) {
 #pragma unroll
             for (int r = 0; r < kCb3DnRows; ++r) {
                 const float v = warp_sum(acc[r]);
-                if (lane == 0) a.z[(size_t)pair * d + r0 + r] = v;
+                if (lane == 0) zr[r0 + r] = v;
             }
         }
     }
@@ -538,9 +543,11 @@ static int launch_down_gl(const Cb3Args& a, size_t smem, int blocks, cudaStream_
 
 int launch_cb3_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
                    const float* w, uint16_t* y, int32_t* status, char* ws, const WsLayout& L, cudaStream_t st,
-                   int num_sms) {
+                   int num_sms, const int32_t* row_dst, float* rows_out) {
     if (T == 0) return MOE_OK;
     Cb3Args a;
+    a.row_dst = rows_out ? row_dst : nullptr;
+    a.rows_out = rows_out;
     a.T = T; a.d = m->d; a.f = m->f; a.k = m->top_k; a.num_slots = ar->num_slots;
     a.x = x; a.slot = slot; a.w = w;
     a.arena = reinterpret_cast<const uint8_t*>(ar->base);
@@ -584,6 +591,7 @@ int launch_cb3_ffn(const moe_dims* m, const moe_arena* ar, int T, const uint16_t
     }
     if (rc) return rc;
     note_launch(1);
+    if (rows_out) return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;   // the caller combines
     cb3_combine_kernel<<<(T * m->d + 255) / 256 < 2 * num_sms ? (T * m->d + 255) / 256 : 2 * num_sms, 256, 0, st>>>(a);
     note_launch(1);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;

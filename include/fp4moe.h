@@ -237,8 +237,9 @@ int moe_combine(const moe_dims* dims, int32_t T, const float* rows, const int32_
  * ascending id and *n_missing (device int32) their count.  One kernel; all device memory.
  *
  * moe_gather_experts: copies, for each of the *n_missing experts e in missing, the slot image
- * at store + e * slot_bytes (n_store images; moe_pack_expert's layout, e.g. packed into a slot
- * and copied out) into slot expert_to_slot[e] of the arena, and sets resident_expert of that
+ * at store + e * slot_bytes (n_store images in the arena's format: moe_pack_expert's layout
+ * for an FP4 arena, moe_pack_cb3's for a cb3 arena, e.g. packed into a slot and copied out)
+ * into slot expert_to_slot[e] of the arena, and sets resident_expert of that
  * slot to e.  store is any device-accessible address: device memory, or pinned host memory
  * mapped into the device (the kernel reads it directly; no copy is issued by the host).
  * 16-byte aligned.  An expert with no valid slot sets MOE_STATUS_BAD_SLOT and is skipped.
@@ -246,7 +247,7 @@ int moe_combine(const moe_dims* dims, int32_t T, const float* rows, const int32_
  * Two waves: split; moe_expert_ffn_fp4 (flags 0) with slot_wave1 into rows; gather; the same
  * call with slot_wave2 into the same rows (each row is written by one of the two calls); then
  * moe_combine.  The result equals the one-wave call (all experts resident, same routing) bit
- * for bit. */
+ * for bit.  On a cb3 arena the calls are moe_expert_ffn_cb3_rows (decode sizes). */
 /* Cache-conditional routing ("DeepSeek-V4.1-Flash on a single NVIDIA DGX Spark", Conventions,
  * and the expert-cache notes list it as an approved approximation, after "Mixture of
  * Cache-Conditional Experts", arXiv 2412.00099; they give no formula, the reading here is an
@@ -289,13 +290,23 @@ int moe_gather_experts(const moe_dims* dims, const moe_arena* arena, const void*
  * h = silu(W_gate x) * (W_up x) rounded once to bf16, y[t] = bf16(sum_j w_j W_down h_j) in
  * ascending j; CUDA cores, bf16 x bf16 products (exact) summed in fp32.  Same routing inputs as the decode call of moe_expert_ffn_fp4 (topk_slot,
  * topk_w [T, k]); uses the workspace of moe_workspace_bytes(dims, T).  Row t equals the T = 1
- * call on token t bit for bit.  Slots outside [0, num_slots) set MOE_STATUS_BAD_SLOT. */
+ * call on token t bit for bit.  Slots outside [0, num_slots) set MOE_STATUS_BAD_SLOT.
+ *
+ * moe_expert_ffn_cb3_rows: the same expert work without the combine, for the two-wave flow
+ * above (cb3 slots gathered like FP4 ones, since moe_gather_experts copies slot images): row
+ * row_dst[t*k + j] of rows_out fp32 [T*k, d] receives z of pair (t, j) (W_down h_j,
+ * unweighted) for every pair with a valid slot and row_dst >= 0 (row_dst < T*k, e.g. from
+ * moe_permute); every other row is left untouched.  moe_combine of the rows then equals
+ * moe_expert_ffn_cb3's y bit for bit (the same fma order). */
 int64_t moe_cb3_slot_bytes(const moe_dims* dims);
 int moe_pack_cb3(const moe_dims* dims, const moe_arena* fp4_arena, int32_t fp4_slot, const moe_arena* cb3_arena,
                  int32_t cb3_slot, int32_t* dev_status, void* stream);
 int moe_expert_ffn_cb3(const moe_dims* dims, const moe_arena* cb3_arena, int32_t T, const uint16_t* x,
                        const int32_t* topk_slot, const float* topk_w, uint16_t* y, int32_t* dev_status, void* ws,
                        size_t ws_bytes, void* stream);
+int moe_expert_ffn_cb3_rows(const moe_dims* dims, const moe_arena* cb3_arena, int32_t T, const uint16_t* x,
+                            const int32_t* topk_slot, const int32_t* row_dst, float* rows_out, int32_t* dev_status,
+                            void* ws, size_t ws_bytes, void* stream);
 
 /* Layer chaining for multi-layer workloads (a harness step, not part of the routed-expert
  * layer): x_next[t] = bf16_RNE( v / sqrt(mean_i(v_i^2) + eps) ), v = x[t] + y[t] in fp32 (unit

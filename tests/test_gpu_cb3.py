@@ -127,6 +127,58 @@ def test_cb3_rows_equal_decode_calls(small_cb3):
         np.testing.assert_array_equal(many["y_bits"][t], one["y_bits"][0], err_msg=str(t))
 
 
+@pytest.mark.parametrize("T", [1, 3, 16])
+def test_cb3_two_waves_equal_one_wave(small_cb3, T):
+    """cb3 slots in the two-wave flow: rows of the experts on hand (moe_expert_ffn_cb3_rows with
+    the wave-1 slots), the missing cb3 slot images gathered from pinned host memory, rows of the
+    rest, then moe_combine: equal bit for bit to moe_expert_ffn_cb3 on the fully resident cb3
+    arena, and every row equal to the one-wave rows."""
+    from test_gpu_parity import host_device_pointer
+    wl, cb, _ = small_cb3
+    dims = moe.moe_dims(wl.d, wl.f, wl.E, wl.k)
+    sb, ns = cb.slot_bytes, wl.arena.num_slots
+    store = torch.empty(wl.E * sb, dtype=torch.uint8, pin_memory=True)   # expert e's cb3 image at e * sb
+    for e in range(wl.E):
+        s = int(wl.table[e])
+        store[e * sb:(e + 1) * sb].copy_(cb.buf[s * sb:(s + 1) * sb].cpu())
+    part = Cb3Arena(dims, ns, DEV)
+    part.buf.zero_()
+    resident = torch.full((ns,), -1, dtype=torch.int32, device=DEV)
+    on_hand = (0, 2, 3, 5, 7, 8, 11, 13)
+    for e in on_hand:
+        s = int(wl.table[e])
+        part.buf[s * sb:(s + 1) * sb].copy_(cb.buf[s * sb:(s + 1) * sb])
+        resident[s] = e
+    x_bits = syn.activations(41, 0, T, wl.d, stream=5)
+    x = bits_to_torch(x_bits, DEV)
+    tab = torch.from_numpy(wl.table).to(DEV)
+    layer = MoeLayer(wl.d, wl.f, wl.E, wl.k, T, wl.arena)
+    layer.route(x, bits_to_torch(wl.wr, DEV), tab)
+    n = T * wl.k
+    moe.moe_permute(dims, T, layer.ids, layer.offsets, layer.row_src, layer.row_dst, layer.ws)
+    w1, w2, missing = (torch.empty(n, dtype=torch.int32, device=DEV) for _ in range(3))
+    n_missing = torch.zeros(1, dtype=torch.int32, device=DEV)
+    moe.moe_split_waves(dims, T, layer.ids, layer.slots, resident, ns, w1, w2, missing, n_missing)
+    rows = torch.full((n, wl.d), float("nan"), dtype=torch.float32, device=DEV)
+    moe.moe_expert_ffn_cb3_rows(dims, part.c, T, x, w1, layer.row_dst, rows, layer.status, layer.ws)
+    moe.moe_gather_experts(dims, part.c, host_device_pointer(store), wl.E, missing, n_missing, tab, resident,
+                           layer.status)
+    moe.moe_expert_ffn_cb3_rows(dims, part.c, T, x, w2, layer.row_dst, rows, layer.status, layer.ws)
+    y2 = torch.empty((T, wl.d), dtype=torch.bfloat16, device=DEV)
+    moe.moe_combine(dims, T, rows, layer.row_dst, layer.w, y2)
+    rows1 = torch.full_like(rows, float("nan"))
+    moe.moe_expert_ffn_cb3_rows(dims, cb.c, T, x, layer.slots, layer.row_dst, rows1, layer.status, layer.ws)
+    y1 = layer.experts_cb3(cb, x, T=T)
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    ids = layer.ids[:T].cpu().numpy()
+    want = sorted(set(int(e) for e in ids.ravel() if e >= 0) - set(on_hand))
+    assert int(n_missing.item()) == len(want) and missing[:len(want)].cpu().tolist() == want
+    valid = torch.from_numpy(layer.row_src[:n].cpu().numpy() >= 0).to(DEV)
+    assert torch.equal(rows[valid].view(torch.int32), rows1[valid].view(torch.int32))
+    assert torch.equal(y1[:T].view(torch.int16), y2.view(torch.int16))
+
+
 def test_cb3_zero_tokens_and_bad_slot(small_cb3):
     wl, cb, _ = small_cb3
     dims = moe.moe_dims(wl.d, wl.f, wl.E, wl.k)
