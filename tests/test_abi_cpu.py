@@ -97,5 +97,10 @@ def test_host_argument_errors_return_before_any_launch():
     assert lay(*args(good, ok_ar, 1, y=None)) == -1
     assert lay(*args(good, ok_ar, 1, x=P((1 << 20) + 2))) == -8
     assert lay(*args(good, ok_ar, 1, wsb=16)) == -4
+    cr = L.moe_expert_ffn_cb3_rows
+    assert cr(ctypes.byref(good), ctypes.byref(cb3_ar), 17, fake, fake, fake, fake, fake, fake, 1 << 30, None) == -3
+    assert cr(ctypes.byref(good), ctypes.byref(fp4_ar), 1, fake, fake, fake, fake, fake, fake, 1 << 30, None) == -5
+    assert cr(ctypes.byref(good), ctypes.byref(cb3_ar), 1, fake, fake, fake, None, fake, fake, 1 << 30, None) == -1
+    assert cr(ctypes.byref(good), ctypes.byref(cb3_ar), 1, fake, fake, fake, fake, fake, fake, 16, None) == -4
     assert moe.moe_status_str(-4) == "workspace too small"
     assert moe.moe_kernel_launches() == launched      # every rejected call launched nothing
