@@ -330,12 +330,34 @@ int moe_pack_cb3(const moe_dims* dims, const moe_arena* fp4_arena, int32_t fp4_s
     return launch_pack_cb3(dims, src, dst, dev_status, (cudaStream_t)stream);
 }
 
+}  // extern "C"
+
+namespace fp4moe {
+// The cb3 expert calls in consecutive calls of at most kDecodeMaxT tokens (each the decode-size
+// kernels, whose per-token arithmetic does not depend on the other tokens of the call).
+static int cb3_in_chunks(const moe_dims* m, const moe_arena* ar, int T, const uint16_t* x, const int32_t* slot,
+                         const float* w, uint16_t* y, const int32_t* row_dst, float* rows_out, int32_t* status,
+                         char* ws, const WsLayout& L, cudaStream_t st) {
+    const int sms = num_sms_of_current_device(), d = m->d, k = m->top_k;
+    for (int c0 = 0; c0 < T; c0 += kDecodeMaxT) {
+        const int tc = T - c0 < kDecodeMaxT ? T - c0 : kDecodeMaxT;
+        const int rc = launch_cb3_ffn(m, ar, tc, x + (size_t)c0 * d, slot + (size_t)c0 * k,
+                                      w ? w + (size_t)c0 * k : nullptr, y ? y + (size_t)c0 * d : nullptr, status, ws,
+                                      L, st, sms, row_dst ? row_dst + (size_t)c0 * k : nullptr, rows_out);
+        if (rc) return rc;
+    }
+    return MOE_OK;
+}
+}  // namespace fp4moe
+
+extern "C" {
+
 int moe_expert_ffn_cb3(const moe_dims* dims, const moe_arena* cb3_arena, int32_t T, const uint16_t* x,
                        const int32_t* topk_slot, const float* topk_w, uint16_t* y, int32_t* dev_status, void* ws,
                        size_t ws_bytes, void* stream) {
     if (!dims_ok(dims)) return MOE_ERR_DIMS;
     if (!cb3_ffn_supported(dims)) return MOE_ERR_DIMS;
-    if (T < 0 || T > kDecodeMaxT) return MOE_ERR_TOKENS;
+    if (T < 0) return MOE_ERR_TOKENS;
     int rc = check_arena(dims, cb3_arena, true);
     if (rc) return rc;
     if (!x || !topk_slot || !topk_w || !y || !dev_status) return MOE_ERR_NULL;
@@ -343,8 +365,8 @@ int moe_expert_ffn_cb3(const moe_dims* dims, const moe_arena* cb3_arena, int32_t
     WsLayout L;
     rc = check_ws(dims, T, ws, ws_bytes, &L);
     if (rc) return rc;
-    return launch_cb3_ffn(dims, cb3_arena, T, x, topk_slot, topk_w, y, dev_status, static_cast<char*>(ws), L,
-                          (cudaStream_t)stream, num_sms_of_current_device());
+    return cb3_in_chunks(dims, cb3_arena, T, x, topk_slot, topk_w, y, nullptr, nullptr, dev_status,
+                         static_cast<char*>(ws), L, (cudaStream_t)stream);
 }
 
 int moe_expert_ffn_cb3_rows(const moe_dims* dims, const moe_arena* cb3_arena, int32_t T, const uint16_t* x,
@@ -352,7 +374,7 @@ int moe_expert_ffn_cb3_rows(const moe_dims* dims, const moe_arena* cb3_arena, in
                             void* ws, size_t ws_bytes, void* stream) {
     if (!dims_ok(dims)) return MOE_ERR_DIMS;
     if (!cb3_ffn_supported(dims)) return MOE_ERR_DIMS;
-    if (T < 0 || T > kDecodeMaxT) return MOE_ERR_TOKENS;
+    if (T < 0) return MOE_ERR_TOKENS;
     int rc = check_arena(dims, cb3_arena, true);
     if (rc) return rc;
     if (!x || !topk_slot || !row_dst || !rows_out || !dev_status) return MOE_ERR_NULL;
@@ -360,8 +382,8 @@ int moe_expert_ffn_cb3_rows(const moe_dims* dims, const moe_arena* cb3_arena, in
     WsLayout L;
     rc = check_ws(dims, T, ws, ws_bytes, &L);
     if (rc) return rc;
-    return launch_cb3_ffn(dims, cb3_arena, T, x, topk_slot, nullptr, nullptr, dev_status, static_cast<char*>(ws), L,
-                          (cudaStream_t)stream, num_sms_of_current_device(), row_dst, rows_out);
+    return cb3_in_chunks(dims, cb3_arena, T, x, topk_slot, nullptr, nullptr, row_dst, rows_out, dev_status,
+                         static_cast<char*>(ws), L, (cudaStream_t)stream);
 }
 
 int moe_residual_rmsnorm(int32_t T, int32_t d, const uint16_t* x, const uint16_t* y, float eps, uint16_t* x_next,

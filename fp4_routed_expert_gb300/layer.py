@@ -76,8 +76,8 @@ class MoeLayer:
         self.y = torch.empty((max(T_max, 1), d), dtype=torch.bfloat16, device=dev)
 
     def experts_cb3(self, cb3: Cb3Arena, x, T=None, stream=None, y=None):
-        """Expert FFN + combine on cb3 experts (decode and verify, T <= 16); the routing's slots
-        index the cb3 arena."""
+        """Expert FFN + combine on cb3 experts (any T: more than 16 tokens as consecutive calls
+        of 16); the routing's slots index the cb3 arena."""
         T = x.shape[0] if T is None else T
         y = self.y if y is None else y
         moe_expert_ffn_cb3(self.dims, cb3.c, T, x, self.slots, self.w, y, self.status, self.ws, stream)

@@ -285,8 +285,9 @@ int moe_gather_experts(const moe_dims* dims, const moe_arena* arena, const void*
  * into slot cb3_slot of cb3_arena (slot_bytes = moe_cb3_slot_bytes).  One kernel, one block
  * per row.  A row with more than 256 distinct values or a NaN scale sets MOE_STATUS_CB3_ROW.
  *
- * moe_expert_ffn_cb3: a5-a6 on cb3 experts for 0 <= T <= 16 tokens (decode and multi-token
- * verify; larger T returns MOE_ERR_TOKENS) and d <= 8192, f <= 2304 (else MOE_ERR_DIMS):
+ * moe_expert_ffn_cb3: a5-a6 on cb3 experts for T >= 0 tokens (decode and multi-token verify in
+ * one call; more than 16 tokens, e.g. a prefill chunk, as consecutive calls of 16) and d <= 8192,
+ * f <= 2304 (else MOE_ERR_DIMS):
  * h = silu(W_gate x) * (W_up x) rounded once to bf16, y[t] = bf16(sum_j w_j W_down h_j) in
  * ascending j; CUDA cores, bf16 x bf16 products (exact) summed in fp32.  Same routing inputs as the decode call of moe_expert_ffn_fp4 (topk_slot,
  * topk_w [T, k]); uses the workspace of moe_workspace_bytes(dims, T).  Row t equals the T = 1

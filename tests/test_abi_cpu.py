@@ -77,7 +77,7 @@ def test_host_argument_errors_return_before_any_launch():
     assert L.moe_pack_cb3(ctypes.byref(good), ctypes.byref(fp4_ar), 0, ctypes.byref(cb3_ar), -1, fake, None) == -5
     assert L.moe_pack_cb3(ctypes.byref(good), ctypes.byref(fp4_ar), 0, ctypes.byref(cb3_ar), 0, None, None) == -1
     assert L.moe_pack_cb3(ctypes.byref(bad), ctypes.byref(fp4_ar), 0, ctypes.byref(cb3_ar), 0, fake, None) == -2
-    assert L.moe_expert_ffn_cb3(ctypes.byref(good), ctypes.byref(cb3_ar), 17, fake, fake, fake, fake, fake, fake,
+    assert L.moe_expert_ffn_cb3(ctypes.byref(good), ctypes.byref(cb3_ar), -1, fake, fake, fake, fake, fake, fake,
                                 1 << 30, None) == -3
     assert L.moe_expert_ffn_cb3(ctypes.byref(good), ctypes.byref(fp4_ar), 1, fake, fake, fake, fake, fake, fake,
                                 1 << 30, None) == -5
@@ -98,7 +98,7 @@ def test_host_argument_errors_return_before_any_launch():
     assert lay(*args(good, ok_ar, 1, x=P((1 << 20) + 2))) == -8
     assert lay(*args(good, ok_ar, 1, wsb=16)) == -4
     cr = L.moe_expert_ffn_cb3_rows
-    assert cr(ctypes.byref(good), ctypes.byref(cb3_ar), 17, fake, fake, fake, fake, fake, fake, 1 << 30, None) == -3
+    assert cr(ctypes.byref(good), ctypes.byref(cb3_ar), -1, fake, fake, fake, fake, fake, fake, 1 << 30, None) == -3
     assert cr(ctypes.byref(good), ctypes.byref(fp4_ar), 1, fake, fake, fake, fake, fake, fake, 1 << 30, None) == -5
     assert cr(ctypes.byref(good), ctypes.byref(cb3_ar), 1, fake, fake, fake, None, fake, fake, 1 << 30, None) == -1
     assert cr(ctypes.byref(good), ctypes.byref(cb3_ar), 1, fake, fake, fake, fake, fake, fake, 16, None) == -4

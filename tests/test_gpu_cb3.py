@@ -118,6 +118,21 @@ def test_cb3_ffn_matches_oracle(small_cb3, T):
     check_cb3_tokens(wl, x, got, list(range(T)), packed)
 
 
+def test_cb3_prefill_chunk_in_16_token_calls(small_cb3):
+    """T = 40 (a prefill-size call, the tiled router): the cb3 experts run as consecutive calls
+    of 16 tokens; sampled tokens against the oracle, and every row equal to the T = 1 call on
+    that token bit for bit."""
+    wl, cb, packed = small_cb3
+    x = syn.activations(41, 0, 40, wl.d, stream=6)
+    got = run_cb3(wl, cb, x)
+    assert got["status"] == 0
+    check_cb3_tokens(wl, x, got, [0, 15, 16, 39], packed)
+    for t in (0, 17, 39):
+        one = run_cb3(wl, cb, x[t:t + 1])
+        np.testing.assert_array_equal(one["ids"][0], got["ids"][t])
+        np.testing.assert_array_equal(got["y_bits"][t], one["y_bits"][0], err_msg=str(t))
+
+
 def test_cb3_rows_equal_decode_calls(small_cb3):
     wl, cb, _ = small_cb3
     x = syn.activations(41, 0, 16, wl.d, stream=2)
