@@ -84,7 +84,8 @@ inline int decode_groups(int T, int epb) {
 // quarter order like the lanes'.  The loops are kept short: this code runs once
 // per call and is seldom in the instruction cache.  The last block to finish (a ticket on
 // a.counter, left at zero again) then selects every token's experts, one warp per token, in
-// its own shared memory.
+// its own shared memory -- unless a.handoff is set (moe_layer_decode_fp4): then every block
+// only releases its records on a.counter and the expert kernel launched next selects.
 template <int CH, int EPL>
 __global__ void __launch_bounds__(kDecodeThreads) route_decode_kernel(RouteArgs a) {
     constexpr int NCH = 8 / CH;
